@@ -1,0 +1,174 @@
+/*
+ * tgemm — dense matrix multiplication C = A x B for one NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of libtgemm.so. Every entry point takes plain sizes, pointers and a
+ * CUDA stream; no C++ or framework type crosses this boundary.
+ *
+ * The operation is the product defined in "Tiled Matrix Multiplication in
+ * CUDA", section 1 ("What matrix multiplication actually does"), and
+ * "Tiled GEMM: Matrix Multiplication in CUDA", section 1:
+ *
+ *     C[i][j] = sum over k = 0 .. K-1 of A[i][k] * B[k][j]
+ *
+ * for 0 <= i < M, 0 <= j < N. All three matrices are row-major and addressed
+ * by the flat index row * ld + col ("Tiled Matrix Multiplication in CUDA",
+ * section 2), where ld is the leading dimension: the number of elements
+ * between the starts of two consecutive rows (ld >= the row length; ld larger
+ * than the row length describes a sub-matrix of a wider array). The pages'
+ * square "width" is generalised to M, N, K with one leading dimension per
+ * matrix, following the ragged-edge code of "Tiled GEMM: Matrix
+ * Multiplication in CUDA", section 7.1.
+ *
+ * Common rules for the compute entry points:
+ *   - A, B and C are DEVICE pointers (memory the caller allocated on the
+ *     current CUDA device). The library never allocates, frees or copies the
+ *     caller's buffers, and keeps no reference to them after the call.
+ *   - C is overwritten (there is no alpha/beta); K == 0 writes zeros to the
+ *     M x N block of C; M == 0 or N == 0 is a no-op that returns TGEMM_OK.
+ *   - Elements of A, B and C outside the M x K, K x N and M x N blocks (the
+ *     padding between the row length and ld) are never read or written.
+ *   - C must not overlap A or B; overlap is undefined behaviour.
+ *   - The call is asynchronous: it validates its arguments, enqueues the work
+ *     on `stream` (0 = the legacy default stream) and returns. A launch
+ *     failure is reported as TGEMM_ERR_CUDA. Faults found while the kernel
+ *     runs (a bounded wait that ran out) are reported later, by
+ *     gemm_device_status().
+ *   - Arguments are checked before any CUDA call is made; an invalid call
+ *     returns an error code and enqueues nothing.
+ *   - The calls are thread-safe for distinct streams; configuration setters
+ *     (gemm_set_*) are process-wide and should be called before launching.
+ */
+#ifndef TGEMM_H
+#define TGEMM_H
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+#define TGEMM_OK                    0
+#define TGEMM_ERR_INVALID_ARG       1  /* negative size, ld too small, null pointer, bad in_type */
+#define TGEMM_ERR_ALIGNMENT         2  /* the tensor-core path needs 16-byte aligned pointers and ld */
+#define TGEMM_ERR_CUDA              3  /* a CUDA runtime call or launch failed */
+#define TGEMM_ERR_DEVICE_TIMEOUT    4  /* a bounded wait inside a kernel ran out (see gemm_device_status) */
+#define TGEMM_ERR_UNSUPPORTED       5  /* the current device is not sm_103 / sm_100 class */
+
+/* Input element types of gemm_tc. */
+#define TGEMM_TF32  1   /* A and B are float arrays; products use the TF32 tensor-core format */
+#define TGEMM_BF16  2   /* A and B are bfloat16 arrays (uint16 bit patterns) */
+
+/*
+ * gemm_f32 — exact-FP32 product on the CUDA cores.
+ *
+ * Computes C = A x B with A: M x K floats (leading dimension lda >= K),
+ * B: K x N floats (ldb >= N), C: M x N floats (ldc >= N). Each output is
+ * accumulated in FP32 with fused multiply-adds in ascending k within a thread
+ * (the phase loop over K-tiles and the inner loop inside a tile of "Tiled
+ * GEMM: Matrix Multiplication in CUDA", sections 2 and 4.3-4.6). Tiles of A
+ * and B are staged through shared memory; rows and columns past M, N, K read
+ * as zero (section 7.1 of the same page), so any M, N, K >= 0 is accepted.
+ * Any lda/ldb/ldc and 4-byte aligned pointers work; 16-byte aligned pointers
+ * with ld a multiple of 4 take 16-byte vector loads.
+ *
+ * Returns TGEMM_OK, TGEMM_ERR_INVALID_ARG (M, N or K negative; lda < K,
+ * ldb < N or ldc < N; a null pointer when the product is not empty; a pointer
+ * not 4-byte aligned), TGEMM_ERR_UNSUPPORTED or TGEMM_ERR_CUDA.
+ */
+int gemm_f32(int M, int N, int K,
+             const float* A, long lda,
+             const float* B, long ldb,
+             float* C, long ldc,
+             cudaStream_t stream);
+
+/*
+ * gemm_tc — product on the 5th-generation tensor cores (tcgen05, TMEM
+ * accumulators), FP32 output.
+ *
+ * Same product and layout as gemm_f32. A and B hold `in_type` elements:
+ *   TGEMM_TF32: A and B are float arrays; the tensor core multiplies them in
+ *               the TF32 format (10 explicit mantissa bits) and accumulates in
+ *               FP32.
+ *   TGEMM_BF16: A and B are bfloat16 arrays; products are exact and are
+ *               accumulated in FP32.
+ * C is FP32 (ldc >= N, any alignment). Tiles of A and B are copied by the
+ * Tensor Memory Accelerator, which requires A and B to start on 16-byte
+ * boundaries and lda, ldb to be multiples of 16 bytes (4 floats / 8 bf16);
+ * otherwise TGEMM_ERR_ALIGNMENT is returned and nothing is launched (no other
+ * kernel is substituted). Rows and columns past M, N, K read as zero.
+ *
+ * Returns TGEMM_OK, TGEMM_ERR_INVALID_ARG, TGEMM_ERR_ALIGNMENT,
+ * TGEMM_ERR_UNSUPPORTED or TGEMM_ERR_CUDA.
+ */
+int gemm_tc(int M, int N, int K,
+            const void* A, long lda,
+            const void* B, long ldb,
+            float* C, long ldc,
+            int in_type,
+            cudaStream_t stream);
+
+/*
+ * gemm_device_status — result of the kernels' bounded waits.
+ *
+ * Synchronises `stream`, then returns and clears the library's device-side
+ * status word on the current device: TGEMM_OK if no kernel launched since the
+ * last call gave up on a wait, TGEMM_ERR_DEVICE_TIMEOUT if one did (that
+ * kernel's output is then incomplete), or TGEMM_ERR_CUDA if synchronising or
+ * reading the word failed. A kernel that gives up releases its tensor memory
+ * and exits normally, so the CUDA context stays usable.
+ */
+int gemm_device_status(cudaStream_t stream);
+
+/*
+ * gemm_status_string — a static, human-readable name for a status code.
+ * Never returns NULL; unknown codes give "unknown tgemm status".
+ */
+const char* gemm_status_string(int status);
+
+/*
+ * gemm_set_wait_limit_ns — upper bound, in nanoseconds, on any single wait
+ * inside the tensor-core kernel (a pipeline stage, the accumulator hand-off).
+ * Must be > 0; the default is 2 000 000 000 (2 s). Process-wide; applies to
+ * launches made after the call. Returns TGEMM_OK or TGEMM_ERR_INVALID_ARG.
+ */
+int gemm_set_wait_limit_ns(long long ns);
+
+/*
+ * gemm_set_debug_stall — failure-detection hook for tests. When `enable` is
+ * non-zero, the next gemm_tc launches never signal the first pipeline stage
+ * as loaded, so the consumer's bounded wait runs out and the kernel exits
+ * through its timeout path (reporting TGEMM_ERR_DEVICE_TIMEOUT through
+ * gemm_device_status). Off by default; process-wide. Returns TGEMM_OK.
+ */
+int gemm_set_debug_stall(int enable);
+
+/*
+ * gemm_set_f32_kernel — force one FP32 kernel configuration (for tests and
+ * tuning): -1 restores automatic per-shape selection; 0 .. gemm_f32_kernel_count()-1
+ * selects that entry of the library's table. Process-wide. Returns TGEMM_OK
+ * or TGEMM_ERR_INVALID_ARG.
+ */
+int gemm_set_f32_kernel(int id);
+
+/* Number of FP32 kernel configurations gemm_set_f32_kernel accepts. */
+int gemm_f32_kernel_count(void);
+
+/*
+ * gemm_f32_kernel_name — static name of FP32 configuration `id`
+ * (tile sizes and loader), or "" for an id out of range.
+ */
+const char* gemm_f32_kernel_name(int id);
+
+/*
+ * gemm_last_kernel — static name of the kernel configuration the most
+ * recent successful gemm_f32 or gemm_tc call on this thread launched, or ""
+ * if none did (empty product, error). For tests and benchmarks.
+ */
+const char* gemm_last_kernel(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TGEMM_H */

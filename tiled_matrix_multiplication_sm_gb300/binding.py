@@ -1,0 +1,220 @@
+"""ctypes binding of libtgemm.so (declared in ``include/tgemm.h``).
+
+Argument marshalling only: every step of the product runs in the library's
+CUDA kernels. PyTorch supplies device memory and the current stream. If the
+compiled library is missing, every call raises :class:`TgemmError`; there is
+no fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+TGEMM_OK = 0
+TGEMM_ERR_INVALID_ARG = 1
+TGEMM_ERR_ALIGNMENT = 2
+TGEMM_ERR_CUDA = 3
+TGEMM_ERR_DEVICE_TIMEOUT = 4
+TGEMM_ERR_UNSUPPORTED = 5
+
+TGEMM_TF32 = 1
+TGEMM_BF16 = 2
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+# Every symbol the header declares, with (restype, argtypes).
+_VP = ctypes.c_void_p
+_SIGNATURES = {
+    "gemm_f32": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                _VP, ctypes.c_long, _VP, ctypes.c_long,
+                                _VP, ctypes.c_long, _VP]),
+    "gemm_tc": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                               _VP, ctypes.c_long, _VP, ctypes.c_long,
+                               _VP, ctypes.c_long, ctypes.c_int, _VP]),
+    "gemm_device_status": (ctypes.c_int, [_VP]),
+    "gemm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "gemm_set_wait_limit_ns": (ctypes.c_int, [ctypes.c_longlong]),
+    "gemm_set_debug_stall": (ctypes.c_int, [ctypes.c_int]),
+    "gemm_set_f32_kernel": (ctypes.c_int, [ctypes.c_int]),
+    "gemm_f32_kernel_count": (ctypes.c_int, []),
+    "gemm_f32_kernel_name": (ctypes.c_char_p, [ctypes.c_int]),
+    "gemm_last_kernel": (ctypes.c_char_p, []),
+}
+
+
+class TgemmError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})" if what
+                         else f"{status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return os.environ.get("TGEMM_LIBRARY", os.path.join(_HERE, "_build", "libtgemm.so"))
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libtgemm.so (once). Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"libtgemm.so not found at {path}; build it with "
+                "`python -m tiled_matrix_multiplication_sm_gb300.build`")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().gemm_status_string(int(status)).decode()
+    except RuntimeError:
+        return {0: "ok", 1: "invalid argument", 2: "misaligned operand",
+                3: "CUDA error", 4: "device wait timed out",
+                5: "unsupported device"}.get(status, "unknown tgemm status")
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def gemm_f32_raw(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, stream_handle=0) -> int:
+    """Direct call of the C entry point; returns its status code."""
+    return int(load().gemm_f32(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, stream_handle))
+
+
+def gemm_tc_raw(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, in_type, stream_handle=0) -> int:
+    return int(load().gemm_tc(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, in_type,
+                              stream_handle))
+
+
+def _check_matrix(x: torch.Tensor, name: str, dtype: torch.dtype) -> int:
+    if not isinstance(x, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if x.dim() != 2:
+        raise ValueError(f"{name} must be 2-D, got shape {tuple(x.shape)}")
+    if x.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if x.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {x.dtype}")
+    if x.shape[1] > 1 and x.stride(1) != 1:
+        raise ValueError(f"{name} must have unit column stride (row-major)")
+    return max(int(x.stride(0)), int(x.shape[1]), 1) if x.shape[0] > 1 else max(int(x.shape[1]), 1)
+
+
+def _out(out, M, N, device):
+    if out is None:
+        return torch.empty((M, N), dtype=torch.float32, device=device)
+    if tuple(out.shape) != (M, N):
+        raise ValueError(f"out has shape {tuple(out.shape)}, expected {(M, N)}")
+    return out
+
+
+def gemm_f32(A: torch.Tensor, B: torch.Tensor, out: Optional[torch.Tensor] = None,
+             stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """C = A @ B on the FP32 CUDA-core path (asynchronous on ``stream``)."""
+    lda = _check_matrix(A, "A", torch.float32)
+    ldb = _check_matrix(B, "B", torch.float32)
+    M, K = A.shape
+    if B.shape[0] != K:
+        raise ValueError(f"inner dimensions differ: {tuple(A.shape)} x {tuple(B.shape)}")
+    N = B.shape[1]
+    C = _out(out, M, N, A.device)
+    ldc = _check_matrix(C, "out", torch.float32)
+    with torch.cuda.device(A.device):
+        st = gemm_f32_raw(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb,
+                          C.data_ptr(), ldc, _stream_handle(stream))
+    if st != TGEMM_OK:
+        raise TgemmError(st, "gemm_f32")
+    return C
+
+
+_TC_TYPES = {"tf32": (TGEMM_TF32, torch.float32), "bf16": (TGEMM_BF16, torch.bfloat16)}
+
+
+def gemm_tc(A: torch.Tensor, B: torch.Tensor, in_type: str = "bf16",
+            out: Optional[torch.Tensor] = None,
+            stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """C = A @ B on the tcgen05 tensor-core path; ``in_type`` is "tf32" or "bf16"."""
+    code, dtype = _TC_TYPES[in_type]
+    lda = _check_matrix(A, "A", dtype)
+    ldb = _check_matrix(B, "B", dtype)
+    M, K = A.shape
+    if B.shape[0] != K:
+        raise ValueError(f"inner dimensions differ: {tuple(A.shape)} x {tuple(B.shape)}")
+    N = B.shape[1]
+    C = _out(out, M, N, A.device)
+    ldc = _check_matrix(C, "out", torch.float32)
+    with torch.cuda.device(A.device):
+        st = gemm_tc_raw(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb,
+                         C.data_ptr(), ldc, code, _stream_handle(stream))
+    if st != TGEMM_OK:
+        raise TgemmError(st, "gemm_tc")
+    return C
+
+
+def device_status(stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Synchronise ``stream`` and return (and clear) the kernels' wait status."""
+    return int(load().gemm_device_status(_stream_handle(stream)))
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    return int(load().gemm_set_wait_limit_ns(int(ns)))
+
+
+def set_debug_stall(enable: bool) -> int:
+    return int(load().gemm_set_debug_stall(1 if enable else 0))
+
+
+def set_f32_kernel(kernel_id: int) -> int:
+    return int(load().gemm_set_f32_kernel(int(kernel_id)))
+
+
+def f32_kernel_names():
+    lib = load()
+    return [lib.gemm_f32_kernel_name(i).decode() for i in range(lib.gemm_f32_kernel_count())]
+
+
+def last_kernel() -> str:
+    return load().gemm_last_kernel().decode()
+
+
+def matmul(A: torch.Tensor, B: torch.Tensor, path: str = "f32") -> torch.Tensor:
+    """End-to-end product through the library for host or device operands.
+
+    ``path`` is "f32" (CUDA cores), "tf32" or "bf16" (tensor cores). Host
+    operands are copied to the current CUDA device (from pinned memory when
+    they are pinned), multiplied there, and the result is copied back to the
+    host; device operands give a device result.
+    """
+    on_host = A.device.type == "cpu"
+    if on_host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        A = A.to(dev, non_blocking=A.is_pinned())
+        B = B.to(dev, non_blocking=B.is_pinned())
+    if path == "f32":
+        C = gemm_f32(A, B)
+    elif path in _TC_TYPES:
+        C = gemm_tc(A, B, path)
+    else:
+        raise ValueError(f"unknown path {path!r}")
+    if on_host:
+        host = torch.empty(C.shape, dtype=C.dtype, pin_memory=True)
+        host.copy_(C, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return host
+    return C
