@@ -43,6 +43,12 @@
 
 #include <cuda_runtime_api.h>
 
+#if defined(__GNUC__)
+#define TGEMM_API __attribute__((visibility("default")))
+#else
+#define TGEMM_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -76,7 +82,7 @@ extern "C" {
  * ldb < N or ldc < N; a null pointer when the product is not empty; a pointer
  * not 4-byte aligned), TGEMM_ERR_UNSUPPORTED or TGEMM_ERR_CUDA.
  */
-int gemm_f32(int M, int N, int K,
+TGEMM_API int gemm_f32(int M, int N, int K,
              const float* A, long lda,
              const float* B, long ldb,
              float* C, long ldc,
@@ -101,7 +107,7 @@ int gemm_f32(int M, int N, int K,
  * Returns TGEMM_OK, TGEMM_ERR_INVALID_ARG, TGEMM_ERR_ALIGNMENT,
  * TGEMM_ERR_UNSUPPORTED or TGEMM_ERR_CUDA.
  */
-int gemm_tc(int M, int N, int K,
+TGEMM_API int gemm_tc(int M, int N, int K,
             const void* A, long lda,
             const void* B, long ldb,
             float* C, long ldc,
@@ -118,13 +124,13 @@ int gemm_tc(int M, int N, int K,
  * reading the word failed. A kernel that gives up releases its tensor memory
  * and exits normally, so the CUDA context stays usable.
  */
-int gemm_device_status(cudaStream_t stream);
+TGEMM_API int gemm_device_status(cudaStream_t stream);
 
 /*
  * gemm_status_string — a static, human-readable name for a status code.
  * Never returns NULL; unknown codes give "unknown tgemm status".
  */
-const char* gemm_status_string(int status);
+TGEMM_API const char* gemm_status_string(int status);
 
 /*
  * gemm_set_wait_limit_ns — upper bound, in nanoseconds, on any single wait
@@ -132,7 +138,7 @@ const char* gemm_status_string(int status);
  * Must be > 0; the default is 2 000 000 000 (2 s). Process-wide; applies to
  * launches made after the call. Returns TGEMM_OK or TGEMM_ERR_INVALID_ARG.
  */
-int gemm_set_wait_limit_ns(long long ns);
+TGEMM_API int gemm_set_wait_limit_ns(long long ns);
 
 /*
  * gemm_set_debug_stall — failure-detection hook for tests. When `enable` is
@@ -141,7 +147,7 @@ int gemm_set_wait_limit_ns(long long ns);
  * through its timeout path (reporting TGEMM_ERR_DEVICE_TIMEOUT through
  * gemm_device_status). Off by default; process-wide. Returns TGEMM_OK.
  */
-int gemm_set_debug_stall(int enable);
+TGEMM_API int gemm_set_debug_stall(int enable);
 
 /*
  * gemm_set_f32_kernel — force one FP32 kernel configuration (for tests and
@@ -149,23 +155,23 @@ int gemm_set_debug_stall(int enable);
  * selects that entry of the library's table. Process-wide. Returns TGEMM_OK
  * or TGEMM_ERR_INVALID_ARG.
  */
-int gemm_set_f32_kernel(int id);
+TGEMM_API int gemm_set_f32_kernel(int id);
 
 /* Number of FP32 kernel configurations gemm_set_f32_kernel accepts. */
-int gemm_f32_kernel_count(void);
+TGEMM_API int gemm_f32_kernel_count(void);
 
 /*
  * gemm_f32_kernel_name — static name of FP32 configuration `id`
  * (tile sizes and loader), or "" for an id out of range.
  */
-const char* gemm_f32_kernel_name(int id);
+TGEMM_API const char* gemm_f32_kernel_name(int id);
 
 /*
  * gemm_last_kernel — static name of the kernel configuration the most
  * recent successful gemm_f32 or gemm_tc call on this thread launched, or ""
  * if none did (empty product, error). For tests and benchmarks.
  */
-const char* gemm_last_kernel(void);
+TGEMM_API const char* gemm_last_kernel(void);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,124 @@
+"""The C ABI of libtgemm.so, checked on the host (no compute calls, no GPU).
+
+The library must load, export every entry point that include/tgemm.h
+declares, and reject invalid arguments before it touches the CUDA runtime.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import tiled_matrix_multiplication_sm_gb300 as tg
+from tiled_matrix_multiplication_sm_gb300 import binding
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "tgemm.h")
+
+
+def declared_symbols():
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^TGEMM_API\s+[\w\s\*]*?\b(\w+)\s*\(", text, re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = tg.library_path()
+    if not os.path.exists(path):
+        from tiled_matrix_multiplication_sm_gb300 import build
+        build.build()
+    return tg.load()
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for required in ["gemm_f32", "gemm_tc", "gemm_status_string", "gemm_device_status"]:
+        assert required in names
+    assert len(names) == 10
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert set(declared_symbols()) == set(binding._SIGNATURES)
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        s = tg.status_string(code)
+        assert s and s != "unknown tgemm status"
+    assert tg.status_string(99) == "unknown tgemm status"
+    assert tg.status_string(-7) == "unknown tgemm status"
+
+
+FAKE = 0x10000           # never dereferenced: every call below is rejected first
+
+
+@pytest.mark.parametrize("args", [
+    (-1, 4, 4, FAKE, 4, FAKE, 4, FAKE, 4),        # negative M
+    (4, -1, 4, FAKE, 4, FAKE, 4, FAKE, 4),        # negative N
+    (4, 4, -1, FAKE, 4, FAKE, 4, FAKE, 4),        # negative K
+    (4, 4, 8, FAKE, 7, FAKE, 4, FAKE, 4),         # lda < K
+    (4, 8, 4, FAKE, 4, FAKE, 7, FAKE, 8),         # ldb < N
+    (4, 8, 4, FAKE, 4, FAKE, 8, FAKE, 7),         # ldc < N
+    (4, 4, 4, 0, 4, FAKE, 4, FAKE, 4),            # null A
+    (4, 4, 4, FAKE, 4, 0, 4, FAKE, 4),            # null B
+    (4, 4, 4, FAKE, 4, FAKE, 4, 0, 4),            # null C
+    (4, 4, 4, FAKE + 2, 4, FAKE, 4, FAKE, 4),     # A not 4-byte aligned
+    (4, 4, 4, FAKE, 4, FAKE, 4, FAKE + 1, 4),     # C not 4-byte aligned
+])
+def test_f32_invalid_arguments(lib, args):
+    assert tg.gemm_f32_raw(*args, 0) == binding.TGEMM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("args,code", [
+    ((4, 4, 4, FAKE, 4, FAKE, 4, FAKE, 4, 3), binding.TGEMM_ERR_INVALID_ARG),     # bad in_type
+    ((4, 4, 4, FAKE, 4, FAKE, 4, FAKE, 4, 0), binding.TGEMM_ERR_INVALID_ARG),
+    ((-1, 4, 4, FAKE, 4, FAKE, 4, FAKE, 4, 2), binding.TGEMM_ERR_INVALID_ARG),
+    ((4, 4, 8, FAKE, 4, FAKE, 4, FAKE, 4, 2), binding.TGEMM_ERR_INVALID_ARG),     # lda < K
+    ((4, 8, 8, FAKE + 4, 8, FAKE, 8, FAKE, 8, 2), binding.TGEMM_ERR_ALIGNMENT),   # A off 16 B
+    ((4, 8, 8, FAKE, 8, FAKE + 8, 8, FAKE, 8, 2), binding.TGEMM_ERR_ALIGNMENT),   # B off 16 B
+    ((4, 8, 12, FAKE, 12, FAKE, 8, FAKE, 8, 2), binding.TGEMM_ERR_ALIGNMENT),     # bf16 lda*2 % 16
+    ((4, 6, 8, FAKE, 8, FAKE, 6, FAKE, 6, 1), binding.TGEMM_ERR_ALIGNMENT),       # tf32 ldb*4 % 16
+    ((4, 8, 8, FAKE, 8, FAKE, 8, FAKE + 2, 8, 1), binding.TGEMM_ERR_INVALID_ARG), # C misaligned
+])
+def test_tc_invalid_arguments(lib, args, code):
+    assert tg.gemm_tc_raw(*args, 0) == code
+
+
+@pytest.mark.parametrize("M,N", [(0, 5), (5, 0), (0, 0)])
+def test_empty_output_is_noop(lib, M, N):
+    """Nothing to compute: OK without any CUDA call (null pointers allowed)."""
+    assert tg.gemm_f32_raw(M, N, 3, 0, 3, 0, max(N, 1), 0, max(N, 1), 0) == binding.TGEMM_OK
+    assert tg.gemm_tc_raw(M, N, 8, 0, 8, 0, 8, 0, 8, 2, 0) == binding.TGEMM_OK
+
+
+def test_setters_validate(lib):
+    assert binding.set_wait_limit_ns(0) == binding.TGEMM_ERR_INVALID_ARG
+    assert binding.set_wait_limit_ns(-5) == binding.TGEMM_ERR_INVALID_ARG
+    assert binding.set_wait_limit_ns(2_000_000_000) == binding.TGEMM_OK
+    n = lib.gemm_f32_kernel_count()
+    assert n >= 2
+    assert binding.set_f32_kernel(n) == binding.TGEMM_ERR_INVALID_ARG
+    assert binding.set_f32_kernel(-2) == binding.TGEMM_ERR_INVALID_ARG
+    assert binding.set_f32_kernel(-1) == binding.TGEMM_OK
+    assert lib.gemm_f32_kernel_name(n) == b""
+    names = binding.f32_kernel_names()
+    assert len(set(names)) == n and all(names)
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU failure path")
+def test_valid_call_without_gpu_fails_loudly(lib):
+    """A valid call on a host with no usable GPU returns an error, never falls back."""
+    st = tg.gemm_f32_raw(4, 4, 4, FAKE, 4, FAKE, 4, FAKE, 4, 0)
+    assert st in (binding.TGEMM_ERR_CUDA, binding.TGEMM_ERR_UNSUPPORTED)
+    with pytest.raises((ValueError, RuntimeError)):
+        tg.gemm_f32(torch.ones(4, 4), torch.ones(4, 4))
+
+
+def test_binding_rejects_bad_tensors(lib):
+    with pytest.raises(ValueError):
+        tg.gemm_f32(torch.ones(4), torch.ones(4, 4))
+    with pytest.raises(ValueError):
+        tg.gemm_f32(torch.ones(4, 4), torch.ones(4, 4))   # host tensors need matmul()

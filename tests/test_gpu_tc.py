@@ -1,0 +1,144 @@
+"""Parity of the tcgen05 tensor-core path (gemm_tc, TF32 and BF16) with the
+CPU oracle.
+
+Tolerance (tensor path): |C - C_ref| <= 1e-2 * absAB element by element.
+Small integers are exact in TF32 and BF16 and their products are exact, so
+integer-valued inputs whose partial sums stay below 2^24 must match the
+oracle bit for bit on this path too. All calls go through the C ABI.
+"""
+import pytest
+import torch
+
+import oracle
+from tests.parity import TC_ABS, TC_REL, assert_bit_exact, assert_within
+from tiled_matrix_multiplication_sm_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = {"tf32": torch.float32, "bf16": torch.bfloat16}
+
+
+def run_tc(tg, A, B, kind, out=None):
+    C = tg.gemm_tc(A.cuda() if A.device.type == "cpu" else A,
+                   B.cuda() if B.device.type == "cpu" else B, kind, out=out)
+    assert tg.device_status() == 0
+    return C
+
+
+def operands(M, N, K, dist, kind, seed):
+    g = inputs.generator(seed)
+    A = inputs.draw(M, K, dist, g).to(DTYPES[kind])
+    B = inputs.draw(K, N, dist, g).to(DTYPES[kind])
+    return A, B
+
+
+def padded_cuda(x, ld, pad=float("nan")):
+    rows, cols = x.shape
+    store = torch.full((rows, ld), pad, dtype=x.dtype, device="cuda")
+    store[:, :cols] = x.cuda()
+    return store[:, :cols]
+
+
+# ---------------------------------------------------------------- workloads
+
+def test_workload_n4096_tf32_sampled_rows(tgemm):
+    w = inputs.WORKLOADS["n4096"]
+    A, B = inputs.operands(w)
+    C = run_tc(tgemm, A, B, "tf32").cpu()
+    rows = sorted(set([0, 127, 128, w.M - 1] +
+                      torch.randint(0, w.M, (44,), generator=inputs.generator(17)).tolist()))
+    C_ref, absAB = oracle.gemm_rows(A, B, rows)
+    assert_within(C[rows], C_ref, absAB, TC_REL, TC_ABS, "n4096 tf32")
+
+
+def test_workload_ffn_bf16_checked_rows(tgemm):
+    """Full FFN-shaped launch; the oracle checks the workload's 256 seeded rows."""
+    w = inputs.WORKLOADS["ffn_bf16"]
+    A, B = inputs.operands(w)
+    C = run_tc(tgemm, A, B, "bf16").cpu()
+    rows = inputs.check_rows(w).tolist()
+    C_ref, absAB = oracle.gemm_rows(A, B, rows)
+    assert_within(C[rows], C_ref, absAB, TC_REL, TC_ABS, "ffn bf16")
+
+
+# ---------------------------------------------------------------- shapes
+
+# Shapes keep K a multiple of 8 and N a multiple of 8 so packed operands meet
+# the 16-byte leading-dimension rule of the tensor-memory copies.
+SHAPES = [(1, 8, 8), (8, 8, 8), (128, 256, 64), (129, 264, 72), (127, 248, 40),
+          (300, 520, 200), (64, 1000, 8), (1000, 64, 16), (256, 512, 1024), (5, 16, 4104)]
+
+
+@pytest.mark.parametrize("kind", ["tf32", "bf16"])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_integer_bit_exact(tgemm, kind, shape):
+    M, N, K = shape
+    A, B = operands(M, N, K, "int4", kind, seed=M + 3 * N + 7 * K)
+    C_ref, _ = oracle.gemm(A, B)
+    assert_bit_exact(run_tc(tgemm, A, B, kind), C_ref, f"{kind} {shape}")
+
+
+@pytest.mark.parametrize("kind", ["tf32", "bf16"])
+@pytest.mark.parametrize("shape", [(200, 296, 136), (513, 1032, 520)])
+def test_float_tolerance(tgemm, kind, shape):
+    M, N, K = shape
+    dist = "normal" if kind == "tf32" else "normal002"
+    A, B = operands(M, N, K, dist, kind, seed=sum(shape))
+    C_ref, absAB = oracle.gemm(A, B)
+    assert_within(run_tc(tgemm, A, B, kind), C_ref, absAB, TC_REL, TC_ABS, f"{kind} {shape}")
+
+
+@pytest.mark.parametrize("kind", ["tf32", "bf16"])
+def test_ragged_edges_with_nan_padding(tgemm, kind):
+    """M, N, K not multiples of any tile; NaN in the ld padding must never be
+    read (the copies fill out-of-range elements with zeros)."""
+    M, N, K = 203, 301, 97
+    A, B = operands(M, N, K, "int4", kind, seed=5)
+    Ad = padded_cuda(A, 104)
+    Bd = padded_cuda(B, 312)
+    ldc, guard = 307, 32
+    store = torch.full((guard + M * ldc + guard,), -777.0, device="cuda")
+    C = store[guard:guard + M * ldc].view(M, ldc)[:, :N]
+    tgemm.gemm_tc(Ad, Bd, kind, out=C)
+    assert tgemm.device_status() == 0
+    C_ref, _ = oracle.gemm(A, B)
+    assert_bit_exact(C, C_ref, f"{kind} ragged")
+    host = store.cpu()
+    assert (host[:guard] == -777.0).all() and (host[guard + M * ldc:] == -777.0).all()
+    assert (host[guard:guard + M * ldc].view(M, ldc)[:, N:] == -777.0).all()
+
+
+def test_misaligned_leading_dimension_rejected(tgemm):
+    A = torch.ones(16, 12, dtype=torch.bfloat16, device="cuda")    # lda = 12 -> 24 bytes
+    B = torch.ones(12, 16, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(tgemm.TgemmError) as e:
+        tgemm.gemm_tc(A, B, "bf16")
+    assert e.value.status == 2
+
+
+def test_k_zero_writes_zeros(tgemm):
+    C = torch.full((9, 16), 5.0, device="cuda")
+    tgemm.gemm_tc(torch.empty(9, 0, device="cuda"), torch.empty(0, 16, device="cuda"),
+                  "tf32", out=C)
+    assert tgemm.device_status() == 0
+    assert (C == 0).all()
+
+
+def test_back_to_back_launches_reuse_tensor_memory(tgemm):
+    """Many launches in a row (each allocates and frees tensor memory)."""
+    A, B = operands(256, 512, 256, "int4", "bf16", seed=77)
+    C_ref, _ = oracle.gemm(A, B)
+    Ad, Bd = A.cuda(), B.cuda()
+    outs = [tgemm.gemm_tc(Ad, Bd, "bf16") for _ in range(20)]
+    assert tgemm.device_status() == 0
+    for C in outs:
+        assert_bit_exact(C, C_ref, "repeat")
+
+
+@pytest.mark.parametrize("kind", ["tf32", "bf16"])
+def test_matmul_host_round_trip(tgemm, kind):
+    A, B = operands(64, 72, 40, "int4", kind, seed=3)
+    C = tgemm.matmul(A.pin_memory(), B.pin_memory(), kind)
+    assert C.device.type == "cpu"
+    C_ref, _ = oracle.gemm(A, B)
+    assert_bit_exact(C, C_ref, f"matmul {kind}")

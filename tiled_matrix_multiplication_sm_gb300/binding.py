@@ -113,7 +113,9 @@ def _check_matrix(x: torch.Tensor, name: str, dtype: torch.dtype) -> int:
         raise TypeError(f"{name} must be {dtype}, got {x.dtype}")
     if x.shape[1] > 1 and x.stride(1) != 1:
         raise ValueError(f"{name} must have unit column stride (row-major)")
-    return max(int(x.stride(0)), int(x.shape[1]), 1) if x.shape[0] > 1 else max(int(x.shape[1]), 1)
+    # A one-row view keeps its row stride too, so a padded leading dimension
+    # is passed through unchanged (it decides which loaders may be used).
+    return max(int(x.stride(0)), int(x.shape[1]), 1)
 
 
 def _out(out, M, N, device):

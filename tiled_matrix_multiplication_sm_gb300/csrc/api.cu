@@ -1,0 +1,242 @@
+// C ABI of libtgemm.so: argument checks, kernel selection and launch.
+// The declarations and the contract of every entry point are in
+// include/tgemm.h.
+
+#include "../../include/tgemm.h"
+#include "tgemm_internal.h"
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    bool supported = false;
+    int num_sms = 0;
+    bool pool_ready = false;
+    cudaMemPool_t pool = nullptr;   // scratch for the TF32 path's transposed B
+};
+
+std::mutex g_mutex;
+DeviceInfo g_devices[kMaxDevices];
+void* g_encode_fn = nullptr;
+bool g_encode_looked_up = false;
+
+std::atomic<long long> g_wait_limit_ns{2000000000LL};
+std::atomic<int> g_debug_stall{0};
+std::atomic<int> g_forced_f32{-1};
+thread_local const char* g_last_kernel = "";
+
+// Device properties of the current device, looked up once per device.
+int current_device_info(DeviceInfo* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TGEMM_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return TGEMM_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo& d = g_devices[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return TGEMM_ERR_CUDA;
+        // The library carries sm_103a code only.
+        d.supported = (major == 10 && minor == 3);
+        d.num_sms = sms;
+        d.ready = true;
+    }
+    *out = d;
+    return d.supported ? TGEMM_OK : TGEMM_ERR_UNSUPPORTED;
+}
+
+// The library's stream-ordered scratch pool on device `dev`. Freed blocks
+// stay cached in the pool (no release threshold), so repeated calls do not
+// go back to the driver.
+cudaMemPool_t scratch_pool(int dev) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo& d = g_devices[dev];
+    if (!d.pool_ready) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
+        unsigned long long keep = ~0ull;
+        cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        d.pool = pool;
+        d.pool_ready = true;
+    }
+    return d.pool;
+}
+
+void* encode_fn() {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_encode_looked_up) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode_fn = fn;
+        g_encode_looked_up = true;
+    }
+    return g_encode_fn;
+}
+
+// Checks common to both paths. Returns TGEMM_OK, or an error, or -1 for
+// "valid and empty: nothing to do".
+int check_common(int M, int N, int K, const void* A, long lda, const void* B, long ldb,
+                 const float* C, long ldc) {
+    if (M < 0 || N < 0 || K < 0) return TGEMM_ERR_INVALID_ARG;
+    if (lda < K || ldb < N || ldc < N) return TGEMM_ERR_INVALID_ARG;
+    if (lda < 0 || ldb < 0 || ldc < 0) return TGEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return -1;
+    if (C == nullptr) return TGEMM_ERR_INVALID_ARG;
+    if (K > 0 && (A == nullptr || B == nullptr)) return TGEMM_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(C) % 4 != 0) return TGEMM_ERR_INVALID_ARG;
+    return TGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm_f32(int M, int N, int K, const float* A, long lda, const float* B, long ldb,
+             float* C, long ldc, cudaStream_t stream) {
+    g_last_kernel = "";
+    int st = check_common(M, N, K, A, lda, B, ldb, C, ldc);
+    if (st == -1) return TGEMM_OK;
+    if (st != TGEMM_OK) return st;
+    if (K > 0 && (reinterpret_cast<uintptr_t>(A) % 4 != 0 ||
+                  reinterpret_cast<uintptr_t>(B) % 4 != 0))
+        return TGEMM_ERR_INVALID_ARG;
+
+    DeviceInfo dev;
+    st = current_device_info(&dev);
+    if (st != TGEMM_OK) return st;
+
+    tgemm::GemmArgs a{M, N, K, A, lda, B, ldb, C, ldc};
+    if (K == 0) {
+        if (tgemm::zero_fill(C, ldc, M, N, stream) != cudaSuccess) return TGEMM_ERR_CUDA;
+        g_last_kernel = "zero_fill";
+        return TGEMM_OK;
+    }
+    int id = g_forced_f32.load();
+    if (id >= 0) {
+        if (!tgemm::f32_kernel_accepts(id, a)) return TGEMM_ERR_ALIGNMENT;
+    } else {
+        id = tgemm::f32_select(a, dev.num_sms);
+    }
+    if (tgemm::f32_launch(id, a, stream) != cudaSuccess) return TGEMM_ERR_CUDA;
+    g_last_kernel = tgemm::f32_kernel_name(id);
+    return TGEMM_OK;
+}
+
+int gemm_tc(int M, int N, int K, const void* A, long lda, const void* B, long ldb,
+            float* C, long ldc, int in_type, cudaStream_t stream) {
+    g_last_kernel = "";
+    if (in_type != TGEMM_TF32 && in_type != TGEMM_BF16) return TGEMM_ERR_INVALID_ARG;
+    int st = check_common(M, N, K, A, lda, B, ldb, C, ldc);
+    if (st == -1) return TGEMM_OK;
+    if (st != TGEMM_OK) return st;
+    if (K > 0) {
+        const long esz = in_type == TGEMM_BF16 ? 2 : 4;
+        if (reinterpret_cast<uintptr_t>(A) % 16 != 0 || reinterpret_cast<uintptr_t>(B) % 16 != 0 ||
+            (lda * esz) % 16 != 0 || (ldb * esz) % 16 != 0)
+            return TGEMM_ERR_ALIGNMENT;
+    }
+
+    DeviceInfo dev;
+    st = current_device_info(&dev);
+    if (st != TGEMM_OK) return st;
+
+    if (K == 0) {
+        if (tgemm::zero_fill(C, ldc, M, N, stream) != cudaSuccess) return TGEMM_ERR_CUDA;
+        g_last_kernel = "zero_fill";
+        return TGEMM_OK;
+    }
+    void* enc = encode_fn();
+    if (enc == nullptr) return TGEMM_ERR_CUDA;
+    const unsigned long long limit = (unsigned long long)g_wait_limit_ns.load();
+    const int stall = g_debug_stall.load();
+    if (in_type == TGEMM_BF16) {
+        tgemm::GemmArgs a{M, N, K, A, lda, B, ldb, C, ldc};
+        if (tgemm::tc_launch(a, in_type, 0, dev.num_sms, enc, limit, stall, stream) != cudaSuccess)
+            return TGEMM_ERR_CUDA;
+        g_last_kernel = tgemm::tc_kernel_name(in_type);
+        return TGEMM_OK;
+    }
+    // TF32: the tensor core reads a TF32 B operand only K-major, so B is
+    // first transposed into stream-ordered scratch (N x ldt floats).
+    int devno = 0;
+    if (cudaGetDevice(&devno) != cudaSuccess) return TGEMM_ERR_CUDA;
+    cudaMemPool_t pool = scratch_pool(devno);
+    if (pool == nullptr) return TGEMM_ERR_CUDA;
+    const long ldt = (K + 3) / 4 * 4;
+    void* bt = nullptr;
+    if (cudaMallocFromPoolAsync(&bt, (size_t)N * ldt * sizeof(float), pool, stream) != cudaSuccess)
+        return TGEMM_ERR_CUDA;
+    int rc = TGEMM_OK;
+    if (tgemm::transpose_f32(static_cast<const float*>(B), ldb, static_cast<float*>(bt), ldt, K, N,
+                             stream) != cudaSuccess) {
+        rc = TGEMM_ERR_CUDA;
+    } else {
+        tgemm::GemmArgs a{M, N, K, A, lda, bt, ldt, C, ldc};
+        if (tgemm::tc_launch(a, in_type, 1, dev.num_sms, enc, limit, stall, stream) != cudaSuccess)
+            rc = TGEMM_ERR_CUDA;
+    }
+    if (cudaFreeAsync(bt, stream) != cudaSuccess && rc == TGEMM_OK) rc = TGEMM_ERR_CUDA;
+    if (rc == TGEMM_OK) g_last_kernel = tgemm::tc_kernel_name(in_type);
+    return rc;
+}
+
+int gemm_device_status(cudaStream_t stream) {
+    DeviceInfo dev;
+    int st = current_device_info(&dev);
+    if (st != TGEMM_OK) return st;
+    int v = 0;
+    if (tgemm::tc_read_and_clear_status(&v, stream) != cudaSuccess) return TGEMM_ERR_CUDA;
+    return v == 0 ? TGEMM_OK : TGEMM_ERR_DEVICE_TIMEOUT;
+}
+
+const char* gemm_status_string(int status) {
+    switch (status) {
+        case TGEMM_OK: return "ok";
+        case TGEMM_ERR_INVALID_ARG: return "invalid argument";
+        case TGEMM_ERR_ALIGNMENT: return "misaligned operand (16-byte pointers and ld needed)";
+        case TGEMM_ERR_CUDA: return "CUDA error";
+        case TGEMM_ERR_DEVICE_TIMEOUT: return "a kernel wait timed out";
+        case TGEMM_ERR_UNSUPPORTED: return "unsupported device (sm_103 required)";
+        default: return "unknown tgemm status";
+    }
+}
+
+int gemm_set_wait_limit_ns(long long ns) {
+    if (ns <= 0) return TGEMM_ERR_INVALID_ARG;
+    g_wait_limit_ns.store(ns);
+    return TGEMM_OK;
+}
+
+int gemm_set_debug_stall(int enable) {
+    g_debug_stall.store(enable ? 1 : 0);
+    return TGEMM_OK;
+}
+
+int gemm_set_f32_kernel(int id) {
+    if (id < -1 || id >= tgemm::f32_kernel_count()) return TGEMM_ERR_INVALID_ARG;
+    g_forced_f32.store(id);
+    return TGEMM_OK;
+}
+
+int gemm_f32_kernel_count(void) { return tgemm::f32_kernel_count(); }
+
+const char* gemm_f32_kernel_name(int id) { return tgemm::f32_kernel_name(id); }
+
+const char* gemm_last_kernel(void) { return g_last_kernel; }
+
+}  // extern "C"

@@ -1,0 +1,500 @@
+// Dense product C = A x B on the 5th-generation tensor cores of sm_103a
+// (tcgen05 MMA, accumulators in tensor memory), TF32 or BF16 inputs, FP32
+// output.
+//
+// It is the same tiling as "Tiled GEMM: Matrix Multiplication in CUDA",
+// sections 2 and 4 -- a block owns a tile of C and walks K in phases, staging
+// tiles of A and B on chip -- with each step moved to the unit that does it
+// best on this chip:
+//   * the cooperative load of each phase (section 4.4) is one Tensor Memory
+//     Accelerator copy per operand tile ("Tiled GEMM ...", section 8, TMA),
+//     into a ring of STAGES shared-memory buffers in the 128-byte swizzled
+//     layout the tensor core reads without bank conflicts;
+//   * the two barriers of each phase (sections 4.5 and 4.7: tile loaded
+//     before it is read, read before it is overwritten) are a "full" and an
+//     "empty" mbarrier per ring slot;
+//   * the inner product over the tile (section 4.6) is a chain of
+//     tcgen05.mma instructions issued by one thread, accumulating a
+//     128 x 256 FP32 tile in tensor memory;
+//   * the write-back (section 4.8) is done by four epilogue warps that read
+//     tensor memory with tcgen05.ld while the tensor core already works on
+//     the block's next tile (two accumulators, 2 x 256 columns).
+// The grid is persistent: one block per SM walks tiles in a grouped order so
+// that blocks running together share panels of A and B in L2.
+//
+// Ragged edges (section 7.1 of the same page): the TMA unit fills rows and
+// columns outside the matrices with zeros; stores past M and N are skipped.
+//
+// Operand layouts in shared memory: A (M x K, K contiguous) is K-major. For
+// BF16, B (K x N, N contiguous) is read MN-major through the instruction
+// descriptor's transpose bit, so neither operand is copied. The TF32 kind
+// reads B only K-major (with the MN-major bit set it produced zeros on
+// sm_103a), so the TF32 path hands this kernel B already transposed
+// (N x K, K contiguous) and reads it K-major like A.
+//
+// Every wait is bounded (a limit in nanoseconds, default 2 s). A wait that
+// runs out records TGEMM_ERR_DEVICE_TIMEOUT in a device status word and
+// raises a block-wide abort flag; all roles then leave their loops, wait
+// (bounded) for their own copies and MMAs still in flight, free tensor
+// memory and return. Nothing traps.
+
+#include "tgemm_internal.h"
+
+#include <cuda.h>
+#include <cstdint>
+
+namespace tgemm {
+
+__device__ int g_tc_status;
+
+namespace {
+
+constexpr int kStatusTimeout = 4;      // TGEMM_ERR_DEVICE_TIMEOUT
+
+constexpr int BM = 128;                // rows of a C tile (= MMA M)
+constexpr int BN = 256;                // columns of a C tile (= MMA N)
+constexpr int STAGES = 4;
+constexpr int SW = 128;                // bytes in one swizzled row
+constexpr int A_STAGE_BYTES = BM * SW;                 // 16 KB
+constexpr int B_STAGE_BYTES = 32 * 1024;               // BK x BN elements
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int TMEM_COLS = 2 * BN;                      // two accumulators
+constexpr int NUM_THREADS = 192;       // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int GROUP_M = 8;
+
+template <int ESZ> struct Kind;
+template <> struct Kind<2> {           // bf16 inputs, kind::f16
+    static constexpr int BK = 64;      // K elements per stage (one 128-byte row)
+    static constexpr int UMMA_K = 16;  // K per instruction
+    static constexpr uint32_t FMT = 1; // BF16
+};
+template <> struct Kind<4> {           // fp32 storage, kind::tf32
+    static constexpr int BK = 32;
+    static constexpr int UMMA_K = 8;
+    static constexpr uint32_t FMT = 2; // TF32
+};
+
+struct Sync {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tmem_full[2];
+    uint64_t tmem_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + (int)sizeof(Sync);
+
+struct TcParams {
+    int M, N, K;
+    float* C;
+    long ldc;
+    int tiles_m, tiles_n, num_tiles, kblocks;
+    unsigned long long wait_limit_ns;
+    int debug_stall;
+    int vec_c;
+};
+
+// ------------------------------------------------------------------ PTX
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Wait until the phase of `bar` with parity `parity` has completed. Gives up
+// (returns false) when the block's abort flag is raised or, if
+// `honour_abort` is false, only when `limit_ns` has passed; a wait that runs
+// out raises the abort flag and records the timeout.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Sync* sy,
+                                       unsigned long long limit_ns, bool honour_abort) {
+    if (mbar_try(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try(bar, parity)) return true;
+        if ((it & 15u) == 0) {
+            if (honour_abort && *(volatile int*)&sy->abort) return false;
+            if (globaltimer() - t0 > limit_ns || it >= (1u << 30)) {
+                *(volatile int*)&sy->abort = 1;
+                atomicCAS(&g_tc_status, 0, kStatusTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(bar) : "memory");
+}
+
+template <int ESZ>
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+    if constexpr (ESZ == 2) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+            :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
+            :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+    }
+}
+
+// 32 consecutive accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start
+// address, leading and stride byte offsets in 16-byte units, version 1).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFF) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+    d |= 1ull << 46;                     // descriptor version for tcgen05
+    d |= 2ull << 61;                     // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: FP32 accumulator, A K-major, B K-major or
+// MN-major, M x N.
+template <int ESZ, bool B_KMAJOR>
+__host__ __device__ constexpr uint32_t instr_desc() {
+    return (1u << 4)                         // D format F32
+         | (Kind<ESZ>::FMT << 7)             // A format
+         | (Kind<ESZ>::FMT << 10)            // B format
+         | (0u << 15)                        // A: K-major
+         | ((B_KMAJOR ? 0u : 1u) << 16)      // B: K-major (0) or MN-major (1)
+         | ((uint32_t)(BN >> 3) << 17)
+         | ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& mb, int& nb) {
+    const int per_group = GROUP_M * p.tiles_n;
+    const int first_m = (t / per_group) * GROUP_M;
+    const int gm = min(p.tiles_m - first_m, GROUP_M);
+    mb = first_m + (t % per_group) % gm;
+    nb = (t % per_group) / gm;
+}
+
+// B_KMAJOR: B arrives transposed (N x K, K contiguous) and is read K-major;
+// otherwise B is K x N (N contiguous) and is read MN-major.
+template <int ESZ, bool B_KMAJOR>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+               const __grid_constant__ CUtensorMap tmB,
+               const TcParams p) {
+    using KD = Kind<ESZ>;
+    constexpr int BK = KD::BK;
+    constexpr int K_STEPS = BK / KD::UMMA_K;
+    constexpr int B_CHUNK_COLS = SW / ESZ;               // N columns per swizzled row
+    constexpr int B_CHUNKS = BN / B_CHUNK_COLS;
+    constexpr int B_CHUNK_BYTES = BK * SW;
+    constexpr uint32_t A_K_STEP = KD::UMMA_K * ESZ;      // bytes along a K-major row
+    constexpr uint32_t B_K_STEP = KD::UMMA_K * SW;       // rows of the MN-major tile
+    static_assert(B_CHUNKS * B_CHUNK_BYTES == B_STAGE_BYTES, "B stage size");
+    constexpr uint32_t IDESC = instr_desc<ESZ, B_KMAJOR>();
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
+    Sync* sy = reinterpret_cast<Sync*>(smem + STAGES * STAGE_BYTES);
+    const uint32_t a_base = smem_u32(smem);
+    const uint32_t b_base = a_base + STAGES * A_STAGE_BYTES;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&sy->full[s]), 1);
+            mbar_init(smem_u32(&sy->empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&sy->tmem_full[a]), 1);
+            mbar_init(smem_u32(&sy->tmem_empty[a]), 128);
+        }
+        mbar_init(smem_u32(&sy->drain), 1);
+        sy->abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(smem_u32(&sy->tmem_base)), "n"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = sy->tmem_base;
+    const unsigned long long lim = p.wait_limit_ns;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t armed = 0, armed_parity = 0;   // per-stage fills in flight
+            int g = 0;
+            for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+                int mb, nb;
+                tile_coords(t, p, mb, nb);
+                for (int kb = 0; kb < p.kblocks; ++kb, ++g) {
+                    const int s = g % STAGES;
+                    const uint32_t ph = (uint32_t)(g / STAGES) & 1u;
+                    if (!mbar_wait(smem_u32(&sy->empty[s]), ph ^ 1u, sy, lim, true)) goto producer_done;
+                    if (p.debug_stall && g == 0) continue;     // test hook: never fill stage 0
+                    const uint32_t full = smem_u32(&sy->full[s]);
+                    mbar_arrive_expect_tx(full, STAGE_BYTES);
+                    tma_load_2d(a_base + s * A_STAGE_BYTES, &tmA, kb * BK, mb * BM, full);
+                    const uint32_t bdst = b_base + s * B_STAGE_BYTES;
+                    if constexpr (B_KMAJOR) {
+                        tma_load_2d(bdst, &tmB, kb * BK, nb * BN, full);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < B_CHUNKS; ++c)
+                            tma_load_2d(bdst + c * B_CHUNK_BYTES, &tmB, nb * BN + c * B_CHUNK_COLS,
+                                        kb * BK, full);
+                    }
+                    armed |= 1u << s;
+                    armed_parity = (armed_parity & ~(1u << s)) | (ph << s);
+                }
+            }
+        producer_done:
+            // Copies still in flight must land before the block may exit.
+            for (int s = 0; s < STAGES; ++s)
+                if (armed & (1u << s))
+                    mbar_wait(smem_u32(&sy->full[s]), (armed_parity >> s) & 1u, sy, lim, false);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int g = 0, it = 0;
+            for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+                const int acc = it & 1;
+                const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+                if (!mbar_wait(smem_u32(&sy->tmem_empty[acc]), aph ^ 1u, sy, lim, true)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                bool ok = true;
+                for (int kb = 0; kb < p.kblocks; ++kb, ++g) {
+                    const int s = g % STAGES;
+                    const uint32_t ph = (uint32_t)(g / STAGES) & 1u;
+                    if (!mbar_wait(smem_u32(&sy->full[s]), ph, sy, lim, true)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_addr = a_base + s * A_STAGE_BYTES;
+                    const uint32_t b_addr = b_base + s * B_STAGE_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < K_STEPS; ++kk) {
+                        const uint64_t ad = smem_desc(a_addr + kk * A_K_STEP, 16, 1024);
+                        const uint64_t bd =
+                            B_KMAJOR ? smem_desc(b_addr + kk * A_K_STEP, 16, 1024)
+                                     : smem_desc(b_addr + kk * B_K_STEP, B_CHUNK_BYTES, 1024);
+                        tc_mma<ESZ>(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    tc_commit(smem_u32(&sy->empty[s]));      // frees the slot when done
+                }
+                if (!ok) break;
+                tc_commit(smem_u32(&sy->tmem_full[acc]));    // accumulator ready
+            }
+            // Every MMA this thread issued must finish before TMEM is freed.
+            tc_commit(smem_u32(&sy->drain));
+            mbar_wait(smem_u32(&sy->drain), 0, sy, lim, false);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue (warps 2-5)
+        const int q = warp & 3;                 // TMEM lanes 32q .. 32q+31
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        int it = 0;
+        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+            int mb, nb;
+            tile_coords(t, p, mb, nb);
+            const int acc = it & 1;
+            const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+            bool ok = mbar_wait(smem_u32(&sy->tmem_full[acc]), aph, sy, lim, true);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            const int row = mb * BM + q * 32 + lane;
+            float* crow = p.C + (long)row * p.ldc;
+            for (int c = 0; c < BN / 32; ++c) {
+                const int col0 = nb * BN + c * 32;
+                if (col0 >= p.N) break;                     // uniform across the warp
+                uint32_t r[32];
+                tmem_ld32(tmem_base + lane_off + (uint32_t)(acc * BN + c * 32), r);
+                if (row < p.M) {
+                    if (p.vec_c && col0 + 31 < p.N) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<float4*>(crow + col0 + j) =
+                                make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                                            __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col0 + j < p.N) crow[col0 + j] = __uint_as_float(r[j]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(smem_u32(&sy->tmem_empty[acc]));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                     :: "r"(tmem_base), "n"(TMEM_COLS) : "memory");
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// 2-D row-major tensor map: `cols` contiguous elements per row, `rows`
+// rows `ld` elements apart; boxes of box_cols x box_rows, 128-byte swizzle.
+bool encode_2d(EncodeTiledFn enc, CUtensorMap* map, const void* base, int esz, long rows,
+               long cols, long ld, int box_cols, int box_rows) {
+    const CUtensorMapDataType dt =
+        esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * esz};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int ESZ, bool B_KMAJOR>
+cudaError_t launch_tc(const GemmArgs& a, int num_sms, EncodeTiledFn enc,
+                      unsigned long long wait_limit_ns, int debug_stall, cudaStream_t s) {
+    constexpr int BK = Kind<ESZ>::BK;
+    CUtensorMap tmA, tmB;
+    if (!encode_2d(enc, &tmA, a.A, ESZ, a.M, a.K, a.lda, BK, BM)) return cudaErrorInvalidValue;
+    const bool okb = B_KMAJOR ? encode_2d(enc, &tmB, a.B, ESZ, a.N, a.K, a.ldb, BK, BN)
+                              : encode_2d(enc, &tmB, a.B, ESZ, a.K, a.N, a.ldb, SW / ESZ, BK);
+    if (!okb) return cudaErrorInvalidValue;
+
+    TcParams p;
+    p.M = a.M; p.N = a.N; p.K = a.K;
+    p.C = a.C; p.ldc = a.ldc;
+    p.tiles_m = (a.M + BM - 1) / BM;
+    p.tiles_n = (a.N + BN - 1) / BN;
+    p.num_tiles = p.tiles_m * p.tiles_n;
+    p.kblocks = (a.K + BK - 1) / BK;
+    p.wait_limit_ns = wait_limit_ns;
+    p.debug_stall = debug_stall;
+    p.vec_c = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0 && a.ldc % 4 == 0) ? 1 : 0;
+
+    auto kern = tc_gemm_kernel<ESZ, B_KMAJOR>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
+    kern<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tmA, tmB, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+const char* tc_kernel_name(int in_type) {
+    return in_type == TC_BF16 ? "tc_bf16_128x256x64_s4_persistent"
+                              : "transpose_b+tc_tf32_128x256x32_s4_persistent";
+}
+
+cudaError_t tc_launch(const GemmArgs& a, int in_type, int b_kmajor, int num_sms, void* encode_fn,
+                      unsigned long long wait_limit_ns, int debug_stall, cudaStream_t s) {
+    auto enc = reinterpret_cast<EncodeTiledFn>(encode_fn);
+    if (in_type == TC_BF16)
+        return b_kmajor ? launch_tc<2, true>(a, num_sms, enc, wait_limit_ns, debug_stall, s)
+                        : launch_tc<2, false>(a, num_sms, enc, wait_limit_ns, debug_stall, s);
+    return b_kmajor ? launch_tc<4, true>(a, num_sms, enc, wait_limit_ns, debug_stall, s)
+                    : launch_tc<4, false>(a, num_sms, enc, wait_limit_ns, debug_stall, s);
+}
+
+cudaError_t tc_read_and_clear_status(int* status, cudaStream_t s) {
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_tc_status, sizeof(int), 0,
+                                              cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    if (v != 0) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbolAsync(g_tc_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return e;
+        e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return e;
+    }
+    *status = v;
+    return cudaSuccess;
+}
+
+}  // namespace tgemm

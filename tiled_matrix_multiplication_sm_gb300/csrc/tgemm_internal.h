@@ -1,0 +1,49 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel files.
+// Not installed; callers use include/tgemm.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace tgemm {
+
+// Arguments of one product, already validated by the API layer.
+struct GemmArgs {
+    int M, N, K;
+    const void* A; long lda;
+    const void* B; long ldb;
+    float* C;      long ldc;
+};
+
+// ---- FP32 CUDA-core path (sgemm_f32.cu) ---------------------------------
+int  f32_kernel_count();
+const char* f32_kernel_name(int id);
+// True if configuration `id` may read these operands (vector loaders need
+// 16-byte aligned pointers and leading dimensions that are multiples of 4).
+bool f32_kernel_accepts(int id, const GemmArgs& a);
+// Pick a configuration for this shape and alignment.
+int  f32_select(const GemmArgs& a, int num_sms);
+// Launch configuration `id`; returns a cudaError_t.
+cudaError_t f32_launch(int id, const GemmArgs& a, cudaStream_t s);
+
+// ---- tcgen05 tensor-core path (gemm_tcgen05.cu) -------------------------
+enum TcType { TC_TF32 = 1, TC_BF16 = 2 };
+const char* tc_kernel_name(int in_type);
+// Launch the persistent tcgen05 kernel. `encode_fn` is cuTensorMapEncodeTiled.
+// With b_kmajor, a.B / a.ldb describe B transposed (N x K, K contiguous).
+cudaError_t tc_launch(const GemmArgs& a, int in_type, int b_kmajor, int num_sms,
+                      void* encode_fn, unsigned long long wait_limit_ns,
+                      int debug_stall, cudaStream_t s);
+// Read and clear the tensor-core kernel's status word on the current device.
+cudaError_t tc_read_and_clear_status(int* status, cudaStream_t s);
+
+// ---- layout pre-pass (transpose_f32.cu) ---------------------------------
+// Bt[n][k] = B[k][n] for a K x N matrix B (ldb) into Bt (N x K, ldt >= K).
+cudaError_t transpose_f32(const float* B, long ldb, float* Bt, long ldt, int K, int N,
+                          cudaStream_t s);
+
+// ---- shared helper (sgemm_f32.cu) -----------------------------------------
+// Write zeros to the M x N block of C (the K == 0 product).
+cudaError_t zero_fill(float* C, long ldc, int M, int N, cudaStream_t s);
+
+}  // namespace tgemm

@@ -1,0 +1,53 @@
+// Out-of-place transpose of an FP32 matrix: Bt[n][k] = B[k][n].
+//
+// The TF32 kind of the tcgen05 tensor-core instruction reads its B operand
+// only K-major (measured on sm_103a: with the MN-major bit set it produces
+// zeros), while the library's B is row-major K x N. The TF32 path therefore
+// first writes B transposed (N x K, K contiguous) into scratch memory.
+//
+// This is pure data movement, bound by HBM bandwidth: every element is read
+// once and written once. A 64 x 64 tile goes through shared memory so that
+// both the reads (along a row of B) and the writes (along a row of Bt) are
+// coalesced; the tile row is padded by one float so that reading it by
+// columns hits 32 different banks -- the padding of "Tiled GEMM: Matrix
+// Multiplication in CUDA", section 7.2, which the page recommends for
+// exactly this case of transposed tile accesses.
+
+#include "tgemm_internal.h"
+
+namespace tgemm {
+namespace {
+
+constexpr int TT = 64;          // tile edge
+constexpr int TROWS = 4;        // thread rows: 64 x 4 = 256 threads
+
+__global__ void __launch_bounds__(TT * TROWS)
+transpose_kernel(const float* __restrict__ B, long ldb, float* __restrict__ Bt, long ldt,
+                 int K, int N) {
+    __shared__ float tile[TT][TT + 1];
+    const int tx = threadIdx.x % TT, ty = threadIdx.x / TT;
+    const int n0 = blockIdx.x * TT, k0 = blockIdx.y * TT;
+#pragma unroll
+    for (int r = ty; r < TT; r += TROWS) {
+        const int k = k0 + r, n = n0 + tx;
+        tile[r][tx] = (k < K && n < N) ? B[(long)k * ldb + n] : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = ty; r < TT; r += TROWS) {
+        const int n = n0 + r, k = k0 + tx;
+        if (n < N && k < K) Bt[(long)n * ldt + k] = tile[tx][r];
+    }
+}
+
+}  // namespace
+
+cudaError_t transpose_f32(const float* B, long ldb, float* Bt, long ldt, int K, int N,
+                          cudaStream_t s) {
+    dim3 grid((N + TT - 1) / TT, (K + TT - 1) / TT);
+    if (grid.y > 65535) return cudaErrorInvalidValue;
+    transpose_kernel<<<grid, TT * TROWS, 0, s>>>(B, ldb, Bt, ldt, K, N);
+    return cudaGetLastError();
+}
+
+}  // namespace tgemm
