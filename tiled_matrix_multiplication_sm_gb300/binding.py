@@ -195,28 +195,31 @@ def last_kernel() -> str:
     return load().gemm_last_kernel().decode()
 
 
-def matmul(A: torch.Tensor, B: torch.Tensor, path: str = "f32") -> torch.Tensor:
+def matmul(A: torch.Tensor, B: torch.Tensor, path: str = "f32",
+           out: Optional[torch.Tensor] = None) -> torch.Tensor:
     """End-to-end product through the library for host or device operands.
 
     ``path`` is "f32" (CUDA cores), "tf32" or "bf16" (tensor cores). Host
     operands are copied to the current CUDA device (from pinned memory when
     they are pinned), multiplied there, and the result is copied back to the
-    host; device operands give a device result.
+    host (into ``out`` if given, ideally pinned) before the call returns;
+    device operands give a device result (in ``out`` if given).
     """
     on_host = A.device.type == "cpu"
     if on_host:
         dev = torch.device("cuda", torch.cuda.current_device())
         A = A.to(dev, non_blocking=A.is_pinned())
         B = B.to(dev, non_blocking=B.is_pinned())
+    dev_out = None if on_host else out
     if path == "f32":
-        C = gemm_f32(A, B)
+        C = gemm_f32(A, B, out=dev_out)
     elif path in _TC_TYPES:
-        C = gemm_tc(A, B, path)
+        C = gemm_tc(A, B, path, out=dev_out)
     else:
         raise ValueError(f"unknown path {path!r}")
     if on_host:
-        host = torch.empty(C.shape, dtype=C.dtype, pin_memory=True)
-        host.copy_(C, non_blocking=True)
+        host = out if out is not None else torch.empty(C.shape, dtype=C.dtype, pin_memory=True)
+        host.copy_(C, non_blocking=host.is_pinned())
         torch.cuda.current_stream().synchronize()
         return host
     return C
