@@ -173,6 +173,47 @@ TGEMM_API const char* gemm_f32_kernel_name(int id);
  */
 TGEMM_API const char* gemm_last_kernel(void);
 
+/*
+ * gemm_tc_tf32_noalloc — the TF32 product of gemm_tc(..., TGEMM_TF32, ...)
+ * for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point; it exists for the
+ * library's callers. gemm_tc's TF32 path needs scratch memory for B
+ * transposed and takes it from a stream-ordered memory pool. Callers that
+ * must not let a library allocate -- an application or plugin that reserves
+ * all of its device memory at start-up and treats any later allocation as a
+ * failure, or code that must not touch the device allocator while it runs
+ * -- call this instead: it allocates nothing (no cudaMalloc, cudaFree or
+ * allocating library routine) and keeps the transposed B in a fixed array of
+ * TGEMM_NOALLOC_SCRATCH_FLOATS floats (16 MiB) in the library's own device
+ * memory, which every device that loads the library holds until the process
+ * exits.
+ *
+ * Arguments, layout and result are those of gemm_tc with in_type TGEMM_TF32:
+ * A is M x K floats (16-byte aligned, lda >= K and a multiple of 4), B is
+ * K x N floats (4-byte aligned, ldb >= N), C is M x N floats (ldc >= N).
+ *
+ * Returns TGEMM_OK; TGEMM_ERR_INVALID_ARG for the argument errors of gemm_tc
+ * and when N * round_up(K, 4) > TGEMM_NOALLOC_SCRATCH_FLOATS (the problem does
+ * not fit the fixed scratch; nothing is launched); TGEMM_ERR_ALIGNMENT;
+ * TGEMM_ERR_UNSUPPORTED; TGEMM_ERR_CUDA.
+ *
+ * The first call on each device does that device's set-up (it looks up the
+ * device address of the scratch array with cudaGetSymbolAddress), so make
+ * the first call on a device before any stream capture. Every call shares
+ * the one array and leaves its contents behind; nothing in it has to start
+ * at zero because each call writes the part it reads first. Calls whose work
+ * overlaps on the GPU (on different streams or from different host threads)
+ * race on the array and give wrong results: serialise them.
+ */
+#define TGEMM_NOALLOC_SCRATCH_FLOATS 4194304L   /* 16 MiB of floats */
+
+TGEMM_API int gemm_tc_tf32_noalloc(int M, int N, int K,
+                                   const float* A, long lda,
+                                   const float* B, long ldb,
+                                   float* C, long ldc,
+                                   cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

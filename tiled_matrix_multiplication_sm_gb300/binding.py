@@ -42,6 +42,9 @@ _SIGNATURES = {
     "gemm_f32_kernel_count": (ctypes.c_int, []),
     "gemm_f32_kernel_name": (ctypes.c_char_p, [ctypes.c_int]),
     "gemm_last_kernel": (ctypes.c_char_p, []),
+    "gemm_tc_tf32_noalloc": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            _VP, ctypes.c_long, _VP, ctypes.c_long,
+                                            _VP, ctypes.c_long, _VP]),
 }
 
 
@@ -100,6 +103,12 @@ def gemm_f32_raw(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, stream_handle=0) -
 def gemm_tc_raw(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, in_type, stream_handle=0) -> int:
     return int(load().gemm_tc(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, in_type,
                               stream_handle))
+
+
+def gemm_tc_tf32_noalloc_raw(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, stream_handle=0) -> int:
+    """The allocation-free TF32 entry point; returns its status code."""
+    return int(load().gemm_tc_tf32_noalloc(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc,
+                                           stream_handle))
 
 
 def _check_matrix(x: torch.Tensor, name: str, dtype: torch.dtype) -> int:

@@ -1,0 +1,120 @@
+// gemm_tc_tf32_noalloc: the TF32 tensor-core product for callers that must
+// not allocate device memory.
+//
+// gemm_tc with TGEMM_TF32 needs scratch memory for B transposed (the TF32
+// kind of the tensor-core instruction reads B only K-major) and draws it from
+// a stream-ordered memory pool. Some callers cannot let a library allocate:
+// an application or plugin that reserves all of its device memory up front
+// and treats any later allocation as a failure, or code that must not touch
+// the device allocator while it runs. This entry point gives them the same
+// product with the scratch in a fixed array in the library's own device
+// memory (TGEMM_NOALLOC_SCRATCH_FLOATS floats, 16 MiB). Every device that
+// loads the library holds that array until the process exits.
+//
+// It runs the same two kernels as gemm_tc's TF32 path (transpose of B, then
+// the persistent tcgen05 GEMM), through the same launchers; only the
+// scratch pointer differs. Nothing in the scratch has to start at zero: each
+// call writes the N x round_up(K, 4) block it reads before reading it, and
+// the padding columns are never read. All calls share the one array, so
+// calls whose work overlaps on the GPU (different streams, or different
+// host threads) race on it and give wrong results; serialise them.
+
+#include "../../include/tgemm.h"
+#include "tgemm_internal.h"
+
+#include <cstdint>
+#include <mutex>
+
+namespace {
+
+static __device__ __align__(256) float g_noalloc_scratch[TGEMM_NOALLOC_SCRATCH_FLOATS];
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+struct Device {
+    bool ready = false;
+    bool supported = false;
+    int num_sms = 0;
+    float* scratch = nullptr;   // device address of g_noalloc_scratch
+};
+
+std::mutex g_mutex;
+Device g_devices[kMaxDevices];
+void* g_encode = nullptr;
+bool g_encode_done = false;
+
+// Set-up, once per device, with that device current: device attributes and
+// the device address of the scratch array. The array's name is a host-side
+// stand-in in host code; only the address from cudaGetSymbolAddress may be
+// handed to a kernel.
+int device_setup(Device* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TGEMM_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return TGEMM_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    Device& d = g_devices[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return TGEMM_ERR_CUDA;
+        d.supported = (major == 10 && minor == 3);
+        d.num_sms = sms;
+        if (d.supported) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+                return TGEMM_ERR_CUDA;
+            d.scratch = static_cast<float*>(p);
+        }
+        d.ready = true;
+    }
+    *out = d;
+    return d.supported ? TGEMM_OK : TGEMM_ERR_UNSUPPORTED;
+}
+
+void* encoder() {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_encode_done) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = fn;
+        g_encode_done = true;
+    }
+    return g_encode;
+}
+
+}  // namespace
+
+extern "C" int gemm_tc_tf32_noalloc(int M, int N, int K, const float* A, long lda,
+                                    const float* B, long ldb, float* C, long ldc,
+                                    cudaStream_t stream) {
+    if (M < 0 || N < 0 || K < 0) return TGEMM_ERR_INVALID_ARG;
+    if (lda < K || ldb < N || ldc < N || lda < 0 || ldb < 0 || ldc < 0) return TGEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return TGEMM_OK;
+    if (C == nullptr || reinterpret_cast<uintptr_t>(C) % 4 != 0) return TGEMM_ERR_INVALID_ARG;
+    if (K > 0 && (A == nullptr || B == nullptr)) return TGEMM_ERR_INVALID_ARG;
+    const long ldt = (K + 3) / 4 * 4;
+    if ((long long)N * ldt > (long long)TGEMM_NOALLOC_SCRATCH_FLOATS) return TGEMM_ERR_INVALID_ARG;
+    if (K > 0 && (reinterpret_cast<uintptr_t>(A) % 16 != 0 || reinterpret_cast<uintptr_t>(B) % 4 != 0 ||
+                  (lda * 4) % 16 != 0))
+        return TGEMM_ERR_ALIGNMENT;
+
+    Device d;
+    int st = device_setup(&d);
+    if (st != TGEMM_OK) return st;
+    if (K == 0)
+        return tgemm::zero_fill(C, ldc, M, N, stream) == cudaSuccess ? TGEMM_OK : TGEMM_ERR_CUDA;
+    void* enc = encoder();
+    if (enc == nullptr) return TGEMM_ERR_CUDA;
+    if (tgemm::transpose_f32(B, ldb, d.scratch, ldt, K, N, stream) != cudaSuccess)
+        return TGEMM_ERR_CUDA;
+    tgemm::GemmArgs a{M, N, K, A, lda, d.scratch, ldt, C, ldc};
+    if (tgemm::tc_launch(a, tgemm::TC_TF32, 1, d.num_sms, enc, kWaitLimitNs, 0, stream) != cudaSuccess)
+        return TGEMM_ERR_CUDA;
+    return TGEMM_OK;
+}
