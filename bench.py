@@ -280,14 +280,14 @@ def run_gpu(args):
     C32 = torch.empty(w.M, w.N, device=dev)
     Ctf = torch.empty(w.M, w.N, device=dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    launches_per_step = 3      # SGEMM; B transpose + tcgen05 GEMM
-
     def step():
         tg.gemm_f32(A, B, out=C32)
+        n32 = len(tg.binding.last_kernel().split("+"))
         tg.gemm_tc(A, B, "tf32", out=Ctf)
+        return n32 + len(tg.binding.last_kernel().split("+"))
 
     for _ in range(args.warmup):
-        step()
+        launches_per_step = step()     # kernels of the library per step
     torch.cuda.synchronize()
     if tg.device_status() != 0:
         raise RuntimeError("a kernel wait timed out during warm-up")

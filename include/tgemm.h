@@ -167,9 +167,11 @@ TGEMM_API int gemm_f32_kernel_count(void);
 TGEMM_API const char* gemm_f32_kernel_name(int id);
 
 /*
- * gemm_last_kernel — static name of the kernel configuration the most
- * recent successful gemm_f32 or gemm_tc call on this thread launched, or ""
- * if none did (empty product, error). For tests and benchmarks.
+ * gemm_last_kernel — name of the kernel(s) the most recent successful
+ * gemm_f32 or gemm_tc call on this thread launched, joined by '+' when a call
+ * launched more than one (e.g. a split-K reduction or the TF32 transpose), or
+ * "" if none did (empty product, error). Valid until the thread's next call.
+ * For tests and benchmarks.
  */
 TGEMM_API const char* gemm_last_kernel(void);
 

@@ -7,6 +7,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cstdio>
 #include <mutex>
 
 namespace {
@@ -30,6 +31,16 @@ std::atomic<long long> g_wait_limit_ns{2000000000LL};
 std::atomic<int> g_debug_stall{0};
 std::atomic<int> g_forced_f32{-1};
 thread_local const char* g_last_kernel = "";
+thread_local char g_last_kernel_buf[160];
+
+// Name of an FP32 launch: the configuration, plus the reduction kernel when
+// the plan splits the last wave along K.
+const char* f32_launch_name(int id, const tgemm::F32Plan& plan) {
+    if (plan.split <= 1) return tgemm::f32_kernel_name(id);
+    snprintf(g_last_kernel_buf, sizeof(g_last_kernel_buf), "%s+splitk_reduce(split=%d)",
+             tgemm::f32_kernel_name(id), plan.split);
+    return g_last_kernel_buf;
+}
 
 // Device properties of the current device, looked up once per device.
 int current_device_info(DeviceInfo* out) {
@@ -132,9 +143,25 @@ int gemm_f32(int M, int N, int K, const float* A, long lda, const float* B, long
     } else {
         id = tgemm::f32_select(a, dev.num_sms);
     }
-    if (tgemm::f32_launch(id, a, stream) != cudaSuccess) return TGEMM_ERR_CUDA;
-    g_last_kernel = tgemm::f32_kernel_name(id);
-    return TGEMM_OK;
+    const tgemm::F32Plan plan = tgemm::f32_plan(id, a, dev.num_sms);
+    if (plan.scratch_bytes == 0) {
+        if (tgemm::f32_launch(id, a, plan, nullptr, stream) != cudaSuccess) return TGEMM_ERR_CUDA;
+        g_last_kernel = f32_launch_name(id, plan);
+        return TGEMM_OK;
+    }
+    // Partial tiles of the split last wave live in stream-ordered scratch.
+    int devno = 0;
+    if (cudaGetDevice(&devno) != cudaSuccess) return TGEMM_ERR_CUDA;
+    cudaMemPool_t pool = scratch_pool(devno);
+    if (pool == nullptr) return TGEMM_ERR_CUDA;
+    void* ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, plan.scratch_bytes, pool, stream) != cudaSuccess)
+        return TGEMM_ERR_CUDA;
+    int rc = tgemm::f32_launch(id, a, plan, static_cast<float*>(ws), stream) == cudaSuccess
+                 ? TGEMM_OK : TGEMM_ERR_CUDA;
+    if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == TGEMM_OK) rc = TGEMM_ERR_CUDA;
+    if (rc == TGEMM_OK) g_last_kernel = f32_launch_name(id, plan);
+    return rc;
 }
 
 int gemm_tc(int M, int N, int K, const void* A, long lda, const void* B, long ldb,

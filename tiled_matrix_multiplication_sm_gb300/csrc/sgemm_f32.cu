@@ -8,8 +8,8 @@
 // its outputs from those on-chip copies. On top of that sit the refinements
 // the pages list as the next steps:
 //   * register blocking ("Tiling and Blocking for Reuse", "the next level:
-//     register blocking"): each thread owns a TM x TN patch of C in registers
-//     and reads 128-bit fragments of A and B from shared memory;
+//     register blocking"): each thread owns an 8 x 16 (default) patch of C in
+//     registers and reads 128-bit fragments of A and B from shared memory;
 //   * asynchronous copies and a multi-stage ring ("Tiled GEMM ...",
 //     section 8): cp.async moves global memory straight into shared memory,
 //     STAGES-1 phases ahead of the math, so the load of phase t+1 overlaps
@@ -18,13 +18,25 @@
 //     zero-filled (cp.async with a short source size), stores past M or N
 //     are skipped;
 //   * bank-conflict-free fragment reads (section 7.2 of the same page): A is
-//     kept row-major with a 4-float pad per row, so the four rows a warp
-//     reads at once fall in four different bank groups, and each quarter-warp
-//     reads one 128-byte run of B.
+//     kept row-major with a 4-float pad per row, a thread's rows are 4 apart,
+//     so the four rows a warp reads at once fall in four different bank
+//     groups, and each quarter-warp reads one 128-byte run of B.
 // The two barriers of the pages (after the load, before the overwrite) become
 // one __syncthreads per phase: with a ring of STAGES buffers, the barrier at
 // the top of phase t both publishes tile t and retires the buffer that the
 // prefetch issued right after it overwrites.
+//
+// The packed variants issue Blackwell's two-wide FP32 FMA (__ffma2_rn: two
+// independent round-to-nearest fused multiply-adds per instruction) on pairs
+// of adjacent output columns; each lane computes exactly what fmaf computes,
+// so packed and scalar kernels give identical bits.
+//
+// Tail balancing: tiles are independent ("every cell of C is independent",
+// "Tiled Matrix Multiplication in CUDA", section 1), so when the tile count
+// is not a multiple of the resident blocks, the tiles of the last partial
+// wave are split along K into `split` pieces. Each piece writes its partial
+// tile to scratch and splitk_reduce adds the pieces in a fixed order; the
+// result is deterministic.
 //
 // Within a thread every output accumulates its products in ascending k with
 // FP32 fused multiply-adds.
@@ -63,12 +75,13 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 // ------------------------------------------------------------ configuration
-template <int BM_, int BN_, int BK_, int WM_, int WN_, int STAGES_, int MIN_BLOCKS_>
+template <int BM_, int BN_, int BK_, int WM_, int WN_, int STAGES_, int MIN_BLOCKS_, bool PACKED_>
 struct Tile {
     static constexpr int BM = BM_, BN = BN_, BK = BK_;
     static constexpr int WM = WM_, WN = WN_;
     static constexpr int STAGES = STAGES_;
     static constexpr int MIN_BLOCKS = MIN_BLOCKS_;
+    static constexpr bool PACKED = PACKED_;
     static constexpr int WARPS_M = BM / WM, WARPS_N = BN / WN;
     static constexpr int THREADS = 32 * WARPS_M * WARPS_N;
     // A warp is 4 rows x 8 columns of threads.
@@ -87,6 +100,34 @@ struct Tile {
     static_assert((BM * BK) % THREADS == 0 && (BK * BN) % THREADS == 0,
                   "scalar loads must divide evenly over the threads");
 };
+
+struct F32Params {
+    const float* A;
+    long lda;
+    const float* B;
+    long ldb;
+    float* C;
+    long ldc;
+    int M, N, K;
+    int tiles_m, tiles_n;
+    int ktiles;          // ceil(K / BK)
+    int dp_tiles;        // tiles [0, dp_tiles) are computed whole
+    int split;           // the others in `split` K-pieces each
+    float* partials;     // (tiles - dp_tiles) * split partial tiles of BM x BN
+    int vec_c;           // C rows may take 16-byte stores
+};
+
+constexpr int GROUP_M = 8;
+
+// Grouped raster: GROUP_M tile-rows at a time, so that blocks running
+// together share panels of A and B in L2.
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& tm, int& tn) {
+    const int per_group = GROUP_M * tiles_n;
+    const int first_m = (t / per_group) * GROUP_M;
+    const int gm = min(tiles_m - first_m, GROUP_M);
+    tm = first_m + (t % per_group) % gm;
+    tn = (t % per_group) / gm;
+}
 
 // Copy the A tile (rows m0.., columns k0..) into shared memory.
 template <class T, bool VEC>
@@ -156,12 +197,61 @@ __device__ __forceinline__ void load_b(float* Bs, const float* __restrict__ B, l
     }
 }
 
+__device__ __forceinline__ float pick(const float4& v, int kk) {
+    return kk == 0 ? v.x : kk == 1 ? v.y : kk == 2 ? v.z : v.w;
+}
+
+// Register accumulators of one thread: TM rows x TN columns, stored as
+// pairs of adjacent columns (v[i][p] holds columns 2p and 2p+1 of row i), the
+// operand shape of the two-wide FMA.
+template <class T>
+struct Acc {
+    float2 v[T::TM][T::TN / 2];
+};
+
+// One BK-deep phase of outer products from shared memory.
+template <class T>
+__device__ __forceinline__ void mma_phase(Acc<T>& acc, const float* as, const float* bs) {
+#pragma unroll
+    for (int k4 = 0; k4 < T::BK; k4 += 4) {
+        float4 a[T::TM];
+#pragma unroll
+        for (int i = 0; i < T::TM; ++i)
+            a[i] = *reinterpret_cast<const float4*>(as + (4 * i) * T::ALD + k4);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            float4 b[T::NG];
+#pragma unroll
+            for (int g = 0; g < T::NG; ++g)
+                b[g] = *reinterpret_cast<const float4*>(bs + (k4 + kk) * T::BLD + g * 32);
+#pragma unroll
+            for (int i = 0; i < T::TM; ++i) {
+                const float av = pick(a[i], kk);
+                if constexpr (T::PACKED) {
+                    const float2 a2 = make_float2(av, av);
+#pragma unroll
+                    for (int g = 0; g < T::NG; ++g) {
+                        acc.v[i][2 * g] = __ffma2_rn(a2, make_float2(b[g].x, b[g].y), acc.v[i][2 * g]);
+                        acc.v[i][2 * g + 1] =
+                            __ffma2_rn(a2, make_float2(b[g].z, b[g].w), acc.v[i][2 * g + 1]);
+                    }
+                } else {
+#pragma unroll
+                    for (int g = 0; g < T::NG; ++g) {
+                        acc.v[i][2 * g].x = fmaf(av, b[g].x, acc.v[i][2 * g].x);
+                        acc.v[i][2 * g].y = fmaf(av, b[g].y, acc.v[i][2 * g].y);
+                        acc.v[i][2 * g + 1].x = fmaf(av, b[g].z, acc.v[i][2 * g + 1].x);
+                        acc.v[i][2 * g + 1].y = fmaf(av, b[g].w, acc.v[i][2 * g + 1].y);
+                    }
+                }
+            }
+        }
+    }
+}
+
 template <class T, bool VA, bool VB>
 __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
-sgemm_kernel(const float* __restrict__ A, long lda,
-             const float* __restrict__ B, long ldb,
-             float* __restrict__ C, long ldc,
-             int M, int N, int K, int vec_c) {
+sgemm_kernel(const F32Params p) {
     extern __shared__ __align__(16) float smem[];
     float* As = smem;                               // [STAGES][BM][ALD]
     float* Bs = smem + T::STAGES * T::A_STAGE;      // [STAGES][BK][BLD]
@@ -171,40 +261,48 @@ sgemm_kernel(const float* __restrict__ A, long lda,
     const int warp_m = warp / T::WARPS_N, warp_n = warp % T::WARPS_N;
     const int ty = lane >> 3, tx = lane & 7;
 
-    // Tile raster: walk GROUP tile-rows at a time so that blocks running
-    // together share panels of A and B in L2.
-    constexpr int GROUP = 8;
-    const int tiles_m = (M + T::BM - 1) / T::BM;
-    const int tiles_n = (N + T::BN - 1) / T::BN;
-    const int pid = blockIdx.x;
-    const int per_group = GROUP * tiles_n;
-    const int first_m = (pid / per_group) * GROUP;
-    const int group_m = min(tiles_m - first_m, GROUP);
-    const int tile_m = first_m + (pid % per_group) % group_m;
-    const int tile_n = (pid % per_group) / group_m;
+    // Work item: a whole tile, or one K-piece of a tile of the last wave.
+    int tile, kt_begin, kt_end;
+    long piece = -1;
+    if ((int)blockIdx.x < p.dp_tiles) {
+        tile = blockIdx.x;
+        kt_begin = 0;
+        kt_end = p.ktiles;
+    } else {
+        piece = (long)blockIdx.x - p.dp_tiles;
+        const int j = (int)(piece % p.split);
+        tile = p.dp_tiles + (int)(piece / p.split);
+        kt_begin = (int)((long)j * p.ktiles / p.split);
+        kt_end = (int)((long)(j + 1) * p.ktiles / p.split);
+    }
+    int tile_m, tile_n;
+    tile_coords(tile, p.tiles_m, p.tiles_n, tile_m, tile_n);
     const int m0 = tile_m * T::BM, n0 = tile_n * T::BN;
-
     const int wm0 = warp_m * T::WM, wn0 = warp_n * T::WN;
+    const float* __restrict__ A = p.A;
+    const float* __restrict__ B = p.B;
+    const int M = p.M, N = p.N, K = p.K;
 
-    float acc[T::TM][T::TN];
+    Acc<T> acc;
 #pragma unroll
     for (int i = 0; i < T::TM; ++i)
 #pragma unroll
-        for (int j = 0; j < T::TN; ++j) acc[i][j] = 0.0f;
+        for (int j = 0; j < T::TN / 2; ++j) acc.v[i][j] = make_float2(0.0f, 0.0f);
 
-    const int ktiles = (K + T::BK - 1) / T::BK;
+    const int nk = kt_end - kt_begin;
 
-    // Prologue: put phases 0 .. STAGES-2 in flight.
+    // Prologue: put phases 0 .. STAGES-2 of this work item in flight.
 #pragma unroll
     for (int s = 0; s < T::STAGES - 1; ++s) {
-        if (s < ktiles) {
-            load_a<T, VA>(As + s * T::A_STAGE, A, lda, M, K, m0, s * T::BK, tid);
-            load_b<T, VB>(Bs + s * T::B_STAGE, B, ldb, N, K, s * T::BK, n0, tid);
+        if (s < nk) {
+            const int k0 = (kt_begin + s) * T::BK;
+            load_a<T, VA>(As + s * T::A_STAGE, A, p.lda, M, K, m0, k0, tid);
+            load_b<T, VB>(Bs + s * T::B_STAGE, B, p.ldb, N, K, k0, n0, tid);
         }
         cp_async_commit();
     }
 
-    for (int kt = 0; kt < ktiles; ++kt) {
+    for (int kt = 0; kt < nk; ++kt) {
         // Phase kt's copies are done (for this thread) ...
         cp_async_wait<T::STAGES - 2>();
         // ... and for every thread; also, everyone has finished phase kt-1,
@@ -212,62 +310,89 @@ sgemm_kernel(const float* __restrict__ A, long lda,
         __syncthreads();
 
         const int pf = kt + T::STAGES - 1;
-        if (pf < ktiles) {
+        if (pf < nk) {
             const int ps = pf % T::STAGES;
-            load_a<T, VA>(As + ps * T::A_STAGE, A, lda, M, K, m0, pf * T::BK, tid);
-            load_b<T, VB>(Bs + ps * T::B_STAGE, B, ldb, N, K, pf * T::BK, n0, tid);
+            const int k0 = (kt_begin + pf) * T::BK;
+            load_a<T, VA>(As + ps * T::A_STAGE, A, p.lda, M, K, m0, k0, tid);
+            load_b<T, VB>(Bs + ps * T::B_STAGE, B, p.ldb, N, K, k0, n0, tid);
         }
         cp_async_commit();
 
         const int st = kt % T::STAGES;
-        const float* as = As + st * T::A_STAGE + (wm0 + ty) * T::ALD;
-        const float* bs = Bs + st * T::B_STAGE + wn0 + tx * 4;
-#pragma unroll
-        for (int k4 = 0; k4 < T::BK; k4 += 4) {
-            float4 a[T::TM];
-#pragma unroll
-            for (int i = 0; i < T::TM; ++i)
-                a[i] = *reinterpret_cast<const float4*>(as + (4 * i) * T::ALD + k4);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                float4 b[T::NG];
-#pragma unroll
-                for (int g = 0; g < T::NG; ++g)
-                    b[g] = *reinterpret_cast<const float4*>(bs + (k4 + kk) * T::BLD + g * 32);
-#pragma unroll
-                for (int i = 0; i < T::TM; ++i) {
-                    const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
-#pragma unroll
-                    for (int g = 0; g < T::NG; ++g) {
-                        acc[i][4 * g + 0] = fmaf(av, b[g].x, acc[i][4 * g + 0]);
-                        acc[i][4 * g + 1] = fmaf(av, b[g].y, acc[i][4 * g + 1]);
-                        acc[i][4 * g + 2] = fmaf(av, b[g].z, acc[i][4 * g + 2]);
-                        acc[i][4 * g + 3] = fmaf(av, b[g].w, acc[i][4 * g + 3]);
-                    }
-                }
-            }
-        }
+        mma_phase<T>(acc, As + st * T::A_STAGE + (wm0 + ty) * T::ALD,
+                     Bs + st * T::B_STAGE + wn0 + tx * 4);
     }
     cp_async_wait<0>();
 
-    // Epilogue: one store per output (section 4.8 of the second page),
-    // 16-byte stores where C allows them, skipped past M and N.
+    if (piece < 0) {
+        // Epilogue: one store per output (section 4.8 of the second page),
+        // 16-byte stores where C allows them, skipped past M and N.
 #pragma unroll
-    for (int i = 0; i < T::TM; ++i) {
-        const int row = m0 + wm0 + ty + 4 * i;
-        if (row >= M) continue;
-        float* crow = C + (long)row * ldc;
+        for (int i = 0; i < T::TM; ++i) {
+            const int row = m0 + wm0 + ty + 4 * i;
+            if (row >= M) continue;
+            float* crow = p.C + (long)row * p.ldc;
 #pragma unroll
-        for (int g = 0; g < T::NG; ++g) {
-            const int col = n0 + wn0 + g * 32 + tx * 4;
-            if (vec_c && col + 3 < N) {
-                *reinterpret_cast<float4*>(crow + col) =
-                    make_float4(acc[i][4 * g], acc[i][4 * g + 1], acc[i][4 * g + 2], acc[i][4 * g + 3]);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (col + j < N) crow[col + j] = acc[i][4 * g + j];
+            for (int g = 0; g < T::NG; ++g) {
+                const int col = n0 + wn0 + g * 32 + tx * 4;
+                const float4 v = make_float4(acc.v[i][2 * g].x, acc.v[i][2 * g].y,
+                                             acc.v[i][2 * g + 1].x, acc.v[i][2 * g + 1].y);
+                if (p.vec_c && col + 3 < N) {
+                    *reinterpret_cast<float4*>(crow + col) = v;
+                } else {
+                    if (col < N) crow[col] = v.x;
+                    if (col + 1 < N) crow[col + 1] = v.y;
+                    if (col + 2 < N) crow[col + 2] = v.z;
+                    if (col + 3 < N) crow[col + 3] = v.w;
+                }
             }
+        }
+    } else {
+        // A K-piece: the whole BM x BN partial tile goes to scratch.
+        float* part = p.partials + piece * (long)(T::BM * T::BN);
+#pragma unroll
+        for (int i = 0; i < T::TM; ++i) {
+            float* prow = part + (long)(wm0 + ty + 4 * i) * T::BN;
+#pragma unroll
+            for (int g = 0; g < T::NG; ++g)
+                *reinterpret_cast<float4*>(prow + wn0 + g * 32 + tx * 4) =
+                    make_float4(acc.v[i][2 * g].x, acc.v[i][2 * g].y, acc.v[i][2 * g + 1].x,
+                                acc.v[i][2 * g + 1].y);
+        }
+    }
+}
+
+// Sum the K-pieces of every split tile, piece 0 first, and store to C.
+template <class T>
+__global__ void __launch_bounds__(256)
+splitk_reduce(const F32Params p) {
+    constexpr int Q = T::BN / 4;                       // float4 per tile row
+    const long per_tile = (long)T::BM * Q;
+    const long total = (long)(p.tiles_m * p.tiles_n - p.dp_tiles) * per_tile;
+    for (long u = blockIdx.x * (long)blockDim.x + threadIdx.x; u < total;
+         u += (long)gridDim.x * blockDim.x) {
+        const int r = (int)(u / per_tile);
+        const int e = (int)(u % per_tile);
+        const int row = e / Q, c4 = (e % Q) * 4;
+        int tm, tn;
+        tile_coords(p.dp_tiles + r, p.tiles_m, p.tiles_n, tm, tn);
+        const int grow = tm * T::BM + row, gcol = tn * T::BN + c4;
+        if (grow >= p.M || gcol >= p.N) continue;
+        const float* src = p.partials + (long)r * p.split * (T::BM * T::BN) + row * T::BN + c4;
+        float4 s = *reinterpret_cast<const float4*>(src);
+        for (int j = 1; j < p.split; ++j) {
+            const float4 v = *reinterpret_cast<const float4*>(src + (long)j * (T::BM * T::BN));
+            s.x += v.x;
+            s.y += v.y;
+            s.z += v.z;
+            s.w += v.w;
+        }
+        float* dst = p.C + (long)grow * p.ldc + gcol;
+        if (p.vec_c && gcol + 3 < p.N) {
+            *reinterpret_cast<float4*>(dst) = s;
+        } else {
+            const float v[4] = {s.x, s.y, s.z, s.w};
+            for (int j = 0; j < 4 && gcol + j < p.N; ++j) dst[j] = v[j];
         }
     }
 }
@@ -282,40 +407,85 @@ __global__ void zero_fill_kernel(float* __restrict__ C, long ldc, int M, int N) 
 }
 
 // ------------------------------------------------------------ the table
-using Big = Tile<128, 128, 16, 32, 64, 4, 2>;    // 256 threads, 8x8 per thread
-using Small = Tile<64, 64, 16, 32, 32, 4, 4>;    // 128 threads, 8x4 per thread
+// Default: 128 x 256 block tile, 8 warps of 32 x 128, 8 x 16 outputs per
+// thread in column pairs (two-wide FMA), BK = 32, 3 stages, one block per SM.
+using Wide32P1 = Tile<128, 256, 32, 32, 128, 3, 1, true>;
+// Alternatives kept for tile selection by measurement and for tests.
+using Wide16P1 = Tile<128, 256, 16, 32, 128, 4, 1, true>;
+using Big32P1 = Tile<128, 128, 32, 32, 64, 3, 1, true>;
+using Big16P = Tile<128, 128, 16, 32, 64, 4, 2, true>;
+using Big16 = Tile<128, 128, 16, 32, 64, 4, 2, false>;   // scalar FFMA, 8 x 8 per thread
+using Small = Tile<64, 64, 16, 32, 32, 4, 4, false>;     // 128 threads, 8 x 4 per thread
+
+// Work split of one launch: dp_tiles whole tiles, the rest in `split`
+// K-pieces each. `slots` is the number of blocks resident at once.
+void plan_split(int tiles, int slots, int ktiles, int& dp_tiles, int& split) {
+    dp_tiles = tiles;
+    split = 1;
+    const int rem = tiles % slots;
+    if (rem == 0) return;
+    const int full = tiles - rem;
+    // Time of the tail in units of one whole-tile time, for s pieces per
+    // tile: ceil(rem * s / slots) rounds of 1/s.
+    double best = 1.0;
+    int best_s = 1;
+    for (int s = 2; s <= 16; ++s) {
+        if (ktiles / s < 4) break;                 // pieces of at least 4 phases
+        const double t = (double)((rem * s + slots - 1) / slots) / s;
+        if (t < best * 0.95) {
+            best = t;
+            best_s = s;
+        }
+    }
+    if (best_s > 1) {
+        dp_tiles = full;
+        split = best_s;
+    }
+}
 
 struct Entry {
     const char* name;
     bool va, vb;
-    int bm, bn;
-    cudaError_t (*launch)(const GemmArgs&, cudaStream_t);
+    int bm, bn, bk, min_blocks;
+    cudaError_t (*launch)(const F32Params&, int blocks, cudaStream_t);
+    cudaError_t (*reduce)(const F32Params&, cudaStream_t);
 };
 
 template <class T, bool VA, bool VB>
-cudaError_t launch_cfg(const GemmArgs& a, cudaStream_t s) {
+cudaError_t launch_cfg(const F32Params& p, int blocks, cudaStream_t s) {
     auto kern = sgemm_kernel<T, VA, VB>;
     static_assert(T::SMEM_BYTES <= 227 * 1024, "shared memory budget");
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          T::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const int tiles = ((a.M + T::BM - 1) / T::BM) * ((a.N + T::BN - 1) / T::BN);
-    const bool vec_c = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) && (a.ldc % 4 == 0);
-    kern<<<tiles, T::THREADS, T::SMEM_BYTES, s>>>(
-        static_cast<const float*>(a.A), a.lda, static_cast<const float*>(a.B), a.ldb,
-        a.C, a.ldc, a.M, a.N, a.K, vec_c ? 1 : 0);
+    kern<<<blocks, T::THREADS, T::SMEM_BYTES, s>>>(p);
     return cudaGetLastError();
 }
 
+template <class T>
+cudaError_t reduce_cfg(const F32Params& p, cudaStream_t s) {
+    const long units = (long)(p.tiles_m * p.tiles_n - p.dp_tiles) * T::BM * (T::BN / 4);
+    long blocks = (units + 255) / 256;
+    if (blocks > 8192) blocks = 8192;
+    splitk_reduce<T><<<(int)blocks, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+#define TGEMM_ENTRY(name, T, VA, VB)                                                       \
+    {name, VA, VB, T::BM, T::BN, T::BK, T::MIN_BLOCKS, launch_cfg<T, VA, VB>, reduce_cfg<T>}
+
 const Entry kTable[] = {
-    {"f32_128x128x16_s4_vecA_vecB", true, true, 128, 128, launch_cfg<Big, true, true>},
-    {"f32_128x128x16_s4_vecA_b4", true, false, 128, 128, launch_cfg<Big, true, false>},
-    {"f32_128x128x16_s4_a4_vecB", false, true, 128, 128, launch_cfg<Big, false, true>},
-    {"f32_128x128x16_s4_a4_b4", false, false, 128, 128, launch_cfg<Big, false, false>},
-    {"f32_64x64x16_s4_vecA_vecB", true, true, 64, 64, launch_cfg<Small, true, true>},
-    {"f32_64x64x16_s4_vecA_b4", true, false, 64, 64, launch_cfg<Small, true, false>},
-    {"f32_64x64x16_s4_a4_vecB", false, true, 64, 64, launch_cfg<Small, false, true>},
-    {"f32_64x64x16_s4_a4_b4", false, false, 64, 64, launch_cfg<Small, false, false>},
+    TGEMM_ENTRY("f32_128x256x32_s3_ffma2_vecA_vecB", Wide32P1, true, true),
+    TGEMM_ENTRY("f32_128x256x32_s3_ffma2_vecA_b4", Wide32P1, true, false),
+    TGEMM_ENTRY("f32_128x256x32_s3_ffma2_a4_vecB", Wide32P1, false, true),
+    TGEMM_ENTRY("f32_128x256x32_s3_ffma2_a4_b4", Wide32P1, false, false),
+    TGEMM_ENTRY("f32_128x256x16_s4_ffma2_vecA_vecB", Wide16P1, true, true),
+    TGEMM_ENTRY("f32_128x128x32_s3_ffma2_1blk_vecA_vecB", Big32P1, true, true),
+    TGEMM_ENTRY("f32_128x128x16_s4_ffma2_2blk_vecA_vecB", Big16P, true, true),
+    TGEMM_ENTRY("f32_128x128x16_s4_ffma_vecA_vecB", Big16, true, true),
+    TGEMM_ENTRY("f32_128x128x16_s4_ffma_a4_b4", Big16, false, false),
+    TGEMM_ENTRY("f32_64x64x16_s4_ffma_vecA_vecB", Small, true, true),
+    TGEMM_ENTRY("f32_64x64x16_s4_ffma_a4_b4", Small, false, false),
 };
 constexpr int kTableSize = sizeof(kTable) / sizeof(kTable[0]);
 
@@ -339,15 +509,50 @@ bool f32_kernel_accepts(int id, const GemmArgs& a) {
 }
 
 int f32_select(const GemmArgs& a, int num_sms) {
+    (void)num_sms;   // one tile shape wins on every measured shape class
     const bool va = vec_ok(a.A, a.lda), vb = vec_ok(a.B, a.ldb);
-    const long big_tiles = (long)((a.M + 127) / 128) * ((a.N + 127) / 128);
-    const int base = big_tiles >= num_sms ? 0 : 4;
-    const int loader = (va ? 0 : 2) + (vb ? 0 : 1);
-    return base + loader;
+    return (va ? 0 : 2) + (vb ? 0 : 1);
 }
 
-cudaError_t f32_launch(int id, const GemmArgs& a, cudaStream_t s) {
-    return kTable[id].launch(a, s);
+F32Plan f32_plan(int id, const GemmArgs& a, int num_sms) {
+    const Entry& e = kTable[id];
+    F32Plan pl;
+    pl.tiles_m = (a.M + e.bm - 1) / e.bm;
+    pl.tiles_n = (a.N + e.bn - 1) / e.bn;
+    pl.ktiles = (a.K + e.bk - 1) / e.bk;
+    plan_split(pl.tiles_m * pl.tiles_n, num_sms * e.min_blocks, pl.ktiles, pl.dp_tiles,
+               pl.split);
+    pl.scratch_bytes = pl.split > 1
+        ? (size_t)(pl.tiles_m * pl.tiles_n - pl.dp_tiles) * pl.split * e.bm * e.bn * sizeof(float)
+        : 0;
+    return pl;
+}
+
+cudaError_t f32_launch(int id, const GemmArgs& a, const F32Plan& pl, float* scratch,
+                       cudaStream_t s) {
+    const Entry& e = kTable[id];
+    F32Params p;
+    p.A = static_cast<const float*>(a.A);
+    p.lda = a.lda;
+    p.B = static_cast<const float*>(a.B);
+    p.ldb = a.ldb;
+    p.C = a.C;
+    p.ldc = a.ldc;
+    p.M = a.M;
+    p.N = a.N;
+    p.K = a.K;
+    p.tiles_m = pl.tiles_m;
+    p.tiles_n = pl.tiles_n;
+    p.ktiles = pl.ktiles;
+    p.dp_tiles = pl.dp_tiles;
+    p.split = pl.split;
+    p.partials = scratch;
+    p.vec_c = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0 && a.ldc % 4 == 0) ? 1 : 0;
+    const int tiles = pl.tiles_m * pl.tiles_n;
+    const int blocks = pl.dp_tiles + (tiles - pl.dp_tiles) * (pl.split > 1 ? pl.split : 0);
+    cudaError_t err = e.launch(p, blocks, s);
+    if (err != cudaSuccess || pl.split <= 1) return err;
+    return e.reduce(p, s);
 }
 
 cudaError_t zero_fill(float* C, long ldc, int M, int N, cudaStream_t s) {

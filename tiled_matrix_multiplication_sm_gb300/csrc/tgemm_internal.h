@@ -23,8 +23,19 @@ const char* f32_kernel_name(int id);
 bool f32_kernel_accepts(int id, const GemmArgs& a);
 // Pick a configuration for this shape and alignment.
 int  f32_select(const GemmArgs& a, int num_sms);
-// Launch configuration `id`; returns a cudaError_t.
-cudaError_t f32_launch(int id, const GemmArgs& a, cudaStream_t s);
+// How configuration `id` covers this problem: tiles computed whole, and the
+// tiles of a partial last wave split into K-pieces whose partial tiles need
+// `scratch_bytes` of device scratch (0 when nothing is split).
+struct F32Plan {
+    int tiles_m, tiles_n, ktiles;
+    int dp_tiles, split;
+    size_t scratch_bytes;
+};
+F32Plan f32_plan(int id, const GemmArgs& a, int num_sms);
+// Launch configuration `id` under plan `pl` (plus the split-K reduction when
+// the plan splits); `scratch` holds pl.scratch_bytes. Returns a cudaError_t.
+cudaError_t f32_launch(int id, const GemmArgs& a, const F32Plan& pl, float* scratch,
+                       cudaStream_t s);
 
 // ---- tcgen05 tensor-core path (gemm_tcgen05.cu) -------------------------
 enum TcType { TC_TF32 = 1, TC_BF16 = 2 };
