@@ -157,6 +157,15 @@ TGEMM_API int gemm_set_debug_stall(int enable);
  */
 TGEMM_API int gemm_set_f32_kernel(int id);
 
+/*
+ * gemm_set_tc_kernel — choose the tensor-core kernel (for tests and tuning):
+ * -1 (default) picks by shape (the 2-SM kernel, a CTA pair computing
+ * 256 x 256 tiles, when M > 128; otherwise the one-SM kernel with 128 x 256
+ * tiles), 0 forces the one-SM kernel, 1 the 2-SM kernel. Process-wide.
+ * Returns TGEMM_OK or TGEMM_ERR_INVALID_ARG.
+ */
+TGEMM_API int gemm_set_tc_kernel(int mode);
+
 /* Number of FP32 kernel configurations gemm_set_f32_kernel accepts. */
 TGEMM_API int gemm_f32_kernel_count(void);
 

@@ -78,6 +78,37 @@ def test_integer_bit_exact(tgemm, kind, shape):
     assert_bit_exact(run_tc(tgemm, A, B, kind), C_ref, f"{kind} {shape}")
 
 
+@pytest.fixture(params=[0, 1], ids=["one_sm", "sm_pair"])
+def tc_mode(request, tgemm):
+    """Force the one-SM kernel (0) or the 2-SM CTA-pair kernel (1)."""
+    assert tgemm.binding.set_tc_kernel(request.param) == 0
+    yield request.param
+    tgemm.binding.set_tc_kernel(-1)
+
+
+@pytest.mark.parametrize("kind", ["tf32", "bf16"])
+@pytest.mark.parametrize("shape", [(1, 8, 8), (129, 264, 72), (300, 520, 200), (256, 512, 1024),
+                                   (513, 1000, 136), (640, 256, 4104)])
+def test_both_kernels_integer_bit_exact(tgemm, tc_mode, kind, shape):
+    M, N, K = shape
+    A, B = operands(M, N, K, "int4", kind, seed=11 * M + N + K)
+    C_ref, _ = oracle.gemm(A, B)
+    C = run_tc(tgemm, A, B, kind)
+    assert ("2sm" in tgemm.binding.last_kernel()) == (tc_mode == 1)
+    assert_bit_exact(C, C_ref, f"{kind} {shape} mode {tc_mode}")
+
+
+@pytest.mark.parametrize("kind", ["tf32", "bf16"])
+def test_both_kernels_ragged_nan_padding(tgemm, tc_mode, kind):
+    M, N, K = 389, 301, 97
+    A, B = operands(M, N, K, "int4", kind, seed=6)
+    C = torch.full((M, N), -1.0, device="cuda")
+    tgemm.gemm_tc(padded_cuda(A, 104), padded_cuda(B, 312), kind, out=C)
+    assert tgemm.device_status() == 0
+    C_ref, _ = oracle.gemm(A, B)
+    assert_bit_exact(C, C_ref, f"{kind} ragged mode {tc_mode}")
+
+
 @pytest.mark.parametrize("kind", ["tf32", "bf16"])
 @pytest.mark.parametrize("shape", [(200, 296, 136), (513, 1032, 520)])
 def test_float_tolerance(tgemm, kind, shape):

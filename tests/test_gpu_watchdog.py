@@ -18,8 +18,10 @@ from tiled_matrix_multiplication_sm_gb300 import inputs
 pytestmark = pytest.mark.gpu
 
 
-def test_stalled_pipeline_reports_timeout_and_recovers(tgemm):
+@pytest.mark.parametrize("mode", [0, 1], ids=["one_sm", "sm_pair"])
+def test_stalled_pipeline_reports_timeout_and_recovers(tgemm, mode):
     b = tgemm.binding
+    assert b.set_tc_kernel(mode) == 0
     g = inputs.generator(4)
     A = inputs.draw(256, 128, "int4", g).to(torch.bfloat16).cuda()
     B = inputs.draw(128, 512, "int4", g).to(torch.bfloat16).cuda()
@@ -34,12 +36,17 @@ def test_stalled_pipeline_reports_timeout_and_recovers(tgemm):
     finally:
         b.set_debug_stall(False)
         b.set_wait_limit_ns(2_000_000_000)
+        b.set_tc_kernel(-1)
     assert st == b.TGEMM_ERR_DEVICE_TIMEOUT
     assert elapsed < 10.0
     # The status word is cleared by the read ...
     assert tgemm.device_status() == 0
     # ... and the next launch is correct.
-    C = tgemm.gemm_tc(A, B, "bf16")
+    b.set_tc_kernel(mode)
+    try:
+        C = tgemm.gemm_tc(A, B, "bf16")
+    finally:
+        b.set_tc_kernel(-1)
     assert tgemm.device_status() == 0
     C_ref, _ = oracle.gemm(A.cpu(), B.cpu())
     assert_bit_exact(C, C_ref, "after timeout")

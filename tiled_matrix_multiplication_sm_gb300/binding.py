@@ -39,6 +39,7 @@ _SIGNATURES = {
     "gemm_set_wait_limit_ns": (ctypes.c_int, [ctypes.c_longlong]),
     "gemm_set_debug_stall": (ctypes.c_int, [ctypes.c_int]),
     "gemm_set_f32_kernel": (ctypes.c_int, [ctypes.c_int]),
+    "gemm_set_tc_kernel": (ctypes.c_int, [ctypes.c_int]),
     "gemm_f32_kernel_count": (ctypes.c_int, []),
     "gemm_f32_kernel_name": (ctypes.c_char_p, [ctypes.c_int]),
     "gemm_last_kernel": (ctypes.c_char_p, []),
@@ -193,6 +194,11 @@ def set_debug_stall(enable: bool) -> int:
 
 def set_f32_kernel(kernel_id: int) -> int:
     return int(load().gemm_set_f32_kernel(int(kernel_id)))
+
+
+def set_tc_kernel(mode: int) -> int:
+    """-1: by shape; 0: one-SM tcgen05 kernel; 1: 2-SM (CTA pair) kernel."""
+    return int(load().gemm_set_tc_kernel(int(mode)))
 
 
 def f32_kernel_names():

@@ -30,6 +30,7 @@ bool g_encode_looked_up = false;
 std::atomic<long long> g_wait_limit_ns{2000000000LL};
 std::atomic<int> g_debug_stall{0};
 std::atomic<int> g_forced_f32{-1};
+std::atomic<int> g_tc_mode{-1};
 thread_local const char* g_last_kernel = "";
 thread_local char g_last_kernel_buf[160];
 
@@ -191,11 +192,13 @@ int gemm_tc(int M, int N, int K, const void* A, long lda, const void* B, long ld
     if (enc == nullptr) return TGEMM_ERR_CUDA;
     const unsigned long long limit = (unsigned long long)g_wait_limit_ns.load();
     const int stall = g_debug_stall.load();
+    const bool pair = tgemm::tc_use_pair(M, g_tc_mode.load());
     if (in_type == TGEMM_BF16) {
         tgemm::GemmArgs a{M, N, K, A, lda, B, ldb, C, ldc};
-        if (tgemm::tc_launch(a, in_type, 0, dev.num_sms, enc, limit, stall, stream) != cudaSuccess)
+        if (tgemm::tc_launch(a, in_type, 0, dev.num_sms, enc, limit, stall, pair, stream) !=
+            cudaSuccess)
             return TGEMM_ERR_CUDA;
-        g_last_kernel = tgemm::tc_kernel_name(in_type);
+        g_last_kernel = tgemm::tc_kernel_name(in_type, pair);
         return TGEMM_OK;
     }
     // TF32: the tensor core reads a TF32 B operand only K-major, so B is
@@ -214,11 +217,16 @@ int gemm_tc(int M, int N, int K, const void* A, long lda, const void* B, long ld
         rc = TGEMM_ERR_CUDA;
     } else {
         tgemm::GemmArgs a{M, N, K, A, lda, bt, ldt, C, ldc};
-        if (tgemm::tc_launch(a, in_type, 1, dev.num_sms, enc, limit, stall, stream) != cudaSuccess)
+        if (tgemm::tc_launch(a, in_type, 1, dev.num_sms, enc, limit, stall, pair, stream) !=
+            cudaSuccess)
             rc = TGEMM_ERR_CUDA;
     }
     if (cudaFreeAsync(bt, stream) != cudaSuccess && rc == TGEMM_OK) rc = TGEMM_ERR_CUDA;
-    if (rc == TGEMM_OK) g_last_kernel = tgemm::tc_kernel_name(in_type);
+    if (rc == TGEMM_OK) {
+        snprintf(g_last_kernel_buf, sizeof(g_last_kernel_buf), "transpose_b+%s",
+                 tgemm::tc_kernel_name(in_type, pair));
+        g_last_kernel = g_last_kernel_buf;
+    }
     return rc;
 }
 
@@ -257,6 +265,12 @@ int gemm_set_debug_stall(int enable) {
 int gemm_set_f32_kernel(int id) {
     if (id < -1 || id >= tgemm::f32_kernel_count()) return TGEMM_ERR_INVALID_ARG;
     g_forced_f32.store(id);
+    return TGEMM_OK;
+}
+
+int gemm_set_tc_kernel(int mode) {
+    if (mode < -1 || mode > 1) return TGEMM_ERR_INVALID_ARG;
+    g_tc_mode.store(mode);
     return TGEMM_OK;
 }
 

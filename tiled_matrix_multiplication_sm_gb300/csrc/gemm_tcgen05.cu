@@ -134,16 +134,16 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 // (returns false) when the block's abort flag is raised or, if
 // `honour_abort` is false, only when `limit_ns` has passed; a wait that runs
 // out raises the abort flag and records the timeout.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Sync* sy,
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* abort_flag,
                                        unsigned long long limit_ns, bool honour_abort) {
     if (mbar_try(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try(bar, parity)) return true;
         if ((it & 15u) == 0) {
-            if (honour_abort && *(volatile int*)&sy->abort) return false;
+            if (honour_abort && *(volatile int*)abort_flag) return false;
             if (globaltimer() - t0 > limit_ns || it >= (1u << 30)) {
-                *(volatile int*)&sy->abort = 1;
+                *(volatile int*)abort_flag = 1;
                 atomicCAS(&g_tc_status, 0, kStatusTimeout);
                 return false;
             }
@@ -170,6 +170,71 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                  :: "r"(bar) : "memory");
+}
+
+// ---- CTA-pair (cluster of 2) helpers for the 2-SM kernel
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
+                 :: "r"(cluster_addr) : "memory");
+}
+
+// TMA load into this CTA's shared memory whose completion is counted on an
+// mbarrier that may live in the peer CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                                 uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+        : "memory");
+}
+
+// Arrive (once the MMAs issued so far complete) on the barrier at `bar` in
+// both CTAs of the pair.
+__device__ __forceinline__ void tc_commit_pair_multicast(uint32_t bar) {
+    const uint16_t both = 0x3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" :: "r"(bar), "h"(both) : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(bar) : "memory");
+}
+
+template <int ESZ>
+__device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    if constexpr (ESZ == 2) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+            :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
+            :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+    }
 }
 
 template <int ESZ>
@@ -218,7 +283,7 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 
 // Instruction descriptor: FP32 accumulator, A K-major, B K-major or
 // MN-major, M x N.
-template <int ESZ, bool B_KMAJOR>
+template <int ESZ, bool B_KMAJOR, int MMA_M = BM>
 __host__ __device__ constexpr uint32_t instr_desc() {
     return (1u << 4)                         // D format F32
          | (Kind<ESZ>::FMT << 7)             // A format
@@ -226,7 +291,7 @@ __host__ __device__ constexpr uint32_t instr_desc() {
          | (0u << 15)                        // A: K-major
          | ((B_KMAJOR ? 0u : 1u) << 16)      // B: K-major (0) or MN-major (1)
          | ((uint32_t)(BN >> 3) << 17)
-         | ((uint32_t)(BM >> 4) << 24);
+         | ((uint32_t)(MMA_M >> 4) << 24);
 }
 
 __device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& mb, int& nb) {
@@ -302,7 +367,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                 for (int kb = 0; kb < p.kblocks; ++kb, ++g) {
                     const int s = g % STAGES;
                     const uint32_t ph = (uint32_t)(g / STAGES) & 1u;
-                    if (!mbar_wait(smem_u32(&sy->empty[s]), ph ^ 1u, sy, lim, true)) goto producer_done;
+                    if (!mbar_wait(smem_u32(&sy->empty[s]), ph ^ 1u, &sy->abort, lim, true)) goto producer_done;
                     if (p.debug_stall && g == 0) continue;     // test hook: never fill stage 0
                     const uint32_t full = smem_u32(&sy->full[s]);
                     mbar_arrive_expect_tx(full, STAGE_BYTES);
@@ -324,7 +389,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             // Copies still in flight must land before the block may exit.
             for (int s = 0; s < STAGES; ++s)
                 if (armed & (1u << s))
-                    mbar_wait(smem_u32(&sy->full[s]), (armed_parity >> s) & 1u, sy, lim, false);
+                    mbar_wait(smem_u32(&sy->full[s]), (armed_parity >> s) & 1u, &sy->abort, lim, false);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -334,14 +399,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
                 const int acc = it & 1;
                 const uint32_t aph = (uint32_t)(it >> 1) & 1u;
-                if (!mbar_wait(smem_u32(&sy->tmem_empty[acc]), aph ^ 1u, sy, lim, true)) break;
+                if (!mbar_wait(smem_u32(&sy->tmem_empty[acc]), aph ^ 1u, &sy->abort, lim, true)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 bool ok = true;
                 for (int kb = 0; kb < p.kblocks; ++kb, ++g) {
                     const int s = g % STAGES;
                     const uint32_t ph = (uint32_t)(g / STAGES) & 1u;
-                    if (!mbar_wait(smem_u32(&sy->full[s]), ph, sy, lim, true)) { ok = false; break; }
+                    if (!mbar_wait(smem_u32(&sy->full[s]), ph, &sy->abort, lim, true)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a_addr = a_base + s * A_STAGE_BYTES;
                     const uint32_t b_addr = b_base + s * B_STAGE_BYTES;
@@ -360,7 +425,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             }
             // Every MMA this thread issued must finish before TMEM is freed.
             tc_commit(smem_u32(&sy->drain));
-            mbar_wait(smem_u32(&sy->drain), 0, sy, lim, false);
+            mbar_wait(smem_u32(&sy->drain), 0, &sy->abort, lim, false);
         }
         __syncwarp();
     } else {
@@ -373,7 +438,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             tile_coords(t, p, mb, nb);
             const int acc = it & 1;
             const uint32_t aph = (uint32_t)(it >> 1) & 1u;
-            bool ok = mbar_wait(smem_u32(&sy->tmem_full[acc]), aph, sy, lim, true);
+            bool ok = mbar_wait(smem_u32(&sy->tmem_full[acc]), aph, &sy->abort, lim, true);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
             const int row = mb * BM + q * 32 + lane;
@@ -407,6 +472,236 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     tc_fence_after();
     if (warp == 1) {
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                     :: "r"(tmem_base), "n"(TMEM_COLS) : "memory");
+    }
+}
+
+// ===================================================================
+// 2-SM variant: a cluster of two CTAs on a pair of SMs computes a 256 x 256
+// tile with tcgen05.mma.cta_group::2 (M = 256, N = 256). CTA r of the pair
+// stages rows 128r..128r+127 of the A tile and columns 128r..128r+127 of the
+// B tile; the leader CTA (r = 0) issues the MMAs for both, and each CTA's
+// tensor memory receives its 128 rows of the 256 x 256 accumulator. Each SM
+// thus streams half of B instead of all of it, which halves the shared-
+// memory traffic of the B operand per SM: the one-SM kernel's ring is
+// shared-memory-bandwidth bound at about two thirds of the tensor rate.
+//
+// Hand-offs:
+//   full[s]     leader only: the leader's producer expects both CTAs'
+//               bytes; both producers' copies complete on it.
+//   empty[s]    both CTAs: arrived by the leader's commit (multicast).
+//   tmem_full   both CTAs: arrived by the leader's commit (multicast).
+//   tmem_empty  leader only: all 256 epilogue threads of the pair arrive.
+// Both CTAs allocate and free tensor memory jointly (cta_group::2); cluster
+// barriers after set-up and before the free keep the pair in step.
+
+constexpr int P_STAGES = 6;
+constexpr int P_A_STAGE_BYTES = 128 * SW;                  // 16 KB: this CTA's 128 rows of A
+constexpr int P_B_STAGE_BYTES = 16 * 1024;                 // this CTA's 128 columns of B
+constexpr int P_STAGE_BYTES = P_A_STAGE_BYTES + P_B_STAGE_BYTES;
+constexpr int P_BM = 256;                                  // pair tile rows (= MMA M)
+// The 16 KB after the ring are never used by this kernel's layout; they keep
+// every shared-memory address an MMA descriptor can reach (a descriptor
+// walks at most one 256-column B tile past its start) inside the block's
+// allocation.
+constexpr int P_GUARD_BYTES = 16 * 1024;
+constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + P_GUARD_BYTES + 256;
+
+struct PairSync {
+    uint64_t full[P_STAGES];
+    uint64_t empty[P_STAGES];
+    uint64_t tmem_full[2];
+    uint64_t tmem_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+static_assert(sizeof(PairSync) <= 256, "pair barrier block");
+
+template <int ESZ, bool B_KMAJOR>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
+                   const __grid_constant__ CUtensorMap tmB,
+                   const TcParams p) {
+    using KD = Kind<ESZ>;
+    constexpr int BK = KD::BK;
+    constexpr int K_STEPS = BK / KD::UMMA_K;
+    constexpr int B_CHUNK_COLS = SW / ESZ;               // N columns per swizzled row
+    constexpr int B_CHUNKS = 128 / B_CHUNK_COLS;         // per CTA (its 128 columns)
+    constexpr int B_CHUNK_BYTES = BK * SW;
+    constexpr uint32_t A_K_STEP = KD::UMMA_K * ESZ;
+    constexpr uint32_t B_K_STEP = KD::UMMA_K * SW;
+    static_assert(B_KMAJOR || B_CHUNKS * B_CHUNK_BYTES == P_B_STAGE_BYTES, "B stage size");
+    static_assert(!B_KMAJOR || 128 * SW == P_B_STAGE_BYTES, "B stage size");
+    constexpr uint32_t IDESC = instr_desc<ESZ, B_KMAJOR, P_BM>();
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
+    PairSync* sy = reinterpret_cast<PairSync*>(smem + P_STAGES * P_STAGE_BYTES + P_GUARD_BYTES);
+    const uint32_t a_base = smem_u32(smem);
+    const uint32_t b_base = a_base + P_STAGES * P_A_STAGE_BYTES;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P_STAGES; ++s) {
+            mbar_init(smem_u32(&sy->full[s]), 1);
+            mbar_init(smem_u32(&sy->empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&sy->tmem_full[a]), 1);
+            mbar_init(smem_u32(&sy->tmem_empty[a]), 256);
+        }
+        mbar_init(smem_u32(&sy->drain), 1);
+        sy->abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(smem_u32(&sy->tmem_base)), "n"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    cluster_sync_all();        // barriers of both CTAs initialised, TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem_base = sy->tmem_base;
+    const unsigned long long lim = p.wait_limit_ns;
+    // The leader's copies of the shared hand-off barriers, as cluster addresses.
+    const uint32_t full0 = map_to_rank(smem_u32(&sy->full[0]), 0);
+    const uint32_t tmem_empty0 = map_to_rank(smem_u32(&sy->tmem_empty[0]), 0);
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            uint32_t armed = 0, armed_parity = 0;
+            int g = 0;
+            for (int t = pair; t < p.num_tiles; t += num_pairs) {
+                int mb, nb;
+                tile_coords(t, p, mb, nb);
+                const int row0 = mb * P_BM + (int)rank * 128;
+                const int col0 = nb * BN + (int)rank * 128;
+                for (int kb = 0; kb < p.kblocks; ++kb, ++g) {
+                    const int s = g % P_STAGES;
+                    const uint32_t ph = (uint32_t)(g / P_STAGES) & 1u;
+                    if (!mbar_wait(smem_u32(&sy->empty[s]), ph ^ 1u, &sy->abort, lim, true)) goto pair_producer_done;
+                    if (p.debug_stall && g == 0) continue;     // test hook: stage 0 never filled
+                    const uint32_t full = full0 + (uint32_t)(s * sizeof(uint64_t));
+                    if (leader) mbar_arrive_expect_tx(smem_u32(&sy->full[s]), 2 * P_STAGE_BYTES);
+                    tma_load_2d_pair(a_base + s * P_A_STAGE_BYTES, &tmA, kb * BK, row0, full);
+                    const uint32_t bdst = b_base + s * P_B_STAGE_BYTES;
+                    if constexpr (B_KMAJOR) {
+                        tma_load_2d_pair(bdst, &tmB, kb * BK, col0, full);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < B_CHUNKS; ++c)
+                            tma_load_2d_pair(bdst + c * B_CHUNK_BYTES, &tmB, col0 + c * B_CHUNK_COLS,
+                                             kb * BK, full);
+                    }
+                    armed |= 1u << s;
+                    armed_parity = (armed_parity & ~(1u << s)) | (ph << s);
+                }
+            }
+        pair_producer_done:
+            if (leader) {
+                // Both CTAs' copies complete on the leader's barriers.
+                for (int s = 0; s < P_STAGES; ++s)
+                    if (armed & (1u << s))
+                        mbar_wait(smem_u32(&sy->full[s]), (armed_parity >> s) & 1u, &sy->abort, lim, false);
+            } else if (*(volatile int*)&sy->abort) {
+                // After a timeout the peer cannot observe its own copies; give
+                // any still in flight time to land (a copy takes microseconds).
+                const unsigned long long t0 = globaltimer();
+                while (globaltimer() - t0 < 2000000ull) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (leader CTA)
+        if (lane == 0 && leader) {
+            int g = 0, it = 0;
+            for (int t = pair; t < p.num_tiles; t += num_pairs, ++it) {
+                const int acc = it & 1;
+                const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+                if (!mbar_wait(smem_u32(&sy->tmem_empty[acc]), aph ^ 1u, &sy->abort, lim, true)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                bool ok = true;
+                for (int kb = 0; kb < p.kblocks; ++kb, ++g) {
+                    const int s = g % P_STAGES;
+                    const uint32_t ph = (uint32_t)(g / P_STAGES) & 1u;
+                    if (!mbar_wait(smem_u32(&sy->full[s]), ph, &sy->abort, lim, true)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_addr = a_base + s * P_A_STAGE_BYTES;
+                    const uint32_t b_addr = b_base + s * P_B_STAGE_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < K_STEPS; ++kk) {
+                        const uint64_t ad = smem_desc(a_addr + kk * A_K_STEP, 16, 1024);
+                        const uint64_t bd =
+                            B_KMAJOR ? smem_desc(b_addr + kk * A_K_STEP, 16, 1024)
+                                     : smem_desc(b_addr + kk * B_K_STEP, B_CHUNK_BYTES, 1024);
+                        tc_mma_pair<ESZ>(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    tc_commit_pair_multicast(smem_u32(&sy->empty[s]));   // slot free in both CTAs
+                }
+                if (!ok) break;
+                tc_commit_pair_multicast(smem_u32(&sy->tmem_full[acc]));  // accumulator ready in both
+            }
+            tc_commit_pair(smem_u32(&sy->drain));
+            mbar_wait(smem_u32(&sy->drain), 0, &sy->abort, lim, false);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue (warps 2-5, both CTAs)
+        const int q = warp & 3;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        int it = 0;
+        for (int t = pair; t < p.num_tiles; t += num_pairs, ++it) {
+            int mb, nb;
+            tile_coords(t, p, mb, nb);
+            const int acc = it & 1;
+            const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+            bool ok = mbar_wait(smem_u32(&sy->tmem_full[acc]), aph, &sy->abort, lim, true);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            const int row = mb * P_BM + (int)rank * 128 + q * 32 + lane;
+            float* crow = p.C + (long)row * p.ldc;
+            for (int c = 0; c < BN / 32; ++c) {
+                const int col0 = nb * BN + c * 32;
+                if (col0 >= p.N) break;                     // uniform across the warp
+                uint32_t r[32];
+                tmem_ld32(tmem_base + lane_off + (uint32_t)(acc * BN + c * 32), r);
+                if (row < p.M) {
+                    if (p.vec_c && col0 + 31 < p.N) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<float4*>(crow + col0 + j) =
+                                make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                                            __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col0 + j < p.N) crow[col0 + j] = __uint_as_float(r[j]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive_cluster(tmem_empty0 + (uint32_t)(acc * sizeof(uint64_t)));
+        }
+    }
+
+    tc_fence_before();
+    cluster_sync_all();        // the leader's MMAs are drained; no copy in flight
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;"
                      :: "r"(tmem_base), "n"(TMEM_COLS) : "memory");
     }
 }
@@ -462,16 +757,79 @@ cudaError_t launch_tc(const GemmArgs& a, int num_sms, EncodeTiledFn enc,
     return cudaGetLastError();
 }
 
+// The 2-SM kernel: clusters of two CTAs, one CTA per SM, persistent over
+// 256 x 256 tiles.
+template <int ESZ, bool B_KMAJOR>
+cudaError_t launch_tc_pair(const GemmArgs& a, int num_sms, EncodeTiledFn enc,
+                           unsigned long long wait_limit_ns, int debug_stall, cudaStream_t s) {
+    constexpr int BK = Kind<ESZ>::BK;
+    CUtensorMap tmA, tmB;
+    if (!encode_2d(enc, &tmA, a.A, ESZ, a.M, a.K, a.lda, BK, 128)) return cudaErrorInvalidValue;
+    const bool okb = B_KMAJOR ? encode_2d(enc, &tmB, a.B, ESZ, a.N, a.K, a.ldb, BK, 128)
+                              : encode_2d(enc, &tmB, a.B, ESZ, a.K, a.N, a.ldb, SW / ESZ, BK);
+    if (!okb) return cudaErrorInvalidValue;
+
+    TcParams p;
+    p.M = a.M; p.N = a.N; p.K = a.K;
+    p.C = a.C; p.ldc = a.ldc;
+    p.tiles_m = (a.M + P_BM - 1) / P_BM;
+    p.tiles_n = (a.N + BN - 1) / BN;
+    p.num_tiles = p.tiles_m * p.tiles_n;
+    p.kblocks = (a.K + BK - 1) / BK;
+    p.wait_limit_ns = wait_limit_ns;
+    p.debug_stall = debug_stall;
+    p.vec_c = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0 && a.ldc % 4 == 0) ? 1 : 0;
+
+    auto kern = tc_gemm_2sm_kernel<ESZ, B_KMAJOR>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         P_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int pairs = p.num_tiles < num_sms / 2 ? p.num_tiles : num_sms / 2;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * pairs, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = P_SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+const char* kNames[2][2] = {
+    {"tc_tf32_128x256x32_s4_persistent", "tc_tf32_2sm_256x256x32_s6_persistent"},
+    {"tc_bf16_128x256x64_s4_persistent", "tc_bf16_2sm_256x256x64_s6_persistent"},
+};
+
 }  // namespace
 
-const char* tc_kernel_name(int in_type) {
-    return in_type == TC_BF16 ? "tc_bf16_128x256x64_s4_persistent"
-                              : "transpose_b+tc_tf32_128x256x32_s4_persistent";
+bool tc_use_pair(int M, int mode) {
+    if (mode == 0) return false;
+    if (mode == 1) return true;
+    return M > BM;          // a pair tile is 256 rows tall
+}
+
+const char* tc_kernel_name(int in_type, bool pair) {
+    return kNames[in_type == TC_BF16 ? 1 : 0][pair ? 1 : 0];
 }
 
 cudaError_t tc_launch(const GemmArgs& a, int in_type, int b_kmajor, int num_sms, void* encode_fn,
-                      unsigned long long wait_limit_ns, int debug_stall, cudaStream_t s) {
+                      unsigned long long wait_limit_ns, int debug_stall, bool pair,
+                      cudaStream_t s) {
     auto enc = reinterpret_cast<EncodeTiledFn>(encode_fn);
+    if (pair) {
+        if (in_type == TC_BF16)
+            return b_kmajor ? launch_tc_pair<2, true>(a, num_sms, enc, wait_limit_ns, debug_stall, s)
+                            : launch_tc_pair<2, false>(a, num_sms, enc, wait_limit_ns, debug_stall, s);
+        return b_kmajor ? launch_tc_pair<4, true>(a, num_sms, enc, wait_limit_ns, debug_stall, s)
+                        : launch_tc_pair<4, false>(a, num_sms, enc, wait_limit_ns, debug_stall, s);
+    }
     if (in_type == TC_BF16)
         return b_kmajor ? launch_tc<2, true>(a, num_sms, enc, wait_limit_ns, debug_stall, s)
                         : launch_tc<2, false>(a, num_sms, enc, wait_limit_ns, debug_stall, s);

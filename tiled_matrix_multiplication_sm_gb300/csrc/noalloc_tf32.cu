@@ -114,7 +114,8 @@ extern "C" int gemm_tc_tf32_noalloc(int M, int N, int K, const float* A, long ld
     if (tgemm::transpose_f32(B, ldb, d.scratch, ldt, K, N, stream) != cudaSuccess)
         return TGEMM_ERR_CUDA;
     tgemm::GemmArgs a{M, N, K, A, lda, d.scratch, ldt, C, ldc};
-    if (tgemm::tc_launch(a, tgemm::TC_TF32, 1, d.num_sms, enc, kWaitLimitNs, 0, stream) != cudaSuccess)
+    if (tgemm::tc_launch(a, tgemm::TC_TF32, 1, d.num_sms, enc, kWaitLimitNs, 0,
+                         tgemm::tc_use_pair(M, -1), stream) != cudaSuccess)
         return TGEMM_ERR_CUDA;
     return TGEMM_OK;
 }

@@ -39,12 +39,16 @@ cudaError_t f32_launch(int id, const GemmArgs& a, const F32Plan& pl, float* scra
 
 // ---- tcgen05 tensor-core path (gemm_tcgen05.cu) -------------------------
 enum TcType { TC_TF32 = 1, TC_BF16 = 2 };
-const char* tc_kernel_name(int in_type);
-// Launch the persistent tcgen05 kernel. `encode_fn` is cuTensorMapEncodeTiled.
-// With b_kmajor, a.B / a.ldb describe B transposed (N x K, K contiguous).
+// Whether the 2-SM (CTA-pair) kernel runs: mode -1 = by shape, 0 = never,
+// 1 = always.
+bool tc_use_pair(int M, int mode);
+const char* tc_kernel_name(int in_type, bool pair);
+// Launch the persistent tcgen05 kernel (one-SM, or 2-SM when `pair`).
+// `encode_fn` is cuTensorMapEncodeTiled. With b_kmajor, a.B / a.ldb describe
+// B transposed (N x K, K contiguous).
 cudaError_t tc_launch(const GemmArgs& a, int in_type, int b_kmajor, int num_sms,
                       void* encode_fn, unsigned long long wait_limit_ns,
-                      int debug_stall, cudaStream_t s);
+                      int debug_stall, bool pair, cudaStream_t s);
 // Read and clear the tensor-core kernel's status word on the current device.
 cudaError_t tc_read_and_clear_status(int* status, cudaStream_t s);
 
