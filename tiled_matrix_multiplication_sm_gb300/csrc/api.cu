@@ -193,38 +193,45 @@ int gemm_tc(int M, int N, int K, const void* A, long lda, const void* B, long ld
     const unsigned long long limit = (unsigned long long)g_wait_limit_ns.load();
     const int stall = g_debug_stall.load();
     const bool pair = tgemm::tc_use_pair(M, g_tc_mode.load());
-    if (in_type == TGEMM_BF16) {
-        tgemm::GemmArgs a{M, N, K, A, lda, B, ldb, C, ldc};
-        if (tgemm::tc_launch(a, in_type, 0, dev.num_sms, enc, limit, stall, pair, stream) !=
-            cudaSuccess)
-            return TGEMM_ERR_CUDA;
-        g_last_kernel = tgemm::tc_kernel_name(in_type, pair);
-        return TGEMM_OK;
-    }
-    // TF32: the tensor core reads a TF32 B operand only K-major, so B is
-    // first transposed into stream-ordered scratch (N x ldt floats).
-    int devno = 0;
-    if (cudaGetDevice(&devno) != cudaSuccess) return TGEMM_ERR_CUDA;
-    cudaMemPool_t pool = scratch_pool(devno);
-    if (pool == nullptr) return TGEMM_ERR_CUDA;
+    const tgemm::TcPlan plan = tgemm::tc_plan(M, N, K, in_type, pair, dev.num_sms, true);
+
+    // Stream-ordered scratch: B transposed for TF32 (the TF32 kind reads B
+    // only K-major), then the partial tiles of a split last wave.
+    const bool tf32 = in_type == TGEMM_TF32;
     const long ldt = (K + 3) / 4 * 4;
-    void* bt = nullptr;
-    if (cudaMallocFromPoolAsync(&bt, (size_t)N * ldt * sizeof(float), pool, stream) != cudaSuccess)
-        return TGEMM_ERR_CUDA;
+    const size_t bt_bytes = tf32 ? (((size_t)N * ldt * sizeof(float) + 255) & ~(size_t)255) : 0;
+    const size_t total = bt_bytes + plan.scratch_bytes;
+    void* ws = nullptr;
+    if (total > 0) {
+        int devno = 0;
+        if (cudaGetDevice(&devno) != cudaSuccess) return TGEMM_ERR_CUDA;
+        cudaMemPool_t pool = scratch_pool(devno);
+        if (pool == nullptr) return TGEMM_ERR_CUDA;
+        if (cudaMallocFromPoolAsync(&ws, total, pool, stream) != cudaSuccess) return TGEMM_ERR_CUDA;
+    }
+    float* bt = static_cast<float*>(ws);
+    float* partials = plan.scratch_bytes ? reinterpret_cast<float*>(static_cast<char*>(ws) + bt_bytes)
+                                         : nullptr;
     int rc = TGEMM_OK;
-    if (tgemm::transpose_f32(static_cast<const float*>(B), ldb, static_cast<float*>(bt), ldt, K, N,
-                             stream) != cudaSuccess) {
-        rc = TGEMM_ERR_CUDA;
-    } else {
-        tgemm::GemmArgs a{M, N, K, A, lda, bt, ldt, C, ldc};
-        if (tgemm::tc_launch(a, in_type, 1, dev.num_sms, enc, limit, stall, pair, stream) !=
+    tgemm::GemmArgs a{M, N, K, A, lda, B, ldb, C, ldc};
+    if (tf32) {
+        if (tgemm::transpose_f32(static_cast<const float*>(B), ldb, bt, ldt, K, N, stream) !=
             cudaSuccess)
             rc = TGEMM_ERR_CUDA;
+        a.B = bt;
+        a.ldb = ldt;
     }
-    if (cudaFreeAsync(bt, stream) != cudaSuccess && rc == TGEMM_OK) rc = TGEMM_ERR_CUDA;
+    if (rc == TGEMM_OK &&
+        tgemm::tc_launch(a, in_type, tf32 ? 1 : 0, dev.num_sms, enc, limit, stall, pair, plan,
+                         partials, stream) != cudaSuccess)
+        rc = TGEMM_ERR_CUDA;
+    if (ws != nullptr && cudaFreeAsync(ws, stream) != cudaSuccess && rc == TGEMM_OK)
+        rc = TGEMM_ERR_CUDA;
     if (rc == TGEMM_OK) {
-        snprintf(g_last_kernel_buf, sizeof(g_last_kernel_buf), "transpose_b+%s",
-                 tgemm::tc_kernel_name(in_type, pair));
+        char split[48] = "";
+        if (plan.split > 1) snprintf(split, sizeof(split), "+splitk_reduce(split=%d)", plan.split);
+        snprintf(g_last_kernel_buf, sizeof(g_last_kernel_buf), "%s%s%s",
+                 tf32 ? "transpose_b+" : "", tgemm::tc_kernel_name(in_type, pair), split);
         g_last_kernel = g_last_kernel_buf;
     }
     return rc;

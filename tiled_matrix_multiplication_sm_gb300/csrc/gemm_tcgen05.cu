@@ -91,10 +91,40 @@ struct TcParams {
     float* C;
     long ldc;
     int tiles_m, tiles_n, num_tiles, kblocks;
+    int tile_rows;       // rows of a tile: 128 (one SM) or 256 (SM pair)
+    int dp_tiles;        // tiles [0, dp_tiles) are computed whole
+    int split;           // the others in `split` K-pieces each (1: none)
+    int num_units;       // dp_tiles + (num_tiles - dp_tiles) * split
+    float* partials;     // one tile_rows x BN partial tile per K-piece
     unsigned long long wait_limit_ns;
     int debug_stall;
     int vec_c;
 };
+
+// A unit of persistent work: a whole tile, or K-blocks [kb0, kb1) of a tile
+// whose partial result goes to scratch (piece >= 0).
+struct Unit {
+    int tile, kb0, kb1;
+    int piece;
+};
+
+__device__ __forceinline__ Unit decode_unit(int u, const TcParams& p) {
+    Unit w;
+    if (u < p.dp_tiles) {
+        w.tile = u;
+        w.kb0 = 0;
+        w.kb1 = p.kblocks;
+        w.piece = -1;
+    } else {
+        const int pc = u - p.dp_tiles;
+        const int j = pc % p.split;
+        w.tile = p.dp_tiles + pc / p.split;
+        w.kb0 = (int)((long)j * p.kblocks / p.split);
+        w.kb1 = (int)((long)(j + 1) * p.kblocks / p.split);
+        w.piece = pc;
+    }
+    return w;
+}
 
 // ------------------------------------------------------------------ PTX
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -302,6 +332,79 @@ __device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& mb, i
     nb = (t % per_group) / gm;
 }
 
+// Epilogue of one unit for this thread's accumulator row `row_in_tile`:
+// 256 columns from TMEM (address `taddr`) to C, or, for a K-piece, to its
+// partial tile in scratch. Rows past M and columns past N are skipped (the
+// reduction never reads them). All lanes of the warp call this together.
+__device__ __forceinline__ void store_accumulator(const TcParams& p, const Unit& w, int mb, int nb,
+                                                 int row_in_tile, uint32_t taddr) {
+    const int row = mb * p.tile_rows + row_in_tile;
+    float* dst;
+    bool vec;
+    if (w.piece < 0) {
+        dst = p.C + (long)row * p.ldc + (long)nb * BN;
+        vec = p.vec_c != 0;
+    } else {
+        dst = p.partials + ((long)w.piece * p.tile_rows + row_in_tile) * BN;
+        vec = true;
+    }
+    for (int c = 0; c < BN / 32; ++c) {
+        const int col0 = nb * BN + c * 32;
+        if (col0 >= p.N) break;                     // uniform across the warp
+        uint32_t r[32];
+        tmem_ld32(taddr + (uint32_t)(c * 32), r);
+        if (row < p.M) {
+            float* d = dst + c * 32;
+            if (vec && col0 + 31 < p.N) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4*>(d + j) =
+                        make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                                    __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (col0 + j < p.N) d[j] = __uint_as_float(r[j]);
+            }
+        }
+    }
+}
+
+// Sum the K-pieces of every split tile, piece 0 first, into C.
+__global__ void __launch_bounds__(256)
+tc_splitk_reduce(const TcParams p) {
+    constexpr int Q = BN / 4;                              // float4 per tile row
+    const long per_tile = (long)p.tile_rows * Q;
+    const long total = (long)(p.num_tiles - p.dp_tiles) * per_tile;
+    const long piece_floats = (long)p.tile_rows * BN;
+    for (long u = blockIdx.x * (long)blockDim.x + threadIdx.x; u < total;
+         u += (long)gridDim.x * blockDim.x) {
+        const int r = (int)(u / per_tile);
+        const int e = (int)(u % per_tile);
+        const int row = e / Q, c4 = (e % Q) * 4;
+        int mb, nb;
+        tile_coords(p.dp_tiles + r, p, mb, nb);
+        const int grow = mb * p.tile_rows + row, gcol = nb * BN + c4;
+        if (grow >= p.M || gcol >= p.N) continue;
+        const float* src = p.partials + (long)r * p.split * piece_floats + (long)row * BN + c4;
+        float4 s = *reinterpret_cast<const float4*>(src);
+        for (int j = 1; j < p.split; ++j) {
+            const float4 v = *reinterpret_cast<const float4*>(src + j * piece_floats);
+            s.x += v.x;
+            s.y += v.y;
+            s.z += v.z;
+            s.w += v.w;
+        }
+        float* dst = p.C + (long)grow * p.ldc + gcol;
+        if (p.vec_c && gcol + 3 < p.N) {
+            *reinterpret_cast<float4*>(dst) = s;
+        } else {
+            const float v[4] = {s.x, s.y, s.z, s.w};
+            for (int j = 0; j < 4 && gcol + j < p.N; ++j) dst[j] = v[j];
+        }
+    }
+}
+
 // B_KMAJOR: B arrives transposed (N x K, K contiguous) and is read K-major;
 // otherwise B is K x N (N contiguous) and is read MN-major.
 template <int ESZ, bool B_KMAJOR>
@@ -361,10 +464,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         if (lane == 0) {
             uint32_t armed = 0, armed_parity = 0;   // per-stage fills in flight
             int g = 0;
-            for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+            for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+                const Unit w = decode_unit(u, p);
                 int mb, nb;
-                tile_coords(t, p, mb, nb);
-                for (int kb = 0; kb < p.kblocks; ++kb, ++g) {
+                tile_coords(w.tile, p, mb, nb);
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++g) {
                     const int s = g % STAGES;
                     const uint32_t ph = (uint32_t)(g / STAGES) & 1u;
                     if (!mbar_wait(smem_u32(&sy->empty[s]), ph ^ 1u, &sy->abort, lim, true)) goto producer_done;
@@ -396,14 +500,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             int g = 0, it = 0;
-            for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+            for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++it) {
+                const Unit w = decode_unit(u, p);
                 const int acc = it & 1;
                 const uint32_t aph = (uint32_t)(it >> 1) & 1u;
                 if (!mbar_wait(smem_u32(&sy->tmem_empty[acc]), aph ^ 1u, &sy->abort, lim, true)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 bool ok = true;
-                for (int kb = 0; kb < p.kblocks; ++kb, ++g) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++g) {
                     const int s = g % STAGES;
                     const uint32_t ph = (uint32_t)(g / STAGES) & 1u;
                     if (!mbar_wait(smem_u32(&sy->full[s]), ph, &sy->abort, lim, true)) { ok = false; break; }
@@ -416,7 +521,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const uint64_t bd =
                             B_KMAJOR ? smem_desc(b_addr + kk * A_K_STEP, 16, 1024)
                                      : smem_desc(b_addr + kk * B_K_STEP, B_CHUNK_BYTES, 1024);
-                        tc_mma<ESZ>(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                        tc_mma<ESZ>(d_tmem, ad, bd, IDESC, (kb != w.kb0 || kk != 0) ? 1u : 0u);
                     }
                     tc_commit(smem_u32(&sy->empty[s]));      // frees the slot when done
                 }
@@ -433,35 +538,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         const int q = warp & 3;                 // TMEM lanes 32q .. 32q+31
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         int it = 0;
-        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++it) {
+            const Unit w = decode_unit(u, p);
             int mb, nb;
-            tile_coords(t, p, mb, nb);
+            tile_coords(w.tile, p, mb, nb);
             const int acc = it & 1;
             const uint32_t aph = (uint32_t)(it >> 1) & 1u;
             bool ok = mbar_wait(smem_u32(&sy->tmem_full[acc]), aph, &sy->abort, lim, true);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
-            const int row = mb * BM + q * 32 + lane;
-            float* crow = p.C + (long)row * p.ldc;
-            for (int c = 0; c < BN / 32; ++c) {
-                const int col0 = nb * BN + c * 32;
-                if (col0 >= p.N) break;                     // uniform across the warp
-                uint32_t r[32];
-                tmem_ld32(tmem_base + lane_off + (uint32_t)(acc * BN + c * 32), r);
-                if (row < p.M) {
-                    if (p.vec_c && col0 + 31 < p.N) {
-#pragma unroll
-                        for (int j = 0; j < 32; j += 4)
-                            *reinterpret_cast<float4*>(crow + col0 + j) =
-                                make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                                            __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (col0 + j < p.N) crow[col0 + j] = __uint_as_float(r[j]);
-                    }
-                }
-            }
+            store_accumulator(p, w, mb, nb, q * 32 + lane, tmem_base + lane_off + (uint32_t)(acc * BN));
             tc_fence_before();
             mbar_arrive(smem_u32(&sy->tmem_empty[acc]));
         }
@@ -582,12 +668,13 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
         if (lane == 0) {
             uint32_t armed = 0, armed_parity = 0;
             int g = 0;
-            for (int t = pair; t < p.num_tiles; t += num_pairs) {
+            for (int u = pair; u < p.num_units; u += num_pairs) {
+                const Unit w = decode_unit(u, p);
                 int mb, nb;
-                tile_coords(t, p, mb, nb);
+                tile_coords(w.tile, p, mb, nb);
                 const int row0 = mb * P_BM + (int)rank * 128;
                 const int col0 = nb * BN + (int)rank * 128;
-                for (int kb = 0; kb < p.kblocks; ++kb, ++g) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++g) {
                     const int s = g % P_STAGES;
                     const uint32_t ph = (uint32_t)(g / P_STAGES) & 1u;
                     if (!mbar_wait(smem_u32(&sy->empty[s]), ph ^ 1u, &sy->abort, lim, true)) goto pair_producer_done;
@@ -627,14 +714,15 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
         // ------------------------------------------------ MMA issuer (leader CTA)
         if (lane == 0 && leader) {
             int g = 0, it = 0;
-            for (int t = pair; t < p.num_tiles; t += num_pairs, ++it) {
+            for (int u = pair; u < p.num_units; u += num_pairs, ++it) {
+                const Unit w = decode_unit(u, p);
                 const int acc = it & 1;
                 const uint32_t aph = (uint32_t)(it >> 1) & 1u;
                 if (!mbar_wait(smem_u32(&sy->tmem_empty[acc]), aph ^ 1u, &sy->abort, lim, true)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 bool ok = true;
-                for (int kb = 0; kb < p.kblocks; ++kb, ++g) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++g) {
                     const int s = g % P_STAGES;
                     const uint32_t ph = (uint32_t)(g / P_STAGES) & 1u;
                     if (!mbar_wait(smem_u32(&sy->full[s]), ph, &sy->abort, lim, true)) { ok = false; break; }
@@ -647,7 +735,7 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const uint64_t bd =
                             B_KMAJOR ? smem_desc(b_addr + kk * A_K_STEP, 16, 1024)
                                      : smem_desc(b_addr + kk * B_K_STEP, B_CHUNK_BYTES, 1024);
-                        tc_mma_pair<ESZ>(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                        tc_mma_pair<ESZ>(d_tmem, ad, bd, IDESC, (kb != w.kb0 || kk != 0) ? 1u : 0u);
                     }
                     tc_commit_pair_multicast(smem_u32(&sy->empty[s]));   // slot free in both CTAs
                 }
@@ -663,35 +751,17 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
         const int q = warp & 3;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         int it = 0;
-        for (int t = pair; t < p.num_tiles; t += num_pairs, ++it) {
+        for (int u = pair; u < p.num_units; u += num_pairs, ++it) {
+            const Unit w = decode_unit(u, p);
             int mb, nb;
-            tile_coords(t, p, mb, nb);
+            tile_coords(w.tile, p, mb, nb);
             const int acc = it & 1;
             const uint32_t aph = (uint32_t)(it >> 1) & 1u;
             bool ok = mbar_wait(smem_u32(&sy->tmem_full[acc]), aph, &sy->abort, lim, true);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
-            const int row = mb * P_BM + (int)rank * 128 + q * 32 + lane;
-            float* crow = p.C + (long)row * p.ldc;
-            for (int c = 0; c < BN / 32; ++c) {
-                const int col0 = nb * BN + c * 32;
-                if (col0 >= p.N) break;                     // uniform across the warp
-                uint32_t r[32];
-                tmem_ld32(tmem_base + lane_off + (uint32_t)(acc * BN + c * 32), r);
-                if (row < p.M) {
-                    if (p.vec_c && col0 + 31 < p.N) {
-#pragma unroll
-                        for (int j = 0; j < 32; j += 4)
-                            *reinterpret_cast<float4*>(crow + col0 + j) =
-                                make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                                            __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (col0 + j < p.N) crow[col0 + j] = __uint_as_float(r[j]);
-                    }
-                }
-            }
+            store_accumulator(p, w, mb, nb, (int)rank * 128 + q * 32 + lane,
+                              tmem_base + lane_off + (uint32_t)(acc * BN));
             tc_fence_before();
             mbar_arrive_cluster(tmem_empty0 + (uint32_t)(acc * sizeof(uint64_t)));
         }
@@ -727,64 +797,76 @@ bool encode_2d(EncodeTiledFn enc, CUtensorMap* map, const void* base, int esz, l
     return r == CUDA_SUCCESS;
 }
 
+TcParams make_params(const GemmArgs& a, const TcPlan& pl, float* partials,
+                     unsigned long long wait_limit_ns, int debug_stall) {
+    TcParams p;
+    p.M = a.M; p.N = a.N; p.K = a.K;
+    p.C = a.C; p.ldc = a.ldc;
+    p.tiles_m = pl.tiles_m;
+    p.tiles_n = pl.tiles_n;
+    p.num_tiles = pl.tiles_m * pl.tiles_n;
+    p.kblocks = pl.kblocks;
+    p.tile_rows = pl.tile_rows;
+    p.dp_tiles = pl.dp_tiles;
+    p.split = pl.split;
+    p.num_units = pl.dp_tiles + (p.num_tiles - pl.dp_tiles) * pl.split;
+    p.partials = partials;
+    p.wait_limit_ns = wait_limit_ns;
+    p.debug_stall = debug_stall;
+    p.vec_c = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0 && a.ldc % 4 == 0) ? 1 : 0;
+    return p;
+}
+
+cudaError_t launch_reduce(const TcParams& p, cudaStream_t s) {
+    const long units = (long)(p.num_tiles - p.dp_tiles) * p.tile_rows * (BN / 4);
+    long blocks = (units + 255) / 256;
+    if (blocks > 8192) blocks = 8192;
+    tc_splitk_reduce<<<(int)blocks, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
 template <int ESZ, bool B_KMAJOR>
-cudaError_t launch_tc(const GemmArgs& a, int num_sms, EncodeTiledFn enc,
-                      unsigned long long wait_limit_ns, int debug_stall, cudaStream_t s) {
+cudaError_t launch_tc(const GemmArgs& a, const TcPlan& pl, float* partials, int num_sms,
+                      EncodeTiledFn enc, unsigned long long wait_limit_ns, int debug_stall,
+                      cudaStream_t s) {
     constexpr int BK = Kind<ESZ>::BK;
     CUtensorMap tmA, tmB;
     if (!encode_2d(enc, &tmA, a.A, ESZ, a.M, a.K, a.lda, BK, BM)) return cudaErrorInvalidValue;
     const bool okb = B_KMAJOR ? encode_2d(enc, &tmB, a.B, ESZ, a.N, a.K, a.ldb, BK, BN)
                               : encode_2d(enc, &tmB, a.B, ESZ, a.K, a.N, a.ldb, SW / ESZ, BK);
     if (!okb) return cudaErrorInvalidValue;
-
-    TcParams p;
-    p.M = a.M; p.N = a.N; p.K = a.K;
-    p.C = a.C; p.ldc = a.ldc;
-    p.tiles_m = (a.M + BM - 1) / BM;
-    p.tiles_n = (a.N + BN - 1) / BN;
-    p.num_tiles = p.tiles_m * p.tiles_n;
-    p.kblocks = (a.K + BK - 1) / BK;
-    p.wait_limit_ns = wait_limit_ns;
-    p.debug_stall = debug_stall;
-    p.vec_c = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0 && a.ldc % 4 == 0) ? 1 : 0;
+    const TcParams p = make_params(a, pl, partials, wait_limit_ns, debug_stall);
 
     auto kern = tc_gemm_kernel<ESZ, B_KMAJOR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const int grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
+    const int grid = p.num_units < num_sms ? p.num_units : num_sms;
     kern<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tmA, tmB, p);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess || p.split <= 1) return e;
+    return launch_reduce(p, s);
 }
 
 // The 2-SM kernel: clusters of two CTAs, one CTA per SM, persistent over
 // 256 x 256 tiles.
 template <int ESZ, bool B_KMAJOR>
-cudaError_t launch_tc_pair(const GemmArgs& a, int num_sms, EncodeTiledFn enc,
-                           unsigned long long wait_limit_ns, int debug_stall, cudaStream_t s) {
+cudaError_t launch_tc_pair(const GemmArgs& a, const TcPlan& pl, float* partials, int num_sms,
+                           EncodeTiledFn enc, unsigned long long wait_limit_ns, int debug_stall,
+                           cudaStream_t s) {
     constexpr int BK = Kind<ESZ>::BK;
     CUtensorMap tmA, tmB;
     if (!encode_2d(enc, &tmA, a.A, ESZ, a.M, a.K, a.lda, BK, 128)) return cudaErrorInvalidValue;
     const bool okb = B_KMAJOR ? encode_2d(enc, &tmB, a.B, ESZ, a.N, a.K, a.ldb, BK, 128)
                               : encode_2d(enc, &tmB, a.B, ESZ, a.K, a.N, a.ldb, SW / ESZ, BK);
     if (!okb) return cudaErrorInvalidValue;
-
-    TcParams p;
-    p.M = a.M; p.N = a.N; p.K = a.K;
-    p.C = a.C; p.ldc = a.ldc;
-    p.tiles_m = (a.M + P_BM - 1) / P_BM;
-    p.tiles_n = (a.N + BN - 1) / BN;
-    p.num_tiles = p.tiles_m * p.tiles_n;
-    p.kblocks = (a.K + BK - 1) / BK;
-    p.wait_limit_ns = wait_limit_ns;
-    p.debug_stall = debug_stall;
-    p.vec_c = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0 && a.ldc % 4 == 0) ? 1 : 0;
+    const TcParams p = make_params(a, pl, partials, wait_limit_ns, debug_stall);
 
     auto kern = tc_gemm_2sm_kernel<ESZ, B_KMAJOR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          P_SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const int pairs = p.num_tiles < num_sms / 2 ? p.num_tiles : num_sms / 2;
+    const int pairs = p.num_units < num_sms / 2 ? p.num_units : num_sms / 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs, 1, 1);
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
@@ -799,7 +881,9 @@ cudaError_t launch_tc_pair(const GemmArgs& a, int num_sms, EncodeTiledFn enc,
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
     if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess || p.split <= 1) return e;
+    return launch_reduce(p, s);
 }
 
 const char* kNames[2][2] = {
@@ -808,6 +892,32 @@ const char* kNames[2][2] = {
 };
 
 }  // namespace
+
+TcPlan tc_plan(int M, int N, int K, int in_type, bool pair, int num_sms, bool allow_split) {
+    TcPlan pl;
+    pl.tile_rows = pair ? P_BM : BM;
+    pl.tiles_m = (M + pl.tile_rows - 1) / pl.tile_rows;
+    pl.tiles_n = (N + BN - 1) / BN;
+    const int bk = in_type == TC_BF16 ? Kind<2>::BK : Kind<4>::BK;
+    pl.kblocks = (K + bk - 1) / bk;
+    const int tiles = pl.tiles_m * pl.tiles_n;
+    pl.dp_tiles = tiles;
+    pl.split = 1;
+    if (allow_split) {
+        // Rate of one resident work unit (an SM pair or an SM), measured:
+        // BF16 ~1650 TFLOP/s over 76 pairs / ~1420 over 152 SMs; TF32 at
+        // half the BF16 rate.
+        double unit_tflops = pair ? 21.7 : 9.3;
+        if (in_type != TC_BF16) unit_tflops *= 0.5;
+        const double tile_us = 2.0 * pl.tile_rows * BN * (double)K / (unit_tflops * 1e6);
+        plan_tail_split(tiles, pair ? num_sms / 2 : num_sms, pl.kblocks, tile_us,
+                        (double)pl.tile_rows * BN * sizeof(float), pl.dp_tiles, pl.split);
+    }
+    pl.scratch_bytes = pl.split > 1 ? (size_t)(tiles - pl.dp_tiles) * pl.split * pl.tile_rows *
+                                          BN * sizeof(float)
+                                    : 0;
+    return pl;
+}
 
 bool tc_use_pair(int M, int mode) {
     if (mode == 0) return false;
@@ -821,20 +931,22 @@ const char* tc_kernel_name(int in_type, bool pair) {
 
 cudaError_t tc_launch(const GemmArgs& a, int in_type, int b_kmajor, int num_sms, void* encode_fn,
                       unsigned long long wait_limit_ns, int debug_stall, bool pair,
-                      cudaStream_t s) {
+                      const TcPlan& pl, float* partials, cudaStream_t s) {
     auto enc = reinterpret_cast<EncodeTiledFn>(encode_fn);
+    const unsigned long long w = wait_limit_ns;
+    const int st = debug_stall;
     if (pair) {
         if (in_type == TC_BF16)
-            return b_kmajor ? launch_tc_pair<2, true>(a, num_sms, enc, wait_limit_ns, debug_stall, s)
-                            : launch_tc_pair<2, false>(a, num_sms, enc, wait_limit_ns, debug_stall, s);
-        return b_kmajor ? launch_tc_pair<4, true>(a, num_sms, enc, wait_limit_ns, debug_stall, s)
-                        : launch_tc_pair<4, false>(a, num_sms, enc, wait_limit_ns, debug_stall, s);
+            return b_kmajor ? launch_tc_pair<2, true>(a, pl, partials, num_sms, enc, w, st, s)
+                            : launch_tc_pair<2, false>(a, pl, partials, num_sms, enc, w, st, s);
+        return b_kmajor ? launch_tc_pair<4, true>(a, pl, partials, num_sms, enc, w, st, s)
+                        : launch_tc_pair<4, false>(a, pl, partials, num_sms, enc, w, st, s);
     }
     if (in_type == TC_BF16)
-        return b_kmajor ? launch_tc<2, true>(a, num_sms, enc, wait_limit_ns, debug_stall, s)
-                        : launch_tc<2, false>(a, num_sms, enc, wait_limit_ns, debug_stall, s);
-    return b_kmajor ? launch_tc<4, true>(a, num_sms, enc, wait_limit_ns, debug_stall, s)
-                    : launch_tc<4, false>(a, num_sms, enc, wait_limit_ns, debug_stall, s);
+        return b_kmajor ? launch_tc<2, true>(a, pl, partials, num_sms, enc, w, st, s)
+                        : launch_tc<2, false>(a, pl, partials, num_sms, enc, w, st, s);
+    return b_kmajor ? launch_tc<4, true>(a, pl, partials, num_sms, enc, w, st, s)
+                    : launch_tc<4, false>(a, pl, partials, num_sms, enc, w, st, s);
 }
 
 cudaError_t tc_read_and_clear_status(int* status, cudaStream_t s) {

@@ -43,14 +43,34 @@ enum TcType { TC_TF32 = 1, TC_BF16 = 2 };
 // 1 = always.
 bool tc_use_pair(int M, int mode);
 const char* tc_kernel_name(int in_type, bool pair);
-// Launch the persistent tcgen05 kernel (one-SM, or 2-SM when `pair`).
-// `encode_fn` is cuTensorMapEncodeTiled. With b_kmajor, a.B / a.ldb describe
-// B transposed (N x K, K contiguous).
+// Tiling of one tensor-core product: tiles of tile_rows x 256, the first
+// dp_tiles whole, the rest (a partial last wave) in `split` K-pieces whose
+// partial tiles take scratch_bytes of device scratch (0 when split == 1).
+struct TcPlan {
+    int tile_rows, tiles_m, tiles_n, kblocks;
+    int dp_tiles, split;
+    size_t scratch_bytes;
+};
+TcPlan tc_plan(int M, int N, int K, int in_type, bool pair, int num_sms, bool allow_split);
+// Launch the persistent tcgen05 kernel (one-SM, or 2-SM when `pair`) under
+// plan `pl`, plus the K-piece reduction when pl.split > 1 (`partials` holds
+// pl.scratch_bytes). `encode_fn` is cuTensorMapEncodeTiled. With b_kmajor,
+// a.B / a.ldb describe B transposed (N x K, K contiguous).
 cudaError_t tc_launch(const GemmArgs& a, int in_type, int b_kmajor, int num_sms,
                       void* encode_fn, unsigned long long wait_limit_ns,
-                      int debug_stall, bool pair, cudaStream_t s);
+                      int debug_stall, bool pair, const TcPlan& pl, float* partials,
+                      cudaStream_t s);
 // Read and clear the tensor-core kernel's status word on the current device.
 cudaError_t tc_read_and_clear_status(int* status, cudaStream_t s);
+
+// ---- tail balancing (sgemm_f32.cu) --------------------------------------
+// Split of `tiles` work tiles over `slots` resident units: the first
+// dp_tiles whole, the tiles of a partial last wave in `split` K-pieces of at
+// least 4 K-blocks (of `ktiles`). `tile_us` is the time of one whole tile on
+// one unit and `tile_bytes` the size of its FP32 partial; the split that
+// saves the most time net of its scratch traffic is taken (split = 1: none).
+void plan_tail_split(int tiles, int slots, int ktiles, double tile_us, double tile_bytes,
+                     int& dp_tiles, int& split);
 
 // ---- layout pre-pass (transpose_f32.cu) ---------------------------------
 // Bt[n][k] = B[k][n] for a K x N matrix B (ldb) into Bt (N x K, ldt >= K).
