@@ -398,7 +398,8 @@ def run_e2e(tg, A_host, B_host, w, dev, reps):
     out_bytes = C1.numel() * 4 + C2.numel() * 4
     return {"value": round(2 * w.flops / (ms * 1e-3) / 1e12, 3), "unit": UNIT,
             "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
-            "ms_per_step": round(ms, 4), "api": "tiled_matrix_multiplication_sm_gb300.matmul"}
+            "ms_per_step": round(ms, 4),
+            "api": "tiled_matrix_multiplication_sm_gb300.matmul -> C ABI gemm_host (copies overlapped)"}
 
 
 def run_workloads(tg, inputs, dev, flush, peaks, fp32_peak):
@@ -479,6 +480,48 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def run_single(args):
+    """Time one (workload, path) product alone: --workload NAME:PATH."""
+    import torch
+    import tiled_matrix_multiplication_sm_gb300 as tg
+    from tiled_matrix_multiplication_sm_gb300 import inputs
+
+    name, _, path = args.workload.partition(":")
+    w = inputs.WORKLOADS[name]
+    path = path or w.paths[0]
+    if path not in ("f32", "tf32", "bf16"):
+        raise SystemExit(f"unknown path {path!r}")
+    dev = torch.device("cuda", 0)
+    tg.load()
+    props = torch.cuda.get_device_properties(0)
+    peaks = load_peaks()
+    A_host, B_host = inputs.operands(w)
+    A, B = A_host.to(dev), B_host.to(dev)
+    C = torch.empty(w.M, w.N, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    if path == "f32":
+        fn = lambda: tg.gemm_f32(A, B, out=C)          # noqa: E731
+        peak, bound = fp32_peak_tflops(props.multi_processor_count, peaks["sm_max_mhz"]), "alu"
+    else:
+        fn = lambda: tg.gemm_tc(A, B, path, out=C)     # noqa: E731
+        peak = peaks["bf16_tflops"] * (NOMINAL_TF32_OVER_BF16 if path == "tf32" else 1.0)
+        bound = "tensor"
+    for _ in range(args.warmup):
+        fn()
+    ms = time_calls(fn, args.steps, flush)
+    if tg.device_status() != 0:
+        raise RuntimeError("a kernel wait timed out")
+    tf = w.flops / (ms * 1e-3) / 1e12
+    print(json.dumps({"metric": METRIC, "value": round(tf, 3), "unit": UNIT, "n_gpus": 1,
+                      "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+                      "higher_is_better": True, "config": {"workload": w.description,
+                                                          "path": path},
+                      "kernel": tg.binding.last_kernel(),
+                      "roofline": {"bound": bound, "achieved": round(tf, 3),
+                                   "peak": round(peak, 3), "unit": UNIT,
+                                   "frac": round(tf / peak, 4)}}), flush=True)
+
+
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -489,6 +532,9 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--ref-seconds", type=float, default=90.0)
+    p.add_argument("--workload", default=None,
+                   help="time one product alone, NAME:PATH (e.g. ffn_bf16:bf16); median "
+                        "of --steps calls")
     args = p.parse_args(argv)
     args.warmup = max(args.warmup, 3)      # at least three warm-up steps, always
     return args
@@ -498,6 +544,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload:
+        run_single(args)
     else:
         run_gpu(args)
 

@@ -114,6 +114,39 @@ TGEMM_API int gemm_tc(int M, int N, int K,
             int in_type,
             cudaStream_t stream);
 
+/* Paths of gemm_host. */
+#define TGEMM_PATH_F32   0   /* gemm_f32: FP32 on the CUDA cores, A and B float */
+#define TGEMM_PATH_TF32  1   /* gemm_tc TGEMM_TF32: A and B float */
+#define TGEMM_PATH_BF16  2   /* gemm_tc TGEMM_BF16: A and B bfloat16 */
+
+/*
+ * gemm_host — the same product for operands and result in HOST memory.
+ *
+ * A (M x K, lda >= K), B (K x N, ldb >= N) and C (M x N floats, ldc >= N)
+ * are host pointers, ideally page-locked (cudaHostAlloc / pinned), with
+ * elements of the path's type. The call stages them through stream-ordered
+ * device scratch from the library's pool and overlaps the transfers with
+ * the multiplication: B is copied first, A follows in up to four row panels
+ * on a copy stream, each panel is multiplied on `stream` as soon as its rows
+ * have arrived (the TF32 path transposes B once for all panels), and each
+ * panel of C is copied back on a second copy stream while the next panel
+ * computes. Same arithmetic and result as gemm_f32 / gemm_tc on device
+ * copies of the operands.
+ *
+ * The call is asynchronous like cudaMemcpyAsync: it returns once the work is
+ * enqueued; C is complete (and A, B may be reused) when `stream` has been
+ * synchronised. With pageable host memory the CUDA copies become
+ * synchronous and there is no overlap. Returns TGEMM_OK,
+ * TGEMM_ERR_INVALID_ARG (as gemm_f32, or an unknown path, or an operand not
+ * aligned to its element size), TGEMM_ERR_UNSUPPORTED or TGEMM_ERR_CUDA.
+ */
+TGEMM_API int gemm_host(int M, int N, int K,
+                        const void* A, long lda,
+                        const void* B, long ldb,
+                        float* C, long ldc,
+                        int path,
+                        cudaStream_t stream);
+
 /*
  * gemm_device_status — result of the kernels' bounded waits.
  *

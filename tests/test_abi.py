@@ -35,7 +35,7 @@ def test_header_declares_the_boundary():
     names = declared_symbols()
     for required in ["gemm_f32", "gemm_tc", "gemm_status_string", "gemm_device_status"]:
         assert required in names
-    assert len(names) == 12
+    assert len(names) == 13
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -85,6 +85,13 @@ def test_f32_invalid_arguments(lib, args):
 ])
 def test_tc_invalid_arguments(lib, args, code):
     assert tg.gemm_tc_raw(*args, 0) == code
+
+
+def test_host_entry_rejects_bad_arguments(lib):
+    assert lib.gemm_host(4, 4, 4, FAKE, 4, FAKE, 4, FAKE, 4, 7, 0) == binding.TGEMM_ERR_INVALID_ARG
+    assert lib.gemm_host(4, 4, 4, FAKE, 3, FAKE, 4, FAKE, 4, 0, 0) == binding.TGEMM_ERR_INVALID_ARG
+    assert lib.gemm_host(4, 4, 4, FAKE + 2, 4, FAKE, 4, FAKE, 4, 0, 0) == binding.TGEMM_ERR_INVALID_ARG
+    assert lib.gemm_host(0, 4, 4, 0, 4, 0, 4, 0, 4, 0, 0) == binding.TGEMM_OK
 
 
 @pytest.mark.parametrize("M,N", [(0, 5), (5, 0), (0, 0)])

@@ -1,0 +1,94 @@
+"""gemm_host: the product for operands in host memory, with the transfers
+overlapped with the multiplication (row panels of A and C), checked against
+the CPU oracle through the C ABI on all three paths."""
+import pytest
+import torch
+
+import oracle
+from tests.parity import (F32_ABS, F32_REL, TC_ABS, TC_REL, assert_bit_exact,
+                          assert_within)
+from tiled_matrix_multiplication_sm_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+DTYPE = {"f32": torch.float32, "tf32": torch.float32, "bf16": torch.bfloat16}
+
+
+def host_padded(x, ld, pinned=True, pad=float("nan")):
+    rows, cols = x.shape
+    store = torch.full((rows, ld), pad, dtype=x.dtype, pin_memory=pinned)
+    store[:, :cols] = x
+    return store[:, :cols]
+
+
+@pytest.mark.parametrize("path", ["f32", "tf32", "bf16"])
+@pytest.mark.parametrize("shape", [(1, 1, 1), (7, 9, 3), (300, 520, 200), (1024, 264, 136),
+                                   (2100, 300, 64), (513, 1000, 1)])
+def test_integer_bit_exact(tgemm, path, shape):
+    M, N, K = shape
+    g = inputs.generator(M + 7 * N + 13 * K)
+    A = inputs.draw(M, K, "int4", g).to(DTYPE[path]).pin_memory()
+    B = inputs.draw(K, N, "int4", g).to(DTYPE[path]).pin_memory()
+    C = tgemm.matmul(A, B, path)
+    assert C.device.type == "cpu"
+    assert tgemm.binding.last_kernel().startswith("host_pipeline")
+    assert tgemm.device_status() == 0
+    C_ref, _ = oracle.gemm(A, B)
+    assert_bit_exact(C, C_ref, f"host {path} {shape}")
+
+
+@pytest.mark.parametrize("path", ["f32", "tf32", "bf16"])
+def test_padded_host_layouts_and_canaries(tgemm, path):
+    """Host leading dimensions with NaN padding (never read) and a C whose
+    padding columns must stay untouched."""
+    M, N, K = 1100, 333, 97
+    g = inputs.generator(55)
+    A = host_padded(inputs.draw(M, K, "int4", g).to(DTYPE[path]), 101)
+    B = host_padded(inputs.draw(K, N, "int4", g).to(DTYPE[path]), 350)
+    Cstore = torch.full((M, 341), 4321.0, pin_memory=True)
+    C = Cstore[:, :N]
+    tgemm.binding.gemm_host(A, B, path, out=C)
+    C_ref, _ = oracle.gemm(A, B)
+    assert_bit_exact(C, C_ref, f"padded host {path}")
+    assert (Cstore[:, N:] == 4321.0).all()
+
+
+@pytest.mark.parametrize("path", ["f32", "tf32", "bf16"])
+def test_float_tolerance_pageable(tgemm, path):
+    M, N, K = 700, 640, 300
+    g = inputs.generator(66)
+    dist = "normal002" if path == "bf16" else "normal"
+    A = inputs.draw(M, K, dist, g).to(DTYPE[path])          # pageable host memory
+    B = inputs.draw(K, N, dist, g).to(DTYPE[path])
+    C = tgemm.binding.gemm_host(A, B, path)
+    C_ref, absAB = oracle.gemm(A, B)
+    rel, abs_ = (F32_REL, F32_ABS) if path == "f32" else (TC_REL, TC_ABS)
+    assert_within(C, C_ref, absAB, rel, abs_, f"pageable {path}")
+
+
+def test_k_zero_and_empty(tgemm):
+    C = tgemm.binding.gemm_host(torch.empty(5, 0), torch.empty(0, 7), "f32")
+    assert (C == 0).all()
+    C = tgemm.binding.gemm_host(torch.empty(0, 4), torch.ones(4, 7), "f32")
+    assert C.shape == (0, 7)
+
+
+def test_workload_n4096_host_sampled(tgemm):
+    """The benchmark's end-to-end call on its full workload (FP32 path)."""
+    w = inputs.WORKLOADS["n4096"]
+    A, B = inputs.operands(w)
+    C = tgemm.matmul(A.pin_memory(), B.pin_memory(), "f32")
+    rows = [0, 1, 1023, 1024, 2047, 2048, 3071, 3072, 4095]
+    C_ref, absAB = oracle.gemm_rows(A, B, rows)
+    assert_within(C[rows], C_ref, absAB, F32_REL, F32_ABS, "n4096 host")
+
+
+def test_invalid_path_and_misaligned_host_operand(tgemm):
+    b = tgemm.binding
+    A = torch.ones(4, 4, dtype=torch.bfloat16)
+    B = torch.ones(4, 4, dtype=torch.bfloat16)
+    C = torch.empty(4, 4)
+    assert b.load().gemm_host(4, 4, 4, A.data_ptr(), 4, B.data_ptr(), 4, C.data_ptr(), 4, 7,
+                              0) == b.TGEMM_ERR_INVALID_ARG
+    assert b.load().gemm_host(4, 4, 4, A.data_ptr() + 1, 4, B.data_ptr(), 4, C.data_ptr(), 4, 2,
+                              0) == b.TGEMM_ERR_INVALID_ARG

@@ -34,6 +34,9 @@ _SIGNATURES = {
     "gemm_tc": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                _VP, ctypes.c_long, _VP, ctypes.c_long,
                                _VP, ctypes.c_long, ctypes.c_int, _VP]),
+    "gemm_host": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                 _VP, ctypes.c_long, _VP, ctypes.c_long,
+                                 _VP, ctypes.c_long, ctypes.c_int, _VP]),
     "gemm_device_status": (ctypes.c_int, [_VP]),
     "gemm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gemm_set_wait_limit_ns": (ctypes.c_int, [ctypes.c_longlong]),
@@ -210,31 +213,61 @@ def last_kernel() -> str:
     return load().gemm_last_kernel().decode()
 
 
+TGEMM_PATH = {"f32": 0, "tf32": 1, "bf16": 2}
+_PATH_DTYPE = {"f32": torch.float32, "tf32": torch.float32, "bf16": torch.bfloat16}
+
+
+def _check_host_matrix(x: torch.Tensor, name: str, dtype: torch.dtype) -> int:
+    if not isinstance(x, torch.Tensor) or x.dim() != 2:
+        raise ValueError(f"{name} must be a 2-D tensor")
+    if x.device.type != "cpu":
+        raise ValueError(f"{name} must be a host tensor")
+    if x.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {x.dtype}")
+    if x.shape[1] > 1 and x.stride(1) != 1:
+        raise ValueError(f"{name} must have unit column stride (row-major)")
+    return max(int(x.stride(0)), int(x.shape[1]), 1)
+
+
+def gemm_host(A: torch.Tensor, B: torch.Tensor, path: str = "f32",
+              out: Optional[torch.Tensor] = None,
+              stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """C = A @ B for HOST operands through gemm_host (copies overlapped with
+    the product). Returns once C is complete on the host."""
+    dtype = _PATH_DTYPE[path]
+    lda = _check_host_matrix(A, "A", dtype)
+    ldb = _check_host_matrix(B, "B", dtype)
+    M, K = A.shape
+    if B.shape[0] != K:
+        raise ValueError(f"inner dimensions differ: {tuple(A.shape)} x {tuple(B.shape)}")
+    N = B.shape[1]
+    C = out if out is not None else torch.empty((M, N), dtype=torch.float32, pin_memory=True)
+    if tuple(C.shape) != (M, N) or C.dtype != torch.float32:
+        raise ValueError("out must be a float32 M x N host tensor")
+    ldc = _check_host_matrix(C, "out", torch.float32)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    st = int(load().gemm_host(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(), ldc,
+                              TGEMM_PATH[path], int(s.cuda_stream)))
+    if st != TGEMM_OK:
+        raise TgemmError(st, "gemm_host")
+    s.synchronize()
+    return C
+
+
 def matmul(A: torch.Tensor, B: torch.Tensor, path: str = "f32",
            out: Optional[torch.Tensor] = None) -> torch.Tensor:
     """End-to-end product through the library for host or device operands.
 
     ``path`` is "f32" (CUDA cores), "tf32" or "bf16" (tensor cores). Host
-    operands are copied to the current CUDA device (from pinned memory when
-    they are pinned), multiplied there, and the result is copied back to the
-    host (into ``out`` if given, ideally pinned) before the call returns;
-    device operands give a device result (in ``out`` if given).
+    operands go through gemm_host (copies to the device overlapped with the
+    product, result copied back, into ``out`` if given -- ideally pinned)
+    and the call returns once C is on the host; device operands give a
+    device result (in ``out`` if given).
     """
-    on_host = A.device.type == "cpu"
-    if on_host:
-        dev = torch.device("cuda", torch.cuda.current_device())
-        A = A.to(dev, non_blocking=A.is_pinned())
-        B = B.to(dev, non_blocking=B.is_pinned())
-    dev_out = None if on_host else out
-    if path == "f32":
-        C = gemm_f32(A, B, out=dev_out)
-    elif path in _TC_TYPES:
-        C = gemm_tc(A, B, path, out=dev_out)
-    else:
+    if path not in _PATH_DTYPE:
         raise ValueError(f"unknown path {path!r}")
-    if on_host:
-        host = out if out is not None else torch.empty(C.shape, dtype=C.dtype, pin_memory=True)
-        host.copy_(C, non_blocking=host.is_pinned())
-        torch.cuda.current_stream().synchronize()
-        return host
-    return C
+    if A.device.type == "cpu":
+        return gemm_host(A, B, path, out=out)
+    if path == "f32":
+        return gemm_f32(A, B, out=out)
+    return gemm_tc(A, B, path, out=out)

@@ -19,7 +19,9 @@ struct DeviceInfo {
     bool supported = false;
     int num_sms = 0;
     bool pool_ready = false;
-    cudaMemPool_t pool = nullptr;   // scratch for the TF32 path's transposed B
+    cudaMemPool_t pool = nullptr;   // stream-ordered scratch (see scratch_pool)
+    cudaStream_t copy_in = nullptr; // host-operand pipeline of gemm_host
+    cudaStream_t copy_out = nullptr;
 };
 
 std::mutex g_mutex;
@@ -85,6 +87,21 @@ cudaMemPool_t scratch_pool(int dev) {
     }
     return d.pool;
 }
+
+// The two copy streams gemm_host uses on device `dev` (created once).
+bool copy_streams(int dev, cudaStream_t* in, cudaStream_t* out) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo& d = g_devices[dev];
+    if (d.copy_in == nullptr) {
+        if (cudaStreamCreateWithFlags(&d.copy_in, cudaStreamNonBlocking) != cudaSuccess) return false;
+        if (cudaStreamCreateWithFlags(&d.copy_out, cudaStreamNonBlocking) != cudaSuccess) return false;
+    }
+    *in = d.copy_in;
+    *out = d.copy_out;
+    return true;
+}
+
+size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
 
 void* encode_fn() {
     std::lock_guard<std::mutex> lock(g_mutex);
@@ -232,6 +249,173 @@ int gemm_tc(int M, int N, int K, const void* A, long lda, const void* B, long ld
         if (plan.split > 1) snprintf(split, sizeof(split), "+splitk_reduce(split=%d)", plan.split);
         snprintf(g_last_kernel_buf, sizeof(g_last_kernel_buf), "%s%s%s",
                  tf32 ? "transpose_b+" : "", tgemm::tc_kernel_name(in_type, pair), split);
+        g_last_kernel = g_last_kernel_buf;
+    }
+    return rc;
+}
+
+int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long ldb, float* C,
+              long ldc, int path, cudaStream_t stream) {
+    g_last_kernel = "";
+    if (path != TGEMM_PATH_F32 && path != TGEMM_PATH_TF32 && path != TGEMM_PATH_BF16)
+        return TGEMM_ERR_INVALID_ARG;
+    int st = check_common(M, N, K, A, lda, B, ldb, C, ldc);
+    if (st == -1) return TGEMM_OK;
+    if (st != TGEMM_OK) return st;
+    const size_t esz = path == TGEMM_PATH_BF16 ? 2 : 4;
+    if (K > 0 && (reinterpret_cast<uintptr_t>(A) % esz != 0 ||
+                  reinterpret_cast<uintptr_t>(B) % esz != 0))
+        return TGEMM_ERR_INVALID_ARG;
+
+    DeviceInfo dev;
+    st = current_device_info(&dev);
+    if (st != TGEMM_OK) return st;
+    int devno = 0;
+    if (cudaGetDevice(&devno) != cudaSuccess) return TGEMM_ERR_CUDA;
+    cudaStream_t s_in, s_out;
+    if (!copy_streams(devno, &s_in, &s_out)) return TGEMM_ERR_CUDA;
+    cudaMemPool_t pool = scratch_pool(devno);
+    if (pool == nullptr) return TGEMM_ERR_CUDA;
+
+    // Device copies with 16-byte rows (what every loader and TMA copy takes).
+    const long per16 = (long)(16 / esz);
+    const long lda_d = (K + per16 - 1) / per16 * per16;
+    const long ldb_d = (N + per16 - 1) / per16 * per16;
+    const long ldc_d = (N + 3) / 4 * 4;
+
+    // Row panels: each panel is multiplied as soon as its rows of A have
+    // arrived, and its rows of C leave while the next panel computes.
+    // Panels are >= 512 rows on 256-row boundaries, at most 4.
+    int panels = M >= 1024 ? (M >= 2048 ? 4 : 2) : 1;
+    long bounds[5];
+    for (int i = 0; i <= panels; ++i) {
+        long r = (long)M * i / panels;
+        if (i > 0 && i < panels) r = r / 256 * 256;
+        bounds[i] = r;
+    }
+
+    // Plans and scratch: one pool block for A, B, C, (B transposed), partials.
+    const bool tc = path != TGEMM_PATH_F32;
+    const int in_type = path == TGEMM_PATH_BF16 ? TGEMM_BF16 : TGEMM_TF32;
+    const long ldt = (K + 3) / 4 * 4;
+    size_t off_b = align256((size_t)M * lda_d * esz);
+    size_t off_c = off_b + align256((size_t)K * ldb_d * esz);
+    size_t off_t = off_c + align256((size_t)M * ldc_d * 4);
+    size_t off_p = off_t + (path == TGEMM_PATH_TF32 ? align256((size_t)N * ldt * 4) : 0);
+    int f32_id[4] = {0, 0, 0, 0};
+    tgemm::F32Plan f32_plan[4];
+    tgemm::TcPlan tc_plan[4];
+    bool pair[4] = {false, false, false, false};
+    size_t part_off[4];
+    size_t total = off_p;
+    for (int i = 0; i < panels; ++i) {
+        const int rows = (int)(bounds[i + 1] - bounds[i]);
+        part_off[i] = total;
+        if (K == 0) continue;
+        if (tc) {
+            pair[i] = tgemm::tc_use_pair(rows, g_tc_mode.load());
+            tc_plan[i] = tgemm::tc_plan(rows, N, K, in_type, pair[i], dev.num_sms, true);
+            total += align256(tc_plan[i].scratch_bytes);
+        } else {
+            // Device operands are 16-byte aligned: the vector loaders apply.
+            tgemm::GemmArgs pa{rows, N, K, nullptr, lda_d, nullptr, ldb_d, nullptr, ldc_d};
+            const int forced = g_forced_f32.load();
+            f32_id[i] = forced >= 0 ? forced : 0;
+            f32_plan[i] = tgemm::f32_plan(f32_id[i], pa, dev.num_sms);
+            total += align256(f32_plan[i].scratch_bytes);
+        }
+    }
+    void* ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, total, pool, stream) != cudaSuccess) return TGEMM_ERR_CUDA;
+    char* base = static_cast<char*>(ws);
+    char* Ad = base;
+    char* Bd = base + off_b;
+    float* Cd = reinterpret_cast<float*>(base + off_c);
+    float* Bt = reinterpret_cast<float*>(base + off_t);
+
+    const int nev = 2 * panels + 3;
+    cudaEvent_t ev[2 * 4 + 3];
+    for (int i = 0; i < nev; ++i)
+        if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) {
+            for (int j = 0; j < i; ++j) cudaEventDestroy(ev[j]);
+            cudaFreeAsync(ws, stream);
+            return TGEMM_ERR_CUDA;
+        }
+    cudaEvent_t ev_ready = ev[0], ev_b = ev[1], ev_out = ev[2];
+    cudaEvent_t* ev_a = ev + 3;
+    cudaEvent_t* ev_c = ev + 3 + panels;
+    int rc = TGEMM_OK;
+    auto ok = [&](cudaError_t e) {
+        if (e != cudaSuccess && rc == TGEMM_OK) rc = TGEMM_ERR_CUDA;
+        return e == cudaSuccess;
+    };
+    const unsigned long long limit = (unsigned long long)g_wait_limit_ns.load();
+    const int stall = g_debug_stall.load();
+    void* enc = tc ? encode_fn() : nullptr;
+    if (tc && enc == nullptr) rc = TGEMM_ERR_CUDA;
+
+    // The scratch block is valid on `stream` from here on.
+    ok(cudaEventRecord(ev_ready, stream));
+    ok(cudaStreamWaitEvent(s_in, ev_ready, 0));
+    ok(cudaStreamWaitEvent(s_out, ev_ready, 0));
+    if (K > 0)
+        ok(cudaMemcpy2DAsync(Bd, ldb_d * esz, B, ldb * esz, N * esz, K, cudaMemcpyHostToDevice,
+                             s_in));
+    ok(cudaEventRecord(ev_b, s_in));
+    for (int i = 0; i < panels; ++i) {
+        const long r0 = bounds[i], rows = bounds[i + 1] - bounds[i];
+        if (K > 0)
+            ok(cudaMemcpy2DAsync(Ad + r0 * lda_d * esz, lda_d * esz,
+                                 static_cast<const char*>(A) + r0 * lda * esz, lda * esz, K * esz,
+                                 rows, cudaMemcpyHostToDevice, s_in));
+        ok(cudaEventRecord(ev_a[i], s_in));
+    }
+    ok(cudaStreamWaitEvent(stream, ev_b, 0));
+    if (rc == TGEMM_OK && path == TGEMM_PATH_TF32 && K > 0)
+        ok(tgemm::transpose_f32(reinterpret_cast<const float*>(Bd), ldb_d, Bt, ldt, K, N, stream));
+    const char* name = "";
+    for (int i = 0; i < panels && rc == TGEMM_OK; ++i) {
+        const long r0 = bounds[i];
+        const int rows = (int)(bounds[i + 1] - bounds[i]);
+        ok(cudaStreamWaitEvent(stream, ev_a[i], 0));
+        float* Cp = Cd + r0 * ldc_d;
+        float* part = reinterpret_cast<float*>(base + part_off[i]);
+        if (K == 0) {
+            ok(tgemm::zero_fill(Cp, ldc_d, rows, N, stream));
+            name = "zero_fill";
+        } else if (tc) {
+            const bool tf32 = path == TGEMM_PATH_TF32;
+            tgemm::GemmArgs pa{rows, N, K, Ad + r0 * lda_d * esz, lda_d,
+                               tf32 ? static_cast<const void*>(Bt) : Bd, tf32 ? ldt : ldb_d, Cp,
+                               ldc_d};
+            ok(tgemm::tc_launch(pa, in_type, tf32 ? 1 : 0, dev.num_sms, enc, limit, stall, pair[i],
+                                tc_plan[i], part, stream));
+            name = tgemm::tc_kernel_name(in_type, pair[i]);
+        } else {
+            tgemm::GemmArgs pa{rows, N, K, Ad + r0 * lda_d * esz, lda_d, Bd, ldb_d, Cp, ldc_d};
+            ok(tgemm::f32_launch(f32_id[i], pa, f32_plan[i], part, stream));
+            name = tgemm::f32_kernel_name(f32_id[i]);
+        }
+        ok(cudaEventRecord(ev_c[i], stream));
+    }
+    for (int i = 0; i < panels && rc == TGEMM_OK; ++i) {
+        const long r0 = bounds[i], rows = bounds[i + 1] - bounds[i];
+        ok(cudaStreamWaitEvent(s_out, ev_c[i], 0));
+        ok(cudaMemcpy2DAsync(C + r0 * ldc, ldc * sizeof(float), Cd + r0 * ldc_d,
+                             ldc_d * sizeof(float), N * sizeof(float), rows,
+                             cudaMemcpyDeviceToHost, s_out));
+    }
+    ok(cudaEventRecord(ev_out, s_out));
+    // Whatever happened above, the caller's stream orders after every copy
+    // before the scratch goes back to the pool.
+    cudaStreamWaitEvent(stream, ev_out, 0);
+    cudaStreamWaitEvent(stream, ev_b, 0);
+    for (int i = 0; i < panels; ++i) cudaStreamWaitEvent(stream, ev_a[i], 0);
+    if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == TGEMM_OK) rc = TGEMM_ERR_CUDA;
+    for (int i = 0; i < nev; ++i) cudaEventDestroy(ev[i]);
+    if (rc == TGEMM_OK) {
+        snprintf(g_last_kernel_buf, sizeof(g_last_kernel_buf), "host_pipeline(panels=%d)+%s%s",
+                 panels, path == TGEMM_PATH_TF32 && K > 0 ? "transpose_b+" : "", name);
         g_last_kernel = g_last_kernel_buf;
     }
     return rc;
