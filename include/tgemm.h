@@ -56,7 +56,7 @@ extern "C" {
 /* Status codes returned by every entry point. */
 #define TGEMM_OK                    0
 #define TGEMM_ERR_INVALID_ARG       1  /* negative size, ld too small, null pointer, bad in_type */
-#define TGEMM_ERR_ALIGNMENT         2  /* the tensor-core path needs 16-byte aligned pointers and ld */
+#define TGEMM_ERR_ALIGNMENT         2  /* a forced kernel or the no-alloc entry cannot read this layout */
 #define TGEMM_ERR_CUDA              3  /* a CUDA runtime call or launch failed */
 #define TGEMM_ERR_DEVICE_TIMEOUT    4  /* a bounded wait inside a kernel ran out (see gemm_device_status) */
 #define TGEMM_ERR_UNSUPPORTED       5  /* the current device is not sm_103 / sm_100 class */
@@ -99,13 +99,17 @@ TGEMM_API int gemm_f32(int M, int N, int K,
  *   TGEMM_BF16: A and B are bfloat16 arrays; products are exact and are
  *               accumulated in FP32.
  * C is FP32 (ldc >= N, any alignment). Tiles of A and B are copied by the
- * Tensor Memory Accelerator, which requires A and B to start on 16-byte
- * boundaries and lda, ldb to be multiples of 16 bytes (4 floats / 8 bf16);
- * otherwise TGEMM_ERR_ALIGNMENT is returned and nothing is launched (no other
- * kernel is substituted). Rows and columns past M, N, K read as zero.
+ * Tensor Memory Accelerator, which needs rows that start on 16-byte
+ * boundaries: an operand whose pointer or leading dimension breaks that
+ * (any lda, ldb and element-aligned pointer are accepted) is first repacked
+ * by an HBM-bound kernel into stream-ordered scratch with 16-byte rows; for
+ * TF32, B is always rewritten transposed (the TF32 kind reads B only
+ * K-major), which also absorbs any alignment of B. Rows and columns past M,
+ * N, K read as zero.
  *
- * Returns TGEMM_OK, TGEMM_ERR_INVALID_ARG, TGEMM_ERR_ALIGNMENT,
- * TGEMM_ERR_UNSUPPORTED or TGEMM_ERR_CUDA.
+ * Returns TGEMM_OK, TGEMM_ERR_INVALID_ARG (as gemm_f32, a bad in_type, or
+ * a pointer not aligned to its element size), TGEMM_ERR_UNSUPPORTED or
+ * TGEMM_ERR_CUDA.
  */
 TGEMM_API int gemm_tc(int M, int N, int K,
             const void* A, long lda,

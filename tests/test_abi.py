@@ -77,10 +77,10 @@ def test_f32_invalid_arguments(lib, args):
     ((4, 4, 4, FAKE, 4, FAKE, 4, FAKE, 4, 0), binding.TGEMM_ERR_INVALID_ARG),
     ((-1, 4, 4, FAKE, 4, FAKE, 4, FAKE, 4, 2), binding.TGEMM_ERR_INVALID_ARG),
     ((4, 4, 8, FAKE, 4, FAKE, 4, FAKE, 4, 2), binding.TGEMM_ERR_INVALID_ARG),     # lda < K
-    ((4, 8, 8, FAKE + 4, 8, FAKE, 8, FAKE, 8, 2), binding.TGEMM_ERR_ALIGNMENT),   # A off 16 B
-    ((4, 8, 8, FAKE, 8, FAKE + 8, 8, FAKE, 8, 2), binding.TGEMM_ERR_ALIGNMENT),   # B off 16 B
-    ((4, 8, 12, FAKE, 12, FAKE, 8, FAKE, 8, 2), binding.TGEMM_ERR_ALIGNMENT),     # bf16 lda*2 % 16
-    ((4, 6, 8, FAKE, 8, FAKE, 6, FAKE, 6, 1), binding.TGEMM_ERR_ALIGNMENT),       # tf32 ldb*4 % 16
+    ((4, 8, 8, FAKE + 1, 8, FAKE, 8, FAKE, 8, 2), binding.TGEMM_ERR_INVALID_ARG), # bf16 A odd byte
+    ((4, 8, 8, FAKE, 8, FAKE + 3, 8, FAKE, 8, 2), binding.TGEMM_ERR_INVALID_ARG), # bf16 B odd byte
+    ((4, 8, 8, FAKE + 2, 8, FAKE, 8, FAKE, 8, 1), binding.TGEMM_ERR_INVALID_ARG), # tf32 A not 4-B
+    ((4, 8, 8, FAKE, 8, FAKE + 6, 8, FAKE, 8, 1), binding.TGEMM_ERR_INVALID_ARG), # tf32 B not 4-B
     ((4, 8, 8, FAKE, 8, FAKE, 8, FAKE + 2, 8, 1), binding.TGEMM_ERR_INVALID_ARG), # C misaligned
 ])
 def test_tc_invalid_arguments(lib, args, code):

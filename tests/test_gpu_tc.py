@@ -139,12 +139,46 @@ def test_ragged_edges_with_nan_padding(tgemm, kind):
     assert (host[guard:guard + M * ldc].view(M, ldc)[:, N:] == -777.0).all()
 
 
-def test_misaligned_leading_dimension_rejected(tgemm):
-    A = torch.ones(16, 12, dtype=torch.bfloat16, device="cuda")    # lda = 12 -> 24 bytes
-    B = torch.ones(12, 16, dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(tgemm.TgemmError) as e:
-        tgemm.gemm_tc(A, B, "bf16")
-    assert e.value.status == 2
+@pytest.mark.parametrize("kind", ["tf32", "bf16"])
+@pytest.mark.parametrize("shape", [(16, 12, 12), (130, 261, 77), (300, 1001, 517)])
+def test_unaligned_leading_dimensions(tgemm, tc_mode, kind, shape):
+    """Packed operands whose rows do not start on 16-byte boundaries: the
+    library repacks them for the tensor-memory copies (bit-exact on integers)."""
+    M, N, K = shape
+    A, B = operands(M, N, K, "int4", kind, seed=M * N + K)
+    C = run_tc(tgemm, A, B, kind)
+    name = tgemm.binding.last_kernel()
+    assert ("repack_a" in name) == ((K * A.element_size()) % 16 != 0)
+    C_ref, _ = oracle.gemm(A, B)
+    assert_bit_exact(C, C_ref, f"{kind} unaligned {shape}")
+
+
+def test_unaligned_operand_offsets(tgemm):
+    """A and B starting 2 and 6 bytes past a 16-byte boundary (bf16)."""
+    M, N, K = 100, 90, 64
+    A, B = operands(M, N, K, "int4", "bf16", seed=9)
+    baseA = torch.zeros(M * K + 1, dtype=torch.bfloat16, device="cuda")
+    baseB = torch.zeros(K * N + 3, dtype=torch.bfloat16, device="cuda")
+    Ad = baseA[1:].view(M, K)
+    Bd = baseB[3:].view(K, N)
+    Ad.copy_(A)
+    Bd.copy_(B)
+    C = run_tc(tgemm, Ad, Bd, "bf16")
+    C_ref, _ = oracle.gemm(A, B)
+    assert_bit_exact(C, C_ref, "bf16 offset operands")
+
+
+def test_workload_ragged_tf32_sampled_rows(tgemm):
+    """The 3000 x 5001 x 1537 packed workload on the tensor path (TF32)."""
+    w = inputs.WORKLOADS["ragged"]
+    A, B = inputs.operands(w)
+    C = run_tc(tgemm, A, B, "tf32").cpu()
+    assert "repack_a" in tgemm.binding.last_kernel()
+    rows = [0, 1, 255, 256, 2999] + torch.randint(0, w.M, (30,),
+                                                  generator=inputs.generator(19)).tolist()
+    rows = sorted(set(rows))
+    C_ref, absAB = oracle.gemm_rows(A, B, rows)
+    assert_within(C[rows], C_ref, absAB, TC_REL, TC_ABS, "ragged tf32")
 
 
 def test_k_zero_writes_zeros(tgemm):

@@ -189,12 +189,10 @@ int gemm_tc(int M, int N, int K, const void* A, long lda, const void* B, long ld
     int st = check_common(M, N, K, A, lda, B, ldb, C, ldc);
     if (st == -1) return TGEMM_OK;
     if (st != TGEMM_OK) return st;
-    if (K > 0) {
-        const long esz = in_type == TGEMM_BF16 ? 2 : 4;
-        if (reinterpret_cast<uintptr_t>(A) % 16 != 0 || reinterpret_cast<uintptr_t>(B) % 16 != 0 ||
-            (lda * esz) % 16 != 0 || (ldb * esz) % 16 != 0)
-            return TGEMM_ERR_ALIGNMENT;
-    }
+    const long esz = in_type == TGEMM_BF16 ? 2 : 4;
+    if (K > 0 && (reinterpret_cast<uintptr_t>(A) % esz != 0 ||
+                  reinterpret_cast<uintptr_t>(B) % esz != 0))
+        return TGEMM_ERR_INVALID_ARG;
 
     DeviceInfo dev;
     st = current_device_info(&dev);
@@ -213,11 +211,20 @@ int gemm_tc(int M, int N, int K, const void* A, long lda, const void* B, long ld
     const tgemm::TcPlan plan = tgemm::tc_plan(M, N, K, in_type, pair, dev.num_sms, true);
 
     // Stream-ordered scratch: B transposed for TF32 (the TF32 kind reads B
-    // only K-major), then the partial tiles of a split last wave.
+    // only K-major); A (and BF16 B) repacked when its rows do not start on
+    // 16-byte boundaries (the tensor-memory copies need that); then the
+    // partial tiles of a split last wave.
     const bool tf32 = in_type == TGEMM_TF32;
     const long ldt = (K + 3) / 4 * 4;
-    const size_t bt_bytes = tf32 ? (((size_t)N * ldt * sizeof(float) + 255) & ~(size_t)255) : 0;
-    const size_t total = bt_bytes + plan.scratch_bytes;
+    const long per16 = 16 / esz;
+    const bool pack_a = reinterpret_cast<uintptr_t>(A) % 16 != 0 || (lda * esz) % 16 != 0;
+    const bool pack_b = !tf32 && (reinterpret_cast<uintptr_t>(B) % 16 != 0 || (ldb * esz) % 16 != 0);
+    const long lda_p = (K + per16 - 1) / per16 * per16;
+    const long ldb_p = (N + per16 - 1) / per16 * per16;
+    const size_t bt_bytes = tf32 ? align256((size_t)N * ldt * sizeof(float)) : 0;
+    const size_t ap_bytes = pack_a ? align256((size_t)M * lda_p * esz) : 0;
+    const size_t bp_bytes = pack_b ? align256((size_t)K * ldb_p * esz) : 0;
+    const size_t total = bt_bytes + ap_bytes + bp_bytes + plan.scratch_bytes;
     void* ws = nullptr;
     if (total > 0) {
         int devno = 0;
@@ -226,12 +233,26 @@ int gemm_tc(int M, int N, int K, const void* A, long lda, const void* B, long ld
         if (pool == nullptr) return TGEMM_ERR_CUDA;
         if (cudaMallocFromPoolAsync(&ws, total, pool, stream) != cudaSuccess) return TGEMM_ERR_CUDA;
     }
-    float* bt = static_cast<float*>(ws);
-    float* partials = plan.scratch_bytes ? reinterpret_cast<float*>(static_cast<char*>(ws) + bt_bytes)
-                                         : nullptr;
+    char* wsb = static_cast<char*>(ws);
+    float* bt = reinterpret_cast<float*>(wsb);
+    char* ap = wsb + bt_bytes;
+    char* bp = ap + ap_bytes;
+    float* partials = plan.scratch_bytes ? reinterpret_cast<float*>(bp + bp_bytes) : nullptr;
     int rc = TGEMM_OK;
     tgemm::GemmArgs a{M, N, K, A, lda, B, ldb, C, ldc};
-    if (tf32) {
+    if (pack_a) {
+        if (tgemm::repack_rows(A, lda, ap, lda_p, M, K, (int)esz, stream) != cudaSuccess)
+            rc = TGEMM_ERR_CUDA;
+        a.A = ap;
+        a.lda = lda_p;
+    }
+    if (pack_b) {
+        if (tgemm::repack_rows(B, ldb, bp, ldb_p, K, N, (int)esz, stream) != cudaSuccess)
+            rc = TGEMM_ERR_CUDA;
+        a.B = bp;
+        a.ldb = ldb_p;
+    }
+    if (tf32 && rc == TGEMM_OK) {
         if (tgemm::transpose_f32(static_cast<const float*>(B), ldb, bt, ldt, K, N, stream) !=
             cudaSuccess)
             rc = TGEMM_ERR_CUDA;
@@ -247,7 +268,8 @@ int gemm_tc(int M, int N, int K, const void* A, long lda, const void* B, long ld
     if (rc == TGEMM_OK) {
         char split[48] = "";
         if (plan.split > 1) snprintf(split, sizeof(split), "+splitk_reduce(split=%d)", plan.split);
-        snprintf(g_last_kernel_buf, sizeof(g_last_kernel_buf), "%s%s%s",
+        snprintf(g_last_kernel_buf, sizeof(g_last_kernel_buf), "%s%s%s%s%s",
+                 pack_a ? "repack_a+" : "", pack_b ? "repack_b+" : "",
                  tf32 ? "transpose_b+" : "", tgemm::tc_kernel_name(in_type, pair), split);
         g_last_kernel = g_last_kernel_buf;
     }

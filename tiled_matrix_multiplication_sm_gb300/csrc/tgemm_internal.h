@@ -77,6 +77,11 @@ void plan_tail_split(int tiles, int slots, int ktiles, double tile_us, double ti
 cudaError_t transpose_f32(const float* B, long ldb, float* Bt, long ldt, int K, int N,
                           cudaStream_t s);
 
+// Copy a rows x cols matrix of `esz`-byte elements (2 or 4) from leading
+// dimension ld_src to ld_dst (in elements).
+cudaError_t repack_rows(const void* src, long ld_src, void* dst, long ld_dst, int rows, int cols,
+                        int esz, cudaStream_t s);
+
 // ---- shared helper (sgemm_f32.cu) -----------------------------------------
 // Write zeros to the M x N block of C (the K == 0 product).
 cudaError_t zero_fill(float* C, long ldc, int M, int N, cudaStream_t s);

@@ -5,8 +5,9 @@
 // zeros), while the library's B is row-major K x N. The TF32 path therefore
 // first writes B transposed (N x K, K contiguous) into scratch memory.
 //
-// This is pure data movement, bound by HBM bandwidth: every element is read
-// once and written once. A 64 x 64 tile goes through shared memory so that
+// Both kernels here are pure data movement, bound by HBM bandwidth. The
+// transpose reads every element once and writes it once
+// (8 K N bytes); a 64 x 64 tile goes through shared memory so that
 // both the reads (along a row of B) and the writes (along a row of Bt) are
 // coalesced; the tile row is padded by one float so that reading it by
 // columns hits 32 different banks -- the padding of "Tiled GEMM: Matrix
@@ -40,7 +41,41 @@ transpose_kernel(const float* __restrict__ B, long ldb, float* __restrict__ Bt, 
     }
 }
 
+// Row-by-row copy of a rows x cols matrix of `esz`-byte elements from
+// leading dimension ld_src to ld_dst (both in elements). Used to give the
+// tensor-memory copies rows that start on 16-byte boundaries.
+template <typename T>
+__global__ void __launch_bounds__(256)
+repack_kernel(const T* __restrict__ src, long ld_src, T* __restrict__ dst, long ld_dst, int rows,
+              int cols) {
+    for (int r = blockIdx.y; r < rows; r += gridDim.y) {
+        const T* s = src + (long)r * ld_src;
+        T* d = dst + (long)r * ld_dst;
+        for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < cols; c += gridDim.x * blockDim.x)
+            d[c] = s[c];
+    }
+}
+
 }  // namespace
+
+cudaError_t repack_rows(const void* src, long ld_src, void* dst, long ld_dst, int rows, int cols,
+                        int esz, cudaStream_t s) {
+    // A 2-D grid: columns across x (coalesced), rows across y.
+    int gx = (cols + 255) / 256;
+    if (gx > 64) gx = 64;
+    if (gx < 1) gx = 1;
+    int gy = rows < 16384 ? rows : 16384;
+    if (gy < 1) gy = 1;
+    const dim3 grid(gx, gy);
+    if (esz == 2)
+        repack_kernel<unsigned short><<<grid, 256, 0, s>>>(
+            static_cast<const unsigned short*>(src), ld_src, static_cast<unsigned short*>(dst),
+            ld_dst, rows, cols);
+    else
+        repack_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(src), ld_src,
+                                                  static_cast<float*>(dst), ld_dst, rows, cols);
+    return cudaGetLastError();
+}
 
 cudaError_t transpose_f32(const float* B, long ldb, float* Bt, long ldt, int K, int N,
                           cudaStream_t s) {
