@@ -84,7 +84,9 @@ struct Sync {
     int abort;
 };
 
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + (int)sizeof(Sync);
+// Epilogue staging: one 32 x 32 FP32 block per epilogue warp.
+constexpr int EPI_STAGE_BYTES = 4 * 32 * 32 * 4;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_STAGE_BYTES + (int)sizeof(Sync);
 
 struct TcParams {
     int M, N, K;
@@ -336,9 +338,16 @@ __device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& mb, i
 // 256 columns from TMEM (address `taddr`) to C, or, for a K-piece, to its
 // partial tile in scratch. Rows past M and columns past N are skipped (the
 // reduction never reads them). All lanes of the warp call this together.
+//
+// With 16-byte rows each thread stores its row as 16-byte vectors. When C's
+// rows are not 16-byte aligned, each 32 x 32 block instead goes through this
+// warp's `stage` (32 x 32 floats, XOR-swizzled so that writing by rows and
+// reading by columns are both free of bank conflicts) and leaves as 32
+// coalesced row segments, instead of 32 x 32 stores scattered over 32 rows.
 __device__ __forceinline__ void store_accumulator(const TcParams& p, const Unit& w, int mb, int nb,
-                                                 int row_in_tile, uint32_t taddr) {
+                                                 int row_in_tile, uint32_t taddr, float* stage) {
     const int row = mb * p.tile_rows + row_in_tile;
+    const int lane = threadIdx.x & 31;
     float* dst;
     bool vec;
     if (w.piece < 0) {
@@ -353,6 +362,20 @@ __device__ __forceinline__ void store_accumulator(const TcParams& p, const Unit&
         if (col0 >= p.N) break;                     // uniform across the warp
         uint32_t r[32];
         tmem_ld32(taddr + (uint32_t)(c * 32), r);
+        if (!vec) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) stage[lane * 32 + (j ^ lane)] = __uint_as_float(r[j]);
+            __syncwarp();
+            const int gcol = col0 + lane;
+            const int row0 = row - lane;                // the warp's first row
+#pragma unroll 4
+            for (int i = 0; i < 32; ++i) {
+                const float v = stage[i * 32 + (lane ^ i)];
+                if (row0 + i < p.M && gcol < p.N) p.C[(long)(row0 + i) * p.ldc + gcol] = v;
+            }
+            __syncwarp();
+            continue;
+        }
         if (row < p.M) {
             float* d = dst + c * 32;
             if (vec && col0 + 31 < p.N) {
@@ -426,7 +449,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
-    Sync* sy = reinterpret_cast<Sync*>(smem + STAGES * STAGE_BYTES);
+    float* epi_stage = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES);
+    Sync* sy = reinterpret_cast<Sync*>(smem + STAGES * STAGE_BYTES + EPI_STAGE_BYTES);
     const uint32_t a_base = smem_u32(smem);
     const uint32_t b_base = a_base + STAGES * A_STAGE_BYTES;
 
@@ -547,7 +571,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             bool ok = mbar_wait(smem_u32(&sy->tmem_full[acc]), aph, &sy->abort, lim, true);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
-            store_accumulator(p, w, mb, nb, q * 32 + lane, tmem_base + lane_off + (uint32_t)(acc * BN));
+            store_accumulator(p, w, mb, nb, q * 32 + lane, tmem_base + lane_off + (uint32_t)(acc * BN),
+                              epi_stage + q * 32 * 32);
             tc_fence_before();
             mbar_arrive(smem_u32(&sy->tmem_empty[acc]));
         }
@@ -586,10 +611,10 @@ constexpr int P_A_STAGE_BYTES = 128 * SW;                  // 16 KB: this CTA's 
 constexpr int P_B_STAGE_BYTES = 16 * 1024;                 // this CTA's 128 columns of B
 constexpr int P_STAGE_BYTES = P_A_STAGE_BYTES + P_B_STAGE_BYTES;
 constexpr int P_BM = 256;                                  // pair tile rows (= MMA M)
-// The 16 KB after the ring are never used by this kernel's layout; they keep
-// every shared-memory address an MMA descriptor can reach (a descriptor
-// walks at most one 256-column B tile past its start) inside the block's
-// allocation.
+// The 16 KB after the ring keep every shared-memory address an MMA
+// descriptor can reach (a descriptor walks at most one 256-column B tile
+// past its start) inside the block's allocation; the epilogue warps use them
+// as their 32 x 32 staging blocks.
 constexpr int P_GUARD_BYTES = 16 * 1024;
 constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + P_GUARD_BYTES + 256;
 
@@ -761,7 +786,8 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
             store_accumulator(p, w, mb, nb, (int)rank * 128 + q * 32 + lane,
-                              tmem_base + lane_off + (uint32_t)(acc * BN));
+                              tmem_base + lane_off + (uint32_t)(acc * BN),
+                              reinterpret_cast<float*>(smem + P_STAGES * P_STAGE_BYTES) + q * 32 * 32);
             tc_fence_before();
             mbar_arrive_cluster(tmem_empty0 + (uint32_t)(acc * sizeof(uint64_t)));
         }
