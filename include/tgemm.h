@@ -64,6 +64,9 @@ extern "C" {
 /* Input element types of gemm_tc. */
 #define TGEMM_TF32  1   /* A and B are float arrays; products use the TF32 tensor-core format */
 #define TGEMM_BF16  2   /* A and B are bfloat16 arrays (uint16 bit patterns) */
+#define TGEMM_TF32X3 3  /* A and B are float arrays; each is split into a high and a low
+                           TF32 part and three tensor-core products (lo*hi + hi*lo + hi*hi)
+                           give FP32-level accuracy */
 
 /*
  * gemm_f32 — exact-FP32 product on the CUDA cores.
@@ -98,6 +101,13 @@ TGEMM_API int gemm_f32(int M, int N, int K,
  *               FP32.
  *   TGEMM_BF16: A and B are bfloat16 arrays; products are exact and are
  *               accumulated in FP32.
+ *   TGEMM_TF32X3: A and B are float arrays. Each element x is split into
+ *               hi = x rounded to TF32 and lo = (x - hi) rounded to TF32
+ *               (stream-ordered scratch: A as hi/lo copies, B transposed as
+ *               hi/lo copies), and every K step accumulates
+ *               lo(A)hi(B) + hi(A)lo(B) + hi(A)hi(B) in FP32; the omitted
+ *               lo(A)lo(B) term is below 2^-22 of each product, so the result
+ *               meets the FP32 path's accuracy at a third of the TF32 rate.
  * C is FP32 (ldc >= N, any alignment). Tiles of A and B are copied by the
  * Tensor Memory Accelerator, which needs rows that start on 16-byte
  * boundaries: an operand whose pointer or leading dimension breaks that

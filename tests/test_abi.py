@@ -73,7 +73,8 @@ def test_f32_invalid_arguments(lib, args):
 
 
 @pytest.mark.parametrize("args,code", [
-    ((4, 4, 4, FAKE, 4, FAKE, 4, FAKE, 4, 3), binding.TGEMM_ERR_INVALID_ARG),     # bad in_type
+    ((4, 4, 4, FAKE, 4, FAKE, 4, FAKE, 4, 4), binding.TGEMM_ERR_INVALID_ARG),     # bad in_type
+    ((4, 4, 4, FAKE, 4, FAKE, 4, FAKE, 4, -1), binding.TGEMM_ERR_INVALID_ARG),
     ((4, 4, 4, FAKE, 4, FAKE, 4, FAKE, 4, 0), binding.TGEMM_ERR_INVALID_ARG),
     ((-1, 4, 4, FAKE, 4, FAKE, 4, FAKE, 4, 2), binding.TGEMM_ERR_INVALID_ARG),
     ((4, 4, 8, FAKE, 4, FAKE, 4, FAKE, 4, 2), binding.TGEMM_ERR_INVALID_ARG),     # lda < K

@@ -207,3 +207,49 @@ def test_matmul_host_round_trip(tgemm, kind):
     assert C.device.type == "cpu"
     C_ref, _ = oracle.gemm(A, B)
     assert_bit_exact(C, C_ref, f"matmul {kind}")
+
+
+# ---------------------------------------------------------------- split TF32 (TGEMM_TF32X3)
+
+@pytest.mark.parametrize("shape", [(1, 8, 8), (130, 261, 77), (300, 520, 200), (513, 1032, 520),
+                                   (256, 512, 4104)])
+def test_tf32x3_meets_fp32_tolerance(tgemm, shape):
+    """Three TF32 products on hi/lo splits reach the FP32 path's bound
+    |C - C_ref| <= 1e-5 absAB + 1e-6."""
+    M, N, K = shape
+    g = inputs.generator(3 * M + N + K)
+    A = inputs.draw(M, K, "normal", g)
+    B = inputs.draw(K, N, "normal", g)
+    C = run_tc(tgemm, A, B, "tf32x3")
+    assert "tf32x3" in tgemm.binding.last_kernel()
+    C_ref, absAB = oracle.gemm(A, B)
+    from tests.parity import F32_ABS, F32_REL
+    assert_within(C, C_ref, absAB, F32_REL, F32_ABS, f"tf32x3 {shape}")
+
+
+def test_tf32x3_integer_bit_exact(tgemm):
+    A, B = operands(333, 517, 300, "int4", "tf32", seed=8)
+    C_ref, _ = oracle.gemm(A, B)
+    assert_bit_exact(run_tc(tgemm, A, B, "tf32x3"), C_ref, "tf32x3 int")
+
+
+def test_tf32x3_much_closer_than_tf32(tgemm):
+    """The split form's worst error relative to absAB is far below plain TF32's."""
+    g = inputs.generator(31337)
+    A = inputs.draw(256, 384, "uniform", g)
+    B = inputs.draw(384, 320, "uniform", g)
+    C_ref, absAB = oracle.gemm(A, B)
+    e1 = (run_tc(tgemm, A, B, "tf32").cpu().double().numpy() - C_ref) / absAB
+    e3 = (run_tc(tgemm, A, B, "tf32x3").cpu().double().numpy() - C_ref) / absAB
+    assert abs(e3).max() < abs(e1).max() / 50
+
+
+def test_workload_n4096_tf32x3_sampled_rows(tgemm):
+    w = inputs.WORKLOADS["n4096"]
+    A, B = inputs.operands(w)
+    C = run_tc(tgemm, A, B, "tf32x3").cpu()
+    rows = [0, 255, 256, 4095] + torch.randint(0, w.M, (20,), generator=inputs.generator(23)).tolist()
+    rows = sorted(set(rows))
+    C_ref, absAB = oracle.gemm_rows(A, B, rows)
+    from tests.parity import F32_ABS, F32_REL
+    assert_within(C[rows], C_ref, absAB, F32_REL, F32_ABS, "n4096 tf32x3")

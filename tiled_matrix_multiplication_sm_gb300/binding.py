@@ -158,13 +158,16 @@ def gemm_f32(A: torch.Tensor, B: torch.Tensor, out: Optional[torch.Tensor] = Non
     return C
 
 
-_TC_TYPES = {"tf32": (TGEMM_TF32, torch.float32), "bf16": (TGEMM_BF16, torch.bfloat16)}
+TGEMM_TF32X3 = 3
+_TC_TYPES = {"tf32": (TGEMM_TF32, torch.float32), "bf16": (TGEMM_BF16, torch.bfloat16),
+             "tf32x3": (TGEMM_TF32X3, torch.float32)}
 
 
 def gemm_tc(A: torch.Tensor, B: torch.Tensor, in_type: str = "bf16",
             out: Optional[torch.Tensor] = None,
             stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
-    """C = A @ B on the tcgen05 tensor-core path; ``in_type`` is "tf32" or "bf16"."""
+    """C = A @ B on the tcgen05 tensor-core path; ``in_type`` is "tf32", "bf16"
+    or "tf32x3" (split TF32, FP32-level accuracy)."""
     code, dtype = _TC_TYPES[in_type]
     lda = _check_matrix(A, "A", dtype)
     ldb = _check_matrix(B, "B", dtype)

@@ -185,7 +185,8 @@ int gemm_f32(int M, int N, int K, const float* A, long lda, const float* B, long
 int gemm_tc(int M, int N, int K, const void* A, long lda, const void* B, long ldb,
             float* C, long ldc, int in_type, cudaStream_t stream) {
     g_last_kernel = "";
-    if (in_type != TGEMM_TF32 && in_type != TGEMM_BF16) return TGEMM_ERR_INVALID_ARG;
+    if (in_type != TGEMM_TF32 && in_type != TGEMM_BF16 && in_type != TGEMM_TF32X3)
+        return TGEMM_ERR_INVALID_ARG;
     int st = check_common(M, N, K, A, lda, B, ldb, C, ldc);
     if (st == -1) return TGEMM_OK;
     if (st != TGEMM_OK) return st;
@@ -214,17 +215,23 @@ int gemm_tc(int M, int N, int K, const void* A, long lda, const void* B, long ld
     // only K-major); A (and BF16 B) repacked when its rows do not start on
     // 16-byte boundaries (the tensor-memory copies need that); then the
     // partial tiles of a split last wave.
+    // TF32X3 splits A into hi/lo copies and writes B transposed in hi/lo
+    // copies, all with 16-byte rows.
     const bool tf32 = in_type == TGEMM_TF32;
+    const bool x3 = in_type == TGEMM_TF32X3;
     const long ldt = (K + 3) / 4 * 4;
     const long per16 = 16 / esz;
-    const bool pack_a = reinterpret_cast<uintptr_t>(A) % 16 != 0 || (lda * esz) % 16 != 0;
-    const bool pack_b = !tf32 && (reinterpret_cast<uintptr_t>(B) % 16 != 0 || (ldb * esz) % 16 != 0);
+    const bool pack_a = !x3 && (reinterpret_cast<uintptr_t>(A) % 16 != 0 || (lda * esz) % 16 != 0);
+    const bool pack_b = !tf32 && !x3 &&
+                        (reinterpret_cast<uintptr_t>(B) % 16 != 0 || (ldb * esz) % 16 != 0);
     const long lda_p = (K + per16 - 1) / per16 * per16;
     const long ldb_p = (N + per16 - 1) / per16 * per16;
-    const size_t bt_bytes = tf32 ? align256((size_t)N * ldt * sizeof(float)) : 0;
-    const size_t ap_bytes = pack_a ? align256((size_t)M * lda_p * esz) : 0;
+    const size_t bt_bytes = (tf32 || x3) ? align256((size_t)N * ldt * sizeof(float)) : 0;
+    const size_t bt2_bytes = x3 ? bt_bytes : 0;
+    const size_t ap_bytes = pack_a ? align256((size_t)M * lda_p * esz)
+                                   : x3 ? 2 * align256((size_t)M * ldt * sizeof(float)) : 0;
     const size_t bp_bytes = pack_b ? align256((size_t)K * ldb_p * esz) : 0;
-    const size_t total = bt_bytes + ap_bytes + bp_bytes + plan.scratch_bytes;
+    const size_t total = bt_bytes + bt2_bytes + ap_bytes + bp_bytes + plan.scratch_bytes;
     void* ws = nullptr;
     if (total > 0) {
         int devno = 0;
@@ -235,7 +242,8 @@ int gemm_tc(int M, int N, int K, const void* A, long lda, const void* B, long ld
     }
     char* wsb = static_cast<char*>(ws);
     float* bt = reinterpret_cast<float*>(wsb);
-    char* ap = wsb + bt_bytes;
+    float* bt2 = reinterpret_cast<float*>(wsb + bt_bytes);
+    char* ap = wsb + bt_bytes + bt2_bytes;
     char* bp = ap + ap_bytes;
     float* partials = plan.scratch_bytes ? reinterpret_cast<float*>(bp + bp_bytes) : nullptr;
     int rc = TGEMM_OK;
@@ -252,6 +260,21 @@ int gemm_tc(int M, int N, int K, const void* A, long lda, const void* B, long ld
         a.B = bp;
         a.ldb = ldb_p;
     }
+    if (x3) {
+        float* a_hi = reinterpret_cast<float*>(ap);
+        float* a_lo = reinterpret_cast<float*>(ap + ap_bytes / 2);
+        if (tgemm::split_rows_tf32(static_cast<const float*>(A), lda, a_hi, a_lo, ldt, M, K,
+                                   stream) != cudaSuccess ||
+            tgemm::transpose_split_tf32(static_cast<const float*>(B), ldb, bt, bt2, ldt, K, N,
+                                        stream) != cudaSuccess)
+            rc = TGEMM_ERR_CUDA;
+        a.A = a_hi;
+        a.A2 = a_lo;
+        a.lda = ldt;
+        a.B = bt;
+        a.B2 = bt2;
+        a.ldb = ldt;
+    }
     if (tf32 && rc == TGEMM_OK) {
         if (tgemm::transpose_f32(static_cast<const float*>(B), ldb, bt, ldt, K, N, stream) !=
             cudaSuccess)
@@ -260,8 +283,8 @@ int gemm_tc(int M, int N, int K, const void* A, long lda, const void* B, long ld
         a.ldb = ldt;
     }
     if (rc == TGEMM_OK &&
-        tgemm::tc_launch(a, in_type, tf32 ? 1 : 0, dev.num_sms, enc, limit, stall, pair, plan,
-                         partials, stream) != cudaSuccess)
+        tgemm::tc_launch(a, in_type, (tf32 || x3) ? 1 : 0, dev.num_sms, enc, limit, stall,
+                         pair || x3, plan, partials, stream) != cudaSuccess)
         rc = TGEMM_ERR_CUDA;
     if (ws != nullptr && cudaFreeAsync(ws, stream) != cudaSuccess && rc == TGEMM_OK)
         rc = TGEMM_ERR_CUDA;
@@ -270,7 +293,8 @@ int gemm_tc(int M, int N, int K, const void* A, long lda, const void* B, long ld
         if (plan.split > 1) snprintf(split, sizeof(split), "+splitk_reduce(split=%d)", plan.split);
         snprintf(g_last_kernel_buf, sizeof(g_last_kernel_buf), "%s%s%s%s%s",
                  pack_a ? "repack_a+" : "", pack_b ? "repack_b+" : "",
-                 tf32 ? "transpose_b+" : "", tgemm::tc_kernel_name(in_type, pair), split);
+                 tf32 ? "transpose_b+" : x3 ? "split_a+transpose_split_b+" : "",
+                 tgemm::tc_kernel_name(in_type, pair), split);
         g_last_kernel = g_last_kernel_buf;
     }
     return rc;

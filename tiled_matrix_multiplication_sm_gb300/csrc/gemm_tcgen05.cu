@@ -606,17 +606,30 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 // Both CTAs allocate and free tensor memory jointly (cta_group::2); cluster
 // barriers after set-up and before the free keep the pair in step.
 
-constexpr int P_STAGES = 6;
-constexpr int P_A_STAGE_BYTES = 128 * SW;                  // 16 KB: this CTA's 128 rows of A
-constexpr int P_B_STAGE_BYTES = 16 * 1024;                 // this CTA's 128 columns of B
-constexpr int P_STAGE_BYTES = P_A_STAGE_BYTES + P_B_STAGE_BYTES;
+constexpr int P_STAGES = 6;                                // ring depth (3 for the split-TF32 form)
+constexpr int P_A_TILE = 128 * SW;                         // 16 KB: this CTA's 128 rows of A
+constexpr int P_B_TILE = 16 * 1024;                        // this CTA's 128 columns of B
 constexpr int P_BM = 256;                                  // pair tile rows (= MMA M)
+
+// Ring geometry. X3 (the three-product split-TF32 form) stages a high and a
+// low copy of each operand per K block.
+template <bool X3>
+struct PairRing {
+    static constexpr int COPIES = X3 ? 2 : 1;
+    static constexpr int STAGES = X3 ? 3 : P_STAGES;
+    static constexpr int A_STAGE = COPIES * P_A_TILE;
+    static constexpr int B_STAGE = COPIES * P_B_TILE;
+    static constexpr int STAGE = A_STAGE + B_STAGE;
+};
 // The 16 KB after the ring keep every shared-memory address an MMA
 // descriptor can reach (a descriptor walks at most one 256-column B tile
 // past its start) inside the block's allocation; the epilogue warps use them
 // as their 32 x 32 staging blocks.
 constexpr int P_GUARD_BYTES = 16 * 1024;
-constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + P_GUARD_BYTES + 256;
+template <bool X3>
+constexpr int pair_smem_bytes() {
+    return 1024 + PairRing<X3>::STAGES * PairRing<X3>::STAGE + P_GUARD_BYTES + 256;
+}
 
 struct PairSync {
     uint64_t full[P_STAGES];
@@ -629,11 +642,20 @@ struct PairSync {
 };
 static_assert(sizeof(PairSync) <= 256, "pair barrier block");
 
-template <int ESZ, bool B_KMAJOR>
+// X3 (TF32 only, B K-major): A and B each arrive as a high and a low TF32
+// part (tmA/tmB and tmA2/tmB2), and every K step issues three MMAs into the
+// same accumulator, lo(A) hi(B) + hi(A) lo(B) + hi(A) hi(B), which carries
+// the product to FP32-level accuracy (the lo x lo term is below FP32's own
+// rounding).
+template <int ESZ, bool B_KMAJOR, bool X3>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmA2,
+                   const __grid_constant__ CUtensorMap tmB2,
                    const TcParams p) {
+    using R = PairRing<X3>;
+    static_assert(!X3 || (ESZ == 4 && B_KMAJOR), "the split form is TF32 with B K-major");
     using KD = Kind<ESZ>;
     constexpr int BK = KD::BK;
     constexpr int K_STEPS = BK / KD::UMMA_K;
@@ -642,16 +664,16 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
     constexpr int B_CHUNK_BYTES = BK * SW;
     constexpr uint32_t A_K_STEP = KD::UMMA_K * ESZ;
     constexpr uint32_t B_K_STEP = KD::UMMA_K * SW;
-    static_assert(B_KMAJOR || B_CHUNKS * B_CHUNK_BYTES == P_B_STAGE_BYTES, "B stage size");
-    static_assert(!B_KMAJOR || 128 * SW == P_B_STAGE_BYTES, "B stage size");
+    static_assert(B_KMAJOR || B_CHUNKS * B_CHUNK_BYTES == P_B_TILE, "B stage size");
+    static_assert(!B_KMAJOR || 128 * SW == P_B_TILE, "B stage size");
     constexpr uint32_t IDESC = instr_desc<ESZ, B_KMAJOR, P_BM>();
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
-    PairSync* sy = reinterpret_cast<PairSync*>(smem + P_STAGES * P_STAGE_BYTES + P_GUARD_BYTES);
+    PairSync* sy = reinterpret_cast<PairSync*>(smem + R::STAGES * R::STAGE + P_GUARD_BYTES);
     const uint32_t a_base = smem_u32(smem);
-    const uint32_t b_base = a_base + P_STAGES * P_A_STAGE_BYTES;
+    const uint32_t b_base = a_base + R::STAGES * R::A_STAGE;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();
@@ -659,13 +681,17 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
     const int pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < P_STAGES; ++s) {
+        for (int s = 0; s < R::STAGES; ++s) {
             mbar_init(smem_u32(&sy->full[s]), 1);
             mbar_init(smem_u32(&sy->empty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&sy->tmem_full[a]), 1);
             mbar_init(smem_u32(&sy->tmem_empty[a]), 256);
+        }
+        if constexpr (X3) {
+            asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmA2)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmB2)) : "memory");
         }
         mbar_init(smem_u32(&sy->drain), 1);
         sy->abort = 0;
@@ -700,15 +726,20 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
                 const int row0 = mb * P_BM + (int)rank * 128;
                 const int col0 = nb * BN + (int)rank * 128;
                 for (int kb = w.kb0; kb < w.kb1; ++kb, ++g) {
-                    const int s = g % P_STAGES;
-                    const uint32_t ph = (uint32_t)(g / P_STAGES) & 1u;
+                    const int s = g % R::STAGES;
+                    const uint32_t ph = (uint32_t)(g / R::STAGES) & 1u;
                     if (!mbar_wait(smem_u32(&sy->empty[s]), ph ^ 1u, &sy->abort, lim, true)) goto pair_producer_done;
                     if (p.debug_stall && g == 0) continue;     // test hook: stage 0 never filled
                     const uint32_t full = full0 + (uint32_t)(s * sizeof(uint64_t));
-                    if (leader) mbar_arrive_expect_tx(smem_u32(&sy->full[s]), 2 * P_STAGE_BYTES);
-                    tma_load_2d_pair(a_base + s * P_A_STAGE_BYTES, &tmA, kb * BK, row0, full);
-                    const uint32_t bdst = b_base + s * P_B_STAGE_BYTES;
-                    if constexpr (B_KMAJOR) {
+                    if (leader) mbar_arrive_expect_tx(smem_u32(&sy->full[s]), 2 * R::STAGE);
+                    const uint32_t adst = a_base + s * R::A_STAGE;
+                    tma_load_2d_pair(adst, &tmA, kb * BK, row0, full);
+                    const uint32_t bdst = b_base + s * R::B_STAGE;
+                    if constexpr (X3) {
+                        tma_load_2d_pair(adst + P_A_TILE, &tmA2, kb * BK, row0, full);
+                        tma_load_2d_pair(bdst, &tmB, kb * BK, col0, full);
+                        tma_load_2d_pair(bdst + P_B_TILE, &tmB2, kb * BK, col0, full);
+                    } else if constexpr (B_KMAJOR) {
                         tma_load_2d_pair(bdst, &tmB, kb * BK, col0, full);
                     } else {
 #pragma unroll
@@ -723,7 +754,7 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
         pair_producer_done:
             if (leader) {
                 // Both CTAs' copies complete on the leader's barriers.
-                for (int s = 0; s < P_STAGES; ++s)
+                for (int s = 0; s < R::STAGES; ++s)
                     if (armed & (1u << s))
                         mbar_wait(smem_u32(&sy->full[s]), (armed_parity >> s) & 1u, &sy->abort, lim, false);
             } else if (*(volatile int*)&sy->abort) {
@@ -748,19 +779,28 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 bool ok = true;
                 for (int kb = w.kb0; kb < w.kb1; ++kb, ++g) {
-                    const int s = g % P_STAGES;
-                    const uint32_t ph = (uint32_t)(g / P_STAGES) & 1u;
+                    const int s = g % R::STAGES;
+                    const uint32_t ph = (uint32_t)(g / R::STAGES) & 1u;
                     if (!mbar_wait(smem_u32(&sy->full[s]), ph, &sy->abort, lim, true)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t a_addr = a_base + s * P_A_STAGE_BYTES;
-                    const uint32_t b_addr = b_base + s * P_B_STAGE_BYTES;
+                    const uint32_t a_addr = a_base + s * R::A_STAGE;
+                    const uint32_t b_addr = b_base + s * R::B_STAGE;
 #pragma unroll
                     for (int kk = 0; kk < K_STEPS; ++kk) {
+                        const uint32_t first = (kb != w.kb0 || kk != 0) ? 1u : 0u;
                         const uint64_t ad = smem_desc(a_addr + kk * A_K_STEP, 16, 1024);
                         const uint64_t bd =
                             B_KMAJOR ? smem_desc(b_addr + kk * A_K_STEP, 16, 1024)
                                      : smem_desc(b_addr + kk * B_K_STEP, B_CHUNK_BYTES, 1024);
-                        tc_mma_pair<ESZ>(d_tmem, ad, bd, IDESC, (kb != w.kb0 || kk != 0) ? 1u : 0u);
+                        if constexpr (X3) {
+                            const uint64_t ad_lo = smem_desc(a_addr + P_A_TILE + kk * A_K_STEP, 16, 1024);
+                            const uint64_t bd_lo = smem_desc(b_addr + P_B_TILE + kk * A_K_STEP, 16, 1024);
+                            tc_mma_pair<ESZ>(d_tmem, ad_lo, bd, IDESC, first);    // lo(A) hi(B)
+                            tc_mma_pair<ESZ>(d_tmem, ad, bd_lo, IDESC, 1u);       // hi(A) lo(B)
+                            tc_mma_pair<ESZ>(d_tmem, ad, bd, IDESC, 1u);          // hi(A) hi(B)
+                        } else {
+                            tc_mma_pair<ESZ>(d_tmem, ad, bd, IDESC, first);
+                        }
                     }
                     tc_commit_pair_multicast(smem_u32(&sy->empty[s]));   // slot free in both CTAs
                 }
@@ -787,7 +827,7 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
             tc_fence_after();
             store_accumulator(p, w, mb, nb, (int)rank * 128 + q * 32 + lane,
                               tmem_base + lane_off + (uint32_t)(acc * BN),
-                              reinterpret_cast<float*>(smem + P_STAGES * P_STAGE_BYTES) + q * 32 * 32);
+                              reinterpret_cast<float*>(smem + R::STAGES * R::STAGE) + q * 32 * 32);
             tc_fence_before();
             mbar_arrive_cluster(tmem_empty0 + (uint32_t)(acc * sizeof(uint64_t)));
         }
@@ -876,27 +916,35 @@ cudaError_t launch_tc(const GemmArgs& a, const TcPlan& pl, float* partials, int 
 
 // The 2-SM kernel: clusters of two CTAs, one CTA per SM, persistent over
 // 256 x 256 tiles.
-template <int ESZ, bool B_KMAJOR>
+template <int ESZ, bool B_KMAJOR, bool X3 = false>
 cudaError_t launch_tc_pair(const GemmArgs& a, const TcPlan& pl, float* partials, int num_sms,
                            EncodeTiledFn enc, unsigned long long wait_limit_ns, int debug_stall,
                            cudaStream_t s) {
     constexpr int BK = Kind<ESZ>::BK;
-    CUtensorMap tmA, tmB;
+    constexpr int SMEM = pair_smem_bytes<X3>();
+    CUtensorMap tmA, tmB, tmA2, tmB2;
     if (!encode_2d(enc, &tmA, a.A, ESZ, a.M, a.K, a.lda, BK, 128)) return cudaErrorInvalidValue;
     const bool okb = B_KMAJOR ? encode_2d(enc, &tmB, a.B, ESZ, a.N, a.K, a.ldb, BK, 128)
                               : encode_2d(enc, &tmB, a.B, ESZ, a.K, a.N, a.ldb, SW / ESZ, BK);
     if (!okb) return cudaErrorInvalidValue;
+    if constexpr (X3) {
+        if (!encode_2d(enc, &tmA2, a.A2, ESZ, a.M, a.K, a.lda, BK, 128) ||
+            !encode_2d(enc, &tmB2, a.B2, ESZ, a.N, a.K, a.ldb, BK, 128))
+            return cudaErrorInvalidValue;
+    } else {
+        tmA2 = tmA;
+        tmB2 = tmB;
+    }
     const TcParams p = make_params(a, pl, partials, wait_limit_ns, debug_stall);
 
-    auto kern = tc_gemm_2sm_kernel<ESZ, B_KMAJOR>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         P_SMEM_BYTES);
+    auto kern = tc_gemm_2sm_kernel<ESZ, B_KMAJOR, X3>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     const int pairs = p.num_units < num_sms / 2 ? p.num_units : num_sms / 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs, 1, 1);
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = P_SMEM_BYTES;
+    cfg.dynamicSmemBytes = SMEM;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -905,21 +953,23 @@ cudaError_t launch_tc_pair(const GemmArgs& a, const TcPlan& pl, float* partials,
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
+    e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmA2, tmB2, p);
     if (e != cudaSuccess) return e;
     e = cudaGetLastError();
     if (e != cudaSuccess || p.split <= 1) return e;
     return launch_reduce(p, s);
 }
 
-const char* kNames[2][2] = {
+const char* kNames[3][2] = {
     {"tc_tf32_128x256x32_s4_persistent", "tc_tf32_2sm_256x256x32_s6_persistent"},
     {"tc_bf16_128x256x64_s4_persistent", "tc_bf16_2sm_256x256x64_s6_persistent"},
+    {"tc_tf32x3_2sm_256x256x32_s3_persistent", "tc_tf32x3_2sm_256x256x32_s3_persistent"},
 };
 
 }  // namespace
 
 TcPlan tc_plan(int M, int N, int K, int in_type, bool pair, int num_sms, bool allow_split) {
+    if (in_type == TC_TF32X3) pair = true;    // the split form exists as a CTA-pair kernel only
     TcPlan pl;
     pl.tile_rows = pair ? P_BM : BM;
     pl.tiles_m = (M + pl.tile_rows - 1) / pl.tile_rows;
@@ -935,6 +985,7 @@ TcPlan tc_plan(int M, int N, int K, int in_type, bool pair, int num_sms, bool al
         // half the BF16 rate.
         double unit_tflops = pair ? 21.7 : 9.3;
         if (in_type != TC_BF16) unit_tflops *= 0.5;
+        if (in_type == TC_TF32X3) unit_tflops /= 3.0;
         const double tile_us = 2.0 * pl.tile_rows * BN * (double)K / (unit_tflops * 1e6);
         plan_tail_split(tiles, pair ? num_sms / 2 : num_sms, pl.kblocks, tile_us,
                         (double)pl.tile_rows * BN * sizeof(float), pl.dp_tiles, pl.split);
@@ -952,7 +1003,7 @@ bool tc_use_pair(int M, int mode) {
 }
 
 const char* tc_kernel_name(int in_type, bool pair) {
-    return kNames[in_type == TC_BF16 ? 1 : 0][pair ? 1 : 0];
+    return kNames[in_type == TC_BF16 ? 1 : in_type == TC_TF32X3 ? 2 : 0][pair ? 1 : 0];
 }
 
 cudaError_t tc_launch(const GemmArgs& a, int in_type, int b_kmajor, int num_sms, void* encode_fn,
@@ -961,6 +1012,8 @@ cudaError_t tc_launch(const GemmArgs& a, int in_type, int b_kmajor, int num_sms,
     auto enc = reinterpret_cast<EncodeTiledFn>(encode_fn);
     const unsigned long long w = wait_limit_ns;
     const int st = debug_stall;
+    if (in_type == TC_TF32X3)       // always the CTA-pair kernel, B K-major
+        return launch_tc_pair<4, true, true>(a, pl, partials, num_sms, enc, w, st, s);
     if (pair) {
         if (in_type == TC_BF16)
             return b_kmajor ? launch_tc_pair<2, true>(a, pl, partials, num_sms, enc, w, st, s)

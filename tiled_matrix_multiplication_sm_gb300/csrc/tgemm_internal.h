@@ -13,6 +13,9 @@ struct GemmArgs {
     const void* A; long lda;
     const void* B; long ldb;
     float* C;      long ldc;
+    // Low parts of A and B for the split-TF32 form (same layouts as A, B).
+    const void* A2 = nullptr;
+    const void* B2 = nullptr;
 };
 
 // ---- FP32 CUDA-core path (sgemm_f32.cu) ---------------------------------
@@ -38,7 +41,7 @@ cudaError_t f32_launch(int id, const GemmArgs& a, const F32Plan& pl, float* scra
                        cudaStream_t s);
 
 // ---- tcgen05 tensor-core path (gemm_tcgen05.cu) -------------------------
-enum TcType { TC_TF32 = 1, TC_BF16 = 2 };
+enum TcType { TC_TF32 = 1, TC_BF16 = 2, TC_TF32X3 = 3 };
 // Whether the 2-SM (CTA-pair) kernel runs: mode -1 = by shape, 0 = never,
 // 1 = always.
 bool tc_use_pair(int M, int mode);
@@ -73,6 +76,13 @@ void plan_tail_split(int tiles, int slots, int ktiles, double tile_us, double ti
                      int& dp_tiles, int& split);
 
 // ---- layout pre-pass (transpose_f32.cu) ---------------------------------
+// Split-TF32 operands: hi = x rounded to TF32 (nearest), lo = (x - hi)
+// rounded to TF32. split_rows writes hi/lo of a rows x cols matrix with
+// leading dimension ld_out; transpose_split writes hi/lo of B transposed.
+cudaError_t split_rows_tf32(const float* X, long ldx, float* hi, float* lo, long ld_out, int rows,
+                            int cols, cudaStream_t s);
+cudaError_t transpose_split_tf32(const float* B, long ldb, float* hi_t, float* lo_t, long ldt,
+                                 int K, int N, cudaStream_t s);
 // Bt[n][k] = B[k][n] for a K x N matrix B (ldb) into Bt (N x K, ldt >= K).
 cudaError_t transpose_f32(const float* B, long ldb, float* Bt, long ldt, int K, int N,
                           cudaStream_t s);

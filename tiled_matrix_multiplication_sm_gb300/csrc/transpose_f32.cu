@@ -16,6 +16,8 @@
 
 #include "tgemm_internal.h"
 
+#include <cstdint>
+
 namespace tgemm {
 namespace {
 
@@ -56,7 +58,81 @@ repack_kernel(const T* __restrict__ src, long ld_src, T* __restrict__ dst, long 
     }
 }
 
+// x rounded to the TF32 format (10 explicit mantissa bits), to nearest with
+// ties away from zero; the low 13 bits of the result are zero.
+__device__ __forceinline__ float tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+// hi = tf32(x), lo = tf32(x - hi). x - hi is exact in FP32: hi is within a
+// factor of two of x, so the difference needs no rounding (Sterbenz).
+__device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
+    hi = tf32_rna(x);
+    lo = tf32_rna(x - hi);
+}
+
+__global__ void __launch_bounds__(256)
+split_rows_kernel(const float* __restrict__ X, long ldx, float* __restrict__ hi,
+                  float* __restrict__ lo, long ld_out, int rows, int cols) {
+    for (int r = blockIdx.y; r < rows; r += gridDim.y) {
+        const float* s = X + (long)r * ldx;
+        for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < cols; c += gridDim.x * blockDim.x) {
+            float h, l;
+            split_tf32(s[c], h, l);
+            hi[(long)r * ld_out + c] = h;
+            lo[(long)r * ld_out + c] = l;
+        }
+    }
+}
+
+// Transpose of B (K x N) into hi/lo parts of Bt (N x K), through a padded
+// shared-memory tile as in transpose_kernel.
+__global__ void __launch_bounds__(TT * TROWS)
+transpose_split_kernel(const float* __restrict__ B, long ldb, float* __restrict__ hi_t,
+                       float* __restrict__ lo_t, long ldt, int K, int N) {
+    __shared__ float tile[TT][TT + 1];
+    const int tx = threadIdx.x % TT, ty = threadIdx.x / TT;
+    const int n0 = blockIdx.x * TT, k0 = blockIdx.y * TT;
+#pragma unroll
+    for (int r = ty; r < TT; r += TROWS) {
+        const int k = k0 + r, n = n0 + tx;
+        tile[r][tx] = (k < K && n < N) ? B[(long)k * ldb + n] : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = ty; r < TT; r += TROWS) {
+        const int n = n0 + r, k = k0 + tx;
+        if (n < N && k < K) {
+            float h, l;
+            split_tf32(tile[tx][r], h, l);
+            hi_t[(long)n * ldt + k] = h;
+            lo_t[(long)n * ldt + k] = l;
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t split_rows_tf32(const float* X, long ldx, float* hi, float* lo, long ld_out, int rows,
+                            int cols, cudaStream_t s) {
+    int gx = (cols + 255) / 256;
+    if (gx > 64) gx = 64;
+    if (gx < 1) gx = 1;
+    int gy = rows < 16384 ? rows : 16384;
+    if (gy < 1) gy = 1;
+    split_rows_kernel<<<dim3(gx, gy), 256, 0, s>>>(X, ldx, hi, lo, ld_out, rows, cols);
+    return cudaGetLastError();
+}
+
+cudaError_t transpose_split_tf32(const float* B, long ldb, float* hi_t, float* lo_t, long ldt,
+                                 int K, int N, cudaStream_t s) {
+    dim3 grid((N + TT - 1) / TT, (K + TT - 1) / TT);
+    if (grid.y > 65535) return cudaErrorInvalidValue;
+    transpose_split_kernel<<<grid, TT * TROWS, 0, s>>>(B, ldb, hi_t, lo_t, ldt, K, N);
+    return cudaGetLastError();
+}
 
 cudaError_t repack_rows(const void* src, long ld_src, void* dst, long ld_dst, int rows, int cols,
                         int esz, cudaStream_t s) {
