@@ -25,7 +25,7 @@ import numpy as np
 
 from . import build as _build
 
-__all__ = ["Oracle", "default", "gemm", "gemm_rows", "set_threads",
+__all__ = ["Oracle", "default", "gemm", "gemm_rows", "gemm_ex", "set_threads",
            "max_threads", "to_float64"]
 
 _c_double_p = ctypes.POINTER(ctypes.c_double)
@@ -83,6 +83,14 @@ class Oracle:
             _c_double_p, ctypes.c_long, _c_double_p, ctypes.c_long,
             _c_long_p, ctypes.c_int,
             _c_double_p, ctypes.c_long, _c_double_p, ctypes.c_long]
+        lib.oracle_gemm_ex.restype = ctypes.c_int
+        lib.oracle_gemm_ex.argtypes = [
+            ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            _c_double_p, ctypes.c_long, ctypes.c_int,
+            _c_double_p, ctypes.c_long, ctypes.c_int,
+            ctypes.c_double, ctypes.c_double,
+            _c_double_p, ctypes.c_long, _c_double_p,
+            _c_double_p, ctypes.c_long, _c_double_p, ctypes.c_long]
         lib.oracle_set_threads.restype = None
         lib.oracle_set_threads.argtypes = [ctypes.c_int]
         lib.oracle_max_threads.restype = ctypes.c_int
@@ -135,6 +143,49 @@ class Oracle:
             raise ValueError("oracle_gemm_rows rejected its arguments")
         return C, absAB
 
+    def gemm_ex(self, A, B, trans_a=False, trans_b=False, alpha=1.0, beta=0.0, C0=None,
+                bias=None) -> Tuple[np.ndarray, np.ndarray]:
+        """alpha * op(A) op(B) + beta * C0 + bias; returns (C, scale).
+
+        ``A`` and ``B`` are the STORED matrices: A is K x M when ``trans_a``
+        (else M x K), B is N x K when ``trans_b`` (else K x N). ``bias`` has
+        one entry per column of C. C0 is not read when ``beta == 0``.
+        """
+        A = to_float64(A)
+        B = to_float64(B)
+        M, K = (A.shape[1], A.shape[0]) if trans_a else A.shape
+        K2, N = (B.shape[1], B.shape[0]) if trans_b else B.shape
+        if K != K2:
+            raise ValueError(f"inner dimensions differ: {A.shape} / {B.shape}")
+        A, lda = _ld(A)
+        B, ldb = _ld(B)
+        if beta != 0.0:
+            if C0 is None:
+                raise ValueError("beta != 0 needs C0")
+            C0 = to_float64(C0)
+            if C0.shape != (M, N):
+                raise ValueError("C0 must be M x N")
+            C0, ldc0 = _ld(C0)
+            c0_p = self._ptr(C0)
+        else:
+            ldc0, c0_p = max(N, 1), ctypes.cast(None, _c_double_p)
+        if bias is not None:
+            bias = np.ascontiguousarray(np.asarray(bias, dtype=np.float64).reshape(-1))
+            if bias.shape[0] != N:
+                raise ValueError("bias must have N entries")
+            bias_p = self._ptr(bias)
+        else:
+            bias_p = ctypes.cast(None, _c_double_p)
+        C = np.empty((M, N), dtype=np.float64)
+        S = np.empty((M, N), dtype=np.float64)
+        rc = self._lib.oracle_gemm_ex(M, N, K, self._ptr(A), lda, int(bool(trans_a)),
+                                      self._ptr(B), ldb, int(bool(trans_b)), float(alpha),
+                                      float(beta), c0_p, ldc0, bias_p, self._ptr(C), max(N, 1),
+                                      self._ptr(S), max(N, 1))
+        if rc != 0:
+            raise ValueError("oracle_gemm_ex rejected its arguments")
+        return C, S
+
     def set_threads(self, n: int) -> None:
         self._lib.oracle_set_threads(int(n))
 
@@ -159,6 +210,10 @@ def gemm(A, B):
 
 def gemm_rows(A, B, rows):
     return default().gemm_rows(A, B, rows)
+
+
+def gemm_ex(A, B, **kw):
+    return default().gemm_ex(A, B, **kw)
 
 
 def set_threads(n: int) -> None:

@@ -111,6 +111,69 @@ int oracle_gemm(int M, int N, int K,
     return 0;
 }
 
+/*
+ * Extended form, for the library's gemm_ex (operands given transposed, and
+ * the scaled-and-shifted output of the usual BLAS convention):
+ *
+ *     C[i][j] = alpha * sum_k opA[i][k] * opB[k][j] + beta * C0[i][j] + bias[j]
+ *
+ * opA[i][k] is A[i][k] (A stored M x K, lda >= K) or, with trans_a, A[k][i]
+ * (A stored K x M, lda >= M; the column-major reading of an M x K matrix,
+ * "Tiled Matrix Multiplication in CUDA", section 2). opB likewise: B[k][j]
+ * (B stored K x N) or, with trans_b, B[j][k] (B stored N x K). The sum is
+ * the definition above, accumulated in double in ascending k; the output
+ * terms are then added in double. C0 is not read when beta == 0 (it may be
+ * NULL); bias may be NULL (no shift).
+ *
+ * scale[i][j] = |alpha| * sum_k |opA[i][k]| |opB[k][j]| + |beta C0[i][j]| + |bias[j]|
+ * is the magnitude the tolerances of this form are stated in.
+ */
+int oracle_gemm_ex(int M, int N, int K,
+                   const double* A, long lda, int trans_a,
+                   const double* B, long ldb, int trans_b,
+                   double alpha, double beta,
+                   const double* C0, long ldc0, const double* bias,
+                   double* C, long ldc, double* scale, long ldscale)
+{
+    if (M < 0 || N < 0 || K < 0) return -1;
+    if (lda < (trans_a ? M : K) || ldb < (trans_b ? K : N)) return -1;
+    if (ldc < N || ldscale < N) return -1;
+    if (beta != 0.0 && (C0 == NULL || ldc0 < N)) return -1;
+
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (long i = 0; i < M; ++i) {
+        double* c_row = C + i * ldc;
+        double* s_row = scale + i * ldscale;
+        for (int j = 0; j < N; ++j) {
+            c_row[j] = 0.0;
+            s_row[j] = 0.0;
+        }
+        for (int k = 0; k < K; ++k) {
+            const double a = trans_a ? A[(long)k * lda + i] : A[i * lda + k];
+            for (int j = 0; j < N; ++j) {
+                const double b = trans_b ? B[(long)j * ldb + k] : B[(long)k * ldb + j];
+                c_row[j] += a * b;
+                s_row[j] += fabs(a) * fabs(b);
+            }
+        }
+        for (int j = 0; j < N; ++j) {
+            double v = alpha * c_row[j];
+            double m = fabs(alpha) * s_row[j];
+            if (beta != 0.0) {
+                v += beta * C0[i * ldc0 + j];
+                m += fabs(beta * C0[i * ldc0 + j]);
+            }
+            if (bias != NULL) {
+                v += bias[j];
+                m += fabs(bias[j]);
+            }
+            c_row[j] = v;
+            s_row[j] = m;
+        }
+    }
+    return 0;
+}
+
 /* Thread control, so that callers can state how many cores a timing used. */
 void oracle_set_threads(int n)
 {

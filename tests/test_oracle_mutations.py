@@ -19,8 +19,10 @@ from tests import test_oracle_pins as pins
 SOURCE = oracle_build.SOURCE
 
 MUTATIONS = {
-    "dropped_last_term": ("for (int k = 0; k < K; ++k)", "for (int k = 0; k < K - 1; ++k)"),
-    "dropped_first_term": ("for (int k = 0; k < K; ++k)", "for (int k = 1; k < K; ++k)"),
+    "dropped_last_term": ("    for (int k = 0; k < K; ++k) {\n        const double a = A[i * lda + k];",
+                          "    for (int k = 0; k < K - 1; ++k) {\n        const double a = A[i * lda + k];"),
+    "dropped_first_term": ("    for (int k = 0; k < K; ++k) {\n        const double a = A[i * lda + k];",
+                           "    for (int k = 1; k < K; ++k) {\n        const double a = A[i * lda + k];"),
     "wrong_sign": ("c_row[j] += a * b_row[j];", "c_row[j] -= a * b_row[j];"),
     "reversed_k_in_A": ("const double a = A[i * lda + k];",
                         "const double a = A[i * lda + (K - 1 - k)];"),
@@ -29,13 +31,28 @@ MUTATIONS = {
                     "const double* b_row = B + (long)k * N;"),
     "lost_abs_in_scale": ("abs_row[j] += abs_a * fabs(b_row[j]);",
                           "abs_row[j] += a * b_row[j];"),
-    "bad_init": ("        c_row[j] = 0.0;\n", "        c_row[j] = (j == 0) ? 1.0 : 0.0;\n"),
+    "bad_init": ("        c_row[j] = 0.0;\n        abs_row[j] = 0.0;",
+                 "        c_row[j] = (j == 0) ? 1.0 : 0.0;\n        abs_row[j] = 0.0;"),
+    # the extended form
+    "ex_trans_a_index": ("trans_a ? A[(long)k * lda + i]", "trans_a ? A[(long)k * lda + (M - 1 - i)]"),
+    "ex_trans_b_index": ("trans_b ? B[(long)j * ldb + k]", "trans_b ? B[(long)(N - 1 - j) * ldb + k]"),
+    "ex_alpha_dropped": ("double v = alpha * c_row[j];", "double v = c_row[j];"),
+    "ex_beta_sign": ("v += beta * C0[i * ldc0 + j];", "v -= beta * C0[i * ldc0 + j];"),
+    "ex_bias_dropped": ("                v += bias[j];\n", "                v += 0.0;\n"),
+    "ex_dropped_last_term": ("        for (int k = 0; k < K; ++k) {\n            const double a = trans_a",
+                             "        for (int k = 0; k < K - 1; ++k) {\n            const double a = trans_a"),
 }
 
 
 def battery(o):
     """The pins, as (name, call) pairs run against oracle handle ``o``."""
+    from tests import test_oracle_ex_pins as ex
     return [
+        ("ex_transposed", lambda: ex.test_transposed_storage_equals_plain_product(o, True, True)),
+        ("ex_alpha", lambda: ex.test_alpha_power_of_two_scales_exactly(o)),
+        ("ex_beta", lambda: ex.test_beta_only_returns_scaled_C0(o)),
+        ("ex_bias", lambda: ex.test_bias_only_broadcasts_over_rows(o)),
+        ("ex_int", lambda: ex.test_integer_full_expression_exact(o)),
         ("worked_block00", lambda: pins.test_worked_example_block00(o)),
         ("worked_phases", lambda: pins.test_worked_example_phases(o)),
         ("identity_right", lambda: pins.test_identity_right(o, 7, 3)),
