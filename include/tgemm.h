@@ -128,10 +128,51 @@ TGEMM_API int gemm_tc(int M, int N, int K,
             int in_type,
             cudaStream_t stream);
 
-/* Paths of gemm_host. */
-#define TGEMM_PATH_F32   0   /* gemm_f32: FP32 on the CUDA cores, A and B float */
-#define TGEMM_PATH_TF32  1   /* gemm_tc TGEMM_TF32: A and B float */
-#define TGEMM_PATH_BF16  2   /* gemm_tc TGEMM_BF16: A and B bfloat16 */
+/* Paths of gemm_ex and gemm_host. */
+#define TGEMM_PATH_F32    0   /* gemm_f32: FP32 on the CUDA cores, A and B float */
+#define TGEMM_PATH_TF32   1   /* gemm_tc TGEMM_TF32: A and B float */
+#define TGEMM_PATH_BF16   2   /* gemm_tc TGEMM_BF16: A and B bfloat16 */
+#define TGEMM_PATH_TF32X3 3   /* gemm_tc TGEMM_TF32X3: A and B float (gemm_ex only) */
+
+/* Storage flags of gemm_ex. */
+#define TGEMM_TRANS_A 1   /* A is stored K x M (lda >= M): op(A) = A^T, i.e. A column-major */
+#define TGEMM_TRANS_B 2   /* B is stored N x K (ldb >= K): op(B) = B^T, i.e. B column-major */
+
+/*
+ * gemm_ex — the product with transposed storage and the usual output rule:
+ *
+ *     C = alpha * op(A) * op(B) + beta * C + bias
+ *
+ * for the M x N block of C, with op(A) M x K and op(B) K x N: op(A) = A
+ * (stored M x K, lda >= K) or, with TGEMM_TRANS_A, A stored K x M
+ * (lda >= M) read transposed -- an M x K matrix kept column-major, the
+ * opposite convention "Tiled Matrix Multiplication in CUDA", section 2 names;
+ * op(B) likewise with TGEMM_TRANS_B (B stored N x K, ldb >= K). `bias` is
+ * NULL or N floats (device memory), added to every row (the per-feature
+ * bias of a feed-forward layer); C is not read when beta == 0, so it may
+ * hold anything then. Each output is computed as
+ *     v = alpha * acc;  if (beta != 0) v = fmaf(beta, C_old, v);  v += bias[j]
+ * in FP32, acc being the path's accumulated product.
+ *
+ * `path` is one of TGEMM_PATH_F32 (gemm_f32's arithmetic), _TF32, _BF16,
+ * _TF32X3 (gemm_tc's), with A and B of that path's element type. Storage the
+ * path's kernels cannot read directly is rewritten first by HBM-bound
+ * kernels into stream-ordered scratch (transposes; the tensor paths read A
+ * K-major and TF32 reads B K-major, so TRANS_B needs no copy there). With
+ * flags 0, alpha 1, beta 0 and no bias it is exactly gemm_f32 / gemm_tc.
+ *
+ * Returns TGEMM_OK, TGEMM_ERR_INVALID_ARG (as gemm_f32 with the ld rules
+ * above, an unknown path or flag, a bias pointer not 4-byte aligned),
+ * TGEMM_ERR_ALIGNMENT (a forced FP32 configuration cannot read the layout),
+ * TGEMM_ERR_UNSUPPORTED or TGEMM_ERR_CUDA.
+ */
+TGEMM_API int gemm_ex(int M, int N, int K,
+                      const void* A, long lda,
+                      const void* B, long ldb,
+                      float* C, long ldc,
+                      int path, int flags,
+                      float alpha, float beta, const float* bias,
+                      cudaStream_t stream);
 
 /*
  * gemm_host — the same product for operands and result in HOST memory.

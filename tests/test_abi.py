@@ -35,7 +35,7 @@ def test_header_declares_the_boundary():
     names = declared_symbols()
     for required in ["gemm_f32", "gemm_tc", "gemm_status_string", "gemm_device_status"]:
         assert required in names
-    assert len(names) == 13
+    assert len(names) == 14
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -86,6 +86,19 @@ def test_f32_invalid_arguments(lib, args):
 ])
 def test_tc_invalid_arguments(lib, args, code):
     assert tg.gemm_tc_raw(*args, 0) == code
+
+
+def test_ex_entry_rejects_bad_arguments(lib):
+    ok = (4, 4, 4, FAKE, 4, FAKE, 4, FAKE, 4)
+    bad = binding.TGEMM_ERR_INVALID_ARG
+    assert lib.gemm_ex(*ok, 4, 0, 1.0, 0.0, None, 0) == bad            # unknown path
+    assert lib.gemm_ex(*ok, 0, 4, 1.0, 0.0, None, 0) == bad            # unknown flag
+    assert lib.gemm_ex(*ok, 0, 0, 1.0, 0.0, FAKE + 2, 0) == bad        # bias not 4-B aligned
+    # trans_a: A stored K x M needs lda >= M
+    assert lib.gemm_ex(6, 4, 4, FAKE, 5, FAKE, 4, FAKE, 4, 0, 1, 1.0, 0.0, None, 0) == bad
+    # trans_b: B stored N x K needs ldb >= K
+    assert lib.gemm_ex(4, 4, 6, FAKE, 6, FAKE, 5, FAKE, 4, 0, 2, 1.0, 0.0, None, 0) == bad
+    assert lib.gemm_ex(0, 4, 4, 0, 4, 0, 4, 0, 4, 0, 3, 2.0, 1.0, None, 0) == binding.TGEMM_OK
 
 
 def test_host_entry_rejects_bad_arguments(lib):

@@ -34,6 +34,10 @@ _SIGNATURES = {
     "gemm_tc": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                _VP, ctypes.c_long, _VP, ctypes.c_long,
                                _VP, ctypes.c_long, ctypes.c_int, _VP]),
+    "gemm_ex": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                               _VP, ctypes.c_long, _VP, ctypes.c_long,
+                               _VP, ctypes.c_long, ctypes.c_int, ctypes.c_int,
+                               ctypes.c_float, ctypes.c_float, _VP, _VP]),
     "gemm_host": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                  _VP, ctypes.c_long, _VP, ctypes.c_long,
                                  _VP, ctypes.c_long, ctypes.c_int, _VP]),
@@ -216,8 +220,48 @@ def last_kernel() -> str:
     return load().gemm_last_kernel().decode()
 
 
-TGEMM_PATH = {"f32": 0, "tf32": 1, "bf16": 2}
-_PATH_DTYPE = {"f32": torch.float32, "tf32": torch.float32, "bf16": torch.bfloat16}
+TGEMM_PATH = {"f32": 0, "tf32": 1, "bf16": 2, "tf32x3": 3}
+TGEMM_TRANS_A = 1
+TGEMM_TRANS_B = 2
+_PATH_DTYPE = {"f32": torch.float32, "tf32": torch.float32, "bf16": torch.bfloat16,
+               "tf32x3": torch.float32}
+
+
+def gemm_ex(A: torch.Tensor, B: torch.Tensor, path: str = "f32", trans_a: bool = False,
+            trans_b: bool = False, alpha: float = 1.0, beta: float = 0.0,
+            bias: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+            stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """C = alpha * op(A) @ op(B) + beta * C + bias through gemm_ex.
+
+    ``A``/``B`` are the stored matrices: A is K x M when ``trans_a`` (else
+    M x K), B is N x K when ``trans_b`` (else K x N). ``bias`` is a CUDA
+    float32 vector of N entries; ``out`` is read when ``beta != 0``.
+    """
+    dtype = _PATH_DTYPE[path]
+    lda = _check_matrix(A, "A", dtype)
+    ldb = _check_matrix(B, "B", dtype)
+    M, K = (A.shape[1], A.shape[0]) if trans_a else (A.shape[0], A.shape[1])
+    K2, N = (B.shape[1], B.shape[0]) if trans_b else (B.shape[0], B.shape[1])
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: {tuple(A.shape)} / {tuple(B.shape)}")
+    if beta != 0.0 and out is None:
+        raise ValueError("beta != 0 needs out (the C that is read)")
+    C = _out(out, M, N, A.device)
+    ldc = _check_matrix(C, "out", torch.float32)
+    bias_ptr = None
+    if bias is not None:
+        if bias.device.type != "cuda" or bias.dtype != torch.float32 or bias.numel() != N:
+            raise ValueError("bias must be a CUDA float32 tensor of N entries")
+        bias = bias.contiguous()
+        bias_ptr = bias.data_ptr()
+    flags = (TGEMM_TRANS_A if trans_a else 0) | (TGEMM_TRANS_B if trans_b else 0)
+    with torch.cuda.device(A.device):
+        st = int(load().gemm_ex(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(),
+                                ldc, TGEMM_PATH[path], flags, float(alpha), float(beta),
+                                bias_ptr, _stream_handle(stream)))
+    if st != TGEMM_OK:
+        raise TgemmError(st, "gemm_ex")
+    return C
 
 
 def _check_host_matrix(x: torch.Tensor, name: str, dtype: torch.dtype) -> int:

@@ -8,6 +8,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstdio>
+#include <cstring>
 #include <mutex>
 
 namespace {
@@ -133,53 +134,275 @@ int check_common(int M, int N, int K, const void* A, long lda, const void* B, lo
 
 }  // namespace
 
+namespace {
+
+// One product request: C = alpha * op(A) op(B) + beta * C + bias, on `path`.
+struct Request {
+    int M, N, K;
+    const void* A;
+    long lda;
+    const void* B;
+    long ldb;
+    float* C;
+    long ldc;
+    int path;            // TGEMM_PATH_*
+    int flags;           // TGEMM_TRANS_A | TGEMM_TRANS_B
+    tgemm::Epilogue ep;
+};
+
+// Scratch carving: consecutive 256-byte-aligned pieces of one pool block.
+struct Carve {
+    size_t used = 0;
+    size_t take(size_t bytes) {
+        const size_t at = used;
+        used += align256(bytes);
+        return at;
+    }
+};
+
+int run_product(const Request& r, cudaStream_t stream) {
+    g_last_kernel = "";
+    const bool ta = (r.flags & TGEMM_TRANS_A) != 0, tb = (r.flags & TGEMM_TRANS_B) != 0;
+    const int M = r.M, N = r.N, K = r.K;
+    if (M < 0 || N < 0 || K < 0) return TGEMM_ERR_INVALID_ARG;
+    if (r.lda < (ta ? M : K) || r.ldb < (tb ? K : N) || r.ldc < N) return TGEMM_ERR_INVALID_ARG;
+    if (r.lda < 0 || r.ldb < 0) return TGEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return TGEMM_OK;
+    if (r.C == nullptr || reinterpret_cast<uintptr_t>(r.C) % 4 != 0) return TGEMM_ERR_INVALID_ARG;
+    if (r.ep.bias != nullptr && reinterpret_cast<uintptr_t>(r.ep.bias) % 4 != 0)
+        return TGEMM_ERR_INVALID_ARG;
+    const int path = r.path;
+    const size_t esz = path == TGEMM_PATH_BF16 ? 2 : 4;
+    if (K > 0) {
+        if (r.A == nullptr || r.B == nullptr) return TGEMM_ERR_INVALID_ARG;
+        if (reinterpret_cast<uintptr_t>(r.A) % esz != 0 || reinterpret_cast<uintptr_t>(r.B) % esz != 0)
+            return TGEMM_ERR_INVALID_ARG;
+    }
+
+    DeviceInfo dev;
+    int st = current_device_info(&dev);
+    if (st != TGEMM_OK) return st;
+
+    if (K == 0) {
+        if (tgemm::empty_product(r.C, r.ldc, M, N, r.ep, stream) != cudaSuccess)
+            return TGEMM_ERR_CUDA;
+        g_last_kernel = "empty_product";
+        return TGEMM_OK;
+    }
+
+    // ---- plan the operand layouts each path reads, and the scratch for them
+    const long per16 = (long)(16 / esz);
+    auto aligned16 = [&](const void* p, long ld) {
+        return reinterpret_cast<uintptr_t>(p) % 16 == 0 && (ld * (long)esz) % 16 == 0;
+    };
+    const long ldk = (K + per16 - 1) / per16 * per16;    // 16-byte rows of length K
+    const long ldn = (N + per16 - 1) / per16 * per16;    // 16-byte rows of length N
+    const bool f32 = path == TGEMM_PATH_F32;
+    const bool tf32 = path == TGEMM_PATH_TF32;
+    const bool x3 = path == TGEMM_PATH_TF32X3;
+    const bool bf16 = path == TGEMM_PATH_BF16;
+    // What has to be produced before the GEMM kernel:
+    //   A: M x K K-major. Transposed storage -> transpose (all paths);
+    //      X3 -> hi/lo split; tensor paths with rows off 16 bytes -> repack.
+    //   B: F32: K x N row-major (transposed storage -> transpose).
+    //      BF16: K x N read MN-major, or N x K K-major when stored
+    //      transposed; rows off 16 bytes -> repack.
+    //      TF32: N x K K-major: transpose unless stored transposed (then
+    //      repack if needed). X3: hi/lo of the N x K form.
+    enum Prep { NONE, TRANSPOSE, REPACK, SPLIT, TRANSPOSE_SPLIT };
+    Prep prep_a = NONE, prep_b = NONE;
+    if (x3) {
+        prep_a = ta ? TRANSPOSE_SPLIT : SPLIT;
+        prep_b = tb ? SPLIT : TRANSPOSE_SPLIT;
+    } else if (f32) {
+        prep_a = ta ? TRANSPOSE : NONE;
+        prep_b = tb ? TRANSPOSE : NONE;
+    } else {
+        prep_a = ta ? TRANSPOSE : (aligned16(r.A, r.lda) ? NONE : REPACK);
+        if (tf32)
+            prep_b = tb ? (aligned16(r.B, r.ldb) ? NONE : REPACK) : TRANSPOSE;
+        else
+            prep_b = aligned16(r.B, r.ldb) ? NONE : REPACK;      // bf16, either storage
+    }
+    const bool b_kmajor = tb || tf32 || x3;   // tensor paths: B read K-major
+    // Layout the GEMM reads: A M x K (ld_a), B K x N or N x K (ld_b).
+    const long ld_a = prep_a == NONE ? r.lda : ldk;
+    const long ld_b = prep_b == NONE ? r.ldb : (f32 ? (tb ? ldn : r.ldb) : (b_kmajor ? ldk : ldn));
+    Carve cv;
+    const size_t a_off = prep_a == NONE ? 0 : cv.take((size_t)M * ldk * esz);
+    const size_t a2_off = x3 ? cv.take((size_t)M * ldk * esz) : 0;
+    // Rows of the B the GEMM reads: K (F32, BF16 MN-major) or N (K-major).
+    const size_t b_rows = (f32 || !b_kmajor) ? (size_t)K : (size_t)N;
+    const size_t b_off = prep_b == NONE ? 0 : cv.take(b_rows * (size_t)ld_b * esz);
+    const size_t b2_off = x3 ? cv.take((size_t)N * ldk * esz) : 0;
+
+    int f32_id = 0;
+    tgemm::F32Plan fplan;
+    tgemm::TcPlan tplan;
+    bool pair = false;
+    tgemm::GemmArgs probe{M, N, K, r.A, ld_a, r.B, ld_b, r.C, r.ldc};
+    if (f32) {
+        // Operands the kernel will read: the caller's, or 16-byte-row scratch.
+        probe.A = prep_a == NONE ? r.A : nullptr;
+        probe.B = prep_b == NONE ? r.B : nullptr;
+        const int forced = g_forced_f32.load();
+        if (forced >= 0) {
+            tgemm::GemmArgs chk = probe;
+            if (chk.A == nullptr) chk.A = reinterpret_cast<const void*>(256);   // scratch: aligned
+            if (chk.B == nullptr) chk.B = reinterpret_cast<const void*>(256);
+            if (!tgemm::f32_kernel_accepts(forced, chk)) return TGEMM_ERR_ALIGNMENT;
+            f32_id = forced;
+        } else {
+            tgemm::GemmArgs chk = probe;
+            if (chk.A == nullptr) chk.A = reinterpret_cast<const void*>(256);
+            if (chk.B == nullptr) chk.B = reinterpret_cast<const void*>(256);
+            f32_id = tgemm::f32_select(chk, dev.num_sms);
+        }
+        fplan = tgemm::f32_plan(f32_id, probe, dev.num_sms);
+    } else {
+        pair = tgemm::tc_use_pair(M, g_tc_mode.load()) || x3;
+        tplan = tgemm::tc_plan(M, N, K, path, pair, dev.num_sms, true);
+    }
+    const size_t part_bytes = f32 ? fplan.scratch_bytes : tplan.scratch_bytes;
+    const size_t p_off = part_bytes ? cv.take(part_bytes) : 0;
+
+    void* enc = nullptr;
+    if (!f32) {
+        enc = encode_fn();
+        if (enc == nullptr) return TGEMM_ERR_CUDA;
+    }
+    void* ws = nullptr;
+    if (cv.used > 0) {
+        int devno = 0;
+        if (cudaGetDevice(&devno) != cudaSuccess) return TGEMM_ERR_CUDA;
+        cudaMemPool_t pool = scratch_pool(devno);
+        if (pool == nullptr) return TGEMM_ERR_CUDA;
+        if (cudaMallocFromPoolAsync(&ws, cv.used, pool, stream) != cudaSuccess)
+            return TGEMM_ERR_CUDA;
+    }
+    char* base = static_cast<char*>(ws);
+
+    // ---- pre-passes
+    int rc = TGEMM_OK;
+    auto ok = [&](cudaError_t e) {
+        if (e != cudaSuccess && rc == TGEMM_OK) rc = TGEMM_ERR_CUDA;
+    };
+    tgemm::GemmArgs a{M, N, K, r.A, ld_a, r.B, ld_b, r.C, r.ldc};
+    a.ep = r.ep;
+    char name_pre[64] = "";
+    auto note = [&](const char* what) {
+        strncat(name_pre, what, sizeof(name_pre) - strlen(name_pre) - 1);
+    };
+    switch (prep_a) {
+        case TRANSPOSE:
+            a.A = base + a_off;
+            ok(bf16 ? tgemm::transpose_u16(r.A, r.lda, base + a_off, ldk, K, M, stream)
+                    : tgemm::transpose_f32(static_cast<const float*>(r.A), r.lda,
+                                           reinterpret_cast<float*>(base + a_off), ldk, K, M,
+                                           stream));
+            note("transpose_a+");
+            break;
+        case REPACK:
+            a.A = base + a_off;
+            ok(tgemm::repack_rows(r.A, r.lda, base + a_off, ldk, M, K, (int)esz, stream));
+            note("repack_a+");
+            break;
+        case SPLIT:
+            a.A = base + a_off;
+            a.A2 = base + a2_off;
+            ok(tgemm::split_rows_tf32(static_cast<const float*>(r.A), r.lda,
+                                      reinterpret_cast<float*>(base + a_off),
+                                      reinterpret_cast<float*>(base + a2_off), ldk, M, K, stream));
+            note("split_a+");
+            break;
+        case TRANSPOSE_SPLIT:
+            a.A = base + a_off;
+            a.A2 = base + a2_off;
+            ok(tgemm::transpose_split_tf32(static_cast<const float*>(r.A), r.lda,
+                                           reinterpret_cast<float*>(base + a_off),
+                                           reinterpret_cast<float*>(base + a2_off), ldk, K, M,
+                                           stream));
+            note("transpose_split_a+");
+            break;
+        default:
+            break;
+    }
+    switch (prep_b) {
+        case TRANSPOSE:
+            a.B = base + b_off;
+            if (f32)     // stored N x K -> K x N
+                ok(tgemm::transpose_f32(static_cast<const float*>(r.B), r.ldb,
+                                        reinterpret_cast<float*>(base + b_off), ldn, N, K, stream));
+            else         // TF32: stored K x N -> N x K
+                ok(tgemm::transpose_f32(static_cast<const float*>(r.B), r.ldb,
+                                        reinterpret_cast<float*>(base + b_off), ldk, K, N, stream));
+            note("transpose_b+");
+            break;
+        case REPACK:
+            a.B = base + b_off;
+            if (b_kmajor)
+                ok(tgemm::repack_rows(r.B, r.ldb, base + b_off, ldk, N, K, (int)esz, stream));
+            else
+                ok(tgemm::repack_rows(r.B, r.ldb, base + b_off, ldn, K, N, (int)esz, stream));
+            note("repack_b+");
+            break;
+        case SPLIT:     // stored N x K
+            a.B = base + b_off;
+            a.B2 = base + b2_off;
+            ok(tgemm::split_rows_tf32(static_cast<const float*>(r.B), r.ldb,
+                                      reinterpret_cast<float*>(base + b_off),
+                                      reinterpret_cast<float*>(base + b2_off), ldk, N, K, stream));
+            note("split_b+");
+            break;
+        case TRANSPOSE_SPLIT:    // stored K x N
+            a.B = base + b_off;
+            a.B2 = base + b2_off;
+            ok(tgemm::transpose_split_tf32(static_cast<const float*>(r.B), r.ldb,
+                                           reinterpret_cast<float*>(base + b_off),
+                                           reinterpret_cast<float*>(base + b2_off), ldk, K, N,
+                                           stream));
+            note("transpose_split_b+");
+            break;
+        default:
+            break;
+    }
+
+    // ---- the product
+    float* partials = part_bytes ? reinterpret_cast<float*>(base + p_off) : nullptr;
+    const char* kname = "";
+    int split = 1;
+    if (rc == TGEMM_OK) {
+        if (f32) {
+            ok(tgemm::f32_launch(f32_id, a, fplan, partials, stream));
+            kname = tgemm::f32_kernel_name(f32_id);
+            split = fplan.split;
+        } else {
+            ok(tgemm::tc_launch(a, path, b_kmajor ? 1 : 0, dev.num_sms, enc,
+                                (unsigned long long)g_wait_limit_ns.load(), g_debug_stall.load(),
+                                pair, tplan, partials, stream));
+            kname = tgemm::tc_kernel_name(path, pair);
+            split = tplan.split;
+        }
+    }
+    if (ws != nullptr && cudaFreeAsync(ws, stream) != cudaSuccess && rc == TGEMM_OK)
+        rc = TGEMM_ERR_CUDA;
+    if (rc == TGEMM_OK) {
+        char tail[48] = "";
+        if (split > 1) snprintf(tail, sizeof(tail), "+splitk_reduce(split=%d)", split);
+        snprintf(g_last_kernel_buf, sizeof(g_last_kernel_buf), "%s%s%s", name_pre, kname, tail);
+        g_last_kernel = g_last_kernel_buf;
+    }
+    return rc;
+}
+
+}  // namespace
+
 extern "C" {
 
 int gemm_f32(int M, int N, int K, const float* A, long lda, const float* B, long ldb,
              float* C, long ldc, cudaStream_t stream) {
-    g_last_kernel = "";
-    int st = check_common(M, N, K, A, lda, B, ldb, C, ldc);
-    if (st == -1) return TGEMM_OK;
-    if (st != TGEMM_OK) return st;
-    if (K > 0 && (reinterpret_cast<uintptr_t>(A) % 4 != 0 ||
-                  reinterpret_cast<uintptr_t>(B) % 4 != 0))
-        return TGEMM_ERR_INVALID_ARG;
-
-    DeviceInfo dev;
-    st = current_device_info(&dev);
-    if (st != TGEMM_OK) return st;
-
-    tgemm::GemmArgs a{M, N, K, A, lda, B, ldb, C, ldc};
-    if (K == 0) {
-        if (tgemm::zero_fill(C, ldc, M, N, stream) != cudaSuccess) return TGEMM_ERR_CUDA;
-        g_last_kernel = "zero_fill";
-        return TGEMM_OK;
-    }
-    int id = g_forced_f32.load();
-    if (id >= 0) {
-        if (!tgemm::f32_kernel_accepts(id, a)) return TGEMM_ERR_ALIGNMENT;
-    } else {
-        id = tgemm::f32_select(a, dev.num_sms);
-    }
-    const tgemm::F32Plan plan = tgemm::f32_plan(id, a, dev.num_sms);
-    if (plan.scratch_bytes == 0) {
-        if (tgemm::f32_launch(id, a, plan, nullptr, stream) != cudaSuccess) return TGEMM_ERR_CUDA;
-        g_last_kernel = f32_launch_name(id, plan);
-        return TGEMM_OK;
-    }
-    // Partial tiles of the split last wave live in stream-ordered scratch.
-    int devno = 0;
-    if (cudaGetDevice(&devno) != cudaSuccess) return TGEMM_ERR_CUDA;
-    cudaMemPool_t pool = scratch_pool(devno);
-    if (pool == nullptr) return TGEMM_ERR_CUDA;
-    void* ws = nullptr;
-    if (cudaMallocFromPoolAsync(&ws, plan.scratch_bytes, pool, stream) != cudaSuccess)
-        return TGEMM_ERR_CUDA;
-    int rc = tgemm::f32_launch(id, a, plan, static_cast<float*>(ws), stream) == cudaSuccess
-                 ? TGEMM_OK : TGEMM_ERR_CUDA;
-    if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == TGEMM_OK) rc = TGEMM_ERR_CUDA;
-    if (rc == TGEMM_OK) g_last_kernel = f32_launch_name(id, plan);
-    return rc;
+    Request r{M, N, K, A, lda, B, ldb, C, ldc, TGEMM_PATH_F32, 0, tgemm::Epilogue()};
+    return run_product(r, stream);
 }
 
 int gemm_tc(int M, int N, int K, const void* A, long lda, const void* B, long ldb,
@@ -187,117 +410,23 @@ int gemm_tc(int M, int N, int K, const void* A, long lda, const void* B, long ld
     g_last_kernel = "";
     if (in_type != TGEMM_TF32 && in_type != TGEMM_BF16 && in_type != TGEMM_TF32X3)
         return TGEMM_ERR_INVALID_ARG;
-    int st = check_common(M, N, K, A, lda, B, ldb, C, ldc);
-    if (st == -1) return TGEMM_OK;
-    if (st != TGEMM_OK) return st;
-    const long esz = in_type == TGEMM_BF16 ? 2 : 4;
-    if (K > 0 && (reinterpret_cast<uintptr_t>(A) % esz != 0 ||
-                  reinterpret_cast<uintptr_t>(B) % esz != 0))
-        return TGEMM_ERR_INVALID_ARG;
+    // The input-type codes are the path codes of the tensor paths.
+    Request r{M, N, K, A, lda, B, ldb, C, ldc, in_type, 0, tgemm::Epilogue()};
+    return run_product(r, stream);
+}
 
-    DeviceInfo dev;
-    st = current_device_info(&dev);
-    if (st != TGEMM_OK) return st;
-
-    if (K == 0) {
-        if (tgemm::zero_fill(C, ldc, M, N, stream) != cudaSuccess) return TGEMM_ERR_CUDA;
-        g_last_kernel = "zero_fill";
-        return TGEMM_OK;
-    }
-    void* enc = encode_fn();
-    if (enc == nullptr) return TGEMM_ERR_CUDA;
-    const unsigned long long limit = (unsigned long long)g_wait_limit_ns.load();
-    const int stall = g_debug_stall.load();
-    const bool pair = tgemm::tc_use_pair(M, g_tc_mode.load());
-    const tgemm::TcPlan plan = tgemm::tc_plan(M, N, K, in_type, pair, dev.num_sms, true);
-
-    // Stream-ordered scratch: B transposed for TF32 (the TF32 kind reads B
-    // only K-major); A (and BF16 B) repacked when its rows do not start on
-    // 16-byte boundaries (the tensor-memory copies need that); then the
-    // partial tiles of a split last wave.
-    // TF32X3 splits A into hi/lo copies and writes B transposed in hi/lo
-    // copies, all with 16-byte rows.
-    const bool tf32 = in_type == TGEMM_TF32;
-    const bool x3 = in_type == TGEMM_TF32X3;
-    const long ldt = (K + 3) / 4 * 4;
-    const long per16 = 16 / esz;
-    const bool pack_a = !x3 && (reinterpret_cast<uintptr_t>(A) % 16 != 0 || (lda * esz) % 16 != 0);
-    const bool pack_b = !tf32 && !x3 &&
-                        (reinterpret_cast<uintptr_t>(B) % 16 != 0 || (ldb * esz) % 16 != 0);
-    const long lda_p = (K + per16 - 1) / per16 * per16;
-    const long ldb_p = (N + per16 - 1) / per16 * per16;
-    const size_t bt_bytes = (tf32 || x3) ? align256((size_t)N * ldt * sizeof(float)) : 0;
-    const size_t bt2_bytes = x3 ? bt_bytes : 0;
-    const size_t ap_bytes = pack_a ? align256((size_t)M * lda_p * esz)
-                                   : x3 ? 2 * align256((size_t)M * ldt * sizeof(float)) : 0;
-    const size_t bp_bytes = pack_b ? align256((size_t)K * ldb_p * esz) : 0;
-    const size_t total = bt_bytes + bt2_bytes + ap_bytes + bp_bytes + plan.scratch_bytes;
-    void* ws = nullptr;
-    if (total > 0) {
-        int devno = 0;
-        if (cudaGetDevice(&devno) != cudaSuccess) return TGEMM_ERR_CUDA;
-        cudaMemPool_t pool = scratch_pool(devno);
-        if (pool == nullptr) return TGEMM_ERR_CUDA;
-        if (cudaMallocFromPoolAsync(&ws, total, pool, stream) != cudaSuccess) return TGEMM_ERR_CUDA;
-    }
-    char* wsb = static_cast<char*>(ws);
-    float* bt = reinterpret_cast<float*>(wsb);
-    float* bt2 = reinterpret_cast<float*>(wsb + bt_bytes);
-    char* ap = wsb + bt_bytes + bt2_bytes;
-    char* bp = ap + ap_bytes;
-    float* partials = plan.scratch_bytes ? reinterpret_cast<float*>(bp + bp_bytes) : nullptr;
-    int rc = TGEMM_OK;
-    tgemm::GemmArgs a{M, N, K, A, lda, B, ldb, C, ldc};
-    if (pack_a) {
-        if (tgemm::repack_rows(A, lda, ap, lda_p, M, K, (int)esz, stream) != cudaSuccess)
-            rc = TGEMM_ERR_CUDA;
-        a.A = ap;
-        a.lda = lda_p;
-    }
-    if (pack_b) {
-        if (tgemm::repack_rows(B, ldb, bp, ldb_p, K, N, (int)esz, stream) != cudaSuccess)
-            rc = TGEMM_ERR_CUDA;
-        a.B = bp;
-        a.ldb = ldb_p;
-    }
-    if (x3) {
-        float* a_hi = reinterpret_cast<float*>(ap);
-        float* a_lo = reinterpret_cast<float*>(ap + ap_bytes / 2);
-        if (tgemm::split_rows_tf32(static_cast<const float*>(A), lda, a_hi, a_lo, ldt, M, K,
-                                   stream) != cudaSuccess ||
-            tgemm::transpose_split_tf32(static_cast<const float*>(B), ldb, bt, bt2, ldt, K, N,
-                                        stream) != cudaSuccess)
-            rc = TGEMM_ERR_CUDA;
-        a.A = a_hi;
-        a.A2 = a_lo;
-        a.lda = ldt;
-        a.B = bt;
-        a.B2 = bt2;
-        a.ldb = ldt;
-    }
-    if (tf32 && rc == TGEMM_OK) {
-        if (tgemm::transpose_f32(static_cast<const float*>(B), ldb, bt, ldt, K, N, stream) !=
-            cudaSuccess)
-            rc = TGEMM_ERR_CUDA;
-        a.B = bt;
-        a.ldb = ldt;
-    }
-    if (rc == TGEMM_OK &&
-        tgemm::tc_launch(a, in_type, (tf32 || x3) ? 1 : 0, dev.num_sms, enc, limit, stall,
-                         pair || x3, plan, partials, stream) != cudaSuccess)
-        rc = TGEMM_ERR_CUDA;
-    if (ws != nullptr && cudaFreeAsync(ws, stream) != cudaSuccess && rc == TGEMM_OK)
-        rc = TGEMM_ERR_CUDA;
-    if (rc == TGEMM_OK) {
-        char split[48] = "";
-        if (plan.split > 1) snprintf(split, sizeof(split), "+splitk_reduce(split=%d)", plan.split);
-        snprintf(g_last_kernel_buf, sizeof(g_last_kernel_buf), "%s%s%s%s%s",
-                 pack_a ? "repack_a+" : "", pack_b ? "repack_b+" : "",
-                 tf32 ? "transpose_b+" : x3 ? "split_a+transpose_split_b+" : "",
-                 tgemm::tc_kernel_name(in_type, pair), split);
-        g_last_kernel = g_last_kernel_buf;
-    }
-    return rc;
+int gemm_ex(int M, int N, int K, const void* A, long lda, const void* B, long ldb, float* C,
+            long ldc, int path, int flags, float alpha, float beta, const float* bias,
+            cudaStream_t stream) {
+    g_last_kernel = "";
+    if (path < TGEMM_PATH_F32 || path > TGEMM_PATH_TF32X3) return TGEMM_ERR_INVALID_ARG;
+    if ((flags & ~(TGEMM_TRANS_A | TGEMM_TRANS_B)) != 0) return TGEMM_ERR_INVALID_ARG;
+    tgemm::Epilogue ep;
+    ep.alpha = alpha;
+    ep.beta = beta;
+    ep.bias = bias;
+    Request r{M, N, K, A, lda, B, ldb, C, ldc, path, flags, ep};
+    return run_product(r, stream);
 }
 
 int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long ldb, float* C,
@@ -427,8 +556,8 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
         float* Cp = Cd + r0 * ldc_d;
         float* part = reinterpret_cast<float*>(base + part_off[i]);
         if (K == 0) {
-            ok(tgemm::zero_fill(Cp, ldc_d, rows, N, stream));
-            name = "zero_fill";
+            ok(tgemm::empty_product(Cp, ldc_d, rows, N, tgemm::Epilogue(), stream));
+            name = "empty_product";
         } else if (tc) {
             const bool tf32 = path == TGEMM_PATH_TF32;
             tgemm::GemmArgs pa{rows, N, K, Ad + r0 * lda_d * esz, lda_d,

@@ -101,7 +101,21 @@ struct TcParams {
     unsigned long long wait_limit_ns;
     int debug_stall;
     int vec_c;
+    // Output rule C = alpha * acc + beta * C_old + bias[col]; ep_simple when
+    // it is the plain product.
+    float alpha, beta;
+    const float* bias;
+    int ep_simple;
 };
+
+// One output under the rule (C_old read only when beta != 0).
+__device__ __forceinline__ float apply_epilogue(float acc, const TcParams& p, const float* c_old,
+                                                int col) {
+    float v = p.alpha * acc;
+    if (p.beta != 0.0f) v = fmaf(p.beta, *c_old, v);
+    if (p.bias != nullptr) v += p.bias[col];
+    return v;
+}
 
 // A unit of persistent work: a whole tile, or K-blocks [kb0, kb1) of a tile
 // whose partial result goes to scratch (piece >= 0).
@@ -349,13 +363,15 @@ __device__ __forceinline__ void store_accumulator(const TcParams& p, const Unit&
     const int row = mb * p.tile_rows + row_in_tile;
     const int lane = threadIdx.x & 31;
     float* dst;
-    bool vec;
+    bool vec, ep;
     if (w.piece < 0) {
         dst = p.C + (long)row * p.ldc + (long)nb * BN;
         vec = p.vec_c != 0;
+        ep = p.ep_simple == 0;                  // a whole tile writes final outputs
     } else {
         dst = p.partials + ((long)w.piece * p.tile_rows + row_in_tile) * BN;
         vec = true;
+        ep = false;                             // partial sums: the reduction applies the rule
     }
     for (int c = 0; c < BN / 32; ++c) {
         const int col0 = nb * BN + c * 32;
@@ -371,13 +387,23 @@ __device__ __forceinline__ void store_accumulator(const TcParams& p, const Unit&
 #pragma unroll 4
             for (int i = 0; i < 32; ++i) {
                 const float v = stage[i * 32 + (lane ^ i)];
-                if (row0 + i < p.M && gcol < p.N) p.C[(long)(row0 + i) * p.ldc + gcol] = v;
+                if (row0 + i < p.M && gcol < p.N) {
+                    float* o = p.C + (long)(row0 + i) * p.ldc + gcol;
+                    *o = ep ? apply_epilogue(v, p, o, gcol) : v;
+                }
             }
             __syncwarp();
             continue;
         }
         if (row < p.M) {
             float* d = dst + c * 32;
+            if (ep) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (col0 + j < p.N)
+                        r[j] = __float_as_uint(apply_epilogue(__uint_as_float(r[j]), p, d + j,
+                                                              col0 + j));
+            }
             if (vec && col0 + 31 < p.N) {
 #pragma unroll
                 for (int j = 0; j < 32; j += 4)
@@ -419,10 +445,13 @@ tc_splitk_reduce(const TcParams p) {
             s.w += v.w;
         }
         float* dst = p.C + (long)grow * p.ldc + gcol;
+        float v[4] = {s.x, s.y, s.z, s.w};
+        if (!p.ep_simple)
+            for (int j = 0; j < 4 && gcol + j < p.N; ++j)
+                v[j] = apply_epilogue(v[j], p, dst + j, gcol + j);
         if (p.vec_c && gcol + 3 < p.N) {
-            *reinterpret_cast<float4*>(dst) = s;
+            *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
         } else {
-            const float v[4] = {s.x, s.y, s.z, s.w};
             for (int j = 0; j < 4 && gcol + j < p.N; ++j) dst[j] = v[j];
         }
     }
@@ -880,6 +909,10 @@ TcParams make_params(const GemmArgs& a, const TcPlan& pl, float* partials,
     p.wait_limit_ns = wait_limit_ns;
     p.debug_stall = debug_stall;
     p.vec_c = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0 && a.ldc % 4 == 0) ? 1 : 0;
+    p.alpha = a.ep.alpha;
+    p.beta = a.ep.beta;
+    p.bias = a.ep.bias;
+    p.ep_simple = a.ep.simple() ? 1 : 0;
     return p;
 }
 

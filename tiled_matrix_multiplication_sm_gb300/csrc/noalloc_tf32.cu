@@ -108,7 +108,8 @@ extern "C" int gemm_tc_tf32_noalloc(int M, int N, int K, const float* A, long ld
     int st = device_setup(&d);
     if (st != TGEMM_OK) return st;
     if (K == 0)
-        return tgemm::zero_fill(C, ldc, M, N, stream) == cudaSuccess ? TGEMM_OK : TGEMM_ERR_CUDA;
+        return tgemm::empty_product(C, ldc, M, N, tgemm::Epilogue(), stream) == cudaSuccess
+                   ? TGEMM_OK : TGEMM_ERR_CUDA;
     void* enc = encoder();
     if (enc == nullptr) return TGEMM_ERR_CUDA;
     if (tgemm::transpose_f32(B, ldb, d.scratch, ldt, K, N, stream) != cudaSuccess)

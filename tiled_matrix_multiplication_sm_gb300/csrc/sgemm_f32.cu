@@ -115,7 +115,21 @@ struct F32Params {
     int split;           // the others in `split` K-pieces each
     float* partials;     // (tiles - dp_tiles) * split partial tiles of BM x BN
     int vec_c;           // C rows may take 16-byte stores
+    // Output rule C = alpha * acc + beta * C_old + bias[col]; ep_simple when
+    // it is the plain product (alpha 1, beta 0, no bias).
+    float alpha, beta;
+    const float* bias;
+    int ep_simple;
 };
+
+// One output under the rule (C_old read only when beta != 0).
+__device__ __forceinline__ float apply_epilogue(float acc, const F32Params& p, const float* c_old,
+                                                int col) {
+    float v = p.alpha * acc;
+    if (p.beta != 0.0f) v = fmaf(p.beta, *c_old, v);
+    if (p.bias != nullptr) v += p.bias[col];
+    return v;
+}
 
 constexpr int GROUP_M = 8;
 
@@ -335,15 +349,24 @@ sgemm_kernel(const F32Params p) {
 #pragma unroll
             for (int g = 0; g < T::NG; ++g) {
                 const int col = n0 + wn0 + g * 32 + tx * 4;
-                const float4 v = make_float4(acc.v[i][2 * g].x, acc.v[i][2 * g].y,
-                                             acc.v[i][2 * g + 1].x, acc.v[i][2 * g + 1].y);
+                float4 v = make_float4(acc.v[i][2 * g].x, acc.v[i][2 * g].y,
+                                       acc.v[i][2 * g + 1].x, acc.v[i][2 * g + 1].y);
                 if (p.vec_c && col + 3 < N) {
+                    if (!p.ep_simple) {
+                        v.x = apply_epilogue(v.x, p, crow + col, col);
+                        v.y = apply_epilogue(v.y, p, crow + col + 1, col + 1);
+                        v.z = apply_epilogue(v.z, p, crow + col + 2, col + 2);
+                        v.w = apply_epilogue(v.w, p, crow + col + 3, col + 3);
+                    }
                     *reinterpret_cast<float4*>(crow + col) = v;
                 } else {
-                    if (col < N) crow[col] = v.x;
-                    if (col + 1 < N) crow[col + 1] = v.y;
-                    if (col + 2 < N) crow[col + 2] = v.z;
-                    if (col + 3 < N) crow[col + 3] = v.w;
+                    const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (col + j < N)
+                            crow[col + j] = p.ep_simple ? e[j]
+                                                        : apply_epilogue(e[j], p, crow + col + j,
+                                                                         col + j);
                 }
             }
         }
@@ -388,21 +411,29 @@ splitk_reduce(const F32Params p) {
             s.w += v.w;
         }
         float* dst = p.C + (long)grow * p.ldc + gcol;
+        float v[4] = {s.x, s.y, s.z, s.w};
+        if (!p.ep_simple)
+            for (int j = 0; j < 4 && gcol + j < p.N; ++j)
+                v[j] = apply_epilogue(v[j], p, dst + j, gcol + j);
         if (p.vec_c && gcol + 3 < p.N) {
-            *reinterpret_cast<float4*>(dst) = s;
+            *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
         } else {
-            const float v[4] = {s.x, s.y, s.z, s.w};
             for (int j = 0; j < 4 && gcol + j < p.N; ++j) dst[j] = v[j];
         }
     }
 }
 
-__global__ void zero_fill_kernel(float* __restrict__ C, long ldc, int M, int N) {
-    const long total = (long)M * N;
-    for (long e = blockIdx.x * (long)blockDim.x + threadIdx.x; e < total;
-         e += (long)gridDim.x * blockDim.x) {
-        const long r = e / N, c = e % N;
-        C[r * ldc + c] = 0.0f;
+// C = beta * C_old + bias[col] (the product of an empty sum is zero).
+__global__ void __launch_bounds__(256)
+empty_product_kernel(float* __restrict__ C, long ldc, int M, int N, float beta,
+                     const float* __restrict__ bias) {
+    for (int r = blockIdx.y; r < M; r += gridDim.y) {
+        float* row = C + (long)r * ldc;
+        for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < N; c += gridDim.x * blockDim.x) {
+            float v = beta != 0.0f ? beta * row[c] : 0.0f;
+            if (bias != nullptr) v += bias[c];
+            row[c] = v;
+        }
     }
 }
 
@@ -558,6 +589,10 @@ cudaError_t f32_launch(int id, const GemmArgs& a, const F32Plan& pl, float* scra
     p.split = pl.split;
     p.partials = scratch;
     p.vec_c = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0 && a.ldc % 4 == 0) ? 1 : 0;
+    p.alpha = a.ep.alpha;
+    p.beta = a.ep.beta;
+    p.bias = a.ep.bias;
+    p.ep_simple = a.ep.simple() ? 1 : 0;
     const int tiles = pl.tiles_m * pl.tiles_n;
     const int blocks = pl.dp_tiles + (tiles - pl.dp_tiles) * (pl.split > 1 ? pl.split : 0);
     cudaError_t err = e.launch(p, blocks, s);
@@ -565,11 +600,12 @@ cudaError_t f32_launch(int id, const GemmArgs& a, const F32Plan& pl, float* scra
     return e.reduce(p, s);
 }
 
-cudaError_t zero_fill(float* C, long ldc, int M, int N, cudaStream_t s) {
-    const long total = (long)M * N;
-    long blocks = (total + 255) / 256;
-    if (blocks > 4096) blocks = 4096;
-    zero_fill_kernel<<<(int)blocks, 256, 0, s>>>(C, ldc, M, N);
+cudaError_t empty_product(float* C, long ldc, int M, int N, const Epilogue& ep, cudaStream_t s) {
+    int gx = (N + 255) / 256;
+    if (gx > 64) gx = 64;
+    if (gx < 1) gx = 1;
+    const int gy = M < 16384 ? (M > 0 ? M : 1) : 16384;
+    empty_product_kernel<<<dim3(gx, gy), 256, 0, s>>>(C, ldc, M, N, ep.beta, ep.bias);
     return cudaGetLastError();
 }
 

@@ -7,6 +7,16 @@
 
 namespace tgemm {
 
+// Output rule of a product: C = alpha * acc + beta * C_old + bias[col]
+// (C_old is not read when beta == 0; bias may be null). The default is the
+// plain product C = acc.
+struct Epilogue {
+    float alpha = 1.0f;
+    float beta = 0.0f;
+    const float* bias = nullptr;
+    bool simple() const { return alpha == 1.0f && beta == 0.0f && bias == nullptr; }
+};
+
 // Arguments of one product, already validated by the API layer.
 struct GemmArgs {
     int M, N, K;
@@ -16,6 +26,7 @@ struct GemmArgs {
     // Low parts of A and B for the split-TF32 form (same layouts as A, B).
     const void* A2 = nullptr;
     const void* B2 = nullptr;
+    Epilogue ep = Epilogue();
 };
 
 // ---- FP32 CUDA-core path (sgemm_f32.cu) ---------------------------------
@@ -86,6 +97,9 @@ cudaError_t transpose_split_tf32(const float* B, long ldb, float* hi_t, float* l
 // Bt[n][k] = B[k][n] for a K x N matrix B (ldb) into Bt (N x K, ldt >= K).
 cudaError_t transpose_f32(const float* B, long ldb, float* Bt, long ldt, int K, int N,
                           cudaStream_t s);
+// The same for 2-byte elements (bf16 bit patterns).
+cudaError_t transpose_u16(const void* B, long ldb, void* Bt, long ldt, int K, int N,
+                          cudaStream_t s);
 
 // Copy a rows x cols matrix of `esz`-byte elements (2 or 4) from leading
 // dimension ld_src to ld_dst (in elements).
@@ -93,7 +107,7 @@ cudaError_t repack_rows(const void* src, long ld_src, void* dst, long ld_dst, in
                         int esz, cudaStream_t s);
 
 // ---- shared helper (sgemm_f32.cu) -----------------------------------------
-// Write zeros to the M x N block of C (the K == 0 product).
-cudaError_t zero_fill(float* C, long ldc, int M, int N, cudaStream_t s);
+// The K == 0 product: C = beta * C_old + bias (zeros for the default rule).
+cudaError_t empty_product(float* C, long ldc, int M, int N, const Epilogue& ep, cudaStream_t s);
 
 }  // namespace tgemm

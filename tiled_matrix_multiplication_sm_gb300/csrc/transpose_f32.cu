@@ -24,16 +24,17 @@ namespace {
 constexpr int TT = 64;          // tile edge
 constexpr int TROWS = 4;        // thread rows: 64 x 4 = 256 threads
 
+template <typename T>
 __global__ void __launch_bounds__(TT * TROWS)
-transpose_kernel(const float* __restrict__ B, long ldb, float* __restrict__ Bt, long ldt,
+transpose_kernel(const T* __restrict__ B, long ldb, T* __restrict__ Bt, long ldt,
                  int K, int N) {
-    __shared__ float tile[TT][TT + 1];
+    __shared__ T tile[TT][TT + 1];
     const int tx = threadIdx.x % TT, ty = threadIdx.x / TT;
     const int n0 = blockIdx.x * TT, k0 = blockIdx.y * TT;
 #pragma unroll
     for (int r = ty; r < TT; r += TROWS) {
         const int k = k0 + r, n = n0 + tx;
-        tile[r][tx] = (k < K && n < N) ? B[(long)k * ldb + n] : 0.0f;
+        tile[r][tx] = (k < K && n < N) ? B[(long)k * ldb + n] : T(0);
     }
     __syncthreads();
 #pragma unroll
@@ -157,7 +158,16 @@ cudaError_t transpose_f32(const float* B, long ldb, float* Bt, long ldt, int K, 
                           cudaStream_t s) {
     dim3 grid((N + TT - 1) / TT, (K + TT - 1) / TT);
     if (grid.y > 65535) return cudaErrorInvalidValue;
-    transpose_kernel<<<grid, TT * TROWS, 0, s>>>(B, ldb, Bt, ldt, K, N);
+    transpose_kernel<float><<<grid, TT * TROWS, 0, s>>>(B, ldb, Bt, ldt, K, N);
+    return cudaGetLastError();
+}
+
+cudaError_t transpose_u16(const void* B, long ldb, void* Bt, long ldt, int K, int N,
+                          cudaStream_t s) {
+    dim3 grid((N + TT - 1) / TT, (K + TT - 1) / TT);
+    if (grid.y > 65535) return cudaErrorInvalidValue;
+    transpose_kernel<unsigned short><<<grid, TT * TROWS, 0, s>>>(
+        static_cast<const unsigned short*>(B), ldb, static_cast<unsigned short*>(Bt), ldt, K, N);
     return cudaGetLastError();
 }
 
