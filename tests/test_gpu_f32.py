@@ -64,11 +64,32 @@ def test_workload_ragged_sampled_rows(tgemm):
     w = inputs.WORKLOADS["ragged"]
     A, B = inputs.operands(w)
     C = run_f32(tgemm, A, B).cpu()
-    assert "a4_b4" in tgemm.binding.last_kernel()
+    # Large and unaligned: both operands are repacked to 16-byte rows first.
+    assert "repack_a+repack_b+" in tgemm.binding.last_kernel()
     rows = sorted(set([0, 1, 127, 128, 2999, 2944, 2943] +
                       torch.randint(0, w.M, (40,), generator=inputs.generator(8)).tolist()))
     C_ref, absAB = oracle.gemm_rows(A, B, rows)
     assert_within(C[rows], C_ref, absAB, F32_REL, F32_ABS, "ragged")
+
+
+def test_repacked_and_four_byte_loaders_agree_with_oracle(tgemm):
+    """The same unaligned operands through the 4-byte loaders (forced kernel)
+    and through the repack + 16-byte loader route."""
+    g = inputs.generator(41)
+    A = inputs.draw(300, 257, "int4", g)        # lda = 257, ldb = 301: rows off 16 bytes
+    B = inputs.draw(257, 301, "int4", g)
+    C_ref, _ = oracle.gemm(A, B)
+    C = run_f32(tgemm, A, B)
+    assert "repack_a+repack_b+" in tgemm.binding.last_kernel()
+    assert_bit_exact(C, C_ref, "repacked")
+    names = tgemm.binding.f32_kernel_names()
+    try:
+        assert tgemm.binding.set_f32_kernel(names.index("f32_128x256x32_s3_ffma2_a4_b4")) == 0
+        C = run_f32(tgemm, A, B)
+        assert "repack" not in tgemm.binding.last_kernel()
+        assert_bit_exact(C, C_ref, "4-byte loaders")
+    finally:
+        tgemm.binding.set_f32_kernel(-1)
 
 
 def test_ragged_reduced_full(tgemm):
