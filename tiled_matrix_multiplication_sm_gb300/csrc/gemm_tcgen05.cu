@@ -42,6 +42,7 @@
 
 #include <cuda.h>
 #include <cstdint>
+#include <cstring>
 
 namespace tgemm {
 
@@ -106,6 +107,7 @@ struct TcParams {
     float alpha, beta;
     const float* bias;
     int ep_simple;
+    int tma_c;           // whole tiles leave through TMA stores (plain rule, 16-byte rows of C)
 };
 
 // One output under the rule (C_old read only when beta != 0).
@@ -204,6 +206,21 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         " [%0], [%1, {%2, %3}], [%4];"
         :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
+}
+
+// TMA store of a box from shared memory (completion tracked by bulk groups).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(src) : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until the shared-memory sources of this thread's bulk stores are read.
+__device__ __forceinline__ void tma_store_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until this thread's bulk stores are complete.
+__device__ __forceinline__ void tma_store_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -359,9 +376,44 @@ __device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& mb, i
 // reading by columns are both free of bank conflicts) and leaves as 32
 // coalesced row segments, instead of 32 x 32 stores scattered over 32 rows.
 __device__ __forceinline__ void store_accumulator(const TcParams& p, const Unit& w, int mb, int nb,
-                                                 int row_in_tile, uint32_t taddr, float* stage) {
+                                                 int row_in_tile, uint32_t taddr, float* stage,
+                                                 const CUtensorMap* tmC) {
     const int row = mb * p.tile_rows + row_in_tile;
     const int lane = threadIdx.x & 31;
+    if (w.piece < 0 && p.tma_c) {
+        // Whole tile, beta = 0: alpha and bias are applied in registers, then
+        // each 32 x 32 block goes to the warp's staging buffer in the
+        // 128-byte-swizzled layout of the C tensor map (row i holds 128 bytes,
+        // 16-byte chunk j at j ^ (i % 8)) and leaves as one TMA store, which
+        // also clips rows and columns past M and N.
+        const uint32_t st_addr = smem_u32(stage);
+        const int row0 = row - lane;
+        if (row0 >= p.M) return;                        // the warp's rows are all past M
+        for (int c = 0; c < BN / 32; ++c) {
+            const int col0 = nb * BN + c * 32;
+            if (col0 >= p.N) break;                     // uniform across the warp
+            uint32_t r[32];
+            tmem_ld32(taddr + (uint32_t)(c * 32), r);
+            if (!p.ep_simple) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (col0 + j < p.N)
+                        r[j] = __float_as_uint(apply_epilogue(__uint_as_float(r[j]), p, nullptr,
+                                                              col0 + j));
+            }
+            if (lane == 0) tma_store_wait_read();      // previous block has left the buffer
+            __syncwarp();
+            float4* srow = reinterpret_cast<float4*>(stage + lane * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                srow[j ^ (lane & 7)] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                   __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) tma_store_2d(tmC, col0, row0, st_addr);
+        }
+        return;
+    }
     float* dst;
     bool vec, ep;
     if (w.piece < 0) {
@@ -463,6 +515,7 @@ template <int ESZ, bool B_KMAJOR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmC,
                const TcParams p) {
     using KD = Kind<ESZ>;
     constexpr int BK = KD::BK;
@@ -601,10 +654,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
             store_accumulator(p, w, mb, nb, q * 32 + lane, tmem_base + lane_off + (uint32_t)(acc * BN),
-                              epi_stage + q * 32 * 32);
+                              epi_stage + q * 32 * 32, &tmC);
             tc_fence_before();
             mbar_arrive(smem_u32(&sy->tmem_empty[acc]));
         }
+        if (lane == 0) tma_store_wait_all();    // C stores done before the block retires
     }
 
     tc_fence_before();
@@ -682,6 +736,7 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmA2,
                    const __grid_constant__ CUtensorMap tmB2,
+                   const __grid_constant__ CUtensorMap tmC,
                    const TcParams p) {
     using R = PairRing<X3>;
     static_assert(!X3 || (ESZ == 4 && B_KMAJOR), "the split form is TF32 with B K-major");
@@ -856,10 +911,12 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
             tc_fence_after();
             store_accumulator(p, w, mb, nb, (int)rank * 128 + q * 32 + lane,
                               tmem_base + lane_off + (uint32_t)(acc * BN),
-                              reinterpret_cast<float*>(smem + R::STAGES * R::STAGE) + q * 32 * 32);
+                              reinterpret_cast<float*>(smem + R::STAGES * R::STAGE) + q * 32 * 32,
+                              &tmC);
             tc_fence_before();
             mbar_arrive_cluster(tmem_empty0 + (uint32_t)(acc * sizeof(uint64_t)));
         }
+        if (lane == 0) tma_store_wait_all();    // C stores done before the block retires
     }
 
     tc_fence_before();
@@ -913,7 +970,18 @@ TcParams make_params(const GemmArgs& a, const TcPlan& pl, float* partials,
     p.beta = a.ep.beta;
     p.bias = a.ep.bias;
     p.ep_simple = a.ep.simple() ? 1 : 0;
+    p.tma_c = 0;
     return p;
+}
+
+// Tensor map over C for the TMA-store epilogue (32 x 32 boxes, 128-byte
+// swizzle). Used when C's base and rows are 16-byte aligned and beta = 0;
+// otherwise the epilogue stores from registers and `map` stays unused.
+void encode_c(EncodeTiledFn enc, CUtensorMap* map, const GemmArgs& a, TcParams& p) {
+    memset(map, 0, sizeof(*map));
+    if (p.vec_c && a.ep.beta == 0.0f && a.M > 0 && a.N > 0 &&
+        encode_2d(enc, map, a.C, 4, a.M, a.N, a.ldc, 32, 32))
+        p.tma_c = 1;
 }
 
 cudaError_t launch_reduce(const TcParams& p, cudaStream_t s) {
@@ -934,14 +1002,16 @@ cudaError_t launch_tc(const GemmArgs& a, const TcPlan& pl, float* partials, int 
     const bool okb = B_KMAJOR ? encode_2d(enc, &tmB, a.B, ESZ, a.N, a.K, a.ldb, BK, BN)
                               : encode_2d(enc, &tmB, a.B, ESZ, a.K, a.N, a.ldb, SW / ESZ, BK);
     if (!okb) return cudaErrorInvalidValue;
-    const TcParams p = make_params(a, pl, partials, wait_limit_ns, debug_stall);
+    TcParams p = make_params(a, pl, partials, wait_limit_ns, debug_stall);
+    CUtensorMap tmC;
+    encode_c(enc, &tmC, a, p);
 
     auto kern = tc_gemm_kernel<ESZ, B_KMAJOR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int grid = p.num_units < num_sms ? p.num_units : num_sms;
-    kern<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tmA, tmB, p);
+    kern<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tmA, tmB, tmC, p);
     e = cudaGetLastError();
     if (e != cudaSuccess || p.split <= 1) return e;
     return launch_reduce(p, s);
@@ -968,7 +1038,9 @@ cudaError_t launch_tc_pair(const GemmArgs& a, const TcPlan& pl, float* partials,
         tmA2 = tmA;
         tmB2 = tmB;
     }
-    const TcParams p = make_params(a, pl, partials, wait_limit_ns, debug_stall);
+    TcParams p = make_params(a, pl, partials, wait_limit_ns, debug_stall);
+    CUtensorMap tmC;
+    encode_c(enc, &tmC, a, p);
 
     auto kern = tc_gemm_2sm_kernel<ESZ, B_KMAJOR, X3>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
@@ -986,7 +1058,7 @@ cudaError_t launch_tc_pair(const GemmArgs& a, const TcPlan& pl, float* partials,
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmA2, tmB2, p);
+    e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmA2, tmB2, tmC, p);
     if (e != cudaSuccess) return e;
     e = cudaGetLastError();
     if (e != cudaSuccess || p.split <= 1) return e;
