@@ -247,10 +247,12 @@ TGEMM_API int gemm_set_f32_kernel(int id);
 
 /*
  * gemm_set_tc_kernel — choose the tensor-core kernel (for tests and tuning):
- * -1 (default) picks by shape (the 2-SM kernel, a CTA pair computing
- * 256 x 256 tiles, when M > 128; otherwise the one-SM kernel with 128 x 256
- * tiles), 0 forces the one-SM kernel, 1 the 2-SM kernel. Process-wide.
- * Returns TGEMM_OK or TGEMM_ERR_INVALID_ARG.
+ * 0 forces the one-SM kernel (128 x 256 tiles), 1 the 2-SM kernel (a CTA
+ * pair computing 256 x 256 tiles), 2 the 2-SM kernel with 256 x 512 tiles;
+ * -1 (default) picks by shape: the one-SM kernel when M <= 128, 256 x 512
+ * tiles when N > 256 and there are at least as many of them as SM pairs,
+ * else 256 x 256. TGEMM_TF32X3 always runs 256 x 256 pair tiles.
+ * Process-wide. Returns TGEMM_OK or TGEMM_ERR_INVALID_ARG.
  */
 TGEMM_API int gemm_set_tc_kernel(int mode);
 

@@ -3,7 +3,8 @@
 Random M, N, K (with the edge values 1 and tile boundaries mixed in), random
 storage (row- or column-major A and B, optional NaN-filled padding of the
 leading dimension), random small-integer alpha, beta and bias, on every
-path. The data are small integers, so every product, partial sum and output
+path, with the tensor-core tile shape (one SM, SM pair, wide SM pair) drawn
+too. The data are small integers, so every product, partial sum and output
 rule step is exact: each case must equal the oracle bit for bit.
 """
 import random
@@ -58,11 +59,16 @@ def test_fuzz_case(tgemm, seed):
     Ad = device_view(As, rng.random() < 0.3, rng)
     Bd = device_view(Bs, rng.random() < 0.3, rng)
     C = C0.clone().cuda()
-    tgemm.binding.gemm_ex(Ad, Bd, path, trans_a=ta, trans_b=tb, alpha=alpha, beta=beta,
-                          bias=None if bias is None else bias.cuda(), out=C)
+    mode = rng.choice([-1, 0, 1, 2])
+    assert tgemm.binding.set_tc_kernel(mode) == 0
+    try:
+        tgemm.binding.gemm_ex(Ad, Bd, path, trans_a=ta, trans_b=tb, alpha=alpha, beta=beta,
+                              bias=None if bias is None else bias.cuda(), out=C)
+    finally:
+        tgemm.binding.set_tc_kernel(-1)
     assert tgemm.device_status() == 0
     ref, _ = oracle.gemm_ex(As, Bs, trans_a=ta, trans_b=tb, alpha=alpha, beta=beta, C0=C0,
                             bias=bias)
     assert_bit_exact(C, ref, f"seed {seed}: {path} {M}x{N}x{K} ta={ta} tb={tb} "
-                             f"alpha={alpha} beta={beta} bias={use_bias} "
+                             f"alpha={alpha} beta={beta} bias={use_bias} tc_mode={mode} "
                              f"kernel={tgemm.binding.last_kernel()}")

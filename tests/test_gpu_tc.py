@@ -78,9 +78,10 @@ def test_integer_bit_exact(tgemm, kind, shape):
     assert_bit_exact(run_tc(tgemm, A, B, kind), C_ref, f"{kind} {shape}")
 
 
-@pytest.fixture(params=[0, 1], ids=["one_sm", "sm_pair"])
+@pytest.fixture(params=[0, 1, 2], ids=["one_sm", "sm_pair", "sm_pair_wide"])
 def tc_mode(request, tgemm):
-    """Force the one-SM kernel (0) or the 2-SM CTA-pair kernel (1)."""
+    """Force the one-SM kernel (0), the 2-SM CTA-pair kernel with 256 x 256
+    tiles (1) or with 256 x 512 tiles (2)."""
     assert tgemm.binding.set_tc_kernel(request.param) == 0
     yield request.param
     tgemm.binding.set_tc_kernel(-1)
@@ -94,7 +95,9 @@ def test_both_kernels_integer_bit_exact(tgemm, tc_mode, kind, shape):
     A, B = operands(M, N, K, "int4", kind, seed=11 * M + N + K)
     C_ref, _ = oracle.gemm(A, B)
     C = run_tc(tgemm, A, B, kind)
-    assert ("2sm" in tgemm.binding.last_kernel()) == (tc_mode == 1)
+    name = tgemm.binding.last_kernel()
+    assert ("2sm" in name) == (tc_mode >= 1)
+    assert ("256x512" in name) == (tc_mode == 2)
     assert_bit_exact(C, C_ref, f"{kind} {shape} mode {tc_mode}")
 
 

@@ -18,7 +18,7 @@ from tiled_matrix_multiplication_sm_gb300 import inputs
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("mode", [0, 1], ids=["one_sm", "sm_pair"])
+@pytest.mark.parametrize("mode", [0, 1, 2], ids=["one_sm", "sm_pair", "sm_pair_wide"])
 def test_stalled_pipeline_reports_timeout_and_recovers(tgemm, mode):
     b = tgemm.binding
     assert b.set_tc_kernel(mode) == 0

@@ -207,7 +207,8 @@ def set_f32_kernel(kernel_id: int) -> int:
 
 
 def set_tc_kernel(mode: int) -> int:
-    """-1: by shape; 0: one-SM tcgen05 kernel; 1: 2-SM (CTA pair) kernel."""
+    """-1: by shape; 0: one-SM tcgen05 kernel (128 x 256 tiles); 1: 2-SM
+    (CTA pair) kernel, 256 x 256 tiles; 2: 2-SM kernel, 256 x 512 tiles."""
     return int(load().gemm_set_tc_kernel(int(mode)))
 
 

@@ -245,7 +245,7 @@ int run_product(const Request& r, cudaStream_t stream) {
     int f32_id = 0;
     tgemm::F32Plan fplan;
     tgemm::TcPlan tplan;
-    bool pair = false;
+    int shape = tgemm::TC_ONE_SM;
     tgemm::GemmArgs probe{M, N, K, r.A, ld_a, r.B, ld_b, r.C, r.ldc};
     if (f32) {
         // Operands the kernel will read: the caller's, or 16-byte-row scratch.
@@ -266,8 +266,8 @@ int run_product(const Request& r, cudaStream_t stream) {
         }
         fplan = tgemm::f32_plan(f32_id, probe, dev.num_sms);
     } else {
-        pair = tgemm::tc_use_pair(M, g_tc_mode.load()) || x3;
-        tplan = tgemm::tc_plan(M, N, K, path, pair, dev.num_sms, true);
+        shape = tgemm::tc_shape(M, N, K, path, g_tc_mode.load(), dev.num_sms, true);
+        tplan = tgemm::tc_plan(M, N, K, path, shape, dev.num_sms, true);
     }
     const size_t part_bytes = f32 ? fplan.scratch_bytes : tplan.scratch_bytes;
     const size_t p_off = part_bytes ? cv.take(part_bytes) : 0;
@@ -385,8 +385,8 @@ int run_product(const Request& r, cudaStream_t stream) {
         } else {
             ok(tgemm::tc_launch(a, path, b_kmajor ? 1 : 0, dev.num_sms, enc,
                                 (unsigned long long)g_wait_limit_ns.load(), g_debug_stall.load(),
-                                pair, tplan, partials, stream));
-            kname = tgemm::tc_kernel_name(path, pair);
+                                shape, tplan, partials, stream));
+            kname = tgemm::tc_kernel_name(path, shape);
             split = tplan.split;
         }
     }
@@ -486,7 +486,7 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
     int f32_id[4] = {0, 0, 0, 0};
     tgemm::F32Plan f32_plan[4];
     tgemm::TcPlan tc_plan[4];
-    bool pair[4] = {false, false, false, false};
+    int shape[4] = {0, 0, 0, 0};
     size_t part_off[4];
     size_t total = off_p;
     for (int i = 0; i < panels; ++i) {
@@ -494,8 +494,8 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
         part_off[i] = total;
         if (K == 0) continue;
         if (tc) {
-            pair[i] = tgemm::tc_use_pair(rows, g_tc_mode.load());
-            tc_plan[i] = tgemm::tc_plan(rows, N, K, in_type, pair[i], dev.num_sms, true);
+            shape[i] = tgemm::tc_shape(rows, N, K, in_type, g_tc_mode.load(), dev.num_sms, true);
+            tc_plan[i] = tgemm::tc_plan(rows, N, K, in_type, shape[i], dev.num_sms, true);
             total += align256(tc_plan[i].scratch_bytes);
         } else {
             // Device operands are 16-byte aligned: the vector loaders apply.
@@ -569,9 +569,9 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
             tgemm::GemmArgs pa{rows, N, K, Ad + r0 * lda_d * esz, lda_d,
                                tf32 ? static_cast<const void*>(Bt) : Bd, tf32 ? ldt : ldb_d, Cp,
                                ldc_d};
-            ok(tgemm::tc_launch(pa, in_type, tf32 ? 1 : 0, dev.num_sms, enc, limit, stall, pair[i],
+            ok(tgemm::tc_launch(pa, in_type, tf32 ? 1 : 0, dev.num_sms, enc, limit, stall, shape[i],
                                 tc_plan[i], part, stream));
-            name = tgemm::tc_kernel_name(in_type, pair[i]);
+            name = tgemm::tc_kernel_name(in_type, shape[i]);
         } else {
             tgemm::GemmArgs pa{rows, N, K, Ad + r0 * lda_d * esz, lda_d, Bd, ldb_d, Cp, ldc_d};
             ok(tgemm::f32_launch(f32_id[i], pa, f32_plan[i], part, stream));
@@ -641,7 +641,7 @@ int gemm_set_f32_kernel(int id) {
 }
 
 int gemm_set_tc_kernel(int mode) {
-    if (mode < -1 || mode > 1) return TGEMM_ERR_INVALID_ARG;
+    if (mode < -1 || mode > 2) return TGEMM_ERR_INVALID_ARG;
     g_tc_mode.store(mode);
     return TGEMM_OK;
 }

@@ -85,9 +85,12 @@ struct Sync {
     int abort;
 };
 
-// Epilogue staging: one 32 x 32 FP32 block per epilogue warp.
-constexpr int EPI_STAGE_BYTES = 4 * 32 * 32 * 4;
+// Epilogue staging: EPI_BUFS 32 x 32 FP32 blocks per epilogue warp.
+constexpr int EPI_BUFS = 1;
+constexpr int EPI_WARP_BYTES = EPI_BUFS * 32 * 32 * 4;
+constexpr int EPI_STAGE_BYTES = 4 * EPI_WARP_BYTES;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_STAGE_BYTES + (int)sizeof(Sync);
+static_assert(SMEM_BYTES <= 227 * 1024, "one-SM kernel exceeds the shared memory of a block");
 
 struct TcParams {
     int M, N, K;
@@ -95,10 +98,11 @@ struct TcParams {
     long ldc;
     int tiles_m, tiles_n, num_tiles, kblocks;
     int tile_rows;       // rows of a tile: 128 (one SM) or 256 (SM pair)
+    int tile_cols;       // columns of a tile: 256, or 512 (wide SM-pair tiles)
     int dp_tiles;        // tiles [0, dp_tiles) are computed whole
     int split;           // the others in `split` K-pieces each (1: none)
     int num_units;       // dp_tiles + (num_tiles - dp_tiles) * split
-    float* partials;     // one tile_rows x BN partial tile per K-piece
+    float* partials;     // one tile_rows x tile_cols partial tile per K-piece
     unsigned long long wait_limit_ns;
     int debug_stall;
     int vec_c;
@@ -214,9 +218,11 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int 
                  :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(src) : "memory");
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-// Wait until the shared-memory sources of this thread's bulk stores are read.
+// Wait until the shared-memory sources of all but the newest `N` of this
+// thread's bulk store groups are read.
+template <int N>
 __device__ __forceinline__ void tma_store_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group.read %0;" :: "n"(N) : "memory");
 }
 // Wait until this thread's bulk stores are complete.
 __device__ __forceinline__ void tma_store_wait_all() {
@@ -316,8 +322,9 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
     }
 }
 
-// 32 consecutive accumulator columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+// Start loading 32 consecutive accumulator columns of this thread's TMEM
+// lane; the registers hold them after tmem_wait_ld.
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
@@ -329,7 +336,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
           "=r"(r[31])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Wait for this thread's TMEM loads. `r` is tied to the wait, so no use of
+// the loaded registers can be scheduled above it.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :: "memory");
+}
+
+// 32 consecutive accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    tmem_ld32_async(taddr, r);
+    tmem_wait_ld(r);
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start
@@ -366,9 +386,10 @@ __device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& mb, i
 }
 
 // Epilogue of one unit for this thread's accumulator row `row_in_tile`:
-// 256 columns from TMEM (address `taddr`) to C, or, for a K-piece, to its
-// partial tile in scratch. Rows past M and columns past N are skipped (the
-// reduction never reads them). All lanes of the warp call this together.
+// the 32-column blocks [c_begin, c_end) of the tile from TMEM (the tile's
+// column 0 at address `taddr`) to C, or, for a K-piece, to its partial tile
+// in scratch. Rows past M and columns past N are skipped (the reduction never
+// reads them). All lanes of the warp call this together.
 //
 // With 16-byte rows each thread stores its row as 16-byte vectors. When C's
 // rows are not 16-byte aligned, each 32 x 32 block instead goes through this
@@ -377,23 +398,28 @@ __device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& mb, i
 // coalesced row segments, instead of 32 x 32 stores scattered over 32 rows.
 __device__ __forceinline__ void store_accumulator(const TcParams& p, const Unit& w, int mb, int nb,
                                                  int row_in_tile, uint32_t taddr, float* stage,
-                                                 const CUtensorMap* tmC) {
+                                                 const CUtensorMap* tmC, int c_begin, int c_end) {
     const int row = mb * p.tile_rows + row_in_tile;
     const int lane = threadIdx.x & 31;
     if (w.piece < 0 && p.tma_c) {
         // Whole tile, beta = 0: alpha and bias are applied in registers, then
-        // each 32 x 32 block goes to the warp's staging buffer in the
-        // 128-byte-swizzled layout of the C tensor map (row i holds 128 bytes,
-        // 16-byte chunk j at j ^ (i % 8)) and leaves as one TMA store, which
-        // also clips rows and columns past M and N.
-        const uint32_t st_addr = smem_u32(stage);
+        // each 32 x 32 block goes to one of the warp's two staging buffers in
+        // the 128-byte-swizzled layout of the C tensor map (row i holds 128
+        // bytes, 16-byte chunk j at j ^ (i % 8)) and leaves as one TMA store,
+        // which also clips rows and columns past M and N. The next block's
+        // TMEM load is in flight while a block is staged, and a buffer is
+        // reused once the store issued two blocks earlier has read it.
         const int row0 = row - lane;
         if (row0 >= p.M) return;                        // the warp's rows are all past M
-        for (int c = 0; c < BN / 32; ++c) {
-            const int col0 = nb * BN + c * 32;
-            if (col0 >= p.N) break;                     // uniform across the warp
-            uint32_t r[32];
-            tmem_ld32(taddr + (uint32_t)(c * 32), r);
+        const int n_blocks = (p.N - nb * p.tile_cols + 31) / 32;   // blocks with columns < N
+        const int c_stop = c_end < n_blocks ? c_end : n_blocks;
+        if (c_begin >= c_stop) return;
+        uint32_t r[32], nx[32];
+        tmem_ld32(taddr + (uint32_t)(c_begin * 32), r);
+        for (int c = c_begin; c < c_stop; ++c) {
+            const int col0 = nb * p.tile_cols + c * 32;
+            const bool more = c + 1 < c_stop;
+            if (more) tmem_ld32_async(taddr + (uint32_t)((c + 1) * 32), nx);
             if (!p.ep_simple) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
@@ -401,32 +427,38 @@ __device__ __forceinline__ void store_accumulator(const TcParams& p, const Unit&
                         r[j] = __float_as_uint(apply_epilogue(__uint_as_float(r[j]), p, nullptr,
                                                               col0 + j));
             }
-            if (lane == 0) tma_store_wait_read();      // previous block has left the buffer
+            float* buf = stage + ((c - c_begin) % EPI_BUFS) * (32 * 32);
+            if (lane == 0) tma_store_wait_read<EPI_BUFS - 1>();   // buf's previous store has read it
             __syncwarp();
-            float4* srow = reinterpret_cast<float4*>(stage + lane * 32);
+            float4* srow = reinterpret_cast<float4*>(buf + lane * 32);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
                 srow[j ^ (lane & 7)] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
                                                    __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
-            if (lane == 0) tma_store_2d(tmC, col0, row0, st_addr);
+            if (lane == 0) tma_store_2d(tmC, col0, row0, smem_u32(buf));
+            if (more) {
+                tmem_wait_ld(nx);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) r[j] = nx[j];
+            }
         }
         return;
     }
     float* dst;
     bool vec, ep;
     if (w.piece < 0) {
-        dst = p.C + (long)row * p.ldc + (long)nb * BN;
+        dst = p.C + (long)row * p.ldc + (long)nb * p.tile_cols;
         vec = p.vec_c != 0;
         ep = p.ep_simple == 0;                  // a whole tile writes final outputs
     } else {
-        dst = p.partials + ((long)w.piece * p.tile_rows + row_in_tile) * BN;
+        dst = p.partials + ((long)w.piece * p.tile_rows + row_in_tile) * p.tile_cols;
         vec = true;
         ep = false;                             // partial sums: the reduction applies the rule
     }
-    for (int c = 0; c < BN / 32; ++c) {
-        const int col0 = nb * BN + c * 32;
+    for (int c = c_begin; c < c_end; ++c) {
+        const int col0 = nb * p.tile_cols + c * 32;
         if (col0 >= p.N) break;                     // uniform across the warp
         uint32_t r[32];
         tmem_ld32(taddr + (uint32_t)(c * 32), r);
@@ -474,10 +506,10 @@ __device__ __forceinline__ void store_accumulator(const TcParams& p, const Unit&
 // Sum the K-pieces of every split tile, piece 0 first, into C.
 __global__ void __launch_bounds__(256)
 tc_splitk_reduce(const TcParams p) {
-    constexpr int Q = BN / 4;                              // float4 per tile row
+    const int Q = p.tile_cols / 4;                         // float4 per tile row
     const long per_tile = (long)p.tile_rows * Q;
     const long total = (long)(p.num_tiles - p.dp_tiles) * per_tile;
-    const long piece_floats = (long)p.tile_rows * BN;
+    const long piece_floats = (long)p.tile_rows * p.tile_cols;
     for (long u = blockIdx.x * (long)blockDim.x + threadIdx.x; u < total;
          u += (long)gridDim.x * blockDim.x) {
         const int r = (int)(u / per_tile);
@@ -485,9 +517,9 @@ tc_splitk_reduce(const TcParams p) {
         const int row = e / Q, c4 = (e % Q) * 4;
         int mb, nb;
         tile_coords(p.dp_tiles + r, p, mb, nb);
-        const int grow = mb * p.tile_rows + row, gcol = nb * BN + c4;
+        const int grow = mb * p.tile_rows + row, gcol = nb * p.tile_cols + c4;
         if (grow >= p.M || gcol >= p.N) continue;
-        const float* src = p.partials + (long)r * p.split * piece_floats + (long)row * BN + c4;
+        const float* src = p.partials + (long)r * p.split * piece_floats + (long)row * p.tile_cols + c4;
         float4 s = *reinterpret_cast<const float4*>(src);
         for (int j = 1; j < p.split; ++j) {
             const float4 v = *reinterpret_cast<const float4*>(src + j * piece_floats);
@@ -654,7 +686,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
             store_accumulator(p, w, mb, nb, q * 32 + lane, tmem_base + lane_off + (uint32_t)(acc * BN),
-                              epi_stage + q * 32 * 32, &tmC);
+                              epi_stage + q * (EPI_WARP_BYTES / 4), &tmC, 0, BN / 32);
             tc_fence_before();
             mbar_arrive(smem_u32(&sy->tmem_empty[acc]));
         }
@@ -685,23 +717,33 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 //               bytes; both producers' copies complete on it.
 //   empty[s]    both CTAs: arrived by the leader's commit (multicast).
 //   tmem_full   both CTAs: arrived by the leader's commit (multicast).
-//   tmem_empty  leader only: all 256 epilogue threads of the pair arrive.
+//   tmem_empty  leader only: all epilogue threads of the pair arrive.
 // Both CTAs allocate and free tensor memory jointly (cta_group::2); cluster
 // barriers after set-up and before the free keep the pair in step.
+//
+// Wide tiles (NW = 2): the pair computes a 256 x 512 tile as two N = 256
+// MMAs per K step that share the staged A, so each SM stages 128 rows of A
+// and 256 columns of B per K block: a quarter less TMA traffic and an eighth
+// less shared-memory traffic per FLOP than 256 x 256 tiles. The 128 x 512
+// FP32 accumulator of each CTA fills its tensor memory, so there is one
+// accumulator, and the MMAs of the next tile wait for the epilogue; eight
+// epilogue warps (two per TMEM lane quarter, one per half of the columns)
+// keep that wait short.
 
 constexpr int P_STAGES = 6;                                // ring depth (3 for the split-TF32 form)
+constexpr int P_WIDE_STAGES = 4;                           // ring depth of the wide tiles
 constexpr int P_A_TILE = 128 * SW;                         // 16 KB: this CTA's 128 rows of A
 constexpr int P_B_TILE = 16 * 1024;                        // this CTA's 128 columns of B
 constexpr int P_BM = 256;                                  // pair tile rows (= MMA M)
 
 // Ring geometry. X3 (the three-product split-TF32 form) stages a high and a
 // low copy of each operand per K block.
-template <bool X3>
+template <bool X3, int NW = 1>
 struct PairRing {
     static constexpr int COPIES = X3 ? 2 : 1;
-    static constexpr int STAGES = X3 ? 3 : P_STAGES;
+    static constexpr int STAGES = X3 ? 3 : NW == 2 ? P_WIDE_STAGES : P_STAGES;
     static constexpr int A_STAGE = COPIES * P_A_TILE;
-    static constexpr int B_STAGE = COPIES * P_B_TILE;
+    static constexpr int B_STAGE = COPIES * NW * P_B_TILE;
     static constexpr int STAGE = A_STAGE + B_STAGE;
 };
 // The 16 KB after the ring keep every shared-memory address an MMA
@@ -709,10 +751,22 @@ struct PairRing {
 // past its start) inside the block's allocation; the epilogue warps use them
 // as their 32 x 32 staging blocks.
 constexpr int P_GUARD_BYTES = 16 * 1024;
-template <bool X3>
+// Epilogue geometry: warps, block size, and their staging blocks (two
+// 4 KB blocks per warp, at least the guard).
+template <int NW>
+struct PairEpi {
+    static constexpr int WARPS = NW == 2 ? 8 : 4;
+    static constexpr int THREADS = 64 + 32 * WARPS;
+    static constexpr int BYTES =
+        WARPS * EPI_WARP_BYTES > P_GUARD_BYTES ? WARPS * EPI_WARP_BYTES : P_GUARD_BYTES;
+};
+template <bool X3, int NW>
 constexpr int pair_smem_bytes() {
-    return 1024 + PairRing<X3>::STAGES * PairRing<X3>::STAGE + P_GUARD_BYTES + 256;
+    return 1024 + PairRing<X3, NW>::STAGES * PairRing<X3, NW>::STAGE + PairEpi<NW>::BYTES + 256;
 }
+static_assert(pair_smem_bytes<false, 1>() <= 227 * 1024 && pair_smem_bytes<true, 1>() <= 227 * 1024 &&
+                  pair_smem_bytes<false, 2>() <= 227 * 1024,
+              "CTA-pair kernels exceed the shared memory of a block");
 
 struct PairSync {
     uint64_t full[P_STAGES];
@@ -730,16 +784,18 @@ static_assert(sizeof(PairSync) <= 256, "pair barrier block");
 // same accumulator, lo(A) hi(B) + hi(A) lo(B) + hi(A) hi(B), which carries
 // the product to FP32-level accuracy (the lo x lo term is below FP32's own
 // rounding).
-template <int ESZ, bool B_KMAJOR, bool X3>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+template <int ESZ, bool B_KMAJOR, bool X3, int NW>
+__global__ void __launch_bounds__(PairEpi<NW>::THREADS, 1)
 tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmA2,
                    const __grid_constant__ CUtensorMap tmB2,
                    const __grid_constant__ CUtensorMap tmC,
                    const TcParams p) {
-    using R = PairRing<X3>;
+    using R = PairRing<X3, NW>;
     static_assert(!X3 || (ESZ == 4 && B_KMAJOR), "the split form is TF32 with B K-major");
+    static_assert(NW == 1 || (NW == 2 && !X3), "wide tiles are for the one-product forms");
+    constexpr int NACC = 2 / NW;                         // accumulators in tensor memory
     using KD = Kind<ESZ>;
     constexpr int BK = KD::BK;
     constexpr int K_STEPS = BK / KD::UMMA_K;
@@ -755,7 +811,7 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
-    PairSync* sy = reinterpret_cast<PairSync*>(smem + R::STAGES * R::STAGE + P_GUARD_BYTES);
+    PairSync* sy = reinterpret_cast<PairSync*>(smem + R::STAGES * R::STAGE + PairEpi<NW>::BYTES);
     const uint32_t a_base = smem_u32(smem);
     const uint32_t b_base = a_base + R::STAGES * R::A_STAGE;
 
@@ -771,7 +827,7 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&sy->tmem_full[a]), 1);
-            mbar_init(smem_u32(&sy->tmem_empty[a]), 256);
+            mbar_init(smem_u32(&sy->tmem_empty[a]), 2 * 32 * PairEpi<NW>::WARPS);
         }
         if constexpr (X3) {
             asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmA2)) : "memory");
@@ -808,7 +864,7 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
                 int mb, nb;
                 tile_coords(w.tile, p, mb, nb);
                 const int row0 = mb * P_BM + (int)rank * 128;
-                const int col0 = nb * BN + (int)rank * 128;
+                const int col0 = nb * (NW * BN) + (int)rank * 128;
                 for (int kb = w.kb0; kb < w.kb1; ++kb, ++g) {
                     const int s = g % R::STAGES;
                     const uint32_t ph = (uint32_t)(g / R::STAGES) & 1u;
@@ -823,13 +879,20 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
                         tma_load_2d_pair(adst + P_A_TILE, &tmA2, kb * BK, row0, full);
                         tma_load_2d_pair(bdst, &tmB, kb * BK, col0, full);
                         tma_load_2d_pair(bdst + P_B_TILE, &tmB2, kb * BK, col0, full);
-                    } else if constexpr (B_KMAJOR) {
-                        tma_load_2d_pair(bdst, &tmB, kb * BK, col0, full);
                     } else {
 #pragma unroll
-                        for (int c = 0; c < B_CHUNKS; ++c)
-                            tma_load_2d_pair(bdst + c * B_CHUNK_BYTES, &tmB, col0 + c * B_CHUNK_COLS,
-                                             kb * BK, full);
+                        for (int h = 0; h < NW; ++h) {          // B tile h: columns h*256.. of the tile
+                            const uint32_t bh = bdst + h * P_B_TILE;
+                            const int ch = col0 + h * BN;
+                            if constexpr (B_KMAJOR) {
+                                tma_load_2d_pair(bh, &tmB, kb * BK, ch, full);
+                            } else {
+#pragma unroll
+                                for (int c = 0; c < B_CHUNKS; ++c)
+                                    tma_load_2d_pair(bh + c * B_CHUNK_BYTES, &tmB, ch + c * B_CHUNK_COLS,
+                                                     kb * BK, full);
+                            }
+                        }
                     }
                     armed |= 1u << s;
                     armed_parity = (armed_parity & ~(1u << s)) | (ph << s);
@@ -854,38 +917,75 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
         // ------------------------------------------------ MMA issuer (leader CTA)
         if (lane == 0 && leader) {
             int g = 0, it = 0;
+            // The MMAs of ring stage s (K block kb of unit w) for B tiles [h0, h1).
+            auto issue = [&](int s, int kb, const Unit& w, uint32_t d_tmem, int h0, int h1) {
+                const uint32_t a_addr = a_base + s * R::A_STAGE;
+                const uint32_t b_addr = b_base + s * R::B_STAGE;
+#pragma unroll
+                for (int kk = 0; kk < K_STEPS; ++kk) {
+                    const uint32_t first = (kb != w.kb0 || kk != 0) ? 1u : 0u;
+                    const uint64_t ad = smem_desc(a_addr + kk * A_K_STEP, 16, 1024);
+                    if constexpr (X3) {
+                        const uint64_t bd = smem_desc(b_addr + kk * A_K_STEP, 16, 1024);
+                        const uint64_t ad_lo = smem_desc(a_addr + P_A_TILE + kk * A_K_STEP, 16, 1024);
+                        const uint64_t bd_lo = smem_desc(b_addr + P_B_TILE + kk * A_K_STEP, 16, 1024);
+                        tc_mma_pair<ESZ>(d_tmem, ad_lo, bd, IDESC, first);    // lo(A) hi(B)
+                        tc_mma_pair<ESZ>(d_tmem, ad, bd_lo, IDESC, 1u);       // hi(A) lo(B)
+                        tc_mma_pair<ESZ>(d_tmem, ad, bd, IDESC, 1u);          // hi(A) hi(B)
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < NW; ++h) {
+                            if (h < h0 || h >= h1) continue;
+                            const uint32_t bh = b_addr + h * P_B_TILE;
+                            const uint64_t bdh =
+                                B_KMAJOR ? smem_desc(bh + kk * A_K_STEP, 16, 1024)
+                                         : smem_desc(bh + kk * B_K_STEP, B_CHUNK_BYTES, 1024);
+                            tc_mma_pair<ESZ>(d_tmem + (uint32_t)(h * BN), ad, bdh, IDESC, first);
+                        }
+                    }
+                }
+            };
             for (int u = pair; u < p.num_units; u += num_pairs, ++it) {
                 const Unit w = decode_unit(u, p);
-                const int acc = it & 1;
-                const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+                const int acc = it % NACC;
+                const uint32_t aph = (uint32_t)(it / NACC) & 1u;
                 if (!mbar_wait(smem_u32(&sy->tmem_empty[acc]), aph ^ 1u, &sy->abort, lim, true)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 bool ok = true;
-                for (int kb = w.kb0; kb < w.kb1; ++kb, ++g) {
+                int kb = w.kb0;
+                if constexpr (NW == 2) {
+                    // The epilogue frees the accumulator's column halves one after
+                    // the other (tmem_empty[0], then tmem_empty[1]). Run the first
+                    // half's MMAs on the stages already loaded while the second
+                    // half still drains, then catch up on the second half's.
+                    const int held = min(R::STAGES, w.kb1 - w.kb0);
+                    for (int i = 0; i < held; ++i) {
+                        const int s = (g + i) % R::STAGES;
+                        const uint32_t ph = (uint32_t)((g + i) / R::STAGES) & 1u;
+                        if (!mbar_wait(smem_u32(&sy->full[s]), ph, &sy->abort, lim, true)) { ok = false; break; }
+                        tc_fence_after();
+                        issue(s, w.kb0 + i, w, d_tmem, 0, 1);
+                    }
+                    if (ok && !mbar_wait(smem_u32(&sy->tmem_empty[1]), aph ^ 1u, &sy->abort, lim, true))
+                        ok = false;
+                    if (ok) {
+                        tc_fence_after();
+                        for (int i = 0; i < held; ++i) {
+                            const int s = (g + i) % R::STAGES;
+                            issue(s, w.kb0 + i, w, d_tmem, 1, 2);
+                            tc_commit_pair_multicast(smem_u32(&sy->empty[s]));   // slot free in both CTAs
+                        }
+                    }
+                    g += held;
+                    kb += held;
+                }
+                for (; ok && kb < w.kb1; ++kb, ++g) {
                     const int s = g % R::STAGES;
                     const uint32_t ph = (uint32_t)(g / R::STAGES) & 1u;
                     if (!mbar_wait(smem_u32(&sy->full[s]), ph, &sy->abort, lim, true)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t a_addr = a_base + s * R::A_STAGE;
-                    const uint32_t b_addr = b_base + s * R::B_STAGE;
-#pragma unroll
-                    for (int kk = 0; kk < K_STEPS; ++kk) {
-                        const uint32_t first = (kb != w.kb0 || kk != 0) ? 1u : 0u;
-                        const uint64_t ad = smem_desc(a_addr + kk * A_K_STEP, 16, 1024);
-                        const uint64_t bd =
-                            B_KMAJOR ? smem_desc(b_addr + kk * A_K_STEP, 16, 1024)
-                                     : smem_desc(b_addr + kk * B_K_STEP, B_CHUNK_BYTES, 1024);
-                        if constexpr (X3) {
-                            const uint64_t ad_lo = smem_desc(a_addr + P_A_TILE + kk * A_K_STEP, 16, 1024);
-                            const uint64_t bd_lo = smem_desc(b_addr + P_B_TILE + kk * A_K_STEP, 16, 1024);
-                            tc_mma_pair<ESZ>(d_tmem, ad_lo, bd, IDESC, first);    // lo(A) hi(B)
-                            tc_mma_pair<ESZ>(d_tmem, ad, bd_lo, IDESC, 1u);       // hi(A) lo(B)
-                            tc_mma_pair<ESZ>(d_tmem, ad, bd, IDESC, 1u);          // hi(A) hi(B)
-                        } else {
-                            tc_mma_pair<ESZ>(d_tmem, ad, bd, IDESC, first);
-                        }
-                    }
+                    issue(s, kb, w, d_tmem, 0, NW);
                     tc_commit_pair_multicast(smem_u32(&sy->empty[s]));   // slot free in both CTAs
                 }
                 if (!ok) break;
@@ -896,25 +996,41 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------ epilogue (warps 2-5, both CTAs)
-        const int q = warp & 3;
+        // ------------------------------------------------ epilogue (warps 2.., both CTAs)
+        const int q = warp & 3;                              // TMEM lanes 32q .. 32q+31
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        constexpr int PARTS = PairEpi<NW>::WARPS / 4;      // warps sharing a lane quarter
+        const int part = (warp - 2) >> 2;
+        const int blocks = p.tile_cols / 32 / PARTS;         // 32-column blocks per warp
         int it = 0;
         for (int u = pair; u < p.num_units; u += num_pairs, ++it) {
             const Unit w = decode_unit(u, p);
             int mb, nb;
             tile_coords(w.tile, p, mb, nb);
-            const int acc = it & 1;
-            const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+            const int acc = it % NACC;
+            const uint32_t aph = (uint32_t)(it / NACC) & 1u;
             bool ok = mbar_wait(smem_u32(&sy->tmem_full[acc]), aph, &sy->abort, lim, true);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
-            store_accumulator(p, w, mb, nb, (int)rank * 128 + q * 32 + lane,
-                              tmem_base + lane_off + (uint32_t)(acc * BN),
-                              reinterpret_cast<float*>(smem + R::STAGES * R::STAGE) + q * 32 * 32,
-                              &tmC);
-            tc_fence_before();
-            mbar_arrive_cluster(tmem_empty0 + (uint32_t)(acc * sizeof(uint64_t)));
+            float* stage = reinterpret_cast<float*>(smem + R::STAGES * R::STAGE) +
+                           (warp - 2) * (EPI_WARP_BYTES / 4);
+            if constexpr (NW == 2) {
+                // Column halves in order, each freed (tmem_empty[half]) as soon
+                // as it has left tensor memory.
+                for (int half = 0; half < 2; ++half) {
+                    const int c0 = half * (blocks * PARTS / 2) + part * (blocks / 2);
+                    store_accumulator(p, w, mb, nb, (int)rank * 128 + q * 32 + lane,
+                                      tmem_base + lane_off, stage, &tmC, c0, c0 + blocks / 2);
+                    tc_fence_before();
+                    mbar_arrive_cluster(tmem_empty0 + (uint32_t)(half * sizeof(uint64_t)));
+                }
+            } else {
+                store_accumulator(p, w, mb, nb, (int)rank * 128 + q * 32 + lane,
+                                  tmem_base + lane_off + (uint32_t)(acc * BN), stage, &tmC,
+                                  part * blocks, (part + 1) * blocks);
+                tc_fence_before();
+                mbar_arrive_cluster(tmem_empty0 + (uint32_t)(acc * sizeof(uint64_t)));
+            }
         }
         if (lane == 0) tma_store_wait_all();    // C stores done before the block retires
     }
@@ -959,6 +1075,7 @@ TcParams make_params(const GemmArgs& a, const TcPlan& pl, float* partials,
     p.num_tiles = pl.tiles_m * pl.tiles_n;
     p.kblocks = pl.kblocks;
     p.tile_rows = pl.tile_rows;
+    p.tile_cols = pl.tile_cols;
     p.dp_tiles = pl.dp_tiles;
     p.split = pl.split;
     p.num_units = pl.dp_tiles + (p.num_tiles - pl.dp_tiles) * pl.split;
@@ -985,7 +1102,7 @@ void encode_c(EncodeTiledFn enc, CUtensorMap* map, const GemmArgs& a, TcParams& 
 }
 
 cudaError_t launch_reduce(const TcParams& p, cudaStream_t s) {
-    const long units = (long)(p.num_tiles - p.dp_tiles) * p.tile_rows * (BN / 4);
+    const long units = (long)(p.num_tiles - p.dp_tiles) * p.tile_rows * (p.tile_cols / 4);
     long blocks = (units + 255) / 256;
     if (blocks > 8192) blocks = 8192;
     tc_splitk_reduce<<<(int)blocks, 256, 0, s>>>(p);
@@ -1018,13 +1135,13 @@ cudaError_t launch_tc(const GemmArgs& a, const TcPlan& pl, float* partials, int 
 }
 
 // The 2-SM kernel: clusters of two CTAs, one CTA per SM, persistent over
-// 256 x 256 tiles.
-template <int ESZ, bool B_KMAJOR, bool X3 = false>
+// 256 x 256 tiles (NW = 1) or 256 x 512 tiles (NW = 2).
+template <int ESZ, bool B_KMAJOR, bool X3 = false, int NW = 1>
 cudaError_t launch_tc_pair(const GemmArgs& a, const TcPlan& pl, float* partials, int num_sms,
                            EncodeTiledFn enc, unsigned long long wait_limit_ns, int debug_stall,
                            cudaStream_t s) {
     constexpr int BK = Kind<ESZ>::BK;
-    constexpr int SMEM = pair_smem_bytes<X3>();
+    constexpr int SMEM = pair_smem_bytes<X3, NW>();
     CUtensorMap tmA, tmB, tmA2, tmB2;
     if (!encode_2d(enc, &tmA, a.A, ESZ, a.M, a.K, a.lda, BK, 128)) return cudaErrorInvalidValue;
     const bool okb = B_KMAJOR ? encode_2d(enc, &tmB, a.B, ESZ, a.N, a.K, a.ldb, BK, 128)
@@ -1042,13 +1159,13 @@ cudaError_t launch_tc_pair(const GemmArgs& a, const TcPlan& pl, float* partials,
     CUtensorMap tmC;
     encode_c(enc, &tmC, a, p);
 
-    auto kern = tc_gemm_2sm_kernel<ESZ, B_KMAJOR, X3>;
+    auto kern = tc_gemm_2sm_kernel<ESZ, B_KMAJOR, X3, NW>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     const int pairs = p.num_units < num_sms / 2 ? p.num_units : num_sms / 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs, 1, 1);
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.blockDim = dim3(PairEpi<NW>::THREADS, 1, 1);
     cfg.dynamicSmemBytes = SMEM;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -1065,61 +1182,109 @@ cudaError_t launch_tc_pair(const GemmArgs& a, const TcPlan& pl, float* partials,
     return launch_reduce(p, s);
 }
 
-const char* kNames[3][2] = {
-    {"tc_tf32_128x256x32_s4_persistent", "tc_tf32_2sm_256x256x32_s6_persistent"},
-    {"tc_bf16_128x256x64_s4_persistent", "tc_bf16_2sm_256x256x64_s6_persistent"},
-    {"tc_tf32x3_2sm_256x256x32_s3_persistent", "tc_tf32x3_2sm_256x256x32_s3_persistent"},
+const char* kNames[3][3] = {
+    {"tc_tf32_128x256x32_s4_persistent", "tc_tf32_2sm_256x256x32_s6_persistent",
+     "tc_tf32_2sm_256x512x32_s4_persistent"},
+    {"tc_bf16_128x256x64_s4_persistent", "tc_bf16_2sm_256x256x64_s6_persistent",
+     "tc_bf16_2sm_256x512x64_s4_persistent"},
+    {"tc_tf32x3_2sm_256x256x32_s3_persistent", "tc_tf32x3_2sm_256x256x32_s3_persistent",
+     "tc_tf32x3_2sm_256x256x32_s3_persistent"},
 };
 
 }  // namespace
 
-TcPlan tc_plan(int M, int N, int K, int in_type, bool pair, int num_sms, bool allow_split) {
-    if (in_type == TC_TF32X3) pair = true;    // the split form exists as a CTA-pair kernel only
+// Timing model of one tile on one resident unit (an SM pair, or an SM),
+// fitted to measurements on the FFN and square BF16/TF32 shapes:
+// the main loop runs at `tflops` per unit and a wide tile's accumulator
+// write-out (128 x 512 FP32 per SM, about 6.5 us) is not hidden behind the
+// next tile's MMAs; the other shapes overlap it (two accumulators).
+struct TileModel {
+    double main_us, epi_us;
+};
+
+TileModel tile_model(int in_type, int shape, int tile_rows, int tile_cols, int K) {
+    double tflops = shape == TC_ONE_SM ? 9.3 : shape == TC_PAIR ? 22.8 : 30.0;   // BF16
+    if (in_type != TC_BF16) tflops *= 0.5;                                      // TF32 rate
+    if (in_type == TC_TF32X3) tflops /= 3.0;                                    // three products
+    TileModel m;
+    m.main_us = 2.0 * tile_rows * tile_cols * (double)K / (tflops * 1e6);
+    m.epi_us = shape == TC_PAIR_WIDE ? 6.5 : 0.0;
+    return m;
+}
+
+TcPlan tc_plan(int M, int N, int K, int in_type, int shape, int num_sms, bool allow_split) {
+    if (in_type == TC_TF32X3) shape = TC_PAIR;   // the split form: 256 x 256 CTA-pair tiles only
+    const bool pair = shape != TC_ONE_SM;
     TcPlan pl;
     pl.tile_rows = pair ? P_BM : BM;
+    pl.tile_cols = shape == TC_PAIR_WIDE ? 2 * BN : BN;
     pl.tiles_m = (M + pl.tile_rows - 1) / pl.tile_rows;
-    pl.tiles_n = (N + BN - 1) / BN;
+    pl.tiles_n = (N + pl.tile_cols - 1) / pl.tile_cols;
     const int bk = in_type == TC_BF16 ? Kind<2>::BK : Kind<4>::BK;
     pl.kblocks = (K + bk - 1) / bk;
     const int tiles = pl.tiles_m * pl.tiles_n;
+    const int slots = pair ? num_sms / 2 : num_sms;
+    const TileModel tm = tile_model(in_type, shape, pl.tile_rows, pl.tile_cols, K);
+    const double tile_us = tm.main_us + tm.epi_us;
+    const double tile_bytes = (double)pl.tile_rows * pl.tile_cols * sizeof(float);
     pl.dp_tiles = tiles;
     pl.split = 1;
-    if (allow_split) {
-        // Rate of one resident work unit (an SM pair or an SM), measured:
-        // BF16 ~1650 TFLOP/s over 76 pairs / ~1420 over 152 SMs; TF32 at
-        // half the BF16 rate.
-        double unit_tflops = pair ? 21.7 : 9.3;
-        if (in_type != TC_BF16) unit_tflops *= 0.5;
-        if (in_type == TC_TF32X3) unit_tflops /= 3.0;
-        const double tile_us = 2.0 * pl.tile_rows * BN * (double)K / (unit_tflops * 1e6);
-        plan_tail_split(tiles, pair ? num_sms / 2 : num_sms, pl.kblocks, tile_us,
-                        (double)pl.tile_rows * BN * sizeof(float), pl.dp_tiles, pl.split);
-    }
+    if (allow_split) plan_tail_split(tiles, slots, pl.kblocks, tile_us, tile_bytes, pl.dp_tiles, pl.split);
     pl.scratch_bytes = pl.split > 1 ? (size_t)(tiles - pl.dp_tiles) * pl.split * pl.tile_rows *
-                                          BN * sizeof(float)
+                                          pl.tile_cols * sizeof(float)
                                     : 0;
+    // Estimated duration: whole-tile rounds, then the rounds of K-pieces (each
+    // with its own epilogue) plus the cost of their partial tiles.
+    if (slots <= 0 || tiles == 0) {
+        pl.est_us = 0.0;
+    } else if (pl.split <= 1) {
+        pl.est_us = (double)((tiles + slots - 1) / slots) * tile_us;
+    } else {
+        const int rem = tiles - pl.dp_tiles;
+        const int rounds = (rem * pl.split + slots - 1) / slots;
+        pl.est_us = (double)(pl.dp_tiles / slots) * tile_us +
+                    rounds * (tm.main_us / pl.split + tm.epi_us) +
+                    tail_split_cost_us(rem, tile_bytes, pl.split);
+    }
     return pl;
 }
 
-bool tc_use_pair(int M, int mode) {
-    if (mode == 0) return false;
-    if (mode == 1) return true;
-    return M > BM;          // a pair tile is 256 rows tall
+int tc_shape(int M, int N, int K, int in_type, int mode, int num_sms, bool allow_split) {
+    if (in_type == TC_TF32X3) return TC_PAIR;
+    if (mode == 0) return TC_ONE_SM;
+    if (mode == 1) return TC_PAIR;
+    if (mode == 2) return TC_PAIR_WIDE;
+    if (M <= BM) return TC_ONE_SM;        // a pair tile is 256 rows tall
+    if (N <= BN) return TC_PAIR;
+    // The shape the timing model expects to finish first; near-ties go to
+    // the narrow tiles, whose epilogue is hidden.
+    const TcPlan narrow = tc_plan(M, N, K, in_type, TC_PAIR, num_sms, allow_split);
+    const TcPlan wide = tc_plan(M, N, K, in_type, TC_PAIR_WIDE, num_sms, allow_split);
+    return wide.est_us < 0.97 * narrow.est_us ? TC_PAIR_WIDE : TC_PAIR;
 }
 
-const char* tc_kernel_name(int in_type, bool pair) {
-    return kNames[in_type == TC_BF16 ? 1 : in_type == TC_TF32X3 ? 2 : 0][pair ? 1 : 0];
+const char* tc_kernel_name(int in_type, int shape) {
+    const int sh = shape < 0 ? 0 : shape > 2 ? 2 : shape;
+    return kNames[in_type == TC_BF16 ? 1 : in_type == TC_TF32X3 ? 2 : 0][sh];
 }
 
 cudaError_t tc_launch(const GemmArgs& a, int in_type, int b_kmajor, int num_sms, void* encode_fn,
-                      unsigned long long wait_limit_ns, int debug_stall, bool pair,
+                      unsigned long long wait_limit_ns, int debug_stall, int shape,
                       const TcPlan& pl, float* partials, cudaStream_t s) {
     auto enc = reinterpret_cast<EncodeTiledFn>(encode_fn);
     const unsigned long long w = wait_limit_ns;
     const int st = debug_stall;
     if (in_type == TC_TF32X3)       // always the CTA-pair kernel, B K-major
         return launch_tc_pair<4, true, true>(a, pl, partials, num_sms, enc, w, st, s);
-    if (pair) {
+    if ((shape == TC_PAIR_WIDE) != (pl.tile_cols == 2 * BN)) return cudaErrorInvalidValue;
+    if (shape == TC_PAIR_WIDE) {
+        if (in_type == TC_BF16)
+            return b_kmajor ? launch_tc_pair<2, true, false, 2>(a, pl, partials, num_sms, enc, w, st, s)
+                            : launch_tc_pair<2, false, false, 2>(a, pl, partials, num_sms, enc, w, st, s);
+        if (!b_kmajor) return cudaErrorInvalidValue;    // TF32 reads B K-major only
+        return launch_tc_pair<4, true, false, 2>(a, pl, partials, num_sms, enc, w, st, s);
+    }
+    if (shape == TC_PAIR) {
         if (in_type == TC_BF16)
             return b_kmajor ? launch_tc_pair<2, true>(a, pl, partials, num_sms, enc, w, st, s)
                             : launch_tc_pair<2, false>(a, pl, partials, num_sms, enc, w, st, s);

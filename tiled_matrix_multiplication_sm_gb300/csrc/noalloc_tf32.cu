@@ -115,10 +115,10 @@ extern "C" int gemm_tc_tf32_noalloc(int M, int N, int K, const float* A, long ld
     if (tgemm::transpose_f32(B, ldb, d.scratch, ldt, K, N, stream) != cudaSuccess)
         return TGEMM_ERR_CUDA;
     tgemm::GemmArgs a{M, N, K, A, lda, d.scratch, ldt, C, ldc};
-    const bool pair = tgemm::tc_use_pair(M, -1);
+    const int shape = tgemm::tc_shape(M, N, K, tgemm::TC_TF32, -1, d.num_sms, false);
     // No split of the last wave: its partial tiles would need more scratch.
-    const tgemm::TcPlan plan = tgemm::tc_plan(M, N, K, tgemm::TC_TF32, pair, d.num_sms, false);
-    if (tgemm::tc_launch(a, tgemm::TC_TF32, 1, d.num_sms, enc, kWaitLimitNs, 0, pair, plan,
+    const tgemm::TcPlan plan = tgemm::tc_plan(M, N, K, tgemm::TC_TF32, shape, d.num_sms, false);
+    if (tgemm::tc_launch(a, tgemm::TC_TF32, 1, d.num_sms, enc, kWaitLimitNs, 0, shape, plan,
                          nullptr, stream) != cudaSuccess)
         return TGEMM_ERR_CUDA;
     return TGEMM_OK;

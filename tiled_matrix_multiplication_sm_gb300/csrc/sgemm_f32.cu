@@ -505,14 +505,20 @@ bool vec_ok(const void* p, long ld) {
 // split is taken only when the time it saves on the partial last wave beats
 // what it costs: each piece writes a partial tile and the reduction reads it
 // back (plus one more launch).
+double tail_split_cost_us(int rem, double tile_bytes, int split) {
+    const double hbm_bytes_per_us = 6.5e6;        // a little under the measured copy rate
+    const double launch_us = 5.0;                 // the reduction kernel
+    // Each piece writes a partial tile, the reduction reads them all and
+    // writes the tile.
+    return launch_us + rem * tile_bytes * (2.0 * split + 1.0) / hbm_bytes_per_us;
+}
+
 void plan_tail_split(int tiles, int slots, int ktiles, double tile_us, double tile_bytes,
                      int& dp_tiles, int& split) {
     dp_tiles = tiles;
     split = 1;
     const int rem = tiles % slots;
     if (rem == 0) return;
-    const double hbm_bytes_per_us = 6.5e6;        // a little under the measured copy rate
-    const double launch_us = 5.0;
     double best_net = 0.0;
     int best_s = 1;
     for (int s = 2; s <= 16; ++s) {
@@ -520,7 +526,7 @@ void plan_tail_split(int tiles, int slots, int ktiles, double tile_us, double ti
         // Tail in units of one whole-tile time: ceil(rem*s/slots) rounds of 1/s.
         const double tail = (double)((rem * s + slots - 1) / slots) / s;
         const double gain = (1.0 - tail) * tile_us;
-        const double cost = launch_us + rem * tile_bytes * (2.0 * s + 1.0) / hbm_bytes_per_us;
+        const double cost = tail_split_cost_us(rem, tile_bytes, s);
         if (gain - cost > best_net) {
             best_net = gain - cost;
             best_s = s;

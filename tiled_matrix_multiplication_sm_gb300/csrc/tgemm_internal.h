@@ -53,31 +53,39 @@ cudaError_t f32_launch(int id, const GemmArgs& a, const F32Plan& pl, float* scra
 
 // ---- tcgen05 tensor-core path (gemm_tcgen05.cu) -------------------------
 enum TcType { TC_TF32 = 1, TC_BF16 = 2, TC_TF32X3 = 3 };
-// Whether the 2-SM (CTA-pair) kernel runs: mode -1 = by shape, 0 = never,
-// 1 = always.
-bool tc_use_pair(int M, int mode);
-const char* tc_kernel_name(int in_type, bool pair);
-// Tiling of one tensor-core product: tiles of tile_rows x 256, the first
-// dp_tiles whole, the rest (a partial last wave) in `split` K-pieces whose
-// partial tiles take scratch_bytes of device scratch (0 when split == 1).
+// Tile shapes of the tensor-core kernels: 128 x 256 on one SM, 256 x 256 on
+// an SM pair, 256 x 512 on an SM pair (two N = 256 MMAs per K step).
+enum TcShape { TC_ONE_SM = 0, TC_PAIR = 1, TC_PAIR_WIDE = 2 };
+// The shape a product runs with: mode -1 = the shape a timing model expects
+// to finish first, 0/1/2 = that TcShape (the split-TF32 form always takes
+// TC_PAIR). allow_split as for tc_plan.
+int tc_shape(int M, int N, int K, int in_type, int mode, int num_sms, bool allow_split);
+const char* tc_kernel_name(int in_type, int shape);
+// Tiling of one tensor-core product: tiles of tile_rows x tile_cols, the
+// first dp_tiles whole, the rest (a partial last wave) in `split` K-pieces
+// whose partial tiles take scratch_bytes of device scratch (0 when split == 1).
 struct TcPlan {
-    int tile_rows, tiles_m, tiles_n, kblocks;
+    int tile_rows, tile_cols, tiles_m, tiles_n, kblocks;
     int dp_tiles, split;
     size_t scratch_bytes;
+    double est_us;       // modelled duration, for choosing between shapes
 };
-TcPlan tc_plan(int M, int N, int K, int in_type, bool pair, int num_sms, bool allow_split);
-// Launch the persistent tcgen05 kernel (one-SM, or 2-SM when `pair`) under
-// plan `pl`, plus the K-piece reduction when pl.split > 1 (`partials` holds
-// pl.scratch_bytes). `encode_fn` is cuTensorMapEncodeTiled. With b_kmajor,
-// a.B / a.ldb describe B transposed (N x K, K contiguous).
+TcPlan tc_plan(int M, int N, int K, int in_type, int shape, int num_sms, bool allow_split);
+// Launch the persistent tcgen05 kernel of TcShape `shape` under plan `pl`
+// (made for the same shape), plus the K-piece reduction when pl.split > 1
+// (`partials` holds pl.scratch_bytes). `encode_fn` is cuTensorMapEncodeTiled.
+// With b_kmajor, a.B / a.ldb describe B transposed (N x K, K contiguous).
 cudaError_t tc_launch(const GemmArgs& a, int in_type, int b_kmajor, int num_sms,
                       void* encode_fn, unsigned long long wait_limit_ns,
-                      int debug_stall, bool pair, const TcPlan& pl, float* partials,
+                      int debug_stall, int shape, const TcPlan& pl, float* partials,
                       cudaStream_t s);
 // Read and clear the tensor-core kernel's status word on the current device.
 cudaError_t tc_read_and_clear_status(int* status, cudaStream_t s);
 
 // ---- tail balancing (sgemm_f32.cu) --------------------------------------
+// Modelled cost (us) of computing `rem` tiles of tile_bytes in `split`
+// K-pieces: the partial tiles' HBM traffic and the reduction launch.
+double tail_split_cost_us(int rem, double tile_bytes, int split);
 // Split of `tiles` work tiles over `slots` resident units: the first
 // dp_tiles whole, the tiles of a partial last wave in `split` K-pieces of at
 // least 4 K-blocks (of `ktiles`). `tile_us` is the time of one whole tile on
