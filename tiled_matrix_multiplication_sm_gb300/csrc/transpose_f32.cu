@@ -47,15 +47,31 @@ transpose_kernel(const T* __restrict__ B, long ldb, T* __restrict__ Bt, long ldt
 // Row-by-row copy of a rows x cols matrix of `esz`-byte elements from
 // leading dimension ld_src to ld_dst (both in elements). Used to give the
 // tensor-memory copies rows that start on 16-byte boundaries.
+// Each block copies REPACK_ROWS rows of one REPACK_COLS-wide column chunk;
+// every thread keeps four loads in flight (columns c, c + 256, c + 512,
+// c + 768) before it stores.
+constexpr int REPACK_ROWS = 4;
+constexpr int REPACK_COLS = 4096;
+
 template <typename T>
 __global__ void __launch_bounds__(256)
 repack_kernel(const T* __restrict__ src, long ld_src, T* __restrict__ dst, long ld_dst, int rows,
               int cols) {
-    for (int r = blockIdx.y; r < rows; r += gridDim.y) {
+    const int r0 = blockIdx.x * REPACK_ROWS;
+    const int c0 = blockIdx.y * REPACK_COLS;
+    const int c1 = cols - c0 < REPACK_COLS ? cols : c0 + REPACK_COLS;
+    for (int r = r0; r < rows && r < r0 + REPACK_ROWS; ++r) {
         const T* s = src + (long)r * ld_src;
         T* d = dst + (long)r * ld_dst;
-        for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < cols; c += gridDim.x * blockDim.x)
-            d[c] = s[c];
+        int c = c0 + threadIdx.x;
+        for (; c + 768 < c1; c += 1024) {
+            const T v0 = s[c], v1 = s[c + 256], v2 = s[c + 512], v3 = s[c + 768];
+            d[c] = v0;
+            d[c + 256] = v1;
+            d[c + 512] = v2;
+            d[c + 768] = v3;
+        }
+        for (; c < c1; c += 256) d[c] = s[c];
     }
 }
 
@@ -137,13 +153,13 @@ cudaError_t transpose_split_tf32(const float* B, long ldb, float* hi_t, float* l
 
 cudaError_t repack_rows(const void* src, long ld_src, void* dst, long ld_dst, int rows, int cols,
                         int esz, cudaStream_t s) {
-    // A 2-D grid: columns across x (coalesced), rows across y.
-    int gx = (cols + 255) / 256;
-    if (gx > 64) gx = 64;
-    if (gx < 1) gx = 1;
-    int gy = rows < 16384 ? rows : 16384;
-    if (gy < 1) gy = 1;
-    const dim3 grid(gx, gy);
+    // One block per REPACK_ROWS rows and REPACK_COLS columns; consecutive
+    // threads copy consecutive columns (coalesced).
+    if (rows <= 0 || cols <= 0) return cudaSuccess;
+    const long gx = ((long)rows + REPACK_ROWS - 1) / REPACK_ROWS;
+    const long gy = ((long)cols + REPACK_COLS - 1) / REPACK_COLS;
+    if (gx > 2147483647L || gy > 65535) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)gx, (unsigned)gy);
     if (esz == 2)
         repack_kernel<unsigned short><<<grid, 256, 0, s>>>(
             static_cast<const unsigned short*>(src), ld_src, static_cast<unsigned short*>(dst),
