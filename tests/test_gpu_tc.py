@@ -212,6 +212,49 @@ def test_matmul_host_round_trip(tgemm, kind):
     assert_bit_exact(C, C_ref, f"matmul {kind}")
 
 
+# ---------------------------------------------------------------- tile shapes
+
+def test_auto_shape_takes_wide_tiles_for_long_k(tgemm):
+    """By shape (mode -1): 256 x 512 tiles where the main loop dominates (the
+    FFN-shaped product, K = 4096), 256 x 256 tiles at small K."""
+    g = inputs.generator(31)
+    A = inputs.draw(2048, 2048, "int4", g).to(torch.bfloat16).cuda()
+    B = inputs.draw(2048, 2048, "int4", g).to(torch.bfloat16).cuda()
+    run_tc(tgemm, A, B, "bf16")
+    assert "2sm_256x256" in tgemm.binding.last_kernel()
+    w = inputs.WORKLOADS["ffn_bf16"]
+    A = torch.zeros(w.M, w.K, dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros(w.K, w.N, dtype=torch.bfloat16, device="cuda")
+    C = run_tc(tgemm, A, B, "bf16")
+    assert "2sm_256x512" in tgemm.binding.last_kernel()
+    assert (C == 0).all()
+
+
+@pytest.mark.parametrize("kind", ["tf32", "bf16"])
+def test_wide_tiles_split_tail_full_output_rule(tgemm, kind):
+    """256 x 512 tiles whose only (partial) wave is split along K: the pieces
+    leave raw partial tiles and the reduction applies alpha, beta and bias;
+    C's rows are not 16-byte aligned. Integer data: bit-exact."""
+    M, N, K = 512, 1530, 2048
+    g = inputs.generator(32)
+    A = inputs.draw(M, K, "int4", g).to(DTYPES[kind])
+    B = inputs.draw(K, N, "int4", g).to(DTYPES[kind])
+    C0 = inputs.draw(M, N, "int4", g)
+    bias = inputs.draw(1, N, "int4", g)[0]
+    C = C0.clone().cuda()
+    assert tgemm.binding.set_tc_kernel(2) == 0
+    try:
+        tgemm.binding.gemm_ex(A.cuda(), B.cuda(), kind, alpha=2.0, beta=-1.0, bias=bias.cuda(),
+                              out=C)
+        name = tgemm.binding.last_kernel()
+    finally:
+        tgemm.binding.set_tc_kernel(-1)
+    assert tgemm.device_status() == 0
+    assert "256x512" in name and "splitk_reduce" in name, name
+    ref, _ = oracle.gemm_ex(A, B, alpha=2.0, beta=-1.0, C0=C0, bias=bias)
+    assert_bit_exact(C, ref, f"wide split {kind}")
+
+
 # ---------------------------------------------------------------- split TF32 (TGEMM_TF32X3)
 
 @pytest.mark.parametrize("shape", [(1, 8, 8), (130, 261, 77), (300, 520, 200), (513, 1032, 520),
