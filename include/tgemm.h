@@ -190,7 +190,10 @@ TGEMM_API int gemm_ex(int M, int N, int K,
  *
  * The call is asynchronous like cudaMemcpyAsync: it returns once the work is
  * enqueued; C is complete (and A, B may be reused) when `stream` has been
- * synchronised. With pageable host memory the CUDA copies become
+ * synchronised. Calls in flight together (on different streams) copy their
+ * operands to the device in call order on one library stream and copy their
+ * results back on separate library streams (four, taken in turn), so one
+ * call's results do not wait for another's. With pageable host memory the CUDA copies become
  * synchronous and there is no overlap. Returns TGEMM_OK,
  * TGEMM_ERR_INVALID_ARG (as gemm_f32, or an unknown path, or an operand not
  * aligned to its element size), TGEMM_ERR_UNSUPPORTED or TGEMM_ERR_CUDA.

@@ -92,3 +92,24 @@ def test_invalid_path_and_misaligned_host_operand(tgemm):
                               0) == b.TGEMM_ERR_INVALID_ARG
     assert b.load().gemm_host(4, 4, 4, A.data_ptr() + 1, 4, B.data_ptr(), 4, C.data_ptr(), 4, 2,
                               0) == b.TGEMM_ERR_INVALID_ARG
+
+
+def test_calls_in_flight_together_on_two_streams(tgemm):
+    """Six gemm_host calls enqueued on two streams before either is
+    synchronised (the result copy streams are taken in turn): every result is
+    the oracle's, bit for bit."""
+    s = [torch.cuda.Stream(), torch.cuda.Stream()]
+    jobs = []
+    for i, path in enumerate(["f32", "tf32", "bf16", "f32", "tf32", "bf16"]):
+        M, N, K = 2100 + 64 * i, 264 + 8 * i, 136
+        g = inputs.generator(900 + i)
+        A = inputs.draw(M, K, "int4", g).to(DTYPE[path]).pin_memory()
+        B = inputs.draw(K, N, "int4", g).to(DTYPE[path]).pin_memory()
+        C = tgemm.binding.gemm_host(A, B, path, stream=s[i % 2], synchronize=False)
+        jobs.append((A, B, C, path))
+    for st in s:
+        st.synchronize()
+    assert tgemm.device_status() == 0
+    for A, B, C, path in jobs:
+        C_ref, _ = oracle.gemm(A, B)
+        assert_bit_exact(C, C_ref, f"async host {path} {tuple(A.shape)}")

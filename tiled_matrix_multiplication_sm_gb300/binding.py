@@ -279,9 +279,13 @@ def _check_host_matrix(x: torch.Tensor, name: str, dtype: torch.dtype) -> int:
 
 def gemm_host(A: torch.Tensor, B: torch.Tensor, path: str = "f32",
               out: Optional[torch.Tensor] = None,
-              stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+              stream: Optional[torch.cuda.Stream] = None,
+              synchronize: bool = True) -> torch.Tensor:
     """C = A @ B for HOST operands through gemm_host (copies overlapped with
-    the product). Returns once C is complete on the host."""
+    the product). Returns once C is complete on the host; with
+    ``synchronize=False`` it returns once the work is enqueued on ``stream``,
+    and C (and the reuse of A, B) waits for that stream to be synchronised --
+    two such calls on two streams overlap."""
     dtype = _PATH_DTYPE[path]
     lda = _check_host_matrix(A, "A", dtype)
     ldb = _check_host_matrix(B, "B", dtype)
@@ -298,7 +302,8 @@ def gemm_host(A: torch.Tensor, B: torch.Tensor, path: str = "f32",
                               TGEMM_PATH[path], int(s.cuda_stream)))
     if st != TGEMM_OK:
         raise TgemmError(st, "gemm_host")
-    s.synchronize()
+    if synchronize:
+        s.synchronize()
     return C
 
 

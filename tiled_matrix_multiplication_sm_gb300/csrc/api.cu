@@ -14,6 +14,7 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr int kCopyOutStreams = 4;      // result streams of gemm_host, taken in turn
 
 struct DeviceInfo {
     bool ready = false;
@@ -22,7 +23,8 @@ struct DeviceInfo {
     bool pool_ready = false;
     cudaMemPool_t pool = nullptr;   // stream-ordered scratch (see scratch_pool)
     cudaStream_t copy_in = nullptr; // host-operand pipeline of gemm_host
-    cudaStream_t copy_out = nullptr;
+    cudaStream_t copy_out[kCopyOutStreams] = {};
+    unsigned next_out = 0;
 };
 
 std::mutex g_mutex;
@@ -89,16 +91,25 @@ cudaMemPool_t scratch_pool(int dev) {
     return d.pool;
 }
 
-// The two copy streams gemm_host uses on device `dev` (created once).
+// The copy streams of one gemm_host call on device `dev` (created once):
+// the operands of every call go to the device on one stream, in call order;
+// each call's results come back on the next of kCopyOutStreams streams, so
+// calls in flight together return their results independently.
 bool copy_streams(int dev, cudaStream_t* in, cudaStream_t* out) {
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceInfo& d = g_devices[dev];
     if (d.copy_in == nullptr) {
-        if (cudaStreamCreateWithFlags(&d.copy_in, cudaStreamNonBlocking) != cudaSuccess) return false;
-        if (cudaStreamCreateWithFlags(&d.copy_out, cudaStreamNonBlocking) != cudaSuccess) return false;
+        cudaStream_t made[1 + kCopyOutStreams] = {};
+        for (int i = 0; i <= kCopyOutStreams; ++i)
+            if (cudaStreamCreateWithFlags(&made[i], cudaStreamNonBlocking) != cudaSuccess) {
+                for (int j = 0; j < i; ++j) cudaStreamDestroy(made[j]);
+                return false;
+            }
+        d.copy_in = made[0];
+        for (int i = 0; i < kCopyOutStreams; ++i) d.copy_out[i] = made[1 + i];
     }
     *in = d.copy_in;
-    *out = d.copy_out;
+    *out = d.copy_out[d.next_out++ % kCopyOutStreams];
     return true;
 }
 
