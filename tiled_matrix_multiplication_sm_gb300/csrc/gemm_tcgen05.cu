@@ -14,16 +14,23 @@
 //     before it is read, read before it is overwritten) are a "full" and an
 //     "empty" mbarrier per ring slot;
 //   * the inner product over the tile (section 4.6) is a chain of
-//     tcgen05.mma instructions issued by one thread, accumulating a
-//     128 x 256 FP32 tile in tensor memory;
-//   * the write-back (section 4.8) is done by four epilogue warps that read
-//     tensor memory with tcgen05.ld while the tensor core already works on
-//     the block's next tile (two accumulators, 2 x 256 columns).
-// The grid is persistent: one block per SM walks tiles in a grouped order so
-// that blocks running together share panels of A and B in L2.
+//     tcgen05.mma instructions issued by one thread, accumulating an FP32
+//     tile in tensor memory;
+//   * the write-back (section 4.8) is done by epilogue warps that read
+//     tensor memory with tcgen05.ld and, where C's rows allow, hand 32 x 32
+//     blocks to TMA stores.
+// Three tile shapes: 128 x 256 on one SM and 256 x 256 on an SM pair
+// (cta_group::2), both with two accumulators so the epilogue of one tile
+// overlaps the MMAs of the next; and 256 x 512 on an SM pair, whose two
+// N = 256 MMAs per K step share the staged A (less operand traffic per
+// FLOP) at the price of a single accumulator that the epilogue frees in two
+// halves. The grid is persistent: one block (or pair) per SM (pair) walks
+// tiles in a grouped order so that blocks running together share panels of
+// A and B in L2.
 //
 // Ragged edges (section 7.1 of the same page): the TMA unit fills rows and
-// columns outside the matrices with zeros; stores past M and N are skipped.
+// columns outside the matrices with zeros; stores past M and N are skipped
+// (TMA stores clip them).
 //
 // Operand layouts in shared memory: A (M x K, K contiguous) is K-major. For
 // BF16, B (K x N, N contiguous) is read MN-major through the instruction
