@@ -362,6 +362,7 @@ def run_gpu(args):
     if not args.no_extras:
         out["e2e"] = run_e2e(tg, A_host, B_host, w, dev, max(3, min(K, 20)))
         out["workloads"] = run_workloads(tg, inputs, dev, flush, peaks, fp32_peak)
+        out["tensor_probe"] = run_tensor_probe(tg, dev, peaks)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         rate, rows, dt, threads, passes = oracle_rate(A_host, B_host, args.cpu_seconds)
         what = (f"{rows} of {w.M} rows of the 4096^3 product" if passes == 1 else
@@ -418,6 +419,24 @@ def run_e2e(tg, A_host, B_host, w, dev, reps):
             "api": "tiled_matrix_multiplication_sm_gb300.binding.gemm_host -> C ABI gemm_host: "
                    "the f32 and tf32 products in flight together on two streams, each "
                    "copying its operands in and its result out (copies overlapped)"}
+
+
+def run_tensor_probe(tg, dev, peaks):
+    """The tensor cores' dense MMA rate on this GPU (gemm_tc_peak: back-to-back
+    SM-pair MMAs from resident shared memory), as context next to the
+    measured cuBLAS peak that the roofline fractions use."""
+    import torch
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    out = {}
+    for kind in ("bf16", "tf32"):
+        per_clk, tflops = tg.binding.tc_peak(kind, True, iters=200000)
+        out[kind] = {"flop_per_clk_per_sm": round(per_clk, 1),
+                     "tflops_probe": round(tflops, 1),
+                     "tflops_at_max_clock": round(per_clk * sms * peaks["sm_max_mhz"] * 1e6 / 1e12,
+                                                  1)}
+    out["note"] = ("back-to-back 256x256 cta_group::2 MMAs, no loads; tflops_probe at the "
+                   "clock the probe ran at, tflops_at_max_clock = FLOP/clk/SM x SMs x max SM clock")
+    return out
 
 
 def run_workloads(tg, inputs, dev, flush, peaks, fp32_peak):

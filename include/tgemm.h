@@ -218,6 +218,25 @@ TGEMM_API int gemm_host(int M, int N, int K,
 TGEMM_API int gemm_device_status(cudaStream_t stream);
 
 /*
+ * gemm_tc_peak — diagnostic: the dense MMA rate of this device's tensor
+ * cores, the denominator a tensor-core roofline can be stated against.
+ *
+ * Every SM (pair = 0: 128 x 256 MMAs, cta_group::1) or SM pair (pair = 1:
+ * 256 x 256 MMAs, cta_group::2) issues `iters` (1 .. 1e8) MMAs of in_type
+ * TGEMM_BF16 (K = 16 per MMA) or TGEMM_TF32 (K = 8) back to back, from
+ * operands resident in shared memory into one tensor-memory accumulator;
+ * nothing is loaded or stored. Writes *flop_per_clk_sm, the dense FLOP per
+ * SM clock cycle (2*M*N*K per MMA, median over the units, measured with the
+ * SM clock counter), and *tflops, the rate of all SMs over the launch's
+ * device time (start-up included) at whatever clock the GPU ran. Allocates
+ * and frees a small device buffer and synchronises `stream`. Returns
+ * TGEMM_OK, TGEMM_ERR_INVALID_ARG, TGEMM_ERR_UNSUPPORTED, TGEMM_ERR_CUDA or
+ * TGEMM_ERR_DEVICE_TIMEOUT (a bounded wait ran out).
+ */
+TGEMM_API int gemm_tc_peak(int in_type, int pair, long iters, double* flop_per_clk_sm,
+                           double* tflops, cudaStream_t stream);
+
+/*
  * gemm_status_string — a static, human-readable name for a status code.
  * Never returns NULL; unknown codes give "unknown tgemm status".
  */

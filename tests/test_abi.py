@@ -35,7 +35,7 @@ def test_header_declares_the_boundary():
     names = declared_symbols()
     for required in ["gemm_f32", "gemm_tc", "gemm_status_string", "gemm_device_status"]:
         assert required in names
-    assert len(names) == 14
+    assert len(names) == 15
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -86,6 +86,20 @@ def test_f32_invalid_arguments(lib, args):
 ])
 def test_tc_invalid_arguments(lib, args, code):
     assert tg.gemm_tc_raw(*args, 0) == code
+
+
+def test_tc_peak_rejects_bad_arguments(lib):
+    """Argument checks of the tensor-rate probe come before any device work."""
+    import ctypes
+    d = ctypes.c_double(0.0)
+    ref = ctypes.byref(d)
+    bad = binding.TGEMM_ERR_INVALID_ARG
+    assert lib.gemm_tc_peak(4, 1, 1000, ref, ref, None) == bad          # unknown in_type
+    assert lib.gemm_tc_peak(binding.TGEMM_TF32X3, 1, 1000, ref, ref, None) == bad
+    assert lib.gemm_tc_peak(binding.TGEMM_BF16, 2, 1000, ref, ref, None) == bad   # pair not 0/1
+    assert lib.gemm_tc_peak(binding.TGEMM_BF16, 1, 0, ref, ref, None) == bad      # no MMAs
+    assert lib.gemm_tc_peak(binding.TGEMM_BF16, 1, 10 ** 9, ref, ref, None) == bad
+    assert lib.gemm_tc_peak(binding.TGEMM_BF16, 1, 1000, None, ref, None) == bad  # null output
 
 
 def test_ex_entry_rejects_bad_arguments(lib):

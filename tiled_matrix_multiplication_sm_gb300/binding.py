@@ -53,6 +53,9 @@ _SIGNATURES = {
     "gemm_tc_tf32_noalloc": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                             _VP, ctypes.c_long, _VP, ctypes.c_long,
                                             _VP, ctypes.c_long, _VP]),
+    "gemm_tc_peak": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_long,
+                                    ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
+                                    _VP]),
 }
 
 
@@ -196,6 +199,21 @@ def device_status(stream: Optional[torch.cuda.Stream] = None) -> int:
 
 def set_wait_limit_ns(ns: int) -> int:
     return int(load().gemm_set_wait_limit_ns(int(ns)))
+
+
+def tc_peak(kind: str = "bf16", pair: bool = True, iters: int = 200000,
+            stream: Optional[torch.cuda.Stream] = None):
+    """Dense MMA rate of the tensor cores (gemm_tc_peak): returns
+    (FLOP per SM clock cycle, TFLOP/s over the launch at the running clock)."""
+    in_type = {"bf16": TGEMM_BF16, "tf32": TGEMM_TF32}[kind]
+    per_clk = ctypes.c_double(0.0)
+    tflops = ctypes.c_double(0.0)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    st = int(load().gemm_tc_peak(in_type, 1 if pair else 0, int(iters), ctypes.byref(per_clk),
+                                 ctypes.byref(tflops), int(s.cuda_stream)))
+    if st != TGEMM_OK:
+        raise TgemmError(st, "gemm_tc_peak")
+    return per_clk.value, tflops.value
 
 
 def set_debug_stall(enable: bool) -> int:

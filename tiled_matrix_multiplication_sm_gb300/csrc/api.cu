@@ -5,11 +5,13 @@
 #include "../../include/tgemm.h"
 #include "tgemm_internal.h"
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 namespace {
 
@@ -620,6 +622,50 @@ int gemm_device_status(cudaStream_t stream) {
     int v = 0;
     if (tgemm::tc_read_and_clear_status(&v, stream) != cudaSuccess) return TGEMM_ERR_CUDA;
     return v == 0 ? TGEMM_OK : TGEMM_ERR_DEVICE_TIMEOUT;
+}
+
+int gemm_tc_peak(int in_type, int pair, long iters, double* flop_per_clk_sm, double* tflops,
+                 cudaStream_t stream) {
+    if (in_type != TGEMM_TF32 && in_type != TGEMM_BF16) return TGEMM_ERR_INVALID_ARG;
+    if (pair != 0 && pair != 1) return TGEMM_ERR_INVALID_ARG;
+    if (iters < 1 || iters > 100000000L || flop_per_clk_sm == nullptr || tflops == nullptr)
+        return TGEMM_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    int st = current_device_info(&dev);
+    if (st != TGEMM_OK) return st;
+    long long* cycles = nullptr;
+    if (cudaMalloc(&cycles, sizeof(long long) * (size_t)dev.num_sms) != cudaSuccess)
+        return TGEMM_ERR_CUDA;
+    std::vector<long long> host((size_t)dev.num_sms, -1);
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    int units = 0;
+    int rc = TGEMM_OK;
+    float ms = 0.0f;
+    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess ||
+        cudaEventRecord(e0, stream) != cudaSuccess ||
+        tgemm::tc_peak(in_type, pair != 0, iters, dev.num_sms,
+                       (unsigned long long)g_wait_limit_ns.load(), cycles, &units,
+                       stream) != cudaSuccess ||
+        cudaEventRecord(e1, stream) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess ||
+        cudaMemcpy(host.data(), cycles, sizeof(long long) * (size_t)units,
+                   cudaMemcpyDeviceToHost) != cudaSuccess)
+        rc = TGEMM_ERR_CUDA;
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+    cudaFree(cycles);
+    if (rc != TGEMM_OK) return rc;
+    int status = 0;
+    if (tgemm::tc_read_and_clear_status(&status, stream) != cudaSuccess) return TGEMM_ERR_CUDA;
+    host.resize((size_t)units);
+    for (long long c : host)
+        if (c <= 0 || status != 0) return TGEMM_ERR_DEVICE_TIMEOUT;
+    std::sort(host.begin(), host.end());
+    const double median = (double)host[host.size() / 2];
+    const double per_unit = tgemm::tc_peak_flop_per_mma(in_type, pair != 0) * (double)iters;
+    *flop_per_clk_sm = per_unit / median / (pair ? 2.0 : 1.0);
+    *tflops = per_unit * units / (ms * 1e-3) / 1e12;
+    return TGEMM_OK;
 }
 
 const char* gemm_status_string(int status) {

@@ -1189,6 +1189,114 @@ cudaError_t launch_tc_pair(const GemmArgs& a, const TcPlan& pl, float* partials,
     return launch_reduce(p, s);
 }
 
+// ===================================================================
+// Dense MMA rate of the tensor cores (a diagnostic, not part of the
+// product): every block -- or SM pair -- issues `iters` MMAs back to back
+// from one resident shared-memory stage (zeros: the values do not change the
+// rate) into one tensor-memory accumulator, and records the SM clock cycles
+// from the first issue to the completion of the last. One SM: 128 x 256
+// MMAs (cta_group::1); pair: 256 x 256 (cta_group::2, the leader issues).
+template <int ESZ, bool PAIR>
+__global__ void __launch_bounds__(128, 1)
+tc_peak_kernel(long iters, unsigned long long wait_limit_ns, long long* cycles) {
+    using KD = Kind<ESZ>;
+    constexpr int K_STEPS = KD::BK / KD::UMMA_K;
+    constexpr uint32_t K_STEP_BYTES = KD::UMMA_K * ESZ;
+    constexpr int A_BYTES = 128 * SW;                    // 128 rows, one 128-byte K block
+    constexpr int B_BYTES = (PAIR ? 128 : BN) * SW;      // this CTA's rows of B (K-major)
+    constexpr uint32_t IDESC = instr_desc<ESZ, true, PAIR ? P_BM : BM>();
+    constexpr uint32_t COLS = BN;                        // one 128 x 256 FP32 accumulator
+    struct PeakSync {
+        uint64_t done;
+        uint32_t tmem_base;
+        int abort;
+    };
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
+    PeakSync* sy = reinterpret_cast<PeakSync*>(smem + A_BYTES + B_BYTES);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool issuer = warp == 0 && lane == 0 && (!PAIR || cluster_rank() == 0);
+
+    uint4* z = reinterpret_cast<uint4*>(smem);
+    for (int i = threadIdx.x; i < (A_BYTES + B_BYTES) / 16; i += blockDim.x) z[i] = make_uint4(0, 0, 0, 0);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // zeros visible to the MMA
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&sy->done), 1);
+        sy->abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        if constexpr (PAIR) {
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                         :: "r"(smem_u32(&sy->tmem_base)), "n"(COLS) : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                         :: "r"(smem_u32(&sy->tmem_base)), "n"(COLS) : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
+    }
+    tc_fence_before();
+    if constexpr (PAIR) cluster_sync_all(); else __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = sy->tmem_base;
+
+    if (issuer) {
+        const uint32_t a = smem_u32(smem), b = a + A_BYTES;
+        const long long t0 = clock64();
+        for (long i = 0; i < iters; ++i) {
+            const uint32_t kk = (uint32_t)(i % K_STEPS) * K_STEP_BYTES;
+            const uint64_t ad = smem_desc(a + kk, 16, 1024);
+            const uint64_t bd = smem_desc(b + kk, 16, 1024);
+            if constexpr (PAIR) tc_mma_pair<ESZ>(tmem_base, ad, bd, IDESC, i > 0 ? 1u : 0u);
+            else tc_mma<ESZ>(tmem_base, ad, bd, IDESC, i > 0 ? 1u : 0u);
+        }
+        if constexpr (PAIR) tc_commit_pair(smem_u32(&sy->done));
+        else tc_commit(smem_u32(&sy->done));
+        const bool ok = mbar_wait(smem_u32(&sy->done), 0, &sy->abort, wait_limit_ns, false);
+        const long long t1 = clock64();
+        cycles[PAIR ? blockIdx.x / 2 : blockIdx.x] = ok ? t1 - t0 : -1;
+    }
+    tc_fence_before();
+    if constexpr (PAIR) cluster_sync_all(); else __syncthreads();
+    tc_fence_after();
+    if (warp == 0) {
+        if constexpr (PAIR)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;"
+                         :: "r"(tmem_base), "n"(COLS) : "memory");
+        else
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                         :: "r"(tmem_base), "n"(COLS) : "memory");
+    }
+}
+
+template <int ESZ, bool PAIR>
+cudaError_t launch_peak(long iters, int num_sms, unsigned long long wait_ns, long long* cycles,
+                        int* units, cudaStream_t s) {
+    constexpr int SMEM = 1024 + 128 * SW + (PAIR ? 128 : BN) * SW + 64;
+    auto kern = tc_peak_kernel<ESZ, PAIR>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (e != cudaSuccess) return e;
+    const int blocks = PAIR ? num_sms / 2 * 2 : num_sms;
+    *units = PAIR ? blocks / 2 : blocks;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks, 1, 1);
+    cfg.blockDim = dim3(128, 1, 1);
+    cfg.dynamicSmemBytes = SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = PAIR ? 2 : 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, iters, wait_ns, cycles);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
 const char* kNames[3][3] = {
     {"tc_tf32_128x256x32_s4_persistent", "tc_tf32_2sm_256x256x32_s6_persistent",
      "tc_tf32_2sm_256x512x32_s4_persistent"},
@@ -1303,6 +1411,20 @@ cudaError_t tc_launch(const GemmArgs& a, int in_type, int b_kmajor, int num_sms,
                         : launch_tc<2, false>(a, pl, partials, num_sms, enc, w, st, s);
     return b_kmajor ? launch_tc<4, true>(a, pl, partials, num_sms, enc, w, st, s)
                     : launch_tc<4, false>(a, pl, partials, num_sms, enc, w, st, s);
+}
+
+cudaError_t tc_peak(int in_type, bool pair, long iters, int num_sms, unsigned long long wait_ns,
+                    long long* cycles, int* units, cudaStream_t s) {
+    if (in_type == TC_BF16)
+        return pair ? launch_peak<2, true>(iters, num_sms, wait_ns, cycles, units, s)
+                    : launch_peak<2, false>(iters, num_sms, wait_ns, cycles, units, s);
+    return pair ? launch_peak<4, true>(iters, num_sms, wait_ns, cycles, units, s)
+                : launch_peak<4, false>(iters, num_sms, wait_ns, cycles, units, s);
+}
+
+double tc_peak_flop_per_mma(int in_type, bool pair) {
+    const int uk = in_type == TC_BF16 ? Kind<2>::UMMA_K : Kind<4>::UMMA_K;
+    return 2.0 * (pair ? P_BM : BM) * BN * uk;
 }
 
 cudaError_t tc_read_and_clear_status(int* status, cudaStream_t s) {

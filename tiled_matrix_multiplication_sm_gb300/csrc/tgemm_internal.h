@@ -81,6 +81,14 @@ cudaError_t tc_launch(const GemmArgs& a, int in_type, int b_kmajor, int num_sms,
                       cudaStream_t s);
 // Read and clear the tensor-core kernel's status word on the current device.
 cudaError_t tc_read_and_clear_status(int* status, cudaStream_t s);
+// Dense MMA rate probe: every SM (or SM pair) issues `iters` MMAs from
+// resident shared memory; cycles[u] receives the SM clock cycles of unit u
+// (-1 if its wait ran out) for the *units launched. `cycles` holds >= num_sms
+// entries. tc_peak_flop_per_mma gives the FLOP of one of those MMAs (per
+// unit).
+cudaError_t tc_peak(int in_type, bool pair, long iters, int num_sms, unsigned long long wait_ns,
+                    long long* cycles, int* units, cudaStream_t s);
+double tc_peak_flop_per_mma(int in_type, bool pair);
 
 // ---- tail balancing (sgemm_f32.cu) --------------------------------------
 // Modelled cost (us) of computing `rem` tiles of tile_bytes in `split`
