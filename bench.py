@@ -564,6 +564,48 @@ def run_single(args):
                                    "frac": round(pipe_tf / peak, 4)}}), flush=True)
 
 
+def run_cublas_context(args):
+    """Context only, not the product: torch.matmul (cuBLAS) on the same
+    workloads and paths, timed like the product (L2 flushed, CUDA events,
+    median). FP32 with TF32 math off, TF32 with it on; BF16 writes a BF16
+    result (half the output bytes of the product's FP32 C) and, where torch
+    offers it, an FP32 result ("_fp32_out")."""
+    import torch
+    from tiled_matrix_multiplication_sm_gb300 import inputs
+
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    res = {}
+    cases = {"u1024": ("f32",), "n4096": ("f32", "tf32"), "ragged": ("f32", "tf32"),
+             "ffn_bf16": ("bf16",)}
+    for name, paths in cases.items():
+        w = inputs.WORKLOADS[name]
+        A_host, B_host = inputs.operands(w)
+        A, B = A_host.to(dev), B_host.to(dev)
+        for path in paths:
+            torch.backends.cuda.matmul.allow_tf32 = path == "tf32"
+            fns = {"": lambda: torch.matmul(A, B)}
+            if path == "bf16":
+                # FP32 result like the product, where this torch offers it
+                try:
+                    torch.mm(A[:8, :8], B[:8, :8], out_dtype=torch.float32)
+                    fns["_fp32_out"] = lambda: torch.mm(A, B, out_dtype=torch.float32)
+                except (TypeError, RuntimeError):
+                    pass
+            for tag, fn in fns.items():
+                for _ in range(args.warmup):
+                    fn()
+                ms = time_calls(fn, args.steps, flush)
+                res[f"{name}_{path}{tag}"] = {"M": w.M, "N": w.N, "K": w.K, "ms": round(ms, 4),
+                                              "tflops": round(w.flops / (ms * 1e-3) / 1e12, 3)}
+        del A, B
+    torch.backends.cuda.matmul.allow_tf32 = False
+    print(json.dumps({"context": "cuBLAS via torch.matmul on the bench workloads (not the "
+                                 "product; torch " + torch.__version__ + ")",
+                      "unit": UNIT, "steps": args.steps, "warmup": args.warmup,
+                      "results": res}), flush=True)
+
+
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -574,6 +616,8 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--ref-seconds", type=float, default=90.0)
+    p.add_argument("--cublas-context", action="store_true",
+                   help="time torch.matmul (cuBLAS) on the same workloads as context and exit")
     p.add_argument("--workload", default=None,
                    help="time one product alone, NAME:PATH (e.g. ffn_bf16:bf16); median "
                         "of --steps calls")
@@ -588,6 +632,8 @@ def main(argv=None):
         run_reference(args)
     elif args.workload:
         run_single(args)
+    elif args.cublas_context:
+        run_cublas_context(args)
     else:
         run_gpu(args)
 
