@@ -132,7 +132,7 @@ TGEMM_API int gemm_tc(int M, int N, int K,
 #define TGEMM_PATH_F32    0   /* gemm_f32: FP32 on the CUDA cores, A and B float */
 #define TGEMM_PATH_TF32   1   /* gemm_tc TGEMM_TF32: A and B float */
 #define TGEMM_PATH_BF16   2   /* gemm_tc TGEMM_BF16: A and B bfloat16 */
-#define TGEMM_PATH_TF32X3 3   /* gemm_tc TGEMM_TF32X3: A and B float (gemm_ex only) */
+#define TGEMM_PATH_TF32X3 3   /* gemm_tc TGEMM_TF32X3: A and B float */
 
 /* Storage flags of gemm_ex. */
 #define TGEMM_TRANS_A 1   /* A is stored K x M (lda >= M): op(A) = A^T, i.e. A column-major */
@@ -179,22 +179,23 @@ TGEMM_API int gemm_ex(int M, int N, int K,
  *
  * A (M x K, lda >= K), B (K x N, ldb >= N) and C (M x N floats, ldc >= N)
  * are host pointers, ideally page-locked (cudaHostAlloc / pinned), with
- * elements of the path's type. The call stages them through stream-ordered
- * device scratch from the library's pool and overlaps the transfers with
- * the multiplication: B is copied first, A follows in up to four row panels
- * on a copy stream, each panel is multiplied on `stream` as soon as its rows
- * have arrived (the TF32 path transposes B once for all panels), and each
- * panel of C is copied back on a second copy stream while the next panel
- * computes. Same arithmetic and result as gemm_f32 / gemm_tc on device
- * copies of the operands.
+ * elements of the path's type; `path` is any TGEMM_PATH_*. The call stages
+ * them through stream-ordered device scratch from the library's pool and
+ * overlaps the transfers with the multiplication: B is copied first, A
+ * follows in up to four row panels on a copy stream, each panel is
+ * multiplied on `stream` as soon as its rows have arrived (the TF32 path
+ * transposes B once for all panels; TF32X3 splits B once and each panel of
+ * A as it arrives), and each panel of C is copied back on a second copy
+ * stream while the next panel computes. Same arithmetic and result as
+ * gemm_f32 / gemm_tc on device copies of the operands.
  *
  * The call is asynchronous like cudaMemcpyAsync: it returns once the work is
  * enqueued; C is complete (and A, B may be reused) when `stream` has been
  * synchronised. Calls in flight together (on different streams) copy their
  * operands to the device in call order on one library stream and copy their
  * results back on separate library streams (four, taken in turn), so one
- * call's results do not wait for another's. With pageable host memory the CUDA copies become
- * synchronous and there is no overlap. Returns TGEMM_OK,
+ * call's results do not wait for another's. With pageable host memory the
+ * CUDA copies become synchronous and there is no overlap. Returns TGEMM_OK,
  * TGEMM_ERR_INVALID_ARG (as gemm_f32, or an unknown path, or an operand not
  * aligned to its element size), TGEMM_ERR_UNSUPPORTED or TGEMM_ERR_CUDA.
  */

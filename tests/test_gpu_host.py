@@ -1,6 +1,6 @@
 """gemm_host: the product for operands in host memory, with the transfers
 overlapped with the multiplication (row panels of A and C), checked against
-the CPU oracle through the C ABI on all three paths."""
+the CPU oracle through the C ABI on every path."""
 import pytest
 import torch
 
@@ -11,7 +11,8 @@ from tiled_matrix_multiplication_sm_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
 
-DTYPE = {"f32": torch.float32, "tf32": torch.float32, "bf16": torch.bfloat16}
+DTYPE = {"f32": torch.float32, "tf32": torch.float32, "bf16": torch.bfloat16,
+         "tf32x3": torch.float32}
 
 
 def host_padded(x, ld, pinned=True, pad=float("nan")):
@@ -21,7 +22,7 @@ def host_padded(x, ld, pinned=True, pad=float("nan")):
     return store[:, :cols]
 
 
-@pytest.mark.parametrize("path", ["f32", "tf32", "bf16"])
+@pytest.mark.parametrize("path", ["f32", "tf32", "bf16", "tf32x3"])
 @pytest.mark.parametrize("shape", [(1, 1, 1), (7, 9, 3), (300, 520, 200), (1024, 264, 136),
                                    (2100, 300, 64), (513, 1000, 1)])
 def test_integer_bit_exact(tgemm, path, shape):
@@ -37,7 +38,7 @@ def test_integer_bit_exact(tgemm, path, shape):
     assert_bit_exact(C, C_ref, f"host {path} {shape}")
 
 
-@pytest.mark.parametrize("path", ["f32", "tf32", "bf16"])
+@pytest.mark.parametrize("path", ["f32", "tf32", "bf16", "tf32x3"])
 def test_padded_host_layouts_and_canaries(tgemm, path):
     """Host leading dimensions with NaN padding (never read) and a C whose
     padding columns must stay untouched."""
@@ -53,7 +54,7 @@ def test_padded_host_layouts_and_canaries(tgemm, path):
     assert (Cstore[:, N:] == 4321.0).all()
 
 
-@pytest.mark.parametrize("path", ["f32", "tf32", "bf16"])
+@pytest.mark.parametrize("path", ["f32", "tf32", "bf16", "tf32x3"])
 def test_float_tolerance_pageable(tgemm, path):
     M, N, K = 700, 640, 300
     g = inputs.generator(66)
@@ -62,7 +63,7 @@ def test_float_tolerance_pageable(tgemm, path):
     B = inputs.draw(K, N, dist, g).to(DTYPE[path])
     C = tgemm.binding.gemm_host(A, B, path)
     C_ref, absAB = oracle.gemm(A, B)
-    rel, abs_ = (F32_REL, F32_ABS) if path == "f32" else (TC_REL, TC_ABS)
+    rel, abs_ = (F32_REL, F32_ABS) if path in ("f32", "tf32x3") else (TC_REL, TC_ABS)
     assert_within(C, C_ref, absAB, rel, abs_, f"pageable {path}")
 
 
@@ -100,7 +101,7 @@ def test_calls_in_flight_together_on_two_streams(tgemm):
     the oracle's, bit for bit."""
     s = [torch.cuda.Stream(), torch.cuda.Stream()]
     jobs = []
-    for i, path in enumerate(["f32", "tf32", "bf16", "f32", "tf32", "bf16"]):
+    for i, path in enumerate(["f32", "tf32", "bf16", "tf32x3", "f32", "tf32"]):
         M, N, K = 2100 + 64 * i, 264 + 8 * i, 136
         g = inputs.generator(900 + i)
         A = inputs.draw(M, K, "int4", g).to(DTYPE[path]).pin_memory()

@@ -329,7 +329,8 @@ def matmul(A: torch.Tensor, B: torch.Tensor, path: str = "f32",
            out: Optional[torch.Tensor] = None) -> torch.Tensor:
     """End-to-end product through the library for host or device operands.
 
-    ``path`` is "f32" (CUDA cores), "tf32" or "bf16" (tensor cores). Host
+    ``path`` is "f32" (CUDA cores), "tf32", "bf16" or "tf32x3" (tensor cores;
+    "tf32x3" at FP32-level accuracy). Host
     operands go through gemm_host (copies to the device overlapped with the
     product, result copied back, into ``out`` if given -- ideally pinned)
     and the call returns once C is on the host; device operands give a

@@ -451,8 +451,7 @@ int gemm_ex(int M, int N, int K, const void* A, long lda, const void* B, long ld
 int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long ldb, float* C,
               long ldc, int path, cudaStream_t stream) {
     g_last_kernel = "";
-    if (path != TGEMM_PATH_F32 && path != TGEMM_PATH_TF32 && path != TGEMM_PATH_BF16)
-        return TGEMM_ERR_INVALID_ARG;
+    if (path < TGEMM_PATH_F32 || path > TGEMM_PATH_TF32X3) return TGEMM_ERR_INVALID_ARG;
     int st = check_common(M, N, K, A, lda, B, ldb, C, ldc);
     if (st == -1) return TGEMM_OK;
     if (st != TGEMM_OK) return st;
@@ -488,14 +487,20 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
         bounds[i] = r;
     }
 
-    // Plans and scratch: one pool block for A, B, C, (B transposed), partials.
+    // Plans and scratch: one pool block for A, B, C, B transposed (TF32: one
+    // copy; TF32X3: its high and low parts), the high and low parts of A
+    // (TF32X3), partials.
     const bool tc = path != TGEMM_PATH_F32;
-    const int in_type = path == TGEMM_PATH_BF16 ? TGEMM_BF16 : TGEMM_TF32;
+    const bool x3 = path == TGEMM_PATH_TF32X3;
+    const int in_type = path == TGEMM_PATH_BF16 ? TGEMM_BF16 : x3 ? TGEMM_TF32X3 : TGEMM_TF32;
     const long ldt = (K + 3) / 4 * 4;
-    size_t off_b = align256((size_t)M * lda_d * esz);
+    const size_t bt_bytes = align256((size_t)N * ldt * 4);
+    const size_t a_bytes = align256((size_t)M * lda_d * esz);
+    size_t off_b = a_bytes;
     size_t off_c = off_b + align256((size_t)K * ldb_d * esz);
     size_t off_t = off_c + align256((size_t)M * ldc_d * 4);
-    size_t off_p = off_t + (path == TGEMM_PATH_TF32 ? align256((size_t)N * ldt * 4) : 0);
+    size_t off_a2 = off_t + (path == TGEMM_PATH_TF32 ? bt_bytes : x3 ? 2 * bt_bytes : 0);
+    size_t off_p = off_a2 + (x3 ? 2 * a_bytes : 0);
     int f32_id[4] = {0, 0, 0, 0};
     tgemm::F32Plan f32_plan[4];
     tgemm::TcPlan tc_plan[4];
@@ -526,6 +531,9 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
     char* Bd = base + off_b;
     float* Cd = reinterpret_cast<float*>(base + off_c);
     float* Bt = reinterpret_cast<float*>(base + off_t);
+    float* Bt_lo = reinterpret_cast<float*>(base + off_t + bt_bytes);    // TF32X3
+    float* A_hi = reinterpret_cast<float*>(base + off_a2);               // TF32X3
+    float* A_lo = reinterpret_cast<float*>(base + off_a2 + a_bytes);
 
     const int nev = 2 * panels + 3;
     cudaEvent_t ev[2 * 4 + 3];
@@ -567,6 +575,9 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
     ok(cudaStreamWaitEvent(stream, ev_b, 0));
     if (rc == TGEMM_OK && path == TGEMM_PATH_TF32 && K > 0)
         ok(tgemm::transpose_f32(reinterpret_cast<const float*>(Bd), ldb_d, Bt, ldt, K, N, stream));
+    if (rc == TGEMM_OK && x3 && K > 0)
+        ok(tgemm::transpose_split_tf32(reinterpret_cast<const float*>(Bd), ldb_d, Bt, Bt_lo, ldt,
+                                       K, N, stream));
     const char* name = "";
     for (int i = 0; i < panels && rc == TGEMM_OK; ++i) {
         const long r0 = bounds[i];
@@ -577,6 +588,17 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
         if (K == 0) {
             ok(tgemm::empty_product(Cp, ldc_d, rows, N, tgemm::Epilogue(), stream));
             name = "empty_product";
+        } else if (x3) {
+            // This panel's rows of A split into high and low TF32 parts.
+            const float* Ap = reinterpret_cast<const float*>(Ad + r0 * lda_d * esz);
+            ok(tgemm::split_rows_tf32(Ap, lda_d, A_hi + r0 * lda_d, A_lo + r0 * lda_d, lda_d,
+                                      rows, K, stream));
+            tgemm::GemmArgs pa{rows, N, K, A_hi + r0 * lda_d, lda_d, Bt, ldt, Cp, ldc_d};
+            pa.A2 = A_lo + r0 * lda_d;
+            pa.B2 = Bt_lo;
+            ok(tgemm::tc_launch(pa, in_type, 1, dev.num_sms, enc, limit, stall, shape[i],
+                                tc_plan[i], part, stream));
+            name = tgemm::tc_kernel_name(in_type, shape[i]);
         } else if (tc) {
             const bool tf32 = path == TGEMM_PATH_TF32;
             tgemm::GemmArgs pa{rows, N, K, Ad + r0 * lda_d * esz, lda_d,
@@ -609,7 +631,11 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
     for (int i = 0; i < nev; ++i) cudaEventDestroy(ev[i]);
     if (rc == TGEMM_OK) {
         snprintf(g_last_kernel_buf, sizeof(g_last_kernel_buf), "host_pipeline(panels=%d)+%s%s",
-                 panels, path == TGEMM_PATH_TF32 && K > 0 ? "transpose_b+" : "", name);
+                 panels,
+                 K == 0 ? ""
+                 : path == TGEMM_PATH_TF32 ? "transpose_b+"
+                 : x3 ? "transpose_split_b+split_a+" : "",
+                 name);
         g_last_kernel = g_last_kernel_buf;
     }
     return rc;
