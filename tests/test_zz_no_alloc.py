@@ -28,7 +28,10 @@ def noalloc(tg, A, B, C):
         B.stride(0), C.data_ptr(), C.stride(0), torch.cuda.current_stream().cuda_stream)
 
 
-@pytest.mark.parametrize("first,second", [((300, 1000, 772), (513, 264, 2048))])
+# The second pair's first problem takes the 256 x 512 CTA-pair tiles (64 of
+# them: one round, no split of a tail).
+@pytest.mark.parametrize("first,second", [((300, 1000, 772), (513, 264, 2048)),
+                                          ((8192, 1024, 4096), (256, 512, 8192))])
 def test_noalloc_matches_gemm_tc_on_two_calls(tgemm, first, second):
     for call, (M, N, K) in enumerate([first, second]):
         g = inputs.generator(900 + call)
