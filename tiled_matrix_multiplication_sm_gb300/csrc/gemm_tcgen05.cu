@@ -584,7 +584,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&sy->tmem_full[a]), 1);
-            mbar_init(smem_u32(&sy->tmem_empty[a]), 128);
+            mbar_init(smem_u32(&sy->tmem_empty[a]), 4);      // one arrival per epilogue warp
         }
         mbar_init(smem_u32(&sy->drain), 1);
         sy->abort = 0;
@@ -695,7 +695,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             store_accumulator(p, w, mb, nb, q * 32 + lane, tmem_base + lane_off + (uint32_t)(acc * BN),
                               epi_stage + q * (EPI_WARP_BYTES / 4), &tmC, 0, BN / 32);
             tc_fence_before();
-            mbar_arrive(smem_u32(&sy->tmem_empty[acc]));
+            __syncwarp();                               // the warp's TMEM reads are done
+            if (lane == 31) mbar_arrive(smem_u32(&sy->tmem_empty[acc]));   // not the storing lane
         }
         if (lane == 0) tma_store_wait_all();    // C stores done before the block retires
     }
@@ -724,7 +725,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 //               bytes; both producers' copies complete on it.
 //   empty[s]    both CTAs: arrived by the leader's commit (multicast).
 //   tmem_full   both CTAs: arrived by the leader's commit (multicast).
-//   tmem_empty  leader only: all epilogue threads of the pair arrive.
+//   tmem_empty  leader only: every epilogue warp of the pair arrives once
+//               (one lane, after the warp's TMEM reads).
 // Both CTAs allocate and free tensor memory jointly (cta_group::2); cluster
 // barriers after set-up and before the free keep the pair in step.
 //
@@ -834,7 +836,7 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&sy->tmem_full[a]), 1);
-            mbar_init(smem_u32(&sy->tmem_empty[a]), 2 * 32 * PairEpi<NW>::WARPS);
+            mbar_init(smem_u32(&sy->tmem_empty[a]), 2 * PairEpi<NW>::WARPS);  // one per warp, both CTAs
         }
         if constexpr (X3) {
             asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmA2)) : "memory");
@@ -1029,14 +1031,18 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
                     store_accumulator(p, w, mb, nb, (int)rank * 128 + q * 32 + lane,
                                       tmem_base + lane_off, stage, &tmC, c0, c0 + blocks / 2);
                     tc_fence_before();
-                    mbar_arrive_cluster(tmem_empty0 + (uint32_t)(half * sizeof(uint64_t)));
+                    __syncwarp();                       // the warp's TMEM reads are done
+                    // Lane 31 arrives: lane 0 issued the warp's TMA stores,
+                    // and its release-ordered arrive was measured ~0.2 us later.
+                    if (lane == 31) mbar_arrive_cluster(tmem_empty0 + (uint32_t)(half * sizeof(uint64_t)));
                 }
             } else {
                 store_accumulator(p, w, mb, nb, (int)rank * 128 + q * 32 + lane,
                                   tmem_base + lane_off + (uint32_t)(acc * BN), stage, &tmC,
                                   part * blocks, (part + 1) * blocks);
                 tc_fence_before();
-                mbar_arrive_cluster(tmem_empty0 + (uint32_t)(acc * sizeof(uint64_t)));
+                __syncwarp();                           // the warp's TMEM reads are done
+                if (lane == 31) mbar_arrive_cluster(tmem_empty0 + (uint32_t)(acc * sizeof(uint64_t)));
             }
         }
         if (lane == 0) tma_store_wait_all();    // C stores done before the block retires
