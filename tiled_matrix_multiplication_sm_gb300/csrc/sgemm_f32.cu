@@ -31,10 +31,10 @@
 // of adjacent output columns; each lane computes exactly what fmaf computes,
 // so packed and scalar kernels give identical bits.
 //
-// Tail balancing: tiles are independent ("every cell of C is independent",
-// "Tiled Matrix Multiplication in CUDA", section 1), so when the tile count
-// is not a multiple of the resident blocks, the tiles of the last partial
-// wave are split along K into `split` pieces. Each piece writes its partial
+// Tail balancing: no output of C depends on another ("Tiled Matrix
+// Multiplication in CUDA", section 1), so neither do tiles, and when the
+// tile count is not a multiple of the resident blocks, the tiles of the last
+// partial wave are split along K into `split` pieces. Each piece writes its partial
 // tile to scratch and splitk_reduce adds the pieces in a fixed order; the
 // result is deterministic.
 //
