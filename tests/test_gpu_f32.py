@@ -236,3 +236,18 @@ def test_matmul_host_round_trip(tgemm):
     assert C.device.type == "cpu"
     C_ref, _ = oracle.gemm(A, B)
     assert_bit_exact(C, C_ref, "matmul")
+
+
+@pytest.mark.parametrize("M,tile", [(1, "16x256"), (16, "16x256"), (40, "32x256"), (96, "32x256"),
+                                    (128, "128x256"), (192, "32x256"), (256, "128x256")])
+def test_few_rows_take_short_tiles(tgemm, M, tile):
+    """By shape, products with few rows take 16- or 32-row tiles (no FMAs on
+    rows far past M); results stay bit-exact on integer data."""
+    N, K = 600, 300
+    g = inputs.generator(4000 + M)
+    A = inputs.draw(M, K, "int4", g)
+    B = inputs.draw(K, N, "int4", g)
+    C = run_f32(tgemm, A.cuda(), B.cuda())
+    assert tgemm.binding.last_kernel().startswith("f32_" + tile), tgemm.binding.last_kernel()
+    C_ref, _ = oracle.gemm(A, B)
+    assert_bit_exact(C, C_ref, f"few rows M={M}")

@@ -519,7 +519,9 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
             // Device operands are 16-byte aligned: the vector loaders apply.
             tgemm::GemmArgs pa{rows, N, K, nullptr, lda_d, nullptr, ldb_d, nullptr, ldc_d};
             const int forced = g_forced_f32.load();
-            f32_id[i] = forced >= 0 ? forced : 0;
+            tgemm::GemmArgs chk = pa;
+            chk.A = chk.B = reinterpret_cast<const void*>(256);   // scratch: 16-byte aligned
+            f32_id[i] = forced >= 0 ? forced : tgemm::f32_select(chk, dev.num_sms);
             f32_plan[i] = tgemm::f32_plan(f32_id[i], pa, dev.num_sms);
             total += align256(f32_plan[i].scratch_bytes);
         }

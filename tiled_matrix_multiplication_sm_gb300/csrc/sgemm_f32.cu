@@ -447,6 +447,10 @@ using Big32P1 = Tile<128, 128, 32, 32, 64, 3, 1, true>;
 using Big16P = Tile<128, 128, 16, 32, 64, 4, 2, true>;
 using Big16 = Tile<128, 128, 16, 32, 64, 4, 2, false>;   // scalar FFMA, 8 x 8 per thread
 using Small = Tile<64, 64, 16, 32, 32, 4, 4, false>;     // 128 threads, 8 x 4 per thread
+// Few rows (M small, the product bound by reading B): 32 or 16-row tiles so
+// that few FMAs are spent on rows past M, two blocks of 128 threads per SM.
+using Skinny32 = Tile<32, 256, 32, 32, 64, 3, 2, true>;   // 8 x 8 outputs per thread
+using Skinny16 = Tile<16, 256, 32, 16, 64, 3, 2, true>;   // 4 x 8 outputs per thread
 
 struct Entry {
     const char* name;
@@ -491,8 +495,13 @@ const Entry kTable[] = {
     TGEMM_ENTRY("f32_128x128x16_s4_ffma_a4_b4", Big16, false, false),
     TGEMM_ENTRY("f32_64x64x16_s4_ffma_vecA_vecB", Small, true, true),
     TGEMM_ENTRY("f32_64x64x16_s4_ffma_a4_b4", Small, false, false),
+    TGEMM_ENTRY("f32_32x256x32_s3_ffma2_2blk_vecA_vecB", Skinny32, true, true),
+    TGEMM_ENTRY("f32_16x256x32_s3_ffma2_2blk_vecA_vecB", Skinny16, true, true),
 };
+constexpr int kSkinny32 = 11;
+constexpr int kSkinny16 = 12;
 constexpr int kTableSize = sizeof(kTable) / sizeof(kTable[0]);
+static_assert(kSkinny32 < kTableSize && kSkinny16 < kTableSize, "skinny entries in the table");
 
 bool vec_ok(const void* p, long ld) {
     return reinterpret_cast<uintptr_t>(p) % 16 == 0 && ld % 4 == 0;
@@ -552,8 +561,19 @@ bool f32_kernel_accepts(int id, const GemmArgs& a) {
 }
 
 int f32_select(const GemmArgs& a, int num_sms) {
-    (void)num_sms;   // one tile shape wins on every measured shape class
+    (void)num_sms;
     const bool va = vec_ok(a.A, a.lda), vb = vec_ok(a.B, a.ldb);
+    if (va && vb && a.M > 0) {
+        // Few rows: the 128-row tile spends its FMAs on rows past M. Measured
+        // (N 4096 and 14336, K 4096): 16-row tiles fastest up to M = 16,
+        // 32-row tiles up to 96 rows, and beyond that whenever the 128-row
+        // tiles would pad M by 15 % more (the 32-row tile is ~12 % slower per
+        // useful row on full tiles).
+        if (a.M <= 16) return kSkinny16;
+        const long wide_rows = ((long)a.M + 127) / 128 * 128;
+        const long skinny_rows = ((long)a.M + 31) / 32 * 32;
+        if (a.M <= 96 || (a.M < 512 && wide_rows * 100 > skinny_rows * 115)) return kSkinny32;
+    }
     return (va ? 0 : 2) + (vb ? 0 : 1);
 }
 
