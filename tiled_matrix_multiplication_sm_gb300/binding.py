@@ -100,10 +100,30 @@ def status_string(status: int) -> str:
                 5: "unsupported device"}.get(status, "unknown tgemm status")
 
 
-def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return int(stream.cuda_stream)
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream], device_index: Optional[int] = None) -> int:
+    """The CUDA stream handle to launch on: ``stream``, else the current
+    stream of device ``device_index`` (default: the current device)."""
+    if stream is not None:
+        return int(stream.cuda_stream)
+    if device_index is None:
+        device_index = torch.cuda.current_device()
+    if _raw_stream is not None:
+        return int(_raw_stream(device_index))
+    return int(torch.cuda.current_stream(device_index).cuda_stream)
+
+
+def _on_device(device: torch.device, call):
+    """Run ``call(device_index)`` with ``device`` current; switches devices
+    only when another one is current (a switch costs microseconds)."""
+    current = torch.cuda.current_device()
+    index = device.index if device.index is not None else current
+    if index == current:
+        return call(index)
+    with torch.cuda.device(index):
+        return call(index)
 
 
 def gemm_f32_raw(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, stream_handle=0) -> int:
@@ -125,17 +145,19 @@ def gemm_tc_tf32_noalloc_raw(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, stream
 def _check_matrix(x: torch.Tensor, name: str, dtype: torch.dtype) -> int:
     if not isinstance(x, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if x.dim() != 2:
+    if x.ndim != 2:
         raise ValueError(f"{name} must be 2-D, got shape {tuple(x.shape)}")
-    if x.device.type != "cuda":
+    if not x.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if x.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {x.dtype}")
-    if x.shape[1] > 1 and x.stride(1) != 1:
+    rows_stride, col_stride = x.stride()
+    cols = x.shape[1]
+    if cols > 1 and col_stride != 1:
         raise ValueError(f"{name} must have unit column stride (row-major)")
     # A one-row view keeps its row stride too, so a padded leading dimension
     # is passed through unchanged (it decides which loaders may be used).
-    return max(int(x.stride(0)), int(x.shape[1]), 1)
+    return max(rows_stride, cols, 1)
 
 
 def _out(out, M, N, device):
@@ -157,9 +179,9 @@ def gemm_f32(A: torch.Tensor, B: torch.Tensor, out: Optional[torch.Tensor] = Non
     N = B.shape[1]
     C = _out(out, M, N, A.device)
     ldc = _check_matrix(C, "out", torch.float32)
-    with torch.cuda.device(A.device):
-        st = gemm_f32_raw(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb,
-                          C.data_ptr(), ldc, _stream_handle(stream))
+    st = _on_device(A.device, lambda dev: gemm_f32_raw(
+        M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(), ldc,
+        _stream_handle(stream, dev)))
     if st != TGEMM_OK:
         raise TgemmError(st, "gemm_f32")
     return C
@@ -184,9 +206,9 @@ def gemm_tc(A: torch.Tensor, B: torch.Tensor, in_type: str = "bf16",
     N = B.shape[1]
     C = _out(out, M, N, A.device)
     ldc = _check_matrix(C, "out", torch.float32)
-    with torch.cuda.device(A.device):
-        st = gemm_tc_raw(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb,
-                         C.data_ptr(), ldc, code, _stream_handle(stream))
+    st = _on_device(A.device, lambda dev: gemm_tc_raw(
+        M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(), ldc, code,
+        _stream_handle(stream, dev)))
     if st != TGEMM_OK:
         raise TgemmError(st, "gemm_tc")
     return C
@@ -271,13 +293,15 @@ def gemm_ex(A: torch.Tensor, B: torch.Tensor, path: str = "f32", trans_a: bool =
     if bias is not None:
         if bias.device.type != "cuda" or bias.dtype != torch.float32 or bias.numel() != N:
             raise ValueError("bias must be a CUDA float32 tensor of N entries")
-        bias = bias.contiguous()
+        if not bias.is_contiguous():
+            bias = bias.contiguous()
+            if stream is not None:
+                bias.record_stream(stream)     # the copy lives until `stream` has read it
         bias_ptr = bias.data_ptr()
     flags = (TGEMM_TRANS_A if trans_a else 0) | (TGEMM_TRANS_B if trans_b else 0)
-    with torch.cuda.device(A.device):
-        st = int(load().gemm_ex(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(),
-                                ldc, TGEMM_PATH[path], flags, float(alpha), float(beta),
-                                bias_ptr, _stream_handle(stream)))
+    st = _on_device(A.device, lambda dev: int(load().gemm_ex(
+        M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(), ldc, TGEMM_PATH[path],
+        flags, float(alpha), float(beta), bias_ptr, _stream_handle(stream, dev))))
     if st != TGEMM_OK:
         raise TgemmError(st, "gemm_ex")
     return C
