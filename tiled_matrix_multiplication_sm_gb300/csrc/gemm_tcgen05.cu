@@ -514,7 +514,8 @@ __device__ __forceinline__ void store_accumulator(const TcParams& p, const Unit&
 __global__ void __launch_bounds__(256)
 tc_splitk_reduce(const TcParams p) {
     const int Q = p.tile_cols / 4;                         // float4 per tile row
-    const long per_tile = (long)p.tile_rows * Q;
+    const int rows = p.tile_rows < p.M ? p.tile_rows : p.M; // rows a tile can hold (M small: M)
+    const long per_tile = (long)rows * Q;
     const long total = (long)(p.num_tiles - p.dp_tiles) * per_tile;
     const long piece_floats = (long)p.tile_rows * p.tile_cols;
     for (long u = blockIdx.x * (long)blockDim.x + threadIdx.x; u < total;
@@ -1115,7 +1116,8 @@ void encode_c(EncodeTiledFn enc, CUtensorMap* map, const GemmArgs& a, TcParams& 
 }
 
 cudaError_t launch_reduce(const TcParams& p, cudaStream_t s) {
-    const long units = (long)(p.num_tiles - p.dp_tiles) * p.tile_rows * (p.tile_cols / 4);
+    const int rows = p.tile_rows < p.M ? p.tile_rows : p.M;
+    const long units = (long)(p.num_tiles - p.dp_tiles) * rows * (p.tile_cols / 4);
     long blocks = (units + 255) / 256;
     if (blocks > 8192) blocks = 8192;
     tc_splitk_reduce<<<(int)blocks, 256, 0, s>>>(p);
