@@ -1139,8 +1139,7 @@ cudaError_t launch_tc(const GemmArgs& a, const TcPlan& pl, float* partials, int 
     encode_c(enc, &tmC, a, p);
 
     auto kern = tc_gemm_kernel<ESZ, B_KMAJOR>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SMEM_BYTES);
+    cudaError_t e = set_smem_limit_once<tc_gemm_kernel<ESZ, B_KMAJOR>>(SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int grid = p.num_units < num_sms ? p.num_units : num_sms;
     kern<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tmA, tmB, tmC, p);
@@ -1175,7 +1174,7 @@ cudaError_t launch_tc_pair(const GemmArgs& a, const TcPlan& pl, float* partials,
     encode_c(enc, &tmC, a, p);
 
     auto kern = tc_gemm_2sm_kernel<ESZ, B_KMAJOR, X3, NW>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    cudaError_t e = set_smem_limit_once<tc_gemm_2sm_kernel<ESZ, B_KMAJOR, X3, NW>>(SMEM);
     if (e != cudaSuccess) return e;
     const int pairs = p.num_units < num_sms / 2 ? p.num_units : num_sms / 2;
     cudaLaunchConfig_t cfg = {};
@@ -1284,7 +1283,7 @@ cudaError_t launch_peak(long iters, int num_sms, unsigned long long wait_ns, lon
                         int* units, cudaStream_t s) {
     constexpr int SMEM = 1024 + 128 * SW + (PAIR ? 128 : BN) * SW + 64;
     auto kern = tc_peak_kernel<ESZ, PAIR>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    cudaError_t e = set_smem_limit_once<tc_peak_kernel<ESZ, PAIR>>(SMEM);
     if (e != cudaSuccess) return e;
     const int blocks = PAIR ? num_sms / 2 * 2 : num_sms;
     *units = PAIR ? blocks / 2 : blocks;

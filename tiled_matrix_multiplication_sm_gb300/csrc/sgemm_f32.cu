@@ -464,8 +464,7 @@ template <class T, bool VA, bool VB>
 cudaError_t launch_cfg(const F32Params& p, int blocks, cudaStream_t s) {
     auto kern = sgemm_kernel<T, VA, VB>;
     static_assert(T::SMEM_BYTES <= 227 * 1024, "shared memory budget");
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         T::SMEM_BYTES);
+    cudaError_t e = set_smem_limit_once<sgemm_kernel<T, VA, VB>>(T::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     kern<<<blocks, T::THREADS, T::SMEM_BYTES, s>>>(p);
     return cudaGetLastError();

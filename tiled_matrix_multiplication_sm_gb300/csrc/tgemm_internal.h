@@ -4,6 +4,7 @@
 
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <atomic>
 
 namespace tgemm {
 
@@ -18,6 +19,22 @@ struct Epilogue {
 };
 
 // Arguments of one product, already validated by the API layer.
+// Raise kernel KERNEL's dynamic shared-memory limit to `bytes`, once per
+// device (the attribute stays set for the life of the context), so that a
+// launch does not pay for the call every time.
+template <auto KERNEL>
+cudaError_t set_smem_limit_once(int bytes) {
+    static std::atomic<unsigned long long> done{0};    // bit d: set on device d
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+    if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+    e = cudaFuncSetAttribute(KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
+
 struct GemmArgs {
     int M, N, K;
     const void* A; long lda;
