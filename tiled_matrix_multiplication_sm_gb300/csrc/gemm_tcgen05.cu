@@ -990,7 +990,11 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
                     g += held;
                     kb += held;
                 }
-                for (; ok && kb < w.kb1; ++kb, ++g) {
+                // Wide tiles: the last K blocks (as many as the ring holds) run
+                // the first half's MMAs before the second half's, so the first
+                // half is complete (tmem_full[0]) while the second still computes.
+                const int tail = NW == 2 ? min(R::STAGES, w.kb1 - kb) : 0;
+                for (; ok && kb < w.kb1 - tail; ++kb, ++g) {
                     const int s = g % R::STAGES;
                     const uint32_t ph = (uint32_t)(g / R::STAGES) & 1u;
                     if (!mbar_wait(smem_u32(&sy->full[s]), ph, &sy->abort, lim, true)) { ok = false; break; }
@@ -999,7 +1003,27 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
                     tc_commit_pair_multicast(smem_u32(&sy->empty[s]));   // slot free in both CTAs
                 }
                 if (!ok) break;
-                tc_commit_pair_multicast(smem_u32(&sy->tmem_full[acc]));  // accumulator ready in both
+                if constexpr (NW == 2) {
+                    for (int i = 0; i < tail; ++i) {
+                        const int s = (g + i) % R::STAGES;
+                        const uint32_t ph = (uint32_t)((g + i) / R::STAGES) & 1u;
+                        if (!mbar_wait(smem_u32(&sy->full[s]), ph, &sy->abort, lim, true)) { ok = false; break; }
+                        tc_fence_after();
+                        issue(s, kb + i, w, d_tmem, 0, 1);
+                    }
+                    if (!ok) break;
+                    tc_commit_pair_multicast(smem_u32(&sy->tmem_full[0]));   // first half ready in both
+                    for (int i = 0; i < tail; ++i) {
+                        const int s = (g + i) % R::STAGES;
+                        issue(s, kb + i, w, d_tmem, 1, 2);
+                        tc_commit_pair_multicast(smem_u32(&sy->empty[s]));   // slot free in both CTAs
+                    }
+                    g += tail;
+                    kb += tail;
+                    tc_commit_pair_multicast(smem_u32(&sy->tmem_full[1]));   // second half ready
+                } else {
+                    tc_commit_pair_multicast(smem_u32(&sy->tmem_full[acc]));  // accumulator ready in both
+                }
             }
             tc_commit_pair(smem_u32(&sy->drain));
             mbar_wait(smem_u32(&sy->drain), 0, &sy->abort, lim, false);
@@ -1025,9 +1049,16 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
             float* stage = reinterpret_cast<float*>(smem + R::STAGES * R::STAGE) +
                            (warp - 2) * (EPI_WARP_BYTES / 4);
             if constexpr (NW == 2) {
-                // Column halves in order, each freed (tmem_empty[half]) as soon
-                // as it has left tensor memory.
-                for (int half = 0; half < 2; ++half) {
+                // Column halves in order: each is drained once its MMAs are
+                // complete (tmem_full[half]) and freed (tmem_empty[half]) as
+                // soon as it has left tensor memory.
+                bool ok2 = true;
+                for (int half = 0; half < 2 && ok2; ++half) {
+                    if (half == 1) {
+                        ok2 = mbar_wait(smem_u32(&sy->tmem_full[1]), aph, &sy->abort, lim, true);
+                        if (!__all_sync(0xffffffffu, ok2)) { ok2 = false; break; }
+                        tc_fence_after();
+                    }
                     const int c0 = half * (blocks * PARTS / 2) + part * (blocks / 2);
                     store_accumulator(p, w, mb, nb, (int)rank * 128 + q * 32 + lane,
                                       tmem_base + lane_off, stage, &tmC, c0, c0 + blocks / 2);
@@ -1037,6 +1068,7 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
                     // and its release-ordered arrive was measured ~0.2 us later.
                     if (lane == 31) mbar_arrive_cluster(tmem_empty0 + (uint32_t)(half * sizeof(uint64_t)));
                 }
+                if (!ok2) break;
             } else {
                 store_accumulator(p, w, mb, nb, (int)rank * 128 + q * 32 + lane,
                                   tmem_base + lane_off + (uint32_t)(acc * BN), stage, &tmC,
