@@ -237,6 +237,29 @@ def oracle_rate(A, B, seconds_target: float, max_rows=None):
     return 2.0 * rows * passes * N * K / dt / 1e12, rows, dt, threads, passes
 
 
+def oracle_workloads(inputs, threads):
+    """The oracle on the other workloads, as the parity tests run it: the
+    whole product, or the rows the tests check (the FFN shape's 256)."""
+    import oracle
+    res = {}
+    for name, w in inputs.WORKLOADS.items():
+        if name == "n4096":
+            continue                           # the main figure above
+        A, B = inputs.operands(w)
+        A64, B64 = oracle.to_float64(A), oracle.to_float64(B)
+        rows = inputs.check_rows(w).tolist()
+        t0 = time.perf_counter()
+        if len(rows) == w.M:
+            oracle.gemm(A64, B64)
+        else:
+            oracle.gemm_rows(A64, B64, rows)
+        dt = time.perf_counter() - t0
+        res[name] = {"rows": len(rows), "seconds": round(dt, 3),
+                     "tflops": round(2.0 * len(rows) * w.N * w.K / dt / 1e12, 6)}
+    res["cores"] = threads
+    return res
+
+
 # ---------------------------------------------------------------- GPU arm
 
 def event_pair():
@@ -369,7 +392,8 @@ def run_gpu(args):
                 f"the whole 4096^3 product, {passes} times")
         out["cpu_baseline"] = {
             "value": round(rate, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{what} (double accumulation), {dt:.1f} s"}
+            "sample": f"{what} (double accumulation), {dt:.1f} s",
+            "workloads": oracle_workloads(inputs, threads)}
     if rank == 0:
         print(json.dumps(out), flush=True)
     if ws > 1:
