@@ -112,7 +112,8 @@ TGEMM_API int gemm_f32(int M, int N, int K,
  * Tensor Memory Accelerator, which needs rows that start on 16-byte
  * boundaries: an operand whose pointer or leading dimension breaks that
  * (any lda, ldb and element-aligned pointer are accepted) is first repacked
- * by an HBM-bound kernel into stream-ordered scratch with 16-byte rows; for
+ * by an HBM-bound kernel into stream-ordered scratch with rows on 128-byte
+ * boundaries; for
  * TF32, B is always rewritten transposed (the TF32 kind reads B only
  * K-major), which also absorbs any alignment of B. Rows and columns past M,
  * N, K read as zero.

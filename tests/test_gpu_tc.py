@@ -143,6 +143,28 @@ def test_ragged_edges_with_nan_padding(tgemm, kind):
 
 
 @pytest.mark.parametrize("kind", ["tf32", "bf16"])
+@pytest.mark.parametrize("ldc,offset", [(521, 0), (522, 1), (523, 3), (524, 1)])
+def test_unaligned_output_rows_every_phase(tgemm, tc_mode, kind, ldc, offset):
+    """C rows that start 4, 8 or 12 bytes past a 16-byte boundary (every
+    phase occurs across the rows): each row's values before its first 16-byte
+    boundary are stored one by one, the rest as 16-byte vectors. Bit-exact on
+    integers; the padding columns and the guard bands stay untouched."""
+    M, N, K = 300, 520, 64
+    A, B = operands(M, N, K, "int4", kind, seed=ldc + offset)
+    guard = 64
+    store = torch.full((guard + offset + M * ldc + guard,), -555.0, device="cuda")
+    base = guard + offset
+    C = store[base:base + M * ldc].view(M, ldc)[:, :N]
+    tgemm.gemm_tc(A.cuda(), B.cuda(), kind, out=C)
+    assert tgemm.device_status() == 0
+    C_ref, _ = oracle.gemm(A, B)
+    assert_bit_exact(C, C_ref, f"{kind} ldc={ldc} offset={offset}")
+    host = store.cpu()
+    assert (host[:base] == -555.0).all() and (host[base + M * ldc:] == -555.0).all()
+    assert (host[base:base + M * ldc].view(M, ldc)[:, N:] == -555.0).all()
+
+
+@pytest.mark.parametrize("kind", ["tf32", "bf16"])
 @pytest.mark.parametrize("shape", [(16, 12, 12), (130, 261, 77), (300, 1001, 517)])
 def test_unaligned_leading_dimensions(tgemm, tc_mode, kind, shape):
     """Packed operands whose rows do not start on 16-byte boundaries: the
