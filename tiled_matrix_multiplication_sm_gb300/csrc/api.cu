@@ -42,15 +42,6 @@ std::atomic<int> g_tc_mode{-1};
 thread_local const char* g_last_kernel = "";
 thread_local char g_last_kernel_buf[160];
 
-// Name of an FP32 launch: the configuration, plus the reduction kernel when
-// the plan splits the last wave along K.
-const char* f32_launch_name(int id, const tgemm::F32Plan& plan) {
-    if (plan.split <= 1) return tgemm::f32_kernel_name(id);
-    snprintf(g_last_kernel_buf, sizeof(g_last_kernel_buf), "%s+splitk_reduce(split=%d)",
-             tgemm::f32_kernel_name(id), plan.split);
-    return g_last_kernel_buf;
-}
-
 // Device properties of the current device, looked up once per device.
 int current_device_info(DeviceInfo* out) {
     int dev = 0;
