@@ -48,31 +48,31 @@ transpose_kernel(const T* __restrict__ B, long ldb, T* __restrict__ Bt, long ldt
 // leading dimension ld_src to ld_dst (both in elements). Used to give the
 // tensor-memory copies rows that start on 16-byte boundaries.
 // Each block copies REPACK_ROWS rows of one REPACK_COLS-wide column chunk;
-// every thread keeps four loads in flight (columns c, c + 256, c + 512,
-// c + 768) before it stores.
-constexpr int REPACK_ROWS = 4;
-constexpr int REPACK_COLS = 4096;
+// every thread issues all of its loads (REPACK_ROWS rows x 4 columns, 256
+// apart) before its stores, so that 8 loads per thread are in flight. (With
+// 4 rows copied one after the other, 3000 x 1537 floats moved at 3.6 TB/s.)
+constexpr int REPACK_ROWS = 2;
+constexpr int REPACK_COLS = 1024;
 
 template <typename T>
 __global__ void __launch_bounds__(256)
 repack_kernel(const T* __restrict__ src, long ld_src, T* __restrict__ dst, long ld_dst, int rows,
               int cols) {
     const int r0 = blockIdx.x * REPACK_ROWS;
-    const int c0 = blockIdx.y * REPACK_COLS;
-    const int c1 = cols - c0 < REPACK_COLS ? cols : c0 + REPACK_COLS;
-    for (int r = r0; r < rows && r < r0 + REPACK_ROWS; ++r) {
-        const T* s = src + (long)r * ld_src;
-        T* d = dst + (long)r * ld_dst;
-        int c = c0 + threadIdx.x;
-        for (; c + 768 < c1; c += 1024) {
-            const T v0 = s[c], v1 = s[c + 256], v2 = s[c + 512], v3 = s[c + 768];
-            d[c] = v0;
-            d[c + 256] = v1;
-            d[c + 512] = v2;
-            d[c + 768] = v3;
-        }
-        for (; c < c1; c += 256) d[c] = s[c];
-    }
+    const int c = blockIdx.y * REPACK_COLS + threadIdx.x;
+    T v[REPACK_ROWS][4];
+#pragma unroll
+    for (int i = 0; i < REPACK_ROWS; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (r0 + i < rows && c + 256 * j < cols)
+                v[i][j] = src[(long)(r0 + i) * ld_src + c + 256 * j];
+#pragma unroll
+    for (int i = 0; i < REPACK_ROWS; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (r0 + i < rows && c + 256 * j < cols)
+                dst[(long)(r0 + i) * ld_dst + c + 256 * j] = v[i][j];
 }
 
 // x rounded to the TF32 format (10 explicit mantissa bits), to nearest with
