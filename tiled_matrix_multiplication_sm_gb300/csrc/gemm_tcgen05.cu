@@ -517,6 +517,28 @@ __device__ __forceinline__ void store_accumulator(const TcParams& p, const Unit&
     }
 }
 
+// Sum of `n` float4 at src, src + stride, ... in that order; the loads of
+// four pieces are issued before their adds, so that they are in flight
+// together.
+__device__ __forceinline__ float4 sum_pieces(const float* src, long stride, int n) {
+    float4 s = *reinterpret_cast<const float4*>(src);
+    for (int j = 1; j < n; j += 4) {
+        float4 v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (j + q < n) v[q] = *reinterpret_cast<const float4*>(src + (j + q) * stride);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (j + q < n) {
+                s.x += v[q].x;
+                s.y += v[q].y;
+                s.z += v[q].z;
+                s.w += v[q].w;
+            }
+    }
+    return s;
+}
+
 // Sum the K-pieces of every split tile, piece 0 first, into C.
 __global__ void __launch_bounds__(256)
 tc_splitk_reduce(const TcParams p) {
@@ -535,14 +557,7 @@ tc_splitk_reduce(const TcParams p) {
         const int grow = mb * p.tile_rows + row, gcol = nb * p.tile_cols + c4;
         if (grow >= p.M || gcol >= p.N) continue;
         const float* src = p.partials + (long)r * p.split * piece_floats + (long)row * p.tile_cols + c4;
-        float4 s = *reinterpret_cast<const float4*>(src);
-        for (int j = 1; j < p.split; ++j) {
-            const float4 v = *reinterpret_cast<const float4*>(src + j * piece_floats);
-            s.x += v.x;
-            s.y += v.y;
-            s.z += v.z;
-            s.w += v.w;
-        }
+        const float4 s = sum_pieces(src, piece_floats, p.split);
         float* dst = p.C + (long)grow * p.ldc + gcol;
         float v[4] = {s.x, s.y, s.z, s.w};
         if (!p.ep_simple)

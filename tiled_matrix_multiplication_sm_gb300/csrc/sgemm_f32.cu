@@ -402,13 +402,22 @@ splitk_reduce(const F32Params p) {
         const int grow = tm * T::BM + row, gcol = tn * T::BN + c4;
         if (grow >= p.M || gcol >= p.N) continue;
         const float* src = p.partials + (long)r * p.split * (T::BM * T::BN) + row * T::BN + c4;
+        constexpr long kPiece = (long)T::BM * T::BN;
+        // Pieces in order; four loads in flight before their adds.
         float4 s = *reinterpret_cast<const float4*>(src);
-        for (int j = 1; j < p.split; ++j) {
-            const float4 v = *reinterpret_cast<const float4*>(src + (long)j * (T::BM * T::BN));
-            s.x += v.x;
-            s.y += v.y;
-            s.z += v.z;
-            s.w += v.w;
+        for (int j = 1; j < p.split; j += 4) {
+            float4 v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (j + q < p.split) v[q] = *reinterpret_cast<const float4*>(src + (j + q) * kPiece);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (j + q < p.split) {
+                    s.x += v[q].x;
+                    s.y += v[q].y;
+                    s.z += v[q].z;
+                    s.w += v[q].w;
+                }
         }
         float* dst = p.C + (long)grow * p.ldc + gcol;
         float v[4] = {s.x, s.y, s.z, s.w};
