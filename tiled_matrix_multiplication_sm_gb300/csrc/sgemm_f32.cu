@@ -238,18 +238,29 @@ __device__ __forceinline__ void mma_phase(Acc<T>& acc, const float* as, const fl
 #pragma unroll
             for (int g = 0; g < T::NG; ++g)
                 b[g] = *reinterpret_cast<const float4*>(bs + (k4 + kk) * T::BLD + g * 32);
+            if constexpr (T::PACKED) {
+                // (a, a) pairs of this k for all rows first, then the column
+                // pairs one by one, each multiplied into every row: each run
+                // of TM two-wide FMAs shares its B pair. (Row by row instead,
+                // with each row's pair built where it is used, measured
+                // 57.4 against 58.1 TFLOP/s on 4096^3.)
+                float2 a2[T::TM];
 #pragma unroll
-            for (int i = 0; i < T::TM; ++i) {
-                const float av = pick(a[i], kk);
-                if constexpr (T::PACKED) {
-                    const float2 a2 = make_float2(av, av);
+                for (int i = 0; i < T::TM; ++i) {
+                    const float av = pick(a[i], kk);
+                    a2[i] = make_float2(av, av);
+                }
 #pragma unroll
-                    for (int g = 0; g < T::NG; ++g) {
-                        acc.v[i][2 * g] = __ffma2_rn(a2, make_float2(b[g].x, b[g].y), acc.v[i][2 * g]);
-                        acc.v[i][2 * g + 1] =
-                            __ffma2_rn(a2, make_float2(b[g].z, b[g].w), acc.v[i][2 * g + 1]);
-                    }
-                } else {
+                for (int h = 0; h < T::TN / 2; ++h) {
+                    const float4& bg = b[h / 2];
+                    const float2 bp = (h % 2) ? make_float2(bg.z, bg.w) : make_float2(bg.x, bg.y);
+#pragma unroll
+                    for (int i = 0; i < T::TM; ++i) acc.v[i][h] = __ffma2_rn(a2[i], bp, acc.v[i][h]);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < T::TM; ++i) {
+                    const float av = pick(a[i], kk);
 #pragma unroll
                     for (int g = 0; g < T::NG; ++g) {
                         acc.v[i][2 * g].x = fmaf(av, b[g].x, acc.v[i][2 * g].x);
