@@ -114,3 +114,23 @@ def test_calls_in_flight_together_on_two_streams(tgemm):
     for A, B, C, path in jobs:
         C_ref, _ = oracle.gemm(A, B)
         assert_bit_exact(C, C_ref, f"async host {path} {tuple(A.shape)}")
+
+
+@pytest.mark.parametrize("path,M,panels", [("f32", 512, 1), ("f32", 1024, 3), ("f32", 1300, 3),
+                                           ("f32", 2048, 4), ("f32", 2333, 4), ("tf32", 1024, 2),
+                                           ("tf32", 2333, 4), ("bf16", 2048, 4)])
+def test_row_panels(tgemm, path, M, panels):
+    """The row-panel schedule: FP32 (compute-bound) takes a 256-row first
+    panel, a 256-511-row last panel and one or two panels between; the
+    tensor paths (bound by the CPU-GPU link) take 2 or 4 equal panels. Every
+    boundary row and every panel's first and last rows come out bit-exact."""
+    N, K = 136, 72
+    g = inputs.generator(M + N + K)
+    A = inputs.draw(M, K, "int4", g).to(DTYPE[path]).pin_memory()
+    B = inputs.draw(K, N, "int4", g).to(DTYPE[path]).pin_memory()
+    C = tgemm.matmul(A, B, path)
+    assert tgemm.binding.last_kernel().startswith(f"host_pipeline(panels={panels})"), \
+        tgemm.binding.last_kernel()
+    assert tgemm.device_status() == 0
+    C_ref, _ = oracle.gemm(A, B)
+    assert_bit_exact(C, C_ref, f"host panels {path} M={M}")
