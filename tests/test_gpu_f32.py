@@ -239,11 +239,11 @@ def test_matmul_host_round_trip(tgemm):
 
 
 @pytest.mark.parametrize("M,tile", [(1, "16x256"), (16, "16x256"), (40, "32x256"), (96, "32x256"),
-                                    (128, "128x256"), (192, "32x256"), (256, "128x256")])
+                                    (128, "128x128"), (192, "32x256"), (256, "128x128")])
 def test_few_rows_take_short_tiles(tgemm, M, tile):
     """By shape, products with few rows take 16- or 32-row tiles (no FMAs on
     rows far past M); results stay bit-exact on integer data."""
-    N, K = 600, 300
+    N, K = 2048, 700
     g = inputs.generator(4000 + M)
     A = inputs.draw(M, K, "int4", g)
     B = inputs.draw(K, N, "int4", g)
@@ -251,3 +251,23 @@ def test_few_rows_take_short_tiles(tgemm, M, tile):
     assert tgemm.binding.last_kernel().startswith("f32_" + tile), tgemm.binding.last_kernel()
     C_ref, _ = oracle.gemm(A, B)
     assert_bit_exact(C, C_ref, f"few rows M={M}")
+
+
+@pytest.mark.parametrize("shape,tile", [((128, 128, 128), "64x64"), ((384, 384, 384), "64x64"),
+                                        ((512, 512, 512), "64x64"), ((256, 256, 4096), "64x64"),
+                                        ((640, 640, 640), "128x128"), ((1024, 256, 1024), "128x128"),
+                                        ((2048, 2048, 256), "128x128"), ((1024, 1024, 1024), "128x256"),
+                                        ((4096, 4096, 8), "128x256")])
+def test_small_products_take_smaller_tiles(tgemm, shape, tile):
+    """Products whose 128 x 256 tiles would not fill one wave of the GPU take
+    64 x 64 or 128 x 128 tiles by a rule fitted to measurements; results stay
+    bit-exact on integer data."""
+    M, N, K = shape
+    g = inputs.generator(M + 5 * N + 11 * K)
+    A = inputs.draw(M, K, "int4", g)
+    B = inputs.draw(K, N, "int4", g)
+    C = run_f32(tgemm, A.cuda(), B.cuda())
+    assert tgemm.binding.last_kernel().startswith("f32_" + tile), tgemm.binding.last_kernel()
+    rows = sorted(set([0, M - 1] + torch.randint(0, M, (40,), generator=g).tolist()))
+    C_ref, _ = oracle.gemm_rows(A, B, rows)
+    assert_bit_exact(C.cpu()[rows], C_ref, f"small product {shape}")

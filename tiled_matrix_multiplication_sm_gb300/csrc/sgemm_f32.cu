@@ -517,6 +517,8 @@ const Entry kTable[] = {
     TGEMM_ENTRY("f32_32x256x32_s3_ffma2_2blk_vecA_vecB", Skinny32, true, true),
     TGEMM_ENTRY("f32_16x256x32_s3_ffma2_2blk_vecA_vecB", Skinny16, true, true),
 };
+constexpr int kBig32 = 5;
+constexpr int kSmall = 9;
 constexpr int kSkinny32 = 11;
 constexpr int kSkinny16 = 12;
 constexpr int kTableSize = sizeof(kTable) / sizeof(kTable[0]);
@@ -580,7 +582,6 @@ bool f32_kernel_accepts(int id, const GemmArgs& a) {
 }
 
 int f32_select(const GemmArgs& a, int num_sms) {
-    (void)num_sms;
     const bool va = vec_ok(a.A, a.lda), vb = vec_ok(a.B, a.ldb);
     if (va && vb && a.M > 0) {
         // Few rows: the 128-row tile spends its FMAs on rows past M. Measured
@@ -592,6 +593,21 @@ int f32_select(const GemmArgs& a, int num_sms) {
         const long wide_rows = ((long)a.M + 127) / 128 * 128;
         const long skinny_rows = ((long)a.M + 31) / 32 * 32;
         if (a.M <= 96 || (a.M < 512 && wide_rows * 100 > skinny_rows * 115)) return kSkinny32;
+        // Small products, where the 128 x 256 tiles cannot fill the GPU. Measured
+        // (us, L2 flushed; 128 x 256 / 128 x 128 / 64 x 64 tiles): 128^3 43.6 /
+        // 19.1 / 12.9, 512^3 34.5 / 24.2 / 20.1, 768^3 38.1 / 30.3 / 34.4,
+        // 2048 x 2048 x 256 66.2 / 58.0 / 58.0, 256 x 256 x 4096 57.0 / 37.5 /
+        // 30.4, 1024^3 59.0 / 60.6 / 73.4. While the 128 x 256 tiles fill
+        // less than one wave: up to 512^3 of work, or a K at least 8 times
+        // both M and N, 64 x 64 tiles; otherwise 128 x 128 tiles, except
+        // for K >= 1024 with at least 32 of the 128 x 256 tiles.
+        const long tiles_wide = ((long)a.M + 127) / 128 * (((long)a.N + 255) / 256);
+        if (tiles_wide < num_sms) {
+            const long mnk = (long)a.M * a.N * a.K;
+            if (mnk <= 512L * 512 * 512 || ((long)a.K >= 8L * a.M && (long)a.K >= 8L * a.N))
+                return kSmall;
+            if (!(a.K >= 1024 && tiles_wide >= 32)) return kBig32;
+        }
     }
     return (va ? 0 : 2) + (vb ? 0 : 1);
 }
