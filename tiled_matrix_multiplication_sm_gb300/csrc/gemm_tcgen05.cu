@@ -427,8 +427,8 @@ __device__ __forceinline__ void store_row32_peeled(float* d, const uint32_t (&r)
 // stores, after peeling the values before the first 16-byte boundary when
 // C's rows are not 16-byte aligned. (Staging each 32 x 32 block through
 // shared memory to store it as 32 coalesced row segments instead measured
-// 20 % slower on 3072 x 5120 x 1536 TF32: the staging's shared-memory
-// traffic competes with the MMAs' operand reads.)
+// 9 % slower on 3072 x 5120 x 1536 TF32 with ldc = 5121: the staging's
+// shared-memory traffic competes with the MMAs' operand reads.)
 __device__ __forceinline__ void store_accumulator(const TcParams& p, const Unit& w, int mb, int nb,
                                                  int row_in_tile, uint32_t taddr, float* stage,
                                                  const CUtensorMap* tmC, int c_begin, int c_end) {
@@ -436,12 +436,13 @@ __device__ __forceinline__ void store_accumulator(const TcParams& p, const Unit&
     const int lane = threadIdx.x & 31;
     if (w.piece < 0 && p.tma_c) {
         // Whole tile, beta = 0: alpha and bias are applied in registers, then
-        // each 32 x 32 block goes to one of the warp's two staging buffers in
-        // the 128-byte-swizzled layout of the C tensor map (row i holds 128
-        // bytes, 16-byte chunk j at j ^ (i % 8)) and leaves as one TMA store,
-        // which also clips rows and columns past M and N. The next block's
-        // TMEM load is in flight while a block is staged, and a buffer is
-        // reused once the store issued two blocks earlier has read it.
+        // each 32 x 32 block goes to the warp's staging buffer (EPI_BUFS of
+        // them) in the 128-byte-swizzled layout of the C tensor map (row i
+        // holds 128 bytes, 16-byte chunk j at j ^ (i % 8)) and leaves as one
+        // TMA store, which also clips rows and columns past M and N. The next
+        // block's TMEM load is in flight while a block is staged, and a
+        // buffer is reused once the store issued EPI_BUFS blocks earlier has
+        // read it.
         const int row0 = row - lane;
         if (row0 >= p.M) return;                        // the warp's rows are all past M
         const int n_blocks = (p.N - nb * p.tile_cols + 31) / 32;   // blocks with columns < N
