@@ -185,7 +185,9 @@ TGEMM_API int gemm_ex(int M, int N, int K,
  * overlaps the transfers with the multiplication: B is copied first, A
  * follows in up to four row panels on a copy stream (on the FP32 path a
  * short first and last panel, so that the arithmetic starts early and little
- * of C is left to copy out at the end), each panel is
+ * of C is left to copy out at the end; there B goes up in two column halves
+ * and the first panel is multiplied in the same halves, the left one as soon
+ * as it has arrived), each panel is
  * multiplied on `stream` as soon as its rows have arrived (the TF32 path
  * transposes B once for all panels; TF32X3 splits B once and each panel of
  * A as it arrives), and each panel of C is copied back on a second copy

@@ -134,3 +134,21 @@ def test_row_panels(tgemm, path, M, panels):
     assert tgemm.device_status() == 0
     C_ref, _ = oracle.gemm(A, B)
     assert_bit_exact(C, C_ref, f"host panels {path} M={M}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1100, 777, 150), (2300, 1536, 96)])
+def test_fp32_first_panel_in_column_halves(tgemm, M, N, K):
+    """On the FP32 path B goes up in two column halves and the first row
+    panel is multiplied in the same halves (the left one as soon as it has
+    arrived). Padded host layouts; every output bit-exact; C's padding
+    columns untouched."""
+    g = inputs.generator(M * 7 + N + K)
+    A = host_padded(inputs.draw(M, K, "int4", g), K + 3)
+    B = host_padded(inputs.draw(K, N, "int4", g), N + 5)
+    Cstore = torch.full((M, N + 7), 999.0, pin_memory=True)
+    C = Cstore[:, :N]
+    tgemm.binding.gemm_host(A, B, "f32", out=C)
+    assert tgemm.device_status() == 0
+    C_ref, _ = oracle.gemm(A, B)
+    assert_bit_exact(C, C_ref, f"host halves {M}x{N}x{K}")
+    assert (Cstore[:, N:] == 999.0).all()

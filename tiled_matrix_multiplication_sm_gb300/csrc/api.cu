@@ -511,6 +511,11 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
     // short first and last panels, 3.13 ms with four equal ones.
     long bounds[kMaxPanels + 1];
     const int panels = host_panels(M, path == TGEMM_PATH_F32, bounds);
+    // FP32 (compute-bound): B goes up in two column halves, and the first
+    // panel is multiplied in the same halves, its left half as soon as B's
+    // left columns and the panel's rows have arrived. nh: the left half's
+    // width, a multiple of 256 columns (0: B in one piece).
+    const long nh = (path == TGEMM_PATH_F32 && panels > 1 && K > 0) ? (long)(N / 2) / 256 * 256 : 0;
 
     // Plans and scratch: one pool block for A, B, C, B transposed (TF32: one
     // copy; TF32X3: its high and low parts), the high and low parts of A
@@ -526,8 +531,9 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
     size_t off_t = off_c + align256((size_t)M * ldc_d * 4);
     size_t off_a2 = off_t + (path == TGEMM_PATH_TF32 ? bt_bytes : x3 ? 2 * bt_bytes : 0);
     size_t off_p = off_a2 + (x3 ? 2 * a_bytes : 0);
-    int f32_id[kMaxPanels] = {};
-    tgemm::F32Plan f32_plan[kMaxPanels];
+    int f32_id[kMaxPanels] = {}, f32_id_right = 0;
+    tgemm::F32Plan f32_plan[kMaxPanels], f32_plan_right;
+    size_t part_off_right = 0;
     tgemm::TcPlan tc_plan[kMaxPanels];
     int shape[kMaxPanels] = {};
     size_t part_off[kMaxPanels];
@@ -542,13 +548,22 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
             total += align256(tc_plan[i].scratch_bytes);
         } else {
             // Device operands are 16-byte aligned: the vector loaders apply.
-            tgemm::GemmArgs pa{rows, N, K, nullptr, lda_d, nullptr, ldb_d, nullptr, ldc_d};
             const int forced = g_forced_f32.load();
-            tgemm::GemmArgs chk = pa;
-            chk.A = chk.B = reinterpret_cast<const void*>(256);   // scratch: 16-byte aligned
-            f32_id[i] = forced >= 0 ? forced : tgemm::f32_select(chk, dev.num_sms);
-            f32_plan[i] = tgemm::f32_plan(f32_id[i], pa, dev.num_sms);
-            total += align256(f32_plan[i].scratch_bytes);
+            auto plan = [&](int cols, int& id, tgemm::F32Plan& pl) {
+                tgemm::GemmArgs pa{rows, cols, K, nullptr, lda_d, nullptr, ldb_d, nullptr, ldc_d};
+                tgemm::GemmArgs chk = pa;
+                chk.A = chk.B = reinterpret_cast<const void*>(256);   // scratch: 16-byte aligned
+                id = forced >= 0 ? forced : tgemm::f32_select(chk, dev.num_sms);
+                pl = tgemm::f32_plan(id, pa, dev.num_sms);
+                total += align256(pl.scratch_bytes);
+            };
+            if (i == 0 && nh > 0) {
+                plan((int)nh, f32_id[0], f32_plan[0]);
+                part_off_right = total;
+                plan(N - (int)nh, f32_id_right, f32_plan_right);
+            } else {
+                plan(N, f32_id[i], f32_plan[i]);
+            }
         }
     }
     void* ws = nullptr;
@@ -562,17 +577,17 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
     float* A_hi = reinterpret_cast<float*>(base + off_a2);               // TF32X3
     float* A_lo = reinterpret_cast<float*>(base + off_a2 + a_bytes);
 
-    const int nev = 2 * panels + 3;
-    cudaEvent_t ev[2 * kMaxPanels + 3];
+    const int nev = 2 * panels + 4;
+    cudaEvent_t ev[2 * kMaxPanels + 4];
     for (int i = 0; i < nev; ++i)
         if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) {
             for (int j = 0; j < i; ++j) cudaEventDestroy(ev[j]);
             cudaFreeAsync(ws, stream);
             return TGEMM_ERR_CUDA;
         }
-    cudaEvent_t ev_ready = ev[0], ev_b = ev[1], ev_out = ev[2];
-    cudaEvent_t* ev_a = ev + 3;
-    cudaEvent_t* ev_c = ev + 3 + panels;
+    cudaEvent_t ev_ready = ev[0], ev_b = ev[1], ev_out = ev[2], ev_b_left = ev[3];
+    cudaEvent_t* ev_a = ev + 4;
+    cudaEvent_t* ev_c = ev + 4 + panels;
     int rc = TGEMM_OK;
     auto ok = [&](cudaError_t e) {
         if (e != cudaSuccess && rc == TGEMM_OK) rc = TGEMM_ERR_CUDA;
@@ -587,10 +602,14 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
     ok(cudaEventRecord(ev_ready, stream));
     ok(cudaStreamWaitEvent(s_in, ev_ready, 0));
     ok(cudaStreamWaitEvent(s_out, ev_ready, 0));
+    // Upload order: B (or B's left columns), then each panel of A, B's
+    // right columns right after the first panel.
+    const long n_first = nh > 0 ? nh : N;
     if (K > 0)
-        ok(cudaMemcpy2DAsync(Bd, ldb_d * esz, B, ldb * esz, N * esz, K, cudaMemcpyHostToDevice,
-                             s_in));
-    ok(cudaEventRecord(ev_b, s_in));
+        ok(cudaMemcpy2DAsync(Bd, ldb_d * esz, B, ldb * esz, n_first * esz, K,
+                             cudaMemcpyHostToDevice, s_in));
+    ok(cudaEventRecord(ev_b_left, s_in));
+    if (nh == 0) ok(cudaEventRecord(ev_b, s_in));
     for (int i = 0; i < panels; ++i) {
         const long r0 = bounds[i], rows = bounds[i + 1] - bounds[i];
         if (K > 0)
@@ -598,8 +617,14 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
                                  static_cast<const char*>(A) + r0 * lda * esz, lda * esz, K * esz,
                                  rows, cudaMemcpyHostToDevice, s_in));
         ok(cudaEventRecord(ev_a[i], s_in));
+        if (i == 0 && nh > 0) {
+            ok(cudaMemcpy2DAsync(Bd + nh * esz, ldb_d * esz,
+                                 static_cast<const char*>(B) + nh * esz, ldb * esz,
+                                 (N - nh) * esz, K, cudaMemcpyHostToDevice, s_in));
+            ok(cudaEventRecord(ev_b, s_in));
+        }
     }
-    ok(cudaStreamWaitEvent(stream, ev_b, 0));
+    ok(cudaStreamWaitEvent(stream, nh > 0 ? ev_b_left : ev_b, 0));
     if (rc == TGEMM_OK && path == TGEMM_PATH_TF32 && K > 0)
         ok(tgemm::transpose_f32(reinterpret_cast<const float*>(Bd), ldb_d, Bt, ldt, K, N, stream));
     if (rc == TGEMM_OK && x3 && K > 0)
@@ -634,6 +659,16 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
             ok(tgemm::tc_launch(pa, in_type, tf32 ? 1 : 0, dev.num_sms, enc, limit, stall, shape[i],
                                 tc_plan[i], part, stream));
             name = tgemm::tc_kernel_name(in_type, shape[i]);
+        } else if (i == 0 && nh > 0) {
+            // The first panel in B's two column halves.
+            tgemm::GemmArgs left{rows, (int)nh, K, Ad, lda_d, Bd, ldb_d, Cp, ldc_d};
+            ok(tgemm::f32_launch(f32_id[0], left, f32_plan[0], part, stream));
+            ok(cudaStreamWaitEvent(stream, ev_b, 0));
+            tgemm::GemmArgs right{rows, N - (int)nh, K, Ad, lda_d, Bd + nh * esz, ldb_d,
+                                  Cp + nh, ldc_d};
+            ok(tgemm::f32_launch(f32_id_right, right, f32_plan_right,
+                                 reinterpret_cast<float*>(base + part_off_right), stream));
+            name = tgemm::f32_kernel_name(f32_id_right);
         } else {
             tgemm::GemmArgs pa{rows, N, K, Ad + r0 * lda_d * esz, lda_d, Bd, ldb_d, Cp, ldc_d};
             ok(tgemm::f32_launch(f32_id[i], pa, f32_plan[i], part, stream));
