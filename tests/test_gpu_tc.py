@@ -321,3 +321,24 @@ def test_workload_n4096_tf32x3_sampled_rows(tgemm):
     C_ref, absAB = oracle.gemm_rows(A, B, rows)
     from tests.parity import F32_ABS, F32_REL
     assert_within(C[rows], C_ref, absAB, F32_REL, F32_ABS, "n4096 tf32x3")
+
+
+def test_auto_shape_prefers_narrow_tiles_for_unaligned_output_rows(tgemm):
+    """The wide tiles' single accumulator leaves part of each epilogue
+    exposed, more so when C's rows are not 16-byte aligned (no TMA stores):
+    4096 x 14336 x 4096 BF16 takes 256 x 512 tiles with ldc = N and
+    256 x 256 tiles with ldc = N + 1. Sampled rows checked in both layouts."""
+    M, N, K = 4096, 14336, 4096
+    g = inputs.generator(4242)
+    A = inputs.draw(M, K, "normal002", g).to(torch.bfloat16)
+    B = inputs.draw(K, N, "normal002", g).to(torch.bfloat16)
+    Ad, Bd = A.cuda(), B.cuda()
+    rows = [0, 255, 256, 4095] + torch.randint(0, M, (4,), generator=g).tolist()
+    C_ref, absAB = oracle.gemm_rows(A, B, rows)
+    for ldc, tile in ((N, "256x512"), (N + 1, "256x256")):
+        C = torch.empty(M, ldc, device="cuda")[:, :N]
+        tgemm.gemm_tc(Ad, Bd, "bf16", out=C)
+        assert tgemm.device_status() == 0
+        assert tile in tgemm.binding.last_kernel(), (ldc, tgemm.binding.last_kernel())
+        assert_within(C.cpu()[rows], C_ref, absAB, TC_REL, TC_ABS, f"ldc={ldc}")
+        del C

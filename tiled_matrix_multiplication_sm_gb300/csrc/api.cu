@@ -305,8 +305,12 @@ int run_product(const Request& r, cudaStream_t stream) {
         }
         fplan = tgemm::f32_plan(f32_id, probe, dev.num_sms);
     } else {
-        shape = tgemm::tc_shape(M, N, K, path, g_tc_mode.load(), dev.num_sms, true);
-        tplan = tgemm::tc_plan(M, N, K, path, shape, dev.num_sms, true);
+        // Whole tiles leave by TMA stores when C's base and rows are 16-byte
+        // aligned and beta = 0 (the model charges the wide tiles more otherwise).
+        const bool tma_c = reinterpret_cast<uintptr_t>(r.C) % 16 == 0 && r.ldc % 4 == 0 &&
+                           r.ep.beta == 0.0f;
+        shape = tgemm::tc_shape(M, N, K, path, g_tc_mode.load(), dev.num_sms, true, tma_c);
+        tplan = tgemm::tc_plan(M, N, K, path, shape, dev.num_sms, true, tma_c);
     }
     const size_t part_bytes = f32 ? fplan.scratch_bytes : tplan.scratch_bytes;
     const size_t p_off = part_bytes ? cv.take(part_bytes) : 0;

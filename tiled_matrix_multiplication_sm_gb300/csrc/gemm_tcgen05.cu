@@ -1379,17 +1379,23 @@ struct TileModel {
     double main_us, epi_us;
 };
 
-TileModel tile_model(int in_type, int shape, int tile_rows, int tile_cols, int K) {
+TileModel tile_model(int in_type, int shape, int tile_rows, int tile_cols, int K, bool tma_c) {
     double tflops = shape == TC_ONE_SM ? 9.3 : shape == TC_PAIR ? 22.8 : 30.0;   // BF16
     if (in_type != TC_BF16) tflops *= 0.5;                                      // TF32 rate
     if (in_type == TC_TF32X3) tflops /= 3.0;                                    // three products
     TileModel m;
     m.main_us = 2.0 * tile_rows * tile_cols * (double)K / (tflops * 1e6);
-    m.epi_us = shape == TC_PAIR_WIDE ? 6.5 : 0.0;
+    // The wide tiles' single accumulator leaves part of each epilogue exposed:
+    // ~6.5 us with TMA stores, more with per-thread stores when C's rows are
+    // not 16-byte aligned (8192 x 14336 x 4096 BF16 with ldc = 14337: wide
+    // 660 us against narrow 603; fitted together with 4096^3 TF32 and BF16,
+    // where the two shapes come within 3 %).
+    m.epi_us = shape == TC_PAIR_WIDE ? (tma_c ? 6.5 : 12.0) : 0.0;
     return m;
 }
 
-TcPlan tc_plan(int M, int N, int K, int in_type, int shape, int num_sms, bool allow_split) {
+TcPlan tc_plan(int M, int N, int K, int in_type, int shape, int num_sms, bool allow_split,
+               bool tma_c) {
     if (in_type == TC_TF32X3) shape = TC_PAIR;   // the split form: 256 x 256 CTA-pair tiles only
     const bool pair = shape != TC_ONE_SM;
     TcPlan pl;
@@ -1401,7 +1407,7 @@ TcPlan tc_plan(int M, int N, int K, int in_type, int shape, int num_sms, bool al
     pl.kblocks = (K + bk - 1) / bk;
     const int tiles = pl.tiles_m * pl.tiles_n;
     const int slots = pair ? num_sms / 2 : num_sms;
-    const TileModel tm = tile_model(in_type, shape, pl.tile_rows, pl.tile_cols, K);
+    const TileModel tm = tile_model(in_type, shape, pl.tile_rows, pl.tile_cols, K, tma_c);
     const double tile_us = tm.main_us + tm.epi_us;
     const double tile_bytes = (double)pl.tile_rows * pl.tile_cols * sizeof(float);
     pl.dp_tiles = tiles;
@@ -1426,7 +1432,8 @@ TcPlan tc_plan(int M, int N, int K, int in_type, int shape, int num_sms, bool al
     return pl;
 }
 
-int tc_shape(int M, int N, int K, int in_type, int mode, int num_sms, bool allow_split) {
+int tc_shape(int M, int N, int K, int in_type, int mode, int num_sms, bool allow_split,
+             bool tma_c) {
     if (in_type == TC_TF32X3) return TC_PAIR;
     if (mode == 0) return TC_ONE_SM;
     if (mode == 1) return TC_PAIR;
@@ -1435,8 +1442,8 @@ int tc_shape(int M, int N, int K, int in_type, int mode, int num_sms, bool allow
     if (N <= BN) return TC_PAIR;
     // The shape the timing model expects to finish first; near-ties go to
     // the narrow tiles, whose epilogue is hidden.
-    const TcPlan narrow = tc_plan(M, N, K, in_type, TC_PAIR, num_sms, allow_split);
-    const TcPlan wide = tc_plan(M, N, K, in_type, TC_PAIR_WIDE, num_sms, allow_split);
+    const TcPlan narrow = tc_plan(M, N, K, in_type, TC_PAIR, num_sms, allow_split, tma_c);
+    const TcPlan wide = tc_plan(M, N, K, in_type, TC_PAIR_WIDE, num_sms, allow_split, tma_c);
     return wide.est_us < 0.97 * narrow.est_us ? TC_PAIR_WIDE : TC_PAIR;
 }
 

@@ -75,8 +75,9 @@ enum TcType { TC_TF32 = 1, TC_BF16 = 2, TC_TF32X3 = 3 };
 enum TcShape { TC_ONE_SM = 0, TC_PAIR = 1, TC_PAIR_WIDE = 2 };
 // The shape a product runs with: mode -1 = the shape a timing model expects
 // to finish first, 0/1/2 = that TcShape (the split-TF32 form always takes
-// TC_PAIR). allow_split as for tc_plan.
-int tc_shape(int M, int N, int K, int in_type, int mode, int num_sms, bool allow_split);
+// TC_PAIR). allow_split and tma_c as for tc_plan.
+int tc_shape(int M, int N, int K, int in_type, int mode, int num_sms, bool allow_split,
+             bool tma_c = true);
 const char* tc_kernel_name(int in_type, int shape);
 // Tiling of one tensor-core product: tiles of tile_rows x tile_cols, the
 // first dp_tiles whole, the rest (a partial last wave) in `split` K-pieces
@@ -87,7 +88,10 @@ struct TcPlan {
     size_t scratch_bytes;
     double est_us;       // modelled duration, for choosing between shapes
 };
-TcPlan tc_plan(int M, int N, int K, int in_type, int shape, int num_sms, bool allow_split);
+// tma_c: the whole tiles can leave by TMA stores (C's base and rows 16-byte
+// aligned, beta = 0); it changes only the modelled epilogue cost.
+TcPlan tc_plan(int M, int N, int K, int in_type, int shape, int num_sms, bool allow_split,
+               bool tma_c = true);
 // Launch the persistent tcgen05 kernel of TcShape `shape` under plan `pl`
 // (made for the same shape), plus the K-piece reduction when pl.split > 1
 // (`partials` holds pl.scratch_bytes). `encode_fn` is cuTensorMapEncodeTiled.
