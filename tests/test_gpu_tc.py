@@ -165,7 +165,8 @@ def test_unaligned_output_rows_every_phase(tgemm, tc_mode, kind, ldc, offset):
 
 
 @pytest.mark.parametrize("kind", ["tf32", "bf16"])
-@pytest.mark.parametrize("shape", [(16, 12, 12), (130, 261, 77), (300, 1001, 517)])
+@pytest.mark.parametrize("shape", [(16, 12, 12), (130, 261, 77), (300, 1001, 517),
+                                   (203, 2051, 1031)])
 def test_unaligned_leading_dimensions(tgemm, tc_mode, kind, shape):
     """Packed operands whose rows do not start on 16-byte boundaries: the
     library repacks them for the tensor-memory copies (bit-exact on integers)."""
