@@ -383,9 +383,15 @@ def run_gpu(args):
     }
 
     if not args.no_extras:
+        probe = run_tensor_probe(tg, dev, peaks)
+        out["tensor_probe"] = probe
+        if clocks["sm_mhz"]:
+            pipe = pipe_peak_tflops(probe, "tf32", num_sms, clocks["sm_mhz"])
+            out["paths"]["tf32"]["frac_vs_pipe"] = round(tf32_tflops / pipe, 4)
+            out["paths"]["tf32"]["pipe_peak"] = round(pipe, 1)
         out["e2e"] = run_e2e(tg, A_host, B_host, w, dev, max(3, min(K, 20)))
-        out["workloads"] = run_workloads(tg, inputs, dev, flush, peaks, fp32_peak)
-        out["tensor_probe"] = run_tensor_probe(tg, dev, peaks)
+        out["workloads"] = run_workloads(tg, inputs, dev, flush, peaks, fp32_peak, probe, num_sms,
+                                         uuid)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         rate, rows, dt, threads, passes = oracle_rate(A_host, B_host, args.cpu_seconds)
         what = (f"{rows} of {w.M} rows of the 4096^3 product" if passes == 1 else
@@ -466,38 +472,78 @@ def run_tensor_probe(tg, dev, peaks):
     return out
 
 
-def run_workloads(tg, inputs, dev, flush, peaks, fp32_peak):
+def pipe_peak_tflops(probe, kind, num_sms, sm_mhz):
+    """The tensor pipe's dense rate for `kind` ("bf16" or "tf32"; TF32X3 runs
+    TF32 MMAs) from the library's probe, at the SM clock `sm_mhz`."""
+    per_clk = probe["tf32" if kind == "tf32x3" else kind]["flop_per_clk_per_sm"]
+    return per_clk * num_sms * sm_mhz * 1e6 / 1e12
+
+
+# Workloads bound by reading their operands once (few rows): stated against
+# HBM bandwidth with algorithmic bytes A + B read once and C written once.
+HBM_BOUND = ("skinny_bf16", "skinny_f32")
+
+SWEEP = [("int128", "f32"), ("u1024", "f32"), ("ragged", "f32"), ("ragged", "tf32"),
+         ("n4096", "tf32x3"), ("ffn_bf16", "bf16"), ("skinny_bf16", "bf16"),
+         ("skinny_f32", "f32"), ("skinny_f32", "tf32")]
+
+
+def algorithmic_bytes(w):
+    esz = 2 if w.dtype == "bf16" else 4
+    return esz * (w.M * w.K + w.K * w.N) + 4 * w.M * w.N
+
+
+def run_workloads(tg, inputs, dev, flush, peaks, fp32_peak, probe=None, num_sms=None, uuid=None):
     """Device-time TFLOP/s of the other measured shapes (median of 10); the
     128^3 product is bound by launch latency, so its time (us) is the figure
-    to read there."""
+    to read there. Tensor-path entries also carry frac_vs_pipe: the rate
+    against the library's tensor-pipe probe at the SM clock sampled during
+    the sweep; the few-row shapes are stated against HBM bandwidth."""
     import torch
     res = {}
-    for name, path in [("int128", "f32"), ("u1024", "f32"), ("ragged", "f32"),
-                       ("ragged", "tf32"), ("n4096", "tf32x3"), ("ffn_bf16", "bf16")]:
-        w = inputs.WORKLOADS[name]
-        A_host, B_host = inputs.operands(w)
-        A, B = A_host.to(dev), B_host.to(dev)
-        C = torch.empty(w.M, w.N, device=dev)
-        if path == "f32":
-            fn = lambda: tg.gemm_f32(A, B, out=C)   # noqa: E731
-            peak, bound = fp32_peak, "alu"
-        else:
-            fn = lambda: tg.gemm_tc(A, B, path, out=C)   # noqa: E731
-            peak = peaks["bf16_tflops"] * (1.0 if path == "bf16" else NOMINAL_TF32_OVER_BF16)
-            bound = "tensor"
-        for _ in range(3):
-            fn()
-        ms = time_calls(fn, 10, flush)
-        tf = w.flops / (ms * 1e-3) / 1e12
-        pipe = tf * (3 if path == "tf32x3" else 1)    # three tensor products per useful one
-        res[f"{name}_{path}"] = {"M": w.M, "N": w.N, "K": w.K, "ms": round(ms, 4),
-                                 "us": round(ms * 1e3, 2),
-                                 "tflops": round(tf, 3), "peak": round(peak, 3),
-                                 "frac": round(pipe / peak, 4), "bound": bound,
-                                 "kernel": tg.binding.last_kernel()}
-        del A, B, C
+    with ClockSampler(uuid) as sampler:
+        for name, path in SWEEP:
+            w = inputs.WORKLOADS[name]
+            A_host, B_host = inputs.operands(w)
+            A, B = A_host.to(dev), B_host.to(dev)
+            C = torch.empty(w.M, w.N, device=dev)
+            if path == "f32":
+                fn = lambda: tg.gemm_f32(A, B, out=C)   # noqa: E731
+                peak, bound = fp32_peak, "alu"
+            else:
+                fn = lambda: tg.gemm_tc(A, B, path, out=C)   # noqa: E731
+                peak = peaks["bf16_tflops"] * (1.0 if path == "bf16" else NOMINAL_TF32_OVER_BF16)
+                bound = "tensor"
+            for _ in range(3):
+                fn()
+            ms = time_calls(fn, 10, flush)
+            tf = w.flops / (ms * 1e-3) / 1e12
+            pipe = tf * (3 if path == "tf32x3" else 1)    # three tensor products per useful one
+            entry = {"M": w.M, "N": w.N, "K": w.K, "ms": round(ms, 4), "us": round(ms * 1e3, 2),
+                     "tflops": round(tf, 3), "peak": round(peak, 3), "frac": round(pipe / peak, 4),
+                     "bound": bound, "kernel": tg.binding.last_kernel()}
+            if name in HBM_BOUND:
+                nbytes = algorithmic_bytes(w)
+                gbs = nbytes / (ms * 1e-3) / 1e9
+                entry.update({"bound": "hbm", "algorithmic_bytes": nbytes,
+                              "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                              "frac": round(gbs / peaks["hbm_gbs"], 4)})
+            res[f"{name}_{path}"] = entry
+            del A, B, C
+    clocks = sampler.summary()
     if tg.device_status() != 0:
         raise RuntimeError("a kernel wait timed out in the workload sweep")
+    if probe is not None and num_sms and clocks["sm_mhz"]:
+        for key, entry in res.items():
+            path = key.rsplit("_", 1)[1]
+            if path in ("tf32", "bf16", "tf32x3") and entry["bound"] == "tensor":
+                pipe_peak = pipe_peak_tflops(probe, path, num_sms, clocks["sm_mhz"])
+                pipe = entry["tflops"] * (3 if path == "tf32x3" else 1)
+                entry["frac_vs_pipe"] = round(pipe / pipe_peak, 4)
+    res["clocks"] = clocks
+    res["note"] = ("frac: against MEASURED_PEAKS (tensor: cuBLAS bf16 burst, TF32 scaled by the "
+                   "nominal ratio; hbm: measured copy); frac_vs_pipe: against the tensor-pipe "
+                   "probe's FLOP/clk/SM x SMs x the median SM clock sampled during this sweep")
     return res
 
 

@@ -23,6 +23,31 @@
  *   - A, B and C are DEVICE pointers (memory the caller allocated on the
  *     current CUDA device). The library never allocates, frees or copies the
  *     caller's buffers, and keeps no reference to them after the call.
+ *   - Scratch memory. A call may need device memory of its own while it
+ *     runs, for two things:
+ *       (a) operands rewritten into a layout the kernels read: on gemm_tc
+ *           TGEMM_TF32, B transposed (N x round_up(K, 32) floats) on every
+ *           call; on the tensor paths, an operand whose rows do not start
+ *           on 16-byte boundaries, repacked (rows on 128-byte boundaries);
+ *           on gemm_f32, both operands repacked when their rows are off 16
+ *           bytes and M >= 256, N >= 256, K >= 64; on TGEMM_TF32X3, high
+ *           and low copies of A and of B transposed; on gemm_ex, storage a
+ *           path cannot read (transposes);
+ *       (b) the partial tiles of a last wave split along K, when the
+ *           planner splits it: (tiles - whole tiles) x pieces x tile rows x
+ *           tile columns x 4 bytes. gemm_f32 on 4096^3 splits 56 of its 512
+ *           128 x 256 tiles into 8 pieces: 56 x 8 x 128 x 256 x 4 B = 59 MB.
+ *     Such a call takes one block with cudaMallocFromPoolAsync on `stream`
+ *     from a memory pool that the library creates once per device, and
+ *     gives it back with cudaFreeAsync on `stream` before returning. The
+ *     pool keeps the memory it has handed out (no release threshold), so
+ *     once a call of a given size has run, later calls reuse the cached
+ *     memory without going to the driver; it stays reserved until the
+ *     process exits. A call that needs neither (a) nor (b) allocates
+ *     nothing: gemm_f32 and gemm_tc TGEMM_BF16 on operands with 16-byte
+ *     rows whose tiles fill whole waves or whose tail is not split.
+ *     gemm_scratch_bytes() returns the size a call would draw, and
+ *     gemm_tc_tf32_noalloc() never allocates.
  *   - C is overwritten (there is no alpha/beta); K == 0 writes zeros to the
  *     M x N block of C; M == 0 or N == 0 is a no-op that returns TGEMM_OK.
  *   - Elements of A, B and C outside the M x K, K x N and M x N blocks (the
@@ -59,7 +84,7 @@ extern "C" {
 #define TGEMM_ERR_ALIGNMENT         2  /* a forced kernel or the no-alloc entry cannot read this layout */
 #define TGEMM_ERR_CUDA              3  /* a CUDA runtime call or launch failed */
 #define TGEMM_ERR_DEVICE_TIMEOUT    4  /* a bounded wait inside a kernel ran out (see gemm_device_status) */
-#define TGEMM_ERR_UNSUPPORTED       5  /* the current device is not sm_103 / sm_100 class */
+#define TGEMM_ERR_UNSUPPORTED       5  /* the current device is not compute capability 10.3 (sm_103) */
 
 /* Input element types of gemm_tc. */
 #define TGEMM_TF32  1   /* A and B are float arrays; products use the TF32 tensor-core format */
@@ -79,7 +104,11 @@ extern "C" {
  * and B are staged through shared memory; rows and columns past M, N, K read
  * as zero (section 7.1 of the same page), so any M, N, K >= 0 is accepted.
  * Any lda/ldb/ldc and 4-byte aligned pointers work; 16-byte aligned pointers
- * with ld a multiple of 4 take 16-byte vector loads.
+ * with ld a multiple of 4 take 16-byte vector loads. Scratch (see the common
+ * rules): the two operands repacked to 16-byte rows when they are large and
+ * off 16 bytes, and the partial tiles when the tiles of a partial last wave
+ * are split along K; neither when the operands have 16-byte rows and the
+ * 128 x 256 tiles fill whole waves of the SMs.
  *
  * Returns TGEMM_OK, TGEMM_ERR_INVALID_ARG (M, N or K negative; lda < K,
  * ldb < N or ldc < N; a null pointer when the product is not empty; a pointer
@@ -116,7 +145,9 @@ TGEMM_API int gemm_f32(int M, int N, int K,
  * boundaries; for
  * TF32, B is always rewritten transposed (the TF32 kind reads B only
  * K-major), which also absorbs any alignment of B. Rows and columns past M,
- * N, K read as zero.
+ * N, K read as zero. Scratch (see the common rules): those rewritten
+ * operands, and the partial tiles of a split last wave; BF16 on operands
+ * with 16-byte rows whose tail is not split allocates nothing.
  *
  * Returns TGEMM_OK, TGEMM_ERR_INVALID_ARG (as gemm_f32, a bad in_type, or
  * a pointer not aligned to its element size), TGEMM_ERR_UNSUPPORTED or
@@ -212,6 +243,24 @@ TGEMM_API int gemm_host(int M, int N, int K,
                         cudaStream_t stream);
 
 /*
+ * gemm_scratch_bytes — the device scratch, in bytes, that the call
+ *     gemm_ex(M, N, K, A, lda, B, ldb, C, ldc, path, flags, 1, 0, NULL, s)
+ * would draw from the library's pool on the current device (see "Scratch
+ * memory" above); gemm_f32 and gemm_tc are that call with flags 0 and
+ * their path. The pointers are not dereferenced: only their alignment
+ * matters, as it decides which operands are repacked and how C is stored.
+ * Returns the size (0 when the call allocates nothing), or a negative
+ * status code (-TGEMM_ERR_INVALID_ARG for arguments the call would reject,
+ * -TGEMM_ERR_ALIGNMENT, -TGEMM_ERR_UNSUPPORTED, -TGEMM_ERR_CUDA). Makes no
+ * CUDA call other than reading the device's attributes.
+ */
+TGEMM_API long long gemm_scratch_bytes(int M, int N, int K,
+                                       const void* A, long lda,
+                                       const void* B, long ldb,
+                                       const float* C, long ldc,
+                                       int path, int flags);
+
+/*
  * gemm_device_status — result of the kernels' bounded waits.
  *
  * Synchronises `stream`, then returns and clears the library's device-side
@@ -277,10 +326,14 @@ TGEMM_API int gemm_set_f32_kernel(int id);
  * gemm_set_tc_kernel — choose the tensor-core kernel (for tests and tuning):
  * 0 forces the one-SM kernel (128 x 256 tiles), 1 the 2-SM kernel (a CTA
  * pair computing 256 x 256 tiles), 2 the 2-SM kernel with 256 x 512 tiles;
- * -1 (default) picks by shape: the one-SM kernel when M <= 128, 256 x 512
- * tiles when N > 256 and there are at least as many of them as SM pairs,
- * else 256 x 256. TGEMM_TF32X3 always runs 256 x 256 pair tiles.
- * Process-wide. Returns TGEMM_OK or TGEMM_ERR_INVALID_ARG.
+ * -1 (default) picks by shape: the one-SM kernel when M <= 128, 256 x 256
+ * tiles when N <= 256, and otherwise the pair shape that a timing model of
+ * the two expects to finish first (whole-tile rounds over the SM pairs, the
+ * cost of a split last wave, a main-loop rate per shape and type measured
+ * on this GPU, and the exposed write-out of the 256 x 512 tiles), with
+ * near-ties (the wide tiles less than 3 % faster) going to 256 x 256.
+ * TGEMM_TF32X3 always runs 256 x 256 pair tiles. Process-wide. Returns
+ * TGEMM_OK or TGEMM_ERR_INVALID_ARG.
  */
 TGEMM_API int gemm_set_tc_kernel(int mode);
 
@@ -321,11 +374,17 @@ TGEMM_API const char* gemm_last_kernel(void);
  * Arguments, layout and result are those of gemm_tc with in_type TGEMM_TF32:
  * A is M x K floats (16-byte aligned, lda >= K and a multiple of 4), B is
  * K x N floats (4-byte aligned, ldb >= N), C is M x N floats (ldc >= N).
+ * B transposed goes to the array with rows round_up(K, 32) floats apart
+ * (128-byte rows, as gemm_tc) when N * round_up(K, 32) fits in it, else
+ * round_up(K, 4) floats apart (16-byte rows; the GEMM kernel reads such rows
+ * somewhat slower). The tiles of a partial last wave are never split along
+ * K here (that would need more scratch). Waits inside the kernel are bounded
+ * by the limit of gemm_set_wait_limit_ns, as for gemm_tc.
  *
- * Returns TGEMM_OK; TGEMM_ERR_INVALID_ARG for the argument errors of gemm_tc
- * and when N * round_up(K, 4) > TGEMM_NOALLOC_SCRATCH_FLOATS (the problem does
- * not fit the fixed scratch; nothing is launched); TGEMM_ERR_ALIGNMENT;
- * TGEMM_ERR_UNSUPPORTED; TGEMM_ERR_CUDA.
+ * Returns TGEMM_OK; TGEMM_ERR_INVALID_ARG for the argument errors of gemm_tc,
+ * for K > 4194240, and when N * round_up(K, 4) > TGEMM_NOALLOC_SCRATCH_FLOATS
+ * (the problem does not fit the fixed scratch; nothing is launched);
+ * TGEMM_ERR_ALIGNMENT; TGEMM_ERR_UNSUPPORTED; TGEMM_ERR_CUDA.
  *
  * The first call on each device does that device's set-up (it looks up the
  * device address of the scratch array with cudaGetSymbolAddress), so make

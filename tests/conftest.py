@@ -28,3 +28,25 @@ def tgemm():
     import tiled_matrix_multiplication_sm_gb300 as t
     t.load()            # raises if the compiled library is missing
     return t
+
+
+@pytest.fixture(scope="session")
+def workload_reference():
+    """The oracle's full product (C_ref, absAB) of a named workload, computed
+    once per session and shared by the tests of every path that run it.
+
+    Returns a function name -> (A, B, C_ref, absAB) with A and B the host
+    operands the CUDA path receives."""
+    cache = {}
+
+    def get(name):
+        if name not in cache:
+            import oracle
+            from tiled_matrix_multiplication_sm_gb300 import inputs
+            w = inputs.WORKLOADS[name]
+            A, B = inputs.operands(w)
+            C_ref, absAB = oracle.gemm(A, B)
+            cache[name] = (A, B, C_ref, absAB)
+        return cache[name]
+
+    return get

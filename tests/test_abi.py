@@ -35,7 +35,7 @@ def test_header_declares_the_boundary():
     names = declared_symbols()
     for required in ["gemm_f32", "gemm_tc", "gemm_status_string", "gemm_device_status"]:
         assert required in names
-    assert len(names) == 15
+    assert len(names) == 16
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -120,6 +120,21 @@ def test_host_entry_rejects_bad_arguments(lib):
     assert lib.gemm_host(4, 4, 4, FAKE, 3, FAKE, 4, FAKE, 4, 0, 0) == binding.TGEMM_ERR_INVALID_ARG
     assert lib.gemm_host(4, 4, 4, FAKE + 2, 4, FAKE, 4, FAKE, 4, 0, 0) == binding.TGEMM_ERR_INVALID_ARG
     assert lib.gemm_host(0, 4, 4, 0, 4, 0, 4, 0, 4, 0, 0) == binding.TGEMM_OK
+
+
+def test_scratch_query_rejects_bad_arguments(lib):
+    """gemm_scratch_bytes checks its arguments like gemm_ex, before any CUDA
+    call, and answers 0 for an empty product."""
+    bad = -binding.TGEMM_ERR_INVALID_ARG
+    q = lib.gemm_scratch_bytes
+    assert q(4, 4, 4, FAKE, 4, FAKE, 4, FAKE, 4, 4, 0) == bad          # unknown path
+    assert q(4, 4, 4, FAKE, 4, FAKE, 4, FAKE, 4, 0, 8) == bad          # unknown flag
+    assert q(-1, 4, 4, FAKE, 4, FAKE, 4, FAKE, 4, 0, 0) == bad         # negative M
+    assert q(4, 4, 8, FAKE, 7, FAKE, 4, FAKE, 4, 1, 0) == bad          # lda < K
+    assert q(4, 4, 4, FAKE, 4, FAKE, 4, 0, 4, 2, 0) == bad             # null C
+    assert q(4, 8, 8, FAKE + 1, 8, FAKE, 8, FAKE, 8, 2, 0) == bad      # bf16 A odd byte
+    assert q(0, 4, 4, 0, 4, 0, 4, 0, 4, 1, 0) == 0                     # nothing to compute
+    assert q(4, 0, 4, 0, 4, 0, 4, 0, 4, 3, 3) == 0
 
 
 @pytest.mark.parametrize("M,N", [(0, 5), (5, 0), (0, 0)])

@@ -17,6 +17,20 @@ def test_fp32_peak_from_unit_counts():
     assert bench.fp32_peak_tflops(152, 2070.0) == pytest.approx(80.5478, rel=1e-6)
 
 
+def test_pipe_peak_and_algorithmic_bytes():
+    probe = {"bf16": {"flop_per_clk_per_sm": 8192.0}, "tf32": {"flop_per_clk_per_sm": 4096.0}}
+    # 8192 FLOP/clk/SM x 152 SMs x 2070 MHz = 2577.5 TFLOP/s
+    assert bench.pipe_peak_tflops(probe, "bf16", 152, 2070.0) == pytest.approx(2577.5, rel=1e-4)
+    # the split-TF32 form runs TF32 MMAs
+    assert bench.pipe_peak_tflops(probe, "tf32x3", 152, 2070.0) == pytest.approx(1288.7, rel=1e-4)
+    from tiled_matrix_multiplication_sm_gb300 import inputs
+    w = inputs.WORKLOADS["skinny_bf16"]
+    # A and B read once (bf16), C written once (fp32)
+    assert bench.algorithmic_bytes(w) == 2 * (16 * 4096 + 4096 * 14336) + 4 * 16 * 14336
+    assert bench.algorithmic_bytes(inputs.WORKLOADS["skinny_f32"]) == \
+        4 * (16 * 4096 + 4096 * 14336) + 4 * 16 * 14336
+
+
 def test_load_peaks_fallback(tmp_path):
     p = bench.load_peaks(str(tmp_path / "missing.json"))
     assert p["source"] == "fallback" and p["hbm_gbs"] == 6800.0

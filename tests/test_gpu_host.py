@@ -74,14 +74,14 @@ def test_k_zero_and_empty(tgemm):
     assert C.shape == (0, 7)
 
 
-def test_workload_n4096_host_sampled(tgemm):
-    """The benchmark's end-to-end call on its full workload (FP32 path)."""
-    w = inputs.WORKLOADS["n4096"]
-    A, B = inputs.operands(w)
-    C = tgemm.matmul(A.pin_memory(), B.pin_memory(), "f32")
-    rows = [0, 1, 1023, 1024, 2047, 2048, 3071, 3072, 4095]
-    C_ref, absAB = oracle.gemm_rows(A, B, rows)
-    assert_within(C[rows], C_ref, absAB, F32_REL, F32_ABS, "n4096 host")
+@pytest.mark.parametrize("path", ["f32", "tf32"])
+def test_workload_n4096_host_full(tgemm, workload_reference, path):
+    """The benchmark's end-to-end calls on its full workload (both paths of
+    the step), every output checked against the oracle."""
+    A, B, C_ref, absAB = workload_reference("n4096")
+    C = tgemm.matmul(A.pin_memory(), B.pin_memory(), path)
+    rel, abs_ = (F32_REL, F32_ABS) if path == "f32" else (TC_REL, TC_ABS)
+    assert_within(C, C_ref, absAB, rel, abs_, f"n4096 host {path}")
 
 
 def test_invalid_path_and_misaligned_host_operand(tgemm):

@@ -41,14 +41,19 @@ def padded_cuda(x, ld, pad=float("nan")):
 
 # ---------------------------------------------------------------- workloads
 
-def test_workload_n4096_tf32_sampled_rows(tgemm):
-    w = inputs.WORKLOADS["n4096"]
-    A, B = inputs.operands(w)
-    C = run_tc(tgemm, A, B, "tf32").cpu()
-    rows = sorted(set([0, 127, 128, w.M - 1] +
-                      torch.randint(0, w.M, (44,), generator=inputs.generator(17)).tolist()))
-    C_ref, absAB = oracle.gemm_rows(A, B, rows)
-    assert_within(C[rows], C_ref, absAB, TC_REL, TC_ABS, "n4096 tf32")
+def test_workload_n4096_tf32_full(tgemm, workload_reference):
+    """Full-size launch, every output checked against the oracle."""
+    A, B, C_ref, absAB = workload_reference("n4096")
+    C = run_tc(tgemm, A, B, "tf32")
+    assert_within(C, C_ref, absAB, TC_REL, TC_ABS, "n4096 tf32")
+
+
+@pytest.mark.parametrize("name,kind", [("skinny_bf16", "bf16"), ("skinny_f32", "tf32")])
+def test_workload_skinny_full(tgemm, workload_reference, name, kind):
+    """The FFN shape with 16 rows (bound by reading B), every output checked."""
+    A, B, C_ref, absAB = workload_reference(name)
+    C = run_tc(tgemm, A, B, kind)
+    assert_within(C, C_ref, absAB, TC_REL, TC_ABS, f"{name} {kind}")
 
 
 def test_workload_ffn_bf16_checked_rows(tgemm):
@@ -194,17 +199,12 @@ def test_unaligned_operand_offsets(tgemm):
     assert_bit_exact(C, C_ref, "bf16 offset operands")
 
 
-def test_workload_ragged_tf32_sampled_rows(tgemm):
-    """The 3000 x 5001 x 1537 packed workload on the tensor path (TF32)."""
-    w = inputs.WORKLOADS["ragged"]
-    A, B = inputs.operands(w)
-    C = run_tc(tgemm, A, B, "tf32").cpu()
-    assert "repack_a" in tgemm.binding.last_kernel()
-    rows = [0, 1, 255, 256, 2999] + torch.randint(0, w.M, (30,),
-                                                  generator=inputs.generator(19)).tolist()
-    rows = sorted(set(rows))
-    C_ref, absAB = oracle.gemm_rows(A, B, rows)
-    assert_within(C[rows], C_ref, absAB, TC_REL, TC_ABS, "ragged tf32")
+def test_workload_ragged_tf32_full(tgemm, workload_reference):
+    """The 3000 x 5001 x 1537 packed workload on the tensor path (TF32),
+    every output checked."""
+    A, B, C_ref, absAB = workload_reference("ragged")
+    C = run_tc(tgemm, A, B, "tf32")
+    assert_within(C, C_ref, absAB, TC_REL, TC_ABS, "ragged tf32")
 
 
 def test_k_zero_writes_zeros(tgemm):
@@ -313,15 +313,11 @@ def test_tf32x3_much_closer_than_tf32(tgemm):
     assert abs(e3).max() < abs(e1).max() / 50
 
 
-def test_workload_n4096_tf32x3_sampled_rows(tgemm):
-    w = inputs.WORKLOADS["n4096"]
-    A, B = inputs.operands(w)
-    C = run_tc(tgemm, A, B, "tf32x3").cpu()
-    rows = [0, 255, 256, 4095] + torch.randint(0, w.M, (20,), generator=inputs.generator(23)).tolist()
-    rows = sorted(set(rows))
-    C_ref, absAB = oracle.gemm_rows(A, B, rows)
+def test_workload_n4096_tf32x3_full(tgemm, workload_reference):
+    A, B, C_ref, absAB = workload_reference("n4096")
+    C = run_tc(tgemm, A, B, "tf32x3")
     from tests.parity import F32_ABS, F32_REL
-    assert_within(C[rows], C_ref, absAB, F32_REL, F32_ABS, "n4096 tf32x3")
+    assert_within(C, C_ref, absAB, F32_REL, F32_ABS, "n4096 tf32x3")
 
 
 def test_auto_shape_prefers_narrow_tiles_for_unaligned_output_rows(tgemm):

@@ -3,10 +3,16 @@
 It serves callers that cannot allocate device memory (an application that
 reserves all of its memory up front, code that must not touch the device
 allocator while it runs): its scratch is a fixed array inside the library.
-This test calls it through the C ABI twice in a row, on different operands
-and shapes, and checks each result against gemm_tc's TF32 result on the same
-operands with the tensor-path tolerance |C - C_ref| <= 1e-2 * absAB. It also
-checks that a problem too large for the fixed scratch is refused.
+Each case calls it through the C ABI twice in a row, on different operands
+and shapes, and checks both results against the CPU oracle: with the
+tensor-path tolerance |C - C_ref| <= 1e-2 * absAB on random data, bit for
+bit on integer data (small integers and their sums are exact in TF32 and
+FP32). The cases cover both row pitches of the transposed B in the fixed
+array (128-byte rows when they fit, else 16-byte rows: K = 1001 with
+N = 4150), a K that is not a multiple of 4 (A then comes as a padded view
+with lda a multiple of 4), and a C whose rows are not 16-byte aligned
+(ldc = N + 1), which takes the register-store epilogue. It also checks that
+a problem too large for the fixed scratch is refused without launching.
 
 The file is named so that pytest collects it last.
 """
@@ -14,7 +20,7 @@ import pytest
 import torch
 
 import oracle
-from tests.parity import TC_ABS, TC_REL, assert_within
+from tests.parity import TC_ABS, TC_REL, assert_bit_exact, assert_within
 from tiled_matrix_multiplication_sm_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -28,23 +34,46 @@ def noalloc(tg, A, B, C):
         B.stride(0), C.data_ptr(), C.stride(0), torch.cuda.current_stream().cuda_stream)
 
 
-# The second pair's first problem takes the 256 x 512 CTA-pair tiles (64 of
-# them: one round, no split of a tail).
-@pytest.mark.parametrize("first,second", [((300, 1000, 772), (513, 264, 2048)),
-                                          ((8192, 1024, 4096), (256, 512, 8192))])
-def test_noalloc_matches_gemm_tc_on_two_calls(tgemm, first, second):
-    for call, (M, N, K) in enumerate([first, second]):
-        g = inputs.generator(900 + call)
-        A = inputs.draw(M, K, "normal", g)
-        B = inputs.draw(K, N, "normal", g)
-        Ad, Bd = A.cuda(), B.cuda()
-        C_ref = tgemm.gemm_tc(Ad, Bd, "tf32")
-        C = torch.full((M, N), float("nan"), device="cuda")
+def device_view(x, ld, pad=float("nan")):
+    """Device copy of ``x`` as a view with leading dimension ``ld`` (padding
+    columns hold ``pad``)."""
+    rows, cols = x.shape
+    store = torch.full((rows, ld), pad, dtype=x.dtype, device="cuda")
+    store[:, :cols] = x.cuda()
+    return store[:, :cols]
+
+
+# (M, N, K, dist, lda, ldc): lda/ldc None = packed.
+CASES = {
+    # 128-byte pitch for B transposed (1000 x 800 floats fit); then integers.
+    "pitch128": [(300, 1000, 772, "normal", None, None), (640, 768, 1024, "int4", None, None)],
+    # The first problem takes the 256 x 512 CTA-pair tiles (64 of them: one
+    # round, no split tail).
+    "large": [(8192, 1024, 4096, "normal", None, None), (256, 512, 8192, "normal", None, None)],
+    # 16-byte pitch (4150 x 1024 floats would not fit, 4150 x 1004 do), K not
+    # a multiple of 4 (lda = 1004), C rows off 16 bytes (ldc = 4151).
+    "pitch16": [(300, 4150, 1001, "normal", 1004, 4151), (129, 4150, 1001, "int4", 1004, 4151)],
+}
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_noalloc_matches_oracle_on_two_calls(tgemm, case):
+    for call, (M, N, K, dist, lda, ldc) in enumerate(CASES[case]):
+        g = inputs.generator(900 + 10 * sorted(CASES).index(case) + call)
+        A = inputs.draw(M, K, dist, g)
+        B = inputs.draw(K, N, dist, g)
+        Ad = device_view(A, lda) if lda else A.cuda()
+        Bd = B.cuda()
+        C = device_view(torch.empty(M, N), ldc or N)
+        C.fill_(float("nan"))
         assert noalloc(tgemm, Ad, Bd, C) == 0
         assert tgemm.device_status() == 0
-        _, absAB = oracle.gemm(A, B)
-        assert_within(C, C_ref.cpu().double().numpy(), absAB, TC_REL, TC_ABS,
-                      f"no-alloc call {call + 1}")
+        C_ref, absAB = oracle.gemm(A, B)
+        what = f"no-alloc {case} call {call + 1} ({M}x{N}x{K}, {dist})"
+        if dist == "int4":
+            assert_bit_exact(C, C_ref, what)
+        else:
+            assert_within(C, C_ref, absAB, TC_REL, TC_ABS, what)
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch(tgemm):

@@ -53,6 +53,9 @@ _SIGNATURES = {
     "gemm_tc_tf32_noalloc": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                             _VP, ctypes.c_long, _VP, ctypes.c_long,
                                             _VP, ctypes.c_long, _VP]),
+    "gemm_scratch_bytes": (ctypes.c_longlong, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               _VP, ctypes.c_long, _VP, ctypes.c_long,
+                                               _VP, ctypes.c_long, ctypes.c_int, ctypes.c_int]),
     "gemm_tc_peak": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_long,
                                     ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
                                     _VP]),
@@ -305,6 +308,29 @@ def gemm_ex(A: torch.Tensor, B: torch.Tensor, path: str = "f32", trans_a: bool =
     if st != TGEMM_OK:
         raise TgemmError(st, "gemm_ex")
     return C
+
+
+def scratch_bytes(A: torch.Tensor, B: torch.Tensor, path: str = "f32", trans_a: bool = False,
+                  trans_b: bool = False, out: Optional[torch.Tensor] = None) -> int:
+    """Bytes of device scratch the library's pool would give the product
+    ``gemm_ex(A, B, path, trans_a, trans_b, out=out)`` (0: it allocates
+    nothing). Without ``out``, C is taken to be a packed, 16-byte-aligned
+    M x N float32 matrix."""
+    dtype = _PATH_DTYPE[path]
+    lda = _check_matrix(A, "A", dtype)
+    ldb = _check_matrix(B, "B", dtype)
+    M, K = (A.shape[1], A.shape[0]) if trans_a else (A.shape[0], A.shape[1])
+    N = B.shape[0] if trans_b else B.shape[1]
+    if out is None:
+        c_ptr, ldc = 256, max(N, 1)
+    else:
+        c_ptr, ldc = out.data_ptr(), _check_matrix(out, "out", torch.float32)
+    flags = (TGEMM_TRANS_A if trans_a else 0) | (TGEMM_TRANS_B if trans_b else 0)
+    n = _on_device(A.device, lambda dev: int(load().gemm_scratch_bytes(
+        M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, c_ptr, ldc, TGEMM_PATH[path], flags)))
+    if n < 0:
+        raise TgemmError(-n, "gemm_scratch_bytes")
+    return n
 
 
 def _check_host_matrix(x: torch.Tensor, name: str, dtype: torch.dtype) -> int:

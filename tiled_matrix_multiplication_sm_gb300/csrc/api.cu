@@ -169,6 +169,10 @@ int check_common(int M, int N, int K, const void* A, long lda, const void* B, lo
 
 }  // namespace
 
+namespace tgemm {
+unsigned long long wait_limit_ns() { return (unsigned long long)g_wait_limit_ns.load(); }
+}  // namespace tgemm
+
 namespace {
 
 // One product request: C = alpha * op(A) op(B) + beta * C + bias, on `path`.
@@ -195,27 +199,146 @@ struct Carve {
     }
 };
 
-int run_product(const Request& r, cudaStream_t stream) {
-    g_last_kernel = "";
+// What has to be produced before the GEMM kernel, per operand.
+enum Prep { NONE, TRANSPOSE, REPACK, SPLIT, TRANSPOSE_SPLIT };
+
+// How one valid, non-empty (K > 0) request runs: the pre-passes, the
+// layout the GEMM kernel reads, the kernel's plan and the pool scratch the
+// call draws (`scratch` bytes in one block, carved at the offsets below).
+struct ProductPlan {
+    Prep prep_a = NONE, prep_b = NONE;
+    long ldk = 0, ldn = 0;       // scratch row pitches for rows of length K and N
+    long ld_a = 0, ld_b = 0;     // leading dimensions the GEMM kernel reads
+    bool b_kmajor = false;       // tensor paths: B read K-major (N x K)
+    size_t a_off = 0, a2_off = 0, b_off = 0, b2_off = 0, p_off = 0;
+    size_t part_bytes = 0;       // partial tiles of a split last wave
+    size_t scratch = 0;          // total pool scratch of the call (0: none)
+    int f32_id = 0;
+    tgemm::F32Plan fplan{};
+    tgemm::TcPlan tplan{};
+    int shape = tgemm::TC_ONE_SM;
+};
+
+// Argument checks of a request. Returns TGEMM_OK, an error code, or -1 for
+// a valid request with nothing to compute (M or N is 0).
+int check_request(const Request& r) {
     const bool ta = (r.flags & TGEMM_TRANS_A) != 0, tb = (r.flags & TGEMM_TRANS_B) != 0;
     const int M = r.M, N = r.N, K = r.K;
     if (M < 0 || N < 0 || K < 0) return TGEMM_ERR_INVALID_ARG;
     if (r.lda < (ta ? M : K) || r.ldb < (tb ? K : N) || r.ldc < N) return TGEMM_ERR_INVALID_ARG;
     if (r.lda < 0 || r.ldb < 0) return TGEMM_ERR_INVALID_ARG;
-    if (M == 0 || N == 0) return TGEMM_OK;
+    if (M == 0 || N == 0) return -1;
     if (r.C == nullptr || reinterpret_cast<uintptr_t>(r.C) % 4 != 0) return TGEMM_ERR_INVALID_ARG;
     if (r.ep.bias != nullptr && reinterpret_cast<uintptr_t>(r.ep.bias) % 4 != 0)
         return TGEMM_ERR_INVALID_ARG;
-    const int path = r.path;
-    const size_t esz = path == TGEMM_PATH_BF16 ? 2 : 4;
+    const size_t esz = r.path == TGEMM_PATH_BF16 ? 2 : 4;
     if (K > 0) {
         if (r.A == nullptr || r.B == nullptr) return TGEMM_ERR_INVALID_ARG;
         if (reinterpret_cast<uintptr_t>(r.A) % esz != 0 || reinterpret_cast<uintptr_t>(r.B) % esz != 0)
             return TGEMM_ERR_INVALID_ARG;
     }
+    return TGEMM_OK;
+}
+
+// Plan a checked request with K > 0 on a device with dev.num_sms SMs.
+int plan_product(const Request& r, const DeviceInfo& dev, ProductPlan& pp) {
+    const bool ta = (r.flags & TGEMM_TRANS_A) != 0, tb = (r.flags & TGEMM_TRANS_B) != 0;
+    const int M = r.M, N = r.N, K = r.K;
+    const int path = r.path;
+    const size_t esz = path == TGEMM_PATH_BF16 ? 2 : 4;
+    auto aligned16 = [&](const void* p, long ld) {
+        return reinterpret_cast<uintptr_t>(p) % 16 == 0 && (ld * (long)esz) % 16 == 0;
+    };
+    // Scratch rows start on 128-byte boundaries: a TMA box whose rows are
+    // only 16-byte aligned straddles an extra 32-byte sector per row, and
+    // the TF32 kernel measured 16 % slower on such operands (row pitch
+    // 6160 bytes against 6144 or 6272).
+    const long per128 = (long)(128 / esz);
+    pp.ldk = (K + per128 - 1) / per128 * per128;   // rows of length K
+    pp.ldn = (N + per128 - 1) / per128 * per128;   // rows of length N
+    const bool f32 = path == TGEMM_PATH_F32;
+    const bool tf32 = path == TGEMM_PATH_TF32;
+    const bool x3 = path == TGEMM_PATH_TF32X3;
+    // What has to be produced before the GEMM kernel:
+    //   A: M x K K-major. Transposed storage -> transpose (all paths);
+    //      X3 -> hi/lo split; tensor paths with rows off 16 bytes -> repack.
+    //   B: F32: K x N row-major (transposed storage -> transpose).
+    //      BF16: K x N read MN-major, or N x K K-major when stored
+    //      transposed; rows off 16 bytes -> repack.
+    //      TF32: N x K K-major: transpose unless stored transposed (then
+    //      repack if needed). X3: hi/lo of the N x K form.
+    if (x3) {
+        pp.prep_a = ta ? TRANSPOSE_SPLIT : SPLIT;
+        pp.prep_b = tb ? SPLIT : TRANSPOSE_SPLIT;
+    } else if (f32) {
+        // Rows off 16 bytes can be read with 4-byte copies, at about a
+        // quarter of the throughput; for large products it is cheaper to
+        // repack them first (8 (MK + KN) bytes of HBM traffic, ~2 % of the
+        // GEMM at M = 3000, N = 5001) and run the 16-byte loaders.
+        // (A forced configuration reads the caller's layout as given.)
+        const bool big = g_forced_f32.load() < 0 && M >= 256 && N >= 256 && K >= 64;
+        pp.prep_a = ta ? TRANSPOSE : (big && !aligned16(r.A, r.lda) ? REPACK : NONE);
+        pp.prep_b = tb ? TRANSPOSE : (big && !aligned16(r.B, r.ldb) ? REPACK : NONE);
+    } else {
+        pp.prep_a = ta ? TRANSPOSE : (aligned16(r.A, r.lda) ? NONE : REPACK);
+        if (tf32)
+            pp.prep_b = tb ? (aligned16(r.B, r.ldb) ? NONE : REPACK) : TRANSPOSE;
+        else
+            pp.prep_b = aligned16(r.B, r.ldb) ? NONE : REPACK;      // bf16, either storage
+    }
+    pp.b_kmajor = tb || tf32 || x3;   // tensor paths: B read K-major
+    // Layout the GEMM reads: A M x K (ld_a), B K x N or N x K (ld_b).
+    pp.ld_a = pp.prep_a == NONE ? r.lda : pp.ldk;
+    pp.ld_b = pp.prep_b == NONE ? r.ldb : ((f32 || !pp.b_kmajor) ? pp.ldn : pp.ldk);
+    Carve cv;
+    pp.a_off = pp.prep_a == NONE ? 0 : cv.take((size_t)M * pp.ldk * esz);
+    pp.a2_off = x3 ? cv.take((size_t)M * pp.ldk * esz) : 0;
+    // Rows of the B the GEMM reads: K (F32, BF16 MN-major) or N (K-major).
+    const size_t b_rows = (f32 || !pp.b_kmajor) ? (size_t)K : (size_t)N;
+    pp.b_off = pp.prep_b == NONE ? 0 : cv.take(b_rows * (size_t)pp.ld_b * esz);
+    pp.b2_off = x3 ? cv.take((size_t)N * pp.ldk * esz) : 0;
+
+    tgemm::GemmArgs probe{M, N, K, r.A, pp.ld_a, r.B, pp.ld_b, r.C, r.ldc};
+    if (f32) {
+        // Operands the kernel will read: the caller's, or 16-byte-row scratch.
+        probe.A = pp.prep_a == NONE ? r.A : nullptr;
+        probe.B = pp.prep_b == NONE ? r.B : nullptr;
+        tgemm::GemmArgs chk = probe;
+        if (chk.A == nullptr) chk.A = reinterpret_cast<const void*>(256);   // scratch: aligned
+        if (chk.B == nullptr) chk.B = reinterpret_cast<const void*>(256);
+        const int forced = g_forced_f32.load();
+        if (forced >= 0) {
+            if (!tgemm::f32_kernel_accepts(forced, chk)) return TGEMM_ERR_ALIGNMENT;
+            pp.f32_id = forced;
+        } else {
+            pp.f32_id = tgemm::f32_select(chk, dev.num_sms);
+        }
+        pp.fplan = tgemm::f32_plan(pp.f32_id, probe, dev.num_sms);
+    } else {
+        // Whole tiles leave by TMA stores when C's base and rows are 16-byte
+        // aligned and beta = 0 (the model charges the wide tiles more otherwise).
+        const bool tma_c = reinterpret_cast<uintptr_t>(r.C) % 16 == 0 && r.ldc % 4 == 0 &&
+                           r.ep.beta == 0.0f;
+        pp.shape = tgemm::tc_shape(M, N, K, path, g_tc_mode.load(), dev.num_sms, true, tma_c);
+        pp.tplan = tgemm::tc_plan(M, N, K, path, pp.shape, dev.num_sms, true, tma_c);
+    }
+    pp.part_bytes = f32 ? pp.fplan.scratch_bytes : pp.tplan.scratch_bytes;
+    pp.p_off = pp.part_bytes ? cv.take(pp.part_bytes) : 0;
+    pp.scratch = cv.used;
+    return TGEMM_OK;
+}
+
+int run_product(const Request& r, cudaStream_t stream) {
+    g_last_kernel = "";
+    int st = check_request(r);
+    if (st == -1) return TGEMM_OK;
+    if (st != TGEMM_OK) return st;
+    const int M = r.M, N = r.N, K = r.K;
+    const int path = r.path;
+    const size_t esz = path == TGEMM_PATH_BF16 ? 2 : 4;
 
     DeviceInfo dev;
-    int st = current_device_info(&dev);
+    st = current_device_info(&dev);
     if (st != TGEMM_OK) return st;
 
     if (K == 0) {
@@ -225,95 +348,12 @@ int run_product(const Request& r, cudaStream_t stream) {
         return TGEMM_OK;
     }
 
-    // ---- plan the operand layouts each path reads, and the scratch for them
-    auto aligned16 = [&](const void* p, long ld) {
-        return reinterpret_cast<uintptr_t>(p) % 16 == 0 && (ld * (long)esz) % 16 == 0;
-    };
-    // Scratch rows start on 128-byte boundaries: a TMA box whose rows are
-    // only 16-byte aligned straddles an extra 32-byte sector per row, and
-    // the TF32 kernel measured 16 % slower on such operands (row pitch
-    // 6160 bytes against 6144 or 6272).
-    const long per128 = (long)(128 / esz);
-    const long ldk = (K + per128 - 1) / per128 * per128;   // rows of length K
-    const long ldn = (N + per128 - 1) / per128 * per128;   // rows of length N
+    ProductPlan pp;
+    st = plan_product(r, dev, pp);
+    if (st != TGEMM_OK) return st;
     const bool f32 = path == TGEMM_PATH_F32;
-    const bool tf32 = path == TGEMM_PATH_TF32;
-    const bool x3 = path == TGEMM_PATH_TF32X3;
     const bool bf16 = path == TGEMM_PATH_BF16;
-    // What has to be produced before the GEMM kernel:
-    //   A: M x K K-major. Transposed storage -> transpose (all paths);
-    //      X3 -> hi/lo split; tensor paths with rows off 16 bytes -> repack.
-    //   B: F32: K x N row-major (transposed storage -> transpose).
-    //      BF16: K x N read MN-major, or N x K K-major when stored
-    //      transposed; rows off 16 bytes -> repack.
-    //      TF32: N x K K-major: transpose unless stored transposed (then
-    //      repack if needed). X3: hi/lo of the N x K form.
-    enum Prep { NONE, TRANSPOSE, REPACK, SPLIT, TRANSPOSE_SPLIT };
-    Prep prep_a = NONE, prep_b = NONE;
-    if (x3) {
-        prep_a = ta ? TRANSPOSE_SPLIT : SPLIT;
-        prep_b = tb ? SPLIT : TRANSPOSE_SPLIT;
-    } else if (f32) {
-        // Rows off 16 bytes can be read with 4-byte copies, at about a
-        // quarter of the throughput; for large products it is cheaper to
-        // repack them first (8 (MK + KN) bytes of HBM traffic, ~2 % of the
-        // GEMM at M = 3000, N = 5001) and run the 16-byte loaders.
-        // (A forced configuration reads the caller's layout as given.)
-        const bool big = g_forced_f32.load() < 0 && M >= 256 && N >= 256 && K >= 64;
-        prep_a = ta ? TRANSPOSE : (big && !aligned16(r.A, r.lda) ? REPACK : NONE);
-        prep_b = tb ? TRANSPOSE : (big && !aligned16(r.B, r.ldb) ? REPACK : NONE);
-    } else {
-        prep_a = ta ? TRANSPOSE : (aligned16(r.A, r.lda) ? NONE : REPACK);
-        if (tf32)
-            prep_b = tb ? (aligned16(r.B, r.ldb) ? NONE : REPACK) : TRANSPOSE;
-        else
-            prep_b = aligned16(r.B, r.ldb) ? NONE : REPACK;      // bf16, either storage
-    }
-    const bool b_kmajor = tb || tf32 || x3;   // tensor paths: B read K-major
-    // Layout the GEMM reads: A M x K (ld_a), B K x N or N x K (ld_b).
-    const long ld_a = prep_a == NONE ? r.lda : ldk;
-    const long ld_b = prep_b == NONE ? r.ldb : ((f32 || !b_kmajor) ? ldn : ldk);
-    Carve cv;
-    const size_t a_off = prep_a == NONE ? 0 : cv.take((size_t)M * ldk * esz);
-    const size_t a2_off = x3 ? cv.take((size_t)M * ldk * esz) : 0;
-    // Rows of the B the GEMM reads: K (F32, BF16 MN-major) or N (K-major).
-    const size_t b_rows = (f32 || !b_kmajor) ? (size_t)K : (size_t)N;
-    const size_t b_off = prep_b == NONE ? 0 : cv.take(b_rows * (size_t)ld_b * esz);
-    const size_t b2_off = x3 ? cv.take((size_t)N * ldk * esz) : 0;
-
-    int f32_id = 0;
-    tgemm::F32Plan fplan;
-    tgemm::TcPlan tplan;
-    int shape = tgemm::TC_ONE_SM;
-    tgemm::GemmArgs probe{M, N, K, r.A, ld_a, r.B, ld_b, r.C, r.ldc};
-    if (f32) {
-        // Operands the kernel will read: the caller's, or 16-byte-row scratch.
-        probe.A = prep_a == NONE ? r.A : nullptr;
-        probe.B = prep_b == NONE ? r.B : nullptr;
-        const int forced = g_forced_f32.load();
-        if (forced >= 0) {
-            tgemm::GemmArgs chk = probe;
-            if (chk.A == nullptr) chk.A = reinterpret_cast<const void*>(256);   // scratch: aligned
-            if (chk.B == nullptr) chk.B = reinterpret_cast<const void*>(256);
-            if (!tgemm::f32_kernel_accepts(forced, chk)) return TGEMM_ERR_ALIGNMENT;
-            f32_id = forced;
-        } else {
-            tgemm::GemmArgs chk = probe;
-            if (chk.A == nullptr) chk.A = reinterpret_cast<const void*>(256);
-            if (chk.B == nullptr) chk.B = reinterpret_cast<const void*>(256);
-            f32_id = tgemm::f32_select(chk, dev.num_sms);
-        }
-        fplan = tgemm::f32_plan(f32_id, probe, dev.num_sms);
-    } else {
-        // Whole tiles leave by TMA stores when C's base and rows are 16-byte
-        // aligned and beta = 0 (the model charges the wide tiles more otherwise).
-        const bool tma_c = reinterpret_cast<uintptr_t>(r.C) % 16 == 0 && r.ldc % 4 == 0 &&
-                           r.ep.beta == 0.0f;
-        shape = tgemm::tc_shape(M, N, K, path, g_tc_mode.load(), dev.num_sms, true, tma_c);
-        tplan = tgemm::tc_plan(M, N, K, path, shape, dev.num_sms, true, tma_c);
-    }
-    const size_t part_bytes = f32 ? fplan.scratch_bytes : tplan.scratch_bytes;
-    const size_t p_off = part_bytes ? cv.take(part_bytes) : 0;
+    const long ldk = pp.ldk, ldn = pp.ldn;
 
     void* enc = nullptr;
     if (!f32) {
@@ -321,12 +361,12 @@ int run_product(const Request& r, cudaStream_t stream) {
         if (enc == nullptr) return TGEMM_ERR_CUDA;
     }
     void* ws = nullptr;
-    if (cv.used > 0) {
+    if (pp.scratch > 0) {
         int devno = 0;
         if (cudaGetDevice(&devno) != cudaSuccess) return TGEMM_ERR_CUDA;
         cudaMemPool_t pool = scratch_pool(devno);
         if (pool == nullptr) return TGEMM_ERR_CUDA;
-        if (cudaMallocFromPoolAsync(&ws, cv.used, pool, stream) != cudaSuccess)
+        if (cudaMallocFromPoolAsync(&ws, pp.scratch, pool, stream) != cudaSuccess)
             return TGEMM_ERR_CUDA;
     }
     char* base = static_cast<char*>(ws);
@@ -336,13 +376,14 @@ int run_product(const Request& r, cudaStream_t stream) {
     auto ok = [&](cudaError_t e) {
         if (e != cudaSuccess && rc == TGEMM_OK) rc = TGEMM_ERR_CUDA;
     };
-    tgemm::GemmArgs a{M, N, K, r.A, ld_a, r.B, ld_b, r.C, r.ldc};
+    tgemm::GemmArgs a{M, N, K, r.A, pp.ld_a, r.B, pp.ld_b, r.C, r.ldc};
     a.ep = r.ep;
     char name_pre[64] = "";
     auto note = [&](const char* what) {
         strncat(name_pre, what, sizeof(name_pre) - strlen(name_pre) - 1);
     };
-    switch (prep_a) {
+    const size_t a_off = pp.a_off, a2_off = pp.a2_off, b_off = pp.b_off, b2_off = pp.b2_off;
+    switch (pp.prep_a) {
         case TRANSPOSE:
             a.A = base + a_off;
             ok(bf16 ? tgemm::transpose_u16(r.A, r.lda, base + a_off, ldk, K, M, stream)
@@ -376,7 +417,7 @@ int run_product(const Request& r, cudaStream_t stream) {
         default:
             break;
     }
-    switch (prep_b) {
+    switch (pp.prep_b) {
         case TRANSPOSE:
             a.B = base + b_off;
             if (f32)     // stored N x K -> K x N
@@ -389,7 +430,7 @@ int run_product(const Request& r, cudaStream_t stream) {
             break;
         case REPACK:
             a.B = base + b_off;
-            if (b_kmajor)
+            if (pp.b_kmajor)
                 ok(tgemm::repack_rows(r.B, r.ldb, base + b_off, ldk, N, K, (int)esz, stream));
             else
                 ok(tgemm::repack_rows(r.B, r.ldb, base + b_off, ldn, K, N, (int)esz, stream));
@@ -417,20 +458,20 @@ int run_product(const Request& r, cudaStream_t stream) {
     }
 
     // ---- the product
-    float* partials = part_bytes ? reinterpret_cast<float*>(base + p_off) : nullptr;
+    float* partials = pp.part_bytes ? reinterpret_cast<float*>(base + pp.p_off) : nullptr;
     const char* kname = "";
     int split = 1;
     if (rc == TGEMM_OK) {
         if (f32) {
-            ok(tgemm::f32_launch(f32_id, a, fplan, partials, stream));
-            kname = tgemm::f32_kernel_name(f32_id);
-            split = fplan.split;
+            ok(tgemm::f32_launch(pp.f32_id, a, pp.fplan, partials, stream));
+            kname = tgemm::f32_kernel_name(pp.f32_id);
+            split = pp.fplan.split;
         } else {
-            ok(tgemm::tc_launch(a, path, b_kmajor ? 1 : 0, dev.num_sms, enc,
+            ok(tgemm::tc_launch(a, path, pp.b_kmajor ? 1 : 0, dev.num_sms, enc,
                                 (unsigned long long)g_wait_limit_ns.load(), g_debug_stall.load(),
-                                shape, tplan, partials, stream));
-            kname = tgemm::tc_kernel_name(path, shape);
-            split = tplan.split;
+                                pp.shape, pp.tplan, partials, stream));
+            kname = tgemm::tc_kernel_name(path, pp.shape);
+            split = pp.tplan.split;
         }
     }
     if (ws != nullptr && cudaFreeAsync(ws, stream) != cudaSuccess && rc == TGEMM_OK)
@@ -705,6 +746,24 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
         g_last_kernel = g_last_kernel_buf;
     }
     return rc;
+}
+
+long long gemm_scratch_bytes(int M, int N, int K, const void* A, long lda, const void* B,
+                             long ldb, const float* C, long ldc, int path, int flags) {
+    if (path < TGEMM_PATH_F32 || path > TGEMM_PATH_TF32X3) return -TGEMM_ERR_INVALID_ARG;
+    if ((flags & ~(TGEMM_TRANS_A | TGEMM_TRANS_B)) != 0) return -TGEMM_ERR_INVALID_ARG;
+    Request r{M, N, K, A, lda, B, ldb, const_cast<float*>(C), ldc, path, flags, tgemm::Epilogue()};
+    int st = check_request(r);
+    if (st == -1) return 0;
+    if (st != TGEMM_OK) return -st;
+    DeviceInfo dev;
+    st = current_device_info(&dev);
+    if (st != TGEMM_OK) return -st;
+    if (K == 0) return 0;
+    ProductPlan pp;
+    st = plan_product(r, dev, pp);
+    if (st != TGEMM_OK) return -st;
+    return (long long)pp.scratch;
 }
 
 int gemm_device_status(cudaStream_t stream) {

@@ -13,11 +13,15 @@
 //
 // It runs the same two kernels as gemm_tc's TF32 path (transpose of B, then
 // the persistent tcgen05 GEMM), through the same launchers; only the
-// scratch pointer differs. Nothing in the scratch has to start at zero: each
-// call writes the N x round_up(K, 4) block it reads before reading it, and
-// the padding columns are never read. All calls share the one array, so
-// calls whose work overlaps on the GPU (different streams, or different
-// host threads) race on it and give wrong results; serialise them.
+// scratch differs. The transposed rows of B are round_up(K, 32) floats apart
+// (128 bytes, as gemm_tc's scratch: the TF32 kernel ran 16 % slower on rows
+// only 16 bytes aligned) when N of them fit the array, else round_up(K, 4)
+// floats apart (16 bytes, the least the tensor-memory copies accept).
+// Nothing in the scratch has to start at zero: each call writes the N x K
+// block it reads before reading it, and the padding columns are never read.
+// All calls share the one array, so calls whose work overlaps on the GPU
+// (different streams, or different host threads) race on it and give wrong
+// results; serialise them.
 
 #include "../../include/tgemm.h"
 #include "tgemm_internal.h"
@@ -30,7 +34,9 @@ namespace {
 static __device__ __align__(256) float g_noalloc_scratch[TGEMM_NOALLOC_SCRATCH_FLOATS];
 
 constexpr int kMaxDevices = 64;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+// The transpose pre-pass covers K in 64-row tiles on a grid of at most
+// 65535 tile rows.
+constexpr long kMaxK = 65535L * 64;
 
 struct Device {
     bool ready = false;
@@ -98,8 +104,12 @@ extern "C" int gemm_tc_tf32_noalloc(int M, int N, int K, const float* A, long ld
     if (M == 0 || N == 0) return TGEMM_OK;
     if (C == nullptr || reinterpret_cast<uintptr_t>(C) % 4 != 0) return TGEMM_ERR_INVALID_ARG;
     if (K > 0 && (A == nullptr || B == nullptr)) return TGEMM_ERR_INVALID_ARG;
-    const long ldt = (K + 3) / 4 * 4;
-    if ((long long)N * ldt > (long long)TGEMM_NOALLOC_SCRATCH_FLOATS) return TGEMM_ERR_INVALID_ARG;
+    if ((long)K > kMaxK) return TGEMM_ERR_INVALID_ARG;
+    // Row pitch of B transposed: 128-byte rows when they fit, else 16-byte rows.
+    long ldt = ((long)K + 31) / 32 * 32;
+    if ((long long)N * ldt > (long long)TGEMM_NOALLOC_SCRATCH_FLOATS) ldt = ((long)K + 3) / 4 * 4;
+    if (ldt <= 0 || (long long)N * ldt > (long long)TGEMM_NOALLOC_SCRATCH_FLOATS)
+        return TGEMM_ERR_INVALID_ARG;
     if (K > 0 && (reinterpret_cast<uintptr_t>(A) % 16 != 0 || reinterpret_cast<uintptr_t>(B) % 4 != 0 ||
                   (lda * 4) % 16 != 0))
         return TGEMM_ERR_ALIGNMENT;
@@ -120,7 +130,7 @@ extern "C" int gemm_tc_tf32_noalloc(int M, int N, int K, const float* A, long ld
     // No split of the last wave: its partial tiles would need more scratch.
     const tgemm::TcPlan plan =
         tgemm::tc_plan(M, N, K, tgemm::TC_TF32, shape, d.num_sms, false, tma_c);
-    if (tgemm::tc_launch(a, tgemm::TC_TF32, 1, d.num_sms, enc, kWaitLimitNs, 0, shape, plan,
+    if (tgemm::tc_launch(a, tgemm::TC_TF32, 1, d.num_sms, enc, tgemm::wait_limit_ns(), 0, shape, plan,
                          nullptr, stream) != cudaSuccess)
         return TGEMM_ERR_CUDA;
     return TGEMM_OK;

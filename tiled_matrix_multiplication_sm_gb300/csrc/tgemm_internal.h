@@ -143,6 +143,11 @@ cudaError_t transpose_u16(const void* B, long ldb, void* Bt, long ldt, int K, in
 cudaError_t repack_rows(const void* src, long ld_src, void* dst, long ld_dst, int rows, int cols,
                         int esz, cudaStream_t s);
 
+// ---- process-wide settings (api.cu) ---------------------------------------
+// The bound on any single wait inside the tensor-core kernels, as last set
+// by gemm_set_wait_limit_ns (default 2 s).
+unsigned long long wait_limit_ns();
+
 // ---- shared helper (sgemm_f32.cu) -----------------------------------------
 // The K == 0 product: C = beta * C_old + bias (zeros for the default rule).
 cudaError_t empty_product(float* C, long ldc, int M, int N, const Epilogue& ep, cudaStream_t s);

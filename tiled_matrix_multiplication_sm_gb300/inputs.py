@@ -8,7 +8,7 @@ see identical values.
 All draws happen on a CPU ``torch.Generator`` (seed = 20260 + workload index)
 so every machine sees the same values; callers copy them to the device.
 
-The workloads are the five shapes the library is measured and checked on:
+The workloads are the shapes the library is measured and checked on:
 
 ==========  =====================  ==========================================
 name        M x N x K              values
@@ -18,7 +18,12 @@ u1024       1024 x 1024 x 1024     uniform[-1, 1] fp32
 n4096       4096 x 4096 x 4096     normal(0, 1) fp32 (FP32 path and TF32 path)
 ragged      3000 x 5001 x 1537     uniform[-1, 1] fp32, packed lda=K, ldb=N
 ffn_bf16    8192 x 14336 x 4096    bf16 rounded (RNE) from normal(0, 0.02)
+skinny_bf16 16 x 14336 x 4096      bf16 rounded (RNE) from normal(0, 0.02)
+skinny_f32  16 x 14336 x 4096      normal(0, 1) fp32 (FP32 path and TF32 path)
 ==========  =====================  ==========================================
+
+The last two are the FFN shape with only 16 rows (16 tokens): the product is
+bound by reading B once from memory, not by arithmetic.
 """
 from __future__ import annotations
 
@@ -65,6 +70,10 @@ WORKLOADS = {
         Workload(4, "ffn_bf16", 8192, 14336, 4096, "normal002", "bf16", ("bf16",),
                  check_rows=256,
                  description="FFN-shaped M=8192 tokens, K=4096, N=14336, bf16 inputs"),
+        Workload(5, "skinny_bf16", 16, 14336, 4096, "normal002", "bf16", ("bf16",),
+                 description="few rows: M=16 tokens, K=4096, N=14336, bf16 inputs"),
+        Workload(6, "skinny_f32", 16, 14336, 4096, "normal", "f32", ("f32", "tf32"),
+                 description="few rows: M=16, K=4096, N=14336, normal(0,1) fp32"),
     ]
 }
 
