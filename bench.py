@@ -12,7 +12,8 @@ The JSON line also reports
   roofline     - for the dominant kernel (the FP32 SGEMM): achieved TFLOP/s
                  against the FP32 CUDA-core peak (SMs x 128 lanes x 2 FLOP x
                  the maximum SM clock), with DRAM traffic from the committed
-                 ncu summary when it matches the current kernel source;
+                 ncu evidence record (profiles/ncu) when it matches the
+                 current kernel source;
   paths        - each path's own TFLOP/s and roofline fraction in the step;
   workloads    - the other measured shapes: 1024^3 and 3000x5001x1537 on the
                  FP32 path, the FFN shape 8192x14336x4096 on the BF16 path;
@@ -32,7 +33,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -47,8 +47,7 @@ METRIC = "GEMM TFLOP/s (2MNK/device time) and % of FP32 / tensor-core peak"
 UNIT = "TFLOP/s"
 WORKLOAD = "n4096"
 FLUSH_BYTES = 256 * 1024 * 1024
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "sgemm_f32_n4096.md")
-F32_SOURCE = os.path.join(ROOT, "tiled_matrix_multiplication_sm_gb300", "csrc", "sgemm_f32.cu")
+NCU_RECORDS = os.path.join(ROOT, "profiles", "ncu")
 
 # Nominal dense tensor rates (PFLOP/s) used to scale the measured BF16 peak to
 # another input type: TF32 runs at 1.1 / 2.25 of the BF16 rate.
@@ -83,23 +82,19 @@ def file_sha256(path: str) -> str:
     return h.hexdigest()
 
 
-def committed_traffic(summary=PROFILE_SUMMARY, source=F32_SOURCE):
-    """DRAM bytes per launch of the FP32 SGEMM from the committed ncu summary,
-    or None when there is none or the kernel source changed since."""
-    try:
-        with open(summary) as f:
-            text = f.read()
-    except OSError:
-        return None
-    m = re.search(r"^bench-traffic:\s*(\{.*\})\s*$", text, re.M)
-    if not m:
+def committed_traffic(records=NCU_RECORDS, case="n4096:f32", kernel="sgemm_kernel", root=ROOT):
+    """DRAM bytes (read + write) of one launch of `kernel` in `case`, from the
+    committed ncu evidence record, or None when there is none or the kernel's
+    source changed since it was taken."""
+    from tiled_matrix_multiplication_sm_gb300 import evidence
+    rec = evidence.find_record(records, case, kernel)
+    if rec is None or not rec.get("source"):
         return None
     try:
-        rec = json.loads(m.group(1))
-        if rec.get("source_sha256") != file_sha256(source):
+        if rec.get("source_sha256") != file_sha256(os.path.join(root, rec["source"])):
             return None
-        return int(rec["dram_bytes_per_launch"])
-    except (ValueError, KeyError, OSError):
+        return int(rec["derived"]["dram_bytes"])
+    except (OSError, KeyError, TypeError, ValueError):
         return None
 
 

@@ -348,10 +348,14 @@ TGEMM_API const char* gemm_f32_kernel_name(int id);
 
 /*
  * gemm_last_kernel — name of the kernel(s) the most recent successful
- * gemm_f32 or gemm_tc call on this thread launched, joined by '+' when a call
- * launched more than one (e.g. a split-K reduction or the TF32 transpose), or
- * "" if none did (empty product, error). Valid until the thread's next call.
- * For tests and benchmarks.
+ * gemm_f32, gemm_tc or gemm_ex call on this thread launched, in launch
+ * order, joined by '+' when a call launched more than one: the pre-passes
+ * (repack_a, repack_b, transpose_a, transpose_b, split_a, split_b,
+ * transpose_split_a, transpose_split_b), the GEMM kernel's configuration
+ * name, and "splitk_reduce(split=S,tiles=T)" when T tiles of a partial last
+ * wave were computed in S K-pieces each and summed by a reduction kernel;
+ * "empty_product" for K == 0, "" if nothing was launched (empty output,
+ * error). Valid until the thread's next call. For tests and benchmarks.
  */
 TGEMM_API const char* gemm_last_kernel(void);
 

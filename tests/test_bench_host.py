@@ -54,13 +54,15 @@ def test_parse_clock_samples():
 def test_committed_traffic_requires_matching_source(tmp_path):
     src = tmp_path / "k.cu"
     src.write_text("kernel v1")
-    summ = tmp_path / "s.md"
-    rec = {"dram_bytes_per_launch": 123456, "source_sha256": bench.file_sha256(str(src))}
-    summ.write_text("# summary\n\nbench-traffic: " + json.dumps(rec) + "\n")
-    assert bench.committed_traffic(str(summ), str(src)) == 123456
+    recs = tmp_path / "ncu"
+    recs.mkdir()
+    rec = {"source": "k.cu", "source_sha256": bench.file_sha256(str(src)),
+           "derived": {"dram_bytes": 123456}}
+    (recs / "sgemm_kernel__n4096_f32__0_f32_128x256.json").write_text(json.dumps(rec))
+    assert bench.committed_traffic(str(recs), root=str(tmp_path)) == 123456
     src.write_text("kernel v2")
-    assert bench.committed_traffic(str(summ), str(src)) is None
-    assert bench.committed_traffic(str(tmp_path / "none.md"), str(src)) is None
+    assert bench.committed_traffic(str(recs), root=str(tmp_path)) is None
+    assert bench.committed_traffic(str(tmp_path / "none"), root=str(tmp_path)) is None
 
 
 def test_aggregate_uses_slowest_rank():

@@ -1,0 +1,78 @@
+"""Host-side logic of the ncu evidence harness (no GPU, no ncu): parsing of
+ncu's raw CSV, pairing of profiled launches with the library's kernel names,
+algorithmic work and roofline fractions of each kind of kernel."""
+import json
+
+import pytest
+
+from tiled_matrix_multiplication_sm_gb300 import evidence
+
+RAW = '''"ID","Kernel Name","gpu__time_duration.sum","dram__bytes_read.sum","dram__bytes_write.sum","sm__cycles_elapsed.avg.per_second","l1tex__data_bank_conflicts_pipe_lsu_mem_shared_op_ld.sum"
+"","","nsecond","byte","byte","hz",""
+"0","void tgemm::(anonymous namespace)::transpose_kernel<float>(const T1 *, long, T1 *, long, int, int)","20,000","67,108,864","67,108,864","2,070,000,000","0"
+"1","void tgemm::(anonymous namespace)::tc_gemm_2sm_kernel<4, true, false, 2>(CUtensorMap, CUtensorMap)","160,000","134,217,728","67,108,864","2,000,000,000","12"
+'''
+
+
+def test_parse_raw_csv_drops_units_row_and_commas():
+    rows = evidence.parse_raw_csv("==PROF== noise\n" + RAW)
+    assert len(rows) == 2
+    assert evidence.number(rows[0]["gpu__time_duration.sum"]) == 20000.0
+    assert evidence.short_name(rows[1]["Kernel Name"]) == "tc_gemm_2sm_kernel"
+    assert evidence.source_of(rows[0]["Kernel Name"]) == "transpose_f32.cu"
+    assert evidence.source_of(rows[1]["Kernel Name"]) == "gemm_tcgen05.cu"
+
+
+def test_short_names_of_ncu_renderings():
+    for raw in ["void unnamed>::repack_kernel<float>(const T1 *, long, T1 *, long, int, int)",
+                "unnamed>::tc_splitk_reduce(unnamed>::TcParams)",
+                "void tgemm::<unnamed>::tc_gemm_2sm_kernel<4, 1, 0, 1>(CUtensorMap_st, "
+                "unnamed>::TcParams)",
+                "void unnamed>::sgemm_kernel<unnamed>::Tile<128, 256, 32, 32, 128, 3, 1, 1>, 1, "
+                "1>(unnamed>::F32Params)",
+                "void tgemm::(anonymous namespace)::splitk_reduce<tgemm::(anonymous namespace)::"
+                "Tile<1, 2>>(tgemm::(anonymous namespace)::F32Params)"]:
+        assert evidence.short_name(raw) in ("repack_kernel", "tc_splitk_reduce",
+                                            "tc_gemm_2sm_kernel", "sgemm_kernel",
+                                            "splitk_reduce"), raw
+
+
+def test_records_pair_launches_with_library_names():
+    rows = evidence.parse_raw_csv(RAW)
+    peaks = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0, "source": "test"}
+    recs = evidence.make_records(rows, ["transpose_b", "tc_tf32_2sm_256x512x32_s4_persistent"],
+                                 "n4096:tf32", "cmd", "ncu cmd", peaks, 152)
+    t, g = recs
+    # transpose: 8 K N bytes algorithmic, 134 MB in 20 us = 6710.9 GB/s
+    assert t["roofline"]["bound"] == "hbm"
+    assert t["roofline"]["algorithmic_bytes"] == 8 * 4096 * 4096
+    assert t["roofline"]["achieved"] == pytest.approx(8 * 4096 ** 2 / 20000, rel=1e-3)
+    assert t["roofline"]["traffic_over_algorithmic"] == pytest.approx(1.0)
+    # GEMM: 2 M N K over 160 us against 1900 x 1.1 / 2.25
+    assert g["roofline"]["bound"] == "tensor"
+    assert g["roofline"]["achieved"] == pytest.approx(2 * 4096 ** 3 / 160000 / 1e3, rel=1e-3)
+    assert g["roofline"]["peak"] == pytest.approx(1900 * 1.1 / 2.25, rel=1e-3)
+    assert g["metrics"]["l1tex__data_bank_conflicts_pipe_lsu_mem_shared_op_ld.sum"] == 12
+    assert evidence.record_filename(g).startswith("tc_gemm_2sm_kernel__n4096_tf32__1_")
+    json.dumps(recs)
+
+
+def test_algorithmic_work_of_each_kind():
+    w = evidence.algorithmic_work
+    assert w("repack_a", "ragged:tf32")["bytes"] == 2 * 3000 * 1537 * 4
+    assert w("repack_b", "ragged:f32")["bytes"] == 2 * 1537 * 5001 * 4
+    assert w("split_a", "n4096:tf32x3")["bytes"] == 12 * 4096 * 4096
+    assert w("tc_tf32x3_2sm_256x256x32_s3_persistent", "n4096:tf32x3")["flop"] == 3 * 2 * 4096 ** 3
+    assert w("f32_128x256x32_s3_ffma2_vecA_vecB", "u1024:f32") == {"bound": "alu",
+                                                                   "flop": 2 * 1024 ** 3}
+    assert w("empty_product", "k0:f32")["bytes"] == 4 * 4096 * 4096
+    r = w("splitk_reduce(split=8,tiles=56)", "n4096:f32")
+    assert (r["split"], r["tiles"], r["bytes_per_tile_elem"]) == (8, 56, 36)
+    assert evidence.tile_elems("f32_128x256x32_s3_ffma2_vecA_vecB") == 128 * 256
+
+
+def test_every_case_names_a_workload():
+    for case in evidence.CASES:
+        wl, path, M, N, K, dtype = evidence.case_shape(case)
+        assert path in ("f32", "tf32", "bf16", "tf32x3")
+        assert (wl is None) == (K == 0)

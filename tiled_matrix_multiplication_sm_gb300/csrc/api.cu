@@ -460,25 +460,28 @@ int run_product(const Request& r, cudaStream_t stream) {
     // ---- the product
     float* partials = pp.part_bytes ? reinterpret_cast<float*>(base + pp.p_off) : nullptr;
     const char* kname = "";
-    int split = 1;
+    int split = 1, split_tiles = 0;
     if (rc == TGEMM_OK) {
         if (f32) {
             ok(tgemm::f32_launch(pp.f32_id, a, pp.fplan, partials, stream));
             kname = tgemm::f32_kernel_name(pp.f32_id);
             split = pp.fplan.split;
+            split_tiles = pp.fplan.tiles_m * pp.fplan.tiles_n - pp.fplan.dp_tiles;
         } else {
             ok(tgemm::tc_launch(a, path, pp.b_kmajor ? 1 : 0, dev.num_sms, enc,
                                 (unsigned long long)g_wait_limit_ns.load(), g_debug_stall.load(),
                                 pp.shape, pp.tplan, partials, stream));
             kname = tgemm::tc_kernel_name(path, pp.shape);
             split = pp.tplan.split;
+            split_tiles = pp.tplan.tiles_m * pp.tplan.tiles_n - pp.tplan.dp_tiles;
         }
     }
     if (ws != nullptr && cudaFreeAsync(ws, stream) != cudaSuccess && rc == TGEMM_OK)
         rc = TGEMM_ERR_CUDA;
     if (rc == TGEMM_OK) {
         char tail[48] = "";
-        if (split > 1) snprintf(tail, sizeof(tail), "+splitk_reduce(split=%d)", split);
+        if (split > 1)
+            snprintf(tail, sizeof(tail), "+splitk_reduce(split=%d,tiles=%d)", split, split_tiles);
         snprintf(g_last_kernel_buf, sizeof(g_last_kernel_buf), "%s%s%s", name_pre, kname, tail);
         g_last_kernel = g_last_kernel_buf;
     }
