@@ -5,8 +5,9 @@ the square 4096^3 product (A, B ~ N(0,1) fp32, row-major) computed once on
 each path of the library -- the FP32 CUDA-core SGEMM (gemm_f32) and the
 tcgen05 tensor-core GEMM in TF32 (gemm_tc; a B-transpose pre-pass plus the
 GEMM). The metric is TFLOP/s = (2 M N K per product x 2 products) / device
-time, timed with CUDA events on the launching stream, L2 flushed (a 256 MiB
-write) before every timed step.
+time, timed with CUDA events on the launching stream, L2 flushed before
+every timed step (a 256 MiB write, then a 256 MiB read of another buffer, so
+that the timed kernels start on a cold L2 holding no dirty lines).
 
 The JSON line also reports
   roofline     - for the dominant kernel (the FP32 SGEMM): achieved TFLOP/s
@@ -262,6 +263,22 @@ def event_pair():
     return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
 
+class L2Flush:
+    """Leaves the 129 MB L2 cold and clean: a write of one buffer larger than
+    L2 evicts everything, then a read of a second one evicts the written
+    (dirty) lines, so that the next kernel neither hits in L2 nor pays for
+    the write-back of the flush's own lines."""
+
+    def __init__(self, device, nbytes=FLUSH_BYTES):
+        import torch
+        self.w = torch.empty(nbytes // 4, dtype=torch.float32, device=device)
+        self.r = torch.zeros(nbytes // 4, dtype=torch.float32, device=device)
+
+    def zero_(self):
+        self.w.zero_()
+        self.r.sum()
+
+
 def time_calls(fn, reps, flush):
     """Median device time (ms) of fn() with L2 flushed before each call."""
     import torch
@@ -301,7 +318,7 @@ def run_gpu(args):
     B = B_host.to(dev)
     C32 = torch.empty(w.M, w.N, device=dev)
     Ctf = torch.empty(w.M, w.N, device=dev)
-    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     def step():
         tg.gemm_f32(A, B, out=C32)
         n32 = len(tg.binding.last_kernel().split("+"))
@@ -354,7 +371,8 @@ def run_gpu(args):
                                "(seed 20262); one product on the FP32 CUDA-core path and one on "
                                "the tcgen05 TF32 path per step",
                    "M": w.M, "N": w.N, "K": w.K, "paths": ["f32", "tf32"],
-                   "l2": "flushed before every timed step (256 MiB write)",
+                   "l2": "flushed before every timed step: a 256 MiB write, then a 256 MiB "
+                         "read of a second buffer (cold, clean L2)",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "gpu_launches": K * launches_per_step,
         "roofline": {"bound": "alu", "kernel": "gemm_f32 (CUDA-core FFMA)",
@@ -609,7 +627,7 @@ def run_single(args):
     A_host, B_host = inputs.operands(w)
     A, B = A_host.to(dev), B_host.to(dev)
     C = torch.empty(w.M, w.N, device=dev)
-    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     if path == "f32":
         fn = lambda: tg.gemm_f32(A, B, out=C)          # noqa: E731
         peak, bound = fp32_peak_tflops(props.multi_processor_count, peaks["sm_max_mhz"]), "alu"
@@ -645,7 +663,7 @@ def run_cublas_context(args):
     from tiled_matrix_multiplication_sm_gb300 import inputs
 
     dev = torch.device("cuda", 0)
-    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     res = {}
     cases = {"u1024": ("f32",), "n4096": ("f32", "tf32"), "ragged": ("f32", "tf32"),
              "ffn_bf16": ("bf16",)}

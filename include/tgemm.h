@@ -337,6 +337,22 @@ TGEMM_API int gemm_set_f32_kernel(int id);
  */
 TGEMM_API int gemm_set_tc_kernel(int mode);
 
+/*
+ * gemm_set_tc_streamk — the stream-K tail of the tensor-core kernels (for
+ * tests and tuning). When a product's tiles do not fill whole rounds of the
+ * SMs (one-SM kernel) or SM pairs, the tiles of the partial last round can
+ * instead have their K blocks shared evenly by S of them inside the same
+ * launch: each computes a share of at most one tile's length, writes the
+ * partial tile of a share that does not end a tile to scratch, and the SM
+ * or pair whose share ends a tile adds the partial tiles of the shares
+ * before it (fixed order: deterministic) and stores the tile. -1 (default)
+ * takes S from a timing model (or no sharing), 0 never shares, S > 0 shares
+ * the tail among S (clamped to the SMs or pairs available and to the tail's
+ * K blocks; no sharing if that leaves S at or below the tail's tile count).
+ * Process-wide. Returns TGEMM_OK or TGEMM_ERR_INVALID_ARG (slots < -1).
+ */
+TGEMM_API int gemm_set_tc_streamk(int slots);
+
 /* Number of FP32 kernel configurations gemm_set_f32_kernel accepts. */
 TGEMM_API int gemm_f32_kernel_count(void);
 
@@ -353,7 +369,10 @@ TGEMM_API const char* gemm_f32_kernel_name(int id);
  * (repack_a, repack_b, transpose_a, transpose_b, split_a, split_b,
  * transpose_split_a, transpose_split_b), the GEMM kernel's configuration
  * name, and "splitk_reduce(split=S,tiles=T)" when T tiles of a partial last
- * wave were computed in S K-pieces each and summed by a reduction kernel;
+ * wave were computed in S K-pieces each and summed by a reduction kernel
+ * (FP32 path); a tensor-core kernel's name carries "(streamk:slots=S,tiles=T)"
+ * when the K blocks of the T tiles of its partial last round were shared by
+ * S SMs or SM pairs inside the kernel (no extra launch);
  * "empty_product" for K == 0, "" if nothing was launched (empty output,
  * error). Valid until the thread's next call. For tests and benchmarks.
  */

@@ -103,13 +103,20 @@ def test_k_zero_applies_output_rule(tgemm):
 
 @pytest.mark.parametrize("path", PATHS)
 def test_split_k_tail_applies_rule_once(tgemm, path):
-    """A shape whose last wave is split along K: the reduction, not each
-    piece, applies alpha, beta and bias."""
+    """A shape whose last wave is split along K: the reduction (FP32 path) or
+    the owner of each shared tile (tensor paths, stream-K), not each piece,
+    applies alpha, beta and bias."""
     M, N, K = 256, 512, 2048
     As, Bs, C0, bias = case(M, N, K, "int4", path, 77, False, True)
     C = C0.clone().cuda()
-    tgemm.binding.gemm_ex(As.cuda(), Bs.cuda(), path, trans_b=True, alpha=-1.0, beta=1.0,
-                          bias=bias.cuda(), out=C)
-    assert "splitk_reduce" in tgemm.binding.last_kernel()
+    if path != "f32":
+        assert tgemm.binding.set_tc_streamk(40) == 0
+    try:
+        tgemm.binding.gemm_ex(As.cuda(), Bs.cuda(), path, trans_b=True, alpha=-1.0, beta=1.0,
+                              bias=bias.cuda(), out=C)
+        name = tgemm.binding.last_kernel()
+    finally:
+        tgemm.binding.set_tc_streamk(-1)
+    assert ("splitk_reduce" if path == "f32" else "streamk:slots=40") in name, name
     ref, _ = oracle.gemm_ex(As, Bs, trans_b=True, alpha=-1.0, beta=1.0, C0=C0, bias=bias)
     assert_bit_exact(C, ref, f"{path} split rule")

@@ -7,6 +7,8 @@ needs neither allocates nothing. These tests pin the sizes the query reports
 for each case against the rule written in the header, and run each product to
 check that the planned call gives the oracle's result.
 """
+import re
+
 import pytest
 import torch
 
@@ -74,19 +76,28 @@ def test_bf16_whole_waves_allocate_nothing(tgemm):
         tgemm.binding.set_tc_kernel(-1)
 
 
-# Any split tail adds whole FP32 partial tiles of 256 x 256 or 256 x 512.
-PAIR_TILE_BYTES = 256 * 256 * 4
+def streamk_bytes(name):
+    """Scratch of a stream-K tail named in a last-kernel record: one partial
+    tile per sharing slot, then one counter per tail tile."""
+    m = re.search(r"(\d+)x(\d+)x\d+_s\d+_persistent\(streamk:slots=(\d+),tiles=(\d+)\)", name)
+    if not m:
+        return 0
+    rows, cols, slots, tiles = (int(x) for x in m.groups())
+    if "2sm" in name:
+        rows = 256
+    return round_up(slots * rows * cols * 4, 256) + round_up(tiles * 4, 256)
 
 
 def test_tf32_transposes_b(tgemm):
-    """TF32 always writes B transposed, N x round_up(K, 32) floats (plus the
-    partial tiles if the planner splits the two tiles along K)."""
+    """TF32 always writes B transposed, N x round_up(K, 32) floats, plus the
+    stream-K tail's partial tiles and counters when the planner shares the
+    two tiles among SM pairs."""
     M, N, K = 200, 300, 1000
     A, B = int_operands(M, N, K, torch.float32, 3)
-    bt = round_up(N * round_up(K, 32) * 4, 256)
     n = tgemm.binding.scratch_bytes(A, B, "tf32")
-    assert n >= bt and (n - bt) % PAIR_TILE_BYTES == 0
     check_product(tgemm, A, B, "tf32")
+    bt = round_up(N * round_up(K, 32) * 4, 256)
+    assert n == bt + streamk_bytes(tgemm.binding.last_kernel()), tgemm.binding.last_kernel()
 
 
 def test_unaligned_rows_are_repacked(tgemm):
@@ -96,5 +107,23 @@ def test_unaligned_rows_are_repacked(tgemm):
     A, B = int_operands(M, N, K, torch.bfloat16, 4)
     want = round_up(M * round_up(K, 64) * 2, 256) + round_up(K * round_up(N, 64) * 2, 256)
     n = tgemm.binding.scratch_bytes(A, B, "bf16")
-    assert n >= want and (n - want) % PAIR_TILE_BYTES == 0
     check_product(tgemm, A, B, "bf16")
+    assert n == want + streamk_bytes(tgemm.binding.last_kernel()), tgemm.binding.last_kernel()
+
+
+def test_forced_stream_k_draws_partials_and_counters(tgemm):
+    """256 x 256 pair tiles, 6 tiles shared by 40 pairs: 40 partial tiles and
+    6 counters (rows of A and B on 16-byte boundaries: nothing repacked)."""
+    M, N, K = 300, 704, 1032
+    A, B = int_operands(M, N, K, torch.bfloat16, 5)
+    tgemm.binding.set_tc_kernel(1)
+    tgemm.binding.set_tc_streamk(40)
+    try:
+        n = tgemm.binding.scratch_bytes(A, B, "bf16")
+        check_product(tgemm, A, B, "bf16")
+        name = tgemm.binding.last_kernel()
+    finally:
+        tgemm.binding.set_tc_kernel(-1)
+        tgemm.binding.set_tc_streamk(-1)
+    assert "streamk:slots=40,tiles=6" in name, name
+    assert n == round_up(40 * 256 * 256 * 4, 256) + 256

@@ -170,6 +170,26 @@ def test_unaligned_output_rows_every_phase(tgemm, tc_mode, kind, ldc, offset):
 
 
 @pytest.mark.parametrize("kind", ["tf32", "bf16"])
+@pytest.mark.parametrize("N", [33, 34, 35, 289, 291])
+def test_unaligned_output_rows_short_last_block(tgemm, tc_mode, kind, N):
+    """C rows off 16-byte boundaries (ldc = N + 1: every phase occurs) where
+    the last 32-column block at N holds only 1-3 columns after a full block:
+    the values carried from the full block must still be stored. Bit-exact on
+    integers; padding and guard bands untouched."""
+    M, K, ldc = 200, 40, N + 1
+    A, B = operands(M, N, K, "int4", kind, seed=N)
+    guard = 64
+    store = torch.full((guard + M * ldc + guard,), -333.0, device="cuda")
+    C = store[guard:guard + M * ldc].view(M, ldc)[:, :N]
+    tgemm.gemm_tc(A.cuda(), B.cuda(), kind, out=C)
+    assert tgemm.device_status() == 0
+    assert_bit_exact(C, oracle.gemm(A, B)[0], f"{kind} N={N}")
+    host = store.cpu()
+    assert (host[:guard] == -333.0).all() and (host[guard + M * ldc:] == -333.0).all()
+    assert (host[guard:guard + M * ldc].view(M, ldc)[:, N:] == -333.0).all()
+
+
+@pytest.mark.parametrize("kind", ["tf32", "bf16"])
 @pytest.mark.parametrize("shape", [(16, 12, 12), (130, 261, 77), (300, 1001, 517),
                                    (203, 2051, 1031)])
 def test_unaligned_leading_dimensions(tgemm, tc_mode, kind, shape):
@@ -254,10 +274,12 @@ def test_auto_shape_takes_wide_tiles_for_long_k(tgemm):
 
 
 @pytest.mark.parametrize("kind", ["tf32", "bf16"])
-def test_wide_tiles_split_tail_full_output_rule(tgemm, kind):
-    """256 x 512 tiles whose only (partial) wave is split along K: the pieces
-    leave raw partial tiles and the reduction applies alpha, beta and bias;
-    C's rows are not 16-byte aligned. Integer data: bit-exact."""
+@pytest.mark.parametrize("slots", [7, 76])
+def test_wide_tiles_stream_k_full_output_rule(tgemm, kind, slots):
+    """256 x 512 tiles whose only (partial) round is shared by `slots` SM
+    pairs (stream-K): contributions leave raw partial tiles and each owner
+    adds them and applies alpha, beta and bias once; C's rows are not
+    16-byte aligned (register stores). Integer data: bit-exact."""
     M, N, K = 512, 1530, 2048
     g = inputs.generator(32)
     A = inputs.draw(M, K, "int4", g).to(DTYPES[kind])
@@ -266,16 +288,18 @@ def test_wide_tiles_split_tail_full_output_rule(tgemm, kind):
     bias = inputs.draw(1, N, "int4", g)[0]
     C = C0.clone().cuda()
     assert tgemm.binding.set_tc_kernel(2) == 0
+    assert tgemm.binding.set_tc_streamk(slots) == 0
     try:
         tgemm.binding.gemm_ex(A.cuda(), B.cuda(), kind, alpha=2.0, beta=-1.0, bias=bias.cuda(),
                               out=C)
         name = tgemm.binding.last_kernel()
     finally:
         tgemm.binding.set_tc_kernel(-1)
+        tgemm.binding.set_tc_streamk(-1)
     assert tgemm.device_status() == 0
-    assert "256x512" in name and "splitk_reduce" in name, name
+    assert "256x512" in name and f"streamk:slots={slots},tiles=6" in name, name
     ref, _ = oracle.gemm_ex(A, B, alpha=2.0, beta=-1.0, C0=C0, bias=bias)
-    assert_bit_exact(C, ref, f"wide split {kind}")
+    assert_bit_exact(C, ref, f"wide stream-K {kind}")
 
 
 # ---------------------------------------------------------------- split TF32 (TGEMM_TF32X3)

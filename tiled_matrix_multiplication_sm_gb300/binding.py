@@ -47,6 +47,7 @@ _SIGNATURES = {
     "gemm_set_debug_stall": (ctypes.c_int, [ctypes.c_int]),
     "gemm_set_f32_kernel": (ctypes.c_int, [ctypes.c_int]),
     "gemm_set_tc_kernel": (ctypes.c_int, [ctypes.c_int]),
+    "gemm_set_tc_streamk": (ctypes.c_int, [ctypes.c_int]),
     "gemm_f32_kernel_count": (ctypes.c_int, []),
     "gemm_f32_kernel_name": (ctypes.c_char_p, [ctypes.c_int]),
     "gemm_last_kernel": (ctypes.c_char_p, []),
@@ -253,6 +254,12 @@ def set_tc_kernel(mode: int) -> int:
     """-1: by shape; 0: one-SM tcgen05 kernel (128 x 256 tiles); 1: 2-SM
     (CTA pair) kernel, 256 x 256 tiles; 2: 2-SM kernel, 256 x 512 tiles."""
     return int(load().gemm_set_tc_kernel(int(mode)))
+
+
+def set_tc_streamk(slots: int) -> int:
+    """Stream-K tail of the tensor-core kernels: -1 automatic, 0 never, S > 0
+    shared by S SMs or SM pairs where the tail allows it."""
+    return int(load().gemm_set_tc_streamk(int(slots)))
 
 
 def f32_kernel_names():

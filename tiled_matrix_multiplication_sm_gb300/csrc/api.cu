@@ -39,6 +39,7 @@ std::atomic<long long> g_wait_limit_ns{2000000000LL};
 std::atomic<int> g_debug_stall{0};
 std::atomic<int> g_forced_f32{-1};
 std::atomic<int> g_tc_mode{-1};
+std::atomic<int> g_tc_streamk{-1};
 thread_local const char* g_last_kernel = "";
 thread_local char g_last_kernel_buf[160];
 
@@ -318,9 +319,10 @@ int plan_product(const Request& r, const DeviceInfo& dev, ProductPlan& pp) {
         // Whole tiles leave by TMA stores when C's base and rows are 16-byte
         // aligned and beta = 0 (the model charges the wide tiles more otherwise).
         const bool tma_c = reinterpret_cast<uintptr_t>(r.C) % 16 == 0 && r.ldc % 4 == 0 &&
-                           r.ep.beta == 0.0f;
-        pp.shape = tgemm::tc_shape(M, N, K, path, g_tc_mode.load(), dev.num_sms, true, tma_c);
-        pp.tplan = tgemm::tc_plan(M, N, K, path, pp.shape, dev.num_sms, true, tma_c);
+                           N % 4 == 0 && r.ep.beta == 0.0f;
+        const int sk = g_tc_streamk.load();
+        pp.shape = tgemm::tc_shape(M, N, K, path, g_tc_mode.load(), dev.num_sms, sk, tma_c);
+        pp.tplan = tgemm::tc_plan(M, N, K, path, pp.shape, dev.num_sms, sk, tma_c);
     }
     pp.part_bytes = f32 ? pp.fplan.scratch_bytes : pp.tplan.scratch_bytes;
     pp.p_off = pp.part_bytes ? cv.take(pp.part_bytes) : 0;
@@ -460,28 +462,27 @@ int run_product(const Request& r, cudaStream_t stream) {
     // ---- the product
     float* partials = pp.part_bytes ? reinterpret_cast<float*>(base + pp.p_off) : nullptr;
     const char* kname = "";
-    int split = 1, split_tiles = 0;
+    char tail[64] = "";
     if (rc == TGEMM_OK) {
         if (f32) {
             ok(tgemm::f32_launch(pp.f32_id, a, pp.fplan, partials, stream));
             kname = tgemm::f32_kernel_name(pp.f32_id);
-            split = pp.fplan.split;
-            split_tiles = pp.fplan.tiles_m * pp.fplan.tiles_n - pp.fplan.dp_tiles;
+            if (pp.fplan.split > 1)
+                snprintf(tail, sizeof(tail), "+splitk_reduce(split=%d,tiles=%d)", pp.fplan.split,
+                         pp.fplan.tiles_m * pp.fplan.tiles_n - pp.fplan.dp_tiles);
         } else {
-            ok(tgemm::tc_launch(a, path, pp.b_kmajor ? 1 : 0, dev.num_sms, enc,
+            ok(tgemm::tc_launch(a, path, pp.b_kmajor ? 1 : 0, enc,
                                 (unsigned long long)g_wait_limit_ns.load(), g_debug_stall.load(),
                                 pp.shape, pp.tplan, partials, stream));
             kname = tgemm::tc_kernel_name(path, pp.shape);
-            split = pp.tplan.split;
-            split_tiles = pp.tplan.tiles_m * pp.tplan.tiles_n - pp.tplan.dp_tiles;
+            if (pp.tplan.sk_slots > 0)
+                snprintf(tail, sizeof(tail), "(streamk:slots=%d,tiles=%d)", pp.tplan.sk_slots,
+                         pp.tplan.tiles_m * pp.tplan.tiles_n - pp.tplan.dp_tiles);
         }
     }
     if (ws != nullptr && cudaFreeAsync(ws, stream) != cudaSuccess && rc == TGEMM_OK)
         rc = TGEMM_ERR_CUDA;
     if (rc == TGEMM_OK) {
-        char tail[48] = "";
-        if (split > 1)
-            snprintf(tail, sizeof(tail), "+splitk_reduce(split=%d,tiles=%d)", split, split_tiles);
         snprintf(g_last_kernel_buf, sizeof(g_last_kernel_buf), "%s%s%s", name_pre, kname, tail);
         g_last_kernel = g_last_kernel_buf;
     }
@@ -591,8 +592,9 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
         part_off[i] = total;
         if (K == 0) continue;
         if (tc) {
-            shape[i] = tgemm::tc_shape(rows, N, K, in_type, g_tc_mode.load(), dev.num_sms, true);
-            tc_plan[i] = tgemm::tc_plan(rows, N, K, in_type, shape[i], dev.num_sms, true);
+            const int sk = g_tc_streamk.load();
+            shape[i] = tgemm::tc_shape(rows, N, K, in_type, g_tc_mode.load(), dev.num_sms, sk);
+            tc_plan[i] = tgemm::tc_plan(rows, N, K, in_type, shape[i], dev.num_sms, sk);
             total += align256(tc_plan[i].scratch_bytes);
         } else {
             // Device operands are 16-byte aligned: the vector loaders apply.
@@ -696,7 +698,7 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
             tgemm::GemmArgs pa{rows, N, K, A_hi + r0 * lda_d, lda_d, Bt, ldt, Cp, ldc_d};
             pa.A2 = A_lo + r0 * lda_d;
             pa.B2 = Bt_lo;
-            ok(tgemm::tc_launch(pa, in_type, 1, dev.num_sms, enc, limit, stall, shape[i],
+            ok(tgemm::tc_launch(pa, in_type, 1, enc, limit, stall, shape[i],
                                 tc_plan[i], part, stream));
             name = tgemm::tc_kernel_name(in_type, shape[i]);
         } else if (tc) {
@@ -704,7 +706,7 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
             tgemm::GemmArgs pa{rows, N, K, Ad + r0 * lda_d * esz, lda_d,
                                tf32 ? static_cast<const void*>(Bt) : Bd, tf32 ? ldt : ldb_d, Cp,
                                ldc_d};
-            ok(tgemm::tc_launch(pa, in_type, tf32 ? 1 : 0, dev.num_sms, enc, limit, stall, shape[i],
+            ok(tgemm::tc_launch(pa, in_type, tf32 ? 1 : 0, enc, limit, stall, shape[i],
                                 tc_plan[i], part, stream));
             name = tgemm::tc_kernel_name(in_type, shape[i]);
         } else if (i == 0 && nh > 0) {
@@ -854,6 +856,12 @@ int gemm_set_f32_kernel(int id) {
 int gemm_set_tc_kernel(int mode) {
     if (mode < -1 || mode > 2) return TGEMM_ERR_INVALID_ARG;
     g_tc_mode.store(mode);
+    return TGEMM_OK;
+}
+
+int gemm_set_tc_streamk(int slots) {
+    if (slots < -1) return TGEMM_ERR_INVALID_ARG;
+    g_tc_streamk.store(slots);
     return TGEMM_OK;
 }
 

@@ -92,10 +92,18 @@ struct Sync {
     int abort;
 };
 
-// Epilogue staging: EPI_BUFS 32 x 32 FP32 blocks per epilogue warp.
+// Epilogue staging: EPI_BUFS 32 x 32 FP32 blocks per epilogue warp (TMA
+// stores of C). The one-SM and 256 x 256 kernels give each warp a larger
+// region, EPI_REGION bytes (a multiple of 1 KB, so that the swizzled block
+// at its start stays aligned to its swizzle pattern), which also holds the
+// 32 row slots of 36 floats (144 bytes) of the row-copy epilogue.
 constexpr int EPI_BUFS = 1;
 constexpr int EPI_WARP_BYTES = EPI_BUFS * 32 * 32 * 4;
-constexpr int EPI_STAGE_BYTES = 4 * EPI_WARP_BYTES;
+constexpr int ROW_SLOT_FLOATS = 36;
+constexpr int EPI_REGION = 5 * 1024;
+static_assert(32 * ROW_SLOT_FLOATS * 4 <= EPI_REGION && EPI_WARP_BYTES <= EPI_REGION,
+              "epilogue region");
+constexpr int EPI_STAGE_BYTES = 4 * EPI_REGION;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_STAGE_BYTES + (int)sizeof(Sync);
 static_assert(SMEM_BYTES <= 227 * 1024, "one-SM kernel exceeds the shared memory of a block");
 
@@ -106,10 +114,16 @@ struct TcParams {
     int tiles_m, tiles_n, num_tiles, kblocks;
     int tile_rows;       // rows of a tile: 128 (one SM) or 256 (SM pair)
     int tile_cols;       // columns of a tile: 256, or 512 (wide SM-pair tiles)
-    int dp_tiles;        // tiles [0, dp_tiles) are computed whole
-    int split;           // the others in `split` K-pieces each (1: none)
-    int num_units;       // dp_tiles + (num_tiles - dp_tiles) * split
-    float* partials;     // one tile_rows x tile_cols partial tile per K-piece
+    int num_slots;       // resident work units: SMs (one-SM kernel) or SM pairs
+    int dp_tiles;        // tiles [0, dp_tiles) are computed whole, round robin over the slots
+    // Stream-K tail: the K blocks of tiles [dp_tiles, num_tiles), in (tile, K
+    // block) order, are shared evenly by slots [0, sk_slots); 0 = the tail
+    // tiles are computed whole too.
+    int sk_slots;
+    long long sk_total;  // (num_tiles - dp_tiles) * kblocks
+    float* partials;     // sk_slots partial tiles (tile_rows x tile_cols), one per slot
+    unsigned* sk_flags;  // one arrival counter per tail tile, zero at launch
+    int sk_arrivals;     // arrivals of one contribution (the epilogue warps of a slot)
     unsigned long long wait_limit_ns;
     int debug_stall;
     int vec_c;
@@ -119,6 +133,7 @@ struct TcParams {
     const float* bias;
     int ep_simple;
     int tma_c;           // whole tiles leave through TMA stores (plain rule, 16-byte rows of C)
+    int row_copy;        // C not stored by TMA but beta = 0: the row-copy epilogue
 };
 
 // One output under the rule (C_old read only when beta != 0).
@@ -130,27 +145,86 @@ __device__ __forceinline__ float apply_epilogue(float acc, const TcParams& p, co
     return v;
 }
 
-// A unit of persistent work: a whole tile, or K-blocks [kb0, kb1) of a tile
-// whose partial result goes to scratch (piece >= 0).
+// A unit of persistent work: K blocks [kb0, kb1) of one tile.
+//   piece < 0:  the result goes to C -- a whole tile, or the owner's segment
+//               of a tail tile;
+//   piece >= 0: a contributor's segment of a tail tile: its sum goes to the
+//               partial tile of slot `piece`, and the tile's counter is
+//               raised once it has landed.
+// fix_wait > 0: the slots before this one that share the tile (fix_wait of
+// them) have contributed; the last of them, slot fix_slot, left the sum of
+// all their K blocks in its partial tile (each contributor adds its
+// predecessor's partial before publishing), so this unit waits until the
+// counter shows all fix_wait contributions and adds that one partial tile.
 struct Unit {
     int tile, kb0, kb1;
     int piece;
+    int fix_slot, fix_wait;
 };
 
-__device__ __forceinline__ Unit decode_unit(int u, const TcParams& p) {
+// The K-block range [b, e) of the tail that slot `slot` computes.
+__device__ __forceinline__ void sk_range(const TcParams& p, int slot, long long& b, long long& e) {
+    b = (long long)slot * p.sk_total / p.sk_slots;
+    e = (long long)(slot + 1) * p.sk_total / p.sk_slots;
+}
+
+// The slot whose tail range holds flat tail index x (0 <= x < sk_total).
+__device__ __forceinline__ int sk_slot_of(const TcParams& p, long long x) {
+    return (int)(((x + 1) * p.sk_slots - 1) / p.sk_total);
+}
+
+// Units of slot `slot`: its whole tiles (slot, slot + num_slots, ...), then,
+// with a stream-K tail, its tail range split at a tile boundary. A range is
+// never longer than one tile, so it meets at most two tiles: the end of
+// tile t0 (the slot holds that tile's last K block, so it owns t0) and the
+// start of tile t0 + 1 (a contribution). The contribution runs first, so the
+// owners that wait on it -- always slots of higher index -- find it early.
+__device__ __forceinline__ int slot_unit_count(const TcParams& p, int slot) {
+    if (p.sk_slots == 0)
+        return slot < p.num_tiles ? (p.num_tiles - 1 - slot) / p.num_slots + 1 : 0;
+    int n = p.dp_tiles / p.num_slots;
+    if (slot < p.sk_slots) {
+        long long b, e;
+        sk_range(p, slot, b, e);
+        if (e > b) n += (b / p.kblocks == (e - 1) / p.kblocks) ? 1 : 2;
+    }
+    return n;
+}
+
+__device__ __forceinline__ Unit slot_unit(const TcParams& p, int slot, int i) {
     Unit w;
-    if (u < p.dp_tiles) {
-        w.tile = u;
+    w.piece = -1;
+    w.fix_slot = -1;
+    w.fix_wait = 0;
+    const int ndp = p.sk_slots == 0 ? 1 << 30 : p.dp_tiles / p.num_slots;
+    if (i < ndp) {
+        w.tile = slot + i * p.num_slots;
         w.kb0 = 0;
         w.kb1 = p.kblocks;
-        w.piece = -1;
-    } else {
-        const int pc = u - p.dp_tiles;
-        const int j = pc % p.split;
-        w.tile = p.dp_tiles + pc / p.split;
-        w.kb0 = (int)((long)j * p.kblocks / p.split);
-        w.kb1 = (int)((long)(j + 1) * p.kblocks / p.split);
-        w.piece = pc;
+        return w;
+    }
+    const long long KB = p.kblocks;
+    long long b, e;
+    sk_range(p, slot, b, e);
+    const long long t0 = b / KB, t1 = (e - 1) / KB;
+    long long t, s0, s1;
+    if (t1 != t0 && i == ndp) {          // the start of tile t1: a contribution
+        t = t1;
+        s0 = 0;
+        s1 = e - t1 * KB;
+    } else {                              // the end of t0, or a range inside one tile
+        t = t0;
+        s0 = b - t0 * KB;
+        s1 = (t1 != t0) ? KB : e - t0 * KB;
+    }
+    w.tile = p.dp_tiles + (int)t;
+    w.kb0 = (int)s0;
+    w.kb1 = (int)s1;
+    if (s1 != KB) w.piece = slot;               // not the tile's end: a contribution
+    const int first = sk_slot_of(p, t * KB);     // the slot holding the tile's first K block
+    if (slot > first) {
+        w.fix_slot = slot - 1;
+        w.fix_wait = slot - first;
     }
     return w;
 }
@@ -417,43 +491,260 @@ __device__ __forceinline__ void store_row32_peeled(float* d, const uint32_t (&r)
     }
 }
 
+// ---- stream-K hand-off between slots (global memory)
+
+// A contributor warp's arrival on its tile's counter, once every lane's
+// stores of the partial tile are visible device-wide: each lane fences its
+// own stores, then one lane arrives. All lanes of the warp call this.
+__device__ __forceinline__ void sk_arrive(unsigned* flag) {
+    __threadfence();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) atomicAdd(flag, 1u);
+}
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* f) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    return v;
+}
+
+// Wait (lane 0 of the warp polls; bounded) until the counter reaches
+// `target`. A wait that runs out raises the block's abort flag and records
+// the timeout. Returns the same value in every lane.
+__device__ __noinline__ bool sk_wait(const unsigned* flag, unsigned target, int* abort_flag,
+                                     unsigned long long limit_ns) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) {
+        if (ld_acquire(flag) < target) {
+            const unsigned long long t0 = globaltimer();
+            for (uint32_t it = 1;; ++it) {
+                if (ld_acquire(flag) >= target) break;
+                if ((it & 15u) == 0) {
+                    if (*(volatile int*)abort_flag) { ok = 0; break; }
+                    if (globaltimer() - t0 > limit_ns || it >= (1u << 30)) {
+                        *(volatile int*)abort_flag = 1;
+                        atomicCAS(&g_tc_status, 0, kStatusTimeout);
+                        ok = 0;
+                        break;
+                    }
+                }
+                __nanosleep(it < 64 ? 64 : 512);    // back off: many warps poll at once
+            }
+        }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) (void)ld_acquire(flag);          // every lane orders its loads after the counter
+    return ok != 0;
+}
+
+// Partial tiles are kept as 32 x 32 blocks, each block column-major (4 KB:
+// column j of the block is 32 consecutive floats, one per row), blocks in
+// (slot, 32-row band, 32-column block) order. A warp then reads column j of
+// a block -- one value for each of its 32 rows -- as one coalesced 128-byte
+// load.
+__device__ __forceinline__ long partial_block(const TcParams& p, int slot, int row_in_tile, int c) {
+    return ((long)slot * (p.tile_rows / 32) + row_in_tile / 32) * (p.tile_cols / 32) + c;
+}
+
+// Start loading (coalesced, 32 independent loads) the values of this
+// thread's row in column block c of the partial tile of slot `slot`.
+__device__ __forceinline__ void load_partial(const TcParams& p, int slot, int row_in_tile, int c,
+                                             float (&v)[32]) {
+    const float* src = p.partials + partial_block(p, slot, row_in_tile, c) * 1024 + (threadIdx.x & 31);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __ldcg(src + 32 * j);
+}
+
+__device__ __forceinline__ void add_to(uint32_t (&r)[32], const float (&v)[32]) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__fadd_rn(__uint_as_float(r[j]), v[j]));
+}
+
+// Bulk copy of `bytes` (a multiple of 16) from this thread's shared memory
+// at `ssrc` to global memory at `gdst`, both 16-byte aligned.
+__device__ __forceinline__ void bulk_store_row(float* gdst, uint32_t ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 :: "l"(gdst), "r"(ssrc), "r"(bytes) : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Position q of a row-copy slot holds value q - a of the current block, or,
+// for q < a, value 32 + q - a of the previous block (the carry c29..c31).
+template <int Q>
+__device__ __forceinline__ float slot_value(const uint32_t (&v)[32], float c29, float c30, float c31,
+                                            int a) {
+    auto at = [&](int i) -> float {
+        return i >= 32 ? 0.0f : i >= 0 ? __uint_as_float(v[i]) : i == -1 ? c31 : i == -2 ? c30 : c29;
+    };
+    const float lo = (a & 1) ? at(Q - 1) : at(Q);
+    const float hi = (a & 1) ? at(Q - 3) : at(Q - 2);
+    return (a & 2) ? hi : lo;
+}
+
+template <int K>
+__device__ __forceinline__ void write_slot_chunks(float4* slot, const uint32_t (&v)[32], float c29,
+                                                  float c30, float c31, int a) {
+    if constexpr (K < ROW_SLOT_FLOATS / 4) {
+        slot[K] = make_float4(slot_value<4 * K>(v, c29, c30, c31, a),
+                              slot_value<4 * K + 1>(v, c29, c30, c31, a),
+                              slot_value<4 * K + 2>(v, c29, c30, c31, a),
+                              slot_value<4 * K + 3>(v, c29, c30, c31, a));
+        write_slot_chunks<K + 1>(slot, v, c29, c30, c31, a);
+    }
+}
+
+// Row-copy epilogue for C that TMA cannot store (rows not 16-byte aligned,
+// or N not a multiple of 4), beta = 0.
+// Each lane owns one row of the warp's 32. The row's values in global
+// memory start `a` floats past a 16-byte boundary (the same for every
+// 32-column block, as 32 floats are 128 bytes), so each block, together
+// with the last `a` values of the block before it (carried in registers),
+// covers whole 16-byte chunks: the lane writes them, shifted by `a`, to its
+// 144-byte slot in shared memory and one bulk copy moves them to C. Only
+// the values before the first 16-byte boundary of the warp's column range,
+// and after the last one (or past N), are stored one by one. This replaces
+// 16-byte stores from registers whose 32 lanes hit 32 rows at once.
+__device__ __forceinline__ void store_rows_copy(const TcParams& p, const Unit& w, int nb,
+                                                int row, int row_in_tile, uint32_t taddr,
+                                                float* stage, int c_begin, int c_end) {
+    const int lane = threadIdx.x & 31;
+    const bool live = row < p.M;
+    float* crow = p.C + (long)row * p.ldc;
+    const int a = (int)((reinterpret_cast<uintptr_t>(crow) >> 2) & 3);
+    float4* slot = reinterpret_cast<float4*>(stage + lane * ROW_SLOT_FLOATS);
+    const uint32_t slot_s = smem_u32(slot);
+    float c29 = 0.0f, c30 = 0.0f, c31 = 0.0f;
+    const bool fix = w.fix_wait > 0 && live;
+    float pv[32];                                      // the partial tile's block c (fix)
+    if (fix && nb * p.tile_cols + c_begin * 32 < p.N) load_partial(p, w.fix_slot, row_in_tile, c_begin, pv);
+    for (int c = c_begin; c < c_end; ++c) {
+        const int col0 = nb * p.tile_cols + c * 32;
+        if (col0 >= p.N) break;                        // uniform across the warp
+        uint32_t v[32];
+        tmem_ld32(taddr + (uint32_t)(c * 32), v);
+        const int nvalid = p.N - col0 < 32 ? p.N - col0 : 32;
+        const bool first = c == c_begin;
+        const bool last = c + 1 == c_end || col0 + 32 >= p.N;
+        if (fix) {
+            add_to(v, pv);
+            if (!last) load_partial(p, w.fix_slot, row_in_tile, c + 1, pv);   // in flight
+        }
+        if (!p.ep_simple) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (col0 + j < p.N)
+                    v[j] = __float_as_uint(apply_epilogue(__uint_as_float(v[j]), p, nullptr, col0 + j));
+        }
+        // Slot positions [4 klo, 4 khi) -- values [cs, ce) of this block --
+        // leave in one copy; position q is column col0 - a + q.
+        const int lo = first ? a : 0, hi = a + nvalid;
+        const int klo = (lo + 3) >> 2, khi = hi >> 2;
+        const int cs = 4 * klo - a;
+        const int ce = khi > klo ? 4 * khi - a : cs;
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // the slot is free
+        write_slot_chunks<0>(slot, v, c29, c30, c31, a);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        float* g0 = crow + col0 - a;                   // 16-byte aligned: position 0
+        if (live && khi > klo)
+            bulk_store_row(g0 + 4 * klo, slot_s + 16u * (uint32_t)klo, 16u * (uint32_t)(khi - klo));
+        if (live) {
+            if (!first && khi <= klo) {
+                // No whole chunk at N: the values carried from the block
+                // before (columns col0 - a .. col0 - 1) one by one.
+#pragma unroll
+                for (int q = 0; q < 3; ++q)
+                    if (q < a) {
+                        const int i = 32 - a + q;
+                        crow[col0 - a + q] = i == 29 ? c29 : i == 30 ? c30 : c31;
+                    }
+            }
+            if (nvalid == 32) {
+                if (first) {
+#pragma unroll
+                    for (int j = 0; j < 3; ++j)
+                        if (j < cs) crow[col0 + j] = __uint_as_float(v[j]);
+                }
+                if (last) {
+#pragma unroll
+                    for (int j = 29; j < 32; ++j)
+                        if (j >= ce) crow[col0 + j] = __uint_as_float(v[j]);
+                }
+            } else {                                    // the block at N: the rest one by one
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (j < nvalid && ((first && j < cs) || j >= ce))
+                        crow[col0 + j] = __uint_as_float(v[j]);
+            }
+        }
+        c29 = __uint_as_float(v[29]);
+        c30 = __uint_as_float(v[30]);
+        c31 = __uint_as_float(v[31]);
+    }
+}
+
 // Epilogue of one unit for this thread's accumulator row `row_in_tile`:
 // the 32-column blocks [c_begin, c_end) of the tile from TMEM (the tile's
-// column 0 at address `taddr`) to C, or, for a K-piece, to its partial tile
-// in scratch. Rows past M and columns past N are skipped (the reduction never
+// column 0 at address `taddr`) to C -- after the contributors' partial
+// tiles are added, for an owner -- or, for a contribution, to the partial
+// tile of its slot. Rows past M and columns past N are skipped (no owner
 // reads them). All lanes of the warp call this together.
 //
-// Otherwise each thread stores its row's 32-column blocks with 16-byte
-// stores, after peeling the values before the first 16-byte boundary when
-// C's rows are not 16-byte aligned. (Staging each 32 x 32 block through
-// shared memory to store it as 32 coalesced row segments instead measured
-// 9 % slower on 3072 x 5120 x 1536 TF32 with ldc = 5121: the staging's
-// shared-memory traffic competes with the MMAs' operand reads.)
+// Contributions go to their slot's partial tile with coalesced stores from
+// registers. Results for C whose rows are 16-byte aligned (beta = 0) leave
+// through TMA stores of 32 x 32 blocks staged in shared memory. Otherwise
+// each thread stores its row's 32-column blocks
+// with 16-byte stores, after peeling the values before the first 16-byte
+// boundary when C's rows are not 16-byte aligned. (Staging each 32 x 32
+// block through shared memory to store it as 32 coalesced row segments
+// instead measured 9 % slower on 3072 x 5120 x 1536 TF32 with ldc = 5121:
+// the staging's shared-memory traffic competes with the MMAs' operand
+// reads.)
+// ROWS: the kernel's epilogue region holds row slots (p.row_copy may be set).
+template <bool ROWS>
 __device__ __forceinline__ void store_accumulator(const TcParams& p, const Unit& w, int mb, int nb,
                                                  int row_in_tile, uint32_t taddr, float* stage,
                                                  const CUtensorMap* tmC, int c_begin, int c_end) {
     const int row = mb * p.tile_rows + row_in_tile;
     const int lane = threadIdx.x & 31;
-    if (w.piece < 0 && p.tma_c) {
-        // Whole tile, beta = 0: alpha and bias are applied in registers, then
-        // each 32 x 32 block goes to the warp's staging buffer (EPI_BUFS of
-        // them) in the 128-byte-swizzled layout of the C tensor map (row i
-        // holds 128 bytes, 16-byte chunk j at j ^ (i % 8)) and leaves as one
-        // TMA store, which also clips rows and columns past M and N. The next
-        // block's TMEM load is in flight while a block is staged, and a
-        // buffer is reused once the store issued EPI_BUFS blocks earlier has
-        // read it.
+    if (w.piece >= 0) {
+        // A contribution: each 32 x 32 block (after adding the predecessor's
+        // running sum) goes to the slot's partial tile as 32 coalesced
+        // 128-byte rows of the column-major block, straight from registers.
+        // Warps whose rows all lie past M store nothing (no one reads them).
+        if (row - lane >= p.M) return;
+        const int n_blocks = (p.N - nb * p.tile_cols + 31) / 32;
+        const int c_stop = c_end < n_blocks ? c_end : n_blocks;
+        const bool fix = w.fix_wait > 0;
+        uint32_t r[32];
+        float pv[32];
+        for (int c = c_begin; c < c_stop; ++c) {
+            tmem_ld32(taddr + (uint32_t)(c * 32), r);
+            if (fix) {               // a contribution in the middle of a tile (rare): no prefetch
+                load_partial(p, w.fix_slot, row_in_tile, c, pv);
+                add_to(r, pv);
+            }
+            float* dst = p.partials + partial_block(p, w.piece, row_in_tile, c) * 1024 + lane;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) __stcg(dst + 32 * j, __uint_as_float(r[j]));
+        }
+        return;
+    }
+    if (p.tma_c) {
+        // alpha and bias are applied in registers, then each 32 x 32 block
+        // goes to the warp's staging buffer (EPI_BUFS of them) in the
+        // 128-byte-swizzled layout of C's tensor map (row i holds 128 bytes,
+        // 16-byte chunk j at j ^ (i % 8)) and leaves as one TMA store, which
+        // also clips rows and columns past M and N. A buffer is reused once
+        // the store issued EPI_BUFS blocks earlier has read it. Without a
+        // running sum to add, the next block's TMEM load is in flight while a
+        // block is staged; with one, the next block's partial values are.
         const int row0 = row - lane;
         if (row0 >= p.M) return;                        // the warp's rows are all past M
         const int n_blocks = (p.N - nb * p.tile_cols + 31) / 32;   // blocks with columns < N
         const int c_stop = c_end < n_blocks ? c_end : n_blocks;
         if (c_begin >= c_stop) return;
-        uint32_t r[32], nx[32];
-        tmem_ld32(taddr + (uint32_t)(c_begin * 32), r);
-        for (int c = c_begin; c < c_stop; ++c) {
+        auto stage_and_store = [&](uint32_t (&r)[32], int c) {
             const int col0 = nb * p.tile_cols + c * 32;
-            const bool more = c + 1 < c_stop;
-            if (more) tmem_ld32_async(taddr + (uint32_t)((c + 1) * 32), nx);
             if (!p.ep_simple) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
@@ -467,11 +758,31 @@ __device__ __forceinline__ void store_accumulator(const TcParams& p, const Unit&
             float4* srow = reinterpret_cast<float4*>(buf + lane * 32);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                srow[j ^ (lane & 7)] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                                   __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                srow[j ^ (lane & 7)] =
+                    make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) tma_store_2d(tmC, col0, row0, smem_u32(buf));
+        };
+        uint32_t r[32];
+        if (w.fix_wait > 0) {
+            float pv[32];
+            load_partial(p, w.fix_slot, row_in_tile, c_begin, pv);
+            for (int c = c_begin; c < c_stop; ++c) {
+                tmem_ld32(taddr + (uint32_t)(c * 32), r);
+                add_to(r, pv);
+                if (c + 1 < c_stop) load_partial(p, w.fix_slot, row_in_tile, c + 1, pv);
+                stage_and_store(r, c);
+            }
+            return;
+        }
+        uint32_t nx[32];
+        tmem_ld32(taddr + (uint32_t)(c_begin * 32), r);
+        for (int c = c_begin; c < c_stop; ++c) {
+            const bool more = c + 1 < c_stop;
+            if (more) tmem_ld32_async(taddr + (uint32_t)((c + 1) * 32), nx);
+            stage_and_store(r, c);
             if (more) {
                 tmem_wait_ld(nx);
 #pragma unroll
@@ -480,23 +791,29 @@ __device__ __forceinline__ void store_accumulator(const TcParams& p, const Unit&
         }
         return;
     }
-    float* dst;
-    bool vec, ep;
-    if (w.piece < 0) {
-        dst = p.C + (long)row * p.ldc + (long)nb * p.tile_cols;
-        vec = p.vec_c != 0;
-        ep = p.ep_simple == 0;                  // a whole tile writes final outputs
-    } else {
-        dst = p.partials + ((long)w.piece * p.tile_rows + row_in_tile) * p.tile_cols;
-        vec = true;
-        ep = false;                             // partial sums: the reduction applies the rule
+    if constexpr (ROWS) {
+        if (p.row_copy) {
+            store_rows_copy(p, w, nb, row, row_in_tile, taddr, stage, c_begin, c_end);
+            return;
+        }
     }
+    float* dst = p.C + (long)row * p.ldc + (long)nb * p.tile_cols;
+    const bool vec = p.vec_c != 0;
+    const bool ep = p.ep_simple == 0;
+    const bool fix = w.fix_wait > 0 && row < p.M;
+    float pv[32];                                      // the partial tile's block c (fix)
+    if (fix && nb * p.tile_cols + c_begin * 32 < p.N) load_partial(p, w.fix_slot, row_in_tile, c_begin, pv);
     for (int c = c_begin; c < c_end; ++c) {
         const int col0 = nb * p.tile_cols + c * 32;
         if (col0 >= p.N) break;                     // uniform across the warp
         uint32_t r[32];
         tmem_ld32(taddr + (uint32_t)(c * 32), r);
         if (row < p.M) {
+            if (fix) {
+                add_to(r, pv);
+                if (c + 1 < c_end && col0 + 32 < p.N)
+                    load_partial(p, w.fix_slot, row_in_tile, c + 1, pv);   // in flight
+            }
             float* d = dst + c * 32;
             if (ep) {
 #pragma unroll
@@ -514,60 +831,6 @@ __device__ __forceinline__ void store_accumulator(const TcParams& p, const Unit&
                 for (int j = 0; j < 32; ++j)
                     if (col0 + j < p.N) d[j] = __uint_as_float(r[j]);
             }
-        }
-    }
-}
-
-// Sum of `n` float4 at src, src + stride, ... in that order; the loads of
-// four pieces are issued before their adds, so that they are in flight
-// together.
-__device__ __forceinline__ float4 sum_pieces(const float* src, long stride, int n) {
-    float4 s = *reinterpret_cast<const float4*>(src);
-    for (int j = 1; j < n; j += 4) {
-        float4 v[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (j + q < n) v[q] = *reinterpret_cast<const float4*>(src + (j + q) * stride);
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (j + q < n) {
-                s.x += v[q].x;
-                s.y += v[q].y;
-                s.z += v[q].z;
-                s.w += v[q].w;
-            }
-    }
-    return s;
-}
-
-// Sum the K-pieces of every split tile, piece 0 first, into C.
-__global__ void __launch_bounds__(256)
-tc_splitk_reduce(const TcParams p) {
-    const int Q = p.tile_cols / 4;                         // float4 per tile row
-    const int rows = p.tile_rows < p.M ? p.tile_rows : p.M; // rows a tile can hold (M small: M)
-    const long per_tile = (long)rows * Q;
-    const long total = (long)(p.num_tiles - p.dp_tiles) * per_tile;
-    const long piece_floats = (long)p.tile_rows * p.tile_cols;
-    for (long u = blockIdx.x * (long)blockDim.x + threadIdx.x; u < total;
-         u += (long)gridDim.x * blockDim.x) {
-        const int r = (int)(u / per_tile);
-        const int e = (int)(u % per_tile);
-        const int row = e / Q, c4 = (e % Q) * 4;
-        int mb, nb;
-        tile_coords(p.dp_tiles + r, p, mb, nb);
-        const int grow = mb * p.tile_rows + row, gcol = nb * p.tile_cols + c4;
-        if (grow >= p.M || gcol >= p.N) continue;
-        const float* src = p.partials + (long)r * p.split * piece_floats + (long)row * p.tile_cols + c4;
-        const float4 s = sum_pieces(src, piece_floats, p.split);
-        float* dst = p.C + (long)grow * p.ldc + gcol;
-        float v[4] = {s.x, s.y, s.z, s.w};
-        if (!p.ep_simple)
-            for (int j = 0; j < 4 && gcol + j < p.N; ++j)
-                v[j] = apply_epilogue(v[j], p, dst + j, gcol + j);
-        if (p.vec_c && gcol + 3 < p.N) {
-            *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
-        } else {
-            for (int j = 0; j < 4 && gcol + j < p.N; ++j) dst[j] = v[j];
         }
     }
 }
@@ -633,8 +896,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         if (lane == 0) {
             uint32_t armed = 0, armed_parity = 0;   // per-stage fills in flight
             int g = 0;
-            for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-                const Unit w = decode_unit(u, p);
+            const int nu = slot_unit_count(p, blockIdx.x);
+            for (int i = 0; i < nu; ++i) {
+                const Unit w = slot_unit(p, blockIdx.x, i);
                 int mb, nb;
                 tile_coords(w.tile, p, mb, nb);
                 for (int kb = w.kb0; kb < w.kb1; ++kb, ++g) {
@@ -668,9 +932,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            int g = 0, it = 0;
-            for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++it) {
-                const Unit w = decode_unit(u, p);
+            int g = 0;
+            const int nu = slot_unit_count(p, blockIdx.x);
+            for (int it = 0; it < nu; ++it) {
+                const Unit w = slot_unit(p, blockIdx.x, it);
                 const int acc = it & 1;
                 const uint32_t aph = (uint32_t)(it >> 1) & 1u;
                 if (!mbar_wait(smem_u32(&sy->tmem_empty[acc]), aph ^ 1u, &sy->abort, lim, true)) break;
@@ -706,23 +971,31 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         // ------------------------------------------------ epilogue (warps 2-5)
         const int q = warp & 3;                 // TMEM lanes 32q .. 32q+31
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        int it = 0;
-        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++it) {
-            const Unit w = decode_unit(u, p);
+        const int nu = slot_unit_count(p, blockIdx.x);
+        for (int it = 0; it < nu; ++it) {
+            const Unit w = slot_unit(p, blockIdx.x, it);
             int mb, nb;
             tile_coords(w.tile, p, mb, nb);
             const int acc = it & 1;
             const uint32_t aph = (uint32_t)(it >> 1) & 1u;
             bool ok = mbar_wait(smem_u32(&sy->tmem_full[acc]), aph, &sy->abort, lim, true);
             if (!__all_sync(0xffffffffu, ok)) break;
+            unsigned* flag = (w.fix_wait > 0 || w.piece >= 0) ? p.sk_flags + (w.tile - p.dp_tiles)
+                                                              : nullptr;
+            // The earlier shares of this tile must have landed before their
+            // running sum is added.
+            if (w.fix_wait > 0 &&
+                !sk_wait(flag, (unsigned)(w.fix_wait * p.sk_arrivals), &sy->abort, lim))
+                break;
             tc_fence_after();
-            store_accumulator(p, w, mb, nb, q * 32 + lane, tmem_base + lane_off + (uint32_t)(acc * BN),
-                              epi_stage + q * (EPI_WARP_BYTES / 4), &tmC, 0, BN / 32);
+            store_accumulator<true>(p, w, mb, nb, q * 32 + lane, tmem_base + lane_off + (uint32_t)(acc * BN),
+                              epi_stage + q * (EPI_REGION / 4), &tmC, 0, BN / 32);
             tc_fence_before();
             __syncwarp();                               // the warp's TMEM reads are done
             if (lane == 31) mbar_arrive(smem_u32(&sy->tmem_empty[acc]));   // not the storing lane
+            if (w.piece >= 0) sk_arrive(flag);   // this warp's part has landed
         }
-        if (lane == 0) tma_store_wait_all();    // C stores done before the block retires
+        tma_store_wait_all();    // every lane's C stores and row copies done before the block retires
     }
 
     tc_fence_before();
@@ -790,8 +1063,8 @@ template <int NW>
 struct PairEpi {
     static constexpr int WARPS = NW == 2 ? 8 : 4;
     static constexpr int THREADS = 64 + 32 * WARPS;
-    static constexpr int BYTES =
-        WARPS * EPI_WARP_BYTES > P_GUARD_BYTES ? WARPS * EPI_WARP_BYTES : P_GUARD_BYTES;
+    static constexpr int REGION = NW == 2 ? EPI_WARP_BYTES : EPI_REGION;   // per warp
+    static constexpr int BYTES = WARPS * REGION > P_GUARD_BYTES ? WARPS * REGION : P_GUARD_BYTES;
 };
 template <bool X3, int NW>
 constexpr int pair_smem_bytes() {
@@ -851,7 +1124,7 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();
     const bool leader = rank == 0;
-    const int pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
+    const int pair = blockIdx.x >> 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < R::STAGES; ++s) {
@@ -892,8 +1165,9 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
         if (lane == 0) {
             uint32_t armed = 0, armed_parity = 0;
             int g = 0;
-            for (int u = pair; u < p.num_units; u += num_pairs) {
-                const Unit w = decode_unit(u, p);
+            const int nu = slot_unit_count(p, pair);
+            for (int i = 0; i < nu; ++i) {
+                const Unit w = slot_unit(p, pair, i);
                 int mb, nb;
                 tile_coords(w.tile, p, mb, nb);
                 const int row0 = mb * P_BM + (int)rank * 128;
@@ -978,8 +1252,9 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
                     }
                 }
             };
-            for (int u = pair; u < p.num_units; u += num_pairs, ++it) {
-                const Unit w = decode_unit(u, p);
+            const int nu = slot_unit_count(p, pair);
+            for (; it < nu; ++it) {
+                const Unit w = slot_unit(p, pair, it);
                 const int acc = it % NACC;
                 const uint32_t aph = (uint32_t)(it / NACC) & 1u;
                 if (!mbar_wait(smem_u32(&sy->tmem_empty[acc]), aph ^ 1u, &sy->abort, lim, true)) break;
@@ -1059,18 +1334,25 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
         constexpr int PARTS = PairEpi<NW>::WARPS / 4;      // warps sharing a lane quarter
         const int part = (warp - 2) >> 2;
         const int blocks = p.tile_cols / 32 / PARTS;         // 32-column blocks per warp
-        int it = 0;
-        for (int u = pair; u < p.num_units; u += num_pairs, ++it) {
-            const Unit w = decode_unit(u, p);
+        const int nu = slot_unit_count(p, pair);
+        for (int it = 0; it < nu; ++it) {
+            const Unit w = slot_unit(p, pair, it);
             int mb, nb;
             tile_coords(w.tile, p, mb, nb);
             const int acc = it % NACC;
             const uint32_t aph = (uint32_t)(it / NACC) & 1u;
             bool ok = mbar_wait(smem_u32(&sy->tmem_full[acc]), aph, &sy->abort, lim, true);
             if (!__all_sync(0xffffffffu, ok)) break;
+            unsigned* flag = (w.fix_wait > 0 || w.piece >= 0) ? p.sk_flags + (w.tile - p.dp_tiles)
+                                                              : nullptr;
+            // The earlier shares of this tile must have landed before their
+            // running sum is added.
+            if (w.fix_wait > 0 &&
+                !sk_wait(flag, (unsigned)(w.fix_wait * p.sk_arrivals), &sy->abort, lim))
+                break;
             tc_fence_after();
             float* stage = reinterpret_cast<float*>(smem + R::STAGES * R::STAGE) +
-                           (warp - 2) * (EPI_WARP_BYTES / 4);
+                           (warp - 2) * (PairEpi<NW>::REGION / 4);
             if constexpr (NW == 2) {
                 // Column halves in order: each is drained once its MMAs are
                 // complete (tmem_full[half]) and freed (tmem_empty[half]) as
@@ -1083,8 +1365,8 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
                         tc_fence_after();
                     }
                     const int c0 = half * (blocks * PARTS / 2) + part * (blocks / 2);
-                    store_accumulator(p, w, mb, nb, (int)rank * 128 + q * 32 + lane,
-                                      tmem_base + lane_off, stage, &tmC, c0, c0 + blocks / 2);
+                    store_accumulator<false>(p, w, mb, nb, (int)rank * 128 + q * 32 + lane,
+                                             tmem_base + lane_off, stage, &tmC, c0, c0 + blocks / 2);
                     tc_fence_before();
                     __syncwarp();                       // the warp's TMEM reads are done
                     // Lane 31 arrives: lane 0 issued the warp's TMA stores,
@@ -1093,15 +1375,16 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
                 }
                 if (!ok2) break;
             } else {
-                store_accumulator(p, w, mb, nb, (int)rank * 128 + q * 32 + lane,
-                                  tmem_base + lane_off + (uint32_t)(acc * BN), stage, &tmC,
-                                  part * blocks, (part + 1) * blocks);
+                store_accumulator<NW == 1>(p, w, mb, nb, (int)rank * 128 + q * 32 + lane,
+                                           tmem_base + lane_off + (uint32_t)(acc * BN), stage, &tmC,
+                                           part * blocks, (part + 1) * blocks);
                 tc_fence_before();
                 __syncwarp();                           // the warp's TMEM reads are done
                 if (lane == 31) mbar_arrive_cluster(tmem_empty0 + (uint32_t)(acc * sizeof(uint64_t)));
             }
+            if (w.piece >= 0) sk_arrive(flag);   // this warp's part has landed
         }
-        if (lane == 0) tma_store_wait_all();    // C stores done before the block retires
+        tma_store_wait_all();    // every lane's C stores and row copies done before the block retires
     }
 
     tc_fence_before();
@@ -1134,7 +1417,7 @@ bool encode_2d(EncodeTiledFn enc, CUtensorMap* map, const void* base, int esz, l
     return r == CUDA_SUCCESS;
 }
 
-TcParams make_params(const GemmArgs& a, const TcPlan& pl, float* partials,
+TcParams make_params(const GemmArgs& a, const TcPlan& pl, void* scratch, int arrivals,
                      unsigned long long wait_limit_ns, int debug_stall) {
     TcParams p;
     p.M = a.M; p.N = a.N; p.K = a.K;
@@ -1145,10 +1428,17 @@ TcParams make_params(const GemmArgs& a, const TcPlan& pl, float* partials,
     p.kblocks = pl.kblocks;
     p.tile_rows = pl.tile_rows;
     p.tile_cols = pl.tile_cols;
+    p.num_slots = pl.slots;
     p.dp_tiles = pl.dp_tiles;
-    p.split = pl.split;
-    p.num_units = pl.dp_tiles + (p.num_tiles - pl.dp_tiles) * pl.split;
-    p.partials = partials;
+    p.sk_slots = pl.sk_slots;
+    p.sk_total = (long long)(p.num_tiles - pl.dp_tiles) * pl.kblocks;
+    p.partials = nullptr;
+    p.sk_flags = nullptr;
+    if (pl.sk_slots > 0) {
+        p.partials = static_cast<float*>(scratch);
+        p.sk_flags = reinterpret_cast<unsigned*>(static_cast<char*>(scratch) + tc_partial_bytes(pl));
+    }
+    p.sk_arrivals = arrivals;
     p.wait_limit_ns = wait_limit_ns;
     p.debug_stall = debug_stall;
     p.vec_c = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0 && a.ldc % 4 == 0) ? 1 : 0;
@@ -1157,58 +1447,65 @@ TcParams make_params(const GemmArgs& a, const TcPlan& pl, float* partials,
     p.bias = a.ep.bias;
     p.ep_simple = a.ep.simple() ? 1 : 0;
     p.tma_c = 0;
+    p.row_copy = 0;
     return p;
 }
 
 // Tensor map over C for the TMA-store epilogue (32 x 32 boxes, 128-byte
-// swizzle). Used when C's base and rows are 16-byte aligned and beta = 0;
-// otherwise the epilogue stores from registers and `map` stays unused.
+// swizzle). Used when C's base and rows are 16-byte aligned, N is a
+// multiple of 4 and beta = 0; otherwise the epilogue stores from registers
+// (or by row copies) and `map` stays unused. (With N % 4 != 0 a TMA store
+// of the last block of a row also wrote the columns up to the next 16-byte
+// boundary, past N: measured on sm_103a.)
 void encode_c(EncodeTiledFn enc, CUtensorMap* map, const GemmArgs& a, TcParams& p) {
     memset(map, 0, sizeof(*map));
-    if (p.vec_c && a.ep.beta == 0.0f && a.M > 0 && a.N > 0 &&
+    if (p.vec_c && a.N % 4 == 0 && a.ep.beta == 0.0f && a.M > 0 && a.N > 0 &&
         encode_2d(enc, map, a.C, 4, a.M, a.N, a.ldc, 32, 32))
         p.tma_c = 1;
 }
 
-cudaError_t launch_reduce(const TcParams& p, cudaStream_t s) {
-    const int rows = p.tile_rows < p.M ? p.tile_rows : p.M;
-    const long units = (long)(p.num_tiles - p.dp_tiles) * rows * (p.tile_cols / 4);
-    long blocks = (units + 255) / 256;
-    if (blocks > 8192) blocks = 8192;
-    tc_splitk_reduce<<<(int)blocks, 256, 0, s>>>(p);
-    return cudaGetLastError();
+// Zero the tail-tile counters of a stream-K plan, in stream order before
+// the launch.
+bool prepare_stream_k(const TcParams& p, cudaStream_t s) {
+    if (p.sk_slots == 0) return true;
+    return cudaMemsetAsync(p.sk_flags, 0, sizeof(unsigned) * (size_t)(p.num_tiles - p.dp_tiles),
+                           s) == cudaSuccess;
+}
+
+// Slots (SMs or SM pairs) the grid of plan `pl` needs.
+int grid_slots(const TcPlan& pl) {
+    const int tiles = pl.tiles_m * pl.tiles_n;
+    if (pl.sk_slots == 0) return tiles < pl.slots ? tiles : pl.slots;
+    return pl.dp_tiles > 0 ? pl.slots : pl.sk_slots;
 }
 
 template <int ESZ, bool B_KMAJOR>
-cudaError_t launch_tc(const GemmArgs& a, const TcPlan& pl, float* partials, int num_sms,
-                      EncodeTiledFn enc, unsigned long long wait_limit_ns, int debug_stall,
-                      cudaStream_t s) {
+cudaError_t launch_tc(const GemmArgs& a, const TcPlan& pl, void* scratch, EncodeTiledFn enc,
+                      unsigned long long wait_limit_ns, int debug_stall, cudaStream_t s) {
     constexpr int BK = Kind<ESZ>::BK;
     CUtensorMap tmA, tmB;
     if (!encode_2d(enc, &tmA, a.A, ESZ, a.M, a.K, a.lda, BK, BM)) return cudaErrorInvalidValue;
     const bool okb = B_KMAJOR ? encode_2d(enc, &tmB, a.B, ESZ, a.N, a.K, a.ldb, BK, BN)
                               : encode_2d(enc, &tmB, a.B, ESZ, a.K, a.N, a.ldb, SW / ESZ, BK);
     if (!okb) return cudaErrorInvalidValue;
-    TcParams p = make_params(a, pl, partials, wait_limit_ns, debug_stall);
+    TcParams p = make_params(a, pl, scratch, 4, wait_limit_ns, debug_stall);
     CUtensorMap tmC;
     encode_c(enc, &tmC, a, p);
+    p.row_copy = (!p.tma_c && a.ep.beta == 0.0f) ? 1 : 0;
+    if (!prepare_stream_k(p, s)) return cudaErrorInvalidValue;
 
     auto kern = tc_gemm_kernel<ESZ, B_KMAJOR>;
     cudaError_t e = set_smem_limit_once<tc_gemm_kernel<ESZ, B_KMAJOR>>(SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const int grid = p.num_units < num_sms ? p.num_units : num_sms;
-    kern<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tmA, tmB, tmC, p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess || p.split <= 1) return e;
-    return launch_reduce(p, s);
+    kern<<<grid_slots(pl), NUM_THREADS, SMEM_BYTES, s>>>(tmA, tmB, tmC, p);
+    return cudaGetLastError();
 }
 
 // The 2-SM kernel: clusters of two CTAs, one CTA per SM, persistent over
 // 256 x 256 tiles (NW = 1) or 256 x 512 tiles (NW = 2).
 template <int ESZ, bool B_KMAJOR, bool X3 = false, int NW = 1>
-cudaError_t launch_tc_pair(const GemmArgs& a, const TcPlan& pl, float* partials, int num_sms,
-                           EncodeTiledFn enc, unsigned long long wait_limit_ns, int debug_stall,
-                           cudaStream_t s) {
+cudaError_t launch_tc_pair(const GemmArgs& a, const TcPlan& pl, void* scratch, EncodeTiledFn enc,
+                           unsigned long long wait_limit_ns, int debug_stall, cudaStream_t s) {
     constexpr int BK = Kind<ESZ>::BK;
     constexpr int SMEM = pair_smem_bytes<X3, NW>();
     CUtensorMap tmA, tmB, tmA2, tmB2;
@@ -1224,16 +1521,18 @@ cudaError_t launch_tc_pair(const GemmArgs& a, const TcPlan& pl, float* partials,
         tmA2 = tmA;
         tmB2 = tmB;
     }
-    TcParams p = make_params(a, pl, partials, wait_limit_ns, debug_stall);
+    TcParams p = make_params(a, pl, scratch, 2 * PairEpi<NW>::WARPS, wait_limit_ns, debug_stall);
     CUtensorMap tmC;
     encode_c(enc, &tmC, a, p);
+    // The wide tiles' epilogue region has no room for row slots.
+    p.row_copy = (NW == 1 && !p.tma_c && a.ep.beta == 0.0f) ? 1 : 0;
+    if (!prepare_stream_k(p, s)) return cudaErrorInvalidValue;
 
     auto kern = tc_gemm_2sm_kernel<ESZ, B_KMAJOR, X3, NW>;
     cudaError_t e = set_smem_limit_once<tc_gemm_2sm_kernel<ESZ, B_KMAJOR, X3, NW>>(SMEM);
     if (e != cudaSuccess) return e;
-    const int pairs = p.num_units < num_sms / 2 ? p.num_units : num_sms / 2;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * pairs, 1, 1);
+    cfg.gridDim = dim3(2 * grid_slots(pl), 1, 1);
     cfg.blockDim = dim3(PairEpi<NW>::THREADS, 1, 1);
     cfg.dynamicSmemBytes = SMEM;
     cfg.stream = s;
@@ -1246,9 +1545,7 @@ cudaError_t launch_tc_pair(const GemmArgs& a, const TcPlan& pl, float* partials,
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmA2, tmB2, tmC, p);
     if (e != cudaSuccess) return e;
-    e = cudaGetLastError();
-    if (e != cudaSuccess || p.split <= 1) return e;
-    return launch_reduce(p, s);
+    return cudaGetLastError();
 }
 
 // ===================================================================
@@ -1394,7 +1691,20 @@ TileModel tile_model(int in_type, int shape, int tile_rows, int tile_cols, int K
     return m;
 }
 
-TcPlan tc_plan(int M, int N, int K, int in_type, int shape, int num_sms, bool allow_split,
+size_t tc_partial_bytes(const TcPlan& pl) {
+    return ((size_t)pl.sk_slots * pl.tile_rows * pl.tile_cols * sizeof(float) + 255) & ~(size_t)255;
+}
+
+// Whole-tile rounds over the slots; when the last round is partial and
+// `streamk` allows it, its tiles' K blocks may instead be shared by S slots
+// (stream-K, S between the tail's tile count and the slot count), each slot
+// computing an even share of at most one tile's length. The model charges a
+// share its main-loop time, one write-out hand-off per extra share of a tile
+// and the zeroing of the counters; S = the one with the lowest estimate, or
+// no sharing if that is not faster than the partial round itself.
+// streamk: -1 = that choice, 0 = never share, S > 0 = share among S slots
+// where the tail allows it (tests and tuning).
+TcPlan tc_plan(int M, int N, int K, int in_type, int shape, int num_sms, int streamk,
                bool tma_c) {
     if (in_type == TC_TF32X3) shape = TC_PAIR;   // the split form: 256 x 256 CTA-pair tiles only
     const bool pair = shape != TC_ONE_SM;
@@ -1407,32 +1717,62 @@ TcPlan tc_plan(int M, int N, int K, int in_type, int shape, int num_sms, bool al
     pl.kblocks = (K + bk - 1) / bk;
     const int tiles = pl.tiles_m * pl.tiles_n;
     const int slots = pair ? num_sms / 2 : num_sms;
+    pl.slots = slots > 0 ? slots : 1;
+    pl.dp_tiles = tiles;
+    pl.sk_slots = 0;
+    pl.scratch_bytes = 0;
+    pl.est_us = 0.0;
+    if (slots <= 0 || tiles == 0) return pl;
     const TileModel tm = tile_model(in_type, shape, pl.tile_rows, pl.tile_cols, K, tma_c);
     const double tile_us = tm.main_us + tm.epi_us;
-    const double tile_bytes = (double)pl.tile_rows * pl.tile_cols * sizeof(float);
-    pl.dp_tiles = tiles;
-    pl.split = 1;
-    if (allow_split) plan_tail_split(tiles, slots, pl.kblocks, tile_us, tile_bytes, pl.dp_tiles, pl.split);
-    pl.scratch_bytes = pl.split > 1 ? (size_t)(tiles - pl.dp_tiles) * pl.split * pl.tile_rows *
-                                          pl.tile_cols * sizeof(float)
-                                    : 0;
-    // Estimated duration: whole-tile rounds, then the rounds of K-pieces (each
-    // with its own epilogue) plus the cost of their partial tiles.
-    if (slots <= 0 || tiles == 0) {
-        pl.est_us = 0.0;
-    } else if (pl.split <= 1) {
-        pl.est_us = (double)((tiles + slots - 1) / slots) * tile_us;
-    } else {
-        const int rem = tiles - pl.dp_tiles;
-        const int rounds = (rem * pl.split + slots - 1) / slots;
-        pl.est_us = (double)(pl.dp_tiles / slots) * tile_us +
-                    rounds * (tm.main_us / pl.split + tm.epi_us) +
-                    tail_split_cost_us(rem, tile_bytes, pl.split);
+    pl.est_us = (double)((tiles + slots - 1) / slots) * tile_us;
+    const int rem = tiles % slots;
+    if (streamk == 0 || rem == 0) return pl;
+    const long long T = (long long)rem * pl.kblocks;
+    const int full = tiles / slots;
+    if (streamk > 0) {
+        // Forced width (tests and tuning), kept where the tail allows it: more
+        // slots than tail tiles, every share at least one K block.
+        long long S = streamk;
+        if (S > slots) S = slots;
+        if (S > T) S = T;
+        if (S <= rem) return pl;
+        pl.dp_tiles = tiles - rem;
+        pl.sk_slots = (int)S;
+        pl.scratch_bytes = tc_partial_bytes(pl) + (((size_t)rem * sizeof(unsigned) + 255) & ~(size_t)255);
+        return pl;
+    }
+    if (pl.kblocks < 8) return pl;
+    // A share ends with its write-out, and the shares of one tile hand their
+    // running sum on one after the other, so the tail pays one write-out per
+    // extra share of a tile on top of its main loop. Measured per hand-off
+    // (in-kernel timestamps): ~8 us for the 256 x 512 tiles (128 x 512 FP32
+    // per SM leaving all SMs at once), ~3-4 us for the 256 x 256 and
+    // 128 x 256 tiles.
+    const double hop_us = shape == TC_PAIR_WIDE ? 8.0 : 4.0;
+    const double memset_us = 2.0;
+    double best = pl.est_us;
+    int best_s = 0;
+    for (int S = rem + 1; S <= slots && (long long)S * 4 <= T; ++S) {
+        const long long len = (T + S - 1) / S;                 // K blocks of the longest share
+        const double main_us = (double)len / pl.kblocks * tm.main_us;
+        const int per_tile = (S + rem - 1) / rem + 1;          // shares meeting one tile, at most
+        const double est = full * tile_us + main_us + tm.epi_us + (per_tile - 1) * hop_us + memset_us;
+        if (est < best && est < 0.98 * pl.est_us) {            // a clear gain only
+            best = est;
+            best_s = S;
+        }
+    }
+    if (best_s > 0) {
+        pl.dp_tiles = tiles - rem;
+        pl.sk_slots = best_s;
+        pl.est_us = best;
+        pl.scratch_bytes = tc_partial_bytes(pl) + (((size_t)rem * sizeof(unsigned) + 255) & ~(size_t)255);
     }
     return pl;
 }
 
-int tc_shape(int M, int N, int K, int in_type, int mode, int num_sms, bool allow_split,
+int tc_shape(int M, int N, int K, int in_type, int mode, int num_sms, int streamk,
              bool tma_c) {
     if (in_type == TC_TF32X3) return TC_PAIR;
     if (mode == 0) return TC_ONE_SM;
@@ -1442,8 +1782,8 @@ int tc_shape(int M, int N, int K, int in_type, int mode, int num_sms, bool allow
     if (N <= BN) return TC_PAIR;
     // The shape the timing model expects to finish first; near-ties go to
     // the narrow tiles, whose epilogue is hidden.
-    const TcPlan narrow = tc_plan(M, N, K, in_type, TC_PAIR, num_sms, allow_split, tma_c);
-    const TcPlan wide = tc_plan(M, N, K, in_type, TC_PAIR_WIDE, num_sms, allow_split, tma_c);
+    const TcPlan narrow = tc_plan(M, N, K, in_type, TC_PAIR, num_sms, streamk, tma_c);
+    const TcPlan wide = tc_plan(M, N, K, in_type, TC_PAIR_WIDE, num_sms, streamk, tma_c);
     return wide.est_us < 0.97 * narrow.est_us ? TC_PAIR_WIDE : TC_PAIR;
 }
 
@@ -1452,34 +1792,35 @@ const char* tc_kernel_name(int in_type, int shape) {
     return kNames[in_type == TC_BF16 ? 1 : in_type == TC_TF32X3 ? 2 : 0][sh];
 }
 
-cudaError_t tc_launch(const GemmArgs& a, int in_type, int b_kmajor, int num_sms, void* encode_fn,
+cudaError_t tc_launch(const GemmArgs& a, int in_type, int b_kmajor, void* encode_fn,
                       unsigned long long wait_limit_ns, int debug_stall, int shape,
-                      const TcPlan& pl, float* partials, cudaStream_t s) {
+                      const TcPlan& pl, void* scratch, cudaStream_t s) {
     auto enc = reinterpret_cast<EncodeTiledFn>(encode_fn);
     const unsigned long long w = wait_limit_ns;
     const int st = debug_stall;
+    if (pl.sk_slots > 0 && scratch == nullptr) return cudaErrorInvalidValue;
     if (in_type == TC_TF32X3)       // always the CTA-pair kernel, B K-major
-        return launch_tc_pair<4, true, true>(a, pl, partials, num_sms, enc, w, st, s);
+        return launch_tc_pair<4, true, true>(a, pl, scratch, enc, w, st, s);
     if ((shape == TC_PAIR_WIDE) != (pl.tile_cols == 2 * BN)) return cudaErrorInvalidValue;
     if (shape == TC_PAIR_WIDE) {
         if (in_type == TC_BF16)
-            return b_kmajor ? launch_tc_pair<2, true, false, 2>(a, pl, partials, num_sms, enc, w, st, s)
-                            : launch_tc_pair<2, false, false, 2>(a, pl, partials, num_sms, enc, w, st, s);
+            return b_kmajor ? launch_tc_pair<2, true, false, 2>(a, pl, scratch, enc, w, st, s)
+                            : launch_tc_pair<2, false, false, 2>(a, pl, scratch, enc, w, st, s);
         if (!b_kmajor) return cudaErrorInvalidValue;    // TF32 reads B K-major only
-        return launch_tc_pair<4, true, false, 2>(a, pl, partials, num_sms, enc, w, st, s);
+        return launch_tc_pair<4, true, false, 2>(a, pl, scratch, enc, w, st, s);
     }
     if (shape == TC_PAIR) {
         if (in_type == TC_BF16)
-            return b_kmajor ? launch_tc_pair<2, true>(a, pl, partials, num_sms, enc, w, st, s)
-                            : launch_tc_pair<2, false>(a, pl, partials, num_sms, enc, w, st, s);
-        return b_kmajor ? launch_tc_pair<4, true>(a, pl, partials, num_sms, enc, w, st, s)
-                        : launch_tc_pair<4, false>(a, pl, partials, num_sms, enc, w, st, s);
+            return b_kmajor ? launch_tc_pair<2, true>(a, pl, scratch, enc, w, st, s)
+                            : launch_tc_pair<2, false>(a, pl, scratch, enc, w, st, s);
+        return b_kmajor ? launch_tc_pair<4, true>(a, pl, scratch, enc, w, st, s)
+                        : launch_tc_pair<4, false>(a, pl, scratch, enc, w, st, s);
     }
     if (in_type == TC_BF16)
-        return b_kmajor ? launch_tc<2, true>(a, pl, partials, num_sms, enc, w, st, s)
-                        : launch_tc<2, false>(a, pl, partials, num_sms, enc, w, st, s);
-    return b_kmajor ? launch_tc<4, true>(a, pl, partials, num_sms, enc, w, st, s)
-                    : launch_tc<4, false>(a, pl, partials, num_sms, enc, w, st, s);
+        return b_kmajor ? launch_tc<2, true>(a, pl, scratch, enc, w, st, s)
+                        : launch_tc<2, false>(a, pl, scratch, enc, w, st, s);
+    return b_kmajor ? launch_tc<4, true>(a, pl, scratch, enc, w, st, s)
+                    : launch_tc<4, false>(a, pl, scratch, enc, w, st, s);
 }
 
 cudaError_t tc_peak(int in_type, bool pair, long iters, int num_sms, unsigned long long wait_ns,

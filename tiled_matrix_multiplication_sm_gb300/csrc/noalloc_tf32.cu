@@ -125,13 +125,13 @@ extern "C" int gemm_tc_tf32_noalloc(int M, int N, int K, const float* A, long ld
     if (tgemm::transpose_f32(B, ldb, d.scratch, ldt, K, N, stream) != cudaSuccess)
         return TGEMM_ERR_CUDA;
     tgemm::GemmArgs a{M, N, K, A, lda, d.scratch, ldt, C, ldc};
-    const bool tma_c = reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 4 == 0;
-    const int shape = tgemm::tc_shape(M, N, K, tgemm::TC_TF32, -1, d.num_sms, false, tma_c);
-    // No split of the last wave: its partial tiles would need more scratch.
+    const bool tma_c = reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 4 == 0 && N % 4 == 0;
+    const int shape = tgemm::tc_shape(M, N, K, tgemm::TC_TF32, -1, d.num_sms, 0, tma_c);
+    // No stream-K tail: its partial tiles would need more scratch.
     const tgemm::TcPlan plan =
-        tgemm::tc_plan(M, N, K, tgemm::TC_TF32, shape, d.num_sms, false, tma_c);
-    if (tgemm::tc_launch(a, tgemm::TC_TF32, 1, d.num_sms, enc, tgemm::wait_limit_ns(), 0, shape, plan,
-                         nullptr, stream) != cudaSuccess)
+        tgemm::tc_plan(M, N, K, tgemm::TC_TF32, shape, d.num_sms, 0, tma_c);
+    if (tgemm::tc_launch(a, tgemm::TC_TF32, 1, enc, tgemm::wait_limit_ns(), 0, shape, plan, nullptr,
+                         stream) != cudaSuccess)
         return TGEMM_ERR_CUDA;
     return TGEMM_OK;
 }

@@ -75,31 +75,38 @@ enum TcType { TC_TF32 = 1, TC_BF16 = 2, TC_TF32X3 = 3 };
 enum TcShape { TC_ONE_SM = 0, TC_PAIR = 1, TC_PAIR_WIDE = 2 };
 // The shape a product runs with: mode -1 = the shape a timing model expects
 // to finish first, 0/1/2 = that TcShape (the split-TF32 form always takes
-// TC_PAIR). allow_split and tma_c as for tc_plan.
-int tc_shape(int M, int N, int K, int in_type, int mode, int num_sms, bool allow_split,
+// TC_PAIR). streamk and tma_c as for tc_plan.
+int tc_shape(int M, int N, int K, int in_type, int mode, int num_sms, int streamk,
              bool tma_c = true);
 const char* tc_kernel_name(int in_type, int shape);
-// Tiling of one tensor-core product: tiles of tile_rows x tile_cols, the
-// first dp_tiles whole, the rest (a partial last wave) in `split` K-pieces
-// whose partial tiles take scratch_bytes of device scratch (0 when split == 1).
+// Tiling of one tensor-core product: tiles of tile_rows x tile_cols over
+// `slots` resident units (SMs, or SM pairs), computed whole in rounds. With
+// sk_slots > 0 (stream-K), the tiles of a partial last round -- tiles
+// [dp_tiles, tiles) -- are not computed whole: their K blocks are shared
+// evenly by slots [0, sk_slots); a slot whose share ends a tile owns it and
+// adds the partial tiles of the slots before it, which wait for nothing.
+// scratch_bytes then holds sk_slots partial tiles (tc_partial_bytes) and one
+// counter per tail tile; 0 without stream-K.
 struct TcPlan {
     int tile_rows, tile_cols, tiles_m, tiles_n, kblocks;
-    int dp_tiles, split;
+    int slots, dp_tiles, sk_slots;
     size_t scratch_bytes;
     double est_us;       // modelled duration, for choosing between shapes
 };
+size_t tc_partial_bytes(const TcPlan& pl);
 // tma_c: the whole tiles can leave by TMA stores (C's base and rows 16-byte
 // aligned, beta = 0); it changes only the modelled epilogue cost.
-TcPlan tc_plan(int M, int N, int K, int in_type, int shape, int num_sms, bool allow_split,
+// streamk: -1 = a stream-K tail where the timing model prefers it (it needs
+// scratch), 0 = never, S > 0 = a tail shared by S slots where possible.
+TcPlan tc_plan(int M, int N, int K, int in_type, int shape, int num_sms, int streamk,
                bool tma_c = true);
 // Launch the persistent tcgen05 kernel of TcShape `shape` under plan `pl`
-// (made for the same shape), plus the K-piece reduction when pl.split > 1
-// (`partials` holds pl.scratch_bytes). `encode_fn` is cuTensorMapEncodeTiled.
-// With b_kmajor, a.B / a.ldb describe B transposed (N x K, K contiguous).
-cudaError_t tc_launch(const GemmArgs& a, int in_type, int b_kmajor, int num_sms,
-                      void* encode_fn, unsigned long long wait_limit_ns,
-                      int debug_stall, int shape, const TcPlan& pl, float* partials,
-                      cudaStream_t s);
+// (made for the same shape); `scratch` holds pl.scratch_bytes (it may be
+// null when that is 0). `encode_fn` is cuTensorMapEncodeTiled. With
+// b_kmajor, a.B / a.ldb describe B transposed (N x K, K contiguous).
+cudaError_t tc_launch(const GemmArgs& a, int in_type, int b_kmajor, void* encode_fn,
+                      unsigned long long wait_limit_ns, int debug_stall, int shape,
+                      const TcPlan& pl, void* scratch, cudaStream_t s);
 // Read and clear the tensor-core kernel's status word on the current device.
 cudaError_t tc_read_and_clear_status(int* status, cudaStream_t s);
 // Dense MMA rate probe: every SM (or SM pair) issues `iters` MMAs from

@@ -104,6 +104,39 @@ split_rows_kernel(const float* __restrict__ X, long ldx, float* __restrict__ hi,
     }
 }
 
+// The same on 16-byte vectors (X's rows and the outputs' rows 16-byte
+// aligned): a flat grid-stride loop over (row, vector of four columns), then
+// the cols % 4 columns past the last whole vector one by one.
+__global__ void __launch_bounds__(256)
+split_rows_vec_kernel(const float* __restrict__ X, long ldx, float* __restrict__ hi,
+                      float* __restrict__ lo, long ld_out, int rows, int cols) {
+    const int vecs = cols / 4;
+    const long total = (long)rows * vecs;
+    for (long u = blockIdx.x * (long)blockDim.x + threadIdx.x; u < total;
+         u += (long)gridDim.x * blockDim.x) {
+        const int r = (int)(u / vecs), c = (int)(u % vecs) * 4;
+        const float4 x = *reinterpret_cast<const float4*>(X + (long)r * ldx + c);
+        float4 h, l;
+        split_tf32(x.x, h.x, l.x);
+        split_tf32(x.y, h.y, l.y);
+        split_tf32(x.z, h.z, l.z);
+        split_tf32(x.w, h.w, l.w);
+        *reinterpret_cast<float4*>(hi + (long)r * ld_out + c) = h;
+        *reinterpret_cast<float4*>(lo + (long)r * ld_out + c) = l;
+    }
+    const int tail = cols % 4;
+    if (tail) {
+        for (long u = blockIdx.x * (long)blockDim.x + threadIdx.x; u < (long)rows * tail;
+             u += (long)gridDim.x * blockDim.x) {
+            const int r = (int)(u / tail), c = vecs * 4 + (int)(u % tail);
+            float h, l;
+            split_tf32(X[(long)r * ldx + c], h, l);
+            hi[(long)r * ld_out + c] = h;
+            lo[(long)r * ld_out + c] = l;
+        }
+    }
+}
+
 // Transpose of B (K x N) into hi/lo parts of Bt (N x K), through a padded
 // shared-memory tile as in transpose_kernel.
 __global__ void __launch_bounds__(TT * TROWS)
@@ -134,6 +167,16 @@ transpose_split_kernel(const float* __restrict__ B, long ldb, float* __restrict_
 
 cudaError_t split_rows_tf32(const float* X, long ldx, float* hi, float* lo, long ld_out, int rows,
                             int cols, cudaStream_t s) {
+    auto al16 = [](const void* q) { return reinterpret_cast<uintptr_t>(q) % 16 == 0; };
+    if (al16(X) && al16(hi) && al16(lo) && ldx % 4 == 0 && ld_out % 4 == 0 && cols >= 4) {
+        // 16-byte vectors: up to 4 waves of 8 blocks of 256 threads per SM.
+        const long work = (long)rows * (cols / 4);
+        long blocks = (work + 255) / 256;
+        if (blocks > 152L * 8 * 4) blocks = 152L * 8 * 4;
+        if (blocks < 1) blocks = 1;
+        split_rows_vec_kernel<<<(int)blocks, 256, 0, s>>>(X, ldx, hi, lo, ld_out, rows, cols);
+        return cudaGetLastError();
+    }
     int gx = (cols + 255) / 256;
     if (gx > 64) gx = 64;
     if (gx < 1) gx = 1;

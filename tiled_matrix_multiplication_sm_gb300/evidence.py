@@ -81,11 +81,13 @@ KERNEL_SOURCES = [
     ("sgemm_kernel", "sgemm_f32.cu"),
     ("splitk_reduce", "sgemm_f32.cu"),
     ("empty_product_kernel", "sgemm_f32.cu"),
+    ("zero_rows_vec_kernel", "sgemm_f32.cu"),
     ("tc_", "gemm_tcgen05.cu"),
     ("transpose_split_kernel", "transpose_f32.cu"),
     ("transpose_kernel", "transpose_f32.cu"),
     ("repack_kernel", "transpose_f32.cu"),
     ("split_rows_kernel", "transpose_f32.cu"),
+    ("split_rows_vec_kernel", "transpose_f32.cu"),
 ]
 
 
@@ -129,9 +131,10 @@ def case_shape(case: str):
     return w, path, w.M, w.N, w.K, w.dtype
 
 
-def run_case(case: str, products: int) -> str:
+def run_case(case: str, products: int, tc_mode: int = -1, streamk: int = -1) -> str:
     """Run ``products`` products of the case on cuda:0; return the library's
-    record of the kernels the last one launched."""
+    record of the kernels the last one launched. ``tc_mode`` and ``streamk``
+    force the tensor-core tile shape and stream-K width (-1: automatic)."""
     import torch
     import tiled_matrix_multiplication_sm_gb300 as tg
     from . import inputs
@@ -140,6 +143,8 @@ def run_case(case: str, products: int) -> str:
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(0)
     tg.load()
+    tg.binding.set_tc_kernel(tc_mode)
+    tg.binding.set_tc_streamk(streamk)
     if w is None:
         A = torch.empty(M, K, device=dev)
         B = torch.empty(K, N, device=dev)
@@ -419,6 +424,8 @@ def main(argv=None):
     r = sub.add_parser("run", help="run one case's products (the profiled child)")
     r.add_argument("--case", required=True)
     r.add_argument("--products", type=int, default=WARMUP_PRODUCTS + 1)
+    r.add_argument("--tc-mode", type=int, default=-1)
+    r.add_argument("--streamk", type=int, default=-1)
     c = sub.add_parser("capture", help="plain run, then ncu, for each case")
     c.add_argument("--case", action="append", default=None)
     c.add_argument("--out", default=os.path.join(ROOT, "gpurun_out", "evidence"))
@@ -426,7 +433,8 @@ def main(argv=None):
     s.add_argument("--records", default=os.path.join(ROOT, "profiles", "ncu"))
     args = p.parse_args(argv)
     if args.cmd == "run":
-        print(json.dumps({"kernels": run_case(args.case, args.products)}), flush=True)
+        print(json.dumps({"kernels": run_case(args.case, args.products, args.tc_mode,
+                                              args.streamk)}), flush=True)
     elif args.cmd == "capture":
         capture(args.case or CASES, args.out)
     else:
