@@ -353,6 +353,19 @@ TGEMM_API int gemm_set_tc_kernel(int mode);
  */
 TGEMM_API int gemm_set_tc_streamk(int slots);
 
+/*
+ * gemm_set_tc_a_loader — how the tensor paths read an A whose rows are 4-byte
+ * but not 16-byte aligned (for tests and tuning). The Tensor Memory
+ * Accelerator cannot copy such rows ("Tiled GEMM: Matrix Multiplication in
+ * CUDA", section 8, hands tiles to TMA), so A is either repacked first into
+ * scratch with 128-byte rows (0, and the default -1) or read in place by two
+ * extra warps of the GEMM kernel with 4-byte asynchronous copies into the
+ * layout TMA would have written (1; TGEMM_TF32, and TGEMM_BF16 with an even
+ * lda and B stored K x N). Process-wide. Returns TGEMM_OK or
+ * TGEMM_ERR_INVALID_ARG.
+ */
+TGEMM_API int gemm_set_tc_a_loader(int mode);
+
 /* Number of FP32 kernel configurations gemm_set_f32_kernel accepts. */
 TGEMM_API int gemm_f32_kernel_count(void);
 

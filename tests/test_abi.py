@@ -35,7 +35,7 @@ def test_header_declares_the_boundary():
     names = declared_symbols()
     for required in ["gemm_f32", "gemm_tc", "gemm_status_string", "gemm_device_status"]:
         assert required in names
-    assert len(names) == 17
+    assert len(names) == 18
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -159,6 +159,9 @@ def test_setters_validate(lib):
     assert binding.set_tc_streamk(-2) == binding.TGEMM_ERR_INVALID_ARG
     assert binding.set_tc_streamk(40) == binding.TGEMM_OK
     assert binding.set_tc_streamk(-1) == binding.TGEMM_OK
+    assert binding.set_tc_a_loader(2) == binding.TGEMM_ERR_INVALID_ARG
+    assert binding.set_tc_a_loader(-2) == binding.TGEMM_ERR_INVALID_ARG
+    assert binding.set_tc_a_loader(-1) == binding.TGEMM_OK
     assert lib.gemm_f32_kernel_name(n) == b""
     names = binding.f32_kernel_names()
     assert len(set(names)) == n and all(names)

@@ -48,6 +48,7 @@ _SIGNATURES = {
     "gemm_set_f32_kernel": (ctypes.c_int, [ctypes.c_int]),
     "gemm_set_tc_kernel": (ctypes.c_int, [ctypes.c_int]),
     "gemm_set_tc_streamk": (ctypes.c_int, [ctypes.c_int]),
+    "gemm_set_tc_a_loader": (ctypes.c_int, [ctypes.c_int]),
     "gemm_f32_kernel_count": (ctypes.c_int, []),
     "gemm_f32_kernel_name": (ctypes.c_char_p, [ctypes.c_int]),
     "gemm_last_kernel": (ctypes.c_char_p, []),
@@ -260,6 +261,12 @@ def set_tc_streamk(slots: int) -> int:
     """Stream-K tail of the tensor-core kernels: -1 automatic, 0 never, S > 0
     shared by S SMs or SM pairs where the tail allows it."""
     return int(load().gemm_set_tc_streamk(int(slots)))
+
+
+def set_tc_a_loader(mode: int) -> int:
+    """A with rows 4- but not 16-byte aligned on the tensor paths: -1 / 0
+    repacked first, 1 read in place by the GEMM kernel's loader warps."""
+    return int(load().gemm_set_tc_a_loader(int(mode)))
 
 
 def f32_kernel_names():

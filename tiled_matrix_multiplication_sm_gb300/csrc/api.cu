@@ -40,6 +40,7 @@ std::atomic<int> g_debug_stall{0};
 std::atomic<int> g_forced_f32{-1};
 std::atomic<int> g_tc_mode{-1};
 std::atomic<int> g_tc_streamk{-1};
+std::atomic<int> g_tc_a_loader{-1};
 thread_local const char* g_last_kernel = "";
 thread_local char g_last_kernel_buf[160];
 
@@ -211,6 +212,7 @@ struct ProductPlan {
     long ldk = 0, ldn = 0;       // scratch row pitches for rows of length K and N
     long ld_a = 0, ld_b = 0;     // leading dimensions the GEMM kernel reads
     bool b_kmajor = false;       // tensor paths: B read K-major (N x K)
+    bool a_loader = false;       // tensor paths: A (rows 4-byte aligned) read by loader warps
     size_t a_off = 0, a2_off = 0, b_off = 0, b2_off = 0, p_off = 0;
     size_t part_bytes = 0;       // partial tiles of a split last wave
     size_t scratch = 0;          // total pool scratch of the call (0: none)
@@ -260,6 +262,7 @@ int plan_product(const Request& r, const DeviceInfo& dev, ProductPlan& pp) {
     const bool f32 = path == TGEMM_PATH_F32;
     const bool tf32 = path == TGEMM_PATH_TF32;
     const bool x3 = path == TGEMM_PATH_TF32X3;
+    const bool bf16 = path == TGEMM_PATH_BF16;
     // What has to be produced before the GEMM kernel:
     //   A: M x K K-major. Transposed storage -> transpose (all paths);
     //      X3 -> hi/lo split; tensor paths with rows off 16 bytes -> repack.
@@ -286,6 +289,15 @@ int plan_product(const Request& r, const DeviceInfo& dev, ProductPlan& pp) {
             pp.prep_b = tb ? (aligned16(r.B, r.ldb) ? NONE : REPACK) : TRANSPOSE;
         else
             pp.prep_b = aligned16(r.B, r.ldb) ? NONE : REPACK;      // bf16, either storage
+        // A whose rows are 4-byte but not 16-byte aligned: repacked, or read
+        // in place by the GEMM kernel's loader warps (TF32, and BF16 with B
+        // read MN-major). The repack is the default: measured faster.
+        const bool rows4 = reinterpret_cast<uintptr_t>(r.A) % 4 == 0 && (r.lda * (long)esz) % 4 == 0;
+        const bool b_mn = !(tb || tf32);
+        if (pp.prep_a == REPACK && rows4 && (tf32 || (bf16 && b_mn)) && g_tc_a_loader.load() == 1) {
+            pp.prep_a = NONE;
+            pp.a_loader = true;
+        }
     }
     pp.b_kmajor = tb || tf32 || x3;   // tensor paths: B read K-major
     // Layout the GEMM reads: A M x K (ld_a), B K x N or N x K (ld_b).
@@ -380,6 +392,8 @@ int run_product(const Request& r, cudaStream_t stream) {
     };
     tgemm::GemmArgs a{M, N, K, r.A, pp.ld_a, r.B, pp.ld_b, r.C, r.ldc};
     a.ep = r.ep;
+    a.a_loader = pp.a_loader;
+    a.a_esz = (int)esz;
     char name_pre[64] = "";
     auto note = [&](const char* what) {
         strncat(name_pre, what, sizeof(name_pre) - strlen(name_pre) - 1);
@@ -475,8 +489,10 @@ int run_product(const Request& r, cudaStream_t stream) {
                                 (unsigned long long)g_wait_limit_ns.load(), g_debug_stall.load(),
                                 pp.shape, pp.tplan, partials, stream));
             kname = tgemm::tc_kernel_name(path, pp.shape);
+            if (pp.a_loader) strncat(tail, "(a_loader)", sizeof(tail) - strlen(tail) - 1);
             if (pp.tplan.sk_slots > 0)
-                snprintf(tail, sizeof(tail), "(streamk:slots=%d,tiles=%d)", pp.tplan.sk_slots,
+                snprintf(tail + strlen(tail), sizeof(tail) - strlen(tail),
+                         "(streamk:slots=%d,tiles=%d)", pp.tplan.sk_slots,
                          pp.tplan.tiles_m * pp.tplan.tiles_n - pp.tplan.dp_tiles);
         }
     }
@@ -856,6 +872,12 @@ int gemm_set_f32_kernel(int id) {
 int gemm_set_tc_kernel(int mode) {
     if (mode < -1 || mode > 2) return TGEMM_ERR_INVALID_ARG;
     g_tc_mode.store(mode);
+    return TGEMM_OK;
+}
+
+int gemm_set_tc_a_loader(int mode) {
+    if (mode < -1 || mode > 1) return TGEMM_ERR_INVALID_ARG;
+    g_tc_a_loader.store(mode);
     return TGEMM_OK;
 }
 

@@ -134,6 +134,11 @@ struct TcParams {
     int ep_simple;
     int tma_c;           // whole tiles leave through TMA stores (plain rule, 16-byte rows of C)
     int row_copy;        // C not stored by TMA but beta = 0: the row-copy epilogue
+    // A read by the SIMT loader warps (rows only 4-byte aligned): base, row
+    // pitch in bytes, element size.
+    const void* a_ptr;
+    long lda_bytes;
+    int a_esz;
 };
 
 // One output under the rule (C_old read only when beta != 0).
@@ -263,16 +268,30 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try, acquiring at cluster scope: for barriers that threads of the
+// peer CTA arrive on with release.cluster semantics.
+__device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
 // Wait until the phase of `bar` with parity `parity` has completed. Gives up
 // (returns false) when the block's abort flag is raised or, if
 // `honour_abort` is false, only when `limit_ns` has passed; a wait that runs
 // out raises the abort flag and records the timeout.
 __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* abort_flag,
-                                       unsigned long long limit_ns, bool honour_abort) {
-    if (mbar_try(bar, parity)) return true;
+                                       unsigned long long limit_ns, bool honour_abort,
+                                       bool cluster_acquire = false) {
+    auto test = [&]() { return cluster_acquire ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity); };
+    if (test()) return true;
     const unsigned long long t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try(bar, parity)) return true;
+        if (test()) return true;
         if ((it & 15u) == 0) {
             if (honour_abort && *(volatile int*)abort_flag) return false;
             if (globaltimer() - t0 > limit_ns || it >= (1u << 30)) {
@@ -464,6 +483,101 @@ __device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& mb, i
     const int gm = min(p.tiles_m - first_m, GROUP_M);
     mb = first_m + (t % per_group) % gm;
     nb = (t % per_group) / gm;
+}
+
+// ---- SIMT loader for A whose rows are only 4-byte aligned
+//
+// TMA copies need rows that start on 16-byte boundaries. For A without them
+// (fp32 with any lda, bf16 with an even lda) A_LOADER_WARPS extra warps copy
+// each CTA's 128 rows of a K block (128 bytes a row) straight from the
+// caller's A with 4-byte cp.async -- lane l moves word l of a row -- into the
+// same 128-byte-swizzled K-major layout a TMA copy writes (16-byte chunk j of
+// row r at j ^ (r % 8)), zero-filling words past K and rows past M. Each warp
+// commits one group per stage and, A_LOADER_LAG stages later, waits for it,
+// fences its writes into the async proxy (the tensor core reads them) and
+// arrives on the stage's full barrier, which also counts the TMA bytes of B.
+constexpr int A_LOADER_WARPS = 2;
+constexpr int A_LOADER_LAG = 2;       // the wide tiles' (4-stage ring whose MMA holds stages)
+// Stages in flight per loader warp for a ring of NSTAGES whose MMA frees
+// each stage as it consumes it: all but two.
+template <int NSTAGES>
+__host__ __device__ constexpr int loader_lag() { return NSTAGES - 2 > 1 ? NSTAGES - 2 : 1; }
+
+// This warp's 64 rows (from row r0 of the CTA's 128) of K block kb.
+__device__ __forceinline__ void a_loader_stage(uint32_t a_dst, const TcParams& p, int row_first,
+                                               int r0, int kb) {
+    const int lane = threadIdx.x & 31;
+    const long kbyte = (long)kb * SW + lane * 4;              // this word's byte within a row
+    const long row_bytes = (long)p.K * p.a_esz;
+    const int sz = kbyte + 4 <= row_bytes ? 4 : (kbyte < row_bytes ? (int)(row_bytes - kbyte) : 0);
+    const char* a = static_cast<const char*>(p.a_ptr);
+    const uint32_t col = (uint32_t)(lane & 3) * 4;
+    const uint32_t chunk = (uint32_t)lane >> 2;
+#pragma unroll 8
+    for (int r = r0; r < r0 + 64; ++r) {
+        const int grow = row_first + r;
+        const int n = grow < p.M ? sz : 0;
+        const char* src = n ? a + (long)grow * p.lda_bytes + kbyte : a;
+        const uint32_t dst = a_dst + (uint32_t)r * SW + ((chunk ^ (uint32_t)(r & 7)) << 4) + col;
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" :: "r"(dst), "l"(src), "r"(n)
+                     : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Signal stage s loaded (this warp's part): one arrival on the full barrier
+// at `full0` + 8 s -- a shared::cta address (CLUSTER false) or, for the
+// leader's barrier in a CTA pair, a shared::cluster address.
+template <bool CLUSTER>
+__device__ __forceinline__ void a_loader_signal(uint32_t full0, int s) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) {
+        const uint32_t bar = full0 + (uint32_t)(s * sizeof(uint64_t));
+        if constexpr (CLUSTER) mbar_arrive_cluster(bar); else mbar_arrive(bar);
+    }
+}
+
+// The loop of one loader warp (index lw) over the units of `slot`, in the
+// producer's stage order. `rank_rows` is the CTA's first row within a tile.
+template <int NSTAGES, bool CLUSTER, int LAG>
+__device__ __forceinline__ void a_loader_loop(const TcParams& p, int slot, int lw, uint32_t a_base,
+                                              uint32_t a_stage_bytes, uint64_t* empty,
+                                              uint32_t full0, int rank_rows, int* abort_flag,
+                                              unsigned long long lim) {
+    const int lane = threadIdx.x & 31;
+    int g = 0;
+    const int nu = slot_unit_count(p, slot);
+    for (int i = 0; i < nu; ++i) {
+        const Unit w = slot_unit(p, slot, i);
+        int mb, nb;
+        tile_coords(w.tile, p, mb, nb);
+        const int row_first = mb * p.tile_rows + rank_rows;
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++g) {
+            const int s = g % NSTAGES;
+            const uint32_t ph = (uint32_t)(g / NSTAGES) & 1u;
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(smem_u32(&empty[s]), ph ^ 1u, abort_flag, lim, true) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) goto loader_done;
+            if (p.debug_stall && g == 0)
+                asm volatile("cp.async.commit_group;" ::: "memory");   // test hook: stage 0 stays empty
+            else
+                a_loader_stage(a_base + (uint32_t)s * a_stage_bytes, p, row_first, lw * 64, kb);
+            if (g >= LAG) {
+                asm volatile("cp.async.wait_group %0;" :: "n"(LAG) : "memory");
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                const int gd = g - LAG;
+                if (!(p.debug_stall && gd == 0)) a_loader_signal<CLUSTER>(full0, gd % NSTAGES);
+            }
+        }
+    }
+loader_done:
+    // The stages still in flight (also after an abort, so that the
+    // producer's drain of its own copies can complete).
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    for (int gd = g > LAG ? g - LAG : 0; gd < g; ++gd)
+        if (!(p.debug_stall && gd == 0)) a_loader_signal<CLUSTER>(full0, gd % NSTAGES);
 }
 
 // 32 consecutive values to a 4-byte aligned address whose first H values
@@ -837,8 +951,9 @@ __device__ __forceinline__ void store_accumulator(const TcParams& p, const Unit&
 
 // B_KMAJOR: B arrives transposed (N x K, K contiguous) and is read K-major;
 // otherwise B is K x N (N contiguous) and is read MN-major.
-template <int ESZ, bool B_KMAJOR>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+// A_LOADER: A is read by the SIMT loader warps (warps 6..), not by TMA.
+template <int ESZ, bool B_KMAJOR, bool A_LOADER = false>
+__global__ void __launch_bounds__(NUM_THREADS + (A_LOADER ? 32 * A_LOADER_WARPS : 0), 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC,
@@ -866,7 +981,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&sy->full[s]), 1);
+            // The producer's arrival (with the TMA bytes), and each loader warp's.
+            mbar_init(smem_u32(&sy->full[s]), 1 + (A_LOADER ? A_LOADER_WARPS : 0));
             mbar_init(smem_u32(&sy->empty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -877,7 +993,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         sy->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+        if (!A_LOADER)
+            asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
         asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
     }
     if (warp == 1) {
@@ -907,8 +1024,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     if (!mbar_wait(smem_u32(&sy->empty[s]), ph ^ 1u, &sy->abort, lim, true)) goto producer_done;
                     if (p.debug_stall && g == 0) continue;     // test hook: never fill stage 0
                     const uint32_t full = smem_u32(&sy->full[s]);
-                    mbar_arrive_expect_tx(full, STAGE_BYTES);
-                    tma_load_2d(a_base + s * A_STAGE_BYTES, &tmA, kb * BK, mb * BM, full);
+                    mbar_arrive_expect_tx(full, A_LOADER ? B_STAGE_BYTES : STAGE_BYTES);
+                    if constexpr (!A_LOADER)
+                        tma_load_2d(a_base + s * A_STAGE_BYTES, &tmA, kb * BK, mb * BM, full);
                     const uint32_t bdst = b_base + s * B_STAGE_BYTES;
                     if constexpr (B_KMAJOR) {
                         tma_load_2d(bdst, &tmB, kb * BK, nb * BN, full);
@@ -967,6 +1085,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             mbar_wait(smem_u32(&sy->drain), 0, &sy->abort, lim, false);
         }
         __syncwarp();
+    } else if (warp >= 6) {
+        // ------------------------------------------------ A loader (warps 6..)
+        if constexpr (A_LOADER)
+            a_loader_loop<STAGES, false, loader_lag<STAGES>()>(p, blockIdx.x, warp - 6, a_base,
+                                                             A_STAGE_BYTES, sy->empty,
+                                         smem_u32(&sy->full[0]), 0, &sy->abort, lim);
     } else {
         // ------------------------------------------------ epilogue (warps 2-5)
         const int q = warp & 3;                 // TMEM lanes 32q .. 32q+31
@@ -1090,8 +1214,10 @@ static_assert(sizeof(PairSync) <= 256, "pair barrier block");
 // same accumulator, lo(A) hi(B) + hi(A) lo(B) + hi(A) hi(B), which carries
 // the product to FP32-level accuracy (the lo x lo term is below FP32's own
 // rounding).
-template <int ESZ, bool B_KMAJOR, bool X3, int NW>
-__global__ void __launch_bounds__(PairEpi<NW>::THREADS, 1)
+// A_LOADER: A is read by the SIMT loader warps (after the epilogue warps),
+// not by TMA; each CTA loads its own 128 rows.
+template <int ESZ, bool B_KMAJOR, bool X3, int NW, bool A_LOADER = false>
+__global__ void __launch_bounds__(PairEpi<NW>::THREADS + (A_LOADER ? 32 * A_LOADER_WARPS : 0), 1)
 tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmA2,
@@ -1101,6 +1227,7 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
     using R = PairRing<X3, NW>;
     static_assert(!X3 || (ESZ == 4 && B_KMAJOR), "the split form is TF32 with B K-major");
     static_assert(NW == 1 || (NW == 2 && !X3), "wide tiles are for the one-product forms");
+    static_assert(!(A_LOADER && X3), "the split form reads its own aligned copies of A");
     constexpr int NACC = 2 / NW;                         // accumulators in tensor memory
     using KD = Kind<ESZ>;
     constexpr int BK = KD::BK;
@@ -1128,7 +1255,9 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < R::STAGES; ++s) {
-            mbar_init(smem_u32(&sy->full[s]), 1);
+            // The leader producer's arrival (with both CTAs' TMA bytes), and
+            // each loader warp's of both CTAs.
+            mbar_init(smem_u32(&sy->full[s]), 1 + (A_LOADER ? 2 * A_LOADER_WARPS : 0));
             mbar_init(smem_u32(&sy->empty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -1178,9 +1307,10 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
                     if (!mbar_wait(smem_u32(&sy->empty[s]), ph ^ 1u, &sy->abort, lim, true)) goto pair_producer_done;
                     if (p.debug_stall && g == 0) continue;     // test hook: stage 0 never filled
                     const uint32_t full = full0 + (uint32_t)(s * sizeof(uint64_t));
-                    if (leader) mbar_arrive_expect_tx(smem_u32(&sy->full[s]), 2 * R::STAGE);
+                    if (leader)
+                        mbar_arrive_expect_tx(smem_u32(&sy->full[s]), 2 * (A_LOADER ? R::B_STAGE : R::STAGE));
                     const uint32_t adst = a_base + s * R::A_STAGE;
-                    tma_load_2d_pair(adst, &tmA, kb * BK, row0, full);
+                    if constexpr (!A_LOADER) tma_load_2d_pair(adst, &tmA, kb * BK, row0, full);
                     const uint32_t bdst = b_base + s * R::B_STAGE;
                     if constexpr (X3) {
                         tma_load_2d_pair(adst + P_A_TILE, &tmA2, kb * BK, row0, full);
@@ -1224,6 +1354,12 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
         // ------------------------------------------------ MMA issuer (leader CTA)
         if (lane == 0 && leader) {
             int g = 0, it = 0;
+            // Stages the wide tiles' MMA issuer waits for before it frees one.
+            // The loader warps signal a stage only A_LOADER_LAG stages after
+            // they issued it (which needs a freed stage), so with them the
+            // issuer may hold no more than STAGES - A_LOADER_LAG.
+            constexpr int HOLD = A_LOADER ? R::STAGES - A_LOADER_LAG : R::STAGES;
+            static_assert(HOLD >= 1, "stages to hold");
             // The MMAs of ring stage s (K block kb of unit w) for B tiles [h0, h1).
             auto issue = [&](int s, int kb, const Unit& w, uint32_t d_tmem, int h0, int h1) {
                 const uint32_t a_addr = a_base + s * R::A_STAGE;
@@ -1267,11 +1403,11 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
                     // the other (tmem_empty[0], then tmem_empty[1]). Run the first
                     // half's MMAs on the stages already loaded while the second
                     // half still drains, then catch up on the second half's.
-                    const int held = min(R::STAGES, w.kb1 - w.kb0);
+                    const int held = min(HOLD, w.kb1 - w.kb0);
                     for (int i = 0; i < held; ++i) {
                         const int s = (g + i) % R::STAGES;
                         const uint32_t ph = (uint32_t)((g + i) / R::STAGES) & 1u;
-                        if (!mbar_wait(smem_u32(&sy->full[s]), ph, &sy->abort, lim, true)) { ok = false; break; }
+                        if (!mbar_wait(smem_u32(&sy->full[s]), ph, &sy->abort, lim, true, A_LOADER)) { ok = false; break; }
                         tc_fence_after();
                         issue(s, w.kb0 + i, w, d_tmem, 0, 1);
                     }
@@ -1291,11 +1427,11 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
                 // Wide tiles: the last K blocks (as many as the ring holds) run
                 // the first half's MMAs before the second half's, so the first
                 // half is complete (tmem_full[0]) while the second still computes.
-                const int tail = NW == 2 ? min(R::STAGES, w.kb1 - kb) : 0;
+                const int tail = NW == 2 ? min(HOLD, w.kb1 - kb) : 0;
                 for (; ok && kb < w.kb1 - tail; ++kb, ++g) {
                     const int s = g % R::STAGES;
                     const uint32_t ph = (uint32_t)(g / R::STAGES) & 1u;
-                    if (!mbar_wait(smem_u32(&sy->full[s]), ph, &sy->abort, lim, true)) { ok = false; break; }
+                    if (!mbar_wait(smem_u32(&sy->full[s]), ph, &sy->abort, lim, true, A_LOADER)) { ok = false; break; }
                     tc_fence_after();
                     issue(s, kb, w, d_tmem, 0, NW);
                     tc_commit_pair_multicast(smem_u32(&sy->empty[s]));   // slot free in both CTAs
@@ -1305,7 +1441,7 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
                     for (int i = 0; i < tail; ++i) {
                         const int s = (g + i) % R::STAGES;
                         const uint32_t ph = (uint32_t)((g + i) / R::STAGES) & 1u;
-                        if (!mbar_wait(smem_u32(&sy->full[s]), ph, &sy->abort, lim, true)) { ok = false; break; }
+                        if (!mbar_wait(smem_u32(&sy->full[s]), ph, &sy->abort, lim, true, A_LOADER)) { ok = false; break; }
                         tc_fence_after();
                         issue(s, kb + i, w, d_tmem, 0, 1);
                     }
@@ -1327,6 +1463,12 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
             mbar_wait(smem_u32(&sy->drain), 0, &sy->abort, lim, false);
         }
         __syncwarp();
+    } else if (warp >= 2 + PairEpi<NW>::WARPS) {
+        // ------------------------------------------------ A loader (both CTAs)
+        if constexpr (A_LOADER)
+            a_loader_loop<R::STAGES, true, NW == 2 ? A_LOADER_LAG : loader_lag<R::STAGES>()>(
+                p, pair, warp - 2 - PairEpi<NW>::WARPS, a_base, R::A_STAGE, sy->empty, full0,
+                (int)rank * 128, &sy->abort, lim);
     } else {
         // ------------------------------------------------ epilogue (warps 2.., both CTAs)
         const int q = warp & 3;                              // TMEM lanes 32q .. 32q+31
@@ -1448,6 +1590,9 @@ TcParams make_params(const GemmArgs& a, const TcPlan& pl, void* scratch, int arr
     p.ep_simple = a.ep.simple() ? 1 : 0;
     p.tma_c = 0;
     p.row_copy = 0;
+    p.a_ptr = a.A;
+    p.lda_bytes = a.lda * (long)(a.a_esz > 0 ? a.a_esz : 4);
+    p.a_esz = a.a_esz > 0 ? a.a_esz : 4;
     return p;
 }
 
@@ -1479,12 +1624,14 @@ int grid_slots(const TcPlan& pl) {
     return pl.dp_tiles > 0 ? pl.slots : pl.sk_slots;
 }
 
-template <int ESZ, bool B_KMAJOR>
+template <int ESZ, bool B_KMAJOR, bool A_LOADER = false>
 cudaError_t launch_tc(const GemmArgs& a, const TcPlan& pl, void* scratch, EncodeTiledFn enc,
                       unsigned long long wait_limit_ns, int debug_stall, cudaStream_t s) {
     constexpr int BK = Kind<ESZ>::BK;
     CUtensorMap tmA, tmB;
-    if (!encode_2d(enc, &tmA, a.A, ESZ, a.M, a.K, a.lda, BK, BM)) return cudaErrorInvalidValue;
+    memset(&tmA, 0, sizeof(tmA));
+    if (!A_LOADER && !encode_2d(enc, &tmA, a.A, ESZ, a.M, a.K, a.lda, BK, BM))
+        return cudaErrorInvalidValue;
     const bool okb = B_KMAJOR ? encode_2d(enc, &tmB, a.B, ESZ, a.N, a.K, a.ldb, BK, BN)
                               : encode_2d(enc, &tmB, a.B, ESZ, a.K, a.N, a.ldb, SW / ESZ, BK);
     if (!okb) return cudaErrorInvalidValue;
@@ -1494,22 +1641,27 @@ cudaError_t launch_tc(const GemmArgs& a, const TcPlan& pl, void* scratch, Encode
     p.row_copy = (!p.tma_c && a.ep.beta == 0.0f) ? 1 : 0;
     if (!prepare_stream_k(p, s)) return cudaErrorInvalidValue;
 
-    auto kern = tc_gemm_kernel<ESZ, B_KMAJOR>;
-    cudaError_t e = set_smem_limit_once<tc_gemm_kernel<ESZ, B_KMAJOR>>(SMEM_BYTES);
+    p.a_esz = ESZ;
+    p.lda_bytes = a.lda * (long)ESZ;
+    auto kern = tc_gemm_kernel<ESZ, B_KMAJOR, A_LOADER>;
+    cudaError_t e = set_smem_limit_once<tc_gemm_kernel<ESZ, B_KMAJOR, A_LOADER>>(SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<grid_slots(pl), NUM_THREADS, SMEM_BYTES, s>>>(tmA, tmB, tmC, p);
+    kern<<<grid_slots(pl), NUM_THREADS + (A_LOADER ? 32 * A_LOADER_WARPS : 0), SMEM_BYTES, s>>>(
+        tmA, tmB, tmC, p);
     return cudaGetLastError();
 }
 
 // The 2-SM kernel: clusters of two CTAs, one CTA per SM, persistent over
 // 256 x 256 tiles (NW = 1) or 256 x 512 tiles (NW = 2).
-template <int ESZ, bool B_KMAJOR, bool X3 = false, int NW = 1>
+template <int ESZ, bool B_KMAJOR, bool X3 = false, int NW = 1, bool A_LOADER = false>
 cudaError_t launch_tc_pair(const GemmArgs& a, const TcPlan& pl, void* scratch, EncodeTiledFn enc,
                            unsigned long long wait_limit_ns, int debug_stall, cudaStream_t s) {
     constexpr int BK = Kind<ESZ>::BK;
     constexpr int SMEM = pair_smem_bytes<X3, NW>();
     CUtensorMap tmA, tmB, tmA2, tmB2;
-    if (!encode_2d(enc, &tmA, a.A, ESZ, a.M, a.K, a.lda, BK, 128)) return cudaErrorInvalidValue;
+    memset(&tmA, 0, sizeof(tmA));
+    if (!A_LOADER && !encode_2d(enc, &tmA, a.A, ESZ, a.M, a.K, a.lda, BK, 128))
+        return cudaErrorInvalidValue;
     const bool okb = B_KMAJOR ? encode_2d(enc, &tmB, a.B, ESZ, a.N, a.K, a.ldb, BK, 128)
                               : encode_2d(enc, &tmB, a.B, ESZ, a.K, a.N, a.ldb, SW / ESZ, BK);
     if (!okb) return cudaErrorInvalidValue;
@@ -1528,12 +1680,14 @@ cudaError_t launch_tc_pair(const GemmArgs& a, const TcPlan& pl, void* scratch, E
     p.row_copy = (NW == 1 && !p.tma_c && a.ep.beta == 0.0f) ? 1 : 0;
     if (!prepare_stream_k(p, s)) return cudaErrorInvalidValue;
 
-    auto kern = tc_gemm_2sm_kernel<ESZ, B_KMAJOR, X3, NW>;
-    cudaError_t e = set_smem_limit_once<tc_gemm_2sm_kernel<ESZ, B_KMAJOR, X3, NW>>(SMEM);
+    p.a_esz = ESZ;
+    p.lda_bytes = a.lda * (long)ESZ;
+    auto kern = tc_gemm_2sm_kernel<ESZ, B_KMAJOR, X3, NW, A_LOADER>;
+    cudaError_t e = set_smem_limit_once<tc_gemm_2sm_kernel<ESZ, B_KMAJOR, X3, NW, A_LOADER>>(SMEM);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * grid_slots(pl), 1, 1);
-    cfg.blockDim = dim3(PairEpi<NW>::THREADS, 1, 1);
+    cfg.blockDim = dim3(PairEpi<NW>::THREADS + (A_LOADER ? 32 * A_LOADER_WARPS : 0), 1, 1);
     cfg.dynamicSmemBytes = SMEM;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -1800,8 +1954,23 @@ cudaError_t tc_launch(const GemmArgs& a, int in_type, int b_kmajor, void* encode
     const int st = debug_stall;
     if (pl.sk_slots > 0 && scratch == nullptr) return cudaErrorInvalidValue;
     if (in_type == TC_TF32X3)       // always the CTA-pair kernel, B K-major
-        return launch_tc_pair<4, true, true>(a, pl, scratch, enc, w, st, s);
+        return a.a_loader ? cudaErrorInvalidValue
+                          : launch_tc_pair<4, true, true>(a, pl, scratch, enc, w, st, s);
     if ((shape == TC_PAIR_WIDE) != (pl.tile_cols == 2 * BN)) return cudaErrorInvalidValue;
+    if (a.a_loader) {
+        // A read by the loader warps: TF32 (B K-major) and BF16 with B MN-major.
+        const bool tf32 = in_type == TC_TF32 && b_kmajor;
+        const bool bf16 = in_type == TC_BF16 && !b_kmajor;
+        if (!tf32 && !bf16) return cudaErrorInvalidValue;
+        if (shape == TC_PAIR_WIDE)
+            return tf32 ? launch_tc_pair<4, true, false, 2, true>(a, pl, scratch, enc, w, st, s)
+                        : launch_tc_pair<2, false, false, 2, true>(a, pl, scratch, enc, w, st, s);
+        if (shape == TC_PAIR)
+            return tf32 ? launch_tc_pair<4, true, false, 1, true>(a, pl, scratch, enc, w, st, s)
+                        : launch_tc_pair<2, false, false, 1, true>(a, pl, scratch, enc, w, st, s);
+        return tf32 ? launch_tc<4, true, true>(a, pl, scratch, enc, w, st, s)
+                    : launch_tc<2, false, true>(a, pl, scratch, enc, w, st, s);
+    }
     if (shape == TC_PAIR_WIDE) {
         if (in_type == TC_BF16)
             return b_kmajor ? launch_tc_pair<2, true, false, 2>(a, pl, scratch, enc, w, st, s)

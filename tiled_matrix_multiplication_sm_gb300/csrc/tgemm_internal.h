@@ -44,6 +44,10 @@ struct GemmArgs {
     const void* A2 = nullptr;
     const void* B2 = nullptr;
     Epilogue ep = Epilogue();
+    // Tensor paths: A's rows are only 4-byte aligned and are read by the
+    // kernel's SIMT loader warps instead of TMA (a_esz: A's element size).
+    bool a_loader = false;
+    int a_esz = 0;
 };
 
 // ---- FP32 CUDA-core path (sgemm_f32.cu) ---------------------------------
