@@ -26,8 +26,9 @@
  *   - Scratch memory. A call may need device memory of its own while it
  *     runs, for two things:
  *       (a) operands rewritten into a layout the kernels read: on gemm_tc
- *           TGEMM_TF32, B transposed (N x round_up(K, 32) floats) on every
- *           call; on the tensor paths, an operand whose rows do not start
+ *           TGEMM_TF32 with M > 128 (or tensor-core mode 0, 1 or 2
+ *           forced), B transposed (N x round_up(K, 32) floats); on the
+ *           tensor paths, an operand whose rows do not start
  *           on 16-byte boundaries, repacked (rows on 128-byte boundaries);
  *           on gemm_f32, both operands repacked when their rows are off 16
  *           bytes and M >= 256, N >= 256, K >= 64; on TGEMM_TF32X3, high
@@ -44,8 +45,9 @@
  *     once a call of a given size has run, later calls reuse the cached
  *     memory without going to the driver; it stays reserved until the
  *     process exits. A call that needs neither (a) nor (b) allocates
- *     nothing: gemm_f32 and gemm_tc TGEMM_BF16 on operands with 16-byte
- *     rows whose tiles fill whole waves or whose tail is not split.
+ *     nothing: gemm_f32, gemm_tc TGEMM_BF16, and gemm_tc TGEMM_TF32 with
+ *     M <= 128, on operands with 16-byte rows whose tiles fill whole waves
+ *     or whose tail is not split.
  *     gemm_scratch_bytes() returns the size a call would draw, and
  *     gemm_tc_tf32_noalloc() never allocates.
  *   - C is overwritten (there is no alpha/beta); K == 0 writes zeros to the
@@ -142,12 +144,14 @@ TGEMM_API int gemm_f32(int M, int N, int K,
  * boundaries: an operand whose pointer or leading dimension breaks that
  * (any lda, ldb and element-aligned pointer are accepted) is first repacked
  * by an HBM-bound kernel into stream-ordered scratch with rows on 128-byte
- * boundaries; for
- * TF32, B is always rewritten transposed (the TF32 kind reads B only
- * K-major), which also absorbs any alignment of B. Rows and columns past M,
- * N, K read as zero. Scratch (see the common rules): those rewritten
- * operands, and the partial tiles of a split last wave; BF16 on operands
- * with 16-byte rows whose tail is not split allocates nothing.
+ * boundaries. The TF32 kind reads B only K-major: for TF32 with M > 128, B
+ * is first rewritten transposed into scratch, which also absorbs any
+ * alignment of B; with M <= 128 (a product bound by reading B once) the
+ * kernel reads B as stored, K x N, and transposes each 32 x 128 block in
+ * shared memory (128 x 128 tiles). Rows and columns past M, N, K read as
+ * zero. Scratch (see the common rules): those rewritten operands, and the
+ * partial tiles of a split last wave; BF16, and TF32 with M <= 128, on
+ * operands with 16-byte rows whose tail is not split allocate nothing.
  *
  * Returns TGEMM_OK, TGEMM_ERR_INVALID_ARG (as gemm_f32, a bad in_type, or
  * a pointer not aligned to its element size), TGEMM_ERR_UNSUPPORTED or
@@ -325,8 +329,11 @@ TGEMM_API int gemm_set_f32_kernel(int id);
 /*
  * gemm_set_tc_kernel — choose the tensor-core kernel (for tests and tuning):
  * 0 forces the one-SM kernel (128 x 256 tiles), 1 the 2-SM kernel (a CTA
- * pair computing 256 x 256 tiles), 2 the 2-SM kernel with 256 x 512 tiles;
- * -1 (default) picks by shape: the one-SM kernel when M <= 128, 256 x 256
+ * pair computing 256 x 256 tiles), 2 the 2-SM kernel with 256 x 512 tiles,
+ * 3 the one-SM TF32 kernel that transposes B in shared memory (128 x 128
+ * tiles; TGEMM_TF32 with B stored K x N, other products as with -1);
+ * -1 (default) picks by shape: for TGEMM_TF32 with B stored K x N and
+ * M <= 128 the kernel of mode 3, the one-SM kernel when M <= 128, 256 x 256
  * tiles when N <= 256, and otherwise the pair shape that a timing model of
  * the two expects to finish first (whole-tile rounds over the SM pairs, the
  * cost of a split last wave, a main-loop rate per shape and type measured
@@ -380,7 +387,9 @@ TGEMM_API const char* gemm_f32_kernel_name(int id);
  * gemm_f32, gemm_tc or gemm_ex call on this thread launched, in launch
  * order, joined by '+' when a call launched more than one: the pre-passes
  * (repack_a, repack_b, transpose_a, transpose_b, split_a, split_b,
- * transpose_split_a, transpose_split_b), the GEMM kernel's configuration
+ * transpose_split_a, transpose_split_b, and dup_a: A written transposed
+ * with every value twice, for the FP32 configurations that read it so),
+ * the GEMM kernel's configuration
  * name, and "splitk_reduce(split=S,tiles=T)" when T tiles of a partial last
  * wave were computed in S K-pieces each and summed by a reduction kernel
  * (FP32 path); a tensor-core kernel's name carries "(streamk:slots=S,tiles=T)"

@@ -79,7 +79,7 @@ def test_bf16_whole_waves_allocate_nothing(tgemm):
 def streamk_bytes(name):
     """Scratch of a stream-K tail named in a last-kernel record: one partial
     tile per sharing slot, then one counter per tail tile."""
-    m = re.search(r"(\d+)x(\d+)x\d+_s\d+_persistent\(streamk:slots=(\d+),tiles=(\d+)\)", name)
+    m = re.search(r"(\d+)x(\d+)x\d+_s\d+(?:_btrans)?_persistent\(streamk:slots=(\d+),tiles=(\d+)\)", name)
     if not m:
         return 0
     rows, cols, slots, tiles = (int(x) for x in m.groups())
@@ -89,15 +89,27 @@ def streamk_bytes(name):
 
 
 def test_tf32_transposes_b(tgemm):
-    """TF32 always writes B transposed, N x round_up(K, 32) floats, plus the
-    stream-K tail's partial tiles and counters when the planner shares the
-    two tiles among SM pairs."""
+    """TF32 with more than 128 rows of A writes B transposed, N x
+    round_up(K, 32) floats, plus the stream-K tail's partial tiles and
+    counters when the planner shares the two tiles among SM pairs."""
     M, N, K = 200, 300, 1000
     A, B = int_operands(M, N, K, torch.float32, 3)
     n = tgemm.binding.scratch_bytes(A, B, "tf32")
     check_product(tgemm, A, B, "tf32")
     bt = round_up(N * round_up(K, 32) * 4, 256)
     assert n == bt + streamk_bytes(tgemm.binding.last_kernel()), tgemm.binding.last_kernel()
+
+
+def test_tf32_few_rows_read_b_in_place(tgemm):
+    """TF32 with at most 128 rows of A reads B as stored (the kernel
+    transposes it in shared memory): no scratch beyond a stream-K tail's."""
+    M, N, K = 100, 1000, 512
+    A, B = int_operands(M, N, K, torch.float32, 6)
+    n = tgemm.binding.scratch_bytes(A, B, "tf32")
+    check_product(tgemm, A, B, "tf32")
+    name = tgemm.binding.last_kernel()
+    assert "btrans" in name and "transpose_b" not in name, name
+    assert n == streamk_bytes(name), name
 
 
 def test_unaligned_rows_are_repacked(tgemm):

@@ -243,6 +243,16 @@ int check_request(const Request& r) {
     return TGEMM_OK;
 }
 
+// TF32 with B stored K x N: the kernel that transposes B in shared memory
+// (128 x 128 tiles) instead of a transpose pre-pass and the 128 x 256 one-SM
+// kernel. Taken when forced (tensor-core mode 3) and, by default, when A has
+// at most 128 rows: such products are bound by reading B, which the
+// pre-pass would move through memory three times (16 x 14336 x 4096:
+// measured 139 us with the pre-pass).
+bool tf32_in_kernel_transpose(int M, int mode) {
+    return mode == 3 || (mode == -1 && M <= 128);
+}
+
 // Plan a checked request with K > 0 on a device with dev.num_sms SMs.
 int plan_product(const Request& r, const DeviceInfo& dev, ProductPlan& pp) {
     const bool ta = (r.flags & TGEMM_TRANS_A) != 0, tb = (r.flags & TGEMM_TRANS_B) != 0;
@@ -285,21 +295,27 @@ int plan_product(const Request& r, const DeviceInfo& dev, ProductPlan& pp) {
         pp.prep_b = tb ? TRANSPOSE : (big && !aligned16(r.B, r.ldb) ? REPACK : NONE);
     } else {
         pp.prep_a = ta ? TRANSPOSE : (aligned16(r.A, r.lda) ? NONE : REPACK);
-        if (tf32)
+        if (tf32 && !tb && tf32_in_kernel_transpose(M, g_tc_mode.load()))
+            pp.shape = tgemm::TC_ONE_SM_T;
+        const bool b_t = pp.shape == tgemm::TC_ONE_SM_T;
+        if (tf32 && !b_t)
             pp.prep_b = tb ? (aligned16(r.B, r.ldb) ? NONE : REPACK) : TRANSPOSE;
-        else
-            pp.prep_b = aligned16(r.B, r.ldb) ? NONE : REPACK;      // bf16, either storage
+        else     // bf16 (either storage), TF32 read as stored K x N
+            pp.prep_b = aligned16(r.B, r.ldb) ? NONE : REPACK;
         // A whose rows are 4-byte but not 16-byte aligned: repacked, or read
-        // in place by the GEMM kernel's loader warps (TF32, and BF16 with B
-        // read MN-major). The repack is the default: measured faster.
+        // in place by the GEMM kernel's loader warps (TF32 with B K-major, and
+        // BF16 with B read MN-major). The repack is the default: measured faster.
         const bool rows4 = reinterpret_cast<uintptr_t>(r.A) % 4 == 0 && (r.lda * (long)esz) % 4 == 0;
         const bool b_mn = !(tb || tf32);
-        if (pp.prep_a == REPACK && rows4 && (tf32 || (bf16 && b_mn)) && g_tc_a_loader.load() == 1) {
+        if (pp.prep_a == REPACK && rows4 && ((tf32 && !b_t) || (bf16 && b_mn)) &&
+            g_tc_a_loader.load() == 1) {
             pp.prep_a = NONE;
             pp.a_loader = true;
         }
     }
-    pp.b_kmajor = tb || tf32 || x3;   // tensor paths: B read K-major
+    // Tensor paths: B read K-major, except BF16 and the transposing TF32
+    // kernel with B stored K x N.
+    pp.b_kmajor = tb || x3 || (tf32 && pp.shape != tgemm::TC_ONE_SM_T);
     // Layout the GEMM reads: A M x K (ld_a), B K x N or N x K (ld_b).
     pp.ld_a = pp.prep_a == NONE ? r.lda : pp.ldk;
     pp.ld_b = pp.prep_b == NONE ? r.ldb : ((f32 || !pp.b_kmajor) ? pp.ldn : pp.ldk);
@@ -333,7 +349,8 @@ int plan_product(const Request& r, const DeviceInfo& dev, ProductPlan& pp) {
         const bool tma_c = reinterpret_cast<uintptr_t>(r.C) % 16 == 0 && r.ldc % 4 == 0 &&
                            N % 4 == 0 && r.ep.beta == 0.0f;
         const int sk = g_tc_streamk.load();
-        pp.shape = tgemm::tc_shape(M, N, K, path, g_tc_mode.load(), dev.num_sms, sk, tma_c);
+        if (pp.shape != tgemm::TC_ONE_SM_T)
+            pp.shape = tgemm::tc_shape(M, N, K, path, g_tc_mode.load(), dev.num_sms, sk, tma_c);
         pp.tplan = tgemm::tc_plan(M, N, K, path, pp.shape, dev.num_sms, sk, tma_c);
     }
     pp.part_bytes = f32 ? pp.fplan.scratch_bytes : pp.tplan.scratch_bytes;
@@ -480,6 +497,7 @@ int run_product(const Request& r, cudaStream_t stream) {
     if (rc == TGEMM_OK) {
         if (f32) {
             ok(tgemm::f32_launch(pp.f32_id, a, pp.fplan, partials, stream));
+            if (pp.fplan.a2_bytes > 0) note("dup_a+");     // the duplicated-A pre-pass
             kname = tgemm::f32_kernel_name(pp.f32_id);
             if (pp.fplan.split > 1)
                 snprintf(tail, sizeof(tail), "+splitk_reduce(split=%d,tiles=%d)", pp.fplan.split,
@@ -870,7 +888,7 @@ int gemm_set_f32_kernel(int id) {
 }
 
 int gemm_set_tc_kernel(int mode) {
-    if (mode < -1 || mode > 2) return TGEMM_ERR_INVALID_ARG;
+    if (mode < -1 || mode > 3) return TGEMM_ERR_INVALID_ARG;
     g_tc_mode.store(mode);
     return TGEMM_OK;
 }

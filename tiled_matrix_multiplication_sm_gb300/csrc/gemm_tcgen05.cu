@@ -466,14 +466,14 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 
 // Instruction descriptor: FP32 accumulator, A K-major, B K-major or
 // MN-major, M x N.
-template <int ESZ, bool B_KMAJOR, int MMA_M = BM>
+template <int ESZ, bool B_KMAJOR, int MMA_M = BM, int MMA_N = BN>
 __host__ __device__ constexpr uint32_t instr_desc() {
     return (1u << 4)                         // D format F32
          | (Kind<ESZ>::FMT << 7)             // A format
          | (Kind<ESZ>::FMT << 10)            // B format
          | (0u << 15)                        // A: K-major
          | ((B_KMAJOR ? 0u : 1u) << 16)      // B: K-major (0) or MN-major (1)
-         | ((uint32_t)(BN >> 3) << 17)
+         | ((uint32_t)(MMA_N >> 3) << 17)
          | ((uint32_t)(MMA_M >> 4) << 24);
 }
 
@@ -1132,6 +1132,255 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 }
 
 // ===================================================================
+// TF32 with few rows (one SM, M <= 128) and B as the caller stores it
+// (K x N, N contiguous). The TF32 kind reads B only K-major, and for such
+// products a transpose pre-pass would move B through HBM three times (read,
+// write, read) while the product itself is bound by reading B once. Here B
+// is transposed inside the kernel instead: TMA lands each stage's 32 x 128
+// block of B in the stage's own B slot in the MN-major layout it has in
+// memory (boxes of 32 columns x 32 K rows, 128-byte swizzle) next to the
+// stage's A block; both land on the stage's `landed` barrier. Two transposer
+// warps then read the B block into registers (4 bytes a lane, one 128-byte
+// row per warp instruction: no bank conflicts), meet at a named barrier, and
+// write it back in place in the K-major 128-byte-swizzled layout (one
+// 16-byte chunk a lane, eight rows per quarter-warp: no bank conflicts),
+// fence the writes into the async proxy and arrive on the stage's `full`
+// barrier, which the MMA issuer waits on. Tiles are 128 x 128 (a 32 x 128
+// TF32 block is 16 KB: 64 floats a transposer thread), six stages of 32 KB;
+// the rest -- MMA issue, two accumulators, epilogue, stream-K tail -- is the
+// one-SM kernel's.
+constexpr int TT_BN = 128;                         // tile columns
+constexpr int TT_STAGES = 6;
+constexpr int TT_B_STAGE = 32 * TT_BN * 4;         // 32 K rows x 128 columns, fp32: 16 KB
+constexpr int TT_STAGE = A_STAGE_BYTES + TT_B_STAGE;
+constexpr int TT_TMEM_COLS = 2 * TT_BN;            // two accumulators
+constexpr int TT_THREADS = NUM_THREADS + 64;       // + two transposer warps
+struct SyncT {
+    uint64_t full[TT_STAGES];                      // B transposed (both transposer warps)
+    uint64_t landed[TT_STAGES];                    // A and B (MN-major) landed
+    uint64_t empty[TT_STAGES];
+    uint64_t tmem_full[2];
+    uint64_t tmem_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+constexpr int TT_SMEM_BYTES = 1024 + TT_STAGES * TT_STAGE + EPI_STAGE_BYTES + (int)sizeof(SyncT);
+static_assert(TT_SMEM_BYTES <= 227 * 1024, "TF32 transposing kernel exceeds the shared memory of a block");
+
+// True on every thread of the two transposer warps (named barrier 1, 64
+// threads) if `pred` holds on any of them.
+__device__ __forceinline__ bool transposers_any(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, 64, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r) : "r"((uint32_t)pred) : "memory");
+    return r != 0;
+}
+
+__global__ void __launch_bounds__(TT_THREADS, 1)
+tc_gemm_tf32t_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmC,
+                     const TcParams p) {
+    constexpr int BK = Kind<4>::BK;                // 32
+    constexpr int K_STEPS = BK / Kind<4>::UMMA_K;  // 4
+    constexpr uint32_t K_STEP = Kind<4>::UMMA_K * 4;
+    constexpr uint32_t IDESC = instr_desc<4, true, BM, TT_BN>();
+    constexpr int B_BOXES = TT_BN / 32;            // MN-major boxes of 32 columns
+    constexpr int B_BOX_BYTES = BK * SW;           // 32 K rows x 128 bytes
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
+    float* epi_stage = reinterpret_cast<float*>(smem + TT_STAGES * TT_STAGE);
+    SyncT* sy = reinterpret_cast<SyncT*>(smem + TT_STAGES * TT_STAGE + EPI_STAGE_BYTES);
+    const uint32_t a_base = smem_u32(smem);
+    const uint32_t b_base = a_base + TT_STAGES * A_STAGE_BYTES;
+    float* b_gen = reinterpret_cast<float*>(smem + TT_STAGES * A_STAGE_BYTES);   // generic view
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < TT_STAGES; ++s) {
+            mbar_init(smem_u32(&sy->full[s]), 2);            // the transposer warps
+            mbar_init(smem_u32(&sy->landed[s]), 1);          // producer, with the TMA bytes
+            mbar_init(smem_u32(&sy->empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&sy->tmem_full[a]), 1);
+            mbar_init(smem_u32(&sy->tmem_empty[a]), 4);
+        }
+        mbar_init(smem_u32(&sy->drain), 1);
+        sy->abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(smem_u32(&sy->tmem_base)), "n"(TT_TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = sy->tmem_base;
+    const unsigned long long lim = p.wait_limit_ns;
+    const int nu = slot_unit_count(p, blockIdx.x);
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t armed = 0, armed_parity = 0;
+            int g = 0;
+            for (int i = 0; i < nu; ++i) {
+                const Unit w = slot_unit(p, blockIdx.x, i);
+                int mb, nb;
+                tile_coords(w.tile, p, mb, nb);
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++g) {
+                    const int s = g % TT_STAGES;
+                    const uint32_t ph = (uint32_t)(g / TT_STAGES) & 1u;
+                    if (!mbar_wait(smem_u32(&sy->empty[s]), ph ^ 1u, &sy->abort, lim, true)) goto tt_producer_done;
+                    if (p.debug_stall && g == 0) continue;     // test hook: never fill stage 0
+                    const uint32_t landed = smem_u32(&sy->landed[s]);
+                    mbar_arrive_expect_tx(landed, TT_STAGE);
+                    tma_load_2d(a_base + s * A_STAGE_BYTES, &tmA, kb * BK, mb * BM, landed);
+#pragma unroll
+                    for (int c = 0; c < B_BOXES; ++c)
+                        tma_load_2d(b_base + s * TT_B_STAGE + c * B_BOX_BYTES, &tmB,
+                                    nb * TT_BN + c * 32, kb * BK, landed);
+                    armed |= 1u << s;
+                    armed_parity = (armed_parity & ~(1u << s)) | (ph << s);
+                }
+            }
+        tt_producer_done:
+            // Copies still in flight must land before the block may exit.
+            for (int s = 0; s < TT_STAGES; ++s)
+                if (armed & (1u << s))
+                    mbar_wait(smem_u32(&sy->landed[s]), (armed_parity >> s) & 1u, &sy->abort, lim, false);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int g = 0;
+            for (int it = 0; it < nu; ++it) {
+                const Unit w = slot_unit(p, blockIdx.x, it);
+                const int acc = it & 1;
+                const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+                if (!mbar_wait(smem_u32(&sy->tmem_empty[acc]), aph ^ 1u, &sy->abort, lim, true)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * TT_BN);
+                bool ok = true;
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++g) {
+                    const int s = g % TT_STAGES;
+                    const uint32_t ph = (uint32_t)(g / TT_STAGES) & 1u;
+                    if (!mbar_wait(smem_u32(&sy->full[s]), ph, &sy->abort, lim, true)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_addr = a_base + s * A_STAGE_BYTES;
+                    const uint32_t b_addr = b_base + s * TT_B_STAGE;
+#pragma unroll
+                    for (int kk = 0; kk < K_STEPS; ++kk)
+                        tc_mma<4>(d_tmem, smem_desc(a_addr + kk * K_STEP, 16, 1024),
+                                  smem_desc(b_addr + kk * K_STEP, 16, 1024), IDESC,
+                                  (kb != w.kb0 || kk != 0) ? 1u : 0u);
+                    tc_commit(smem_u32(&sy->empty[s]));
+                }
+                if (!ok) break;
+                tc_commit(smem_u32(&sy->tmem_full[acc]));
+            }
+            tc_commit(smem_u32(&sy->drain));
+            mbar_wait(smem_u32(&sy->drain), 0, &sy->abort, lim, false);
+        }
+        __syncwarp();
+    } else if (warp >= 6) {
+        // ------------------------------------------------ B transposers (warps 6-7)
+        // Thread t owns columns n = t and t + 64 of the tile (all 32 K rows).
+        const int t = threadIdx.x - 6 * 32;
+        int g = 0;
+        for (int i = 0; i < nu; ++i) {
+            const Unit w = slot_unit(p, blockIdx.x, i);
+            for (int kb = w.kb0; kb < w.kb1; ++kb, ++g) {
+                const int s = g % TT_STAGES;
+                const uint32_t ph = (uint32_t)(g / TT_STAGES) & 1u;
+                int ok = 1;
+                if (lane == 0) ok = mbar_wait(smem_u32(&sy->landed[s]), ph, &sy->abort, lim, true) ? 1 : 0;
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                // Both warps leave together (they meet at named barriers): a
+                // reduction over the 64 threads decides.
+                if (transposers_any(!ok || *(volatile int*)&sy->abort)) goto tt_transpose_done;
+                float* bs = b_gen + s * (TT_B_STAGE / 4);
+                float v[2][32];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int n = t + 64 * h;
+                    // MN-major: box n / 32, row k, 16-byte chunk ((n % 32) / 4) ^ (k % 8).
+                    const float* box = bs + (n >> 5) * (B_BOX_BYTES / 4) + (n & 3);
+                    const int cn = (n & 31) >> 2;
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) v[h][k] = box[k * 32 + ((cn ^ (k & 7)) << 2)];
+                }
+                asm volatile("bar.sync 1, 64;" ::: "memory");       // every read done
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int n = t + 64 * h;
+                    // K-major: row n (128 bytes), 16-byte chunk c at c ^ (n % 8).
+                    float4* row = reinterpret_cast<float4*>(bs + n * 32);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        row[c ^ (n & 7)] = make_float4(v[h][4 * c], v[h][4 * c + 1], v[h][4 * c + 2],
+                                                      v[h][4 * c + 3]);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sy->full[s]));
+            }
+        }
+    tt_transpose_done:;
+    } else {
+        // ------------------------------------------------ epilogue (warps 2-5)
+        const int q = warp & 3;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        for (int it = 0; it < nu; ++it) {
+            const Unit w = slot_unit(p, blockIdx.x, it);
+            int mb, nb;
+            tile_coords(w.tile, p, mb, nb);
+            const int acc = it & 1;
+            const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+            bool ok = mbar_wait(smem_u32(&sy->tmem_full[acc]), aph, &sy->abort, lim, true);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            unsigned* flag = (w.fix_wait > 0 || w.piece >= 0) ? p.sk_flags + (w.tile - p.dp_tiles)
+                                                              : nullptr;
+            if (w.fix_wait > 0 &&
+                !sk_wait(flag, (unsigned)(w.fix_wait * p.sk_arrivals), &sy->abort, lim))
+                break;
+            tc_fence_after();
+            store_accumulator<true>(p, w, mb, nb, q * 32 + lane,
+                                    tmem_base + lane_off + (uint32_t)(acc * TT_BN),
+                                    epi_stage + q * (EPI_REGION / 4), &tmC, 0, TT_BN / 32);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 31) mbar_arrive(smem_u32(&sy->tmem_empty[acc]));
+            if (w.piece >= 0) sk_arrive(flag);
+        }
+        tma_store_wait_all();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                     :: "r"(tmem_base), "n"(TT_TMEM_COLS) : "memory");
+    }
+}
+
+// ===================================================================
 // 2-SM variant: a cluster of two CTAs on a pair of SMs computes a 256 x 256
 // tile with tcgen05.mma.cta_group::2 (M = 256, N = 256). CTA r of the pair
 // stages rows 128r..128r+127 of the A tile and columns 128r..128r+127 of the
@@ -1651,6 +1900,26 @@ cudaError_t launch_tc(const GemmArgs& a, const TcPlan& pl, void* scratch, Encode
     return cudaGetLastError();
 }
 
+// The TF32 kernel that transposes B in shared memory: one CTA per SM,
+// persistent over 128 x 128 tiles; B is K x N with 16-byte rows, read by TMA
+// in boxes of 32 columns x 32 K rows.
+cudaError_t launch_tc_t(const GemmArgs& a, const TcPlan& pl, void* scratch, EncodeTiledFn enc,
+                        unsigned long long wait_limit_ns, int debug_stall, cudaStream_t s) {
+    constexpr int BK = Kind<4>::BK;
+    CUtensorMap tmA, tmB, tmC;
+    if (!encode_2d(enc, &tmA, a.A, 4, a.M, a.K, a.lda, BK, BM) ||
+        !encode_2d(enc, &tmB, a.B, 4, a.K, a.N, a.ldb, SW / 4, BK))
+        return cudaErrorInvalidValue;
+    TcParams p = make_params(a, pl, scratch, 4, wait_limit_ns, debug_stall);
+    encode_c(enc, &tmC, a, p);
+    p.row_copy = (!p.tma_c && a.ep.beta == 0.0f) ? 1 : 0;
+    if (!prepare_stream_k(p, s)) return cudaErrorInvalidValue;
+    cudaError_t e = set_smem_limit_once<tc_gemm_tf32t_kernel>(TT_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    tc_gemm_tf32t_kernel<<<grid_slots(pl), TT_THREADS, TT_SMEM_BYTES, s>>>(tmA, tmB, tmC, p);
+    return cudaGetLastError();
+}
+
 // The 2-SM kernel: clusters of two CTAs, one CTA per SM, persistent over
 // 256 x 256 tiles (NW = 1) or 256 x 512 tiles (NW = 2).
 template <int ESZ, bool B_KMAJOR, bool X3 = false, int NW = 1, bool A_LOADER = false>
@@ -1831,7 +2100,8 @@ struct TileModel {
 };
 
 TileModel tile_model(int in_type, int shape, int tile_rows, int tile_cols, int K, bool tma_c) {
-    double tflops = shape == TC_ONE_SM ? 9.3 : shape == TC_PAIR ? 22.8 : 30.0;   // BF16
+    double tflops = (shape == TC_ONE_SM || shape == TC_ONE_SM_T) ? 9.3
+                  : shape == TC_PAIR ? 22.8 : 30.0;                            // BF16
     if (in_type != TC_BF16) tflops *= 0.5;                                      // TF32 rate
     if (in_type == TC_TF32X3) tflops /= 3.0;                                    // three products
     TileModel m;
@@ -1861,10 +2131,10 @@ size_t tc_partial_bytes(const TcPlan& pl) {
 TcPlan tc_plan(int M, int N, int K, int in_type, int shape, int num_sms, int streamk,
                bool tma_c) {
     if (in_type == TC_TF32X3) shape = TC_PAIR;   // the split form: 256 x 256 CTA-pair tiles only
-    const bool pair = shape != TC_ONE_SM;
+    const bool pair = shape == TC_PAIR || shape == TC_PAIR_WIDE;
     TcPlan pl;
     pl.tile_rows = pair ? P_BM : BM;
-    pl.tile_cols = shape == TC_PAIR_WIDE ? 2 * BN : BN;
+    pl.tile_cols = shape == TC_PAIR_WIDE ? 2 * BN : shape == TC_ONE_SM_T ? TT_BN : BN;
     pl.tiles_m = (M + pl.tile_rows - 1) / pl.tile_rows;
     pl.tiles_n = (N + pl.tile_cols - 1) / pl.tile_cols;
     const int bk = in_type == TC_BF16 ? Kind<2>::BK : Kind<4>::BK;
@@ -1932,7 +2202,7 @@ int tc_shape(int M, int N, int K, int in_type, int mode, int num_sms, int stream
     if (mode == 0) return TC_ONE_SM;
     if (mode == 1) return TC_PAIR;
     if (mode == 2) return TC_PAIR_WIDE;
-    if (M <= BM) return TC_ONE_SM;        // a pair tile is 256 rows tall
+    if (M <= BM) return TC_ONE_SM;        // a pair tile is 256 rows tall (mode 3: as -1)
     if (N <= BN) return TC_PAIR;
     // The shape the timing model expects to finish first; near-ties go to
     // the narrow tiles, whose epilogue is hidden.
@@ -1942,6 +2212,7 @@ int tc_shape(int M, int N, int K, int in_type, int mode, int num_sms, int stream
 }
 
 const char* tc_kernel_name(int in_type, int shape) {
+    if (shape == TC_ONE_SM_T && in_type == TC_TF32) return "tc_tf32_128x128x32_s6_btrans_persistent";
     const int sh = shape < 0 ? 0 : shape > 2 ? 2 : shape;
     return kNames[in_type == TC_BF16 ? 1 : in_type == TC_TF32X3 ? 2 : 0][sh];
 }
@@ -1956,6 +2227,12 @@ cudaError_t tc_launch(const GemmArgs& a, int in_type, int b_kmajor, void* encode
     if (in_type == TC_TF32X3)       // always the CTA-pair kernel, B K-major
         return a.a_loader ? cudaErrorInvalidValue
                           : launch_tc_pair<4, true, true>(a, pl, scratch, enc, w, st, s);
+    if (shape == TC_ONE_SM_T) {
+        if (in_type != TC_TF32 || b_kmajor || a.a_loader || pl.tile_cols != TT_BN)
+            return cudaErrorInvalidValue;
+        return launch_tc_t(a, pl, scratch, enc, w, st, s);
+    }
+    if (pl.tile_cols == TT_BN && pl.tile_rows == BM) return cudaErrorInvalidValue;
     if ((shape == TC_PAIR_WIDE) != (pl.tile_cols == 2 * BN)) return cudaErrorInvalidValue;
     if (a.a_loader) {
         // A read by the loader warps: TF32 (B K-major) and BF16 with B MN-major.

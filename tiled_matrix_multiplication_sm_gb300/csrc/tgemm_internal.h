@@ -59,27 +59,35 @@ bool f32_kernel_accepts(int id, const GemmArgs& a);
 // Pick a configuration for this shape and alignment.
 int  f32_select(const GemmArgs& a, int num_sms);
 // How configuration `id` covers this problem: tiles computed whole, and the
-// tiles of a partial last wave split into K-pieces whose partial tiles need
-// `scratch_bytes` of device scratch (0 when nothing is split).
+// tiles of a partial last wave split into K-pieces whose partial tiles take
+// part_bytes of device scratch (0 when nothing is split); configurations
+// that read A from its duplicated K x 2M copy (a2_ld floats a row) keep it
+// in the a2_bytes after them. scratch_bytes = the sum (0: no scratch).
 struct F32Plan {
     int tiles_m, tiles_n, ktiles;
     int dp_tiles, split;
+    size_t part_bytes, a2_bytes;
+    long a2_ld;
     size_t scratch_bytes;
 };
 F32Plan f32_plan(int id, const GemmArgs& a, int num_sms);
-// Launch configuration `id` under plan `pl` (plus the split-K reduction when
-// the plan splits); `scratch` holds pl.scratch_bytes. Returns a cudaError_t.
+// Launch configuration `id` under plan `pl` (after the duplicated-A pre-pass
+// and before the split-K reduction, where the plan has them); `scratch`
+// holds pl.scratch_bytes. Returns a cudaError_t.
 cudaError_t f32_launch(int id, const GemmArgs& a, const F32Plan& pl, float* scratch,
                        cudaStream_t s);
 
 // ---- tcgen05 tensor-core path (gemm_tcgen05.cu) -------------------------
 enum TcType { TC_TF32 = 1, TC_BF16 = 2, TC_TF32X3 = 3 };
 // Tile shapes of the tensor-core kernels: 128 x 256 on one SM, 256 x 256 on
-// an SM pair, 256 x 512 on an SM pair (two N = 256 MMAs per K step).
-enum TcShape { TC_ONE_SM = 0, TC_PAIR = 1, TC_PAIR_WIDE = 2 };
+// an SM pair, 256 x 512 on an SM pair (two N = 256 MMAs per K step), and
+// 128 x 128 on one SM for TF32 with B read as stored (K x N) and transposed
+// in shared memory by the kernel (TC_ONE_SM_T).
+enum TcShape { TC_ONE_SM = 0, TC_PAIR = 1, TC_PAIR_WIDE = 2, TC_ONE_SM_T = 3 };
 // The shape a product runs with: mode -1 = the shape a timing model expects
 // to finish first, 0/1/2 = that TcShape (the split-TF32 form always takes
-// TC_PAIR). streamk and tma_c as for tc_plan.
+// TC_PAIR); mode 3 is taken as -1 (the caller picks TC_ONE_SM_T, which
+// depends on how B is stored). streamk and tma_c as for tc_plan.
 int tc_shape(int M, int N, int K, int in_type, int mode, int num_sms, int streamk,
              bool tma_c = true);
 const char* tc_kernel_name(int in_type, int shape);
@@ -108,6 +116,8 @@ TcPlan tc_plan(int M, int N, int K, int in_type, int shape, int num_sms, int str
 // (made for the same shape); `scratch` holds pl.scratch_bytes (it may be
 // null when that is 0). `encode_fn` is cuTensorMapEncodeTiled. With
 // b_kmajor, a.B / a.ldb describe B transposed (N x K, K contiguous).
+// TC_ONE_SM_T takes TC_TF32 with b_kmajor = 0 (B K x N, rows 16-byte
+// aligned) and A read by TMA only.
 cudaError_t tc_launch(const GemmArgs& a, int in_type, int b_kmajor, void* encode_fn,
                       unsigned long long wait_limit_ns, int debug_stall, int shape,
                       const TcPlan& pl, void* scratch, cudaStream_t s);
@@ -145,6 +155,10 @@ cudaError_t transpose_split_tf32(const float* B, long ldb, float* hi_t, float* l
 // Bt[n][k] = B[k][n] for a K x N matrix B (ldb) into Bt (N x K, ldt >= K).
 cudaError_t transpose_f32(const float* B, long ldb, float* Bt, long ldt, int K, int N,
                           cudaStream_t s);
+// A2[k][2m] = A2[k][2m + 1] = A[m][k] for an M x K matrix A (lda), k < K,
+// m < mpad (zeros for M <= m < mpad); A2 has rows of ld2 >= 2 mpad floats.
+cudaError_t dup_transpose_f32(const float* A, long lda, float* A2, long ld2, int M, int K,
+                              int mpad, cudaStream_t s);
 // The same for 2-byte elements (bf16 bit patterns).
 cudaError_t transpose_u16(const void* B, long ldb, void* Bt, long ldt, int K, int N,
                           cudaStream_t s);
