@@ -497,7 +497,6 @@ int run_product(const Request& r, cudaStream_t stream) {
     if (rc == TGEMM_OK) {
         if (f32) {
             ok(tgemm::f32_launch(pp.f32_id, a, pp.fplan, partials, stream));
-            if (pp.fplan.a2_bytes > 0) note("dup_a+");     // the duplicated-A pre-pass
             kname = tgemm::f32_kernel_name(pp.f32_id);
             if (pp.fplan.split > 1)
                 snprintf(tail, sizeof(tail), "+splitk_reduce(split=%d,tiles=%d)", pp.fplan.split,

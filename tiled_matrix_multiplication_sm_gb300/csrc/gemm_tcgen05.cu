@@ -2099,13 +2099,23 @@ struct TileModel {
     double main_us, epi_us;
 };
 
-TileModel tile_model(int in_type, int shape, int tile_rows, int tile_cols, int K, bool tma_c) {
+// b_stream: one row of tiles (M <= tile rows), so every tile streams its
+// panel of B from memory exactly once; the main loop then takes at least
+// the panel's bytes at one SM's share of the rate measured for such reads
+// (about 3.3 TB/s over 152 SMs on 16 x 14336 x 4096, TF32 and BF16).
+TileModel tile_model(int in_type, int shape, int tile_rows, int tile_cols, int K, bool tma_c,
+                     bool b_stream) {
     double tflops = (shape == TC_ONE_SM || shape == TC_ONE_SM_T) ? 9.3
                   : shape == TC_PAIR ? 22.8 : 30.0;                            // BF16
     if (in_type != TC_BF16) tflops *= 0.5;                                      // TF32 rate
     if (in_type == TC_TF32X3) tflops /= 3.0;                                    // three products
     TileModel m;
     m.main_us = 2.0 * tile_rows * tile_cols * (double)K / (tflops * 1e6);
+    if (b_stream) {
+        const double b_bytes = (double)tile_cols * K * (in_type == TC_BF16 ? 2 : 4);
+        const double sm_bytes_per_us = 3.3e6 / 152;
+        if (b_bytes / sm_bytes_per_us > m.main_us) m.main_us = b_bytes / sm_bytes_per_us;
+    }
     // The wide tiles' single accumulator leaves part of each epilogue exposed:
     // ~6.5 us with TMA stores, more with per-thread stores when C's rows are
     // not 16-byte aligned (8192 x 14336 x 4096 BF16 with ldc = 14337: wide
@@ -2147,7 +2157,8 @@ TcPlan tc_plan(int M, int N, int K, int in_type, int shape, int num_sms, int str
     pl.scratch_bytes = 0;
     pl.est_us = 0.0;
     if (slots <= 0 || tiles == 0) return pl;
-    const TileModel tm = tile_model(in_type, shape, pl.tile_rows, pl.tile_cols, K, tma_c);
+    const TileModel tm = tile_model(in_type, shape, pl.tile_rows, pl.tile_cols, K, tma_c,
+                                    pl.tiles_m == 1);
     const double tile_us = tm.main_us + tm.epi_us;
     pl.est_us = (double)((tiles + slots - 1) / slots) * tile_us;
     const int rem = tiles % slots;

@@ -75,44 +75,30 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 // ------------------------------------------------------------ configuration
-// DUPA_: A is read from a copy laid out K x 2M with every value twice
-// (row k holds A[0][k], A[0][k], A[1][k], A[1][k], ...), written by a
-// pre-pass: one 16-byte shared-memory read then yields the (a, a) operand
-// pairs of two rows for the two-wide FMA, with no register moves to build
-// them, and a thread's fragments of the next k fit in registers beside the
-// current ones.
 template <int BM_, int BN_, int BK_, int WM_, int WN_, int STAGES_, int MIN_BLOCKS_, bool PACKED_,
-          bool DUPA_ = false>
+          int KU_ = 0>
 struct Tile {
     static constexpr int BM = BM_, BN = BN_, BK = BK_;
+    // Unrolling of a phase's loop over groups of 4 k (0: fully unrolled).
+    static constexpr int KU = KU_ > 0 ? KU_ : BK_ / 4;
     static constexpr int WM = WM_, WN = WN_;
     static constexpr int STAGES = STAGES_;
     static constexpr int MIN_BLOCKS = MIN_BLOCKS_;
     static constexpr bool PACKED = PACKED_;
-    static constexpr bool DUPA = DUPA_;
     static constexpr int WARPS_M = BM / WM, WARPS_N = BN / WN;
     static constexpr int THREADS = 32 * WARPS_M * WARPS_N;
     // A warp is 4 rows x 8 columns of threads.
-    static constexpr int TM = WM / 4;         // rows per thread
+    static constexpr int TM = WM / 4;         // rows per thread (stride 4)
     static constexpr int TN = WN / 8;         // columns per thread
     static constexpr int NG = TN / 4;         // 4-wide column groups (stride 32)
-    // A tile: BM rows of BK (+4 pad) floats, or (DUPA) BK rows of 2 BM.
-    static constexpr int ALD = DUPA ? 2 * BM : BK + 4;
+    static constexpr int ALD = BK + 4;        // padded row of the A tile (floats)
     static constexpr int BLD = BN;            // row of the B tile (floats)
-    static constexpr int A_STAGE = DUPA ? BK * ALD : BM * ALD;  // floats
+    static constexpr int A_STAGE = BM * ALD;  // floats
     static constexpr int B_STAGE = BK * BLD;
     static constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) * 4;
-    // Row (within the warp tile) of a thread's i-th accumulator row: rows
-    // 4 apart, or (DUPA) pairs of adjacent rows 8 apart, so that the four
-    // thread rows of a warp read four adjacent 16-byte chunks.
-    __host__ __device__ static constexpr int row_of(int ty, int i) {
-        return DUPA ? 8 * (i / 2) + 2 * ty + (i % 2) : ty + 4 * i;
-    }
-    static_assert(!DUPA || (PACKED && TM % 2 == 0), "the duplicated-A form is packed, rows in pairs");
     static_assert(WM % 4 == 0 && WN % 32 == 0 && TN % 4 == 0, "warp tile shape");
     static_assert(BK % 4 == 0, "BK must be a multiple of 4");
-    static_assert((BM * BK / 4) % THREADS == 0 && (BK * BN / 4) % THREADS == 0 &&
-                  (!DUPA || (2 * BM * BK / 4) % THREADS == 0),
+    static_assert((BM * BK / 4) % THREADS == 0 && (BK * BN / 4) % THREADS == 0,
                   "vector loads must divide evenly over the threads");
     static_assert((BM * BK) % THREADS == 0 && (BK * BN) % THREADS == 0,
                   "scalar loads must divide evenly over the threads");
@@ -160,26 +146,11 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
     tn = (t % per_group) / gm;
 }
 
-// Copy the A tile (rows m0.., columns k0..) into shared memory. DUPA: A is
-// the duplicated K x 2M copy (lda its row pitch, covering every tile row:
-// the pre-pass wrote zeros past M) and the tile is its rows k0.. over
-// columns 2 m0 .. 2 (m0 + BM).
+// Copy the A tile (rows m0.., columns k0..) into shared memory.
 template <class T, bool VEC>
 __device__ __forceinline__ void load_a(float* As, const float* __restrict__ A, long lda,
                                        int M, int K, int m0, int k0, int tid) {
-    if constexpr (T::DUPA) {
-        constexpr int CPR = 2 * T::BM / 4;
-        constexpr int ITERS = T::BK * CPR / T::THREADS;
-#pragma unroll
-        for (int it = 0; it < ITERS; ++it) {
-            const int c = tid + it * T::THREADS;
-            const int k = c / CPR, mc = (c % CPR) * 4;
-            const int gk = k0 + k;
-            const int bytes = gk < K ? 16 : 0;
-            const float* src = bytes ? A + (long)gk * lda + 2L * m0 + mc : A;
-            cp_async_16(smem_u32(As + k * T::ALD + mc), src, bytes);
-        }
-    } else if constexpr (VEC) {
+    if constexpr (VEC) {
         constexpr int CPR = T::BK / 4;                 // 16-byte chunks per row
         constexpr int ITERS = T::BM * CPR / T::THREADS;
 #pragma unroll
@@ -256,42 +227,9 @@ struct Acc {
 };
 
 // One BK-deep phase of outer products from shared memory.
-// DUPA: `as` points at the thread's first row pair of k = 0 in the
-// duplicated tile; float4 p of row k holds (a, a, a', a') of rows
-// row_of(ty, 2p) and row_of(ty, 2p + 1).
-template <class T>
-__device__ __forceinline__ void mma_phase_dup(Acc<T>& acc, const float* as, const float* bs) {
-#pragma unroll
-    for (int k = 0; k < T::BK; ++k) {
-        float4 a[T::TM / 2];
-#pragma unroll
-        for (int q = 0; q < T::TM / 2; ++q)
-            a[q] = *reinterpret_cast<const float4*>(as + k * T::ALD + 16 * q);
-        float4 b[T::NG];
-#pragma unroll
-        for (int g = 0; g < T::NG; ++g)
-            b[g] = *reinterpret_cast<const float4*>(bs + k * T::BLD + g * 32);
-#pragma unroll
-        for (int h = 0; h < T::TN / 2; ++h) {
-            const float4& bg = b[h / 2];
-            const float2 bp = (h % 2) ? make_float2(bg.z, bg.w) : make_float2(bg.x, bg.y);
-#pragma unroll
-            for (int q = 0; q < T::TM / 2; ++q) {
-                acc.v[2 * q][h] = __ffma2_rn(make_float2(a[q].x, a[q].y), bp, acc.v[2 * q][h]);
-                acc.v[2 * q + 1][h] =
-                    __ffma2_rn(make_float2(a[q].z, a[q].w), bp, acc.v[2 * q + 1][h]);
-            }
-        }
-    }
-}
-
 template <class T>
 __device__ __forceinline__ void mma_phase(Acc<T>& acc, const float* as, const float* bs) {
-    if constexpr (T::DUPA) {
-        mma_phase_dup<T>(acc, as, bs);
-        return;
-    }
-#pragma unroll
+#pragma unroll (T::KU)
     for (int k4 = 0; k4 < T::BK; k4 += 4) {
         float4 a[T::TM];
 #pragma unroll
@@ -409,8 +347,8 @@ sgemm_kernel(const F32Params p) {
         cp_async_commit();
 
         const int st = kt % T::STAGES;
-        const int a_off = T::DUPA ? 2 * wm0 + 4 * ty : (wm0 + ty) * T::ALD;
-        mma_phase<T>(acc, As + st * T::A_STAGE + a_off, Bs + st * T::B_STAGE + wn0 + tx * 4);
+        mma_phase<T>(acc, As + st * T::A_STAGE + (wm0 + ty) * T::ALD,
+                     Bs + st * T::B_STAGE + wn0 + tx * 4);
     }
     cp_async_wait<0>();
 
@@ -419,7 +357,7 @@ sgemm_kernel(const F32Params p) {
         // 16-byte stores where C allows them, skipped past M and N.
 #pragma unroll
         for (int i = 0; i < T::TM; ++i) {
-            const int row = m0 + wm0 + T::row_of(ty, i);
+            const int row = m0 + wm0 + ty + 4 * i;
             if (row >= M) continue;
             float* crow = p.C + (long)row * p.ldc;
 #pragma unroll
@@ -451,7 +389,7 @@ sgemm_kernel(const F32Params p) {
         float* part = p.partials + piece * (long)(T::BM * T::BN);
 #pragma unroll
         for (int i = 0; i < T::TM; ++i) {
-            float* prow = part + (long)(wm0 + T::row_of(ty, i)) * T::BN;
+            float* prow = part + (long)(wm0 + ty + 4 * i) * T::BN;
 #pragma unroll
             for (int g = 0; g < T::NG; ++g)
                 *reinterpret_cast<float4*>(prow + wn0 + g * 32 + tx * 4) =
@@ -536,14 +474,14 @@ using Small = Tile<64, 64, 16, 32, 32, 4, 4, false>;     // 128 threads, 8 x 4 p
 // that few FMAs are spent on rows past M, two blocks of 128 threads per SM.
 using Skinny32 = Tile<32, 256, 32, 32, 64, 3, 2, true>;   // 8 x 8 outputs per thread
 using Skinny16 = Tile<16, 256, 32, 16, 64, 3, 2, true>;   // 4 x 8 outputs per thread
-// The default tile reading A from its duplicated K x 2M copy.
-using Wide32D = Tile<128, 256, 32, 32, 128, 3, 1, true, true>;
+using Wide32U1 = Tile<128, 256, 32, 32, 128, 3, 1, true, 1>;
+using Wide32U2 = Tile<128, 256, 32, 32, 128, 3, 1, true, 2>;
+using Wide32U4 = Tile<128, 256, 32, 32, 128, 3, 1, true, 4>;
 
 struct Entry {
     const char* name;
     bool va, vb;
     int bm, bn, bk, min_blocks;
-    bool dupa;           // A read from the duplicated copy (any A alignment)
     cudaError_t (*launch)(const F32Params&, int blocks, cudaStream_t);
     cudaError_t (*reduce)(const F32Params&, cudaStream_t);
 };
@@ -568,8 +506,7 @@ cudaError_t reduce_cfg(const F32Params& p, cudaStream_t s) {
 }
 
 #define TGEMM_ENTRY(name, T, VA, VB)                                                       \
-    {name, VA, VB, T::BM, T::BN, T::BK, T::MIN_BLOCKS, T::DUPA, launch_cfg<T, VA, VB>,      \
-     reduce_cfg<T>}
+    {name, VA, VB, T::BM, T::BN, T::BK, T::MIN_BLOCKS, launch_cfg<T, VA, VB>, reduce_cfg<T>}
 
 const Entry kTable[] = {
     TGEMM_ENTRY("f32_128x256x32_s3_ffma2_vecA_vecB", Wide32P1, true, true),
@@ -585,16 +522,16 @@ const Entry kTable[] = {
     TGEMM_ENTRY("f32_64x64x16_s4_ffma_a4_b4", Small, false, false),
     TGEMM_ENTRY("f32_32x256x32_s3_ffma2_2blk_vecA_vecB", Skinny32, true, true),
     TGEMM_ENTRY("f32_16x256x32_s3_ffma2_2blk_vecA_vecB", Skinny16, true, true),
-    TGEMM_ENTRY("f32_128x256x32_s3_ffma2_dupA_vecB", Wide32D, false, true),
+    TGEMM_ENTRY("f32_128x256x32_s3_ffma2_u1_vecA_vecB", Wide32U1, true, true),
+    TGEMM_ENTRY("f32_128x256x32_s3_ffma2_u2_vecA_vecB", Wide32U2, true, true),
+    TGEMM_ENTRY("f32_128x256x32_s3_ffma2_u4_vecA_vecB", Wide32U4, true, true),
 };
 constexpr int kBig32 = 5;
 constexpr int kSmall = 9;
 constexpr int kSkinny32 = 11;
 constexpr int kSkinny16 = 12;
-constexpr int kWideDup = 13;
 constexpr int kTableSize = sizeof(kTable) / sizeof(kTable[0]);
-static_assert(kSkinny32 < kTableSize && kSkinny16 < kTableSize && kWideDup < kTableSize,
-              "named entries in the table");
+static_assert(kSkinny32 < kTableSize && kSkinny16 < kTableSize, "skinny entries in the table");
 
 bool vec_ok(const void* p, long ld) {
     return reinterpret_cast<uintptr_t>(p) % 16 == 0 && ld % 4 == 0;
@@ -696,13 +633,9 @@ F32Plan f32_plan(int id, const GemmArgs& a, int num_sms) {
     const double tile_us = 2.0 * e.bm * e.bn * (double)a.K / slot_flops_per_us;
     plan_tail_split(pl.tiles_m * pl.tiles_n, num_sms * e.min_blocks, pl.ktiles, tile_us,
                     (double)e.bm * e.bn * sizeof(float), pl.dp_tiles, pl.split);
-    pl.part_bytes = pl.split > 1
+    pl.scratch_bytes = pl.split > 1
         ? (size_t)(pl.tiles_m * pl.tiles_n - pl.dp_tiles) * pl.split * e.bm * e.bn * sizeof(float)
         : 0;
-    pl.a2_ld = e.dupa ? 2L * pl.tiles_m * e.bm : 0;
-    pl.a2_bytes = e.dupa ? ((size_t)a.K * pl.a2_ld * sizeof(float) + 255) & ~(size_t)255 : 0;
-    pl.scratch_bytes = ((pl.part_bytes + 255) & ~(size_t)255) + pl.a2_bytes;
-    if (pl.a2_bytes == 0) pl.scratch_bytes = pl.part_bytes;
     return pl;
 }
 
@@ -730,14 +663,6 @@ cudaError_t f32_launch(int id, const GemmArgs& a, const F32Plan& pl, float* scra
     p.beta = a.ep.beta;
     p.bias = a.ep.bias;
     p.ep_simple = a.ep.simple() ? 1 : 0;
-    if (e.dupa) {
-        float* a2 = scratch + ((pl.part_bytes + 255) & ~(size_t)255) / sizeof(float);
-        cudaError_t err = dup_transpose_f32(p.A, p.lda, a2, pl.a2_ld, a.M, a.K,
-                                            pl.tiles_m * e.bm, s);
-        if (err != cudaSuccess) return err;
-        p.A = a2;
-        p.lda = pl.a2_ld;
-    }
     const int tiles = pl.tiles_m * pl.tiles_n;
     const int blocks = pl.dp_tiles + (tiles - pl.dp_tiles) * (pl.split > 1 ? pl.split : 0);
     cudaError_t err = e.launch(p, blocks, s);

@@ -59,21 +59,16 @@ bool f32_kernel_accepts(int id, const GemmArgs& a);
 // Pick a configuration for this shape and alignment.
 int  f32_select(const GemmArgs& a, int num_sms);
 // How configuration `id` covers this problem: tiles computed whole, and the
-// tiles of a partial last wave split into K-pieces whose partial tiles take
-// part_bytes of device scratch (0 when nothing is split); configurations
-// that read A from its duplicated K x 2M copy (a2_ld floats a row) keep it
-// in the a2_bytes after them. scratch_bytes = the sum (0: no scratch).
+// tiles of a partial last wave split into K-pieces whose partial tiles need
+// `scratch_bytes` of device scratch (0 when nothing is split).
 struct F32Plan {
     int tiles_m, tiles_n, ktiles;
     int dp_tiles, split;
-    size_t part_bytes, a2_bytes;
-    long a2_ld;
     size_t scratch_bytes;
 };
 F32Plan f32_plan(int id, const GemmArgs& a, int num_sms);
-// Launch configuration `id` under plan `pl` (after the duplicated-A pre-pass
-// and before the split-K reduction, where the plan has them); `scratch`
-// holds pl.scratch_bytes. Returns a cudaError_t.
+// Launch configuration `id` under plan `pl` (plus the split-K reduction when
+// the plan splits); `scratch` holds pl.scratch_bytes. Returns a cudaError_t.
 cudaError_t f32_launch(int id, const GemmArgs& a, const F32Plan& pl, float* scratch,
                        cudaStream_t s);
 
@@ -155,10 +150,6 @@ cudaError_t transpose_split_tf32(const float* B, long ldb, float* hi_t, float* l
 // Bt[n][k] = B[k][n] for a K x N matrix B (ldb) into Bt (N x K, ldt >= K).
 cudaError_t transpose_f32(const float* B, long ldb, float* Bt, long ldt, int K, int N,
                           cudaStream_t s);
-// A2[k][2m] = A2[k][2m + 1] = A[m][k] for an M x K matrix A (lda), k < K,
-// m < mpad (zeros for M <= m < mpad); A2 has rows of ld2 >= 2 mpad floats.
-cudaError_t dup_transpose_f32(const float* A, long lda, float* A2, long ld2, int M, int K,
-                              int mpad, cudaStream_t s);
 // The same for 2-byte elements (bf16 bit patterns).
 cudaError_t transpose_u16(const void* B, long ldb, void* Bt, long ldt, int K, int N,
                           cudaStream_t s);

@@ -44,33 +44,6 @@ transpose_kernel(const T* __restrict__ B, long ldb, T* __restrict__ Bt, long ldt
     }
 }
 
-// Transposed copy of A with every value written twice: the operand layout
-// of the FP32 kernels that take (a, a) pairs for the two-wide FMA straight
-// from shared memory. A 64 x 64 tile of A goes through the padded
-// shared-memory tile as in transpose_kernel; each thread then writes one
-// 8-byte pair, so a warp writes 256 contiguous bytes of a row of A2.
-__global__ void __launch_bounds__(TT * TROWS)
-dup_transpose_kernel(const float* __restrict__ A, long lda, float* __restrict__ A2, long ld2,
-                     int M, int K, int mpad) {
-    __shared__ float tile[TT][TT + 1];
-    const int tx = threadIdx.x % TT, ty = threadIdx.x / TT;
-    const int m0 = blockIdx.x * TT, k0 = blockIdx.y * TT;
-#pragma unroll
-    for (int r = ty; r < TT; r += TROWS) {
-        const int m = m0 + r, k = k0 + tx;
-        tile[r][tx] = (m < M && k < K) ? A[(long)m * lda + k] : 0.0f;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int r = ty; r < TT; r += TROWS) {
-        const int k = k0 + r, m = m0 + tx;
-        if (k < K && m < mpad) {
-            const float v = tile[tx][r];
-            *reinterpret_cast<float2*>(A2 + (long)k * ld2 + 2L * m) = make_float2(v, v);
-        }
-    }
-}
-
 // Row-by-row copy of a rows x cols matrix of `esz`-byte elements from
 // leading dimension ld_src to ld_dst (both in elements). Used to give the
 // tensor-memory copies rows that start on 16-byte boundaries.
@@ -245,16 +218,6 @@ cudaError_t transpose_f32(const float* B, long ldb, float* Bt, long ldt, int K, 
     dim3 grid((N + TT - 1) / TT, (K + TT - 1) / TT);
     if (grid.y > 65535) return cudaErrorInvalidValue;
     transpose_kernel<float><<<grid, TT * TROWS, 0, s>>>(B, ldb, Bt, ldt, K, N);
-    return cudaGetLastError();
-}
-
-cudaError_t dup_transpose_f32(const float* A, long lda, float* A2, long ld2, int M, int K,
-                              int mpad, cudaStream_t s) {
-    dim3 grid((mpad + TT - 1) / TT, (K + TT - 1) / TT);
-    if (grid.y > 65535 || (reinterpret_cast<uintptr_t>(A2) % 8) != 0 || ld2 % 2 != 0 ||
-        ld2 < 2L * mpad)
-        return cudaErrorInvalidValue;
-    dup_transpose_kernel<<<grid, TT * TROWS, 0, s>>>(A, lda, A2, ld2, M, K, mpad);
     return cudaGetLastError();
 }
 

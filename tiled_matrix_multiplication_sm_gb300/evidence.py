@@ -88,7 +88,6 @@ KERNEL_SOURCES = [
     ("repack_kernel", "transpose_f32.cu"),
     ("split_rows_kernel", "transpose_f32.cu"),
     ("split_rows_vec_kernel", "transpose_f32.cu"),
-    ("dup_transpose_kernel", "transpose_f32.cu"),
 ]
 
 
@@ -178,8 +177,6 @@ def algorithmic_work(token: str, case: str) -> Dict[str, object]:
         return {"bound": "hbm", "bytes": 2 * M * K * esz}
     if token in ("repack_b", "transpose_b"):
         return {"bound": "hbm", "bytes": 2 * K * N * esz}
-    if token == "dup_a":                 # read A, write it transposed twice over
-        return {"bound": "hbm", "bytes": 12 * M * K}
     if token == "split_a":               # read fp32, write hi and lo
         return {"bound": "hbm", "bytes": 12 * M * K}
     if token == "split_b":
