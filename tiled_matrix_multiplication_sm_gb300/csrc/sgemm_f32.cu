@@ -75,12 +75,9 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 // ------------------------------------------------------------ configuration
-template <int BM_, int BN_, int BK_, int WM_, int WN_, int STAGES_, int MIN_BLOCKS_, bool PACKED_,
-          int KU_ = 0>
+template <int BM_, int BN_, int BK_, int WM_, int WN_, int STAGES_, int MIN_BLOCKS_, bool PACKED_>
 struct Tile {
     static constexpr int BM = BM_, BN = BN_, BK = BK_;
-    // Unrolling of a phase's loop over groups of 4 k (0: fully unrolled).
-    static constexpr int KU = KU_ > 0 ? KU_ : BK_ / 4;
     static constexpr int WM = WM_, WN = WN_;
     static constexpr int STAGES = STAGES_;
     static constexpr int MIN_BLOCKS = MIN_BLOCKS_;
@@ -229,7 +226,7 @@ struct Acc {
 // One BK-deep phase of outer products from shared memory.
 template <class T>
 __device__ __forceinline__ void mma_phase(Acc<T>& acc, const float* as, const float* bs) {
-#pragma unroll (T::KU)
+#pragma unroll
     for (int k4 = 0; k4 < T::BK; k4 += 4) {
         float4 a[T::TM];
 #pragma unroll
@@ -474,9 +471,6 @@ using Small = Tile<64, 64, 16, 32, 32, 4, 4, false>;     // 128 threads, 8 x 4 p
 // that few FMAs are spent on rows past M, two blocks of 128 threads per SM.
 using Skinny32 = Tile<32, 256, 32, 32, 64, 3, 2, true>;   // 8 x 8 outputs per thread
 using Skinny16 = Tile<16, 256, 32, 16, 64, 3, 2, true>;   // 4 x 8 outputs per thread
-using Wide32U1 = Tile<128, 256, 32, 32, 128, 3, 1, true, 1>;
-using Wide32U2 = Tile<128, 256, 32, 32, 128, 3, 1, true, 2>;
-using Wide32U4 = Tile<128, 256, 32, 32, 128, 3, 1, true, 4>;
 
 struct Entry {
     const char* name;
@@ -522,9 +516,6 @@ const Entry kTable[] = {
     TGEMM_ENTRY("f32_64x64x16_s4_ffma_a4_b4", Small, false, false),
     TGEMM_ENTRY("f32_32x256x32_s3_ffma2_2blk_vecA_vecB", Skinny32, true, true),
     TGEMM_ENTRY("f32_16x256x32_s3_ffma2_2blk_vecA_vecB", Skinny16, true, true),
-    TGEMM_ENTRY("f32_128x256x32_s3_ffma2_u1_vecA_vecB", Wide32U1, true, true),
-    TGEMM_ENTRY("f32_128x256x32_s3_ffma2_u2_vecA_vecB", Wide32U2, true, true),
-    TGEMM_ENTRY("f32_128x256x32_s3_ffma2_u4_vecA_vecB", Wide32U4, true, true),
 };
 constexpr int kBig32 = 5;
 constexpr int kSmall = 9;
