@@ -186,3 +186,15 @@ def test_stalled_pipeline_reports_timeout_and_recovers(tgemm):
     C = tgemm.gemm_tc(Ad, Bd, "tf32")
     assert tgemm.device_status() == 0
     assert_bit_exact(C, oracle.gemm(A, B)[0], "after timeout")
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 32, 64), (100, 96, 300), (7, 160, 33), (128, 640, 96),
+                                   (33, 4128, 200)])
+def test_whole_chunk_widths_nan_padding(tgemm, M, N, K):
+    """N a multiple of 32: each 32 x 128 block of B lands as one 3-D box of
+    32-column chunks; the chunks past N and the rows past K read as zeros,
+    and the NaN padding of ldb (past N) is never read."""
+    A, B = operands(M, N, K, "int4", seed=N + K)
+    C, name = run(tgemm, lambda: tgemm.gemm_tc(padded_cuda(A, K + 4), padded_cuda(B, N + 12), "tf32"))
+    assert KERNEL in name, name
+    assert_bit_exact(C, oracle.gemm(A, B)[0], f"{M}x{N}x{K}")

@@ -2097,6 +2097,23 @@ const char* kNames[3][3] = {
 // next tile's MMAs; the other shapes overlap it (two accumulators).
 struct TileModel {
     double main_us, epi_us;
+    // One row of tiles (b_stream): each tile streams b_bytes of B from
+    // memory once, at most sm_rate bytes/us per SM and, all SMs together, at
+    // most kStreamRate: measured 47 GB/s per SM for the one-SM kernel (B
+    // boxes of 8 KB or more), 26 GB/s for the B-transposing TF32 kernel
+    // (16 x 14336 x 4096: in-kernel timestamps), and 4.5-5.0 TB/s for TMA
+    // streams of 512-byte row segments over 112-152 SMs.
+    double b_bytes, sm_rate;
+    // Main-loop time of `frac` of a tile with n SMs streaming at once.
+    double share_us(double frac, int n) const {
+        double us = frac * main_us;
+        if (b_bytes > 0.0) {
+            const double rate = sm_rate < kStreamRate / n ? sm_rate : kStreamRate / n;
+            if (frac * b_bytes / rate > us) us = frac * b_bytes / rate;
+        }
+        return us;
+    }
+    static constexpr double kStreamRate = 4.5e6;     // bytes per us, all SMs
 };
 
 // b_stream: one row of tiles (M <= tile rows), so every tile streams its
@@ -2111,11 +2128,8 @@ TileModel tile_model(int in_type, int shape, int tile_rows, int tile_cols, int K
     if (in_type == TC_TF32X3) tflops /= 3.0;                                    // three products
     TileModel m;
     m.main_us = 2.0 * tile_rows * tile_cols * (double)K / (tflops * 1e6);
-    if (b_stream) {
-        const double b_bytes = (double)tile_cols * K * (in_type == TC_BF16 ? 2 : 4);
-        const double sm_bytes_per_us = 3.3e6 / 152;
-        if (b_bytes / sm_bytes_per_us > m.main_us) m.main_us = b_bytes / sm_bytes_per_us;
-    }
+    m.b_bytes = b_stream ? (double)tile_cols * K * (in_type == TC_BF16 ? 2 : 4) : 0.0;
+    m.sm_rate = shape == TC_ONE_SM_T ? 26e3 : 47e3;
     // The wide tiles' single accumulator leaves part of each epilogue exposed:
     // ~6.5 us with TMA stores, more with per-thread stores when C's rows are
     // not 16-byte aligned (8192 x 14336 x 4096 BF16 with ldc = 14337: wide
@@ -2159,12 +2173,13 @@ TcPlan tc_plan(int M, int N, int K, int in_type, int shape, int num_sms, int str
     if (slots <= 0 || tiles == 0) return pl;
     const TileModel tm = tile_model(in_type, shape, pl.tile_rows, pl.tile_cols, K, tma_c,
                                     pl.tiles_m == 1);
-    const double tile_us = tm.main_us + tm.epi_us;
-    pl.est_us = (double)((tiles + slots - 1) / slots) * tile_us;
+    // Whole-tile rounds: full ones over all slots, then the partial one.
     const int rem = tiles % slots;
+    const int full = tiles / slots;
+    const double tile_us = tm.share_us(1.0, slots) + tm.epi_us;
+    pl.est_us = full * tile_us + (rem > 0 ? tm.share_us(1.0, rem) + tm.epi_us : 0.0);
     if (streamk == 0 || rem == 0) return pl;
     const long long T = (long long)rem * pl.kblocks;
-    const int full = tiles / slots;
     if (streamk > 0) {
         // Forced width (tests and tuning), kept where the tail allows it: more
         // slots than tail tiles, every share at least one K block.
@@ -2182,16 +2197,20 @@ TcPlan tc_plan(int M, int N, int K, int in_type, int shape, int num_sms, int str
     // running sum on one after the other, so the tail pays one write-out per
     // extra share of a tile on top of its main loop. Measured per hand-off
     // (in-kernel timestamps): ~8 us for the 256 x 512 tiles (128 x 512 FP32
-    // per SM leaving all SMs at once), ~3-4 us for the 256 x 256 and
-    // 128 x 256 tiles.
-    const double hop_us = shape == TC_PAIR_WIDE ? 8.0 : 4.0;
+    // per SM leaving all SMs at once), ~3-4 us for the one-SM tiles; the
+    // 256 x 256 pair tiles are charged 8 as well (3000 x 5001 x 1537 TF32
+    // with the last round's 12 tiles shared by 24 pairs, one hand-off each:
+    // 120.5 us against 117.5 computed whole).
+    const double hop_us = pair ? 8.0 : 4.0;
     const double memset_us = 2.0;
     double best = pl.est_us;
     int best_s = 0;
     for (int S = rem + 1; S <= slots && (long long)S * 4 <= T; ++S) {
         const long long len = (T + S - 1) / S;                 // K blocks of the longest share
-        const double main_us = (double)len / pl.kblocks * tm.main_us;
-        const int per_tile = (S + rem - 1) / rem + 1;          // shares meeting one tile, at most
+        const double main_us = tm.share_us((double)len / pl.kblocks, S);
+        // Shares meeting one tile: exactly S / rem when the shares divide the
+        // tiles evenly, else at most one more than S / rem rounded up.
+        const int per_tile = S % rem == 0 ? S / rem : (S + rem - 1) / rem + 1;
         const double est = full * tile_us + main_us + tm.epi_us + (per_tile - 1) * hop_us + memset_us;
         if (est < best && est < 0.98 * pl.est_us) {            // a clear gain only
             best = est;
