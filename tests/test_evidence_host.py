@@ -69,6 +69,12 @@ def test_algorithmic_work_of_each_kind():
     r = w("splitk_reduce(split=8,tiles=56)", "n4096:f32")
     assert (r["split"], r["tiles"], r["bytes_per_tile_elem"]) == (8, 56, 36)
     assert evidence.tile_elems("f32_128x256x32_s3_ffma2_vecA_vecB") == 128 * 256
+    # The few-row workloads are stated against HBM: A + B read once, C written once.
+    r = w("tc_bf16_128x256x64_s4_persistent(streamk:slots=112,tiles=56)", "skinny_bf16:bf16")
+    assert r["bound"] == "hbm" and r["bytes"] == 2 * (16 * 4096 + 4096 * 14336) + 4 * 16 * 14336
+    r = w("tc_tf32_128x128x32_s6_btrans_persistent", "skinny_f32:tf32")
+    assert r["bound"] == "hbm" and r["bytes"] == 4 * (16 * 4096 + 4096 * 14336) + 4 * 16 * 14336
+    assert w("f32_16x256x32_s3_ffma2_2blk_vecA_vecB", "skinny_f32:f32")["bound"] == "hbm"
 
 
 def test_every_case_names_a_workload():

@@ -191,6 +191,12 @@ def algorithmic_work(token: str, case: str) -> Dict[str, object]:
         return {"bound": "hbm", "split": split, "tiles": tiles,
                 "tile_shape": "from the GEMM kernel's name",
                 "bytes_per_tile_elem": 4 * (split + 1)}
+    # The few-row workloads are bound by reading B once: their GEMM kernels
+    # are stated against HBM (A and B read once, C written once).
+    few_rows = case.split(":")[0] in ("skinny_bf16", "skinny_f32")
+    if few_rows and (token.startswith("f32_") or token.startswith("tc_")):
+        return {"bound": "hbm", "bytes": esz * (M * K + K * N) + 4 * M * N,
+                "flop": 2 * M * N * K}
     if token.startswith("f32_"):
         return {"bound": "alu", "flop": 2 * M * N * K}
     if token.startswith("tc_"):
