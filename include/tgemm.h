@@ -331,9 +331,12 @@ TGEMM_API int gemm_set_f32_kernel(int id);
  * 0 forces the one-SM kernel (128 x 256 tiles), 1 the 2-SM kernel (a CTA
  * pair computing 256 x 256 tiles), 2 the 2-SM kernel with 256 x 512 tiles,
  * 3 the one-SM TF32 kernel that transposes B in shared memory (128 x 128
- * tiles; TGEMM_TF32 with B stored K x N, other products as with -1);
- * -1 (default) picks by shape: for TGEMM_TF32 with B stored K x N and
- * M <= 128 the kernel of mode 3, the one-SM kernel when M <= 128, 256 x 256
+ * tiles; TGEMM_TF32 with B stored K x N, other products as with -1), 4 the
+ * one-SM kernel with 128 x 128 tiles (B read as the 128 x 256 one-SM kernel
+ * reads it); -1 (default) picks by shape: for TGEMM_TF32 with B stored
+ * K x N and M <= 128 the kernel of mode 3, else for M <= 128 the one-SM
+ * kernel with 128 x 256 or 128 x 128 tiles, whichever the timing model
+ * expects to finish first (the narrower tiles fill more SMs), 256 x 256
  * tiles when N <= 256, and otherwise the pair shape that a timing model of
  * the two expects to finish first (whole-tile rounds over the SM pairs, the
  * cost of a split last wave, a main-loop rate per shape and type measured

@@ -153,7 +153,7 @@ def test_setters_validate(lib):
     assert binding.set_f32_kernel(n) == binding.TGEMM_ERR_INVALID_ARG
     assert binding.set_f32_kernel(-2) == binding.TGEMM_ERR_INVALID_ARG
     assert binding.set_f32_kernel(-1) == binding.TGEMM_OK
-    assert binding.set_tc_kernel(4) == binding.TGEMM_ERR_INVALID_ARG
+    assert binding.set_tc_kernel(5) == binding.TGEMM_ERR_INVALID_ARG
     assert binding.set_tc_kernel(-2) == binding.TGEMM_ERR_INVALID_ARG
     assert binding.set_tc_kernel(-1) == binding.TGEMM_OK
     assert binding.set_tc_streamk(-2) == binding.TGEMM_ERR_INVALID_ARG

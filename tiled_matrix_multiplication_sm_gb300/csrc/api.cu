@@ -351,6 +351,8 @@ int plan_product(const Request& r, const DeviceInfo& dev, ProductPlan& pp) {
         const int sk = g_tc_streamk.load();
         if (pp.shape != tgemm::TC_ONE_SM_T)
             pp.shape = tgemm::tc_shape(M, N, K, path, g_tc_mode.load(), dev.num_sms, sk, tma_c);
+        // The SIMT A loader runs with the 128 x 256 one-SM tiles.
+        if (pp.a_loader && pp.shape == tgemm::TC_ONE_SM_N) pp.shape = tgemm::TC_ONE_SM;
         pp.tplan = tgemm::tc_plan(M, N, K, path, pp.shape, dev.num_sms, sk, tma_c);
     }
     pp.part_bytes = f32 ? pp.fplan.scratch_bytes : pp.tplan.scratch_bytes;
@@ -887,7 +889,7 @@ int gemm_set_f32_kernel(int id) {
 }
 
 int gemm_set_tc_kernel(int mode) {
-    if (mode < -1 || mode > 3) return TGEMM_ERR_INVALID_ARG;
+    if (mode < -1 || mode > 4) return TGEMM_ERR_INVALID_ARG;
     g_tc_mode.store(mode);
     return TGEMM_OK;
 }

@@ -82,9 +82,13 @@ template <> struct Kind<4> {           // fp32 storage, kind::tf32
     static constexpr uint32_t FMT = 2; // TF32
 };
 
+// The one-SM kernel's ring holds STAGES stages of 128 x 256 tiles (192 KB);
+// with 128 x 128 tiles the same bytes hold more, shallower stages.
+constexpr int ONE_SM_RING = STAGES * STAGE_BYTES;
+constexpr int ONE_SM_MAX_STAGES = 6;
 struct Sync {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t full[ONE_SM_MAX_STAGES];
+    uint64_t empty[ONE_SM_MAX_STAGES];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t drain;
@@ -952,7 +956,9 @@ __device__ __forceinline__ void store_accumulator(const TcParams& p, const Unit&
 // B_KMAJOR: B arrives transposed (N x K, K contiguous) and is read K-major;
 // otherwise B is K x N (N contiguous) and is read MN-major.
 // A_LOADER: A is read by the SIMT loader warps (warps 6..), not by TMA.
-template <int ESZ, bool B_KMAJOR, bool A_LOADER = false>
+// TBN: tile columns (= MMA N), 256, or 128 for products whose 128 x 256
+// tiles would leave SMs idle (the same ring bytes then hold 6 stages).
+template <int ESZ, bool B_KMAJOR, bool A_LOADER = false, int TBN = BN>
 __global__ void __launch_bounds__(NUM_THREADS + (A_LOADER ? 32 * A_LOADER_WARPS : 0), 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                const __grid_constant__ CUtensorMap tmB,
@@ -962,18 +968,25 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     constexpr int BK = KD::BK;
     constexpr int K_STEPS = BK / KD::UMMA_K;
     constexpr int B_CHUNK_COLS = SW / ESZ;               // N columns per swizzled row
-    constexpr int B_CHUNKS = BN / B_CHUNK_COLS;
+    constexpr int B_CHUNKS = TBN / B_CHUNK_COLS;
     constexpr int B_CHUNK_BYTES = BK * SW;
+    constexpr int B_STG = BK * TBN * ESZ;                // B bytes of a stage
+    constexpr int NST = ONE_SM_RING / (A_STAGE_BYTES + B_STG);
+    constexpr int STAGES = NST;                          // ring depth of this tile width
+    constexpr int TMEM_COLS = 2 * TBN;                   // two accumulators
     constexpr uint32_t A_K_STEP = KD::UMMA_K * ESZ;      // bytes along a K-major row
     constexpr uint32_t B_K_STEP = KD::UMMA_K * SW;       // rows of the MN-major tile
-    static_assert(B_CHUNKS * B_CHUNK_BYTES == B_STAGE_BYTES, "B stage size");
-    constexpr uint32_t IDESC = instr_desc<ESZ, B_KMAJOR>();
+    static_assert(B_CHUNKS * B_CHUNK_BYTES == B_STG, "B stage size");
+    static_assert(NST <= ONE_SM_MAX_STAGES && NST * (A_STAGE_BYTES + B_STG) <= ONE_SM_RING, "ring");
+    static_assert(!A_LOADER || TBN == BN, "the SIMT A loader runs with 128 x 256 tiles");
+    constexpr uint32_t IDESC = instr_desc<ESZ, B_KMAJOR, BM, TBN>();
+    constexpr int B_STAGE_BYTES = B_STG;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
-    float* epi_stage = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES);
-    Sync* sy = reinterpret_cast<Sync*>(smem + STAGES * STAGE_BYTES + EPI_STAGE_BYTES);
+    float* epi_stage = reinterpret_cast<float*>(smem + ONE_SM_RING);
+    Sync* sy = reinterpret_cast<Sync*>(smem + ONE_SM_RING + EPI_STAGE_BYTES);
     const uint32_t a_base = smem_u32(smem);
     const uint32_t b_base = a_base + STAGES * A_STAGE_BYTES;
 
@@ -1024,16 +1037,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     if (!mbar_wait(smem_u32(&sy->empty[s]), ph ^ 1u, &sy->abort, lim, true)) goto producer_done;
                     if (p.debug_stall && g == 0) continue;     // test hook: never fill stage 0
                     const uint32_t full = smem_u32(&sy->full[s]);
-                    mbar_arrive_expect_tx(full, A_LOADER ? B_STAGE_BYTES : STAGE_BYTES);
+                    mbar_arrive_expect_tx(full, A_LOADER ? B_STAGE_BYTES : A_STAGE_BYTES + B_STAGE_BYTES);
                     if constexpr (!A_LOADER)
                         tma_load_2d(a_base + s * A_STAGE_BYTES, &tmA, kb * BK, mb * BM, full);
                     const uint32_t bdst = b_base + s * B_STAGE_BYTES;
                     if constexpr (B_KMAJOR) {
-                        tma_load_2d(bdst, &tmB, kb * BK, nb * BN, full);
+                        tma_load_2d(bdst, &tmB, kb * BK, nb * TBN, full);
                     } else {
 #pragma unroll
                         for (int c = 0; c < B_CHUNKS; ++c)
-                            tma_load_2d(bdst + c * B_CHUNK_BYTES, &tmB, nb * BN + c * B_CHUNK_COLS,
+                            tma_load_2d(bdst + c * B_CHUNK_BYTES, &tmB, nb * TBN + c * B_CHUNK_COLS,
                                         kb * BK, full);
                     }
                     armed |= 1u << s;
@@ -1058,7 +1071,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                 const uint32_t aph = (uint32_t)(it >> 1) & 1u;
                 if (!mbar_wait(smem_u32(&sy->tmem_empty[acc]), aph ^ 1u, &sy->abort, lim, true)) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * TBN);
                 bool ok = true;
                 for (int kb = w.kb0; kb < w.kb1; ++kb, ++g) {
                     const int s = g % STAGES;
@@ -1112,8 +1125,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                 !sk_wait(flag, (unsigned)(w.fix_wait * p.sk_arrivals), &sy->abort, lim))
                 break;
             tc_fence_after();
-            store_accumulator<true>(p, w, mb, nb, q * 32 + lane, tmem_base + lane_off + (uint32_t)(acc * BN),
-                              epi_stage + q * (EPI_REGION / 4), &tmC, 0, BN / 32);
+            store_accumulator<true>(p, w, mb, nb, q * 32 + lane, tmem_base + lane_off + (uint32_t)(acc * TBN),
+                              epi_stage + q * (EPI_REGION / 4), &tmC, 0, TBN / 32);
             tc_fence_before();
             __syncwarp();                               // the warp's TMEM reads are done
             if (lane == 31) mbar_arrive(smem_u32(&sy->tmem_empty[acc]));   // not the storing lane
@@ -1873,15 +1886,16 @@ int grid_slots(const TcPlan& pl) {
     return pl.dp_tiles > 0 ? pl.slots : pl.sk_slots;
 }
 
-template <int ESZ, bool B_KMAJOR, bool A_LOADER = false>
+template <int ESZ, bool B_KMAJOR, bool A_LOADER = false, int TBN = BN>
 cudaError_t launch_tc(const GemmArgs& a, const TcPlan& pl, void* scratch, EncodeTiledFn enc,
                       unsigned long long wait_limit_ns, int debug_stall, cudaStream_t s) {
     constexpr int BK = Kind<ESZ>::BK;
     CUtensorMap tmA, tmB;
     memset(&tmA, 0, sizeof(tmA));
+    if (pl.tile_cols != TBN) return cudaErrorInvalidValue;
     if (!A_LOADER && !encode_2d(enc, &tmA, a.A, ESZ, a.M, a.K, a.lda, BK, BM))
         return cudaErrorInvalidValue;
-    const bool okb = B_KMAJOR ? encode_2d(enc, &tmB, a.B, ESZ, a.N, a.K, a.ldb, BK, BN)
+    const bool okb = B_KMAJOR ? encode_2d(enc, &tmB, a.B, ESZ, a.N, a.K, a.ldb, BK, TBN)
                               : encode_2d(enc, &tmB, a.B, ESZ, a.K, a.N, a.ldb, SW / ESZ, BK);
     if (!okb) return cudaErrorInvalidValue;
     TcParams p = make_params(a, pl, scratch, 4, wait_limit_ns, debug_stall);
@@ -1892,8 +1906,8 @@ cudaError_t launch_tc(const GemmArgs& a, const TcPlan& pl, void* scratch, Encode
 
     p.a_esz = ESZ;
     p.lda_bytes = a.lda * (long)ESZ;
-    auto kern = tc_gemm_kernel<ESZ, B_KMAJOR, A_LOADER>;
-    cudaError_t e = set_smem_limit_once<tc_gemm_kernel<ESZ, B_KMAJOR, A_LOADER>>(SMEM_BYTES);
+    auto kern = tc_gemm_kernel<ESZ, B_KMAJOR, A_LOADER, TBN>;
+    cudaError_t e = set_smem_limit_once<tc_gemm_kernel<ESZ, B_KMAJOR, A_LOADER, TBN>>(SMEM_BYTES);
     if (e != cudaSuccess) return e;
     kern<<<grid_slots(pl), NUM_THREADS + (A_LOADER ? 32 * A_LOADER_WARPS : 0), SMEM_BYTES, s>>>(
         tmA, tmB, tmC, p);
@@ -2122,7 +2136,7 @@ struct TileModel {
 // (about 3.3 TB/s over 152 SMs on 16 x 14336 x 4096, TF32 and BF16).
 TileModel tile_model(int in_type, int shape, int tile_rows, int tile_cols, int K, bool tma_c,
                      bool b_stream) {
-    double tflops = (shape == TC_ONE_SM || shape == TC_ONE_SM_T) ? 9.3
+    double tflops = (shape == TC_ONE_SM || shape == TC_ONE_SM_T || shape == TC_ONE_SM_N) ? 9.3
                   : shape == TC_PAIR ? 22.8 : 30.0;                            // BF16
     if (in_type != TC_BF16) tflops *= 0.5;                                      // TF32 rate
     if (in_type == TC_TF32X3) tflops /= 3.0;                                    // three products
@@ -2158,7 +2172,8 @@ TcPlan tc_plan(int M, int N, int K, int in_type, int shape, int num_sms, int str
     const bool pair = shape == TC_PAIR || shape == TC_PAIR_WIDE;
     TcPlan pl;
     pl.tile_rows = pair ? P_BM : BM;
-    pl.tile_cols = shape == TC_PAIR_WIDE ? 2 * BN : shape == TC_ONE_SM_T ? TT_BN : BN;
+    pl.tile_cols = shape == TC_PAIR_WIDE ? 2 * BN
+                 : (shape == TC_ONE_SM_T || shape == TC_ONE_SM_N) ? TT_BN : BN;
     pl.tiles_m = (M + pl.tile_rows - 1) / pl.tile_rows;
     pl.tiles_n = (N + pl.tile_cols - 1) / pl.tile_cols;
     const int bk = in_type == TC_BF16 ? Kind<2>::BK : Kind<4>::BK;
@@ -2232,7 +2247,15 @@ int tc_shape(int M, int N, int K, int in_type, int mode, int num_sms, int stream
     if (mode == 0) return TC_ONE_SM;
     if (mode == 1) return TC_PAIR;
     if (mode == 2) return TC_PAIR_WIDE;
-    if (M <= BM) return TC_ONE_SM;        // a pair tile is 256 rows tall (mode 3: as -1)
+    if (mode == 4) return TC_ONE_SM_N;
+    if (M <= BM) {                        // a pair tile is 256 rows tall (mode 3: as -1)
+        // One row of 128 x 256 tiles, or of 128 x 128 tiles, which fill more
+        // SMs without sharing tiles (16 x 14336 x 4096 BF16: 112 tiles on
+        // 112 SMs, no stream-K hand-off or counter zeroing).
+        const TcPlan wide1 = tc_plan(M, N, K, in_type, TC_ONE_SM, num_sms, streamk, tma_c);
+        const TcPlan narrow1 = tc_plan(M, N, K, in_type, TC_ONE_SM_N, num_sms, streamk, tma_c);
+        return narrow1.est_us < 0.97 * wide1.est_us ? TC_ONE_SM_N : TC_ONE_SM;
+    }
     if (N <= BN) return TC_PAIR;
     // The shape the timing model expects to finish first; near-ties go to
     // the narrow tiles, whose epilogue is hidden.
@@ -2243,6 +2266,8 @@ int tc_shape(int M, int N, int K, int in_type, int mode, int num_sms, int stream
 
 const char* tc_kernel_name(int in_type, int shape) {
     if (shape == TC_ONE_SM_T && in_type == TC_TF32) return "tc_tf32_128x128x32_s6_btrans_persistent";
+    if (shape == TC_ONE_SM_N && in_type == TC_TF32) return "tc_tf32_128x128x32_s6_persistent";
+    if (shape == TC_ONE_SM_N && in_type == TC_BF16) return "tc_bf16_128x128x64_s6_persistent";
     const int sh = shape < 0 ? 0 : shape > 2 ? 2 : shape;
     return kNames[in_type == TC_BF16 ? 1 : in_type == TC_TF32X3 ? 2 : 0][sh];
 }
@@ -2257,6 +2282,14 @@ cudaError_t tc_launch(const GemmArgs& a, int in_type, int b_kmajor, void* encode
     if (in_type == TC_TF32X3)       // always the CTA-pair kernel, B K-major
         return a.a_loader ? cudaErrorInvalidValue
                           : launch_tc_pair<4, true, true>(a, pl, scratch, enc, w, st, s);
+    if (shape == TC_ONE_SM_N) {
+        if (a.a_loader || pl.tile_cols != TT_BN || in_type == TC_TF32X3) return cudaErrorInvalidValue;
+        if (in_type == TC_BF16)
+            return b_kmajor ? launch_tc<2, true, false, TT_BN>(a, pl, scratch, enc, w, st, s)
+                            : launch_tc<2, false, false, TT_BN>(a, pl, scratch, enc, w, st, s);
+        if (!b_kmajor) return cudaErrorInvalidValue;    // TF32 reads B K-major only
+        return launch_tc<4, true, false, TT_BN>(a, pl, scratch, enc, w, st, s);
+    }
     if (shape == TC_ONE_SM_T) {
         if (in_type != TC_TF32 || b_kmajor || a.a_loader || pl.tile_cols != TT_BN)
             return cudaErrorInvalidValue;

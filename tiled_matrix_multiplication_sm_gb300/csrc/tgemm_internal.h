@@ -77,10 +77,11 @@ enum TcType { TC_TF32 = 1, TC_BF16 = 2, TC_TF32X3 = 3 };
 // Tile shapes of the tensor-core kernels: 128 x 256 on one SM, 256 x 256 on
 // an SM pair, 256 x 512 on an SM pair (two N = 256 MMAs per K step), and
 // 128 x 128 on one SM for TF32 with B read as stored (K x N) and transposed
-// in shared memory by the kernel (TC_ONE_SM_T).
-enum TcShape { TC_ONE_SM = 0, TC_PAIR = 1, TC_PAIR_WIDE = 2, TC_ONE_SM_T = 3 };
+// in shared memory by the kernel (TC_ONE_SM_T), and 128 x 128 on one SM
+// (TC_ONE_SM_N: more tiles for products with few rows).
+enum TcShape { TC_ONE_SM = 0, TC_PAIR = 1, TC_PAIR_WIDE = 2, TC_ONE_SM_T = 3, TC_ONE_SM_N = 4 };
 // The shape a product runs with: mode -1 = the shape a timing model expects
-// to finish first, 0/1/2 = that TcShape (the split-TF32 form always takes
+// to finish first, 0/1/2/4 = that TcShape (the split-TF32 form always takes
 // TC_PAIR); mode 3 is taken as -1 (the caller picks TC_ONE_SM_T, which
 // depends on how B is stored). streamk and tma_c as for tc_plan.
 int tc_shape(int M, int N, int K, int in_type, int mode, int num_sms, int streamk,
