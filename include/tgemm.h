@@ -355,11 +355,18 @@ TGEMM_API int gemm_set_tc_kernel(int mode);
  * launch: each computes a share of at most one tile's length, writes the
  * partial tile of a share that does not end a tile to scratch, and the SM
  * or pair whose share ends a tile adds the partial tiles of the shares
- * before it (fixed order: deterministic) and stores the tile. -1 (default)
- * takes S from a timing model (or no sharing), 0 never shares, S > 0 shares
- * the tail among S (clamped to the SMs or pairs available and to the tail's
- * K blocks; no sharing if that leaves S at or below the tail's tile count).
- * Process-wide. Returns TGEMM_OK or TGEMM_ERR_INVALID_ARG (slots < -1).
+ * before it (fixed order: deterministic) and stores the tile. In the split
+ * form every tail tile is instead cut into k equal shares on k SMs or
+ * pairs, which all write their partial tiles and wait for nothing, and a
+ * reduction kernel launched after the GEMM kernel adds each tile's shares
+ * in K order, applies the output rule and stores the tile (deterministic).
+ * -1 (default) takes the form and S or k from a timing model (or no
+ * sharing), 0 never shares, S > 0 shares the tail among S (clamped to the
+ * SMs or pairs available and to the tail's K blocks; no sharing if that
+ * leaves S at or below the tail's tile count), S <= -2 takes the split form
+ * with k = -S (clamped so that k times the tail's tiles fits the SMs or
+ * pairs; none below k = 2). Process-wide. Returns TGEMM_OK or
+ * TGEMM_ERR_INVALID_ARG (slots < -64).
  */
 TGEMM_API int gemm_set_tc_streamk(int slots);
 
@@ -395,7 +402,9 @@ TGEMM_API const char* gemm_f32_kernel_name(int id);
  * wave were computed in S K-pieces each and summed by a reduction kernel
  * (FP32 path); a tensor-core kernel's name carries "(streamk:slots=S,tiles=T)"
  * when the K blocks of the T tiles of its partial last round were shared by
- * S SMs or SM pairs inside the kernel (no extra launch);
+ * S SMs or SM pairs inside the kernel (no extra launch), and is followed by
+ * "tc_split_reduce(split=k,tiles=T)" when its T tail tiles were computed in
+ * k shares each and summed by the tensor paths' reduction kernel;
  * "empty_product" for K == 0, "" if nothing was launched (empty output,
  * error). Valid until the thread's next call. For tests and benchmarks.
  */

@@ -156,7 +156,7 @@ def test_setters_validate(lib):
     assert binding.set_tc_kernel(5) == binding.TGEMM_ERR_INVALID_ARG
     assert binding.set_tc_kernel(-2) == binding.TGEMM_ERR_INVALID_ARG
     assert binding.set_tc_kernel(-1) == binding.TGEMM_OK
-    assert binding.set_tc_streamk(-2) == binding.TGEMM_ERR_INVALID_ARG
+    assert binding.set_tc_streamk(-65) == binding.TGEMM_ERR_INVALID_ARG
     assert binding.set_tc_streamk(40) == binding.TGEMM_OK
     assert binding.set_tc_streamk(-1) == binding.TGEMM_OK
     assert binding.set_tc_a_loader(2) == binding.TGEMM_ERR_INVALID_ARG

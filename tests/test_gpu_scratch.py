@@ -77,21 +77,31 @@ def test_bf16_whole_waves_allocate_nothing(tgemm):
 
 
 def streamk_bytes(name):
-    """Scratch of a stream-K tail named in a last-kernel record: one partial
-    tile per sharing slot, then one counter per tail tile."""
+    """Scratch of a shared tail named in a last-kernel record: for stream-K,
+    one partial tile per sharing slot, then one counter per tail tile; for
+    the split form (k shares a tile, a reduction kernel), k partial tiles
+    per tail tile and no counters."""
     m = re.search(r"(\d+)x(\d+)x\d+_s\d+(?:_btrans)?_persistent\(streamk:slots=(\d+),tiles=(\d+)\)", name)
-    if not m:
-        return 0
-    rows, cols, slots, tiles = (int(x) for x in m.groups())
-    if "2sm" in name:
-        rows = 256
-    return round_up(slots * rows * cols * 4, 256) + round_up(tiles * 4, 256)
+    if m:
+        rows, cols, slots, tiles = (int(x) for x in m.groups())
+        if "2sm" in name:
+            rows = 256
+        return round_up(slots * rows * cols * 4, 256) + round_up(tiles * 4, 256)
+    m = re.search(r"(\d+)x(\d+)x\d+_s\d+(?:_btrans)?_persistent\+tc_split_reduce\(split=(\d+),tiles=(\d+)\)",
+                  name)
+    if m:
+        rows, cols, k, tiles = (int(x) for x in m.groups())
+        if "2sm" in name:
+            rows = 256
+        return round_up(k * tiles * rows * cols * 4, 256)
+    return 0
 
 
 def test_tf32_transposes_b(tgemm):
     """TF32 with more than 128 rows of A writes B transposed, N x
-    round_up(K, 32) floats, plus the stream-K tail's partial tiles and
-    counters when the planner shares the two tiles among SM pairs."""
+    round_up(K, 32) floats, plus the shared tail's partial tiles (and
+    stream-K counters) when the planner shares the two tiles among SM
+    pairs."""
     M, N, K = 200, 300, 1000
     A, B = int_operands(M, N, K, torch.float32, 3)
     n = tgemm.binding.scratch_bytes(A, B, "tf32")

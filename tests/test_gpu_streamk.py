@@ -123,3 +123,64 @@ def test_automatic_choice_is_exact(tgemm):
     rows = list(range(0, 4096, 97)) + [4095]
     C_ref, _ = oracle.gemm_rows(A, B, rows)
     assert_bit_exact(C.cpu()[rows], C_ref, f"4096^3 {tgemm.binding.last_kernel()}")
+
+
+# ---------------------------------------------------------------- the split form
+
+@pytest.mark.parametrize("kind", ["tf32", "bf16"])
+@pytest.mark.parametrize("mode,shape,k", [(1, (300, 700, 1032), 4), (1, (2304, 2304, 512), 2),
+                                          (2, (512, 1500, 2048), 3), (0, (100, 1000, 2048), 6),
+                                          (1, (389, 301, 97), 2)])
+def test_split_form_integer_bit_exact(tgemm, kind, mode, shape, k):
+    """The tail tiles in k equal shares that wait for nothing, summed in K
+    order by the reduction kernel (which also stores rows and columns past
+    the shares' tiles exactly once)."""
+    M, N, K = shape
+    g = inputs.generator(M + 3 * N + K + k)
+    A = inputs.draw(M, K, "int4", g).to(DTYPES[kind])
+    B = inputs.draw(K, N, "int4", g).to(DTYPES[kind])
+    C, name = forced(tgemm, mode, -k, lambda: tgemm.gemm_tc(A.cuda(), B.cuda(), kind))
+    m = re.search(r"\+tc_split_reduce\(split=(\d+),tiles=(\d+)\)", name)
+    assert m is not None, name
+    assert_bit_exact(C, oracle.gemm(A, B)[0], f"{kind} {shape} split {k}")
+
+
+@pytest.mark.parametrize("kind", ["tf32", "bf16"])
+def test_split_form_full_output_rule_and_guard_bands(tgemm, kind):
+    """alpha, beta and bias applied once per element by the reduction; C
+    rows off 16-byte boundaries; the padding and guard bands untouched."""
+    M, N, K = 512, 1530, 2048
+    g = inputs.generator(91)
+    A = inputs.draw(M, K, "int4", g).to(DTYPES[kind])
+    B = inputs.draw(K, N, "int4", g).to(DTYPES[kind])
+    C0 = inputs.draw(M, N, "int4", g)
+    bias = inputs.draw(1, N, "int4", g)[0]
+    ldc, guard = N + 3, 64
+    store = torch.full((guard + M * ldc + guard,), -99.0, device="cuda")
+    C = store[guard:guard + M * ldc].view(M, ldc)[:, :N]
+    C.copy_(C0.cuda())
+    _, name = forced(tgemm, 1, -3, lambda: tgemm.binding.gemm_ex(A.cuda(), B.cuda(), kind, alpha=2.0,
+                                                                  beta=-1.0, bias=bias.cuda(), out=C))
+    assert "+tc_split_reduce(split=3," in name, name
+    ref, _ = oracle.gemm_ex(A, B, alpha=2.0, beta=-1.0, C0=C0, bias=bias)
+    assert_bit_exact(C, ref, f"{kind} split rule")
+    host = store.cpu()
+    assert (host[:guard] == -99.0).all() and (host[guard + M * ldc:] == -99.0).all()
+    assert (host[guard:guard + M * ldc].view(M, ldc)[:, N:] == -99.0).all()
+
+
+def test_split_form_float_deterministic(tgemm):
+    M, N, K = 600, 1000, 1537
+    g = inputs.generator(92)
+    A = inputs.draw(M, K, "normal", g)
+    B = inputs.draw(K, N, "normal", g)
+    Ad, Bd = A.cuda(), B.cuda()
+    outs = []
+    for _ in range(4):
+        C, name = forced(tgemm, 1, -4, lambda: tgemm.gemm_tc(Ad, Bd, "tf32"))
+        outs.append(C)
+    assert "+tc_split_reduce(split=4," in name, name
+    C_ref, absAB = oracle.gemm(A, B)
+    assert_within(outs[0], C_ref, absAB, TC_REL, TC_ABS, "split float")
+    for C in outs[1:]:
+        assert torch.equal(C, outs[0])

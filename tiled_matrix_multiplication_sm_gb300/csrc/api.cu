@@ -509,10 +509,14 @@ int run_product(const Request& r, cudaStream_t stream) {
                                 pp.shape, pp.tplan, partials, stream));
             kname = tgemm::tc_kernel_name(path, pp.shape);
             if (pp.a_loader) strncat(tail, "(a_loader)", sizeof(tail) - strlen(tail) - 1);
-            if (pp.tplan.sk_slots > 0)
+            const int tail_tiles = pp.tplan.tiles_m * pp.tplan.tiles_n - pp.tplan.dp_tiles;
+            if (pp.tplan.sk_slots > 0 && pp.tplan.sk_split)
                 snprintf(tail + strlen(tail), sizeof(tail) - strlen(tail),
-                         "(streamk:slots=%d,tiles=%d)", pp.tplan.sk_slots,
-                         pp.tplan.tiles_m * pp.tplan.tiles_n - pp.tplan.dp_tiles);
+                         "+tc_split_reduce(split=%d,tiles=%d)", pp.tplan.sk_slots / tail_tiles,
+                         tail_tiles);
+            else if (pp.tplan.sk_slots > 0)
+                snprintf(tail + strlen(tail), sizeof(tail) - strlen(tail),
+                         "(streamk:slots=%d,tiles=%d)", pp.tplan.sk_slots, tail_tiles);
         }
     }
     if (ws != nullptr && cudaFreeAsync(ws, stream) != cudaSuccess && rc == TGEMM_OK)
@@ -901,7 +905,7 @@ int gemm_set_tc_a_loader(int mode) {
 }
 
 int gemm_set_tc_streamk(int slots) {
-    if (slots < -1) return TGEMM_ERR_INVALID_ARG;
+    if (slots < -64) return TGEMM_ERR_INVALID_ARG;
     g_tc_streamk.store(slots);
     return TGEMM_OK;
 }

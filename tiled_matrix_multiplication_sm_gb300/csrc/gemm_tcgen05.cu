@@ -125,6 +125,12 @@ struct TcParams {
     // tiles are computed whole too.
     int sk_slots;
     long long sk_total;  // (num_tiles - dp_tiles) * kblocks
+    // The split form of the tail (sk_split = 1): sk_slots is a multiple of
+    // the tail's tile count, so each tile's K blocks are sk_slots / tiles
+    // shares of consecutive slots; every share leaves its raw partial tile and
+    // nothing waits -- a separate reduction kernel sums each tile's shares
+    // in K order and stores it (no chain of hand-offs; sk_flags unused).
+    int sk_split;
     float* partials;     // sk_slots partial tiles (tile_rows x tile_cols), one per slot
     unsigned* sk_flags;  // one arrival counter per tail tile, zero at launch
     int sk_arrivals;     // arrivals of one contribution (the epilogue warps of a slot)
@@ -229,6 +235,10 @@ __device__ __forceinline__ Unit slot_unit(const TcParams& p, int slot, int i) {
     w.tile = p.dp_tiles + (int)t;
     w.kb0 = (int)s0;
     w.kb1 = (int)s1;
+    if (p.sk_split) {                            // every share a piece; nothing waits
+        w.piece = slot;
+        return w;
+    }
     if (s1 != KB) w.piece = slot;               // not the tile's end: a contribution
     const int first = sk_slot_of(p, t * KB);     // the slot holding the tile's first K block
     if (slot > first) {
@@ -1117,7 +1127,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             const uint32_t aph = (uint32_t)(it >> 1) & 1u;
             bool ok = mbar_wait(smem_u32(&sy->tmem_full[acc]), aph, &sy->abort, lim, true);
             if (!__all_sync(0xffffffffu, ok)) break;
-            unsigned* flag = (w.fix_wait > 0 || w.piece >= 0) ? p.sk_flags + (w.tile - p.dp_tiles)
+            unsigned* flag = (p.sk_flags != nullptr && (w.fix_wait > 0 || w.piece >= 0))
+                                 ? p.sk_flags + (w.tile - p.dp_tiles)
                                                               : nullptr;
             // The earlier shares of this tile must have landed before their
             // running sum is added.
@@ -1130,7 +1141,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             tc_fence_before();
             __syncwarp();                               // the warp's TMEM reads are done
             if (lane == 31) mbar_arrive(smem_u32(&sy->tmem_empty[acc]));   // not the storing lane
-            if (w.piece >= 0) sk_arrive(flag);   // this warp's part has landed
+            if (w.piece >= 0 && flag != nullptr) sk_arrive(flag);   // this warp's part has landed
         }
         tma_store_wait_all();    // every lane's C stores and row copies done before the block retires
     }
@@ -1367,7 +1378,8 @@ tc_gemm_tf32t_kernel(const __grid_constant__ CUtensorMap tmA,
             const uint32_t aph = (uint32_t)(it >> 1) & 1u;
             bool ok = mbar_wait(smem_u32(&sy->tmem_full[acc]), aph, &sy->abort, lim, true);
             if (!__all_sync(0xffffffffu, ok)) break;
-            unsigned* flag = (w.fix_wait > 0 || w.piece >= 0) ? p.sk_flags + (w.tile - p.dp_tiles)
+            unsigned* flag = (p.sk_flags != nullptr && (w.fix_wait > 0 || w.piece >= 0))
+                                 ? p.sk_flags + (w.tile - p.dp_tiles)
                                                               : nullptr;
             if (w.fix_wait > 0 &&
                 !sk_wait(flag, (unsigned)(w.fix_wait * p.sk_arrivals), &sy->abort, lim))
@@ -1379,7 +1391,7 @@ tc_gemm_tf32t_kernel(const __grid_constant__ CUtensorMap tmA,
             tc_fence_before();
             __syncwarp();
             if (lane == 31) mbar_arrive(smem_u32(&sy->tmem_empty[acc]));
-            if (w.piece >= 0) sk_arrive(flag);
+            if (w.piece >= 0 && flag != nullptr) sk_arrive(flag);
         }
         tma_store_wait_all();
     }
@@ -1747,7 +1759,8 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
             const uint32_t aph = (uint32_t)(it / NACC) & 1u;
             bool ok = mbar_wait(smem_u32(&sy->tmem_full[acc]), aph, &sy->abort, lim, true);
             if (!__all_sync(0xffffffffu, ok)) break;
-            unsigned* flag = (w.fix_wait > 0 || w.piece >= 0) ? p.sk_flags + (w.tile - p.dp_tiles)
+            unsigned* flag = (p.sk_flags != nullptr && (w.fix_wait > 0 || w.piece >= 0))
+                                 ? p.sk_flags + (w.tile - p.dp_tiles)
                                                               : nullptr;
             // The earlier shares of this tile must have landed before their
             // running sum is added.
@@ -1786,7 +1799,7 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
                 __syncwarp();                           // the warp's TMEM reads are done
                 if (lane == 31) mbar_arrive_cluster(tmem_empty0 + (uint32_t)(acc * sizeof(uint64_t)));
             }
-            if (w.piece >= 0) sk_arrive(flag);   // this warp's part has landed
+            if (w.piece >= 0 && flag != nullptr) sk_arrive(flag);   // this warp's part has landed
         }
         tma_store_wait_all();    // every lane's C stores and row copies done before the block retires
     }
@@ -1838,9 +1851,11 @@ TcParams make_params(const GemmArgs& a, const TcPlan& pl, void* scratch, int arr
     p.sk_total = (long long)(p.num_tiles - pl.dp_tiles) * pl.kblocks;
     p.partials = nullptr;
     p.sk_flags = nullptr;
+    p.sk_split = pl.sk_split;
     if (pl.sk_slots > 0) {
         p.partials = static_cast<float*>(scratch);
-        p.sk_flags = reinterpret_cast<unsigned*>(static_cast<char*>(scratch) + tc_partial_bytes(pl));
+        if (!pl.sk_split)
+            p.sk_flags = reinterpret_cast<unsigned*>(static_cast<char*>(scratch) + tc_partial_bytes(pl));
     }
     p.sk_arrivals = arrivals;
     p.wait_limit_ns = wait_limit_ns;
@@ -1871,12 +1886,66 @@ void encode_c(EncodeTiledFn enc, CUtensorMap* map, const GemmArgs& a, TcParams& 
         p.tma_c = 1;
 }
 
+// The split form's reduction: C for the tail tiles from their shares'
+// partial tiles. One block per 32 x 32 output block: warp w sums columns
+// w, w + 8, w + 16, w + 24 of the block over the tile's shares in K order
+// (lane = row: one coalesced 128-byte line per share and column of the
+// column-major partial block), the block transposes them through shared
+// memory, and warp w stores rows w, w + 8, .. as coalesced row segments of
+// C under the output rule.
+__global__ void __launch_bounds__(256)
+tc_split_reduce_kernel(const TcParams p) {
+    __shared__ float blk[32][33];
+    const int rb_n = p.tile_rows / 32, cb_n = p.tile_cols / 32;
+    const int tail_tiles = p.num_tiles - p.dp_tiles;
+    const int k = p.sk_slots / tail_tiles;                 // shares per tile
+    const int idx = blockIdx.x;
+    const int t = idx / (rb_n * cb_n);
+    if (t >= tail_tiles) return;
+    const int rb = (idx / cb_n) % rb_n, cb = idx % cb_n;
+    int mb, nb;
+    tile_coords(p.dp_tiles + t, p, mb, nb);
+    const int row0 = mb * p.tile_rows + rb * 32, col0 = nb * p.tile_cols + cb * 32;
+    if (row0 >= p.M || col0 >= p.N) return;                // uniform over the block
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int c = w + 8 * i;
+        float sum = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            const float* src = p.partials + partial_block(p, t * k + j, rb * 32, cb) * 1024;
+            sum += __ldcg(src + c * 32 + lane);
+        }
+        blk[c][lane] = sum;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = w + 8 * i;
+        const int grow = row0 + r, gcol = col0 + lane;
+        if (grow < p.M && gcol < p.N) {
+            float* dst = p.C + (long)grow * p.ldc + gcol;
+            const float v = blk[lane][r];
+            *dst = p.ep_simple ? v : apply_epilogue(v, p, dst, gcol);
+        }
+    }
+}
+
 // Zero the tail-tile counters of a stream-K plan, in stream order before
 // the launch.
 bool prepare_stream_k(const TcParams& p, cudaStream_t s) {
-    if (p.sk_slots == 0) return true;
+    if (p.sk_slots == 0 || p.sk_flags == nullptr) return true;
     return cudaMemsetAsync(p.sk_flags, 0, sizeof(unsigned) * (size_t)(p.num_tiles - p.dp_tiles),
                            s) == cudaSuccess;
+}
+
+// The split form's reduction, after the GEMM kernel in stream order.
+cudaError_t launch_split_reduce(const TcParams& p, cudaStream_t s) {
+    if (!p.sk_split || p.sk_slots == 0) return cudaSuccess;
+    const long blocks = (long)(p.num_tiles - p.dp_tiles) * (p.tile_rows / 32) * (p.tile_cols / 32);
+    if (blocks <= 0 || blocks > 2147483647L) return cudaErrorInvalidValue;
+    tc_split_reduce_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
+    return cudaGetLastError();
 }
 
 // Slots (SMs or SM pairs) the grid of plan `pl` needs.
@@ -1911,7 +1980,8 @@ cudaError_t launch_tc(const GemmArgs& a, const TcPlan& pl, void* scratch, Encode
     if (e != cudaSuccess) return e;
     kern<<<grid_slots(pl), NUM_THREADS + (A_LOADER ? 32 * A_LOADER_WARPS : 0), SMEM_BYTES, s>>>(
         tmA, tmB, tmC, p);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    return e != cudaSuccess ? e : launch_split_reduce(p, s);
 }
 
 // The TF32 kernel that transposes B in shared memory: one CTA per SM,
@@ -1931,7 +2001,8 @@ cudaError_t launch_tc_t(const GemmArgs& a, const TcPlan& pl, void* scratch, Enco
     cudaError_t e = set_smem_limit_once<tc_gemm_tf32t_kernel>(TT_SMEM_BYTES);
     if (e != cudaSuccess) return e;
     tc_gemm_tf32t_kernel<<<grid_slots(pl), TT_THREADS, TT_SMEM_BYTES, s>>>(tmA, tmB, tmC, p);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    return e != cudaSuccess ? e : launch_split_reduce(p, s);
 }
 
 // The 2-SM kernel: clusters of two CTAs, one CTA per SM, persistent over
@@ -1982,7 +2053,8 @@ cudaError_t launch_tc_pair(const GemmArgs& a, const TcPlan& pl, void* scratch, E
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmA2, tmB2, tmC, p);
     if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    return e != cudaSuccess ? e : launch_split_reduce(p, s);
 }
 
 // ===================================================================
@@ -2138,7 +2210,11 @@ TileModel tile_model(int in_type, int shape, int tile_rows, int tile_cols, int K
                      bool b_stream) {
     double tflops = (shape == TC_ONE_SM || shape == TC_ONE_SM_T || shape == TC_ONE_SM_N) ? 9.3
                   : shape == TC_PAIR ? 22.8 : 30.0;                            // BF16
-    if (in_type != TC_BF16) tflops *= 0.5;                                      // TF32 rate
+    // TF32: half the BF16 rate, and on the 256 x 256 pair tiles less again --
+    // their operand bytes per FLOP double and the shared-memory feed limits
+    // them (3072 x 5120 x 1536: ~9.6 TFLOP/s per pair measured on those
+    // tiles against ~11 on the 256 x 512 tiles).
+    if (in_type != TC_BF16) tflops *= shape == TC_PAIR ? 0.42 : 0.5;
     if (in_type == TC_TF32X3) tflops /= 3.0;                                    // three products
     TileModel m;
     m.main_us = 2.0 * tile_rows * tile_cols * (double)K / (tflops * 1e6);
@@ -2183,6 +2259,7 @@ TcPlan tc_plan(int M, int N, int K, int in_type, int shape, int num_sms, int str
     pl.slots = slots > 0 ? slots : 1;
     pl.dp_tiles = tiles;
     pl.sk_slots = 0;
+    pl.sk_split = 0;
     pl.scratch_bytes = 0;
     pl.est_us = 0.0;
     if (slots <= 0 || tiles == 0) return pl;
@@ -2195,6 +2272,21 @@ TcPlan tc_plan(int M, int N, int K, int in_type, int shape, int num_sms, int str
     pl.est_us = full * tile_us + (rem > 0 ? tm.share_us(1.0, rem) + tm.epi_us : 0.0);
     if (streamk == 0 || rem == 0) return pl;
     const long long T = (long long)rem * pl.kblocks;
+    // The split form: each tail tile in k equal shares of consecutive slots,
+    // summed in K order by a reduction kernel; k <= -streamk when forced.
+    auto set_split = [&](int k) {
+        pl.dp_tiles = tiles - rem;
+        pl.sk_slots = k * rem;
+        pl.sk_split = 1;
+        pl.scratch_bytes = tc_partial_bytes(pl);
+    };
+    if (streamk < -1) {
+        int k = -streamk;
+        if (k * rem > slots) k = slots / rem;
+        if (k > pl.kblocks) k = pl.kblocks;
+        if (k >= 2) set_split(k);
+        return pl;
+    }
     if (streamk > 0) {
         // Forced width (tests and tuning), kept where the tail allows it: more
         // slots than tail tiles, every share at least one K block.
@@ -2231,6 +2323,29 @@ TcPlan tc_plan(int M, int N, int K, int in_type, int shape, int num_sms, int str
             best = est;
             best_s = S;
         }
+    }
+    // The split form, for the pair tiles (whose hand-offs cost most): its
+    // shares run side by side and the reduction kernel reads every share's
+    // partial tile once (about 5 TB/s) after a launch gap.
+    int best_k = 0;
+    if (pair && slots / rem >= 2 && pl.kblocks >= 8) {
+        const int k = slots / rem < pl.kblocks / 4 ? slots / rem : pl.kblocks / 4;
+        if (k >= 2) {
+            const double tile_bytes = (double)pl.tile_rows * pl.tile_cols * 4;
+            const double reduce_us = 3.0 + (k + 1.0) * rem * tile_bytes / 5e6;
+            const long long len = (pl.kblocks + k - 1) / k;
+            const double est = full * tile_us + tm.share_us((double)len / pl.kblocks, k * rem) +
+                               tm.epi_us + reduce_us;
+            if (est < 0.98 * best) {                           // a clear gain over the rest
+                best = est;
+                best_k = k;
+            }
+        }
+    }
+    if (best_k > 0) {
+        set_split(best_k);
+        pl.est_us = best;
+        return pl;
     }
     if (best_s > 0) {
         pl.dp_tiles = tiles - rem;

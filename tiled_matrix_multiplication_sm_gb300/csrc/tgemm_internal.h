@@ -98,6 +98,7 @@ const char* tc_kernel_name(int in_type, int shape);
 struct TcPlan {
     int tile_rows, tile_cols, tiles_m, tiles_n, kblocks;
     int slots, dp_tiles, sk_slots;
+    int sk_split;        // the tail in the split form: equal shares, then a reduction kernel
     size_t scratch_bytes;
     double est_us;       // modelled duration, for choosing between shapes
 };
