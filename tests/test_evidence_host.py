@@ -68,6 +68,8 @@ def test_algorithmic_work_of_each_kind():
     assert w("empty_product", "k0:f32")["bytes"] == 4 * 4096 * 4096
     r = w("splitk_reduce(split=8,tiles=56)", "n4096:f32")
     assert (r["split"], r["tiles"], r["bytes_per_tile_elem"]) == (8, 56, 36)
+    r = w("tc_split_reduce(split=6,tiles=12)", "ragged:tf32")
+    assert (r["bound"], r["split"], r["tiles"], r["bytes_per_tile_elem"]) == ("hbm", 6, 12, 28)
     assert evidence.tile_elems("f32_128x256x32_s3_ffma2_vecA_vecB") == 128 * 256
     # The few-row workloads are stated against HBM: A + B read once, C written once.
     r = w("tc_bf16_128x256x64_s4_persistent(streamk:slots=112,tiles=56)", "skinny_bf16:bf16")

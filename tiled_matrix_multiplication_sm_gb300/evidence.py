@@ -185,7 +185,7 @@ def algorithmic_work(token: str, case: str) -> Dict[str, object]:
         return {"bound": "hbm", "bytes": 12 * M * K}
     if token == "transpose_split_b":
         return {"bound": "hbm", "bytes": 12 * K * N}
-    m = re.match(r"splitk_reduce\(split=(\d+),tiles=(\d+)\)", token)
+    m = re.match(r"(?:tc_split_reduce|splitk_reduce)\(split=(\d+),tiles=(\d+)\)", token)
     if m:
         split, tiles = int(m.group(1)), int(m.group(2))
         return {"bound": "hbm", "split": split, "tiles": tiles,
