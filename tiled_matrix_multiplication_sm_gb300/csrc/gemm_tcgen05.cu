@@ -1908,16 +1908,24 @@ tc_split_reduce_kernel(const TcParams p) {
     const int row0 = mb * p.tile_rows + rb * 32, col0 = nb * p.tile_cols + cb * 32;
     if (row0 >= p.M || col0 >= p.N) return;                // uniform over the block
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    // Eight shares' loads in flight before their adds (in K order).
+    float sum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int j0 = 0; j0 < k; j0 += 8) {
+        float v[8][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int c = w + 8 * i;
-        float sum = 0.0f;
-        for (int j = 0; j < k; ++j) {
-            const float* src = p.partials + partial_block(p, t * k + j, rb * 32, cb) * 1024;
-            sum += __ldcg(src + c * 32 + lane);
+        for (int u = 0; u < 8; ++u) {
+            const float* src = p.partials + partial_block(p, t * k + j0 + u, rb * 32, cb) * 1024 + lane;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[u][i] = j0 + u < k ? __ldcg(src + (w + 8 * i) * 32) : 0.0f;
         }
-        blk[c][lane] = sum;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (j0 + u < k) sum[i] += v[u][i];
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) blk[w + 8 * i][lane] = sum[i];
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
