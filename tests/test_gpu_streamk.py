@@ -130,7 +130,8 @@ def test_automatic_choice_is_exact(tgemm):
 @pytest.mark.parametrize("kind", ["tf32", "bf16"])
 @pytest.mark.parametrize("mode,shape,k", [(1, (300, 700, 1032), 4), (1, (2304, 2304, 512), 2),
                                           (2, (512, 1500, 2048), 3), (0, (100, 1000, 2048), 6),
-                                          (1, (389, 301, 97), 2)])
+                                          (1, (389, 301, 97), 2), (3, (100, 1000, 2048), 5),
+                                          (4, (100, 1000, 2048), 7)])
 def test_split_form_integer_bit_exact(tgemm, kind, mode, shape, k):
     """The tail tiles in k equal shares that wait for nothing, summed in K
     order by the reduction kernel (which also stores rows and columns past
