@@ -21,7 +21,7 @@ For each measured case (a workload and a path), this module
 Usage (on a machine with the GPU, after ``build()``)::
 
     python -m tiled_matrix_multiplication_sm_gb300.evidence capture \\
-        --out gpurun_out/evidence [--case n4096:f32 ...]
+        --out <raw-output-dir> [--case n4096:f32 ...]
     python -m tiled_matrix_multiplication_sm_gb300.evidence summary \\
         --records profiles/ncu > profiles/ncu_evidence.md
 
@@ -434,7 +434,8 @@ def main(argv=None):
     r.add_argument("--streamk", type=int, default=-1)
     c = sub.add_parser("capture", help="plain run, then ncu, for each case")
     c.add_argument("--case", action="append", default=None)
-    c.add_argument("--out", default=os.path.join(ROOT, "gpurun_out", "evidence"))
+    c.add_argument("--out", required=True,
+                   help="directory for the .ncu-rep files, logs and JSON records")
     s = sub.add_parser("summary", help="markdown table of the records in a directory")
     s.add_argument("--records", default=os.path.join(ROOT, "profiles", "ncu"))
     args = p.parse_args(argv)
