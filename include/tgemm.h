@@ -25,9 +25,7 @@
  *     caller's buffers, and keeps no reference to them after the call.
  *   - Scratch memory. A call may need device memory of its own while it
  *     runs, for two things:
- *       (a) operands rewritten into a layout the kernels read: on gemm_tc
- *           TGEMM_TF32 with M > 128 (or tensor-core mode 0, 1 or 2
- *           forced), B transposed (N x round_up(K, 32) floats); on the
+ *       (a) operands rewritten into a layout the kernels read: on the
  *           tensor paths, an operand whose rows do not start
  *           on 16-byte boundaries, repacked (rows on 128-byte boundaries);
  *           on gemm_f32, both operands repacked when their rows are off 16
@@ -45,9 +43,9 @@
  *     once a call of a given size has run, later calls reuse the cached
  *     memory without going to the driver; it stays reserved until the
  *     process exits. A call that needs neither (a) nor (b) allocates
- *     nothing: gemm_f32, gemm_tc TGEMM_BF16, and gemm_tc TGEMM_TF32 with
- *     M <= 128, on operands with 16-byte rows whose tiles fill whole waves
- *     or whose tail is not split.
+ *     nothing: gemm_f32, and gemm_tc TGEMM_BF16 and TGEMM_TF32, on operands
+ *     with 16-byte rows whose tiles fill whole waves or whose tail is not
+ *     split.
  *     gemm_scratch_bytes() returns the size a call would draw, and
  *     gemm_tc_tf32_noalloc() never allocates.
  *   - C is overwritten (there is no alpha/beta); K == 0 writes zeros to the
@@ -144,14 +142,11 @@ TGEMM_API int gemm_f32(int M, int N, int K,
  * boundaries: an operand whose pointer or leading dimension breaks that
  * (any lda, ldb and element-aligned pointer are accepted) is first repacked
  * by an HBM-bound kernel into stream-ordered scratch with rows on 128-byte
- * boundaries. The TF32 kind reads B only K-major: for TF32 with M > 128, B
- * is first rewritten transposed into scratch, which also absorbs any
- * alignment of B; with M <= 128 (a product bound by reading B once) the
- * kernel reads B as stored, K x N, and transposes each 32 x 128 block in
- * shared memory (128 x 128 tiles). Rows and columns past M, N, K read as
- * zero. Scratch (see the common rules): those rewritten operands, and the
- * partial tiles of a split last wave; BF16, and TF32 with M <= 128, on
- * operands with 16-byte rows whose tail is not split allocate nothing.
+ * boundaries. B is read as stored, K x N (MN-major: BF16 in the 128-byte
+ * swizzle, TF32 in the 128-byte swizzle with 32-byte atoms). Rows and
+ * columns past M, N, K read as zero. Scratch (see the common rules): the
+ * repacked operands, and the partial tiles of a split last wave; operands
+ * with 16-byte rows whose tail is not split allocate nothing.
  *
  * Returns TGEMM_OK, TGEMM_ERR_INVALID_ARG (as gemm_f32, a bad in_type, or
  * a pointer not aligned to its element size), TGEMM_ERR_UNSUPPORTED or
@@ -194,7 +189,8 @@ TGEMM_API int gemm_tc(int M, int N, int K,
  * _TF32X3 (gemm_tc's), with A and B of that path's element type. Storage the
  * path's kernels cannot read directly is rewritten first by HBM-bound
  * kernels into stream-ordered scratch (transposes; the tensor paths read A
- * K-major and TF32 reads B K-major, so TRANS_B needs no copy there). With
+ * K-major, and B either MN-major or K-major, so TRANS_B needs no copy
+ * there). With
  * flags 0, alpha 1, beta 0 and no bias it is exactly gemm_f32 / gemm_tc.
  *
  * Returns TGEMM_OK, TGEMM_ERR_INVALID_ARG (as gemm_f32 with the ld rules
@@ -223,9 +219,9 @@ TGEMM_API int gemm_ex(int M, int N, int K,
  * of C is left to copy out at the end; there B goes up in two column halves
  * and the first panel is multiplied in the same halves, the left one as soon
  * as it has arrived), each panel is
- * multiplied on `stream` as soon as its rows have arrived (the TF32 path
- * transposes B once for all panels; TF32X3 splits B once and each panel of
- * A as it arrives), and each panel of C is copied back on a second copy
+ * multiplied on `stream` as soon as its rows have arrived (TF32X3 splits
+ * and transposes B once for all panels and splits each panel of A as it
+ * arrives), and each panel of C is copied back on a second copy
  * stream while the next panel computes. Same arithmetic and result as
  * gemm_f32 / gemm_tc on device copies of the operands.
  *
@@ -333,8 +329,7 @@ TGEMM_API int gemm_set_f32_kernel(int id);
  * 3 the one-SM TF32 kernel that transposes B in shared memory (128 x 128
  * tiles; TGEMM_TF32 with B stored K x N, other products as with -1), 4 the
  * one-SM kernel with 128 x 128 tiles (B read as the 128 x 256 one-SM kernel
- * reads it); -1 (default) picks by shape: for TGEMM_TF32 with B stored
- * K x N and M <= 128 the kernel of mode 3, else for M <= 128 the one-SM
+ * reads it); -1 (default) picks by shape: for M <= 128 the one-SM
  * kernel with 128 x 256 or 128 x 128 tiles, whichever the timing model
  * expects to finish first (the narrower tiles fill more SMs), 256 x 256
  * tiles when N <= 256, and otherwise the pair shape that a timing model of
@@ -415,13 +410,15 @@ TGEMM_API const char* gemm_last_kernel(void);
  * for callers that cannot allocate device memory.
  *
  * The pages have no counterpart to this entry point; it exists for the
- * library's callers. gemm_tc's TF32 path needs scratch memory for B
- * transposed and takes it from a stream-ordered memory pool. Callers that
+ * library's callers. gemm_tc's TF32 path takes scratch memory from a
+ * stream-ordered memory pool for operands whose rows are off 16 bytes and
+ * for the partial tiles of a split last wave. Callers that
  * must not let a library allocate -- an application or plugin that reserves
  * all of its device memory at start-up and treats any later allocation as a
  * failure, or code that must not touch the device allocator while it runs
  * -- call this instead: it allocates nothing (no cudaMalloc, cudaFree or
- * allocating library routine) and keeps the transposed B in a fixed array of
+ * allocating library routine), never splits the last wave, and, when B's
+ * rows are off 16 bytes, keeps a transposed B in a fixed array of
  * TGEMM_NOALLOC_SCRATCH_FLOATS floats (16 MiB) in the library's own device
  * memory, which every device that loads the library holds until the process
  * exits.
@@ -429,7 +426,9 @@ TGEMM_API const char* gemm_last_kernel(void);
  * Arguments, layout and result are those of gemm_tc with in_type TGEMM_TF32:
  * A is M x K floats (16-byte aligned, lda >= K and a multiple of 4), B is
  * K x N floats (4-byte aligned, ldb >= N), C is M x N floats (ldc >= N).
- * B transposed goes to the array with rows round_up(K, 32) floats apart
+ * B whose pointer is 16-byte aligned and ldb a multiple of 4 is read as
+ * stored and the array is not touched. Otherwise B transposed goes to the
+ * array with rows round_up(K, 32) floats apart
  * (128-byte rows, as gemm_tc) when N * round_up(K, 32) fits in it, else
  * round_up(K, 4) floats apart (16-byte rows; the GEMM kernel reads such rows
  * somewhat slower). The tiles of a partial last wave are never split along
@@ -437,8 +436,9 @@ TGEMM_API const char* gemm_last_kernel(void);
  * by the limit of gemm_set_wait_limit_ns, as for gemm_tc.
  *
  * Returns TGEMM_OK; TGEMM_ERR_INVALID_ARG for the argument errors of gemm_tc,
- * for K > 4194240, and when N * round_up(K, 4) > TGEMM_NOALLOC_SCRATCH_FLOATS
- * (the problem does not fit the fixed scratch; nothing is launched);
+ * for K > 4194240, and, when B has to be transposed, for
+ * N * round_up(K, 4) > TGEMM_NOALLOC_SCRATCH_FLOATS (the problem does not
+ * fit the fixed scratch; nothing is launched);
  * TGEMM_ERR_ALIGNMENT; TGEMM_ERR_UNSUPPORTED; TGEMM_ERR_CUDA.
  *
  * The first call on each device does that device's set-up (it looks up the

@@ -102,3 +102,26 @@ def test_bounded_wait_with_loader(tgemm):
         tgemm.binding.set_tc_a_loader(-1)
     C, name = run(tgemm, -1, Ad, B.cuda(), "tf32")
     assert_bit_exact(C, oracle.gemm(A, B)[0], "after the timeout")
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_tf32_b_stored_transposed(tgemm, mode):
+    """TF32 with B stored N x K (read K-major, rows 16-byte aligned: K a
+    multiple of 4) beside the loader's A (lda = K + 1)."""
+    M, N, K = 300, 520, 516
+    g = inputs.generator(7 + mode)
+    A = inputs.draw(M, K, "int4", g)
+    B = inputs.draw(K, N, "int4", g)
+    lda = pick_lda(K, 4)
+    assert tgemm.binding.set_tc_a_loader(1) == 0
+    assert tgemm.binding.set_tc_kernel(mode) == 0
+    try:
+        C = tgemm.binding.gemm_ex(nan_padded(A, lda), B.t().contiguous().cuda(), "tf32",
+                                  trans_b=True)
+        name = tgemm.binding.last_kernel()
+    finally:
+        tgemm.binding.set_tc_a_loader(-1)
+        tgemm.binding.set_tc_kernel(-1)
+    assert tgemm.device_status() == 0
+    assert "(a_loader)" in name and "repack" not in name and "transpose" not in name, name
+    assert_bit_exact(C, oracle.gemm(A, B)[0], f"tf32 B^T mode {mode}")

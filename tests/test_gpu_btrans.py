@@ -1,13 +1,11 @@
 """The TF32 kernel that transposes B in shared memory (128 x 128 tiles).
 
-The TF32 kind of the tensor-core instruction reads B only K-major. TF32
-products whose B is stored K x N (N contiguous) and whose A has at most 128
-rows -- bound by reading B once -- read B as stored: TMA lands each 32 x 128
-block of B in its MN-major layout and two warps of the kernel rewrite it
-K-major in place before the MMAs read it, instead of a transpose pre-pass
-over all of B. Tensor-core mode 3 forces this kernel at any M. Every result
-is checked against the oracle: bit for bit on integer data, within the TF32
-tolerance on random data.
+TMA lands each 32 x 128 block of a B stored K x N (N contiguous) in its
+MN-major layout and two warps of the kernel rewrite it K-major in place
+before the MMAs read it. The other kernels now read such a B MN-major
+directly (faster), so this one runs only when tensor-core mode 3 forces it,
+at any M. Every result is checked against the oracle: bit for bit on
+integer data, within the TF32 tolerance on random data.
 """
 import re
 import time
@@ -49,22 +47,15 @@ def run(tg, fn, mode=-1, slots=-1):
     return out, name
 
 
-@pytest.mark.parametrize("M", [1, 16, 100, 128])
-def test_few_rows_read_b_as_stored(tgemm, M):
-    """By default (mode -1) A with at most 128 rows takes this kernel: no
-    transpose pre-pass of B."""
+@pytest.mark.parametrize("M", [1, 16, 100, 128, 129])
+def test_default_reads_b_as_stored_without_this_kernel(tgemm, M):
+    """By default (mode -1) TF32 reads B MN-major as stored with the other
+    kernels at any M: neither this kernel nor a transpose pre-pass."""
     N, K = 1000, 264
     A, B = operands(M, N, K, "int4", seed=M)
     C, name = run(tgemm, lambda: tgemm.gemm_tc(A.cuda(), B.cuda(), "tf32"))
-    assert KERNEL in name and "transpose_b" not in name, name
+    assert KERNEL not in name and "transpose_b" not in name, name
     assert_bit_exact(C, oracle.gemm(A, B)[0], f"M={M}")
-
-
-def test_more_rows_keep_the_pre_pass(tgemm):
-    A, B = operands(129, 264, 72, "int4", seed=129)
-    C, name = run(tgemm, lambda: tgemm.gemm_tc(A.cuda(), B.cuda(), "tf32"))
-    assert KERNEL not in name and "transpose_b" in name, name
-    assert_bit_exact(C, oracle.gemm(A, B)[0], "M=129")
 
 
 @pytest.mark.parametrize("shape", [(1, 8, 8), (8, 8, 8), (127, 248, 40), (129, 264, 72),
@@ -96,7 +87,7 @@ def test_unaligned_rows_are_repacked(tgemm):
     repacked (B as K x N, 128-byte rows), then read as stored."""
     M, N, K = 100, 261, 77
     A, B = operands(M, N, K, "int4", seed=261)
-    C, name = run(tgemm, lambda: tgemm.gemm_tc(A.cuda(), B.cuda(), "tf32"))
+    C, name = run(tgemm, lambda: tgemm.gemm_tc(A.cuda(), B.cuda(), "tf32"), mode=3)
     assert KERNEL in name and "repack_a" in name and "repack_b" in name, name
     assert_bit_exact(C, oracle.gemm(A, B)[0], "unaligned")
 
@@ -111,7 +102,8 @@ def test_output_rows_and_guard_bands(tgemm, ldc, offset):
     store = torch.full((guard + offset + M * ldc + guard,), -555.0, device="cuda")
     base = guard + offset
     C = store[base:base + M * ldc].view(M, ldc)[:, :N]
-    run(tgemm, lambda: tgemm.gemm_tc(A.cuda(), B.cuda(), "tf32", out=C))
+    _, name = run(tgemm, lambda: tgemm.gemm_tc(A.cuda(), B.cuda(), "tf32", out=C), mode=3)
+    assert KERNEL in name, name
     assert_bit_exact(C, oracle.gemm(A, B)[0], f"ldc={ldc} offset={offset}")
     host = store.cpu()
     assert (host[:base] == -555.0).all() and (host[base + M * ldc:] == -555.0).all()
@@ -131,7 +123,7 @@ def test_full_output_rule_bit_exact(tgemm, ta):
     C = C0.clone().cuda()
     _, name = run(tgemm, lambda: tgemm.binding.gemm_ex(As.cuda(), B.cuda(), "tf32", trans_a=ta,
                                                        alpha=2.0, beta=-1.0, bias=bias.cuda(),
-                                                       out=C))
+                                                       out=C), mode=3)
     assert KERNEL in name, name
     ref, _ = oracle.gemm_ex(As, B, trans_a=ta, alpha=2.0, beta=-1.0, C0=C0, bias=bias)
     assert_bit_exact(C, ref, f"rule ta={ta}")
@@ -154,7 +146,7 @@ def test_stream_k_integer_bit_exact(tgemm, shape, slots):
 def test_float_tolerance(tgemm, slots):
     M, N, K = 100, 1100, 1531
     A, B = operands(M, N, K, "normal", seed=1531)
-    C, name = run(tgemm, lambda: tgemm.gemm_tc(A.cuda(), B.cuda(), "tf32"), slots=slots)
+    C, name = run(tgemm, lambda: tgemm.gemm_tc(A.cuda(), B.cuda(), "tf32"), mode=3, slots=slots)
     assert KERNEL in name, name
     C_ref, absAB = oracle.gemm(A, B)
     assert_within(C, C_ref, absAB, TC_REL, TC_ABS, f"float slots={slots}")
@@ -170,6 +162,7 @@ def test_stalled_pipeline_reports_timeout_and_recovers(tgemm):
     assert tgemm.device_status() == 0
     try:
         assert b.set_wait_limit_ns(50_000_000) == 0
+        assert b.set_tc_kernel(3) == 0
         b.set_debug_stall(True)
         t0 = time.time()
         tgemm.gemm_tc(Ad, Bd, "tf32")
@@ -178,6 +171,7 @@ def test_stalled_pipeline_reports_timeout_and_recovers(tgemm):
         name = b.last_kernel()
     finally:
         b.set_debug_stall(False)
+        b.set_tc_kernel(-1)
         b.set_wait_limit_ns(2_000_000_000)
     assert KERNEL in name, name
     assert st == b.TGEMM_ERR_DEVICE_TIMEOUT
@@ -195,6 +189,7 @@ def test_whole_chunk_widths_nan_padding(tgemm, M, N, K):
     32-column chunks; the chunks past N and the rows past K read as zeros,
     and the NaN padding of ldb (past N) is never read."""
     A, B = operands(M, N, K, "int4", seed=N + K)
-    C, name = run(tgemm, lambda: tgemm.gemm_tc(padded_cuda(A, K + 4), padded_cuda(B, N + 12), "tf32"))
+    C, name = run(tgemm, lambda: tgemm.gemm_tc(padded_cuda(A, K + 4), padded_cuda(B, N + 12), "tf32"),
+                  mode=3)
     assert KERNEL in name, name
     assert_bit_exact(C, oracle.gemm(A, B)[0], f"{M}x{N}x{K}")

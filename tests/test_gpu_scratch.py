@@ -97,29 +97,36 @@ def streamk_bytes(name):
     return 0
 
 
-def test_tf32_transposes_b(tgemm):
-    """TF32 with more than 128 rows of A writes B transposed, N x
-    round_up(K, 32) floats, plus the shared tail's partial tiles (and
-    stream-K counters) when the planner shares the two tiles among SM
-    pairs."""
+def test_tf32_reads_b_as_stored(tgemm):
+    """TF32 with B's rows on 16-byte boundaries reads B MN-major as stored:
+    no scratch beyond the shared tail's partial tiles (and stream-K
+    counters) when the planner shares the two tiles among SM pairs."""
     M, N, K = 200, 300, 1000
     A, B = int_operands(M, N, K, torch.float32, 3)
     n = tgemm.binding.scratch_bytes(A, B, "tf32")
     check_product(tgemm, A, B, "tf32")
-    bt = round_up(N * round_up(K, 32) * 4, 256)
-    assert n == bt + streamk_bytes(tgemm.binding.last_kernel()), tgemm.binding.last_kernel()
-
-
-def test_tf32_few_rows_read_b_in_place(tgemm):
-    """TF32 with at most 128 rows of A reads B as stored (the kernel
-    transposes it in shared memory): no scratch beyond a stream-K tail's."""
-    M, N, K = 100, 1000, 512
-    A, B = int_operands(M, N, K, torch.float32, 6)
-    n = tgemm.binding.scratch_bytes(A, B, "tf32")
-    check_product(tgemm, A, B, "tf32")
     name = tgemm.binding.last_kernel()
-    assert "btrans" in name and "transpose_b" not in name, name
+    assert "transpose_b" not in name and "repack" not in name, name
     assert n == streamk_bytes(name), name
+
+
+@pytest.mark.parametrize("M", [16, 100])
+def test_tf32_few_rows_read_b_in_place(tgemm, M):
+    """TF32 with at most 128 rows of A: no scratch beyond a stream-K tail's,
+    with the default kernel and with the one that transposes B's blocks in
+    shared memory (mode 3)."""
+    N, K = 1000, 512
+    A, B = int_operands(M, N, K, torch.float32, 6)
+    for mode in (-1, 3):
+        assert tgemm.binding.set_tc_kernel(mode) == 0
+        try:
+            n = tgemm.binding.scratch_bytes(A, B, "tf32")
+            check_product(tgemm, A, B, "tf32")
+            name = tgemm.binding.last_kernel()
+        finally:
+            tgemm.binding.set_tc_kernel(-1)
+        assert ("btrans" in name) == (mode == 3) and "transpose_b" not in name, name
+        assert n == streamk_bytes(name), name
 
 
 def test_unaligned_rows_are_repacked(tgemm):

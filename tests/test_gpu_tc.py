@@ -107,6 +107,34 @@ def test_both_kernels_integer_bit_exact(tgemm, tc_mode, kind, shape):
 
 
 @pytest.mark.parametrize("kind", ["tf32", "bf16"])
+@pytest.mark.parametrize("shape", [(129, 264, 72), (513, 1000, 136)])
+def test_both_kernels_b_stored_transposed(tgemm, tc_mode, kind, shape):
+    """B stored N x K: every tile shape reads it K-major (no copy), the
+    default K x N storage MN-major."""
+    M, N, K = shape
+    A, B = operands(M, N, K, "int4", kind, seed=3 * M + N + 7 * K)
+    C = tgemm.binding.gemm_ex(A.cuda(), B.t().contiguous().cuda(), kind, trans_b=True)
+    name = tgemm.binding.last_kernel()
+    assert tgemm.device_status() == 0
+    assert "transpose" not in name and "repack" not in name, name
+    assert_bit_exact(C, oracle.gemm(A, B)[0], f"{kind} {shape} B^T mode {tc_mode}")
+
+
+@pytest.mark.parametrize("kind", ["tf32", "bf16"])
+@pytest.mark.parametrize("N", [64, 256, 544, 1024, 1056, 1064])
+def test_b_column_chunks_nan_padding(tgemm, tc_mode, kind, N):
+    """B read MN-major: a tile whose columns are all whole 128-byte chunks
+    of B arrives as one 3-D copy, the last tile (past N rounded down to a
+    chunk) as 2-D copies per chunk. N whole chunks or not, on every tile
+    shape; ldb's NaN padding must never be read."""
+    M, K = 260, 100
+    A, B = operands(M, N, K, "int4", kind, seed=N + 17 * tc_mode)
+    C = tgemm.gemm_tc(padded_cuda(A, K + 8), padded_cuda(B, N + 40), kind)
+    assert tgemm.device_status() == 0
+    assert_bit_exact(C, oracle.gemm(A, B)[0], f"{kind} N={N} mode {tc_mode}")
+
+
+@pytest.mark.parametrize("kind", ["tf32", "bf16"])
 def test_both_kernels_ragged_nan_padding(tgemm, tc_mode, kind):
     M, N, K = 389, 301, 97
     A, B = operands(M, N, K, "int4", kind, seed=6)

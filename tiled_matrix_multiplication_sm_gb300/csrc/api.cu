@@ -244,13 +244,10 @@ int check_request(const Request& r) {
 }
 
 // TF32 with B stored K x N: the kernel that transposes B in shared memory
-// (128 x 128 tiles) instead of a transpose pre-pass and the 128 x 256 one-SM
-// kernel. Taken when forced (tensor-core mode 3) and, by default, when A has
-// at most 128 rows: such products are bound by reading B, which the
-// pre-pass would move through memory three times (16 x 14336 x 4096:
-// measured 139 us with the pre-pass).
-bool tf32_in_kernel_transpose(int M, int mode) {
-    return mode == 3 || (mode == -1 && M <= 128);
+// (128 x 128 tiles). Taken only when forced (tensor-core mode 3): the other
+// kernels read such a B MN-major as stored.
+bool tf32_in_kernel_transpose(int mode) {
+    return mode == 3;
 }
 
 // Plan a checked request with K > 0 on a device with dev.num_sms SMs.
@@ -277,10 +274,9 @@ int plan_product(const Request& r, const DeviceInfo& dev, ProductPlan& pp) {
     //   A: M x K K-major. Transposed storage -> transpose (all paths);
     //      X3 -> hi/lo split; tensor paths with rows off 16 bytes -> repack.
     //   B: F32: K x N row-major (transposed storage -> transpose).
-    //      BF16: K x N read MN-major, or N x K K-major when stored
-    //      transposed; rows off 16 bytes -> repack.
-    //      TF32: N x K K-major: transpose unless stored transposed (then
-    //      repack if needed). X3: hi/lo of the N x K form.
+    //      BF16, TF32: K x N read MN-major, or N x K K-major when stored
+    //      transposed; rows off 16 bytes -> repack. X3: hi/lo of the N x K
+    //      form.
     if (x3) {
         pp.prep_a = ta ? TRANSPOSE_SPLIT : SPLIT;
         pp.prep_b = tb ? SPLIT : TRANSPOSE_SPLIT;
@@ -295,27 +291,23 @@ int plan_product(const Request& r, const DeviceInfo& dev, ProductPlan& pp) {
         pp.prep_b = tb ? TRANSPOSE : (big && !aligned16(r.B, r.ldb) ? REPACK : NONE);
     } else {
         pp.prep_a = ta ? TRANSPOSE : (aligned16(r.A, r.lda) ? NONE : REPACK);
-        if (tf32 && !tb && tf32_in_kernel_transpose(M, g_tc_mode.load()))
+        if (tf32 && !tb && tf32_in_kernel_transpose(g_tc_mode.load()))
             pp.shape = tgemm::TC_ONE_SM_T;
         const bool b_t = pp.shape == tgemm::TC_ONE_SM_T;
-        if (tf32 && !b_t)
-            pp.prep_b = tb ? (aligned16(r.B, r.ldb) ? NONE : REPACK) : TRANSPOSE;
-        else     // bf16 (either storage), TF32 read as stored K x N
-            pp.prep_b = aligned16(r.B, r.ldb) ? NONE : REPACK;
+        pp.prep_b = aligned16(r.B, r.ldb) ? NONE : REPACK;
         // A whose rows are 4-byte but not 16-byte aligned: repacked, or read
-        // in place by the GEMM kernel's loader warps (TF32 with B K-major, and
-        // BF16 with B read MN-major). The repack is the default: measured faster.
+        // in place by the GEMM kernel's loader warps (TF32 with B either way,
+        // and BF16 with B read MN-major). The repack is the default: measured faster.
         const bool rows4 = reinterpret_cast<uintptr_t>(r.A) % 4 == 0 && (r.lda * (long)esz) % 4 == 0;
-        const bool b_mn = !(tb || tf32);
-        if (pp.prep_a == REPACK && rows4 && ((tf32 && !b_t) || (bf16 && b_mn)) &&
+        if (pp.prep_a == REPACK && rows4 && ((tf32 && !b_t) || (bf16 && !tb)) &&
             g_tc_a_loader.load() == 1) {
             pp.prep_a = NONE;
             pp.a_loader = true;
         }
     }
-    // Tensor paths: B read K-major, except BF16 and the transposing TF32
-    // kernel with B stored K x N.
-    pp.b_kmajor = tb || x3 || (tf32 && pp.shape != tgemm::TC_ONE_SM_T);
+    // Tensor paths: B read K-major when stored transposed (and always by the
+    // split form), otherwise MN-major as stored.
+    pp.b_kmajor = tb || x3;
     // Layout the GEMM reads: A M x K (ld_a), B K x N or N x K (ld_b).
     pp.ld_a = pp.prep_a == NONE ? r.lda : pp.ldk;
     pp.ld_b = pp.prep_b == NONE ? r.ldb : ((f32 || !pp.b_kmajor) ? pp.ldn : pp.ldk);
@@ -453,14 +445,10 @@ int run_product(const Request& r, cudaStream_t stream) {
             break;
     }
     switch (pp.prep_b) {
-        case TRANSPOSE:
+        case TRANSPOSE:     // FP32 only: stored N x K -> K x N
             a.B = base + b_off;
-            if (f32)     // stored N x K -> K x N
-                ok(tgemm::transpose_f32(static_cast<const float*>(r.B), r.ldb,
-                                        reinterpret_cast<float*>(base + b_off), ldn, N, K, stream));
-            else         // TF32: stored K x N -> N x K
-                ok(tgemm::transpose_f32(static_cast<const float*>(r.B), r.ldb,
-                                        reinterpret_cast<float*>(base + b_off), ldk, K, N, stream));
+            ok(tgemm::transpose_f32(static_cast<const float*>(r.B), r.ldb,
+                                    reinterpret_cast<float*>(base + b_off), ldn, N, K, stream));
             note("transpose_b+");
             break;
         case REPACK:
@@ -605,9 +593,9 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
     // width, a multiple of 256 columns (0: B in one piece).
     const long nh = (path == TGEMM_PATH_F32 && panels > 1 && K > 0) ? (long)(N / 2) / 256 * 256 : 0;
 
-    // Plans and scratch: one pool block for A, B, C, B transposed (TF32: one
-    // copy; TF32X3: its high and low parts), the high and low parts of A
-    // (TF32X3), partials.
+    // Plans and scratch: one pool block for A, B, C, B's high and low parts
+    // transposed and the high and low parts of A (TF32X3), partials. BF16 and
+    // TF32 read the device copy of B MN-major as uploaded.
     const bool tc = path != TGEMM_PATH_F32;
     const bool x3 = path == TGEMM_PATH_TF32X3;
     const int in_type = path == TGEMM_PATH_BF16 ? TGEMM_BF16 : x3 ? TGEMM_TF32X3 : TGEMM_TF32;
@@ -617,7 +605,7 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
     size_t off_b = a_bytes;
     size_t off_c = off_b + align256((size_t)K * ldb_d * esz);
     size_t off_t = off_c + align256((size_t)M * ldc_d * 4);
-    size_t off_a2 = off_t + (path == TGEMM_PATH_TF32 ? bt_bytes : x3 ? 2 * bt_bytes : 0);
+    size_t off_a2 = off_t + (x3 ? 2 * bt_bytes : 0);
     size_t off_p = off_a2 + (x3 ? 2 * a_bytes : 0);
     int f32_id[kMaxPanels] = {}, f32_id_right = 0;
     tgemm::F32Plan f32_plan[kMaxPanels], f32_plan_right;
@@ -714,8 +702,6 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
         }
     }
     ok(cudaStreamWaitEvent(stream, nh > 0 ? ev_b_left : ev_b, 0));
-    if (rc == TGEMM_OK && path == TGEMM_PATH_TF32 && K > 0)
-        ok(tgemm::transpose_f32(reinterpret_cast<const float*>(Bd), ldb_d, Bt, ldt, K, N, stream));
     if (rc == TGEMM_OK && x3 && K > 0)
         ok(tgemm::transpose_split_tf32(reinterpret_cast<const float*>(Bd), ldb_d, Bt, Bt_lo, ldt,
                                        K, N, stream));
@@ -741,11 +727,8 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
                                 tc_plan[i], part, stream));
             name = tgemm::tc_kernel_name(in_type, shape[i]);
         } else if (tc) {
-            const bool tf32 = path == TGEMM_PATH_TF32;
-            tgemm::GemmArgs pa{rows, N, K, Ad + r0 * lda_d * esz, lda_d,
-                               tf32 ? static_cast<const void*>(Bt) : Bd, tf32 ? ldt : ldb_d, Cp,
-                               ldc_d};
-            ok(tgemm::tc_launch(pa, in_type, tf32 ? 1 : 0, enc, limit, stall, shape[i],
+            tgemm::GemmArgs pa{rows, N, K, Ad + r0 * lda_d * esz, lda_d, Bd, ldb_d, Cp, ldc_d};
+            ok(tgemm::tc_launch(pa, in_type, 0, enc, limit, stall, shape[i],
                                 tc_plan[i], part, stream));
             name = tgemm::tc_kernel_name(in_type, shape[i]);
         } else if (i == 0 && nh > 0) {
@@ -783,9 +766,7 @@ int gemm_host(int M, int N, int K, const void* A, long lda, const void* B, long 
     if (rc == TGEMM_OK) {
         snprintf(g_last_kernel_buf, sizeof(g_last_kernel_buf), "host_pipeline(panels=%d)+%s%s",
                  panels,
-                 K == 0 ? ""
-                 : path == TGEMM_PATH_TF32 ? "transpose_b+"
-                 : x3 ? "transpose_split_b+split_a+" : "",
+                 K == 0 || !x3 ? "" : "transpose_split_b+split_a+",
                  name);
         g_last_kernel = g_last_kernel_buf;
     }

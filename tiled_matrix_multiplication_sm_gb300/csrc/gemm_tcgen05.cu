@@ -149,6 +149,10 @@ struct TcParams {
     const void* a_ptr;
     long lda_bytes;
     int a_esz;
+    // B read MN-major: columns [0, b3d_cols) are also described by a 3-D
+    // tensor map (128-byte column chunks as its third dimension), so that a
+    // tile's chunks arrive in one copy; 0 = no such map.
+    int b3d_cols;
 };
 
 // One output under the rule (C_old read only when beta != 0).
@@ -326,6 +330,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// A 3-D box: B's column chunks (x: column in the chunk, y: K row, z: chunk).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
 // TMA store of a box from shared memory (completion tracked by bulk groups).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
@@ -387,6 +401,15 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];"
         :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                                 int z, uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster)
         : "memory");
 }
 
@@ -466,16 +489,30 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     tmem_wait_ld(r);
 }
 
-// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start
-// address, leading and stride byte offsets in 16-byte units, version 1).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+// Shared-memory matrix descriptor (tcgen05 format: start address, leading
+// and stride byte offsets in 16-byte units, version 1, layout type): layout
+// 2 is the 128-byte swizzle, layout 1 the 128-byte swizzle with 32-byte atoms.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t layout = 2) {
     uint64_t d = 0;
     d |= (uint64_t)((addr & 0x3FFFF) >> 4);
     d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
     d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
     d |= 1ull << 46;                     // descriptor version for tcgen05
-    d |= 2ull << 61;                     // 128-byte swizzle
+    d |= (uint64_t)layout << 61;
     return d;
+}
+
+// Descriptor of B read MN-major: chunks of 128-byte rows (SW / ESZ columns
+// each, one row per K) `chunk_bytes` apart along N. BF16 takes the 128-byte
+// swizzle, rows grouped by 8 (1024 bytes); TF32 takes the 128-byte swizzle
+// with 32-byte atoms (the tensor map's SWIZZLE_128B_ATOM_32B: each row's four
+// 32-byte pieces permuted by the row index mod 4), rows grouped by 4 (512
+// bytes). The TF32 form was measured on this GPU: a 128 x 64 x 32 integer
+// product through it is exact, and the other offset choices are not.
+template <int ESZ>
+__device__ __forceinline__ uint64_t b_mn_desc(uint32_t addr, uint32_t chunk_bytes) {
+    return ESZ == 4 ? smem_desc(addr, chunk_bytes, 512, 1) : smem_desc(addr, chunk_bytes, 1024, 2);
 }
 
 // Instruction descriptor: FP32 accumulator, A K-major, B K-major or
@@ -972,6 +1009,7 @@ template <int ESZ, bool B_KMAJOR, bool A_LOADER = false, int TBN = BN>
 __global__ void __launch_bounds__(NUM_THREADS + (A_LOADER ? 32 * A_LOADER_WARPS : 0), 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmB3,
                const __grid_constant__ CUtensorMap tmC,
                const TcParams p) {
     using KD = Kind<ESZ>;
@@ -1053,6 +1091,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const uint32_t bdst = b_base + s * B_STAGE_BYTES;
                     if constexpr (B_KMAJOR) {
                         tma_load_2d(bdst, &tmB, kb * BK, nb * TBN, full);
+                    } else if ((nb + 1) * TBN <= p.b3d_cols) {
+                        tma_load_3d(bdst, &tmB3, 0, kb * BK, nb * B_CHUNKS, full);
                     } else {
 #pragma unroll
                         for (int c = 0; c < B_CHUNKS; ++c)
@@ -1095,7 +1135,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const uint64_t ad = smem_desc(a_addr + kk * A_K_STEP, 16, 1024);
                         const uint64_t bd =
                             B_KMAJOR ? smem_desc(b_addr + kk * A_K_STEP, 16, 1024)
-                                     : smem_desc(b_addr + kk * B_K_STEP, B_CHUNK_BYTES, 1024);
+                                     : b_mn_desc<ESZ>(b_addr + kk * B_K_STEP, B_CHUNK_BYTES);
                         tc_mma<ESZ>(d_tmem, ad, bd, IDESC, (kb != w.kb0 || kk != 0) ? 1u : 0u);
                     }
                     tc_commit(smem_u32(&sy->empty[s]));      // frees the slot when done
@@ -1597,6 +1637,8 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
                             const int ch = col0 + h * BN;
                             if constexpr (B_KMAJOR) {
                                 tma_load_2d_pair(bh, &tmB, kb * BK, ch, full);
+                            } else if (ch + 128 <= p.b3d_cols) {   // the 3-D map (in tmB2)
+                                tma_load_3d_pair(bh, &tmB2, 0, kb * BK, ch / B_CHUNK_COLS, full);
                             } else {
 #pragma unroll
                                 for (int c = 0; c < B_CHUNKS; ++c)
@@ -1656,7 +1698,7 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
                             const uint32_t bh = b_addr + h * P_B_TILE;
                             const uint64_t bdh =
                                 B_KMAJOR ? smem_desc(bh + kk * A_K_STEP, 16, 1024)
-                                         : smem_desc(bh + kk * B_K_STEP, B_CHUNK_BYTES, 1024);
+                                         : b_mn_desc<ESZ>(bh + kk * B_K_STEP, B_CHUNK_BYTES);
                             tc_mma_pair<ESZ>(d_tmem + (uint32_t)(h * BN), ad, bdh, IDESC, first);
                         }
                     }
@@ -1821,7 +1863,8 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 // 2-D row-major tensor map: `cols` contiguous elements per row, `rows`
 // rows `ld` elements apart; boxes of box_cols x box_rows, 128-byte swizzle.
 bool encode_2d(EncodeTiledFn enc, CUtensorMap* map, const void* base, int esz, long rows,
-               long cols, long ld, int box_cols, int box_rows) {
+               long cols, long ld, int box_cols, int box_rows,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     const CUtensorMapDataType dt =
         esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
@@ -1829,9 +1872,37 @@ bool encode_2d(EncodeTiledFn enc, CUtensorMap* map, const void* base, int esz, l
     cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// The same B as a 3-D tensor: x a column within a 128-byte chunk, y the K
+// row, z the chunk (whole chunks only: floor(N / chunk columns)), boxes of
+// `chunks` chunks. Returns the columns it covers, 0 when it cannot be made.
+long encode_b_mn3(EncodeTiledFn enc, CUtensorMap* map, const GemmArgs& a, int esz, int bk,
+                  int chunks) {
+    const long ch = SW / esz;
+    const long nc = a.N / ch;
+    if (nc < 1) return 0;
+    cuuint64_t dims[3] = {(cuuint64_t)ch, (cuuint64_t)a.K, (cuuint64_t)nc};
+    cuuint64_t strides[2] = {(cuuint64_t)a.ldb * esz, (cuuint64_t)SW};
+    cuuint32_t box[3] = {(cuuint32_t)ch, (cuuint32_t)bk, (cuuint32_t)chunks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt =
+        esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    CUresult r = enc(map, dt, 3, const_cast<void*>(a.B), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     esz == 4 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? nc * ch : 0;
+}
+
+// B read MN-major (K x N, N contiguous) in boxes of SW / esz columns x BK
+// rows, with the swizzle b_mn_desc expects for the element size.
+bool encode_b_mn(EncodeTiledFn enc, CUtensorMap* map, const GemmArgs& a, int esz, int bk) {
+    return encode_2d(enc, map, a.B, esz, a.K, a.N, a.ldb, SW / esz, bk,
+                     esz == 4 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 TcParams make_params(const GemmArgs& a, const TcPlan& pl, void* scratch, int arrivals,
@@ -1852,6 +1923,7 @@ TcParams make_params(const GemmArgs& a, const TcPlan& pl, void* scratch, int arr
     p.partials = nullptr;
     p.sk_flags = nullptr;
     p.sk_split = pl.sk_split;
+    p.b3d_cols = 0;
     if (pl.sk_slots > 0) {
         p.partials = static_cast<float*>(scratch);
         if (!pl.sk_split)
@@ -1973,9 +2045,11 @@ cudaError_t launch_tc(const GemmArgs& a, const TcPlan& pl, void* scratch, Encode
     if (!A_LOADER && !encode_2d(enc, &tmA, a.A, ESZ, a.M, a.K, a.lda, BK, BM))
         return cudaErrorInvalidValue;
     const bool okb = B_KMAJOR ? encode_2d(enc, &tmB, a.B, ESZ, a.N, a.K, a.ldb, BK, TBN)
-                              : encode_2d(enc, &tmB, a.B, ESZ, a.K, a.N, a.ldb, SW / ESZ, BK);
+                              : encode_b_mn(enc, &tmB, a, ESZ, BK);
     if (!okb) return cudaErrorInvalidValue;
+    CUtensorMap tmB3 = tmB;
     TcParams p = make_params(a, pl, scratch, 4, wait_limit_ns, debug_stall);
+    if (!B_KMAJOR) p.b3d_cols = (int)encode_b_mn3(enc, &tmB3, a, ESZ, BK, TBN / (SW / ESZ));
     CUtensorMap tmC;
     encode_c(enc, &tmC, a, p);
     p.row_copy = (!p.tma_c && a.ep.beta == 0.0f) ? 1 : 0;
@@ -1987,7 +2061,7 @@ cudaError_t launch_tc(const GemmArgs& a, const TcPlan& pl, void* scratch, Encode
     cudaError_t e = set_smem_limit_once<tc_gemm_kernel<ESZ, B_KMAJOR, A_LOADER, TBN>>(SMEM_BYTES);
     if (e != cudaSuccess) return e;
     kern<<<grid_slots(pl), NUM_THREADS + (A_LOADER ? 32 * A_LOADER_WARPS : 0), SMEM_BYTES, s>>>(
-        tmA, tmB, tmC, p);
+        tmA, tmB, tmB3, tmC, p);
     e = cudaGetLastError();
     return e != cudaSuccess ? e : launch_split_reduce(p, s);
 }
@@ -2025,7 +2099,7 @@ cudaError_t launch_tc_pair(const GemmArgs& a, const TcPlan& pl, void* scratch, E
     if (!A_LOADER && !encode_2d(enc, &tmA, a.A, ESZ, a.M, a.K, a.lda, BK, 128))
         return cudaErrorInvalidValue;
     const bool okb = B_KMAJOR ? encode_2d(enc, &tmB, a.B, ESZ, a.N, a.K, a.ldb, BK, 128)
-                              : encode_2d(enc, &tmB, a.B, ESZ, a.K, a.N, a.ldb, SW / ESZ, BK);
+                              : encode_b_mn(enc, &tmB, a, ESZ, BK);
     if (!okb) return cudaErrorInvalidValue;
     if constexpr (X3) {
         if (!encode_2d(enc, &tmA2, a.A2, ESZ, a.M, a.K, a.lda, BK, 128) ||
@@ -2036,6 +2110,8 @@ cudaError_t launch_tc_pair(const GemmArgs& a, const TcPlan& pl, void* scratch, E
         tmB2 = tmB;
     }
     TcParams p = make_params(a, pl, scratch, 2 * PairEpi<NW>::WARPS, wait_limit_ns, debug_stall);
+    if (!X3 && !B_KMAJOR)    // the 3-D map of B rides in tmB2 (unused by the one-product forms)
+        p.b3d_cols = (int)encode_b_mn3(enc, &tmB2, a, ESZ, BK, 128 / (SW / ESZ));
     CUtensorMap tmC;
     encode_c(enc, &tmC, a, p);
     // The wide tiles' epilogue region has no room for row slots.
@@ -2410,8 +2486,8 @@ cudaError_t tc_launch(const GemmArgs& a, int in_type, int b_kmajor, void* encode
         if (in_type == TC_BF16)
             return b_kmajor ? launch_tc<2, true, false, TT_BN>(a, pl, scratch, enc, w, st, s)
                             : launch_tc<2, false, false, TT_BN>(a, pl, scratch, enc, w, st, s);
-        if (!b_kmajor) return cudaErrorInvalidValue;    // TF32 reads B K-major only
-        return launch_tc<4, true, false, TT_BN>(a, pl, scratch, enc, w, st, s);
+        return b_kmajor ? launch_tc<4, true, false, TT_BN>(a, pl, scratch, enc, w, st, s)
+                        : launch_tc<4, false, false, TT_BN>(a, pl, scratch, enc, w, st, s);
     }
     if (shape == TC_ONE_SM_T) {
         if (in_type != TC_TF32 || b_kmajor || a.a_loader || pl.tile_cols != TT_BN)
@@ -2421,25 +2497,27 @@ cudaError_t tc_launch(const GemmArgs& a, int in_type, int b_kmajor, void* encode
     if (pl.tile_cols == TT_BN && pl.tile_rows == BM) return cudaErrorInvalidValue;
     if ((shape == TC_PAIR_WIDE) != (pl.tile_cols == 2 * BN)) return cudaErrorInvalidValue;
     if (a.a_loader) {
-        // A read by the loader warps: TF32 (B K-major) and BF16 with B MN-major.
-        const bool tf32 = in_type == TC_TF32 && b_kmajor;
-        const bool bf16 = in_type == TC_BF16 && !b_kmajor;
-        if (!tf32 && !bf16) return cudaErrorInvalidValue;
+        // A read by the loader warps: TF32 (B either way) and BF16 with B MN-major.
+        if (in_type == TC_BF16 && b_kmajor) return cudaErrorInvalidValue;
+        const int form = in_type == TC_BF16 ? 0 : (b_kmajor ? 1 : 2);
         if (shape == TC_PAIR_WIDE)
-            return tf32 ? launch_tc_pair<4, true, false, 2, true>(a, pl, scratch, enc, w, st, s)
-                        : launch_tc_pair<2, false, false, 2, true>(a, pl, scratch, enc, w, st, s);
+            return form == 0 ? launch_tc_pair<2, false, false, 2, true>(a, pl, scratch, enc, w, st, s)
+                 : form == 1 ? launch_tc_pair<4, true, false, 2, true>(a, pl, scratch, enc, w, st, s)
+                             : launch_tc_pair<4, false, false, 2, true>(a, pl, scratch, enc, w, st, s);
         if (shape == TC_PAIR)
-            return tf32 ? launch_tc_pair<4, true, false, 1, true>(a, pl, scratch, enc, w, st, s)
-                        : launch_tc_pair<2, false, false, 1, true>(a, pl, scratch, enc, w, st, s);
-        return tf32 ? launch_tc<4, true, true>(a, pl, scratch, enc, w, st, s)
-                    : launch_tc<2, false, true>(a, pl, scratch, enc, w, st, s);
+            return form == 0 ? launch_tc_pair<2, false, false, 1, true>(a, pl, scratch, enc, w, st, s)
+                 : form == 1 ? launch_tc_pair<4, true, false, 1, true>(a, pl, scratch, enc, w, st, s)
+                             : launch_tc_pair<4, false, false, 1, true>(a, pl, scratch, enc, w, st, s);
+        return form == 0 ? launch_tc<2, false, true>(a, pl, scratch, enc, w, st, s)
+             : form == 1 ? launch_tc<4, true, true>(a, pl, scratch, enc, w, st, s)
+                         : launch_tc<4, false, true>(a, pl, scratch, enc, w, st, s);
     }
     if (shape == TC_PAIR_WIDE) {
         if (in_type == TC_BF16)
             return b_kmajor ? launch_tc_pair<2, true, false, 2>(a, pl, scratch, enc, w, st, s)
                             : launch_tc_pair<2, false, false, 2>(a, pl, scratch, enc, w, st, s);
-        if (!b_kmajor) return cudaErrorInvalidValue;    // TF32 reads B K-major only
-        return launch_tc_pair<4, true, false, 2>(a, pl, scratch, enc, w, st, s);
+        return b_kmajor ? launch_tc_pair<4, true, false, 2>(a, pl, scratch, enc, w, st, s)
+                        : launch_tc_pair<4, false, false, 2>(a, pl, scratch, enc, w, st, s);
     }
     if (shape == TC_PAIR) {
         if (in_type == TC_BF16)

@@ -1,9 +1,10 @@
 // gemm_tc_tf32_noalloc: the TF32 tensor-core product for callers that must
 // not allocate device memory.
 //
-// gemm_tc with TGEMM_TF32 needs scratch memory for B transposed (the TF32
-// kind of the tensor-core instruction reads B only K-major) and draws it from
-// a stream-ordered memory pool. Some callers cannot let a library allocate:
+// gemm_tc with TGEMM_TF32 draws scratch memory from a stream-ordered memory
+// pool when an operand's rows are not 16-byte aligned (a repacked copy) and
+// when the last wave of tiles is split (partial tiles). Some callers cannot
+// let a library allocate:
 // an application or plugin that reserves all of its device memory up front
 // and treats any later allocation as a failure, or code that must not touch
 // the device allocator while it runs. This entry point gives them the same
@@ -11,12 +12,13 @@
 // memory (TGEMM_NOALLOC_SCRATCH_FLOATS floats, 16 MiB). Every device that
 // loads the library holds that array until the process exits.
 //
-// It runs the same two kernels as gemm_tc's TF32 path (transpose of B, then
-// the persistent tcgen05 GEMM), through the same launchers; only the
-// scratch differs. The transposed rows of B are round_up(K, 32) floats apart
-// (128 bytes, as gemm_tc's scratch: the TF32 kernel ran 16 % slower on rows
-// only 16 bytes aligned) when N of them fit the array, else round_up(K, 4)
-// floats apart (16 bytes, the least the tensor-memory copies accept).
+// With B's rows 16-byte aligned it runs gemm_tc's TF32 kernel alone, B read
+// as stored (MN-major), and touches no scratch. Otherwise B is first
+// transposed into the array and read K-major; the transposed rows are
+// round_up(K, 32) floats apart (128 bytes, as gemm_tc's scratch: the TF32
+// kernel ran 16 % slower on rows only 16 bytes aligned) when N of them fit
+// the array, else round_up(K, 4) floats apart (16 bytes, the least the
+// tensor-memory copies accept). The last wave is never split.
 // Nothing in the scratch has to start at zero: each call writes the N x K
 // block it reads before reading it, and the padding columns are never read.
 // All calls share the one array, so calls whose work overlaps on the GPU
@@ -105,10 +107,12 @@ extern "C" int gemm_tc_tf32_noalloc(int M, int N, int K, const float* A, long ld
     if (C == nullptr || reinterpret_cast<uintptr_t>(C) % 4 != 0) return TGEMM_ERR_INVALID_ARG;
     if (K > 0 && (A == nullptr || B == nullptr)) return TGEMM_ERR_INVALID_ARG;
     if ((long)K > kMaxK) return TGEMM_ERR_INVALID_ARG;
-    // Row pitch of B transposed: 128-byte rows when they fit, else 16-byte rows.
+    // B with 16-byte rows is read as stored; otherwise transposed into the
+    // array, 128-byte rows when they fit, else 16-byte rows.
+    const bool b_direct = reinterpret_cast<uintptr_t>(B) % 16 == 0 && (ldb * 4) % 16 == 0;
     long ldt = ((long)K + 31) / 32 * 32;
     if ((long long)N * ldt > (long long)TGEMM_NOALLOC_SCRATCH_FLOATS) ldt = ((long)K + 3) / 4 * 4;
-    if (ldt <= 0 || (long long)N * ldt > (long long)TGEMM_NOALLOC_SCRATCH_FLOATS)
+    if (!b_direct && (ldt <= 0 || (long long)N * ldt > (long long)TGEMM_NOALLOC_SCRATCH_FLOATS))
         return TGEMM_ERR_INVALID_ARG;
     if (K > 0 && (reinterpret_cast<uintptr_t>(A) % 16 != 0 || reinterpret_cast<uintptr_t>(B) % 4 != 0 ||
                   (lda * 4) % 16 != 0))
@@ -122,16 +126,16 @@ extern "C" int gemm_tc_tf32_noalloc(int M, int N, int K, const float* A, long ld
                    ? TGEMM_OK : TGEMM_ERR_CUDA;
     void* enc = encoder();
     if (enc == nullptr) return TGEMM_ERR_CUDA;
-    if (tgemm::transpose_f32(B, ldb, d.scratch, ldt, K, N, stream) != cudaSuccess)
+    if (!b_direct && tgemm::transpose_f32(B, ldb, d.scratch, ldt, K, N, stream) != cudaSuccess)
         return TGEMM_ERR_CUDA;
-    tgemm::GemmArgs a{M, N, K, A, lda, d.scratch, ldt, C, ldc};
+    tgemm::GemmArgs a{M, N, K, A, lda, b_direct ? B : d.scratch, b_direct ? ldb : ldt, C, ldc};
     const bool tma_c = reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 4 == 0 && N % 4 == 0;
     const int shape = tgemm::tc_shape(M, N, K, tgemm::TC_TF32, -1, d.num_sms, 0, tma_c);
     // No stream-K tail: its partial tiles would need more scratch.
     const tgemm::TcPlan plan =
         tgemm::tc_plan(M, N, K, tgemm::TC_TF32, shape, d.num_sms, 0, tma_c);
-    if (tgemm::tc_launch(a, tgemm::TC_TF32, 1, enc, tgemm::wait_limit_ns(), 0, shape, plan, nullptr,
-                         stream) != cudaSuccess)
+    if (tgemm::tc_launch(a, tgemm::TC_TF32, b_direct ? 0 : 1, enc, tgemm::wait_limit_ns(), 0, shape,
+                         plan, nullptr, stream) != cudaSuccess)
         return TGEMM_ERR_CUDA;
     return TGEMM_OK;
 }
