@@ -3,8 +3,8 @@
 A step is one pass of the whole hot path over one batch of synthetic input:
 the square 4096^3 product (A, B ~ N(0,1) fp32, row-major) computed once on
 each path of the library -- the FP32 CUDA-core SGEMM (gemm_f32) and the
-tcgen05 tensor-core GEMM in TF32 (gemm_tc; a B-transpose pre-pass plus the
-GEMM). The metric is TFLOP/s = (2 M N K per product x 2 products) / device
+tcgen05 tensor-core GEMM in TF32 (gemm_tc; one kernel, B read MN-major as
+stored). The metric is TFLOP/s = (2 M N K per product x 2 products) / device
 time, timed with CUDA events on the launching stream, L2 flushed before
 every timed step (a 256 MiB write, then a 256 MiB read of another buffer, so
 that the timed kernels start on a cold L2 holding no dirty lines).

@@ -32,12 +32,12 @@
 // columns outside the matrices with zeros; stores past M and N are skipped
 // (TMA stores clip them).
 //
-// Operand layouts in shared memory: A (M x K, K contiguous) is K-major. For
-// BF16, B (K x N, N contiguous) is read MN-major through the instruction
-// descriptor's transpose bit, so neither operand is copied. The TF32 kind
-// reads B only K-major (with the MN-major bit set it produced zeros on
-// sm_103a), so the TF32 path hands this kernel B already transposed
-// (N x K, K contiguous) and reads it K-major like A.
+// Operand layouts in shared memory: A (M x K, K contiguous) is K-major. B
+// (K x N, N contiguous) is read MN-major through the instruction
+// descriptor's transpose bit, so neither operand is copied: BF16 in the
+// 128-byte swizzle, TF32 in the 128-byte swizzle with 32-byte atoms (with
+// the plain 128-byte swizzle the TF32 kind produced zeros on sm_103a). A B
+// stored transposed (N x K, K contiguous) is read K-major like A.
 //
 // Every wait is bounded (a limit in nanoseconds, default 2 s). A wait that
 // runs out records TGEMM_ERR_DEVICE_TIMEOUT in a device status word and
@@ -1196,11 +1196,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 }
 
 // ===================================================================
-// TF32 with few rows (one SM, M <= 128) and B as the caller stores it
-// (K x N, N contiguous). The TF32 kind reads B only K-major, and for such
-// products a transpose pre-pass would move B through HBM three times (read,
-// write, read) while the product itself is bound by reading B once. Here B
-// is transposed inside the kernel instead: TMA lands each stage's 32 x 128
+// TF32 with B as the caller stores it (K x N, N contiguous), transposed in
+// shared memory to be read K-major (tensor-core mode 3 only). It was built
+// for products with few rows before the TF32 kind's MN-major read (the
+// 128-byte swizzle with 32-byte atoms) was found; the one-SM kernel reading
+// B MN-major now serves them faster. TMA lands each stage's 32 x 128
 // block of B in the stage's own B slot in the MN-major layout it has in
 // memory (boxes of 32 columns x 32 K rows, 128-byte swizzle) next to the
 // stage's A block; both land on the stage's `landed` barrier. Two transposer

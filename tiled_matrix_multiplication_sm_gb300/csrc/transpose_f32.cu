@@ -1,9 +1,10 @@
 // Out-of-place transpose of an FP32 matrix: Bt[n][k] = B[k][n].
 //
-// The TF32 kind of the tcgen05 tensor-core instruction reads its B operand
-// only K-major (measured on sm_103a: with the MN-major bit set it produces
-// zeros), while the library's B is row-major K x N. The TF32 path therefore
-// first writes B transposed (N x K, K contiguous) into scratch memory.
+// Storage a path's kernel does not read directly is rewritten here: A (or,
+// on the FP32 path, B) stored transposed by gemm_ex, the split form's B
+// (its high and low TF32 parts, read K-major), and the B that the
+// allocation-free TF32 entry point reads K-major when B's rows are not
+// 16-byte aligned.
 //
 // Both kernels here are pure data movement, bound by HBM bandwidth. The
 // transpose reads every element once and writes it once
