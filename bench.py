@@ -86,13 +86,13 @@ def file_sha256(path: str) -> str:
 def committed_traffic(records=NCU_RECORDS, case="n4096:f32", kernel="sgemm_kernel", root=ROOT):
     """DRAM bytes (read + write) of one launch of `kernel` in `case`, from the
     committed ncu evidence record, or None when there is none or the kernel's
-    source changed since it was taken."""
+    code changed since it was taken (comments aside)."""
     from tiled_matrix_multiplication_sm_gb300 import evidence
     rec = evidence.find_record(records, case, kernel)
     if rec is None or not rec.get("source"):
         return None
     try:
-        if rec.get("source_sha256") != file_sha256(os.path.join(root, rec["source"])):
+        if not evidence.record_current(rec, root):
             return None
         return int(rec["derived"]["dram_bytes"])
     except (OSError, KeyError, TypeError, ValueError):

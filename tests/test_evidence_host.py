@@ -84,3 +84,34 @@ def test_every_case_names_a_workload():
         wl, path, M, N, K, dtype = evidence.case_shape(case)
         assert path in ("f32", "tf32", "bf16", "tf32x3")
         assert (wl is None) == (K == 0)
+
+
+def test_code_hash_ignores_comments_and_layout_only(tmp_path):
+    """A record stays current while only comments or layout change, and
+    goes stale when the code does; "//" inside a string is code."""
+    src = tmp_path / "k.cu"
+    src.write_text('// header\n__global__ void k(float* p) {  /* body */\n'
+                   '    const char* s = "a // b";\n    p[0] = 1.0f;  // store\n}\n')
+    h = evidence.code_sha256(str(src))
+    src.write_text('// a new header\n// more words\n__global__ void k(float* p) {\n'
+                   '    const char* s = "a // b";   /* moved */\n        p[0] = 1.0f;\n}\n')
+    assert evidence.code_sha256(str(src)) == h
+    src.write_text('__global__ void k(float* p) {\n    const char* s = "a // c";\n    p[0] = 1.0f;\n}\n')
+    assert evidence.code_sha256(str(src)) != h
+    src.write_text('__global__ void k(float* p) {\n    const char* s = "a // b";\n    p[0] = 2.0f;\n}\n')
+    assert evidence.code_sha256(str(src)) != h
+
+
+def test_record_current_prefers_the_code_hash(tmp_path):
+    src = tmp_path / "k.cu"
+    src.write_text("int f() { return 1; } // v1\n")
+    rec = {"source": "k.cu", "source_sha256": evidence.file_sha256(str(src)),
+           "code_sha256": evidence.code_sha256(str(src))}
+    assert evidence.record_current(rec, str(tmp_path))
+    src.write_text("int f() { return 1; } // v2, a comment edit\n")
+    assert evidence.record_current(rec, str(tmp_path))
+    old = {"source": "k.cu", "source_sha256": rec["source_sha256"]}     # whole-file hash only
+    assert not evidence.record_current(old, str(tmp_path))
+    src.write_text("int f() { return 2; }\n")
+    assert not evidence.record_current(rec, str(tmp_path))
+    assert not evidence.record_current({"source": "gone.cu", "code_sha256": "x"}, str(tmp_path))

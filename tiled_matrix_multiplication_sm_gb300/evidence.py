@@ -106,6 +106,55 @@ def file_sha256(path: str) -> str:
     return h.hexdigest()
 
 
+def strip_comments(text: str) -> str:
+    """C/C++/CUDA source without its comments, whitespace runs collapsed to
+    one space: what the compiler sees, so that a record stays current while
+    only the comments of its kernel's file change. String and character
+    literals are kept as they are (a "//" inside one is not a comment)."""
+    out = []
+    i, n = 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == "/" and i + 1 < n and text[i + 1] == "/":
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+            out.append(" ")
+        elif c == "/" and i + 1 < n and text[i + 1] == "*":
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def code_sha256(path: str) -> str:
+    """SHA-256 of a source file's code with comments and layout removed."""
+    with open(path, encoding="utf-8") as f:
+        return hashlib.sha256(strip_comments(f.read()).encode()).hexdigest()
+
+
+def record_current(rec: dict, root: str = None) -> bool:
+    """Whether the kernel source a record names still has the code it was
+    taken from (by the comment-free hash; records that carry only the
+    whole-file hash are compared by that)."""
+    if not rec.get("source"):
+        return False
+    path = os.path.join(root or ROOT, rec["source"])
+    if not os.path.exists(path):
+        return False
+    if rec.get("code_sha256"):
+        return code_sha256(path) == rec["code_sha256"]
+    return file_sha256(path) == rec.get("source_sha256")
+
+
 def short_name(kernel_name: str) -> str:
     """The kernel's function name without namespaces and template arguments:
     the first identifier of the demangled name that is followed by a template
@@ -302,6 +351,7 @@ def make_records(rows, tokens, case, command, ncu_command, peaks, num_sms=None):
                "command": command, "ncu_command": ncu_command,
                "source": f"tiled_matrix_multiplication_sm_gb300/csrc/{src}" if src else None,
                "source_sha256": file_sha256(os.path.join(CSRC, src)) if src else None,
+               "code_sha256": code_sha256(os.path.join(CSRC, src)) if src else None,
                "metrics": metrics, "derived": derived, "roofline": roof,
                "peaks_source": peaks["source"],
                "taken": datetime.datetime.now(datetime.timezone.utc).strftime("%Y-%m-%d")}
@@ -388,10 +438,7 @@ def summary_table(records_dir: str) -> str:
              "|---|---|---|---|---|---|---|---|---|---|---|---|---|---|---|"]
     for r in recs:
         m, d, roof = r["metrics"], r["derived"], r["roofline"]
-        cur = None
-        if r.get("source"):
-            path = os.path.join(ROOT, r["source"])
-            cur = os.path.exists(path) and file_sha256(path) == r["source_sha256"]
+        cur = record_current(r) if r.get("source") else None
 
         def fmt(v, nd=1):
             return "" if v is None else (f"{v:.{nd}f}" if isinstance(v, float) else str(v))
