@@ -1067,6 +1067,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = sy->tmem_base;
+    // Set-up done (shared memory, barriers, tensor memory): let the next
+    // kernel launch, then wait for the previous one before touching memory.
+    pdl_launch_dependents();
+    pdl_wait();
     const unsigned long long lim = p.wait_limit_ns;
 
     if (warp == 0) {
@@ -1294,6 +1298,10 @@ tc_gemm_tf32t_kernel(const __grid_constant__ CUtensorMap tmA,
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = sy->tmem_base;
+    // Set-up done (shared memory, barriers, tensor memory): let the next
+    // kernel launch, then wait for the previous one before touching memory.
+    pdl_launch_dependents();
+    pdl_wait();
     const unsigned long long lim = p.wait_limit_ns;
     const int nu = slot_unit_count(p, blockIdx.x);
 
@@ -1598,6 +1606,10 @@ tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
     cluster_sync_all();        // barriers of both CTAs initialised, TMEM allocated
     tc_fence_after();
     const uint32_t tmem_base = sy->tmem_base;
+    // Set-up done (shared memory, barriers, tensor memory): let the next
+    // kernel launch, then wait for the previous one before touching memory.
+    pdl_launch_dependents();
+    pdl_wait();
     const unsigned long long lim = p.wait_limit_ns;
     // The leader's copies of the shared hand-off barriers, as cluster addresses.
     const uint32_t full0 = map_to_rank(smem_u32(&sy->full[0]), 0);
@@ -1967,6 +1979,8 @@ void encode_c(EncodeTiledFn enc, CUtensorMap* map, const GemmArgs& a, TcParams& 
 // C under the output rule.
 __global__ void __launch_bounds__(256)
 tc_split_reduce_kernel(const TcParams p) {
+    pdl_launch_dependents();    // the next kernel may launch now
+    pdl_wait();                 // the GEMM kernel's partial tiles are visible
     __shared__ float blk[32][33];
     const int rb_n = p.tile_rows / 32, cb_n = p.tile_cols / 32;
     const int tail_tiles = p.num_tiles - p.dp_tiles;
@@ -2024,8 +2038,7 @@ cudaError_t launch_split_reduce(const TcParams& p, cudaStream_t s) {
     if (!p.sk_split || p.sk_slots == 0) return cudaSuccess;
     const long blocks = (long)(p.num_tiles - p.dp_tiles) * (p.tile_rows / 32) * (p.tile_cols / 32);
     if (blocks <= 0 || blocks > 2147483647L) return cudaErrorInvalidValue;
-    tc_split_reduce_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(tc_split_reduce_kernel, dim3((unsigned)blocks), dim3(256), 0, s, p);
 }
 
 // Slots (SMs or SM pairs) the grid of plan `pl` needs.
@@ -2060,9 +2073,8 @@ cudaError_t launch_tc(const GemmArgs& a, const TcPlan& pl, void* scratch, Encode
     auto kern = tc_gemm_kernel<ESZ, B_KMAJOR, A_LOADER, TBN>;
     cudaError_t e = set_smem_limit_once<tc_gemm_kernel<ESZ, B_KMAJOR, A_LOADER, TBN>>(SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<grid_slots(pl), NUM_THREADS + (A_LOADER ? 32 * A_LOADER_WARPS : 0), SMEM_BYTES, s>>>(
-        tmA, tmB, tmB3, tmC, p);
-    e = cudaGetLastError();
+    e = launch_pdl(kern, dim3(grid_slots(pl)), dim3(NUM_THREADS + (A_LOADER ? 32 * A_LOADER_WARPS : 0)),
+                   SMEM_BYTES, s, tmA, tmB, tmB3, tmC, p);
     return e != cudaSuccess ? e : launch_split_reduce(p, s);
 }
 
@@ -2082,8 +2094,8 @@ cudaError_t launch_tc_t(const GemmArgs& a, const TcPlan& pl, void* scratch, Enco
     if (!prepare_stream_k(p, s)) return cudaErrorInvalidValue;
     cudaError_t e = set_smem_limit_once<tc_gemm_tf32t_kernel>(TT_SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    tc_gemm_tf32t_kernel<<<grid_slots(pl), TT_THREADS, TT_SMEM_BYTES, s>>>(tmA, tmB, tmC, p);
-    e = cudaGetLastError();
+    e = launch_pdl(tc_gemm_tf32t_kernel, dim3(grid_slots(pl)), dim3(TT_THREADS), TT_SMEM_BYTES, s,
+                   tmA, tmB, tmC, p);
     return e != cudaSuccess ? e : launch_split_reduce(p, s);
 }
 
@@ -2128,13 +2140,15 @@ cudaError_t launch_tc_pair(const GemmArgs& a, const TcPlan& pl, void* scratch, E
     cfg.blockDim = dim3(PairEpi<NW>::THREADS + (A_LOADER ? 32 * A_LOADER_WARPS : 0), 1, 1);
     cfg.dynamicSmemBytes = SMEM;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see launch_pdl
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmA2, tmB2, tmC, p);
     if (e != cudaSuccess) return e;
     e = cudaGetLastError();
@@ -2193,6 +2207,10 @@ tc_peak_kernel(long iters, unsigned long long wait_limit_ns, long long* cycles) 
     if constexpr (PAIR) cluster_sync_all(); else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = sy->tmem_base;
+    // Set-up done (shared memory, barriers, tensor memory): let the next
+    // kernel launch, then wait for the previous one before touching memory.
+    pdl_launch_dependents();
+    pdl_wait();
 
     if (issuer) {
         const uint32_t a = smem_u32(smem), b = a + A_BYTES;

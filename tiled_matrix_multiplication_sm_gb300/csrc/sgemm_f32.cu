@@ -277,6 +277,8 @@ __device__ __forceinline__ void mma_phase(Acc<T>& acc, const float* as, const fl
 template <class T, bool VA, bool VB>
 __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
 sgemm_kernel(const F32Params p) {
+    pdl_launch_dependents();    // the next kernel may launch now
+    pdl_wait();                 // the previous kernel's writes are visible
     extern __shared__ __align__(16) float smem[];
     float* As = smem;                               // [STAGES][BM][ALD]
     float* Bs = smem + T::STAGES * T::A_STAGE;      // [STAGES][BK][BLD]
@@ -400,6 +402,8 @@ sgemm_kernel(const F32Params p) {
 template <class T>
 __global__ void __launch_bounds__(256)
 splitk_reduce(const F32Params p) {
+    pdl_launch_dependents();    // the next kernel may launch now
+    pdl_wait();                 // the previous kernel's writes are visible
     constexpr int Q = T::BN / 4;                       // float4 per tile row
     const long per_tile = (long)T::BM * Q;
     const long total = (long)(p.tiles_m * p.tiles_n - p.dp_tiles) * per_tile;
@@ -447,6 +451,8 @@ splitk_reduce(const F32Params p) {
 __global__ void __launch_bounds__(256)
 empty_product_kernel(float* __restrict__ C, long ldc, int M, int N, float beta,
                      const float* __restrict__ bias) {
+    pdl_launch_dependents();    // the next kernel may launch now
+    pdl_wait();                 // the previous kernel's writes are visible
     for (int r = blockIdx.y; r < M; r += gridDim.y) {
         float* row = C + (long)r * ldc;
         for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < N; c += gridDim.x * blockDim.x) {
@@ -486,8 +492,7 @@ cudaError_t launch_cfg(const F32Params& p, int blocks, cudaStream_t s) {
     static_assert(T::SMEM_BYTES <= 227 * 1024, "shared memory budget");
     cudaError_t e = set_smem_limit_once<sgemm_kernel<T, VA, VB>>(T::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<blocks, T::THREADS, T::SMEM_BYTES, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(blocks), dim3(T::THREADS), T::SMEM_BYTES, s, p);
 }
 
 template <class T>
@@ -495,8 +500,7 @@ cudaError_t reduce_cfg(const F32Params& p, cudaStream_t s) {
     const long units = (long)(p.tiles_m * p.tiles_n - p.dp_tiles) * T::BM * (T::BN / 4);
     long blocks = (units + 255) / 256;
     if (blocks > 8192) blocks = 8192;
-    splitk_reduce<T><<<(int)blocks, 256, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(splitk_reduce<T>, dim3((int)blocks), dim3(256), 0, s, p);
 }
 
 #define TGEMM_ENTRY(name, T, VA, VB)                                                       \
@@ -666,6 +670,8 @@ cudaError_t f32_launch(int id, const GemmArgs& a, const F32Plan& pl, float* scra
 // one by one.
 __global__ void __launch_bounds__(256)
 zero_rows_vec_kernel(float* __restrict__ C, long ldc, int M, int N) {
+    pdl_launch_dependents();    // the next kernel may launch now
+    pdl_wait();                 // the previous kernel's writes are visible
     const int vecs = N / 4;
     const long total = (long)M * vecs;
     for (long u = blockIdx.x * (long)blockDim.x + threadIdx.x; u < total;
@@ -685,15 +691,14 @@ cudaError_t empty_product(float* C, long ldc, int M, int N, const Epilogue& ep, 
         long blocks = ((long)M * (N / 4) + 255) / 256;
         if (blocks > 152L * 8 * 4) blocks = 152L * 8 * 4;
         if (blocks < 1) blocks = 1;
-        zero_rows_vec_kernel<<<(int)blocks, 256, 0, s>>>(C, ldc, M, N);
-        return cudaGetLastError();
+        return launch_pdl(zero_rows_vec_kernel, dim3((int)blocks), dim3(256), 0, s, C, ldc, M, N);
     }
     int gx = (N + 255) / 256;
     if (gx > 64) gx = 64;
     if (gx < 1) gx = 1;
     const int gy = M < 16384 ? (M > 0 ? M : 1) : 16384;
-    empty_product_kernel<<<dim3(gx, gy), 256, 0, s>>>(C, ldc, M, N, ep.beta, ep.bias);
-    return cudaGetLastError();
+    return launch_pdl(empty_product_kernel, dim3(gx, gy), dim3(256), 0, s, C, ldc, M, N, ep.beta,
+                      ep.bias);
 }
 
 }  // namespace tgemm

@@ -5,8 +5,43 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 #include <atomic>
+#include <utility>
 
 namespace tgemm {
+
+// Programmatic dependent launch. Every kernel of the library is launched
+// with the stream-serialisation attribute relaxed (launch_pdl), lets the
+// next kernel in the stream launch as soon as all of its own blocks have
+// started (pdl_launch_dependents, first thing in every kernel), and waits
+// for the previous kernel in the stream -- its completion and the
+// visibility of everything it wrote -- before its own first global-memory
+// access (pdl_wait). A kernel's launch and its set-up (barrier init,
+// tensor-memory allocation, tensor-map prefetch) thus overlap the previous
+// kernel's last blocks, and nothing reads or writes memory early.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+#endif
 
 // Output rule of a product: C = alpha * acc + beta * C_old + bias[col]
 // (C_old is not read when beta == 0; bias may be null). The default is the

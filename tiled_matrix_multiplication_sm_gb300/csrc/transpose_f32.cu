@@ -29,6 +29,8 @@ template <typename T>
 __global__ void __launch_bounds__(TT * TROWS)
 transpose_kernel(const T* __restrict__ B, long ldb, T* __restrict__ Bt, long ldt,
                  int K, int N) {
+    pdl_launch_dependents();    // the next kernel may launch now
+    pdl_wait();                 // the previous kernel's writes are visible
     __shared__ T tile[TT][TT + 1];
     const int tx = threadIdx.x % TT, ty = threadIdx.x / TT;
     const int n0 = blockIdx.x * TT, k0 = blockIdx.y * TT;
@@ -59,6 +61,8 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 repack_kernel(const T* __restrict__ src, long ld_src, T* __restrict__ dst, long ld_dst, int rows,
               int cols) {
+    pdl_launch_dependents();    // the next kernel may launch now
+    pdl_wait();                 // the previous kernel's writes are visible
     const int r0 = blockIdx.x * REPACK_ROWS;
     const int c = blockIdx.y * REPACK_COLS + threadIdx.x;
     T v[REPACK_ROWS][4];
@@ -94,6 +98,8 @@ __device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
 __global__ void __launch_bounds__(256)
 split_rows_kernel(const float* __restrict__ X, long ldx, float* __restrict__ hi,
                   float* __restrict__ lo, long ld_out, int rows, int cols) {
+    pdl_launch_dependents();    // the next kernel may launch now
+    pdl_wait();                 // the previous kernel's writes are visible
     for (int r = blockIdx.y; r < rows; r += gridDim.y) {
         const float* s = X + (long)r * ldx;
         for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < cols; c += gridDim.x * blockDim.x) {
@@ -111,6 +117,8 @@ split_rows_kernel(const float* __restrict__ X, long ldx, float* __restrict__ hi,
 __global__ void __launch_bounds__(256)
 split_rows_vec_kernel(const float* __restrict__ X, long ldx, float* __restrict__ hi,
                       float* __restrict__ lo, long ld_out, int rows, int cols) {
+    pdl_launch_dependents();    // the next kernel may launch now
+    pdl_wait();                 // the previous kernel's writes are visible
     const int vecs = cols / 4;
     const long total = (long)rows * vecs;
     for (long u = blockIdx.x * (long)blockDim.x + threadIdx.x; u < total;
@@ -143,6 +151,8 @@ split_rows_vec_kernel(const float* __restrict__ X, long ldx, float* __restrict__
 __global__ void __launch_bounds__(TT * TROWS)
 transpose_split_kernel(const float* __restrict__ B, long ldb, float* __restrict__ hi_t,
                        float* __restrict__ lo_t, long ldt, int K, int N) {
+    pdl_launch_dependents();    // the next kernel may launch now
+    pdl_wait();                 // the previous kernel's writes are visible
     __shared__ float tile[TT][TT + 1];
     const int tx = threadIdx.x % TT, ty = threadIdx.x / TT;
     const int n0 = blockIdx.x * TT, k0 = blockIdx.y * TT;
@@ -175,24 +185,24 @@ cudaError_t split_rows_tf32(const float* X, long ldx, float* hi, float* lo, long
         long blocks = (work + 255) / 256;
         if (blocks > 152L * 8 * 4) blocks = 152L * 8 * 4;
         if (blocks < 1) blocks = 1;
-        split_rows_vec_kernel<<<(int)blocks, 256, 0, s>>>(X, ldx, hi, lo, ld_out, rows, cols);
-        return cudaGetLastError();
+        return launch_pdl(split_rows_vec_kernel, dim3((int)blocks), dim3(256), 0, s, X, ldx, hi, lo,
+                          ld_out, rows, cols);
     }
     int gx = (cols + 255) / 256;
     if (gx > 64) gx = 64;
     if (gx < 1) gx = 1;
     int gy = rows < 16384 ? rows : 16384;
     if (gy < 1) gy = 1;
-    split_rows_kernel<<<dim3(gx, gy), 256, 0, s>>>(X, ldx, hi, lo, ld_out, rows, cols);
-    return cudaGetLastError();
+    return launch_pdl(split_rows_kernel, dim3(gx, gy), dim3(256), 0, s, X, ldx, hi, lo, ld_out, rows,
+                      cols);
 }
 
 cudaError_t transpose_split_tf32(const float* B, long ldb, float* hi_t, float* lo_t, long ldt,
                                  int K, int N, cudaStream_t s) {
     dim3 grid((N + TT - 1) / TT, (K + TT - 1) / TT);
     if (grid.y > 65535) return cudaErrorInvalidValue;
-    transpose_split_kernel<<<grid, TT * TROWS, 0, s>>>(B, ldb, hi_t, lo_t, ldt, K, N);
-    return cudaGetLastError();
+    return launch_pdl(transpose_split_kernel, grid, dim3(TT * TROWS), 0, s, B, ldb, hi_t, lo_t, ldt, K,
+                      N);
 }
 
 cudaError_t repack_rows(const void* src, long ld_src, void* dst, long ld_dst, int rows, int cols,
@@ -205,30 +215,27 @@ cudaError_t repack_rows(const void* src, long ld_src, void* dst, long ld_dst, in
     if (gx > 2147483647L || gy > 65535) return cudaErrorInvalidValue;
     const dim3 grid((unsigned)gx, (unsigned)gy);
     if (esz == 2)
-        repack_kernel<unsigned short><<<grid, 256, 0, s>>>(
-            static_cast<const unsigned short*>(src), ld_src, static_cast<unsigned short*>(dst),
-            ld_dst, rows, cols);
-    else
-        repack_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(src), ld_src,
-                                                  static_cast<float*>(dst), ld_dst, rows, cols);
-    return cudaGetLastError();
+        return launch_pdl(repack_kernel<unsigned short>, grid, dim3(256), 0, s,
+                          static_cast<const unsigned short*>(src), ld_src,
+                          static_cast<unsigned short*>(dst), ld_dst, rows, cols);
+    return launch_pdl(repack_kernel<float>, grid, dim3(256), 0, s, static_cast<const float*>(src),
+                      ld_src, static_cast<float*>(dst), ld_dst, rows, cols);
 }
 
 cudaError_t transpose_f32(const float* B, long ldb, float* Bt, long ldt, int K, int N,
                           cudaStream_t s) {
     dim3 grid((N + TT - 1) / TT, (K + TT - 1) / TT);
     if (grid.y > 65535) return cudaErrorInvalidValue;
-    transpose_kernel<float><<<grid, TT * TROWS, 0, s>>>(B, ldb, Bt, ldt, K, N);
-    return cudaGetLastError();
+    return launch_pdl(transpose_kernel<float>, grid, dim3(TT * TROWS), 0, s, B, ldb, Bt, ldt, K, N);
 }
 
 cudaError_t transpose_u16(const void* B, long ldb, void* Bt, long ldt, int K, int N,
                           cudaStream_t s) {
     dim3 grid((N + TT - 1) / TT, (K + TT - 1) / TT);
     if (grid.y > 65535) return cudaErrorInvalidValue;
-    transpose_kernel<unsigned short><<<grid, TT * TROWS, 0, s>>>(
-        static_cast<const unsigned short*>(B), ldb, static_cast<unsigned short*>(Bt), ldt, K, N);
-    return cudaGetLastError();
+    return launch_pdl(transpose_kernel<unsigned short>, grid, dim3(TT * TROWS), 0, s,
+                      static_cast<const unsigned short*>(B), ldb, static_cast<unsigned short*>(Bt), ldt,
+                      K, N);
 }
 
 }  // namespace tgemm
