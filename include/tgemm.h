@@ -57,7 +57,12 @@
  *     on `stream` (0 = the legacy default stream) and returns. A launch
  *     failure is reported as TGEMM_ERR_CUDA. Faults found while the kernel
  *     runs (a bounded wait that ran out) are reported later, by
- *     gemm_device_status().
+ *     gemm_device_status(). Every kernel is launched with programmatic
+ *     dependent launch: it may be scheduled while the previous kernel on
+ *     `stream` finishes, and sets up its shared and tensor memory then, but
+ *     it touches no global memory before that kernel has completed and its
+ *     writes are visible -- stream order is kept. Calls may be captured in a
+ *     CUDA graph (after a first call outside capture on the device).
  *   - Arguments are checked before any CUDA call is made; an invalid call
  *     returns an error code and enqueues nothing.
  *   - The calls are thread-safe for distinct streams; configuration setters
