@@ -61,6 +61,7 @@ def test_algorithmic_work_of_each_kind():
     w = evidence.algorithmic_work
     assert w("repack_a", "ragged:tf32")["bytes"] == 2 * 3000 * 1537 * 4
     assert w("repack_b", "ragged:f32")["bytes"] == 2 * 1537 * 5001 * 4
+    assert w("repack_ab", "ragged:tf32")["bytes"] == 2 * (3000 * 1537 + 1537 * 5001) * 4
     assert w("split_a", "n4096:tf32x3")["bytes"] == 12 * 4096 * 4096
     assert w("tc_tf32x3_2sm_256x256x32_s3_persistent", "n4096:tf32x3")["flop"] == 3 * 2 * 4096 ** 3
     assert w("f32_128x256x32_s3_ffma2_vecA_vecB", "u1024:f32") == {"bound": "alu",

@@ -227,7 +227,10 @@ def test_unaligned_leading_dimensions(tgemm, tc_mode, kind, shape):
     A, B = operands(M, N, K, "int4", kind, seed=M * N + K)
     C = run_tc(tgemm, A, B, kind)
     name = tgemm.binding.last_kernel()
-    assert ("repack_a" in name) == ((K * A.element_size()) % 16 != 0)
+    a_off = (K * A.element_size()) % 16 != 0
+    b_off = (N * B.element_size()) % 16 != 0
+    expect = "repack_ab+" if a_off and b_off else "repack_a+" if a_off else "repack_b+" if b_off else None
+    assert (expect in name) if expect else ("repack" not in name), name
     C_ref, _ = oracle.gemm(A, B)
     assert_bit_exact(C, C_ref, f"{kind} unaligned {shape}")
 

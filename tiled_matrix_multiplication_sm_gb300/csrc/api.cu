@@ -410,7 +410,19 @@ int run_product(const Request& r, cudaStream_t stream) {
         strncat(name_pre, what, sizeof(name_pre) - strlen(name_pre) - 1);
     };
     const size_t a_off = pp.a_off, a2_off = pp.a2_off, b_off = pp.b_off, b2_off = pp.b2_off;
-    switch (pp.prep_a) {
+    // Both operands' rows off 16 bytes: one launch repacks A and B.
+    const bool repack_both = pp.prep_a == REPACK && pp.prep_b == REPACK;
+    if (repack_both) {
+        a.A = base + a_off;
+        a.B = base + b_off;
+        const tgemm::RepackJob ja{r.A, r.lda, base + a_off, ldk, M, K};
+        const tgemm::RepackJob jb = pp.b_kmajor
+                                        ? tgemm::RepackJob{r.B, r.ldb, base + b_off, ldk, N, K}
+                                        : tgemm::RepackJob{r.B, r.ldb, base + b_off, ldn, K, N};
+        ok(tgemm::repack_rows2(ja, jb, (int)esz, stream));
+        note("repack_ab+");
+    }
+    switch (repack_both ? NONE : pp.prep_a) {
         case TRANSPOSE:
             a.A = base + a_off;
             ok(bf16 ? tgemm::transpose_u16(r.A, r.lda, base + a_off, ldk, K, M, stream)
@@ -444,7 +456,7 @@ int run_product(const Request& r, cudaStream_t stream) {
         default:
             break;
     }
-    switch (pp.prep_b) {
+    switch (repack_both ? NONE : pp.prep_b) {
         case TRANSPOSE:     // FP32 only: stored N x K -> K x N
             a.B = base + b_off;
             ok(tgemm::transpose_f32(static_cast<const float*>(r.B), r.ldb,

@@ -195,6 +195,16 @@ cudaError_t transpose_u16(const void* B, long ldb, void* Bt, long ldt, int K, in
 // dimension ld_src to ld_dst (in elements).
 cudaError_t repack_rows(const void* src, long ld_src, void* dst, long ld_dst, int rows, int cols,
                         int esz, cudaStream_t s);
+// One such copy (rows or cols 0: none).
+struct RepackJob {
+    const void* src = nullptr;
+    long ld_src = 0;
+    void* dst = nullptr;
+    long ld_dst = 0;
+    int rows = 0, cols = 0;
+};
+// Two copies in one launch (A and B of one product).
+cudaError_t repack_rows2(const RepackJob& a, const RepackJob& b, int esz, cudaStream_t s);
 
 // ---- process-wide settings (api.cu) ---------------------------------------
 // The bound on any single wait inside the tensor-core kernels, as last set

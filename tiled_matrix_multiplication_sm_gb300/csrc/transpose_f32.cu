@@ -54,17 +54,27 @@ transpose_kernel(const T* __restrict__ B, long ldb, T* __restrict__ Bt, long ldt
 // every thread issues all of its loads (REPACK_ROWS rows x 4 columns, 256
 // apart) before its stores, so that 8 loads per thread are in flight. (With
 // 4 rows copied one after the other, 3000 x 1537 floats moved at 3.6 TB/s.)
+// One launch may copy two matrices (A and B of one product): blocks
+// [0, blocks_a) copy the first, the rest the second, so the two copies share
+// one launch and one tail instead of two.
 constexpr int REPACK_ROWS = 2;
 constexpr int REPACK_COLS = 1024;
 
 template <typename T>
 __global__ void __launch_bounds__(256)
-repack_kernel(const T* __restrict__ src, long ld_src, T* __restrict__ dst, long ld_dst, int rows,
-              int cols) {
+repack_kernel(const RepackJob ja, const RepackJob jb, long blocks_a) {
     pdl_launch_dependents();    // the next kernel may launch now
     pdl_wait();                 // the previous kernel's writes are visible
-    const int r0 = blockIdx.x * REPACK_ROWS;
-    const int c = blockIdx.y * REPACK_COLS + threadIdx.x;
+    const bool first = (long)blockIdx.x < blocks_a;
+    const RepackJob& j = first ? ja : jb;
+    const long bid = first ? (long)blockIdx.x : (long)blockIdx.x - blocks_a;
+    const long chunks = ((long)j.cols + REPACK_COLS - 1) / REPACK_COLS;
+    const int rows = j.rows, cols = j.cols;
+    const long ld_src = j.ld_src, ld_dst = j.ld_dst;
+    const T* __restrict__ src = static_cast<const T*>(j.src);
+    T* __restrict__ dst = static_cast<T*>(j.dst);
+    const int r0 = (int)(bid / chunks) * REPACK_ROWS;
+    const int c = (int)(bid % chunks) * REPACK_COLS + threadIdx.x;
     T v[REPACK_ROWS][4];
 #pragma unroll
     for (int i = 0; i < REPACK_ROWS; ++i)
@@ -205,21 +215,28 @@ cudaError_t transpose_split_tf32(const float* B, long ldb, float* hi_t, float* l
                       N);
 }
 
+namespace {
+// Blocks of one copy: REPACK_ROWS rows by REPACK_COLS columns each.
+long repack_blocks(const RepackJob& j) {
+    if (j.rows <= 0 || j.cols <= 0) return 0;
+    return ((long)j.rows + REPACK_ROWS - 1) / REPACK_ROWS *
+           (((long)j.cols + REPACK_COLS - 1) / REPACK_COLS);
+}
+}  // namespace
+
+cudaError_t repack_rows2(const RepackJob& a, const RepackJob& b, int esz, cudaStream_t s) {
+    // Consecutive threads copy consecutive columns (coalesced).
+    const long na = repack_blocks(a), nb = repack_blocks(b);
+    if (na + nb == 0) return cudaSuccess;
+    if (na + nb > 2147483647L) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)(na + nb));
+    if (esz == 2) return launch_pdl(repack_kernel<unsigned short>, grid, dim3(256), 0, s, a, b, na);
+    return launch_pdl(repack_kernel<float>, grid, dim3(256), 0, s, a, b, na);
+}
+
 cudaError_t repack_rows(const void* src, long ld_src, void* dst, long ld_dst, int rows, int cols,
                         int esz, cudaStream_t s) {
-    // One block per REPACK_ROWS rows and REPACK_COLS columns; consecutive
-    // threads copy consecutive columns (coalesced).
-    if (rows <= 0 || cols <= 0) return cudaSuccess;
-    const long gx = ((long)rows + REPACK_ROWS - 1) / REPACK_ROWS;
-    const long gy = ((long)cols + REPACK_COLS - 1) / REPACK_COLS;
-    if (gx > 2147483647L || gy > 65535) return cudaErrorInvalidValue;
-    const dim3 grid((unsigned)gx, (unsigned)gy);
-    if (esz == 2)
-        return launch_pdl(repack_kernel<unsigned short>, grid, dim3(256), 0, s,
-                          static_cast<const unsigned short*>(src), ld_src,
-                          static_cast<unsigned short*>(dst), ld_dst, rows, cols);
-    return launch_pdl(repack_kernel<float>, grid, dim3(256), 0, s, static_cast<const float*>(src),
-                      ld_src, static_cast<float*>(dst), ld_dst, rows, cols);
+    return repack_rows2(RepackJob{src, ld_src, dst, ld_dst, rows, cols}, RepackJob{}, esz, s);
 }
 
 cudaError_t transpose_f32(const float* B, long ldb, float* Bt, long ldt, int K, int N,

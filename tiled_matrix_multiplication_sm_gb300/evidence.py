@@ -226,6 +226,8 @@ def algorithmic_work(token: str, case: str) -> Dict[str, object]:
         return {"bound": "hbm", "bytes": 2 * M * K * esz}
     if token in ("repack_b", "transpose_b"):
         return {"bound": "hbm", "bytes": 2 * K * N * esz}
+    if token == "repack_ab":             # both operands in one launch
+        return {"bound": "hbm", "bytes": 2 * (M * K + K * N) * esz}
     if token == "split_a":               # read fp32, write hi and lo
         return {"bound": "hbm", "bytes": 12 * M * K}
     if token == "split_b":
