@@ -396,8 +396,9 @@ TGEMM_API const char* gemm_f32_kernel_name(int id);
  * gemm_last_kernel — name of the kernel(s) the most recent successful
  * gemm_f32, gemm_tc or gemm_ex call on this thread launched, in launch
  * order, joined by '+' when a call launched more than one: the pre-passes
- * (repack_a, repack_b, transpose_a, transpose_b, split_a, split_b,
- * transpose_split_a, transpose_split_b), the GEMM kernel's configuration
+ * (repack_a, repack_b, repack_ab -- both operands in one launch --,
+ * transpose_a, transpose_b, split_a, split_b, transpose_split_a,
+ * transpose_split_b), the GEMM kernel's configuration
  * name, and "splitk_reduce(split=S,tiles=T)" when T tiles of a partial last
  * wave were computed in S K-pieces each and summed by a reduction kernel
  * (FP32 path); a tensor-core kernel's name carries "(streamk:slots=S,tiles=T)"
