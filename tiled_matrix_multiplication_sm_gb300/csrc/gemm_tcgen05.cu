@@ -2287,10 +2287,12 @@ struct TileModel {
     double main_us, epi_us;
     // One row of tiles (b_stream): each tile streams b_bytes of B from
     // memory once, at most sm_rate bytes/us per SM and, all SMs together, at
-    // most kStreamRate: measured 47 GB/s per SM for the one-SM kernel (B
-    // boxes of 8 KB or more), 26 GB/s for the B-transposing TF32 kernel
-    // (16 x 14336 x 4096: in-kernel timestamps), and 4.5-5.0 TB/s for TMA
-    // streams of 512-byte row segments over 112-152 SMs.
+    // most kStreamRate: measured 47 GB/s per SM for the one-SM kernel with
+    // 128 x 256 tiles (32 KB of B a ring stage), 40 GB/s with 128 x 128
+    // tiles (16 KB a stage: TF32 16 x 14336 x 4096 on 112 SMs ran 55.9 us
+    // whole against 52.4 on 128 x 256 tiles shared by 112 SMs), 26 GB/s for
+    // the B-transposing TF32 kernel (in-kernel timestamps), and 5.0-5.2 TB/s
+    // for all SMs together (16 x 28672 x 4096 BF16 on 112 SMs: 45.7 us).
     double b_bytes, sm_rate;
     // Main-loop time of `frac` of a tile with n SMs streaming at once.
     double share_us(double frac, int n) const {
@@ -2301,7 +2303,7 @@ struct TileModel {
         }
         return us;
     }
-    static constexpr double kStreamRate = 4.5e6;     // bytes per us, all SMs
+    static constexpr double kStreamRate = 5.0e6;     // bytes per us, all SMs
 };
 
 // b_stream: one row of tiles (M <= tile rows), so every tile streams its
@@ -2321,7 +2323,7 @@ TileModel tile_model(int in_type, int shape, int tile_rows, int tile_cols, int K
     TileModel m;
     m.main_us = 2.0 * tile_rows * tile_cols * (double)K / (tflops * 1e6);
     m.b_bytes = b_stream ? (double)tile_cols * K * (in_type == TC_BF16 ? 2 : 4) : 0.0;
-    m.sm_rate = shape == TC_ONE_SM_T ? 26e3 : 47e3;
+    m.sm_rate = shape == TC_ONE_SM_T ? 26e3 : shape == TC_ONE_SM_N ? 40e3 : 47e3;
     // The wide tiles' single accumulator leaves part of each epilogue exposed:
     // ~6.5 us with TMA stores, more with per-thread stores when C's rows are
     // not 16-byte aligned (8192 x 14336 x 4096 BF16 with ldc = 14337: wide
