@@ -266,6 +266,25 @@ TGEMM_API long long gemm_scratch_bytes(int M, int N, int K,
                                        int path, int flags);
 
 /*
+ * gemm_plan_name — the kernels that the call
+ *     gemm_ex(M, N, K, A, lda, B, ldb, C, ldc, path, flags, 1, 0, NULL, s)
+ * would launch on a device with `num_sms` SMs, under the current settings
+ * (gemm_set_*), written to `buf` (at most buf_len bytes, NUL-terminated) in
+ * the form gemm_last_kernel reports after the call: the pre-passes, the
+ * GEMM kernel's configuration, its tail. "" when M or N is 0,
+ * "empty_product" when K is 0. The pointers are not dereferenced (only their
+ * alignment matters) and no CUDA call is made, so the planner's choices can
+ * be checked without a GPU. Returns TGEMM_OK, TGEMM_ERR_INVALID_ARG (as
+ * gemm_scratch_bytes, or num_sms < 2, or no buffer) or TGEMM_ERR_ALIGNMENT.
+ */
+TGEMM_API int gemm_plan_name(int M, int N, int K,
+                             const void* A, long lda,
+                             const void* B, long ldb,
+                             const float* C, long ldc,
+                             int path, int flags, int num_sms,
+                             char* buf, int buf_len);
+
+/*
  * gemm_device_status — result of the kernels' bounded waits.
  *
  * Synchronises `stream`, then returns and clears the library's device-side

@@ -58,6 +58,10 @@ _SIGNATURES = {
     "gemm_scratch_bytes": (ctypes.c_longlong, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                _VP, ctypes.c_long, _VP, ctypes.c_long,
                                                _VP, ctypes.c_long, ctypes.c_int, ctypes.c_int]),
+    "gemm_plan_name": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      _VP, ctypes.c_long, _VP, ctypes.c_long,
+                                      _VP, ctypes.c_long, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_int, ctypes.c_char_p, ctypes.c_int]),
     "gemm_tc_peak": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_long,
                                     ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
                                     _VP]),
@@ -322,6 +326,21 @@ def gemm_ex(A: torch.Tensor, B: torch.Tensor, path: str = "f32", trans_a: bool =
     if st != TGEMM_OK:
         raise TgemmError(st, "gemm_ex")
     return C
+
+
+def plan_name_raw(M: int, N: int, K: int, a_ptr: int, lda: int, b_ptr: int, ldb: int,
+                  c_ptr: int, ldc: int, path: str = "f32", trans_a: bool = False,
+                  trans_b: bool = False, num_sms: int = 152) -> str:
+    """The kernels ``gemm_ex`` would launch for this problem on a device with
+    ``num_sms`` SMs (gemm_plan_name: no GPU needed; only the pointers'
+    alignment matters), in gemm_last_kernel's form."""
+    buf = ctypes.create_string_buffer(256)
+    flags = (TGEMM_TRANS_A if trans_a else 0) | (TGEMM_TRANS_B if trans_b else 0)
+    st = int(load().gemm_plan_name(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, TGEMM_PATH[path],
+                                   flags, num_sms, buf, len(buf)))
+    if st != TGEMM_OK:
+        raise TgemmError(st, "gemm_plan_name")
+    return buf.value.decode()
 
 
 def scratch_bytes(A: torch.Tensor, B: torch.Tensor, path: str = "f32", trans_a: bool = False,

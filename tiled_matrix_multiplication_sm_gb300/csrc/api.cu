@@ -11,6 +11,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <string>
 #include <vector>
 
 namespace {
@@ -353,6 +354,39 @@ int plan_product(const Request& r, const DeviceInfo& dev, ProductPlan& pp) {
     return TGEMM_OK;
 }
 
+// The kernels a planned product launches, as gemm_last_kernel reports them:
+// the pre-passes, the GEMM kernel's configuration and its tail.
+void product_name(const ProductPlan& pp, int path, char* out, size_t n) {
+    std::string s;
+    const bool repack_both = pp.prep_a == REPACK && pp.prep_b == REPACK;
+    if (repack_both) s += "repack_ab+";
+    static const char* const kA[] = {"", "transpose_a+", "repack_a+", "split_a+", "transpose_split_a+"};
+    static const char* const kB[] = {"", "transpose_b+", "repack_b+", "split_b+", "transpose_split_b+"};
+    if (!repack_both) {
+        s += kA[pp.prep_a];
+        s += kB[pp.prep_b];
+    }
+    char tail[96] = "";
+    if (path == TGEMM_PATH_F32) {
+        s += tgemm::f32_kernel_name(pp.f32_id);
+        if (pp.fplan.split > 1)
+            snprintf(tail, sizeof(tail), "+splitk_reduce(split=%d,tiles=%d)", pp.fplan.split,
+                     pp.fplan.tiles_m * pp.fplan.tiles_n - pp.fplan.dp_tiles);
+    } else {
+        s += tgemm::tc_kernel_name(path, pp.shape);
+        if (pp.a_loader) strncat(tail, "(a_loader)", sizeof(tail) - strlen(tail) - 1);
+        const int tail_tiles = pp.tplan.tiles_m * pp.tplan.tiles_n - pp.tplan.dp_tiles;
+        if (pp.tplan.sk_slots > 0 && pp.tplan.sk_split)
+            snprintf(tail + strlen(tail), sizeof(tail) - strlen(tail),
+                     "+tc_split_reduce(split=%d,tiles=%d)", pp.tplan.sk_slots / tail_tiles, tail_tiles);
+        else if (pp.tplan.sk_slots > 0)
+            snprintf(tail + strlen(tail), sizeof(tail) - strlen(tail), "(streamk:slots=%d,tiles=%d)",
+                     pp.tplan.sk_slots, tail_tiles);
+    }
+    s += tail;
+    snprintf(out, n, "%s", s.c_str());
+}
+
 int run_product(const Request& r, cudaStream_t stream) {
     g_last_kernel = "";
     int st = check_request(r);
@@ -405,10 +439,6 @@ int run_product(const Request& r, cudaStream_t stream) {
     a.ep = r.ep;
     a.a_loader = pp.a_loader;
     a.a_esz = (int)esz;
-    char name_pre[64] = "";
-    auto note = [&](const char* what) {
-        strncat(name_pre, what, sizeof(name_pre) - strlen(name_pre) - 1);
-    };
     const size_t a_off = pp.a_off, a2_off = pp.a2_off, b_off = pp.b_off, b2_off = pp.b2_off;
     // Both operands' rows off 16 bytes: one launch repacks A and B.
     const bool repack_both = pp.prep_a == REPACK && pp.prep_b == REPACK;
@@ -420,7 +450,6 @@ int run_product(const Request& r, cudaStream_t stream) {
                                         ? tgemm::RepackJob{r.B, r.ldb, base + b_off, ldk, N, K}
                                         : tgemm::RepackJob{r.B, r.ldb, base + b_off, ldn, K, N};
         ok(tgemm::repack_rows2(ja, jb, (int)esz, stream));
-        note("repack_ab+");
     }
     switch (repack_both ? NONE : pp.prep_a) {
         case TRANSPOSE:
@@ -429,12 +458,10 @@ int run_product(const Request& r, cudaStream_t stream) {
                     : tgemm::transpose_f32(static_cast<const float*>(r.A), r.lda,
                                            reinterpret_cast<float*>(base + a_off), ldk, K, M,
                                            stream));
-            note("transpose_a+");
             break;
         case REPACK:
             a.A = base + a_off;
             ok(tgemm::repack_rows(r.A, r.lda, base + a_off, ldk, M, K, (int)esz, stream));
-            note("repack_a+");
             break;
         case SPLIT:
             a.A = base + a_off;
@@ -442,7 +469,6 @@ int run_product(const Request& r, cudaStream_t stream) {
             ok(tgemm::split_rows_tf32(static_cast<const float*>(r.A), r.lda,
                                       reinterpret_cast<float*>(base + a_off),
                                       reinterpret_cast<float*>(base + a2_off), ldk, M, K, stream));
-            note("split_a+");
             break;
         case TRANSPOSE_SPLIT:
             a.A = base + a_off;
@@ -451,7 +477,6 @@ int run_product(const Request& r, cudaStream_t stream) {
                                            reinterpret_cast<float*>(base + a_off),
                                            reinterpret_cast<float*>(base + a2_off), ldk, K, M,
                                            stream));
-            note("transpose_split_a+");
             break;
         default:
             break;
@@ -461,7 +486,6 @@ int run_product(const Request& r, cudaStream_t stream) {
             a.B = base + b_off;
             ok(tgemm::transpose_f32(static_cast<const float*>(r.B), r.ldb,
                                     reinterpret_cast<float*>(base + b_off), ldn, N, K, stream));
-            note("transpose_b+");
             break;
         case REPACK:
             a.B = base + b_off;
@@ -469,7 +493,6 @@ int run_product(const Request& r, cudaStream_t stream) {
                 ok(tgemm::repack_rows(r.B, r.ldb, base + b_off, ldk, N, K, (int)esz, stream));
             else
                 ok(tgemm::repack_rows(r.B, r.ldb, base + b_off, ldn, K, N, (int)esz, stream));
-            note("repack_b+");
             break;
         case SPLIT:     // stored N x K
             a.B = base + b_off;
@@ -477,7 +500,6 @@ int run_product(const Request& r, cudaStream_t stream) {
             ok(tgemm::split_rows_tf32(static_cast<const float*>(r.B), r.ldb,
                                       reinterpret_cast<float*>(base + b_off),
                                       reinterpret_cast<float*>(base + b2_off), ldk, N, K, stream));
-            note("split_b+");
             break;
         case TRANSPOSE_SPLIT:    // stored K x N
             a.B = base + b_off;
@@ -486,7 +508,6 @@ int run_product(const Request& r, cudaStream_t stream) {
                                            reinterpret_cast<float*>(base + b_off),
                                            reinterpret_cast<float*>(base + b2_off), ldk, K, N,
                                            stream));
-            note("transpose_split_b+");
             break;
         default:
             break;
@@ -494,35 +515,18 @@ int run_product(const Request& r, cudaStream_t stream) {
 
     // ---- the product
     float* partials = pp.part_bytes ? reinterpret_cast<float*>(base + pp.p_off) : nullptr;
-    const char* kname = "";
-    char tail[64] = "";
     if (rc == TGEMM_OK) {
-        if (f32) {
+        if (f32)
             ok(tgemm::f32_launch(pp.f32_id, a, pp.fplan, partials, stream));
-            kname = tgemm::f32_kernel_name(pp.f32_id);
-            if (pp.fplan.split > 1)
-                snprintf(tail, sizeof(tail), "+splitk_reduce(split=%d,tiles=%d)", pp.fplan.split,
-                         pp.fplan.tiles_m * pp.fplan.tiles_n - pp.fplan.dp_tiles);
-        } else {
+        else
             ok(tgemm::tc_launch(a, path, pp.b_kmajor ? 1 : 0, enc,
                                 (unsigned long long)g_wait_limit_ns.load(), g_debug_stall.load(),
                                 pp.shape, pp.tplan, partials, stream));
-            kname = tgemm::tc_kernel_name(path, pp.shape);
-            if (pp.a_loader) strncat(tail, "(a_loader)", sizeof(tail) - strlen(tail) - 1);
-            const int tail_tiles = pp.tplan.tiles_m * pp.tplan.tiles_n - pp.tplan.dp_tiles;
-            if (pp.tplan.sk_slots > 0 && pp.tplan.sk_split)
-                snprintf(tail + strlen(tail), sizeof(tail) - strlen(tail),
-                         "+tc_split_reduce(split=%d,tiles=%d)", pp.tplan.sk_slots / tail_tiles,
-                         tail_tiles);
-            else if (pp.tplan.sk_slots > 0)
-                snprintf(tail + strlen(tail), sizeof(tail) - strlen(tail),
-                         "(streamk:slots=%d,tiles=%d)", pp.tplan.sk_slots, tail_tiles);
-        }
     }
     if (ws != nullptr && cudaFreeAsync(ws, stream) != cudaSuccess && rc == TGEMM_OK)
         rc = TGEMM_ERR_CUDA;
     if (rc == TGEMM_OK) {
-        snprintf(g_last_kernel_buf, sizeof(g_last_kernel_buf), "%s%s%s", name_pre, kname, tail);
+        product_name(pp, path, g_last_kernel_buf, sizeof(g_last_kernel_buf));
         g_last_kernel = g_last_kernel_buf;
     }
     return rc;
@@ -801,6 +805,30 @@ long long gemm_scratch_bytes(int M, int N, int K, const void* A, long lda, const
     st = plan_product(r, dev, pp);
     if (st != TGEMM_OK) return -st;
     return (long long)pp.scratch;
+}
+
+int gemm_plan_name(int M, int N, int K, const void* A, long lda, const void* B, long ldb,
+                   const float* C, long ldc, int path, int flags, int num_sms, char* buf,
+                   int buf_len) {
+    if (buf == nullptr || buf_len < 1 || num_sms < 2) return TGEMM_ERR_INVALID_ARG;
+    buf[0] = '\0';
+    if (path < TGEMM_PATH_F32 || path > TGEMM_PATH_TF32X3) return TGEMM_ERR_INVALID_ARG;
+    if ((flags & ~(TGEMM_TRANS_A | TGEMM_TRANS_B)) != 0) return TGEMM_ERR_INVALID_ARG;
+    Request r{M, N, K, A, lda, B, ldb, const_cast<float*>(C), ldc, path, flags, tgemm::Epilogue()};
+    int st = check_request(r);
+    if (st == -1) return TGEMM_OK;                  // nothing to compute
+    if (st != TGEMM_OK) return st;
+    if (K == 0) {
+        snprintf(buf, (size_t)buf_len, "empty_product");
+        return TGEMM_OK;
+    }
+    DeviceInfo dev;                                 // the planner reads only the SM count
+    dev.num_sms = num_sms;
+    ProductPlan pp;
+    st = plan_product(r, dev, pp);
+    if (st != TGEMM_OK) return st;
+    product_name(pp, path, buf, (size_t)buf_len);
+    return TGEMM_OK;
 }
 
 int gemm_device_status(cudaStream_t stream) {
