@@ -105,3 +105,34 @@ def test_invalid_arguments():
         plan(16, 16, 16, "f32", sms=1)
     with pytest.raises(binding.TgemmError):
         plan(16, 16, 16, "f32", lda=8)            # lda < K
+
+
+TOKEN = (r"(repack_ab|repack_a|repack_b|transpose_a|transpose_b|split_a|split_b|transpose_split_a|"
+         r"transpose_split_b)")
+
+
+def test_random_problems_always_plan():
+    """Random shapes, paths, storage, alignment and SM counts (including
+    counts no GB300 has): every valid call gets a plan whose name is made of
+    known parts, and the tensor paths keep one-SM tiles for M <= 128."""
+    import random
+    import re
+    rng = random.Random(20262)
+    name_re = re.compile(rf"^(?:{TOKEN}\+)*(?:f32_\w+|tc_\w+)(?:\(a_loader\))?"
+                         r"(?:\(streamk:slots=\d+,tiles=\d+\)|\+(?:tc_split_reduce|splitk_reduce)"
+                         r"\(split=\d+,tiles=\d+\))?$")
+    for _ in range(3000):
+        path = rng.choice(["f32", "tf32", "bf16", "tf32x3"])
+        M = rng.choice([1, 2, 15, 16, 17, 127, 128, 129, 255, 256, 257]) if rng.random() < 0.4 \
+            else rng.randint(1, 20000)
+        N = rng.randint(1, 30000)
+        K = rng.choice([1, 7, 8, 31, 32, 33, 4096]) if rng.random() < 0.3 else rng.randint(1, 20000)
+        ta, tb = rng.random() < 0.2, rng.random() < 0.2
+        pad = lambda: rng.choice([0, 0, 0, 1, 3, 8])
+        lda = (M if ta else K) + pad()
+        ldb = (K if tb else N) + pad()
+        sms = rng.choice([2, 8, 76, 132, 148, 152])
+        name = plan(M, N, K, path, lda=lda, ldb=ldb, ldc=N + pad(), trans_a=ta, trans_b=tb, sms=sms)
+        assert name_re.match(name), (path, M, N, K, ta, tb, lda, ldb, sms, name)
+        if path != "f32" and M <= 128 and path != "tf32x3":
+            assert "2sm" not in name, (path, M, N, K, name)
